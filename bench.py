@@ -1,0 +1,523 @@
+"""Benchmark of the verify round on one GB300 (or N replicas).
+
+Step = one full greedy verify round (spec_verify_round) of the synthetic
+8-layer decoder: H=4096, 32 q / 8 kv heads of 128, SwiGLU FFN 14336, Q4
+linears, Q6 LM head over V=151936, 4096 cached positions, nt = 8 (anchor +
+7 drafts).  Drafts follow the target's own greedy chain with probability 0.74
+per position; they are recorded by an untimed pass of the same chain, and
+the timed steps replay that chain from the same starting state (every step
+recomputes the whole target pass: nothing is cached between steps).
+
+Printed JSON line: value = emitted tokens per second of the rounds (accepted
+drafts + the one correction/bonus token per round), plus the verify-round
+latency, the weight-stream bandwidth of the verify GEMM against the HBM
+roofline, the nt sweep of the linear layers, the end-to-end number through
+host buffers, and the oracle's CPU rate.
+
+--impl reference times the CPU oracle (the plain fp64 reference of the same
+round) on the host cores, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify-round µs at nt=1..16; weight-stream HBM GB/s vs peak; accepted tok/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# --------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# the workload
+# --------------------------------------------------------------------------
+def build_model(sv, synth, wl, dev, max_ctx):
+    W = synth.decoder_weights_torch(wl, dev)
+    desc = dict(n_layers=wl["n_layers"], hidden=wl["hidden"], n_q_heads=wl["n_q_heads"],
+                n_kv_heads=wl["n_kv_heads"], head_dim=wl["head_dim"], ffn=wl["ffn"],
+                vocab=wl["vocab"], max_ctx=max_ctx, max_nt=wl["d"] + 1, max_seqs=wl["n_seq"])
+    return sv.Model(desc, W), W
+
+
+def fill_context(sv, synth, m, wl, dev, seed=1):
+    import torch
+    gen = synth.torch_gen(seed, dev)
+    for l in range(wl["n_layers"]):
+        for s in range(wl["n_seq"]):
+            k = synth.f16_normal_torch(gen, (wl["n_kv_heads"], wl["ctx"], wl["head_dim"]), dev)
+            v = synth.f16_normal_torch(gen, (wl["n_kv_heads"], wl["ctx"], wl["head_dim"]), dev)
+            sv.spec_kv_fill(m, l, s, 0, wl["ctx"], k.view(torch.int16), v.view(torch.int16))
+    torch.cuda.synchronize()
+
+
+def record_chain(sv, synth, m, wl, dev, n_rounds, anchor, rng):
+    """Untimed: run the speculative chain once, drafting from the target's
+    own greedy continuation (nt = 1 passes from a saved state) with
+    agreement probability p per position.  Returns the per-round drafts."""
+    import torch
+    d, V = wl["d"], wl["vocab"]
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    em = torch.zeros((1, d + 1), dtype=torch.int32, device=dev)
+    em1 = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
+    drafts = []
+    for _ in range(n_rounds):
+        n_past, ei, anc = sv.spec_state_get(m, [0])
+        chain, tok = [], anc[0]
+        for i in range(d):
+            sv.spec_state_set(m, [0], n_past=[n_past[0] + i], anchor=[tok])
+            sv.spec_verify_round(m, 1, sid, None, 0, n_acc=n_acc, emitted=em1)
+            true_next = int(em1.item())
+            tok = true_next if rng.random() < wl["p_agree"] else int(rng.integers(0, V))
+            chain.append(tok)
+        sv.spec_state_set(m, [0], n_past=n_past, emit_idx=ei, anchor=anc)
+        dr = torch.tensor([chain], dtype=torch.int32, device=dev)
+        sv.spec_verify_round(m, 1, sid, dr, d, n_acc=n_acc, emitted=em)
+        drafts.append(chain)
+    assert sv.spec_error_check(m) == 0
+    return drafts
+
+
+def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
+    """The verify GEMM at the decoder's shapes, nt = 8, timed alone with CUDA
+    events on its stream; L2 flushed between launches.  Returns the achieved
+    weight-stream GB/s over one round's mix of launches (8 x [qkv, o,
+    gate/up, down] + the LM head)."""
+    import torch
+    H, F, hd, nq, nkv, V = (wl["hidden"], wl["ffn"], wl["head_dim"], wl["n_q_heads"],
+                            wl["n_kv_heads"], wl["vocab"])
+    shapes = [(4, (nq + 2 * nkv) * hd, H, wl["n_layers"]), (4, H, nq * hd, wl["n_layers"]),
+              (4, 2 * F, H, wl["n_layers"]), (4, H, F, wl["n_layers"]), (6, V, H, 1)]
+    gen = synth.torch_gen(5, dev)
+    st = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    nt = wl["d"] + 1
+    total_bytes, total_s, per = 0.0, 0.0, []
+    for qt, N, K, count in shapes:
+        w = synth.q_weight_torch(gen, qt, N, K, dev)
+        qm = sv.QMat(w, max_rows=16)
+        x = synth.f16_normal_torch(gen, (nt, K), dev).view(torch.int16)
+        y = torch.empty((nt, N), dtype=torch.float32, device=dev)
+        nbytes = N * K * (0.5625 if qt == 4 else 0.8125) + nt * K * 2 + nt * N * 4
+        times = []
+        for i in range(reps + 3):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            sv.spec_linear_q(qm, x, nt, y, st)
+            e1.record(st)
+            e1.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        t = statistics.median(times)
+        per.append({"qtype": qt, "N": N, "K": K, "us": t * 1e6, "gbs": nbytes / t / 1e9})
+        total_bytes += nbytes * count
+        total_s += t * count
+        qm.close()
+        del w
+    gbs = total_bytes / total_s / 1e9
+    return gbs, per, total_bytes / (4 * wl["n_layers"] + 1)
+
+
+def nt_sweep(sv, synth, dev, reps=20):
+    """The linear-layer sweep: Q4 5120x13824 and Q6 13824x5120 at each nt,
+    L2 flushed between launches (verify-GEMM microseconds and GB/s)."""
+    import torch
+    wl = synth.WL_LINEAR_SWEEP
+    gen = synth.torch_gen(wl["seed"], dev)
+    st = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    out = {}
+    for qt, N, K in wl["mats"]:
+        w = synth.q_weight_torch(gen, qt, N, K, dev)
+        qm = sv.QMat(w, max_rows=16)
+        x = synth.f16_normal_torch(gen, (16, K), dev).view(torch.int16)
+        y = torch.empty((16, N), dtype=torch.float32, device=dev)
+        wbytes = N * K * (0.5625 if qt == 4 else 0.8125)
+        row = {}
+        for nt in wl["nts"]:
+            times = []
+            for i in range(reps + 3):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                sv.spec_linear_q(qm, x, nt, y, st)
+                e1.record(st)
+                e1.synchronize()
+                if i >= 3:
+                    times.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(times)
+            row[str(nt)] = {"us": round(t * 1e6, 2), "gbs": round(wbytes / t / 1e9, 1)}
+        out[f"q{qt}_{N}x{K}"] = row
+        qm.close()
+    return out
+
+
+def run_ours(args):
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from speculative_decoding_verification_round_gb300 import synth
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    wl = dict(synth.WL_DECODER8)
+    d, V = wl["d"], wl["vocab"]
+    max_ctx = wl["ctx"] + 8 * (args.warmup + args.steps + 4) + 64
+    hbm_peak, peak_kind = peaks()
+    m, W = build_model(sv, synth, wl, dev, max_ctx)
+    del W
+    torch.cuda.empty_cache()
+    fill_context(sv, synth, m, wl, dev, seed=1 + rank)
+    rng = np.random.default_rng(wl["seed"] + rank)
+    anchor = 1234
+    n_rounds = args.warmup + args.steps
+    drafts = record_chain(sv, synth, m, wl, dev, n_rounds, anchor, rng)
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    dr_dev = [torch.tensor([c], dtype=torch.int32, device=dev) for c in drafts]
+    n_acc = torch.zeros((n_rounds, 1), dtype=torch.int32, device=dev)
+    em = torch.zeros((n_rounds, 1, d + 1), dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+    # replay: warm-up rounds, then exactly K timed rounds
+    sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
+    for j in range(args.warmup):
+        sv.spec_verify_round(m, 1, sid, dr_dev[j], d, n_acc=n_acc[j], emitted=em[j])
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(st)
+        for j in range(args.warmup, n_rounds):
+            sv.spec_verify_round(m, 1, sid, dr_dev[j], d, n_acc=n_acc[j], emitted=em[j])
+        e1.record(st)
+        torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    assert sv.spec_error_check(m) == 0
+    elapsed = e0.elapsed_time(e1) * 1e-3
+    emitted_tokens = int((n_acc[args.warmup:].cpu().numpy() + 1).sum())
+    t_max = max_over_ranks(dist, elapsed, dev)
+    tokens_all = sum_over_ranks(dist, emitted_tokens, dev)
+    ms_per_step = t_max / args.steps * 1e3
+
+    # end to end through host buffers: pinned H2D of the drafts, the round,
+    # D2H of (n_acc, emitted) every step
+    sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
+    h_drafts = [torch.tensor([c], dtype=torch.int32).pin_memory() for c in drafts]
+    d_draft = torch.empty((1, d), dtype=torch.int32, device=dev)
+    h_acc = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_em = torch.empty((1, d + 1), dtype=torch.int32).pin_memory()
+    d_acc = torch.empty(1, dtype=torch.int32, device=dev)
+    d_em = torch.empty((1, d + 1), dtype=torch.int32, device=dev)
+    e2e_tok = 0
+    for j in range(args.warmup):
+        d_draft.copy_(h_drafts[j], non_blocking=True)
+        sv.spec_verify_round(m, 1, sid, d_draft, d, n_acc=d_acc, emitted=d_em)
+        h_acc.copy_(d_acc, non_blocking=True)
+        h_em.copy_(d_em, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t0 = time.perf_counter()
+    for j in range(args.warmup, n_rounds):
+        d_draft.copy_(h_drafts[j], non_blocking=True)
+        sv.spec_verify_round(m, 1, sid, d_draft, d, n_acc=d_acc, emitted=d_em)
+        h_acc.copy_(d_acc, non_blocking=True)
+        h_em.copy_(d_em, non_blocking=True)
+        st.synchronize()
+        e2e_tok += int(h_acc[0]) + 1
+    t_e2e = max_over_ranks(dist, time.perf_counter() - t0, dev)
+    e2e_all = sum_over_ranks(dist, e2e_tok, dev)
+
+    line = None
+    if rank == 0:
+        gbs, per, bytes_per_launch = time_dominant_kernel(sv, synth, wl, dev, hbm_peak)
+        sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
+        n_layers = wl["n_layers"]
+        launches_per_round = 2 + 8 * n_layers + 2 + 2
+        weight_bytes = sum(p["N"] * p["K"] * (0.5625 if p["qtype"] == 4 else 0.8125) *
+                           (n_layers if p["qtype"] == 4 else 1) for p in per)
+        kv_bytes = n_layers * wl["n_kv_heads"] * (wl["ctx"] + d) * wl["head_dim"] * 2 * 2
+        round_s = ms_per_step * 1e-3
+        line = {
+            "metric": METRIC,
+            "value": round(tokens_all / t_max, 2),
+            "unit": "tok/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16",
+            "precision": "Q4/Q6 block ints exact in f16, f16 activations, f32 accumulate",
+            "data": "synthetic (seeded N(0,1) activations and KV, uniform block ints, random-init weights)",
+            "config": {"workload": wl["name"], "n_layers": n_layers, "hidden": wl["hidden"],
+                       "heads": f"{wl['n_q_heads']}/{wl['n_kv_heads']}x{wl['head_dim']}",
+                       "ffn": wl["ffn"], "vocab": V, "context": wl["ctx"], "nt": d + 1,
+                       "n_seq": wl["n_seq"], "p_agree": wl["p_agree"], "graphs": True,
+                       "l2": "inputs larger than L2 (1.49 GB of weights per round)",
+                       "parallelism": f"replicas x{ws}"},
+            "verify_round_us": round(round_s * 1e6, 2),
+            "emitted_tokens_per_round": round(tokens_all / ws / args.steps, 3),
+            "round_bytes": {"weights": weight_bytes, "kv": kv_bytes,
+                            "gbs": round((weight_bytes + kv_bytes) / round_s / 1e9, 1),
+                            "frac_of_hbm": round((weight_bytes + kv_bytes) / round_s / 1e9 / hbm_peak, 4)},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "kernel": "linear_q_kernel (verify GEMM), nt=8, one round's launch mix",
+                         "algorithmic_bytes_per_launch": round(bytes_per_launch),
+                         "peak_kind": peak_kind, "per_shape": per},
+            "sweep": sweep,
+            "e2e": {"value": round(e2e_all / t_e2e, 2), "unit": "tok/s",
+                    "h2d_bytes_per_step": 4 * d, "d2h_bytes_per_step": 4 + 4 * (d + 1)},
+            "gpu_launches": launches_per_round * args.steps,
+            "clocks": clk.summary(),
+        }
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(W=None, wl=wl, drafts=drafts[:1], anchor=anchor,
+                                                m=m, sv=sv, dev=dev)
+    m.close()
+    if line is not None:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle on the same workload
+# --------------------------------------------------------------------------
+def oracle_model_host(wl, dev_or_cpu="cpu"):
+    """The decoder's canonical weights on the host, generated by the same
+    seeded generator (on the GPU when there is one)."""
+    import torch
+    import oracle
+    from speculative_decoding_verification_round_gb300 import synth
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    W = synth.decoder_weights_torch(wl, gen_dev)
+    def hw(w):
+        return oracle.QWeight(w["qtype"], w["qs"].cpu().numpy(),
+                              None if w["qh"] is None else w["qh"].cpu().numpy(),
+                              w["scales"].cpu().view(torch.int16).numpy().view(np.uint16),
+                              w["N"], w["K"])
+    om = oracle.Model(wl["n_layers"], wl["hidden"], wl["n_q_heads"], wl["n_kv_heads"],
+                      wl["head_dim"], wl["ffn"], wl["vocab"], wl["ctx"] + 64,
+                      W["embed"].cpu().view(torch.int16).numpy().view(np.uint16),
+                      W["norm_w"].cpu().numpy(), [hw(w) for w in W["wqkv"]],
+                      [hw(w) for w in W["wo"]], [hw(w) for w in W["wgu"]],
+                      [hw(w) for w in W["wd"]], hw(W["lm_head"]))
+    del W
+    return om
+
+
+def oracle_context(wl, seed=1):
+    import torch
+    from speculative_decoding_verification_round_gb300 import synth
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    gen = synth.torch_gen(seed, gen_dev)
+    L, nkv, hd, ctx = wl["n_layers"], wl["n_kv_heads"], wl["head_dim"], wl["ctx"]
+    kc = np.zeros((L, 1, nkv, ctx + 64, hd), np.uint16)
+    vc = np.zeros_like(kc)
+    for l in range(L):
+        k = synth.f16_normal_torch(gen, (nkv, ctx, hd), gen_dev)
+        v = synth.f16_normal_torch(gen, (nkv, ctx, hd), gen_dev)
+        kc[l, 0, :, :ctx] = k.cpu().view(torch.int16).numpy().view(np.uint16)
+        vc[l, 0, :, :ctx] = v.cpu().view(torch.int16).numpy().view(np.uint16)
+    return kc, vc
+
+
+def oracle_round(orc, om, kc, vc, wl, anchor, draft):
+    tokens = np.array([[anchor] + list(draft)], np.int32)
+    logits = om.forward(tokens, [wl["ctx"]], kc, vc)
+    am = np.array([[orc.argmax(r) for r in logits]], np.int32)
+    n_acc, em = orc.accept_greedy(am, np.array([draft], np.int32))
+    return int(n_acc[0]) + 1
+
+
+def cpu_baseline(W, wl, drafts, anchor, m=None, sv=None, dev=None):
+    import oracle
+    oracle.build()
+    om = oracle_model_host(wl)
+    kc, vc = oracle_context(wl)
+    t0 = time.perf_counter()
+    toks = oracle_round(oracle, om, kc, vc, wl, anchor, drafts[0])
+    t = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(toks / t, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"one full verify round of {wl['name']} (nt={wl['d'] + 1}, all "
+                      f"{wl['n_layers']} layers + LM head, fp64), {t:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decoding_verification_round_gb300 import synth
+    oracle.build()
+    wl = dict(synth.WL_DECODER8)
+    om = oracle_model_host(wl)
+    kc0, vc0 = oracle_context(wl)
+    rng = np.random.default_rng(wl["seed"])
+    anchor = 1234
+    draft = [int(x) for x in rng.integers(0, wl["vocab"], wl["d"])]
+    for _ in range(args.warmup):
+        oracle_round(oracle, om, kc0.copy(), vc0.copy(), wl, anchor, draft)
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(args.steps):
+        toks += oracle_round(oracle, om, kc0.copy(), vc0.copy(), wl, anchor, draft)
+    t = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    val = toks / t
+    sample = (f"{args.steps} full verify rounds of {wl['name']} on the CPU oracle "
+              f"(fp64, all layers + LM head)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "tok/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl["name"], "nt": wl["d"] + 1},
+        "cpu_baseline": {"value": round(val, 4), "unit": "tok/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # each oracle step is a full fp64 round (seconds of CPU work): bound
+        # the run to a few minutes
+        args.steps = min(args.steps, 5)
+        args.warmup = min(args.warmup, 3)
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

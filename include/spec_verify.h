@@ -1,0 +1,252 @@
+/*
+ * spec_verify.h -- C ABI of the target-verification round of speculative
+ * decoding on one GB300 (sm_103a).
+ *
+ * The round (sources, by page title and section):
+ *  - "Model-neutral Speculative Decoding", section "The exactness
+ *    transaction": evaluate the anchor and the proposal block in one target
+ *    pass; sample target rows only through the first mismatch; commit the
+ *    accepted prefix; emit exactly one correction or bonus token; for greedy
+ *    decoding the speculative and autoregressive token ids match exactly; for
+ *    stochastic decoding the target sampler advances once per emitted sample
+ *    and never for a rejected suffix.
+ *  - "Speculative Decoding (D5-R) -- Plan", section 3 "Mechanism -- one
+ *    round": one nt = d+1 forward whose rows are the next token plus the d
+ *    drafted candidates at contiguous positions; greedy argmax per verify row,
+ *    accept while equal to the drafted token, always emit at least one token;
+ *    the target writes d+1 KV rows in place and rejected slots are simply
+ *    overwritten next round ("positions are data"); and the status notes on
+ *    the weights-once batched verify and bitwise position-invariant verify
+ *    attention.
+ *  - "DFlash and DSpark Speculative Decoding", "How DSpark Works" and
+ *    "Notes": lossless output under the strict rejection sampler (accept with
+ *    min(1, p/q), else resample from norm(max(0, p - q))).
+ *
+ * Conventions for every function below:
+ *  - Return value: SPEC_OK (0) or a negative SPEC_E_* code; the message of
+ *    the last failure on the calling thread is in spec_last_error().
+ *  - Pointers are DEVICE pointers owned by the caller unless a parameter says
+ *    "host".  fp16 data is passed as uint16_t (IEEE binary16 bits).  Device
+ *    arrays must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued on it asynchronously, except for create/destroy/state calls,
+ *    which synchronise.
+ *  - On an error return nothing has been enqueued and no state has changed.
+ *    Errors that can only be seen on the device (a token id out of range, a
+ *    position past max_ctx, a non-finite logit) set the model's device error
+ *    word: the round then commits nothing, writes -1 to its n_acc and emitted
+ *    outputs, and spec_error_check() reports SPEC_E_INVALID.
+ *  - A model or packed matrix is used from one stream at a time.
+ *  - The library allocates device memory only in *_create, and, for the
+ *    standalone entry points that need scratch, on first use per device
+ *    (a cached, growing workspace).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_OK 0
+#define SPEC_E_INVALID (-1)     /* bad argument, token id, non-finite value */
+#define SPEC_E_SHAPE (-2)       /* size or alignment precondition violated */
+#define SPEC_E_CUDA (-3)        /* a CUDA runtime call failed */
+#define SPEC_E_OOM (-4)         /* device allocation failed */
+#define SPEC_E_UNSUPPORTED (-5) /* mode not supported: fails closed */
+#define SPEC_E_TIMEOUT (-6)     /* a bounded device wait ran out */
+
+#define SPEC_Q4 4 /* 4-bit signed ints in [-8, 7], blocks of 32, fp16 scale */
+#define SPEC_Q6 6 /* 6-bit signed ints in [-32, 31], blocks of 32, fp16 scale */
+
+#define SPEC_MAX_NT 16 /* rows per sequence in one round: anchor + up to 15 drafts */
+
+/* Copies the last error message of the calling thread into buf. */
+void spec_last_error(char* buf, size_t len);
+
+/* ------------------------------------------------------------------------
+ * Block-quantised matrix W[N][K] in canonical planes (device, caller-owned):
+ *   qs     [N][K/32][16] bytes.  Byte j of block b holds element 32b+j in its
+ *          low nibble and element 32b+j+16 in its high nibble.  Q4 stores
+ *          u = q + 8; Q6 stores the low 4 bits of u = q + 32.
+ *   qh     [N][K/32][8] bytes, Q6 only (NULL for Q4): the high 2 bits of u,
+ *          element j of the block at bits 2*(j%4) of byte j/4.
+ *   scales [N][K/32] fp16.  W[n][k] = scale[n][k/32] * q[n][k].
+ * Preconditions: K % 32 == 0, N % 16 == 0.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t qtype; /* SPEC_Q4 or SPEC_Q6 */
+  int32_t N, K;
+  const void* qs;
+  const void* qh;
+  const void* scales;
+} spec_qweight;
+
+/* A matrix repacked into the streaming layout of the verify GEMM. */
+typedef struct spec_qmat spec_qmat;
+
+/* Repacks `w` into a new device-resident matrix (the caller may free the
+ * canonical planes after return).  max_rows bounds the nt of later
+ * spec_linear_q calls (1..16*1024).  Synchronises `stream`. */
+int spec_qmat_create(const spec_qweight* w, int max_rows, void* stream,
+                     spec_qmat** out);
+int spec_qmat_destroy(spec_qmat* m);
+
+/* Weights-once multi-row dequant GEMM ("Speculative Decoding (D5-R) --
+ * Plan", section 1: the batched verify is a weights-once round, not a
+ * per-row restream):
+ *   y[r][n] = sum_k W[n][k] * x[r][k],  r < nt,
+ * x fp16 [nt][K] row-major, y fp32 [nt][N] row-major.  Every row is computed
+ * by the same instruction sequence whatever nt is, so row r is bitwise equal
+ * to the nt = 1 result for the same x row.  1 <= nt <= max_rows. */
+int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
+                  void* stream);
+
+/* ------------------------------------------------------------------------
+ * Decoder model: RMSNorm -> QKV (Q4) + rotate-half RoPE -> causal GQA
+ * attention over the KV cache -> O (Q4) + residual -> RMSNorm -> gate/up (Q4)
+ * + SwiGLU -> down (Q4) + residual, n_layers times; final RMSNorm; LM head
+ * (Q4 or Q6) over the full vocabulary.  Residual stream fp32, activations
+ * fp16, KV cache fp16.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t n_layers; /* 0 allowed: LM head only (spec_lm_head) */
+  int32_t hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  int32_t max_ctx;  /* KV positions per sequence */
+  int32_t max_nt;   /* rows per sequence per round, <= SPEC_MAX_NT */
+  int32_t max_seqs; /* sequence slots */
+  float rms_eps;    /* e.g. 1e-6 */
+  float rope_theta; /* e.g. 10000 */
+  int32_t use_rope; /* 1: rotate q and new k at their absolute positions */
+} spec_model_desc;
+
+typedef struct {
+  const uint16_t* embed;      /* fp16 [vocab][hidden] (NULL if n_layers == 0) */
+  const float* norm_w;        /* fp32 [2*n_layers+1][hidden]: attn_l, ffn_l ..., final */
+  const spec_qweight* wqkv;   /* HOST array [n_layers]; rows [q heads | k heads | v heads] */
+  const spec_qweight* wo;     /* HOST array [n_layers]; [hidden][n_q_heads*head_dim] */
+  const spec_qweight* wgu;    /* HOST array [n_layers]; rows [gate (ffn) ; up (ffn)] */
+  const spec_qweight* wd;     /* HOST array [n_layers]; [hidden][ffn] */
+  spec_qweight lm_head;       /* [vocab][hidden] */
+} spec_model_weights;
+
+typedef struct spec_model spec_model;
+
+/* Creates a model: repacks all weights, allocates the fp16 KV cache
+ * [n_layers][max_seqs][n_kv_heads][max_ctx][head_dim] (zeroed), activation
+ * buffers for max_seqs*max_nt rows and the per-sequence state
+ * (n_past = 0, emit_idx = 0, anchor = 0).  Synchronises `stream`. */
+int spec_model_create(const spec_model_desc* desc, const spec_model_weights* w,
+                      void* stream, spec_model** out);
+int spec_model_destroy(spec_model* m);
+
+/* Device pointers of layer `layer`'s K and V caches, each
+ * [max_seqs][n_kv_heads][max_ctx][head_dim] fp16, for filling a context. */
+int spec_model_kv_cache(spec_model* m, int layer, uint16_t** k, uint16_t** v);
+
+/* Copies a context into the cache of slot `seq`, layer `layer`, positions
+ * [pos0, pos0 + n_pos): k and v are fp16 [n_kv_heads][n_pos][head_dim]
+ * (device or host memory).  Asynchronous on `stream`. */
+int spec_kv_fill(spec_model* m, int layer, int seq, int pos0, int n_pos,
+                 const uint16_t* k, const uint16_t* v, void* stream);
+
+/* Per-sequence transaction state, HOST arrays of n entries for the slots
+ * seq_ids[0..n): n_past (committed positions), emit_idx (sampler slot of the
+ * next emitted token), anchor (last committed token, row 0 of the next
+ * round).  NULL arrays are skipped.  Synchronous. */
+int spec_state_set(spec_model* m, int n, const int32_t* seq_ids,
+                   const int32_t* n_past, const uint64_t* emit_idx,
+                   const int32_t* anchor);
+int spec_state_get(spec_model* m, int n, const int32_t* seq_ids, int32_t* n_past,
+                   uint64_t* emit_idx, int32_t* anchor);
+
+/* Synchronises `stream`, reads and clears the device error word.
+ * Returns SPEC_OK or SPEC_E_INVALID (the bits are stored in *bits if not NULL). */
+int spec_error_check(spec_model* m, void* stream, uint32_t* bits);
+
+/* 1 (default): spec_verify_round replays one captured CUDA graph per
+ * (n_seq, d, mode) shape; 0: launches kernels one by one. */
+int spec_model_set_graphs(spec_model* m, int enable);
+
+/* Causal GQA attention of nt query rows per sequence over the KV cache of
+ * `layer`, bitwise position-invariant: row i of sequence s (absolute
+ * position n_past[s] + i) is computed exactly as it would be at nt = 1
+ * ("Speculative Decoding (D5-R) -- Plan", status notes: batched verify
+ * attention made bitwise position-invariant).  First writes k_new/v_new
+ * [n_seq*nt][n_kv_heads][head_dim] at positions n_past..n_past+nt-1 of each
+ * sequence; n_past itself is not changed.
+ *   seq_ids  device int32 [n_seq] slots;  q fp16 [n_seq*nt][n_q_heads][head_dim]
+ *   out      fp16 [n_seq*nt][n_q_heads*head_dim] */
+int spec_verify_attn(spec_model* m, int layer, int n_seq, const int32_t* seq_ids,
+                     int nt, const uint16_t* q, const uint16_t* k_new,
+                     const uint16_t* v_new, uint16_t* out, void* stream);
+
+/* Full-vocabulary LM head: logits[r][v] = sum_k W_lm[v][k] x[r][k] (fp32),
+ * with a fused per-row argmax (ties to the lowest id).  x fp16 [R][hidden],
+ * R <= max_seqs*max_nt; logits [R][vocab] or NULL; argmax int32 [R] or NULL.
+ * A NaN logit sets the device error word. */
+int spec_lm_head(spec_model* m, const uint16_t* x, int R, float* logits,
+                 int32_t* argmax, void* stream);
+
+/* Greedy accept ("Speculative Decoding (D5-R) -- Plan", section 3):
+ *   a = number of leading i < d with argmax[s][i] == draft[s][i];
+ *   emitted[s] = draft[s][0..a-1], argmax[s][a], then -1 padding;
+ *   n_acc[s] = a.
+ * argmax [n_seq][d+1], draft [n_seq][d], emitted [n_seq][d+1]. */
+int spec_accept_greedy(const int32_t* argmax, const int32_t* draft, int n_seq,
+                       int d, int32_t* n_acc, int32_t* emitted, void* stream);
+
+/* Strict rejection sampling ("DFlash and DSpark Speculative Decoding",
+ * "Notes"; sampler-advance rule of "Model-neutral Speculative Decoding", "The
+ * exactness transaction").  For each sequence s, slot i < d, draft x:
+ *   z = logits / temperature (fp32, round to nearest);
+ *   W_v = floor(exp(z_v - max z) * 2^32) (own fp32 exp, identical on every
+ *   platform), S = sum W_v; Wq, Sq likewise from q_logits;
+ *   U = Philox4x32-10(key = seed, counter = (j lo, j hi, seq_ids[s], 0)) for
+ *   the emitted slot j = emit_idx[s] + i;
+ *   accept iff U[0] * Wq_x * S < 2^32 * W_x * Sq  (u < p_x / q_x, exact);
+ *   on the first rejection resample from R_v = max(0, W_v*Sq - Wq_v*S) with
+ *   threshold floor(U[1] * sum R / 2^32) and stop; after d accepts sample the
+ *   bonus from row d with floor(U[1] * S / 2^32).
+ * emit_idx[s] += n_acc[s] + 1: one sampler slot per emitted token, none for
+ * the rejected suffix.
+ *   p_logits fp32 [n_seq][d+1][V]; q_logits fp32 [n_seq][d][V] (may be NULL
+ *   when d == 0); draft int32 [n_seq][d]; seq_ids int32 [n_seq];
+ *   emit_idx uint64 [n_seq] (in/out); n_acc [n_seq]; emitted [n_seq][d+1].
+ * Decisions are bit-identical to any correct implementation of the same
+ * integer rules on the same fp32 logits. */
+int spec_accept_stochastic(const float* p_logits, const float* q_logits,
+                           const int32_t* draft, int n_seq, int d, int V,
+                           float temperature, uint64_t seed,
+                           const int32_t* seq_ids, uint64_t* emit_idx,
+                           int32_t* n_acc, int32_t* emitted, void* stream);
+
+typedef struct {
+  int32_t greedy;      /* 1: greedy argmax accept; 0: strict rejection sampling */
+  float temperature;   /* stochastic only, > 0 */
+  uint64_t seed;       /* stochastic only: Philox key */
+} spec_sampling;
+
+/* One verify round ("Model-neutral Speculative Decoding", "The exactness
+ * transaction", steps 3-6): rows [anchor, draft[s][0..d-1]] of each sequence
+ * at positions n_past..n_past+d in one weights-once target pass (all layers
+ * and the LM head), then the accept step, then the commit:
+ *   n_past += n_acc + 1, emit_idx += n_acc + 1, anchor = last emitted token.
+ * The new KV rows are written in place; rejected rows are overwritten later.
+ *   seq_ids int32 [n_seq] (distinct slots < max_seqs); draft int32 [n_seq][d];
+ *   q_logits fp32 [n_seq][d][vocab] (draft distributions; NULL iff greedy);
+ *   sampling: HOST pointer;  n_acc int32 [n_seq]; emitted int32 [n_seq][d+1];
+ *   logits_out fp32 [n_seq*(d+1)][vocab] or NULL.
+ * 1 <= n_seq <= max_seqs, 0 <= d < max_nt. */
+int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_ids,
+                      const int32_t* draft, int d, const float* q_logits,
+                      const spec_sampling* sampling, int32_t* n_acc,
+                      int32_t* emitted, float* logits_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,459 @@
+// accept.cu -- acceptance and commit of the verify round.
+//
+// Greedy ("Speculative Decoding (D5-R) -- Plan", section 3): accept while the
+// target's argmax equals the drafted token; always emit one more token, the
+// correction at the first mismatch or the bonus after a fully accepted block.
+//
+// Strict rejection sampling ("DFlash and DSpark Speculative Decoding",
+// "Notes": use the strict sampler, which is lossless): accept draft x with
+// probability min(1, p_x / q_x), else resample from norm(max(0, p - q)).
+// The probabilities are integer weights W_v = floor(exp(z_v - max z) * 2^32)
+// with an fp32 exp made of individually rounded operations (Cody-Waite
+// reduction with a two-part ln 2, degree-7 Taylor polynomial in Horner form,
+// exact power-of-two scaling), so every decision is an exact integer
+// comparison and is identical on any IEEE-754 implementation.  Uniforms come
+// from Philox4x32-10 (Salmon et al., SC'11) keyed by the seed, with counter
+// (emitted-slot index, sequence id, 0): one counter per emitted token, none
+// for a rejected suffix ("Model-neutral Speculative Decoding", "The exactness
+// transaction").
+#include <cooperative_groups.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+typedef unsigned __int128 u128;
+
+// ---------------------------------------------------------------------------
+// the sampler's exp and integer weight (fp32, no contraction: __f*_rn)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t int_weight(float x) {
+  if (!(x >= -87.0f)) return 0ull;
+  const float LOG2E = 0x1.715476p+0f;     // fl32(1 / ln 2)
+  const float LN2_HI = 0x1.62e4p-1f;      // ln 2 to 12 significant bits
+  const float LN2_LO = 0x1.7f7d1cp-20f;   // fl32(ln 2 - LN2_HI)
+  const float C[8] = {0x1p+0f,        0x1p+0f,        0x1p-1f,         0x1.555556p-3f,
+                      0x1.555556p-5f, 0x1.111112p-7f, 0x1.6c16c2p-10f, 0x1.a01a02p-13f};
+  const float n = rintf(__fmul_rn(x, LOG2E));
+  float r = __fsub_rn(x, __fmul_rn(n, LN2_HI));
+  r = __fsub_rn(r, __fmul_rn(n, LN2_LO));
+  float p = C[7];
+#pragma unroll
+  for (int k = 6; k >= 0; k--) p = __fadd_rn(__fmul_rn(p, r), C[k]);
+  const int e = (int)n + 32;
+  if (e < 0) return 0ull;
+  const float v = __fmul_rn(p, __int_as_float((e + 127) << 23));
+  return (uint64_t)v;  // truncation: exact floor of a non-negative value
+}
+
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+  for (int round = 0; round < 10; round++) {
+    if (round > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const uint32_t hi0 = __umulhi(M0, c[0]), lo0 = M0 * c[0];
+    const uint32_t hi1 = __umulhi(M1, c[2]), lo1 = M1 * c[2];
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+  }
+}
+
+__device__ __forceinline__ void uniforms(uint64_t seed, uint64_t slot, uint32_t seq_id,
+                                         uint32_t out[4]) {
+  out[0] = (uint32_t)slot;
+  out[1] = (uint32_t)(slot >> 32);
+  out[2] = seq_id;
+  out[3] = 0u;  // domain 0: the target sampler
+  philox4x32_10(out, (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// floor(U * total / 2^32) without overflowing 128 bits
+__device__ __forceinline__ u128 scaled_threshold(uint32_t U, u128 total) {
+  const u128 hi = total >> 32, lo = total & 0xFFFFFFFFull;
+  return (u128)U * hi + (((u128)U * lo) >> 32);
+}
+
+// ---------------------------------------------------------------------------
+// greedy
+// ---------------------------------------------------------------------------
+__global__ void accept_greedy_kernel(const int32_t* __restrict__ argmax,
+                                     const int32_t* __restrict__ draft, int n_seq, int d,
+                                     int32_t* __restrict__ n_acc, int32_t* __restrict__ em) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seq) return;
+  const int32_t* am = argmax + (size_t)s * (d + 1);
+  const int32_t* dr = draft + (size_t)s * d;
+  int32_t* e = em + (size_t)s * (d + 1);
+  int a = 0;
+  while (a < d && am[a] == dr[a]) {
+    e[a] = dr[a];
+    a++;
+  }
+  e[a] = am[a];
+  for (int i = a + 1; i <= d; i++) e[i] = -1;
+  n_acc[s] = a;
+}
+
+// ---------------------------------------------------------------------------
+// stochastic, step 1: per-row (max z, S = sum W) with a cluster of CTAs per
+// row; each CTA keeps its slice of z in shared memory, so the row is read
+// from HBM once.  Rows: p rows 0..d then q rows 0..d-1 of every sequence.
+// ---------------------------------------------------------------------------
+constexpr int ST_CLUSTER = 8;
+constexpr int ST_THREADS = 512;
+constexpr int ST_MAX_SMEM = 200 * 1024;  // z slice per CTA: V <= 8 * 51200
+
+__global__ void __launch_bounds__(ST_THREADS)
+row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int d, int V,
+                 float T, float* __restrict__ row_max,
+                 unsigned long long* __restrict__ row_sum, uint32_t* __restrict__ err) {
+  extern __shared__ float zs[];
+  __shared__ float s_red[ST_THREADS / 32];
+  __shared__ unsigned long long s_red64[ST_THREADS / 32];
+  __shared__ float s_cmax;
+  __shared__ unsigned long long s_csum;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.x / ST_CLUSTER;  // global row id: seq * (2d+1) + rr
+  const int rows_per_seq = 2 * d + 1;
+  const int s = row / rows_per_seq, rr = row % rows_per_seq;
+  const float* src = rr <= d ? p + ((size_t)s * (d + 1) + rr) * V
+                             : q + ((size_t)s * d + (rr - d - 1)) * V;
+  const int slice = (V + ST_CLUSTER - 1) / ST_CLUSTER;
+  const int v0 = rank * slice, v1 = min(V, v0 + slice);
+  float mx = -INFINITY;
+  bool bad = false;
+  for (int v = v0 + threadIdx.x; v < v1; v += ST_THREADS) {
+    const float l = __ldcs(src + v);
+    bad |= !isfinite(l);
+    const float z = __fdiv_rn(l, T);
+    zs[v - v0] = z;
+    mx = fmaxf(mx, z);
+  }
+  if (bad) atomicOr(err, ERR_NONFINITE);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = s_red[0];
+    for (int w = 1; w < ST_THREADS / 32; w++) m = fmaxf(m, s_red[w]);
+    s_cmax = m;
+  }
+  cluster.sync();
+  float gmax = -INFINITY;
+  for (int rk = 0; rk < ST_CLUSTER; rk++) gmax = fmaxf(gmax, *cluster.map_shared_rank(&s_cmax, rk));
+  unsigned long long acc = 0ull;
+  for (int v = v0 + threadIdx.x; v < v1; v += ST_THREADS)
+    acc += int_weight(__fsub_rn(zs[v - v0], gmax));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if ((threadIdx.x & 31) == 0) s_red64[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0ull;
+    for (int w = 0; w < ST_THREADS / 32; w++) t += s_red64[w];
+    s_csum = t;
+  }
+  cluster.sync();
+  if (rank == 0 && threadIdx.x == 0) {
+    unsigned long long tot = 0ull;
+    for (int rk = 0; rk < ST_CLUSTER; rk++) tot += *cluster.map_shared_rank(&s_csum, rk);
+    row_max[row] = gmax;
+    row_sum[row] = tot;
+  }
+  cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+// ---------------------------------------------------------------------------
+// stochastic, step 2: the sequential accept scan, one thread per sequence.
+// decision[s] = (a, row to sample from, U2, mode: 1 residual / 2 bonus / 0 error)
+// ---------------------------------------------------------------------------
+__global__ void decide_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                              const int32_t* __restrict__ draft, int n_seq, int d, int V,
+                              float T, uint64_t seed, const int32_t* __restrict__ seq_ids,
+                              const uint64_t* __restrict__ emit_idx, int emit_by_slot,
+                              int n_slots,
+                              const float* __restrict__ row_max,
+                              const unsigned long long* __restrict__ row_sum,
+                              int4* __restrict__ decision, int32_t* __restrict__ n_acc,
+                              int32_t* __restrict__ em, uint32_t* __restrict__ err) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seq) return;
+  const int rows_per_seq = 2 * d + 1;
+  const uint32_t sid = (uint32_t)seq_ids[s];
+  int32_t* e = em + (size_t)s * (d + 1);
+  for (int i = 0; i <= d; i++) e[i] = -1;
+  if (emit_by_slot && (int)sid >= n_slots) {  // also catches negative ids
+    atomicOr(err, ERR_SEQ);
+    decision[s] = make_int4(0, 0, 0, 0);
+    n_acc[s] = -1;
+    return;
+  }
+  const uint64_t e0 = emit_idx[emit_by_slot ? (int)sid : s];
+  int a = 0;
+  for (; a < d; a++) {
+    const int x = draft[(size_t)s * d + a];
+    if (x < 0 || x >= V) {
+      atomicOr(err, ERR_TOKEN);
+      decision[s] = make_int4(a, a, 0, 0);
+      n_acc[s] = -1;
+      return;
+    }
+    const int rp = s * rows_per_seq + a, rq = s * rows_per_seq + d + 1 + a;
+    const float zp = __fdiv_rn(p[((size_t)s * (d + 1) + a) * V + x], T);
+    const float zq = __fdiv_rn(q[((size_t)s * d + a) * V + x], T);
+    const uint64_t Wx = int_weight(__fsub_rn(zp, row_max[rp]));
+    const uint64_t Wqx = int_weight(__fsub_rn(zq, row_max[rq]));
+    const uint64_t S = row_sum[rp], Sq = row_sum[rq];
+    uint32_t U[4];
+    uniforms(seed, e0 + (uint64_t)a, sid, U);
+    bool acc;
+    if (Wqx == 0ull) {
+      acc = Wx > 0ull;
+    } else {
+      const u128 lhs = (u128)U[0] * (u128)Wqx * (u128)S;
+      const u128 rhs = ((u128)Wx << 32) * (u128)Sq;
+      acc = lhs < rhs;
+    }
+    if (!acc) {
+      decision[s] = make_int4(a, a, (int)U[1], 1);
+      n_acc[s] = a;
+      return;
+    }
+    e[a] = x;
+  }
+  uint32_t U[4];
+  uniforms(seed, e0 + (uint64_t)d, sid, U);
+  decision[s] = make_int4(d, d, (int)U[1], 2);
+  n_acc[s] = d;
+}
+
+// ---------------------------------------------------------------------------
+// stochastic, step 3: resample one row per sequence.  One CTA per sequence:
+// per-warp sums of the masses over contiguous ranges (exact 128-bit integer
+// sums, order-free), a prefix over warps to find the range holding the
+// threshold, then one warp scans that range with a 128-bit warp prefix.
+// ---------------------------------------------------------------------------
+constexpr int RS_THREADS = 1024;
+constexpr int RS_WARPS = RS_THREADS / 32;
+
+__device__ __forceinline__ u128 shfl_u128(u128 v, int src) {
+  uint64_t lo = (uint64_t)v, hi = (uint64_t)(v >> 64);
+  lo = __shfl_sync(0xffffffffu, lo, src);
+  hi = __shfl_sync(0xffffffffu, hi, src);
+  return ((u128)hi << 64) | lo;
+}
+__device__ __forceinline__ u128 shfl_up_u128(u128 v, int delta) {
+  uint64_t lo = (uint64_t)v, hi = (uint64_t)(v >> 64);
+  lo = __shfl_up_sync(0xffffffffu, lo, delta);
+  hi = __shfl_up_sync(0xffffffffu, hi, delta);
+  return ((u128)hi << 64) | lo;
+}
+
+__device__ __forceinline__ u128 mass_of(int mode, const float* prow, const float* qrow,
+                                        int v, float T, float mp, float mq, uint64_t S,
+                                        uint64_t Sq) {
+  const uint64_t W = int_weight(__fsub_rn(__fdiv_rn(prow[v], T), mp));
+  if (mode == 2) return (u128)W;
+  const uint64_t Wq = int_weight(__fsub_rn(__fdiv_rn(qrow[v], T), mq));
+  const u128 a = (u128)W * Sq, b = (u128)Wq * S;
+  return a > b ? a - b : (u128)0;
+}
+
+__global__ void __launch_bounds__(RS_THREADS)
+resample_kernel(const float* __restrict__ p, const float* __restrict__ q, int n_seq, int d,
+                int V, float T, const float* __restrict__ row_max,
+                const unsigned long long* __restrict__ row_sum,
+                const int4* __restrict__ decision, int32_t* __restrict__ em,
+                uint32_t* __restrict__ err) {
+  const int s = blockIdx.x;
+  const int4 dec = decision[s];
+  const int mode = dec.w;
+  if (mode == 0) return;
+  const int a = dec.x, row = dec.y;
+  const uint32_t U2 = (uint32_t)dec.z;
+  const int rows_per_seq = 2 * d + 1;
+  const int rp = s * rows_per_seq + row;
+  const int rq = s * rows_per_seq + d + 1 + (row < d ? row : 0);
+  const float* prow = p + ((size_t)s * (d + 1) + row) * V;
+  const float* qrow = mode == 1 ? q + ((size_t)s * d + row) * V : nullptr;
+  const float mp = row_max[rp];
+  const float mq = mode == 1 ? row_max[rq] : 0.0f;
+  const uint64_t S = row_sum[rp];
+  const uint64_t Sq = mode == 1 ? row_sum[rq] : 0ull;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int span = (V + RS_WARPS - 1) / RS_WARPS;
+  const int v0 = warp * span, v1 = min(V, v0 + span);
+  u128 acc = 0;
+  for (int v = v0 + lane; v < v1; v += 32) acc += mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += shfl_u128(acc, lane ^ off);
+  __shared__ u128 s_w[RS_WARPS];
+  __shared__ int s_pick;
+  if (lane == 0) s_w[warp] = acc;
+  if (threadIdx.x == 0) s_pick = -1;
+  __syncthreads();
+  if (warp == 0) {
+    // total, threshold, and the warp range that holds it (lane 0 serially)
+    if (lane == 0) {
+      u128 total = 0;
+      for (int w = 0; w < RS_WARPS; w++) total += s_w[w];
+      if (total == 0) {
+        atomicOr(err, ERR_NONFINITE);
+      } else {
+        const u128 t = scaled_threshold(U2, total);
+        u128 cum = 0;
+        int w = 0;
+        for (; w < RS_WARPS; w++) {
+          if (cum + s_w[w] > t) break;
+          cum += s_w[w];
+        }
+        // stash (w, t - cum) for the scan warp
+        s_w[0] = t - cum;
+        s_pick = -2 - w;
+      }
+    }
+  }
+  __syncthreads();
+  if (s_pick == -1) return;
+  const int w = -2 - s_pick;
+  const u128 rem = s_w[0];  // threshold relative to the start of warp w's range
+  __syncthreads();
+  if (warp == 0) {
+    const int u0 = w * span, u1 = min(V, u0 + span);
+    u128 base = 0;
+    int found = -1;
+    for (int vb = u0; vb < u1 && found < 0; vb += 32) {
+      const int v = vb + lane;
+      u128 m = v < u1 ? mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq) : (u128)0;
+      // inclusive warp prefix
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const u128 o = shfl_up_u128(m, off);
+        if (lane >= off) m += o;
+      }
+      const bool hit = v < u1 && base + m > rem;
+      const unsigned ball = __ballot_sync(0xffffffffu, hit);
+      if (ball) found = vb + __ffs(ball) - 1;
+      base += shfl_u128(m, 31);
+    }
+    if (lane == 0) em[(size_t)s * (d + 1) + a] = found;
+  }
+}
+
+// Standalone accept: on a device error the outputs read -1 and the sampler
+// state is left alone; otherwise emit_idx advances by the emitted count.
+__global__ void stoch_finalize_kernel(int n_seq, int d, int32_t* __restrict__ n_acc,
+                                      int32_t* __restrict__ em, uint64_t* __restrict__ emit_idx,
+                                      const uint32_t* __restrict__ err) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seq) return;
+  const int a = n_acc[s];
+  int32_t* e = em + (size_t)s * (d + 1);
+  if (*err != 0u || a < 0 || a > d || e[a] < 0) {
+    n_acc[s] = -1;
+    for (int i = 0; i <= d; i++) e[i] = -1;
+    return;
+  }
+  emit_idx[s] += (uint64_t)(a + 1);
+}
+
+// Commit ("Model-neutral Speculative Decoding", "The exactness transaction",
+// steps 5-6): advance the position and the sampler slot by the emitted count
+// and make the last emitted token the next anchor; on a device error nothing
+// is committed and the round's outputs read -1.
+__global__ void commit_kernel(const int32_t* __restrict__ seq_ids, int n_seq, int d, int n_slots,
+                              const int32_t* __restrict__ n_acc_in,
+                              int32_t* __restrict__ n_acc, int32_t* __restrict__ em,
+                              int32_t* __restrict__ n_past, uint64_t* __restrict__ emit_idx,
+                              int32_t* __restrict__ anchor, const uint32_t* __restrict__ err) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= n_seq) return;
+  const int a = n_acc_in[s];
+  int32_t* e = em + (size_t)s * (d + 1);
+  const int slot = seq_ids[s];
+  const bool bad = *err != 0u || a < 0 || a > d || slot < 0 || slot >= n_slots || e[a] < 0;
+  if (bad) {
+    n_acc[s] = -1;
+    for (int i = 0; i <= d; i++) e[i] = -1;
+    return;
+  }
+  n_acc[s] = a;
+  n_past[slot] += a + 1;
+  emit_idx[slot] += (uint64_t)(a + 1);
+  anchor[slot] = e[a];
+}
+
+}  // namespace
+
+size_t stoch_rows_needed(int n_seq, int d) { return (size_t)n_seq * (2 * d + 1); }
+
+void launch_accept_greedy(const int32_t* argmax, const int32_t* draft, int n_seq, int d,
+                          int32_t* n_acc, int32_t* emitted, cudaStream_t st) {
+  accept_greedy_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(argmax, draft, n_seq, d, n_acc,
+                                                            emitted);
+}
+
+int launch_accept_stochastic(const float* p, const float* q, const int32_t* draft, int n_seq,
+                             int d, int V, float T, uint64_t seed, const int32_t* seq_ids,
+                             uint64_t* emit_idx, int emit_by_slot, int n_slots, int32_t* n_acc,
+                             int32_t* emitted, const StochScratch& scr, uint32_t* err,
+                             cudaStream_t st) {
+  const size_t nrows = stoch_rows_needed(n_seq, d);
+  if (nrows > scr.rows_cap || (size_t)n_seq > scr.seq_cap)
+    return fail(SPEC_E_SHAPE, "stochastic accept: scratch too small");
+  const int slice = (V + ST_CLUSTER - 1) / ST_CLUSTER;
+  const size_t smem = (size_t)slice * sizeof(float);
+  if (smem > ST_MAX_SMEM) return fail(SPEC_E_SHAPE, "stochastic accept: vocabulary too large");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(nrows * ST_CLUSTER));
+  cfg.blockDim = dim3(ST_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ST_CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, row_stats_kernel, p, q, d, V, T, scr.row_max,
+                                     scr.row_sum, err);
+  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("row stats: ") + cudaGetErrorString(e));
+  decide_kernel<<<(n_seq + 63) / 64, 64, 0, st>>>(p, q, draft, n_seq, d, V, T, seed, seq_ids,
+                                                  emit_idx, emit_by_slot, n_slots, scr.row_max, scr.row_sum,
+                                                  scr.decision, n_acc, emitted, err);
+  resample_kernel<<<n_seq, RS_THREADS, 0, st>>>(p, q, n_seq, d, V, T, scr.row_max, scr.row_sum,
+                                                scr.decision, emitted, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("stochastic accept: ") + cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+void launch_commit(const int32_t* seq_ids, int n_seq, int d, int n_slots, const int32_t* n_acc_in,
+                   int32_t* n_acc, int32_t* emitted, int32_t* n_past, uint64_t* emit_idx,
+                   int32_t* anchor, const uint32_t* err, cudaStream_t st) {
+  commit_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(seq_ids, n_seq, d, n_slots, n_acc_in, n_acc,
+                                                     emitted, n_past, emit_idx, anchor, err);
+}
+
+void stoch_finalize(int n_seq, int d, int32_t* n_acc, int32_t* emitted, uint64_t* emit_idx,
+                    const uint32_t* err, cudaStream_t st) {
+  stoch_finalize_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(n_seq, d, n_acc, emitted, emit_idx,
+                                                             err);
+}
+
+void accept_init_attrs() {
+  cudaFuncSetAttribute(row_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ST_MAX_SMEM);
+}

@@ -1,0 +1,709 @@
+// api.cu -- the C ABI of the verify-round library: packed matrices, the
+// decoder model object, per-sequence transaction state, the verify round
+// (one weights-once target pass, accept, commit) and CUDA-graph replay.
+//
+// The round follows "Model-neutral Speculative Decoding", section "The
+// exactness transaction", steps 3-6, and "Speculative Decoding (D5-R) --
+// Plan", section 3 "Mechanism -- one round".  Step 1 (checkpoint) and step 7
+// (restore) reduce to the per-sequence triple (n_past, emit_idx, anchor):
+// the commit kernel is the only writer of that triple and it is skipped when
+// the device error word is set, so a failed round leaves the last committed
+// transaction in place; rejected KV rows need no restore because positions
+// are data and are overwritten by the next round.
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+static thread_local std::string g_last_error;
+void set_error(const std::string& msg) { g_last_error = msg; }
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+extern "C" void spec_last_error(char* buf, size_t len) {
+  if (buf == nullptr || len == 0) return;
+  size_t n = std::min(len - 1, g_last_error.size());
+  memcpy(buf, g_last_error.data(), n);
+  buf[n] = '\0';
+}
+
+static cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Kernel attributes that must be set before any launch (and outside stream
+// capture); once per device.
+void attn_init_attrs();
+void accept_init_attrs();
+static std::mutex g_attr_mu;
+static std::vector<int> g_attr_done;
+static void init_attrs_once() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (std::find(g_attr_done.begin(), g_attr_done.end(), dev) != g_attr_done.end()) return;
+  attn_init_attrs();
+  accept_init_attrs();
+  g_attr_done.push_back(dev);
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+// ---------------------------------------------------------------------------
+// per-device workspace of the standalone entry points (grown on demand)
+// ---------------------------------------------------------------------------
+struct Workspace {
+  StochScratch st;
+  void* st_base = nullptr;
+  uint32_t* err = nullptr;
+};
+static std::mutex g_ws_mu;
+static std::map<int, Workspace> g_ws;
+
+static int workspace_get(size_t rows, size_t seqs, Workspace** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_ws_mu);
+  Workspace& w = g_ws[dev];
+  if (w.err == nullptr) {
+    if (cudaMalloc(&w.err, sizeof(uint32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(SPEC_E_OOM, "workspace error word");
+    }
+    CUDA_TRY(cudaMemset(w.err, 0, sizeof(uint32_t)));
+  }
+  if (rows > w.st.rows_cap || seqs > w.st.seq_cap) {
+    rows = std::max(rows, w.st.rows_cap);
+    seqs = std::max(seqs, w.st.seq_cap);
+    if (w.st_base) {
+      CUDA_TRY(cudaDeviceSynchronize());
+      cudaFree(w.st_base);
+      w.st_base = nullptr;
+    }
+    size_t bytes = rows * (sizeof(float) + sizeof(unsigned long long)) + seqs * sizeof(int4) + 64;
+    if (cudaMalloc(&w.st_base, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      w.st = StochScratch();
+      return fail(SPEC_E_OOM, "workspace");
+    }
+    char* p = (char*)w.st_base;
+    w.st.row_sum = (unsigned long long*)p;
+    p += rows * sizeof(unsigned long long);
+    w.st.decision = (int4*)p;
+    p += seqs * sizeof(int4);
+    w.st.row_max = (float*)p;
+    w.st.rows_cap = rows;
+    w.st.seq_cap = seqs;
+  }
+  *out = &w;
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// packed matrices
+// ---------------------------------------------------------------------------
+struct spec_qmat {
+  QMat w;
+  int max_rows = 0;
+  LinScratch scr;
+  void* scr_base = nullptr;
+};
+
+static int alloc_lin_scratch(const std::vector<const QMat*>& mats, int R, LinScratch* scr,
+                             void** base) {
+  size_t part = 0, tick = 1, amax = 16;
+  for (const QMat* q : mats) {
+    part = std::max(part, lin_part_floats(*q, R));
+    tick = std::max(tick, lin_tickets_needed(*q, R));
+    amax = std::max(amax, lin_amax_entries(*q, R));
+  }
+  tick = std::max(tick, (size_t)64);
+  const size_t bytes = part * sizeof(float) + amax * sizeof(float2) + tick * sizeof(unsigned) + 256;
+  if (cudaMalloc(base, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SPEC_E_OOM, "linear scratch");
+  }
+  char* p = (char*)*base;
+  scr->part = (float*)p;
+  scr->part_floats = part;
+  p += part * sizeof(float);
+  scr->amax_part = (float2*)p;
+  scr->amax_entries = amax;
+  p += amax * sizeof(float2);
+  scr->tickets = (unsigned*)p;
+  scr->n_tickets = tick;
+  CUDA_TRY(cudaMemset(scr->tickets, 0, tick * sizeof(unsigned)));
+  return SPEC_OK;
+}
+
+extern "C" int spec_qmat_create(const spec_qweight* w, int max_rows, void* stream,
+                                spec_qmat** out) {
+  if (out == nullptr || w == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  *out = nullptr;
+  if (max_rows < 1 || max_rows > 16 * 1024) return fail(SPEC_E_SHAPE, "max_rows out of range");
+  if (!aligned16(w->qs) || !aligned16(w->scales) || (w->qh && !aligned16(w->qh)))
+    ;  // canonical planes are read bytewise: no alignment requirement
+  init_attrs_once();
+  cudaStream_t st = as_stream(stream);
+  spec_qmat* m = new spec_qmat();
+  int rc = qmat_pack(w, PERM_IDENTITY, 0, sm_count(), st, &m->w);
+  if (rc != SPEC_OK) {
+    delete m;
+    return rc;
+  }
+  m->max_rows = max_rows;
+  rc = alloc_lin_scratch({&m->w}, max_rows, &m->scr, &m->scr_base);
+  if (rc == SPEC_OK && cudaStreamSynchronize(st) != cudaSuccess)
+    rc = fail(SPEC_E_CUDA, std::string("repack: ") + cudaGetErrorString(cudaGetLastError()));
+  if (rc != SPEC_OK) {
+    qmat_free(&m->w);
+    if (m->scr_base) cudaFree(m->scr_base);
+    delete m;
+    return rc;
+  }
+  *out = m;
+  return SPEC_OK;
+}
+
+extern "C" int spec_qmat_destroy(spec_qmat* m) {
+  if (m == nullptr) return SPEC_OK;
+  cudaDeviceSynchronize();
+  qmat_free(&m->w);
+  if (m->scr_base) cudaFree(m->scr_base);
+  delete m;
+  return SPEC_OK;
+}
+
+extern "C" int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
+                             void* stream) {
+  if (w == nullptr || x == nullptr || y == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  if (nt < 1 || nt > w->max_rows) return fail(SPEC_E_SHAPE, "nt outside [1, max_rows]");
+  if (!aligned16(x)) return fail(SPEC_E_SHAPE, "x must be 16-byte aligned");
+  LinEpi e;
+  e.kind = EPI_STORE;
+  e.y = y;
+  e.ldy = w->w.N;
+  return linear_launch(w->w, reinterpret_cast<const __half*>(x), nt, e, w->scr, as_stream(stream));
+}
+
+// ---------------------------------------------------------------------------
+// model
+// ---------------------------------------------------------------------------
+struct spec_model {
+  spec_model_desc d{};
+  int device = 0, sms = 1;
+  __half* embed = nullptr;
+  float* norm_w = nullptr;
+  std::vector<QMat> wqkv, wo, wgu, wd;
+  QMat lm;
+  __half* kc = nullptr;
+  __half* vc = nullptr;
+  size_t layer_elems = 0;  // per-layer cache elements
+  float2* rope = nullptr;
+  int32_t* n_past = nullptr;
+  uint64_t* emit_idx = nullptr;
+  int32_t* anchor = nullptr;
+  uint32_t* err = nullptr;
+  int Rmax = 0;
+  float* h = nullptr;
+  __half* xa = nullptr;   // norm output [R][H]
+  __half* xs = nullptr;   // SwiGLU output [R][F]
+  __half* qbuf = nullptr; // [R][nq][hd]
+  __half* ao = nullptr;   // attention output [R][nq*hd]
+  float* logits = nullptr;
+  int32_t* argmax = nullptr;
+  RowInfo* rows = nullptr;
+  int32_t* tokens = nullptr;
+  int32_t* seq_ids_buf = nullptr;
+  int32_t* draft_buf = nullptr;
+  int32_t* nacc_tmp = nullptr;
+  float* attn_part = nullptr;
+  LinScratch lscr;
+  StochScratch sscr;
+  std::vector<void*> allocs;
+  bool use_graphs = true;
+  cudaStream_t cap_stream = nullptr;
+  std::map<long long, cudaGraphExec_t> graphs;
+  size_t weight_bytes = 0;
+};
+
+static int dalloc(spec_model* m, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  if (cudaMalloc(p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(SPEC_E_OOM, "cudaMalloc of " + std::to_string(bytes) + " bytes failed");
+  }
+  m->allocs.push_back(*p);
+  return SPEC_OK;
+}
+template <typename T>
+static int dalloc_t(spec_model* m, T** p, size_t count) {
+  return dalloc(m, reinterpret_cast<void**>(p), count * sizeof(T));
+}
+
+static void model_free(spec_model* m) {
+  cudaDeviceSynchronize();
+  for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
+  m->graphs.clear();
+  for (auto* v : {&m->wqkv, &m->wo, &m->wgu, &m->wd})
+    for (auto& q : *v) qmat_free(&q);
+  qmat_free(&m->lm);
+  for (void* p : m->allocs) cudaFree(p);
+  m->allocs.clear();
+  if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  delete m;
+}
+
+static int check_desc(const spec_model_desc* D, const spec_model_weights* W) {
+  if (D == nullptr || W == nullptr) return fail(SPEC_E_INVALID, "null desc or weights");
+  if (D->n_layers < 0 || D->hidden <= 0 || D->vocab <= 0 || D->max_nt < 1 ||
+      D->max_nt > SPEC_MAX_NT || D->max_seqs < 1 || D->max_ctx < 1)
+    return fail(SPEC_E_SHAPE, "bad model dimensions");
+  if (D->hidden % 64 != 0) return fail(SPEC_E_SHAPE, "hidden must be a multiple of 64");
+  if (D->vocab % 16 != 0) return fail(SPEC_E_SHAPE, "vocab must be a multiple of 16");
+  if (!(D->rms_eps >= 0.0f)) return fail(SPEC_E_INVALID, "rms_eps must be >= 0");
+  if (D->n_layers > 0) {
+    if (D->head_dim != 64 && D->head_dim != 128)
+      return fail(SPEC_E_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (D->n_q_heads <= 0 || D->n_kv_heads <= 0 || D->n_q_heads % D->n_kv_heads != 0)
+      return fail(SPEC_E_SHAPE, "n_q_heads must be a positive multiple of n_kv_heads");
+    if (D->ffn <= 0 || D->ffn % 32 != 0) return fail(SPEC_E_SHAPE, "ffn must be a multiple of 32");
+    if ((D->n_q_heads * D->head_dim) % 32 != 0) return fail(SPEC_E_SHAPE, "bad attention width");
+    if (W->embed == nullptr || W->wqkv == nullptr || W->wo == nullptr || W->wgu == nullptr ||
+        W->wd == nullptr)
+      return fail(SPEC_E_INVALID, "missing layer weights");
+    if (D->use_rope && !(D->rope_theta > 0.0f)) return fail(SPEC_E_INVALID, "rope_theta must be > 0");
+    const int H = D->hidden, hd = D->head_dim, nq = D->n_q_heads, nkv = D->n_kv_heads, F = D->ffn;
+    for (int l = 0; l < D->n_layers; l++) {
+      if (W->wqkv[l].N != (nq + 2 * nkv) * hd || W->wqkv[l].K != H)
+        return fail(SPEC_E_SHAPE, "wqkv shape");
+      if (W->wo[l].N != H || W->wo[l].K != nq * hd) return fail(SPEC_E_SHAPE, "wo shape");
+      if (W->wgu[l].N != 2 * F || W->wgu[l].K != H) return fail(SPEC_E_SHAPE, "wgu shape");
+      if (W->wd[l].N != H || W->wd[l].K != F) return fail(SPEC_E_SHAPE, "wd shape");
+      if (W->wqkv[l].qtype != SPEC_Q4 && W->wqkv[l].qtype != SPEC_Q6)
+        return fail(SPEC_E_UNSUPPORTED, "qtype");
+    }
+  }
+  if (W->lm_head.N != D->vocab || W->lm_head.K != D->hidden) return fail(SPEC_E_SHAPE, "lm_head shape");
+  if (W->norm_w == nullptr) return fail(SPEC_E_INVALID, "missing norm weights");
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_weights* w,
+                                 void* stream, spec_model** out) {
+  if (out == nullptr) return fail(SPEC_E_INVALID, "null out");
+  *out = nullptr;
+  int rc = check_desc(desc, w);
+  if (rc != SPEC_OK) return rc;
+  init_attrs_once();
+  cudaStream_t st = as_stream(stream);
+  spec_model* m = new spec_model();
+  m->d = *desc;
+  cudaGetDevice(&m->device);
+  m->sms = sm_count();
+  const spec_model_desc& D = m->d;
+  const int L = D.n_layers, H = D.hidden, V = D.vocab, hd = D.head_dim, nq = D.n_q_heads,
+            nkv = D.n_kv_heads, F = D.ffn;
+  m->Rmax = D.max_seqs * D.max_nt;
+  const int R = m->Rmax;
+#define TRY(x)                 \
+  do {                         \
+    int rc_ = (x);             \
+    if (rc_ != SPEC_OK) {      \
+      model_free(m);           \
+      return rc_;              \
+    }                          \
+  } while (0)
+  // weights
+  m->wqkv.resize(L);
+  m->wo.resize(L);
+  m->wgu.resize(L);
+  m->wd.resize(L);
+  for (int l = 0; l < L; l++) {
+    TRY(qmat_pack(&w->wqkv[l], PERM_ROPE_PAIRS, hd, m->sms, st, &m->wqkv[l]));
+    TRY(qmat_pack(&w->wo[l], PERM_IDENTITY, 0, m->sms, st, &m->wo[l]));
+    TRY(qmat_pack(&w->wgu[l], PERM_GATE_UP, 0, m->sms, st, &m->wgu[l]));
+    TRY(qmat_pack(&w->wd[l], PERM_IDENTITY, 0, m->sms, st, &m->wd[l]));
+    m->weight_bytes += m->wqkv[l].bytes + m->wo[l].bytes + m->wgu[l].bytes + m->wd[l].bytes;
+  }
+  TRY(qmat_pack(&w->lm_head, PERM_IDENTITY, 0, 0, st, &m->lm));
+  m->weight_bytes += m->lm.bytes;
+  TRY(dalloc_t(m, &m->norm_w, (size_t)(2 * L + 1) * H));
+  if (cudaMemcpyAsync(m->norm_w, w->norm_w, sizeof(float) * (2 * L + 1) * H,
+                      cudaMemcpyDefault, st) != cudaSuccess)
+    TRY(fail(SPEC_E_CUDA, "copy norm weights"));
+  if (L > 0) {
+    TRY(dalloc_t(m, &m->embed, (size_t)V * H));
+    if (cudaMemcpyAsync(m->embed, w->embed, sizeof(__half) * V * H, cudaMemcpyDefault, st) !=
+        cudaSuccess)
+      TRY(fail(SPEC_E_CUDA, "copy embedding"));
+    m->layer_elems = (size_t)D.max_seqs * nkv * D.max_ctx * hd;
+    TRY(dalloc_t(m, &m->kc, m->layer_elems * L));
+    TRY(dalloc_t(m, &m->vc, m->layer_elems * L));
+    if (cudaMemsetAsync(m->kc, 0, sizeof(__half) * m->layer_elems * L, st) != cudaSuccess ||
+        cudaMemsetAsync(m->vc, 0, sizeof(__half) * m->layer_elems * L, st) != cudaSuccess)
+      TRY(fail(SPEC_E_CUDA, "clear KV cache"));
+    TRY(dalloc_t(m, &m->rope, (size_t)D.max_ctx * (hd / 2)));
+    launch_rope_table(m->rope, D.max_ctx, hd, D.rope_theta > 0 ? D.rope_theta : 10000.0f, st);
+    TRY(dalloc_t(m, &m->qbuf, (size_t)R * nq * hd));
+    TRY(dalloc_t(m, &m->ao, (size_t)R * nq * hd));
+    TRY(dalloc_t(m, &m->xs, (size_t)R * F));
+    TRY(dalloc_t(m, &m->attn_part, attn_part_floats(D.max_seqs, nkv, D.max_ctx, D.max_nt,
+                                                    nq / nkv, hd)));
+  }
+  TRY(dalloc_t(m, &m->n_past, D.max_seqs));
+  TRY(dalloc_t(m, &m->emit_idx, D.max_seqs));
+  TRY(dalloc_t(m, &m->anchor, D.max_seqs));
+  TRY(dalloc_t(m, &m->err, 1));
+  cudaMemsetAsync(m->n_past, 0, sizeof(int32_t) * D.max_seqs, st);
+  cudaMemsetAsync(m->emit_idx, 0, sizeof(uint64_t) * D.max_seqs, st);
+  cudaMemsetAsync(m->anchor, 0, sizeof(int32_t) * D.max_seqs, st);
+  cudaMemsetAsync(m->err, 0, sizeof(uint32_t), st);
+  TRY(dalloc_t(m, &m->h, (size_t)R * H));
+  TRY(dalloc_t(m, &m->xa, (size_t)R * H));
+  TRY(dalloc_t(m, &m->logits, (size_t)R * V));
+  TRY(dalloc_t(m, &m->argmax, R));
+  TRY(dalloc_t(m, &m->rows, R));
+  TRY(dalloc_t(m, &m->tokens, R));
+  TRY(dalloc_t(m, &m->seq_ids_buf, D.max_seqs));
+  TRY(dalloc_t(m, &m->draft_buf, (size_t)D.max_seqs * D.max_nt));
+  TRY(dalloc_t(m, &m->nacc_tmp, D.max_seqs));
+  // scratch
+  std::vector<const QMat*> mats{&m->lm};
+  for (int l = 0; l < L; l++) {
+    mats.push_back(&m->wqkv[l]);
+    mats.push_back(&m->wo[l]);
+    mats.push_back(&m->wgu[l]);
+    mats.push_back(&m->wd[l]);
+  }
+  {
+    void* base = nullptr;
+    TRY(alloc_lin_scratch(mats, R, &m->lscr, &base));
+    m->allocs.push_back(base);
+  }
+  m->sscr.rows_cap = stoch_rows_needed(D.max_seqs, D.max_nt - 1);
+  m->sscr.seq_cap = D.max_seqs;
+  TRY(dalloc_t(m, &m->sscr.row_max, m->sscr.rows_cap));
+  TRY(dalloc_t(m, &m->sscr.row_sum, m->sscr.rows_cap));
+  TRY(dalloc_t(m, &m->sscr.decision, m->sscr.seq_cap));
+  if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+    TRY(fail(SPEC_E_CUDA, "capture stream"));
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) TRY(fail(SPEC_E_CUDA, std::string("model create: ") + cudaGetErrorString(e)));
+#undef TRY
+  *out = m;
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_destroy(spec_model* m) {
+  if (m) model_free(m);
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_kv_cache(spec_model* m, int layer, uint16_t** k, uint16_t** v) {
+  if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
+  if (layer < 0 || layer >= m->d.n_layers) return fail(SPEC_E_SHAPE, "layer out of range");
+  if (k) *k = reinterpret_cast<uint16_t*>(m->kc + m->layer_elems * layer);
+  if (v) *v = reinterpret_cast<uint16_t*>(m->vc + m->layer_elems * layer);
+  return SPEC_OK;
+}
+
+extern "C" int spec_kv_fill(spec_model* m, int layer, int seq, int pos0, int n_pos,
+                            const uint16_t* k, const uint16_t* v, void* stream) {
+  if (m == nullptr || k == nullptr || v == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  const spec_model_desc& D = m->d;
+  if (layer < 0 || layer >= D.n_layers || seq < 0 || seq >= D.max_seqs)
+    return fail(SPEC_E_SHAPE, "layer or slot out of range");
+  if (pos0 < 0 || n_pos < 0 || pos0 + n_pos > D.max_ctx) return fail(SPEC_E_SHAPE, "positions out of range");
+  if (n_pos == 0) return SPEC_OK;
+  const size_t row = (size_t)D.head_dim * sizeof(__half);
+  for (int which = 0; which < 2; which++) {
+    __half* base = (which == 0 ? m->kc : m->vc) + m->layer_elems * layer +
+                   ((size_t)seq * D.n_kv_heads * D.max_ctx + pos0) * D.head_dim;
+    const uint16_t* src = which == 0 ? k : v;
+    // n_kv_heads blocks of n_pos rows; destination pitch max_ctx rows
+    CUDA_TRY(cudaMemcpy2DAsync(base, row * D.max_ctx, src, row * n_pos, row * n_pos, D.n_kv_heads,
+                               cudaMemcpyDefault, as_stream(stream)));
+  }
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_set_graphs(spec_model* m, int enable) {
+  if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
+  m->use_graphs = enable != 0;
+  return SPEC_OK;
+}
+
+extern "C" int spec_state_set(spec_model* m, int n, const int32_t* seq_ids,
+                              const int32_t* n_past, const uint64_t* emit_idx,
+                              const int32_t* anchor) {
+  if (m == nullptr || (n > 0 && seq_ids == nullptr)) return fail(SPEC_E_INVALID, "null argument");
+  for (int i = 0; i < n; i++) {
+    const int s = seq_ids[i];
+    if (s < 0 || s >= m->d.max_seqs) return fail(SPEC_E_INVALID, "sequence slot out of range");
+    if (n_past && (n_past[i] < 0 || n_past[i] > m->d.max_ctx))
+      return fail(SPEC_E_INVALID, "n_past out of range");
+    if (anchor && (anchor[i] < 0 || anchor[i] >= m->d.vocab))
+      return fail(SPEC_E_INVALID, "anchor id out of range");
+  }
+  for (int i = 0; i < n; i++) {
+    const int s = seq_ids[i];
+    if (n_past) CUDA_TRY(cudaMemcpy(m->n_past + s, n_past + i, 4, cudaMemcpyHostToDevice));
+    if (emit_idx) CUDA_TRY(cudaMemcpy(m->emit_idx + s, emit_idx + i, 8, cudaMemcpyHostToDevice));
+    if (anchor) CUDA_TRY(cudaMemcpy(m->anchor + s, anchor + i, 4, cudaMemcpyHostToDevice));
+  }
+  return SPEC_OK;
+}
+
+extern "C" int spec_state_get(spec_model* m, int n, const int32_t* seq_ids, int32_t* n_past,
+                              uint64_t* emit_idx, int32_t* anchor) {
+  if (m == nullptr || (n > 0 && seq_ids == nullptr)) return fail(SPEC_E_INVALID, "null argument");
+  CUDA_TRY(cudaDeviceSynchronize());
+  for (int i = 0; i < n; i++) {
+    const int s = seq_ids[i];
+    if (s < 0 || s >= m->d.max_seqs) return fail(SPEC_E_INVALID, "sequence slot out of range");
+    if (n_past) CUDA_TRY(cudaMemcpy(n_past + i, m->n_past + s, 4, cudaMemcpyDeviceToHost));
+    if (emit_idx) CUDA_TRY(cudaMemcpy(emit_idx + i, m->emit_idx + s, 8, cudaMemcpyDeviceToHost));
+    if (anchor) CUDA_TRY(cudaMemcpy(anchor + i, m->anchor + s, 4, cudaMemcpyDeviceToHost));
+  }
+  return SPEC_OK;
+}
+
+extern "C" int spec_error_check(spec_model* m, void* stream, uint32_t* bits) {
+  CUDA_TRY(cudaStreamSynchronize(as_stream(stream)));
+  uint32_t* dev_err = nullptr;
+  if (m != nullptr) {
+    dev_err = m->err;
+  } else {
+    Workspace* w = nullptr;
+    int rc = workspace_get(0, 0, &w);
+    if (rc != SPEC_OK) return rc;
+    dev_err = w->err;
+  }
+  uint32_t v = 0;
+  CUDA_TRY(cudaMemcpy(&v, dev_err, 4, cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(dev_err, 0, 4));
+  if (bits) *bits = v;
+  if (v != 0) return fail(SPEC_E_INVALID, "device error word set: 0x" + std::to_string(v));
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// the target pass
+// ---------------------------------------------------------------------------
+static int enqueue_forward(spec_model* m, int n_seq, int nt, bool write_logits, cudaStream_t st) {
+  const spec_model_desc& D = m->d;
+  const int R = n_seq * nt, H = D.hidden, F = D.ffn, hd = D.head_dim, nq = D.n_q_heads,
+            nkv = D.n_kv_heads, V = D.vocab;
+  launch_embed_rows(m->embed, V, H, m->anchor, m->draft_buf, m->seq_ids_buf, n_seq, nt,
+                    m->n_past, D.max_seqs, D.max_ctx, m->rows, m->tokens, m->h, m->err, st);
+  for (int l = 0; l < D.n_layers; l++) {
+    __half* kc = m->kc + m->layer_elems * l;
+    __half* vc = m->vc + m->layer_elems * l;
+    launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * l) * H, R, H, D.rms_eps, m->xa, st);
+    LinEpi eq;
+    eq.kind = EPI_QKV;
+    eq.out16 = m->qbuf;
+    eq.kcache = kc;
+    eq.vcache = vc;
+    eq.rows = m->rows;
+    eq.rope = D.use_rope ? m->rope : nullptr;
+    eq.nq = nq;
+    eq.nkv = nkv;
+    eq.hd = hd;
+    eq.max_ctx = D.max_ctx;
+    int rc = linear_launch(m->wqkv[l], m->xa, R, eq, m->lscr, st);
+    if (rc) return rc;
+    rc = attn_launch(m->qbuf, kc, vc, m->rows, n_seq, nt, nq, nkv, hd, D.max_ctx, m->attn_part,
+                     m->ao, st);
+    if (rc) return rc;
+    LinEpi er;
+    er.kind = EPI_RESID;
+    er.y = m->h;
+    er.ldy = H;
+    rc = linear_launch(m->wo[l], m->ao, R, er, m->lscr, st);
+    if (rc) return rc;
+    launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * l + 1) * H, R, H, D.rms_eps, m->xa, st);
+    LinEpi es;
+    es.kind = EPI_SWIGLU;
+    es.out16 = m->xs;
+    es.ldo = F;
+    rc = linear_launch(m->wgu[l], m->xa, R, es, m->lscr, st);
+    if (rc) return rc;
+    rc = linear_launch(m->wd[l], m->xs, R, er, m->lscr, st);
+    if (rc) return rc;
+  }
+  launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * D.n_layers) * H, R, H, D.rms_eps, m->xa, st);
+  LinEpi el;
+  el.kind = EPI_LMHEAD;
+  el.y = write_logits ? m->logits : nullptr;
+  el.ldy = V;
+  el.argmax = m->argmax;
+  el.err = m->err;
+  return linear_launch(m->lm, m->xa, R, el, m->lscr, st);
+}
+
+static int run_forward(spec_model* m, int n_seq, int nt, bool write_logits, cudaStream_t st) {
+  if (!m->use_graphs) return enqueue_forward(m, n_seq, nt, write_logits, st);
+  const long long key = ((long long)n_seq << 20) | ((long long)nt << 1) | (write_logits ? 1 : 0);
+  auto it = m->graphs.find(key);
+  if (it == m->graphs.end()) {
+    cudaGraph_t g = nullptr;
+    CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = enqueue_forward(m, n_seq, nt, write_logits, m->cap_stream);
+    cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
+    if (rc != SPEC_OK) {
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+    if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e));
+    it = m->graphs.emplace(key, ex).first;
+  }
+  CUDA_TRY(cudaGraphLaunch(it->second, st));
+  return SPEC_OK;
+}
+
+extern "C" int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_ids,
+                                 const int32_t* draft, int d, const float* q_logits,
+                                 const spec_sampling* sampling, int32_t* n_acc,
+                                 int32_t* emitted, float* logits_out, void* stream) {
+  if (m == nullptr || seq_ids == nullptr || sampling == nullptr || n_acc == nullptr ||
+      emitted == nullptr)
+    return fail(SPEC_E_INVALID, "null argument");
+  const spec_model_desc& D = m->d;
+  if (D.n_layers == 0) return fail(SPEC_E_UNSUPPORTED, "verify round needs a decoder (n_layers > 0)");
+  if (n_seq < 1 || n_seq > D.max_seqs) return fail(SPEC_E_SHAPE, "n_seq outside [1, max_seqs]");
+  if (d < 0 || d + 1 > D.max_nt) return fail(SPEC_E_SHAPE, "d + 1 outside [1, max_nt]");
+  if (d > 0 && draft == nullptr) return fail(SPEC_E_INVALID, "null draft");
+  const bool greedy = sampling->greedy != 0;
+  if (!greedy) {
+    if (!(sampling->temperature > 0.0f) || !std::isfinite(sampling->temperature))
+      return fail(SPEC_E_INVALID, "temperature must be finite and > 0");
+    if (d > 0 && q_logits == nullptr) return fail(SPEC_E_INVALID, "stochastic accept needs q_logits");
+  } else if (q_logits != nullptr) {
+    return fail(SPEC_E_INVALID, "q_logits must be NULL in greedy mode");
+  }
+  cudaStream_t st = as_stream(stream);
+  const int nt = d + 1;
+  CUDA_TRY(cudaMemcpyAsync(m->seq_ids_buf, seq_ids, sizeof(int32_t) * n_seq,
+                           cudaMemcpyDeviceToDevice, st));
+  if (d > 0)
+    CUDA_TRY(cudaMemcpyAsync(m->draft_buf, draft, sizeof(int32_t) * n_seq * d,
+                             cudaMemcpyDeviceToDevice, st));
+  const bool write_logits = !greedy || logits_out != nullptr;
+  int rc = run_forward(m, n_seq, nt, write_logits, st);
+  if (rc != SPEC_OK) return rc;
+  if (greedy) {
+    launch_accept_greedy(m->argmax, m->draft_buf, n_seq, d, m->nacc_tmp, emitted, st);
+  } else {
+    rc = launch_accept_stochastic(m->logits, q_logits, m->draft_buf, n_seq, d, D.vocab,
+                                  sampling->temperature, sampling->seed, m->seq_ids_buf,
+                                  m->emit_idx, 1, D.max_seqs, m->nacc_tmp, emitted, m->sscr,
+                                  m->err, st);
+    if (rc != SPEC_OK) return rc;
+  }
+  launch_commit(m->seq_ids_buf, n_seq, d, D.max_seqs, m->nacc_tmp, n_acc, emitted, m->n_past,
+                m->emit_idx,
+                m->anchor, m->err, st);
+  if (logits_out != nullptr)
+    CUDA_TRY(cudaMemcpyAsync(logits_out, m->logits, sizeof(float) * n_seq * nt * D.vocab,
+                             cudaMemcpyDeviceToDevice, st));
+  CUDA_TRY(cudaGetLastError());
+  return SPEC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// standalone steps
+// ---------------------------------------------------------------------------
+extern "C" int spec_verify_attn(spec_model* m, int layer, int n_seq, const int32_t* seq_ids,
+                                int nt, const uint16_t* q, const uint16_t* k_new,
+                                const uint16_t* v_new, uint16_t* out, void* stream) {
+  if (m == nullptr || seq_ids == nullptr || q == nullptr || k_new == nullptr ||
+      v_new == nullptr || out == nullptr)
+    return fail(SPEC_E_INVALID, "null argument");
+  const spec_model_desc& D = m->d;
+  if (layer < 0 || layer >= D.n_layers) return fail(SPEC_E_SHAPE, "layer out of range");
+  if (n_seq < 1 || n_seq > D.max_seqs || nt < 1 || nt > D.max_nt)
+    return fail(SPEC_E_SHAPE, "n_seq or nt out of range");
+  if (!aligned16(q) || !aligned16(out)) return fail(SPEC_E_SHAPE, "q/out must be 16-byte aligned");
+  cudaStream_t st = as_stream(stream);
+  CUDA_TRY(cudaMemcpyAsync(m->seq_ids_buf, seq_ids, sizeof(int32_t) * n_seq,
+                           cudaMemcpyDeviceToDevice, st));
+  launch_row_info(m->seq_ids_buf, n_seq, nt, m->n_past, D.max_seqs, D.max_ctx, m->rows, m->err, st);
+  __half* kc = m->kc + m->layer_elems * layer;
+  __half* vc = m->vc + m->layer_elems * layer;
+  launch_kv_write(reinterpret_cast<const __half*>(k_new), reinterpret_cast<const __half*>(v_new),
+                  m->rows, n_seq * nt, D.n_kv_heads, D.head_dim, D.max_ctx, kc, vc, st);
+  return attn_launch(reinterpret_cast<const __half*>(q), kc, vc, m->rows, n_seq, nt, D.n_q_heads,
+                     D.n_kv_heads, D.head_dim, D.max_ctx, m->attn_part,
+                     reinterpret_cast<__half*>(out), st);
+}
+
+extern "C" int spec_lm_head(spec_model* m, const uint16_t* x, int R, float* logits,
+                            int32_t* argmax, void* stream) {
+  if (m == nullptr || x == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  if (R < 1 || R > m->Rmax) return fail(SPEC_E_SHAPE, "R outside [1, max_seqs*max_nt]");
+  if (!aligned16(x)) return fail(SPEC_E_SHAPE, "x must be 16-byte aligned");
+  LinEpi e;
+  e.kind = EPI_LMHEAD;
+  e.y = logits;
+  e.ldy = m->d.vocab;
+  e.argmax = argmax != nullptr ? argmax : m->argmax;
+  e.err = m->err;
+  return linear_launch(m->lm, reinterpret_cast<const __half*>(x), R, e, m->lscr, as_stream(stream));
+}
+
+extern "C" int spec_accept_greedy(const int32_t* argmax, const int32_t* draft, int n_seq, int d,
+                                  int32_t* n_acc, int32_t* emitted, void* stream) {
+  if (argmax == nullptr || n_acc == nullptr || emitted == nullptr || (d > 0 && draft == nullptr))
+    return fail(SPEC_E_INVALID, "null argument");
+  if (n_seq < 1 || d < 0) return fail(SPEC_E_SHAPE, "n_seq >= 1 and d >= 0 required");
+  launch_accept_greedy(argmax, draft, n_seq, d, n_acc, emitted, as_stream(stream));
+  CUDA_TRY(cudaGetLastError());
+  return SPEC_OK;
+}
+
+void stoch_finalize(int n_seq, int d, int32_t* n_acc, int32_t* emitted, uint64_t* emit_idx,
+                    const uint32_t* err, cudaStream_t st);
+
+extern "C" int spec_accept_stochastic(const float* p_logits, const float* q_logits,
+                                      const int32_t* draft, int n_seq, int d, int V,
+                                      float temperature, uint64_t seed, const int32_t* seq_ids,
+                                      uint64_t* emit_idx, int32_t* n_acc, int32_t* emitted,
+                                      void* stream) {
+  if (p_logits == nullptr || seq_ids == nullptr || emit_idx == nullptr || n_acc == nullptr ||
+      emitted == nullptr || (d > 0 && (draft == nullptr || q_logits == nullptr)))
+    return fail(SPEC_E_INVALID, "null argument");
+  if (n_seq < 1 || d < 0 || V < 1) return fail(SPEC_E_SHAPE, "n_seq >= 1, d >= 0, V >= 1 required");
+  if (!(temperature > 0.0f) || !std::isfinite(temperature))
+    return fail(SPEC_E_INVALID, "temperature must be finite and > 0");
+  Workspace* w = nullptr;
+  int rc = workspace_get(stoch_rows_needed(n_seq, d), n_seq, &w);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = as_stream(stream);
+  rc = launch_accept_stochastic(p_logits, q_logits, draft, n_seq, d, V, temperature, seed, seq_ids,
+                                emit_idx, 0, 0, n_acc, emitted, w->st, w->err, st);
+  if (rc != SPEC_OK) return rc;
+  stoch_finalize(n_seq, d, n_acc, emitted, emit_idx, w->err, st);
+  CUDA_TRY(cudaGetLastError());
+  return SPEC_OK;
+}

@@ -1,0 +1,306 @@
+// attn.cu -- causal GQA verify attention over the KV cache, bitwise
+// position-invariant ("Speculative Decoding (D5-R) -- Plan", status notes:
+// the batched verify attention was made bitwise position-invariant so that
+// speculative output is byte-identical to sequential decoding).
+//
+// A query row at absolute position P attends to positions 0..P.  The cache is
+// cut into chunks of ATTN_CHUNK positions at absolute multiples; each chunk
+// gives a partial (row max m, row sum l, unnormalised o) computed by an
+// instruction sequence that depends only on the row's own q and P, and the
+// partials of chunks 0..P/ATTN_CHUNK are merged in increasing chunk order.
+// Neither step depends on nt or on the other rows of the batch, so row i of
+// an nt-row round equals the nt = 1 result at the same position bit for bit.
+//
+// One CTA per (chunk, kv head, sequence): the chunk's K and V tiles are
+// staged once in shared memory (cp.async, XOR-swizzled 16-byte units) and
+// shared by all nt x group query rows of that kv head (GQA), which are
+// processed as m16 tiles with mma.sync m16n8k16: S = Q K^T, softmax in fp32
+// (log2 domain), P rounded to fp16, O = P V.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int CH = ATTN_CHUNK;
+constexpr int WARPS = 4;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                        uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// byte offset of 16-byte unit u of cache row p inside a swizzled tile
+template <int HD>
+__device__ __forceinline__ uint32_t tile_off(int p, int u) {
+  return (uint32_t)(p * (HD * 2) + ((u ^ (p & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(WARPS * 32)
+attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
+                  const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
+                  int nt, int nq, int nkv, int max_ctx, int nchunks, float* __restrict__ part) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* Ks = smem;
+  unsigned char* Vs = smem + CH * HD * 2;
+  const int c = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int G = nq / nkv, M = nt * G, Mmax_stride = M;  // rows of this (seq, kv head)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const RowInfo last = rows[s * nt + nt - 1];
+  const int pos_last = last.pos < max_ctx ? last.pos : max_ctx - 1;
+  if (c * CH > pos_last) return;  // no row of this sequence reaches this chunk
+  const int slot = last.slot;
+
+  // ---- stage K and V of positions [c*CH, c*CH + CH)
+  {
+    const size_t head_base = ((size_t)slot * nkv + kvh) * max_ctx;
+    constexpr int UNITS = HD / 8;  // 16-byte units per row
+    for (int idx = threadIdx.x; idx < CH * UNITS; idx += WARPS * 32) {
+      const int p = idx / UNITS, u = idx % UNITS;
+      const int pg = c * CH + p;
+      const uint32_t ko = smem_u32(Ks + tile_off<HD>(p, u));
+      const uint32_t vo = smem_u32(Vs + tile_off<HD>(p, u));
+      if (pg < max_ctx) {
+        const __half* kg = kcache + (head_base + pg) * HD + u * 8;
+        const __half* vg = vcache + (head_base + pg) * HD + u * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ko), "l"(kg));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vo), "l"(vg));
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(ko), "r"(0));
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vo), "r"(0));
+      }
+    }
+    asm volatile("cp.async.commit_group;");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
+
+  const float sc_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs);
+  const int n_mt = (M + 15) / 16;
+  for (int mt = warp; mt < n_mt; mt += WARPS) {
+    const int mA = mt * 16 + g, mB = mA + 8;
+    const bool okA = mA < M, okB = mB < M;
+    int posA = -1, posB = -1;
+    const __half* qA = nullptr;
+    const __half* qB = nullptr;
+    if (okA) {
+      const int i = mA / G, gh = mA % G;
+      const RowInfo ri = rows[s * nt + i];
+      posA = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
+      qA = q + ((size_t)(s * nt + i) * nq + kvh * G + gh) * HD;
+    }
+    if (okB) {
+      const int i = mB / G, gh = mB % G;
+      const RowInfo ri = rows[s * nt + i];
+      posB = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
+      qB = q + ((size_t)(s * nt + i) * nq + kvh * G + gh) * HD;
+    }
+    // ---- S = Q K^T over the chunk (16 rows x CH keys)
+    float sacc[CH / 8][4];
+#pragma unroll
+    for (int nb = 0; nb < CH / 8; nb++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) sacc[nb][e] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; kk += 2) {
+      uint32_t a0[4], a1[4];
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        uint32_t* a = h == 0 ? a0 : a1;
+        const int d0 = 16 * (kk + h) + 2 * t;
+        a[0] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0) : 0u;
+        a[1] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0) : 0u;
+        a[2] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0 + 8) : 0u;
+        a[3] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0 + 8) : 0u;
+      }
+#pragma unroll
+      for (int nb = 0; nb < CH / 8; nb++) {
+        const int key = 8 * nb + (lane & 7);
+        const int unit = 2 * kk + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ks_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
+        mma_16816(sacc[nb], a0, b0, b1);
+        mma_16816(sacc[nb], a1, b2, b3);
+      }
+    }
+    // ---- mask, row max (fixed butterfly over the 4 lanes of a row)
+    float mxA = -INFINITY, mxB = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < CH / 8; nb++)
+#pragma unroll
+      for (int e = 0; e < 2; e++) {
+        const int kg = c * CH + 8 * nb + 2 * t + e;
+        float va = sacc[nb][e] * sc_log2, vb = sacc[nb][2 + e] * sc_log2;
+        va = kg <= posA ? va : -INFINITY;
+        vb = kg <= posB ? vb : -INFINITY;
+        sacc[nb][e] = va;
+        sacc[nb][2 + e] = vb;
+        mxA = fmaxf(mxA, va);
+        mxB = fmaxf(mxB, vb);
+      }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, off));
+      mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, off));
+    }
+    const float uA = mxA == -INFINITY ? 0.0f : mxA;
+    const float uB = mxB == -INFINITY ? 0.0f : mxB;
+    // ---- P (fp16) as A fragments; l = sum of the rounded P
+    uint32_t pf[CH / 16][4];
+    float lA = 0.0f, lB = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < CH / 8; nb++) {
+      const __half2 pa = __floats2half2_rn(exp2f(sacc[nb][0] - uA), exp2f(sacc[nb][1] - uA));
+      const __half2 pb = __floats2half2_rn(exp2f(sacc[nb][2] - uB), exp2f(sacc[nb][3] - uB));
+      const float2 fa = __half22float2(pa), fb = __half22float2(pb);
+      lA += fa.x;
+      lA += fa.y;
+      lB += fb.x;
+      lB += fb.y;
+      pf[nb / 2][(nb & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(&pa);
+      pf[nb / 2][(nb & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&pb);
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+      lA += __shfl_xor_sync(0xffffffffu, lA, off);
+      lB += __shfl_xor_sync(0xffffffffu, lB, off);
+    }
+    // ---- O = P V (16 rows x HD dims)
+    float oacc[HD / 8][4];
+#pragma unroll
+    for (int dn = 0; dn < HD / 8; dn++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) oacc[dn][e] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < CH / 16; kk++) {
+#pragma unroll
+      for (int dn = 0; dn < HD / 8; dn += 2) {
+        const int mi = lane >> 3;
+        const int key = 16 * kk + (lane & 7) + (mi & 1) * 8;
+        const int unit = dn + (mi >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vs_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
+        mma_16816(oacc[dn], pf[kk], b0, b1);
+        mma_16816(oacc[dn + 1], pf[kk], b2, b3);
+      }
+    }
+    // ---- partials: part[s][kvh][c][m] = (o[HD], m, l)
+    const size_t base = (((size_t)s * nkv + kvh) * nchunks + c) * (size_t)Mmax_stride;
+    if (okA) {
+      float* dst = part + (base + mA) * (HD + 2);
+#pragma unroll
+      for (int dn = 0; dn < HD / 8; dn++)
+        *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][0], oacc[dn][1]);
+      if (t == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(mxA, lA);
+    }
+    if (okB) {
+      float* dst = part + (base + mB) * (HD + 2);
+#pragma unroll
+      for (int dn = 0; dn < HD / 8; dn++)
+        *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][2], oacc[dn][3]);
+      if (t == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(mxB, lB);
+    }
+  }
+}
+
+// One warp per (row, q head): merge chunks 0..P/CH in increasing order.
+template <int HD>
+__global__ void __launch_bounds__(128)
+attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
+                  int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
+                  __half* __restrict__ out) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= R * nq) return;
+  const int r = wid / nq, h = wid % nq;
+  const int s = r / nt, i = r % nt;
+  const int G = nq / nkv, kvh = h / G, gh = h % G;
+  const int M = nt * G, m = i * G + gh;
+  const RowInfo ri = rows[r];
+  const int pos = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
+  const int nc = pos / CH + 1;
+  const size_t base = ((size_t)s * nkv + kvh) * nchunks;
+  float mx = -INFINITY;
+  for (int c = 0; c < nc; c++) {
+    const float mc = part[((base + c) * M + m) * (HD + 2) + HD];
+    mx = fmaxf(mx, mc);
+  }
+  constexpr int PER = HD / 32;
+  float o[PER];
+#pragma unroll
+  for (int e = 0; e < PER; e++) o[e] = 0.0f;
+  float l = 0.0f;
+  for (int c = 0; c < nc; c++) {
+    const float* src = part + ((base + c) * M + m) * (HD + 2);
+    const float2 ml = *reinterpret_cast<const float2*>(src + HD);
+    const float w = exp2f(ml.x - mx);
+    l = fmaf(ml.y, w, l);
+#pragma unroll
+    for (int e = 0; e < PER; e++) o[e] = fmaf(src[lane * PER + e], w, o[e]);
+  }
+  const float inv = 1.0f / l;
+  __half* dst = out + (size_t)r * nq * HD + (size_t)h * HD + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2)
+    *reinterpret_cast<__half2*>(dst + e) = __floats2half2_rn(o[e] * inv, o[e + 1] * inv);
+}
+
+template <int HD>
+int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
+                  const RowInfo* rows, int n_seq, int nt, int nq, int nkv, int max_ctx,
+                  float* part, __half* out, cudaStream_t st) {
+  const int nchunks = (max_ctx + CH - 1) / CH;
+  const size_t smem = 2 * (size_t)CH * HD * 2;
+  dim3 grid(nchunks, nkv, n_seq);
+  attn_chunk_kernel<HD><<<grid, WARPS * 32, smem, st>>>(q, kcache, vcache, rows, nt, nq, nkv,
+                                                        max_ctx, nchunks, part);
+  const int R = n_seq * nt;
+  const int warps = R * nq;
+  attn_merge_kernel<HD><<<(warps + 3) / 4, 128, 0, st>>>(part, rows, R, nt, nq, nkv, max_ctx,
+                                                        nchunks, out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+}  // namespace
+
+size_t attn_part_floats(int max_seqs, int nkv, int max_ctx, int max_nt, int group, int hd) {
+  const int nchunks = (max_ctx + CH - 1) / CH;
+  return (size_t)max_seqs * nkv * nchunks * (size_t)max_nt * group * (hd + 2);
+}
+
+int attn_launch(const __half* q, const __half* kcache, const __half* vcache,
+                const RowInfo* rows, int n_seq, int nt, int nq, int nkv, int hd, int max_ctx,
+                float* part, __half* out, cudaStream_t st) {
+  if (hd == 128)
+    return attn_launch_t<128>(q, kcache, vcache, rows, n_seq, nt, nq, nkv, max_ctx, part, out, st);
+  if (hd == 64)
+    return attn_launch_t<64>(q, kcache, vcache, rows, n_seq, nt, nq, nkv, max_ctx, part, out, st);
+  return fail(SPEC_E_UNSUPPORTED, "verify attention supports head_dim 64 or 128");
+}
+
+void attn_init_attrs() {
+  cudaFuncSetAttribute(attn_chunk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       2 * CH * 128 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       2 * CH * 64 * 2);
+}

@@ -1,0 +1,213 @@
+// common.cuh -- internal declarations shared by the CUDA translation units of
+// the verify-round library (sm_103a).  Not part of the public ABI.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/spec_verify.h"
+
+// ---------------------------------------------------------------------------
+// errors
+// ---------------------------------------------------------------------------
+// Device error-word bits (atomicOr'd by kernels; never trap).
+enum : uint32_t {
+  ERR_TOKEN = 1u << 0,     // token id outside [0, vocab)
+  ERR_POS = 1u << 1,       // n_past + nt > max_ctx
+  ERR_NONFINITE = 1u << 2, // NaN/Inf logit
+  ERR_SEQ = 1u << 3,       // sequence slot outside [0, max_seqs)
+  ERR_TIMEOUT = 1u << 4,   // a bounded wait gave up
+};
+
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+#define CUDA_TRY(expr)                                                       \
+  do {                                                                       \
+    cudaError_t e_ = (expr);                                                 \
+    if (e_ != cudaSuccess)                                                   \
+      return fail(SPEC_E_CUDA, std::string(#expr ": ") + cudaGetErrorString(e_)); \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// packed (streaming) layout of a block-quantised matrix
+// ---------------------------------------------------------------------------
+// The matrix is cut into tiles of 16 output rows and chunks of 64 along K
+// (two quantisation blocks).  For tile T, chunk c, lane l = 4g + t of a warp:
+//   qs word [T][c][l][j], j = k16 step (block b = j/2, half jj = j%2):
+//     nibble 0 -> row g,   k = 64c + 32b + 8t + 4jj + 0
+//     nibble 4 -> row g,   ...                     + 1
+//     nibble 2 -> row g,   ...                     + 2
+//     nibble 6 -> row g,   ...                     + 3
+//     nibble 1,5,3,7 -> the same four k of row g+8
+//   i.e. exactly the A fragment of mma.m16n8k16 (rows g/g+8) after the
+//   standard 0x6400 magic-number extraction, with the k order inside each
+//   32-block permuted so that lane t reads 8 consecutive activations.
+//   qh (Q6) word [T][c][l][h], h = block: two k16 steps, high 2-bit fields at
+//     bits 4..11 / 20..27 (step 2h) and 0..3 / 12..19 / 28..31 (step 2h+1,
+//     a rotate by 8 brings them to the step-2h positions).
+//   sc  [T][c][g][4] fp16: (row g, blk0), (row g+8, blk0), (g, blk1), (g+8, blk1).
+// K is zero-padded to a multiple of 64 (padding weights have q = 0, scale 0).
+struct QMat {
+  int qtype = 0;
+  int N = 0, K = 0, Kp = 0;
+  int nch = 0;      // Kp / 64
+  int n_tiles = 0;  // N / 16
+  int S = 1;        // K-split segments (fixed per matrix: independent of nt)
+  uint4* qs = nullptr;   // [n_tiles][nch][32] uint4
+  uint2* qh = nullptr;   // [n_tiles][nch][32] uint2 (Q6)
+  uint2* sc = nullptr;   // [n_tiles][nch][8] uint2
+  void* base = nullptr;  // single allocation
+  size_t bytes = 0;      // streamed bytes (qs + qh + sc)
+};
+
+// Row permutation applied at repack: packed row p <- canonical row perm(p).
+enum PermKind { PERM_IDENTITY = 0, PERM_ROPE_PAIRS = 1, PERM_GATE_UP = 2 };
+
+// split_sms > 0: choose the K-split from the matrix shape and this SM count;
+// split_sms == 0: no K-split (S = 1, as the LM head's fused argmax needs).
+int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int split_sms,
+              cudaStream_t st, QMat* out);
+void qmat_free(QMat* q);
+
+// Epilogue kinds of the verify GEMM.
+enum EpiKind {
+  EPI_STORE = 0,   // y[r][n] = acc (fp32)
+  EPI_RESID = 1,   // y[r][n] += acc (fp32 residual stream)
+  EPI_SWIGLU = 2,  // out16[r][j] = silu(gate) * up (gate/up interleaved by 8 rows)
+  EPI_QKV = 3,     // RoPE on q/k pairs, q -> fp16 buffer, k/v -> KV cache
+  EPI_LMHEAD = 4,  // optional fp32 logits + fused per-row argmax
+};
+
+struct RowInfo {  // per verify row: sequence slot and absolute position
+  int slot;
+  int pos;
+};
+
+struct LinEpi {
+  EpiKind kind = EPI_STORE;
+  float* y = nullptr;        // STORE/RESID/LMHEAD logits (may be null for LMHEAD)
+  int ldy = 0;               // row stride of y (elements)
+  __half* out16 = nullptr;   // SWIGLU output [R][ldo] / QKV q output [R][nq*hd]
+  int ldo = 0;
+  // QKV
+  __half* kcache = nullptr;  // layer base [max_seqs][nkv][max_ctx][hd]
+  __half* vcache = nullptr;
+  const RowInfo* rows = nullptr;
+  const float2* rope = nullptr;  // [max_ctx][hd/2] (cos, sin), null = no rope
+  int nq = 0, nkv = 0, hd = 0, max_ctx = 0;
+  // LMHEAD
+  int32_t* argmax = nullptr;
+  uint32_t* err = nullptr;
+};
+
+struct LinScratch {
+  float* part = nullptr;         // K-split partials
+  size_t part_floats = 0;
+  unsigned* tickets = nullptr;   // zero-initialised, reset by their last user
+  size_t n_tickets = 0;
+  float2* amax_part = nullptr;   // LM-head argmax partials (value, index bits)
+  size_t amax_entries = 0;
+};
+
+size_t lin_part_floats(const QMat& w, int R);
+size_t lin_tickets_needed(const QMat& w, int R);
+size_t lin_amax_entries(const QMat& w, int R);
+int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
+                  const LinScratch& scr, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// small ops (ops.cu)
+// ---------------------------------------------------------------------------
+void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
+                       const int32_t* draft, const int32_t* seq_ids, int n_seq,
+                       int nt, const int32_t* n_past, int max_seqs, int max_ctx,
+                       RowInfo* rows, int32_t* tokens, float* h, uint32_t* err,
+                       cudaStream_t st);
+void launch_rmsnorm(const float* h, const float* gamma, int R, int H, float eps,
+                    __half* out, cudaStream_t st);
+void launch_rope_table(float2* tab, int max_ctx, int hd, float theta, cudaStream_t st);
+void launch_kv_write(const __half* k_new, const __half* v_new, const RowInfo* rows,
+                     int R, int nkv, int hd, int max_ctx, __half* kcache,
+                     __half* vcache, cudaStream_t st);
+void launch_row_info(const int32_t* seq_ids, int n_seq, int nt,
+                     const int32_t* n_past, int max_seqs, int max_ctx,
+                     RowInfo* rows, uint32_t* err, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// attention (attn.cu)
+// ---------------------------------------------------------------------------
+constexpr int ATTN_CHUNK = 128;  // positions per chunk, at absolute multiples
+size_t attn_part_floats(int max_seqs, int nkv, int max_ctx, int max_nt, int group, int hd);
+int attn_launch(const __half* q, const __half* kcache, const __half* vcache,
+                const RowInfo* rows, int n_seq, int nt, int nq, int nkv, int hd,
+                int max_ctx, float* part, __half* out, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// accept (accept.cu)
+// ---------------------------------------------------------------------------
+struct StochScratch {
+  float* row_max = nullptr;            // [n_seq][2d+1]
+  unsigned long long* row_sum = nullptr;  // [n_seq][2d+1]
+  int4* decision = nullptr;            // [n_seq]: (a, row, U2, flags)
+  size_t rows_cap = 0;
+  size_t seq_cap = 0;
+};
+size_t stoch_rows_needed(int n_seq, int d);
+void launch_accept_greedy(const int32_t* argmax, const int32_t* draft, int n_seq,
+                          int d, int32_t* n_acc, int32_t* emitted, cudaStream_t st);
+int launch_accept_stochastic(const float* p, const float* q, const int32_t* draft,
+                             int n_seq, int d, int V, float T, uint64_t seed,
+                             const int32_t* seq_ids, uint64_t* emit_idx,
+                             int emit_by_slot, int n_slots, int32_t* n_acc,
+                             int32_t* emitted, const StochScratch& scr,
+                             uint32_t* err, cudaStream_t st);
+void launch_commit(const int32_t* seq_ids, int n_seq, int d, int n_slots, const int32_t* n_acc_in,
+                   int32_t* n_acc, int32_t* emitted, int32_t* n_past,
+                   uint64_t* emit_idx, int32_t* anchor, const uint32_t* err,
+                   cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;  // (a & b) | c
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_16816_zero(float (&d)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ldg_stream2(const uint2* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+#endif

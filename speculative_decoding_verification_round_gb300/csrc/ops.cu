@@ -1,0 +1,161 @@
+// ops.cu -- small per-row kernels of the verify pass: row bookkeeping and
+// embedding gather, RMSNorm to fp16, the RoPE table and the KV write of the
+// standalone attention entry point.
+//
+// Row layout of one verify round ("Speculative Decoding (D5-R) -- Plan",
+// section 3): sequence s contributes rows [anchor, x_1 .. x_d] at the
+// contiguous absolute positions n_past[s] .. n_past[s] + d.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace {
+
+__global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, int nt,
+                                const int32_t* __restrict__ n_past, int max_seqs,
+                                int max_ctx, RowInfo* __restrict__ rows,
+                                uint32_t* __restrict__ err) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_seq * nt) return;
+  const int s = r / nt, i = r % nt;
+  int slot = seq_ids[s];
+  if (slot < 0 || slot >= max_seqs) {
+    atomicOr(err, ERR_SEQ);
+    slot = 0;
+  }
+  int pos = n_past[slot] + i;
+  if (pos < 0 || pos >= max_ctx) {
+    atomicOr(err, ERR_POS);
+    pos = max_ctx;  // consumers skip writes at pos >= max_ctx
+  }
+  rows[r] = RowInfo{slot, pos};
+}
+
+// One CTA per verify row: token lookup (anchor for row 0, drafts after),
+// id check, fp16 -> fp32 copy of the embedding row.
+__global__ void embed_kernel(const __half* __restrict__ embed, int V, int H,
+                             const int32_t* __restrict__ anchor,
+                             const int32_t* __restrict__ draft,
+                             const RowInfo* __restrict__ rows, int nt,
+                             int32_t* __restrict__ tokens, float* __restrict__ h,
+                             uint32_t* __restrict__ err) {
+  const int r = blockIdx.x;
+  const int s = r / nt, i = r % nt;
+  __shared__ int s_tok;
+  if (threadIdx.x == 0) {
+    int tok = i == 0 ? anchor[rows[r].slot] : draft[s * (nt - 1) + (i - 1)];
+    if (tok < 0 || tok >= V) {
+      atomicOr(err, ERR_TOKEN);
+      tok = 0;
+    }
+    s_tok = tok;
+    tokens[r] = tok;
+  }
+  __syncthreads();
+  const __half2* src = reinterpret_cast<const __half2*>(embed + (size_t)s_tok * H);
+  float2* dst = reinterpret_cast<float2*>(h + (size_t)r * H);
+  for (int j = threadIdx.x; j < H / 2; j += blockDim.x) dst[j] = __half22float2(src[j]);
+}
+
+// One CTA (256 threads) per row.  The sum of squares is reduced in a fixed
+// order (thread-strided partials, warp butterfly, then warps in order), so a
+// row's result does not depend on the other rows in the batch.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ h,
+                                                      const float* __restrict__ gamma,
+                                                      int H, float eps,
+                                                      __half* __restrict__ out) {
+  const int r = blockIdx.x;
+  const float4* x = reinterpret_cast<const float4*>(h + (size_t)r * H);
+  float ss = 0.0f;
+  for (int j = threadIdx.x; j < H / 4; j += 256) {
+    float4 v = x[j];
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  __shared__ float s_part[8];
+  __shared__ float s_inv;
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.0f;
+    for (int w = 0; w < 8; w++) tot += s_part[w];
+    s_inv = 1.0f / sqrtf(tot / (float)H + eps);
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  const float4* gm = reinterpret_cast<const float4*>(gamma);
+  __half2* o = reinterpret_cast<__half2*>(out + (size_t)r * H);
+  for (int j = threadIdx.x; j < H / 4; j += 256) {
+    float4 v = x[j], gg = gm[j];
+    o[2 * j] = __floats2half2_rn(v.x * inv * gg.x, v.y * inv * gg.y);
+    o[2 * j + 1] = __floats2half2_rn(v.z * inv * gg.z, v.w * inv * gg.w);
+  }
+}
+
+// cos/sin of pos * theta^(-2i/hd), evaluated in fp64 and rounded to fp32.
+__global__ void rope_table_kernel(float2* tab, int max_ctx, int hd, double theta) {
+  const int half = hd / 2;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)max_ctx * half) return;
+  const int pos = (int)(idx / half), i = (int)(idx % half);
+  const double f = pow(theta, -2.0 * (double)i / (double)hd);
+  double s, c;
+  sincos((double)pos * f, &s, &c);
+  tab[idx] = make_float2((float)c, (float)s);
+}
+
+__global__ void kv_write_kernel(const __half* __restrict__ k_new,
+                                const __half* __restrict__ v_new,
+                                const RowInfo* __restrict__ rows, int nkv, int hd,
+                                int max_ctx, __half* __restrict__ kc,
+                                __half* __restrict__ vc) {
+  const int r = blockIdx.x;
+  const RowInfo ri = rows[r];
+  if (ri.pos >= max_ctx) return;
+  for (int j = threadIdx.x; j < nkv * hd; j += blockDim.x) {
+    const int kvh = j / hd, d = j % hd;
+    const size_t dst = (((size_t)ri.slot * nkv + kvh) * max_ctx + ri.pos) * hd + d;
+    kc[dst] = k_new[(size_t)r * nkv * hd + j];
+    vc[dst] = v_new[(size_t)r * nkv * hd + j];
+  }
+}
+
+}  // namespace
+
+void launch_row_info(const int32_t* seq_ids, int n_seq, int nt, const int32_t* n_past,
+                     int max_seqs, int max_ctx, RowInfo* rows, uint32_t* err,
+                     cudaStream_t st) {
+  const int R = n_seq * nt;
+  row_info_kernel<<<(R + 127) / 128, 128, 0, st>>>(seq_ids, n_seq, nt, n_past, max_seqs,
+                                                   max_ctx, rows, err);
+}
+
+void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
+                       const int32_t* draft, const int32_t* seq_ids, int n_seq, int nt,
+                       const int32_t* n_past, int max_seqs, int max_ctx, RowInfo* rows,
+                       int32_t* tokens, float* h, uint32_t* err, cudaStream_t st) {
+  launch_row_info(seq_ids, n_seq, nt, n_past, max_seqs, max_ctx, rows, err, st);
+  embed_kernel<<<n_seq * nt, 256, 0, st>>>(embed, V, H, anchor, draft, rows, nt, tokens,
+                                           h, err);
+}
+
+void launch_rmsnorm(const float* h, const float* gamma, int R, int H, float eps,
+                    __half* out, cudaStream_t st) {
+  rmsnorm_kernel<<<R, 256, 0, st>>>(h, gamma, H, eps, out);
+}
+
+void launch_rope_table(float2* tab, int max_ctx, int hd, float theta, cudaStream_t st) {
+  const size_t n = (size_t)max_ctx * (hd / 2);
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(tab, max_ctx, hd,
+                                                                 (double)theta);
+}
+
+void launch_kv_write(const __half* k_new, const __half* v_new, const RowInfo* rows, int R,
+                     int nkv, int hd, int max_ctx, __half* kcache, __half* vcache,
+                     cudaStream_t st) {
+  kv_write_kernel<<<R, 256, 0, st>>>(k_new, v_new, rows, nkv, hd, max_ctx, kcache, vcache);
+}

@@ -1,0 +1,273 @@
+"""The whole verify round on the GPU (spec_verify_round): logits against the
+oracle's target pass, bit-exact greedy and stochastic accepts, commit of the
+transaction state, greedy identity with plain nt=1 decoding, fail-closed
+errors, and the two full-size decoder workloads."""
+import numpy as np
+import pytest
+
+from speculative_decoding_verification_round_gb300 import synth
+
+from util import (LOGIT_RTOL, MARGIN, host_weight, rel_err, small_decoder, to_device_model,
+                  to_oracle_model, top2_margin)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    assert torch.cuda.is_available()
+    return torch.device("cuda:0")
+
+
+def fill_context(sv, m, g, cfg, n_seq, max_ctx, dev):
+    import torch
+    L, nkv, hd = cfg["n_layers"], cfg["n_kv_heads"], cfg["head_dim"]
+    kc = synth.f16_normal(g, (L, n_seq, nkv, max_ctx, hd))
+    vc = synth.f16_normal(g, (L, n_seq, nkv, max_ctx, hd))
+    for l in range(L):
+        for s in range(n_seq):
+            sv.spec_kv_fill(m, l, s, 0, max_ctx, torch.from_numpy(kc[l, s].view(np.int16)).to(dev),
+                            torch.from_numpy(vc[l, s].view(np.int16)).to(dev))
+    torch.cuda.synchronize()
+    return kc, vc
+
+
+def gpu_round(sv, m, dev, draft, d, seq_ids, greedy=True, q=None, T=1.0, seed=0, V=None):
+    import torch
+    n_seq = len(seq_ids)
+    n_acc = torch.empty(n_seq, dtype=torch.int32, device=dev)
+    em = torch.empty((n_seq, d + 1), dtype=torch.int32, device=dev)
+    logits = torch.empty((n_seq * (d + 1), V), dtype=torch.float32, device=dev)
+    sv.spec_verify_round(m, n_seq, torch.tensor(seq_ids, dtype=torch.int32, device=dev),
+                         torch.from_numpy(np.ascontiguousarray(draft, np.int32)).to(dev) if d else None,
+                         d, None if q is None else torch.from_numpy(q).to(dev), greedy, T, seed,
+                         n_acc, em, logits)
+    bits = sv.spec_error_check(m)
+    return n_acc.cpu().numpy(), em.cpu().numpy(), logits.cpu().numpy(), bits
+
+
+def check_greedy(orc, logits_gpu, ref, draft, n_acc, em, nt):
+    assert rel_err(logits_gpu, ref) <= LOGIT_RTOL
+    gam = np.array([orc.argmax(r) for r in logits_gpu], np.int32)
+    for r in range(ref.shape[0]):
+        if top2_margin(ref[r]) > MARGIN:
+            assert gam[r] == orc.argmax(ref[r]), r
+    n_ref, em_ref = orc.accept_greedy(gam.reshape(-1, nt), draft)
+    assert np.array_equal(n_acc, n_ref) and np.array_equal(em, em_ref)
+
+
+@pytest.mark.parametrize("graphs", [True, False])
+def test_round_greedy_matches_oracle(orc, dev, graphs):
+    import speculative_decoding_verification_round_gb300 as sv
+    g = np.random.default_rng(41)
+    cfg, raw = small_decoder(g)
+    n_seq, d, max_ctx = 3, 5, 300
+    m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, n_seq)
+    m.set_graphs(graphs)
+    kc, vc = fill_context(sv, m, g, cfg, n_seq, max_ctx, dev)
+    om = to_oracle_model(orc, cfg, raw, max_ctx)
+    n_past = [100, 129, 250]
+    anchor = [3, 17, 400]
+    sv.spec_state_set(m, [0, 1, 2], n_past=n_past, emit_idx=[0, 5, 9], anchor=anchor)
+    kc_o, vc_o = kc.copy(), vc.copy()
+    # drafts: the oracle's own greedy chain with random substitutions
+    ref0 = om.forward(np.array(anchor, np.int32)[:, None], n_past, kc.copy(), vc.copy())
+    draft = g.integers(0, cfg["vocab"], (n_seq, d)).astype(np.int32)
+    for s in range(n_seq):
+        draft[s, 0] = orc.argmax(ref0[s])
+    tokens = np.concatenate([np.array(anchor)[:, None], draft], 1).astype(np.int32)
+    ref = om.forward(tokens, n_past, kc_o, vc_o)
+    n_acc, em, lg, bits = gpu_round(sv, m, dev, draft, d, [0, 1, 2], V=cfg["vocab"])
+    assert bits == 0
+    check_greedy(orc, lg, ref, draft, n_acc, em, d + 1)
+    npast2, ei2, anc2 = sv.spec_state_get(m, [0, 1, 2])
+    assert npast2 == [n_past[s] + n_acc[s] + 1 for s in range(n_seq)]
+    assert ei2 == [[0, 5, 9][s] + n_acc[s] + 1 for s in range(n_seq)]
+    assert anc2 == [int(em[s, n_acc[s]]) for s in range(n_seq)]
+
+
+def test_round_stochastic_matches_oracle(orc, dev):
+    import speculative_decoding_verification_round_gb300 as sv
+    from test_gpu_accept import sample_drafts_oracle
+    g = np.random.default_rng(42)
+    cfg, raw = small_decoder(g, V=1024)
+    n_seq, d, max_ctx, T, seed = 2, 4, 200, 0.7, 1234
+    m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, 4)
+    fill_context(sv, m, g, cfg, 4, max_ctx, dev)
+    slots = [3, 1]
+    n_past, ei0 = [50, 120], [7, 1000]
+    sv.spec_state_set(m, slots, n_past=n_past, emit_idx=ei0, anchor=[5, 6])
+    q = (g.standard_normal((n_seq, d, cfg["vocab"])) * 2).astype(np.float32)
+    draft = sample_drafts_oracle(orc, q, T, seed, slots, ei0)
+    n_acc, em, lg, bits = gpu_round(sv, m, dev, draft, d, slots, greedy=False, q=q, T=T,
+                                    seed=seed, V=cfg["vocab"])
+    assert bits == 0
+    # decisions bit-exact on the shared (GPU) fp32 logits
+    n_r, em_r, ei_r = orc.accept_stochastic(lg.reshape(n_seq, d + 1, -1), q, draft, T, seed,
+                                            slots, ei0)
+    assert np.array_equal(n_acc, n_r) and np.array_equal(em, em_r)
+    npast2, ei2, anc2 = sv.spec_state_get(m, slots)
+    assert ei2 == [int(x) for x in ei_r]
+    assert npast2 == [n_past[i] + n_r[i] + 1 for i in range(n_seq)]
+
+
+def test_greedy_identity_with_plain_decoding(dev):
+    """Greedy speculative output is byte-identical to plain nt = 1 decoding
+    ("Model-neutral Speculative Decoding", "The exactness transaction")."""
+    import speculative_decoding_verification_round_gb300 as sv
+    g = np.random.default_rng(43)
+    cfg, raw = small_decoder(g, L=2, V=512)
+    max_ctx, d, N = 420, 7, 200
+    m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, 1)
+    fill_context(sv, m, g, cfg, 1, max_ctx, dev)
+    # reference stream: nt = 1 rounds
+    sv.spec_state_set(m, [0], n_past=[64], emit_idx=[0], anchor=[11])
+    ref = []
+    while len(ref) < N:
+        n_acc, em, _, bits = gpu_round(sv, m, dev, None, 0, [0], V=cfg["vocab"])
+        assert bits == 0 and n_acc[0] == 0
+        ref.append(int(em[0, 0]))
+    # speculative stream: drafts are the true continuation w.p. 0.74
+    sv.spec_state_set(m, [0], n_past=[64], emit_idx=[0], anchor=[11])
+    out, rounds, accepted = [], 0, 0
+    while len(out) < N:
+        nxt = ref[len(out):len(out) + d] + [0] * d
+        draft = synth.greedy_drafts(g, np.array(nxt[:d]), cfg["vocab"], 0.74)[None, :]
+        n_acc, em, _, bits = gpu_round(sv, m, dev, draft, d, [0], V=cfg["vocab"])
+        assert bits == 0
+        out += [int(t) for t in em[0, :n_acc[0] + 1]]
+        rounds += 1
+        accepted += int(n_acc[0])
+    assert out[:N] == ref, "speculative greedy stream differs from plain decoding"
+    assert rounds >= 30 and accepted > rounds  # the drafts were used
+
+
+def test_invalid_draft_and_position_fail_closed(dev):
+    import speculative_decoding_verification_round_gb300 as sv
+    g = np.random.default_rng(44)
+    cfg, raw = small_decoder(g)
+    m = to_device_model(sv, cfg, raw, dev, 100, 8, 2)
+    sv.spec_state_set(m, [0, 1], n_past=[10, 20], emit_idx=[3, 4], anchor=[1, 2])
+    draft = np.array([[5, cfg["vocab"] + 7], [1, 2]], np.int32)   # out-of-range id
+    n_acc, em, _, bits = gpu_round(sv, m, dev, draft, 2, [0, 1], V=cfg["vocab"])
+    assert bits != 0 and (n_acc == -1).all() and (em == -1).all()
+    assert sv.spec_state_get(m, [0, 1]) == ([10, 20], [3, 4], [1, 2])
+    sv.spec_state_set(m, [0], n_past=[98])                        # 98 + 3 > 100
+    n_acc, em, _, bits = gpu_round(sv, m, dev, np.array([[1, 2]], np.int32), 2, [0],
+                                   V=cfg["vocab"])
+    assert bits != 0 and n_acc[0] == -1
+    assert sv.spec_state_get(m, [0])[0] == [98]
+    # the next valid round is unaffected
+    sv.spec_state_set(m, [0], n_past=[10])
+    n_acc, em, _, bits = gpu_round(sv, m, dev, np.array([[1, 2]], np.int32), 2, [0],
+                                   V=cfg["vocab"])
+    assert bits == 0 and n_acc[0] >= 0
+    with pytest.raises(sv.SpecError):  # host-side checks
+        gpu_round(sv, m, dev, np.zeros((1, 9), np.int32), 9, [0], V=cfg["vocab"])
+
+
+# --------------------------------------------------------------------------
+# full-size decoders
+# --------------------------------------------------------------------------
+def device_decoder(sv, wl, dev, max_ctx, max_nt, max_seqs):
+    W = synth.decoder_weights_torch(wl, dev)
+    desc = dict(n_layers=wl["n_layers"], hidden=wl["hidden"], n_q_heads=wl["n_q_heads"],
+                n_kv_heads=wl["n_kv_heads"], head_dim=wl["head_dim"], ffn=wl["ffn"],
+                vocab=wl["vocab"], max_ctx=max_ctx, max_nt=max_nt, max_seqs=max_seqs)
+    return sv.Model(desc, W), W
+
+
+def host_decoder(orc, W, wl, max_ctx):
+    import torch
+    H = lambda w: host_weight(w)
+    raw = dict(wqkv=[H(w) for w in W["wqkv"]], wo=[H(w) for w in W["wo"]],
+               wgu=[H(w) for w in W["wgu"]], wd=[H(w) for w in W["wd"]],
+               lm_head=H(W["lm_head"]),
+               embed=W["embed"].cpu().view(torch.int16).numpy().view(np.uint16),
+               norm_w=W["norm_w"].cpu().numpy())
+    cfg = {k: wl[k] for k in ("n_layers", "hidden", "n_q_heads", "n_kv_heads", "head_dim",
+                              "ffn", "vocab")}
+    return to_oracle_model(orc, cfg, raw, max_ctx), cfg
+
+
+def device_context(sv, m, wl, n_seq, ctx, max_ctx, dev, seed):
+    """Fills positions [0, ctx) of each slot with N(0,1) fp16 k/v; returns the
+    host copy [L][n_seq][nkv][max_ctx][hd] (zeros past ctx)."""
+    import torch
+    gen = synth.torch_gen(seed, dev)
+    L, nkv, hd = wl["n_layers"], wl["n_kv_heads"], wl["head_dim"]
+    kc = np.zeros((L, n_seq, nkv, max_ctx, hd), np.uint16)
+    vc = np.zeros_like(kc)
+    for l in range(L):
+        for s in range(n_seq):
+            k = synth.f16_normal_torch(gen, (nkv, ctx, hd), dev)
+            v = synth.f16_normal_torch(gen, (nkv, ctx, hd), dev)
+            sv.spec_kv_fill(m, l, s, 0, ctx, k.view(torch.int16), v.view(torch.int16))
+            kc[l, s, :, :ctx] = k.cpu().view(torch.int16).numpy().view(np.uint16)
+            vc[l, s, :, :ctx] = v.cpu().view(torch.int16).numpy().view(np.uint16)
+    return kc, vc
+
+
+@pytest.mark.slow
+def test_decoder8_full_greedy_round(orc, dev):
+    """8 layers, H=4096, 32/8 heads, FFN 14336, Q6 LM head V=151936, 4096
+    cached positions, nt=8; drafts follow the oracle's greedy chain with
+    probability 0.74."""
+    import speculative_decoding_verification_round_gb300 as sv
+    wl = synth.WL_DECODER8
+    ctx, d, max_ctx = wl["ctx"], wl["d"], wl["ctx"] + 64
+    m, W = device_decoder(sv, wl, dev, max_ctx, d + 1, 1)
+    kc, vc = device_context(sv, m, wl, 1, ctx, max_ctx, dev, seed=1)
+    om, cfg = host_decoder(orc, W, wl, max_ctx)
+    g = np.random.default_rng(wl["seed"])
+    anchor = 1234
+    # the oracle's greedy continuation (nt = 1 passes), then 0.74-agreement drafts
+    chain, tok, kco, vco = [], anchor, kc.copy(), vc.copy()
+    for i in range(d):
+        lg = om.forward(np.array([[tok]], np.int32), [ctx + i], kco, vco)
+        tok = orc.argmax(lg[0])
+        chain.append(tok)
+    draft = synth.greedy_drafts(g, np.array(chain), wl["vocab"], wl["p_agree"])[None, :]
+    tokens = np.concatenate([[[anchor]], draft], 1).astype(np.int32)
+    ref = om.forward(tokens, [ctx], kc.copy(), vc.copy())
+    sv.spec_state_set(m, [0], n_past=[ctx], emit_idx=[0], anchor=[anchor])
+    n_acc, em, lg, bits = gpu_round(sv, m, dev, draft, d, [0], V=wl["vocab"])
+    assert bits == 0
+    check_greedy(orc, lg, ref, draft, n_acc, em, d + 1)
+
+
+@pytest.mark.slow
+def test_decoder14b_batched_stochastic_round(orc, dev):
+    """40 layers, H=5120, 40/8 heads, FFN 13824, Q6 LM head V=248320,
+    12 sequences x 512 cached positions, nt=16, T=0.7, all 192 rows in one
+    launch; the oracle recomputes two of the sequences."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from test_gpu_accept import sample_drafts_oracle
+    wl = synth.WL_DECODER14B
+    n_seq, ctx, d, T, seed = wl["n_seq"], wl["ctx"], wl["d"], wl["temperature"], 99
+    max_ctx = ctx + 32
+    m, W = device_decoder(sv, wl, dev, max_ctx, d + 1, n_seq)
+    om, cfg = host_decoder(orc, W, wl, max_ctx)
+    del W
+    torch.cuda.empty_cache()
+    kc, vc = device_context(sv, m, wl, n_seq, ctx, max_ctx, dev, seed=2)
+    g = np.random.default_rng(wl["seed"])
+    V = wl["vocab"]
+    q = (g.standard_normal((n_seq, d, V)) * 2.0).astype(np.float32)
+    slots = list(range(n_seq))
+    ei0 = [1000 * s for s in slots]
+    draft = sample_drafts_oracle(orc, q, T, seed, slots, ei0)
+    anchors = g.integers(0, V, n_seq).astype(np.int32)
+    sv.spec_state_set(m, slots, n_past=[ctx] * n_seq, emit_idx=ei0, anchor=anchors.tolist())
+    n_acc, em, lg, bits = gpu_round(sv, m, dev, draft, d, slots, greedy=False, q=q, T=T,
+                                    seed=seed, V=V)
+    assert bits == 0
+    n_r, em_r, _ = orc.accept_stochastic(lg.reshape(n_seq, d + 1, V), q, draft, T, seed, slots, ei0)
+    assert np.array_equal(n_acc, n_r) and np.array_equal(em, em_r)
+    for s in (0, 7):
+        tokens = np.concatenate([[anchors[s]], draft[s]])[None, :].astype(np.int32)
+        ref = om.forward(tokens, [ctx], np.ascontiguousarray(kc[:, s:s + 1]),
+                         np.ascontiguousarray(vc[:, s:s + 1]))
+        assert rel_err(lg[s * (d + 1):(s + 1) * (d + 1)], ref) <= LOGIT_RTOL
