@@ -153,6 +153,20 @@ int spec_model_kv_cache(spec_model* m, int layer, uint16_t** k, uint16_t** v);
 int spec_kv_fill(spec_model* m, int layer, int seq, int pos0, int n_pos,
                  const uint16_t* k, const uint16_t* v, void* stream);
 
+/* The reverse of spec_kv_fill: copies positions [pos0, pos0 + n_pos) of slot
+ * `seq`, layer `layer` out to k and v, fp16 [n_kv_heads][n_pos][head_dim]
+ * (device or host memory).  Asynchronous on `stream`. */
+int spec_kv_read(spec_model* m, int layer, int seq, int pos0, int n_pos, uint16_t* k,
+                 uint16_t* v, void* stream);
+
+/* Diagnostics: copies up to `bytes` of an internal activation buffer of the
+ * last target pass to dst (device or host).  which: 0 residual h fp32
+ * [R][hidden], 1 normed input fp16 [R][hidden] (after the final norm: the LM
+ * head input), 2 SwiGLU output fp16 [R][ffn], 3 attention output fp16
+ * [R][n_q_heads*head_dim], 4 rotated q fp16 [R][n_q_heads][head_dim] (the
+ * last layer's), 5 logits fp32 [R][vocab].  Asynchronous on `stream`. */
+int spec_model_debug_read(spec_model* m, int which, void* dst, size_t bytes, void* stream);
+
 /* Per-sequence transaction state, HOST arrays of n entries for the slots
  * seq_ids[0..n): n_past (committed positions), emit_idx (sampler slot of the
  * next emitted token), anchor (last committed token, row 0 of the next

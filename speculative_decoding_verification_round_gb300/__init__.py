@@ -30,6 +30,7 @@ SPEC_MAX_NT = 16
 
 EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_linear_q",
             "spec_model_create", "spec_model_destroy", "spec_model_kv_cache", "spec_kv_fill",
+            "spec_kv_read", "spec_model_debug_read",
             "spec_state_set", "spec_state_get", "spec_error_check", "spec_model_set_graphs",
             "spec_verify_attn", "spec_lm_head", "spec_accept_greedy",
             "spec_accept_stochastic", "spec_verify_round"]
@@ -90,6 +91,8 @@ def lib():
                 "spec_model_destroy": (I32, [P]),
                 "spec_model_kv_cache": (I32, [P, I32, ctypes.POINTER(P), ctypes.POINTER(P)]),
                 "spec_kv_fill": (I32, [P, I32, I32, I32, I32, P, P, P]),
+                "spec_kv_read": (I32, [P, I32, I32, I32, I32, P, P, P]),
+                "spec_model_debug_read": (I32, [P, I32, P, ctypes.c_size_t, P]),
                 "spec_state_set": (I32, [P, I32, P, P, P, P]),
                 "spec_state_get": (I32, [P, I32, P, P, P, P]),
                 "spec_error_check": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -228,6 +231,18 @@ def spec_kv_fill(m: Model, layer: int, seq: int, pos0: int, n_pos: int, k, v, st
     """k, v: fp16 tensors [n_kv_heads][n_pos][head_dim] (device or pinned host)."""
     _check(lib().spec_kv_fill(m.handle, int(layer), int(seq), int(pos0), int(n_pos), _ptr(k),
                               _ptr(v), _stream(stream)))
+
+
+def spec_kv_read(m: Model, layer: int, seq: int, pos0: int, n_pos: int, k, v, stream=None):
+    """Copies cache rows out into k, v: fp16 tensors [n_kv_heads][n_pos][head_dim]."""
+    _check(lib().spec_kv_read(m.handle, int(layer), int(seq), int(pos0), int(n_pos), _ptr(k),
+                              _ptr(v), _stream(stream)))
+
+
+def spec_model_debug_read(m: Model, which: int, dst, stream=None):
+    """Copies an internal activation buffer of the last pass into dst."""
+    _check(lib().spec_model_debug_read(m.handle, int(which), _ptr(dst),
+                                       dst.numel() * dst.element_size(), _stream(stream)))
 
 
 def _host_array(values, ctype):

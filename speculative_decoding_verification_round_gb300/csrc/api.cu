@@ -443,6 +443,46 @@ extern "C" int spec_kv_fill(spec_model* m, int layer, int seq, int pos0, int n_p
   return SPEC_OK;
 }
 
+extern "C" int spec_kv_read(spec_model* m, int layer, int seq, int pos0, int n_pos, uint16_t* k,
+                            uint16_t* v, void* stream) {
+  if (m == nullptr || k == nullptr || v == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  const spec_model_desc& D = m->d;
+  if (layer < 0 || layer >= D.n_layers || seq < 0 || seq >= D.max_seqs)
+    return fail(SPEC_E_SHAPE, "layer or slot out of range");
+  if (pos0 < 0 || n_pos < 0 || pos0 + n_pos > D.max_ctx) return fail(SPEC_E_SHAPE, "positions out of range");
+  if (n_pos == 0) return SPEC_OK;
+  const size_t row = (size_t)D.head_dim * sizeof(__half);
+  for (int which = 0; which < 2; which++) {
+    const __half* base = (which == 0 ? m->kc : m->vc) + m->layer_elems * layer +
+                         ((size_t)seq * D.n_kv_heads * D.max_ctx + pos0) * D.head_dim;
+    uint16_t* dst = which == 0 ? k : v;
+    CUDA_TRY(cudaMemcpy2DAsync(dst, row * n_pos, base, row * D.max_ctx, row * n_pos, D.n_kv_heads,
+                               cudaMemcpyDefault, as_stream(stream)));
+  }
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_debug_read(spec_model* m, int which, void* dst, size_t bytes,
+                                     void* stream) {
+  if (m == nullptr || dst == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  const spec_model_desc& D = m->d;
+  const size_t R = (size_t)m->Rmax;
+  const void* src = nullptr;
+  size_t cap = 0;
+  switch (which) {
+    case 0: src = m->h; cap = R * D.hidden * 4; break;
+    case 1: src = m->xa; cap = R * D.hidden * 2; break;
+    case 2: src = m->xs; cap = R * D.ffn * 2; break;
+    case 3: src = m->ao; cap = R * D.n_q_heads * D.head_dim * 2; break;
+    case 4: src = m->qbuf; cap = R * D.n_q_heads * D.head_dim * 2; break;
+    case 5: src = m->logits; cap = R * D.vocab * 4; break;
+    default: return fail(SPEC_E_INVALID, "unknown buffer");
+  }
+  if (src == nullptr) return fail(SPEC_E_UNSUPPORTED, "buffer not allocated for this model");
+  CUDA_TRY(cudaMemcpyAsync(dst, src, std::min(bytes, cap), cudaMemcpyDefault, as_stream(stream)));
+  return SPEC_OK;
+}
+
 extern "C" int spec_model_set_graphs(spec_model* m, int enable) {
   if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
   m->use_graphs = enable != 0;

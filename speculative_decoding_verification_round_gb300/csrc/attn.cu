@@ -15,7 +15,7 @@
 // staged once in shared memory (cp.async, XOR-swizzled 16-byte units) and
 // shared by all nt x group query rows of that kv head (GQA), which are
 // processed as m16 tiles with mma.sync m16n8k16: S = Q K^T, softmax in fp32
-// (log2 domain), P rounded to fp16, O = P V.
+// (log2 domain), O = P V with P as an exact hi + lo pair of fp16 operands.
 #include <math.h>
 
 #include "common.cuh"
@@ -44,11 +44,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 template <int HD>
 __device__ __forceinline__ uint32_t tile_off(int p, int u) {
   return (uint32_t)(p * (HD * 2) + ((u ^ (p & 7)) << 4));
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 template <int HD>
@@ -163,27 +158,27 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
     }
     const float uA = mxA == -INFINITY ? 0.0f : mxA;
     const float uB = mxB == -INFINITY ? 0.0f : mxB;
-    // ---- P (fp16) as A fragments; l = sum of the rounded P
-    uint32_t pf[CH / 16][4];
+    // ---- p = exp2(s - m) in fp32; l = sum of p in a fixed order
     float lA = 0.0f, lB = 0.0f;
 #pragma unroll
     for (int nb = 0; nb < CH / 8; nb++) {
-      const __half2 pa = __floats2half2_rn(exp2f(sacc[nb][0] - uA), exp2f(sacc[nb][1] - uA));
-      const __half2 pb = __floats2half2_rn(exp2f(sacc[nb][2] - uB), exp2f(sacc[nb][3] - uB));
-      const float2 fa = __half22float2(pa), fb = __half22float2(pb);
-      lA += fa.x;
-      lA += fa.y;
-      lB += fb.x;
-      lB += fb.y;
-      pf[nb / 2][(nb & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(&pa);
-      pf[nb / 2][(nb & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&pb);
+      sacc[nb][0] = exp2f(sacc[nb][0] - uA);
+      sacc[nb][1] = exp2f(sacc[nb][1] - uA);
+      sacc[nb][2] = exp2f(sacc[nb][2] - uB);
+      sacc[nb][3] = exp2f(sacc[nb][3] - uB);
+      lA += sacc[nb][0];
+      lA += sacc[nb][1];
+      lB += sacc[nb][2];
+      lB += sacc[nb][3];
     }
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
       lA += __shfl_xor_sync(0xffffffffu, lA, off);
       lB += __shfl_xor_sync(0xffffffffu, lB, off);
     }
-    // ---- O = P V (16 rows x HD dims)
+    // ---- O = P V (16 rows x HD dims).  P enters the fp16 MMA as an exact
+    // ---- two-term split p = hi + lo (hi = fp16(p), lo = fp16(p - hi)), so
+    // ---- the product carries ~22 bits of p instead of 11.
     float oacc[HD / 8][4];
 #pragma unroll
     for (int dn = 0; dn < HD / 8; dn++)
@@ -191,6 +186,19 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
       for (int e = 0; e < 4; e++) oacc[dn][e] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < CH / 16; kk++) {
+      uint32_t phi[4], plo[4];
+#pragma unroll
+      for (int h = 0; h < 2; h++) {         // key tiles 2kk (h = 0) and 2kk+1 (h = 1)
+#pragma unroll
+        for (int rw = 0; rw < 2; rw++) {    // rows g (rw = 0) and g+8 (rw = 1)
+          const float p0 = sacc[2 * kk + h][2 * rw], p1 = sacc[2 * kk + h][2 * rw + 1];
+          const __half2 hi = __floats2half2_rn(p0, p1);
+          const float2 hf = __half22float2(hi);
+          const __half2 lo = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
+          phi[2 * h + rw] = *reinterpret_cast<const uint32_t*>(&hi);
+          plo[2 * h + rw] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
+      }
 #pragma unroll
       for (int dn = 0; dn < HD / 8; dn += 2) {
         const int mi = lane >> 3;
@@ -198,8 +206,10 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
         const int unit = dn + (mi >> 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vs_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
-        mma_16816(oacc[dn], pf[kk], b0, b1);
-        mma_16816(oacc[dn + 1], pf[kk], b2, b3);
+        mma_16816(oacc[dn], phi, b0, b1);
+        mma_16816(oacc[dn], plo, b0, b1);
+        mma_16816(oacc[dn + 1], phi, b2, b3);
+        mma_16816(oacc[dn + 1], plo, b2, b3);
       }
     }
     // ---- partials: part[s][kvh][c][m] = (o[HD], m, l)

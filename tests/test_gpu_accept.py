@@ -22,7 +22,9 @@ def lm_only_model(sv, dev, w, H, V, max_rows):
     import torch
     W = dict(lm_head=dev_weight(w, dev),
              norm_w=torch.ones((1, H), dtype=torch.float32, device=dev))
-    return sv.Model(dict(n_layers=0, hidden=H, vocab=V, max_nt=max_rows, max_seqs=1), W)
+    nt = min(max_rows, 16)
+    return sv.Model(dict(n_layers=0, hidden=H, vocab=V, max_nt=nt,
+                         max_seqs=(max_rows + nt - 1) // nt), W)
 
 
 @pytest.mark.parametrize("H,V,R,qtype", [(1024, 32000, 3, 4), (256, 2048, 16, 6), (128, 160, 1, 4),

@@ -167,6 +167,67 @@ def test_invalid_draft_and_position_fail_closed(dev):
         gpu_round(sv, m, dev, np.zeros((1, 9), np.int32), 9, [0], V=cfg["vocab"])
 
 
+def test_round_stagewise_parity(orc, dev):
+    """Each stage of the pass against the oracle fed the GPU's own input of
+    that stage (read back from the library's buffers), on a deliberately
+    steep network (block scales 5x the workloads') where end-to-end logits
+    amplify single fp16 rounding flips: every stage must stay within a few
+    fp16 rounding flips (rate) or ~1e-5 relative (fp32 outputs)."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from util import oracle_qweight
+    f16 = lambda a: a.view(np.float16).astype(np.float64)
+    g = np.random.default_rng(45)
+    L, H, nq, nkv, hd, F, V, d, n_past, max_ctx = 1, 256, 8, 2, 128, 128, 512, 5, 200, 300
+    cfg, raw = small_decoder(g, L=L, H=H, nq=nq, nkv=nkv, hd=hd, F=F, V=V, mult=0.05)
+    R = d + 1
+    m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, 1)
+    kc, vc = fill_context(sv, m, g, cfg, 1, max_ctx, dev)
+    sv.spec_state_set(m, [0], n_past=[n_past], emit_idx=[0], anchor=[3])
+    draft = g.integers(0, V, (1, d)).astype(np.int32)
+    tokens = np.concatenate([[3], draft[0]]).astype(np.int32)
+    _, _, lg, bits = gpu_round(sv, m, dev, draft, d, [0], V=V)
+    assert bits == 0
+
+    def rd(which, shape, dt):
+        t = torch.empty(shape, dtype=dt, device=dev)
+        sv.spec_model_debug_read(m, which, t)
+        torch.cuda.synchronize()
+        return t.cpu().numpy()
+    h = rd(0, (R, H), torch.float32)
+    xa = rd(1, (R, H), torch.int16).view(np.uint16)
+    xs = rd(2, (R, F), torch.int16).view(np.uint16)
+    ao = rd(3, (R, nq * hd), torch.int16).view(np.uint16)
+    q = rd(4, (R, nq, hd), torch.int16).view(np.uint16)
+    W = lambda w: oracle_qweight(orc, w)
+    pos = np.arange(n_past, n_past + R)
+    h0 = f16(raw["embed"][tokens]).astype(np.float32)
+    qkv = orc.linear(W(raw["wqkv"][0]), orc.rmsnorm(h0, raw["norm_w"][0], 1e-6))
+    q_o = np.stack([orc.rope(qkv[:, i * hd:(i + 1) * hd], pos, 10000.0) for i in range(nq)], 1)
+    assert np.mean(q_o != q) < 0.01
+    k = torch.empty((nkv, R, hd), dtype=torch.int16, device=dev)
+    v = torch.empty_like(k)
+    sv.spec_kv_read(m, 0, 0, n_past, R, k, v)
+    torch.cuda.synchronize()
+    kcs, vcs = kc[0, 0].copy(), vc[0, 0].copy()
+    kcs[:, n_past:n_past + R] = k.cpu().numpy().view(np.uint16)
+    vcs[:, n_past:n_past + R] = v.cpu().numpy().view(np.uint16)
+    k_o = np.stack([orc.rope(qkv[:, (nq + i) * hd:(nq + i + 1) * hd], pos, 10000.0)
+                    for i in range(nkv)], 0)
+    assert np.mean(k_o != kcs[:, n_past:n_past + R]) < 0.01
+    ao_o = orc.attention(q, kcs, vcs, pos).reshape(R, nq * hd)
+    assert np.mean(ao_o != ao) < 0.01 and rel_err(f16(ao), f16(ao_o)) <= 2.0 ** -10
+    h1 = (h0.astype(np.float64) + orc.linear(W(raw["wo"][0]), ao)).astype(np.float32)
+    gu = orc.linear(W(raw["wgu"][0]), orc.rmsnorm(h1, raw["norm_w"][1], 1e-6))
+    xs_o = orc.swiglu(gu[:, :F], gu[:, F:])
+    assert np.mean(xs_o != xs) < 0.06
+    h2 = (h1.astype(np.float64) + orc.linear(W(raw["wd"][0]), xs)).astype(np.float32)
+    assert rel_err(h, h2) < 2e-5
+    xa_o = orc.rmsnorm(h, raw["norm_w"][2], 1e-6)
+    assert np.mean(xa_o != xa) < 0.01
+    assert rel_err(lg, orc.linear(W(raw["lm_head"]), xa)) < 1e-5
+
+
 # --------------------------------------------------------------------------
 # full-size decoders
 # --------------------------------------------------------------------------

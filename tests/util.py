@@ -41,7 +41,9 @@ def oracle_qweight(orc, w):
     return orc.QWeight(w["qtype"], w["qs"], w["qh"], w["scales"], w["N"], w["K"])
 
 
-def small_decoder(g, L=2, H=256, nq=4, nkv=2, hd=64, F=128, V=512, lm_qtype=6, mult=0.05):
+def small_decoder(g, L=2, H=256, nq=4, nkv=2, hd=64, F=128, V=512, lm_qtype=6, mult=None):
+    """Block scales default to the workloads' (|N(0,1)| * 0.01 for Q4,
+    * 0.005 for Q6)."""
     mk = lambda qt, N, K: synth.q_weight(g, qt, N, K, mult=mult)
     raw = dict(wqkv=[mk(4, (nq + 2 * nkv) * hd, H) for _ in range(L)],
                wo=[mk(4, H, nq * hd) for _ in range(L)],
