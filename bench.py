@@ -191,6 +191,19 @@ def record_chain(sv, synth, m, wl, dev, n_rounds, anchor, rng):
     return drafts
 
 
+class L2Flush:
+    """Evicts L2 by READING a buffer twice the L2 size (a write would leave
+    dirty lines whose write-back the next kernel would pay for)."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.ones(max(2 * l2, 64 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.buf.amax()
+
+
 def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
     """The verify GEMM at the decoder's shapes, nt = 8, timed alone with CUDA
     events on its stream; L2 flushed between launches.  Returns the achieved
@@ -203,7 +216,7 @@ def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
               (4, 2 * F, H, wl["n_layers"]), (4, H, F, wl["n_layers"]), (6, V, H, 1)]
     gen = synth.torch_gen(5, dev)
     st = torch.cuda.current_stream()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     nt = wl["d"] + 1
     total_bytes, total_s, per = 0.0, 0.0, []
     for qt, N, K, count in shapes:
@@ -214,7 +227,7 @@ def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
         nbytes = N * K * (0.5625 if qt == 4 else 0.8125) + nt * K * 2 + nt * N * 4
         times = []
         for i in range(reps + 3):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(st)
             sv.spec_linear_q(qm, x, nt, y, st)
@@ -239,7 +252,7 @@ def nt_sweep(sv, synth, dev, reps=20):
     wl = synth.WL_LINEAR_SWEEP
     gen = synth.torch_gen(wl["seed"], dev)
     st = torch.cuda.current_stream()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     out = {}
     for qt, N, K in wl["mats"]:
         w = synth.q_weight_torch(gen, qt, N, K, dev)
@@ -251,7 +264,7 @@ def nt_sweep(sv, synth, dev, reps=20):
         for nt in wl["nts"]:
             times = []
             for i in range(reps + 3):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(st)
                 sv.spec_linear_q(qm, x, nt, y, st)
@@ -300,11 +313,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
         e0.record(st)
         for j in range(args.warmup, n_rounds):
             sv.spec_verify_round(m, 1, sid, dr_dev[j], d, n_acc=n_acc[j], emitted=em[j])
         e1.record(st)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     barrier(dist)
     torch.cuda.synchronize()
     assert sv.spec_error_check(m) == 0
@@ -498,8 +513,32 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0}}))
 
 
+def linear_only(spec: str, nt: int = 8, reps: int = 3):
+    """Profiling driver: spec_linear_q at nt on packed synthetic matrices,
+    `spec` = 'QT:N:K,QT:N:K,...', each launched `reps` times."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from speculative_decoding_verification_round_gb300 import synth
+    dev = torch.device("cuda:0")
+    gen = synth.torch_gen(3, dev)
+    for item in spec.split(","):
+        qt, N, K = (int(v) for v in item.split(":"))
+        w = synth.q_weight_torch(gen, qt, N, K, dev)
+        qm = sv.QMat(w, max_rows=16)
+        x = synth.f16_normal_torch(gen, (nt, K), dev).view(torch.int16)
+        y = torch.empty((nt, N), dtype=torch.float32, device=dev)
+        for _ in range(reps):
+            sv.spec_linear_q(qm, x, nt, y)
+        torch.cuda.synchronize()
+        qm.close()
+        del w
+    print("linear-only ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--linear-only", default=None,
+                    help="profiling driver: QT:N:K[,QT:N:K...] verify-GEMM launches only")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
@@ -507,6 +546,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.linear_only:
+        linear_only(args.linear_only)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -44,6 +44,7 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // capture); once per device.
 void attn_init_attrs();
 void accept_init_attrs();
+void linear_init_attrs();
 static std::mutex g_attr_mu;
 static std::vector<int> g_attr_done;
 static void init_attrs_once() {
@@ -53,6 +54,7 @@ static void init_attrs_once() {
   if (std::find(g_attr_done.begin(), g_attr_done.end(), dev) != g_attr_done.end()) return;
   attn_init_attrs();
   accept_init_attrs();
+  linear_init_attrs();
   g_attr_done.push_back(dev);
 }
 
@@ -340,7 +342,7 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
     TRY(qmat_pack(&w->wd[l], PERM_IDENTITY, 0, m->sms, st, &m->wd[l]));
     m->weight_bytes += m->wqkv[l].bytes + m->wo[l].bytes + m->wgu[l].bytes + m->wd[l].bytes;
   }
-  TRY(qmat_pack(&w->lm_head, PERM_IDENTITY, 0, 0, st, &m->lm));
+  TRY(qmat_pack(&w->lm_head, PERM_IDENTITY, 0, m->sms, st, &m->lm));
   m->weight_bytes += m->lm.bytes;
   TRY(dalloc_t(m, &m->norm_w, (size_t)(2 * L + 1) * H));
   if (cudaMemcpyAsync(m->norm_w, w->norm_w, sizeof(float) * (2 * L + 1) * H,

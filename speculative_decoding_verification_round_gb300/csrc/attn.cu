@@ -232,6 +232,9 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
 }
 
 // One warp per (row, q head): merge chunks 0..P/CH in increasing order.
+// The chunk maxima are loaded in parallel (one chunk per lane), the global
+// max is a butterfly; the weighted sums then run over the chunks in order
+// with the loads of four chunks in flight at a time.
 template <int HD>
 __global__ void __launch_bounds__(128)
 attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
@@ -248,23 +251,43 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
   const int pos = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
   const int nc = pos / CH + 1;
   const size_t base = ((size_t)s * nkv + kvh) * nchunks;
+  const size_t stride = (size_t)M * (HD + 2);  // floats between consecutive chunks
+  const float* p0 = part + (base * M + m) * (HD + 2);
   float mx = -INFINITY;
-  for (int c = 0; c < nc; c++) {
-    const float mc = part[((base + c) * M + m) * (HD + 2) + HD];
-    mx = fmaxf(mx, mc);
-  }
+  for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldg(p0 + c * stride + HD));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   constexpr int PER = HD / 32;
   float o[PER];
 #pragma unroll
   for (int e = 0; e < PER; e++) o[e] = 0.0f;
   float l = 0.0f;
-  for (int c = 0; c < nc; c++) {
-    const float* src = part + ((base + c) * M + m) * (HD + 2);
-    const float2 ml = *reinterpret_cast<const float2*>(src + HD);
+  int c = 0;
+  for (; c + 4 <= nc; c += 4) {
+    float2 ml[4];
+    float v[4][PER];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float* src = p0 + (c + u) * stride;
+      ml[u] = __ldg(reinterpret_cast<const float2*>(src + HD));
+#pragma unroll
+      for (int e = 0; e < PER; e++) v[u][e] = __ldg(src + lane * PER + e);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float w = exp2f(ml[u].x - mx);
+      l = fmaf(ml[u].y, w, l);
+#pragma unroll
+      for (int e = 0; e < PER; e++) o[e] = fmaf(v[u][e], w, o[e]);
+    }
+  }
+  for (; c < nc; c++) {
+    const float* src = p0 + c * stride;
+    const float2 ml = __ldg(reinterpret_cast<const float2*>(src + HD));
     const float w = exp2f(ml.x - mx);
     l = fmaf(ml.y, w, l);
 #pragma unroll
-    for (int e = 0; e < PER; e++) o[e] = fmaf(src[lane * PER + e], w, o[e]);
+    for (int e = 0; e < PER; e++) o[e] = fmaf(__ldg(src + lane * PER + e), w, o[e]);
   }
   const float inv = 1.0f / l;
   __half* dst = out + (size_t)r * nq * HD + (size_t)h * HD + lane * PER;

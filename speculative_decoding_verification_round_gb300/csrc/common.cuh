@@ -68,7 +68,7 @@ struct QMat {
 enum PermKind { PERM_IDENTITY = 0, PERM_ROPE_PAIRS = 1, PERM_GATE_UP = 2 };
 
 // split_sms > 0: choose the K-split from the matrix shape and this SM count;
-// split_sms == 0: no K-split (S = 1, as the LM head's fused argmax needs).
+// split_sms == 0: no K-split (S = 1).
 int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int split_sms,
               cudaStream_t st, QMat* out);
 void qmat_free(QMat* q);

@@ -21,14 +21,28 @@
 // equal across nt ("Speculative Decoding (D5-R) -- Plan", status notes:
 // batched verify made bitwise position-invariant).
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int WARPS = 8;
-constexpr int TPW = 2;  // tiles (of 16 rows) per warp
+constexpr int WARPS = 4;  // warps per CTA
+constexpr int TPW = 2;    // tiles (of 16 rows) per warp
+// Weight-stream ring per warp: NS stages of one 64-k chunk of TPW tiles,
+// filled with cp.async (16-byte copies that bypass L1) and consumed from
+// shared memory; NS - 1 chunks are in flight while one is computed.
+template <int QT>
+struct Ring {
+  static constexpr int NS = QT == 4 ? 8 : 6;
+  static constexpr int QS = TPW * 512;                  // nibble words
+  static constexpr int SC = TPW * 64;                   // fp16 scales
+  static constexpr int QH = QT == 6 ? TPW * 256 : 0;    // 6-bit high fields
+  static constexpr int STAGE = QS + SC + QH;
+  static constexpr int WARP_BYTES = NS * STAGE;
+  static constexpr int CTA_BYTES = WARPS * WARP_BYTES;
+};
 
 // ---------------------------------------------------------------------------
 // repack: canonical planes -> streaming layout
@@ -124,32 +138,42 @@ struct LinArgs {
   float2* amax_part;
 };
 
-template <int QT, int NCT>
-struct Stage {
-  uint4 a[TPW];
-  uint2 s[TPW];
-  uint2 h[QT == 6 ? TPW : 1];
-  uint4 b[NCT][2];
-};
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-template <int QT, int NCT>
-__device__ __forceinline__ void load_stage(Stage<QT, NCT>& st, const LinArgs& a,
-                                           int tile0, int c, int zrow0, int lane) {
-  const int g = lane >> 2, t = lane & 3;
+// Issue the copies of chunk c of this warp's tiles into ring stage `st`.
+template <int QT>
+__device__ __forceinline__ void issue_chunk(const LinArgs& a, unsigned char* st, int tile0, int c,
+                                            int lane) {
 #pragma unroll
   for (int i = 0; i < TPW; i++) {
     const int T = tile0 + i;
-    if (T < a.n_tiles) {
-      size_t o = ((size_t)T * a.nch + c) * 32 + lane;
-      st.a[i] = ldg_stream(a.qs + o);
-      if constexpr (QT == 6) st.h[i] = ldg_stream2(a.qh + o);
-      st.s[i] = ldg_stream2(a.sc + ((size_t)T * a.nch + c) * 8 + g);
-    } else {
-      st.a[i] = make_uint4(0, 0, 0, 0);
-      st.s[i] = make_uint2(0, 0);
-      if constexpr (QT == 6) st.h[i] = make_uint2(0, 0);
-    }
+    if (T >= a.n_tiles) continue;
+    const size_t u = (size_t)T * a.nch + c;
+    cp_async16(smem_addr(st + i * 512 + lane * 16), a.qs + u * 32 + lane);
+    if (lane < 4) cp_async16(smem_addr(st + Ring<QT>::QS + i * 64 + lane * 16), a.sc + u * 8 + 2 * lane);
+    if constexpr (QT == 6)
+      if (lane < 16)
+        cp_async16(smem_addr(st + Ring<QT>::QS + Ring<QT>::SC + i * 256 + lane * 16),
+                   a.qh + u * 32 + 2 * lane);
   }
+}
+
+// Activations (B operand) of chunk c for this lane: rows zrow0 + ct*8 + g,
+// k = 64c + 32b + 8t .. +7 (zero beyond R or K).
+template <int NCT>
+__device__ __forceinline__ void load_x(uint4 (&xb)[NCT][2], const LinArgs& a, int c, int zrow0,
+                                       int lane) {
+  const int g = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int ct = 0; ct < NCT; ct++) {
     const int r = zrow0 + ct * 8 + g;
@@ -157,9 +181,9 @@ __device__ __forceinline__ void load_stage(Stage<QT, NCT>& st, const LinArgs& a,
     for (int b = 0; b < 2; b++) {
       const int k = 64 * c + 32 * b + 8 * t;
       if (r < a.R && k < a.K)
-        st.b[ct][b] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)r * a.K + k));
+        xb[ct][b] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)r * a.K + k));
       else
-        st.b[ct][b] = make_uint4(0, 0, 0, 0);
+        xb[ct][b] = make_uint4(0, 0, 0, 0);
     }
   }
 }
@@ -198,18 +222,26 @@ __device__ __forceinline__ void dequant_step(uint32_t w, uint32_t hx, uint32_t (
 }
 
 template <int QT, int NCT>
-__device__ __forceinline__ void compute_stage(const Stage<QT, NCT>& st,
+__device__ __forceinline__ void compute_chunk(const unsigned char* st, const uint4 (&xb)[NCT][2],
+                                              int tile0, int n_tiles, int lane,
                                               float (&acc)[TPW][NCT][4]) {
+  const int g = lane >> 2;
 #pragma unroll
   for (int i = 0; i < TPW; i++) {
-    const uint32_t words[4] = {st.a[i].x, st.a[i].y, st.a[i].z, st.a[i].w};
-    const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&st.s[i].x));
-    const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&st.s[i].y));
+    if (tile0 + i >= n_tiles) continue;
+    const uint4 aw = *reinterpret_cast<const uint4*>(st + i * 512 + lane * 16);
+    const uint2 sw = *reinterpret_cast<const uint2*>(st + Ring<QT>::QS + i * 64 + g * 8);
+    uint2 hw = make_uint2(0, 0);
+    if constexpr (QT == 6)
+      hw = *reinterpret_cast<const uint2*>(st + Ring<QT>::QS + Ring<QT>::SC + i * 256 + lane * 8);
+    const uint32_t words[4] = {aw.x, aw.y, aw.z, aw.w};
+    const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sw.x));
+    const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sw.y));
 #pragma unroll
     for (int b = 0; b < 2; b++) {
       uint32_t hA = 0, hB = 0;
       if constexpr (QT == 6) {
-        hA = b == 0 ? st.h[i].x : st.h[i].y;
+        hA = b == 0 ? hw.x : hw.y;
         hB = __funnelshift_l(hA, hA, 8);
       }
       uint32_t A0[4], A1[4];
@@ -220,8 +252,8 @@ __device__ __forceinline__ void compute_stage(const Stage<QT, NCT>& st,
 #pragma unroll
       for (int ct = 0; ct < NCT; ct++) {
         float blk[4];
-        mma_16816_zero(blk, A0, st.b[ct][b].x, st.b[ct][b].y);
-        mma_16816(blk, A1, st.b[ct][b].z, st.b[ct][b].w);
+        mma_16816_zero(blk, A0, xb[ct][b].x, xb[ct][b].y);
+        mma_16816(blk, A1, xb[ct][b].z, xb[ct][b].w);
         acc[i][ct][0] = fmaf(sg, blk[0], acc[i][ct][0]);
         acc[i][ct][1] = fmaf(sg, blk[1], acc[i][ct][1]);
         acc[i][ct][2] = fmaf(sg8, blk[2], acc[i][ct][2]);
@@ -315,15 +347,18 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct,
   }
 }
 
-template <int QT, int NCT, int PF>
+template <int QT, int NCT>
 __global__ void __launch_bounds__(WARPS * 32)
 linear_q_kernel(const LinArgs a) {
+  extern __shared__ __align__(128) unsigned char ring_smem[];
+  constexpr int NS = Ring<QT>::NS;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int z = blockIdx.x, grp = blockIdx.y, seg = blockIdx.z;
   const int tile0 = (grp * WARPS + warp) * TPW;
   const int zrow0 = z * 8 * NCT;
   const int c_begin = (int)((long long)seg * a.nch / a.S);
   const int c_end = (int)((long long)(seg + 1) * a.nch / a.S);
+  unsigned char* ring = ring_smem + warp * Ring<QT>::WARP_BYTES;
 
   float acc[TPW][NCT][4];
 #pragma unroll
@@ -334,20 +369,29 @@ linear_q_kernel(const LinArgs a) {
       for (int q = 0; q < 4; q++) acc[i][ct][q] = 0.0f;
 
   if (tile0 < a.n_tiles) {
-    Stage<QT, NCT> buf[PF];
+    const int nc = c_end - c_begin;
 #pragma unroll
-    for (int i = 0; i < PF; i++)
-      if (c_begin + i < c_end) load_stage<QT, NCT>(buf[i], a, tile0, c_begin + i, zrow0, lane);
-    for (int c = c_begin; c < c_end; c += PF) {
+    for (int j = 0; j < NS - 1; j++) {
+      if (j < nc) issue_chunk<QT>(a, ring + j * Ring<QT>::STAGE, tile0, c_begin + j, lane);
+      cp_async_commit();
+    }
+    uint4 xb[NCT][2], xn[NCT][2];
+    load_x<NCT>(xb, a, c_begin, zrow0, lane);
+    for (int j = 0; j < nc; j++) {
+      cp_async_wait<NS - 2>();  // chunk j has landed (this lane's copies)
+      __syncwarp();             // ... and every lane's
+      const int jn = j + NS - 1;
+      if (jn < nc) issue_chunk<QT>(a, ring + (jn % NS) * Ring<QT>::STAGE, tile0, c_begin + jn, lane);
+      cp_async_commit();
+      if (j + 1 < nc) load_x<NCT>(xn, a, c_begin + j + 1, zrow0, lane);
+      compute_chunk<QT, NCT>(ring + (j % NS) * Ring<QT>::STAGE, xb, tile0, a.n_tiles, lane, acc);
 #pragma unroll
-      for (int i = 0; i < PF; i++) {
-        if (c + i < c_end) {
-          compute_stage<QT, NCT>(buf[i], acc);
-          if (c + i + PF < c_end)
-            load_stage<QT, NCT>(buf[i], a, tile0, c + i + PF, zrow0, lane);
-        }
+      for (int ct = 0; ct < NCT; ct++) {
+        xb[ct][0] = xn[ct][0];
+        xb[ct][1] = xn[ct][1];
       }
     }
+    cp_async_wait<0>();
   }
 
   // ---- K-split: the last CTA of this (column group, tile group) sums the
@@ -453,7 +497,7 @@ linear_q_kernel(const LinArgs a) {
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned prev = atomicAdd(&a.tickets[z], 1u);
+    unsigned prev = atomicAdd(&a.tickets[gridDim.x * a.n_grp + z], 1u);
     s_last_am = (prev == (unsigned)(a.n_grp - 1));
   }
   __syncthreads();
@@ -471,22 +515,35 @@ linear_q_kernel(const LinArgs a) {
     }
     if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = id == 0x7fffffff ? 0 : id;
   }
-  if (threadIdx.x == 0) a.tickets[z] = 0u;
+  if (threadIdx.x == 0) a.tickets[gridDim.x * a.n_grp + z] = 0u;
 }
 
-int choose_split(int n_tiles, int nch, int sm_count) {
-  const int warp_tasks = (n_tiles + TPW - 1) / TPW;
-  const int target = sm_count * 12;  // resident warps we aim to keep busy
-  int S = (target + warp_tasks - 1) / warp_tasks;
-  S = std::max(1, std::min(S, nch / 2));
-  return S;
+// K-split for a matrix: fixed by its shape and the device only (never by
+// nt, so rows stay bitwise nt-invariant).  Cost model: the launch runs
+// ceil(CTAs / resident slots) waves, each as long as one segment (nch / S
+// chunks) plus a start-up latency worth ~2 chunks and the partial-sum write
+// (~0.5 chunk); the last CTA of a group reads S partials (~0.45 chunk each).
+int choose_split(int n_tiles, int nch, int slots) {
+  const int n_grp = (n_tiles + WARPS * TPW - 1) / (WARPS * TPW);
+  const int s_max = std::max(1, nch / 2);
+  int best = 1;
+  double best_cost = 1e30;
+  for (int S = 1; S <= s_max; S++) {
+    const double waves = std::ceil((double)n_grp * S / slots);
+    const double cost = waves * ((double)nch / S + 2.0 + (S > 1 ? 0.5 : 0.0)) +
+                        (S > 1 ? 0.45 * S : 0.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
 }
 
 template <int QT, int NCT>
 void launch_typed(const LinArgs& a, int ZG, cudaStream_t st) {
   dim3 grid(ZG, a.n_grp, a.S);
-  constexpr int PF = NCT == 1 ? 3 : 2;
-  linear_q_kernel<QT, NCT, PF><<<grid, WARPS * 32, 0, st>>>(a);
+  linear_q_kernel<QT, NCT><<<grid, WARPS * 32, Ring<QT>::CTA_BYTES, st>>>(a);
 }
 
 }  // namespace
@@ -514,7 +571,20 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int split_sms,
   q.Kp = (w->K + 63) / 64 * 64;
   q.nch = q.Kp / 64;
   q.n_tiles = q.N / 16;
-  q.S = split_sms > 0 ? choose_split(q.n_tiles, q.nch, split_sms) : 1;
+  if (split_sms > 0) {
+    // resident CTAs per SM of the nt <= 8 variant (the split must not depend on nt)
+    int per_sm = 0;
+    if (q.qtype == 4)
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linear_q_kernel<4, 1>, WARPS * 32,
+                                                    Ring<4>::CTA_BYTES);
+    else
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linear_q_kernel<6, 1>, WARPS * 32,
+                                                    Ring<6>::CTA_BYTES);
+    cudaGetLastError();
+    q.S = choose_split(q.n_tiles, q.nch, split_sms * std::max(per_sm, 1));
+  } else {
+    q.S = 1;
+  }
   const size_t units = (size_t)q.n_tiles * q.nch;
   const size_t b_qs = units * 32 * sizeof(uint4);
   const size_t b_qh = q.qtype == 6 ? units * 32 * sizeof(uint2) : 0;
@@ -555,7 +625,7 @@ size_t lin_part_floats(const QMat& w, int R) {
   return (size_t)w.S * col_groups(R) * w.n_tiles * col_tiles(R) * 32 * 4;
 }
 size_t lin_tickets_needed(const QMat& w, int R) {
-  return (size_t)col_groups(R) * tile_groups(w);
+  return (size_t)col_groups(R) * tile_groups(w) + col_groups(R);  // K-split + argmax
 }
 size_t lin_amax_entries(const QMat& w, int R) {
   return (size_t)col_groups(R) * tile_groups(w) * 16;
@@ -564,7 +634,6 @@ size_t lin_amax_entries(const QMat& w, int R) {
 int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
                   const LinScratch& scr, cudaStream_t st) {
   if (R < 1) return fail(SPEC_E_SHAPE, "linear: R must be >= 1");
-  if (epi.kind == EPI_LMHEAD && w.S != 1) return fail(SPEC_E_INVALID, "LM head needs S == 1");
   if (lin_part_floats(w, R) > scr.part_floats || lin_tickets_needed(w, R) > scr.n_tickets ||
       (epi.kind == EPI_LMHEAD && lin_amax_entries(w, R) > scr.amax_entries))
     return fail(SPEC_E_SHAPE, "linear: scratch too small for this R");
@@ -596,4 +665,11 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("linear launch: ") + cudaGetErrorString(e));
   return SPEC_OK;
+}
+
+void linear_init_attrs() {
+  cudaFuncSetAttribute(linear_q_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<4>::CTA_BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<4>::CTA_BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<6, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<6>::CTA_BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<6>::CTA_BYTES);
 }
