@@ -238,6 +238,33 @@ int spec_accept_stochastic(const float* p_logits, const float* q_logits,
                            const int32_t* seq_ids, uint64_t* emit_idx,
                            int32_t* n_acc, int32_t* emitted, void* stream);
 
+/* Same computation, arguments and results as spec_accept_stochastic, but
+ * this entry point allocates no memory at all.  It is for callers that cannot
+ * call cudaMalloc: code running while a stream is being captured into a CUDA
+ * graph, code whose device memory is owned by a custom allocator that forbids
+ * the driver's, and latency-critical loops that must not risk the implicit
+ * device synchronisation an allocation can cause.  (The pages have no
+ * counterpart for this entry point; it is an addition of this library.)
+ *  - Scratch is one fixed array in the library's device globals (about 64 KB
+ *    per GPU that loads the library, held until the process exits), so the
+ *    batch is limited: n_seq <= 1024 and n_seq * (2d + 1) <= 4096; larger
+ *    batches return SPEC_E_SHAPE with a message.  V is limited as for
+ *    spec_accept_stochastic.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU
+ *    (different streams, or different host threads) race and must be ordered
+ *    by the caller.  Each call clears the array's error word itself.
+ *  - Errors seen on the device (non-finite logit, bad draft id) make the
+ *    affected outputs -1 and leave emit_idx unchanged, as in
+ *    spec_accept_stochastic; spec_error_check does not report them. */
+int spec_accept_stochastic_noalloc(const float* p_logits, const float* q_logits,
+                                   const int32_t* draft, int n_seq, int d, int V,
+                                   float temperature, uint64_t seed,
+                                   const int32_t* seq_ids, uint64_t* emit_idx,
+                                   int32_t* n_acc, int32_t* emitted, void* stream);
+
 typedef struct {
   int32_t greedy;      /* 1: greedy argmax accept; 0: strict rejection sampling */
   float temperature;   /* stochastic only, > 0 */

@@ -33,7 +33,7 @@ EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_li
             "spec_kv_read", "spec_model_debug_read",
             "spec_state_set", "spec_state_get", "spec_error_check", "spec_model_set_graphs",
             "spec_verify_attn", "spec_lm_head", "spec_accept_greedy",
-            "spec_accept_stochastic", "spec_verify_round"]
+            "spec_accept_stochastic", "spec_accept_stochastic_noalloc", "spec_verify_round"]
 
 P = ctypes.c_void_p
 I32 = ctypes.c_int32
@@ -102,6 +102,8 @@ def lib():
                 "spec_accept_greedy": (I32, [P, P, I32, I32, P, P, P]),
                 "spec_accept_stochastic": (I32, [P, P, P, I32, I32, I32, ctypes.c_float, U64,
                                                  P, P, P, P, P]),
+                "spec_accept_stochastic_noalloc": (I32, [P, P, P, I32, I32, I32, ctypes.c_float,
+                                                         U64, P, P, P, P, P]),
                 "spec_verify_round": (I32, [P, I32, P, P, I32, P, ctypes.POINTER(spec_sampling),
                                             P, P, P, P]),
             }
@@ -302,6 +304,16 @@ def spec_accept_stochastic(p_logits, q_logits, draft, n_seq: int, d: int, V: int
                                         int(d), int(V), float(temperature), int(seed),
                                         _ptr(seq_ids), _ptr(emit_idx), _ptr(n_acc),
                                         _ptr(emitted), _stream(stream)))
+
+
+def spec_accept_stochastic_noalloc(p_logits, q_logits, draft, n_seq: int, d: int, V: int,
+                                   temperature: float, seed: int, seq_ids, emit_idx, n_acc,
+                                   emitted, stream=None):
+    """spec_accept_stochastic without any allocation (fixed scratch; see the header)."""
+    _check(lib().spec_accept_stochastic_noalloc(_ptr(p_logits), _ptr(q_logits), _ptr(draft),
+                                                int(n_seq), int(d), int(V), float(temperature),
+                                                int(seed), _ptr(seq_ids), _ptr(emit_idx),
+                                                _ptr(n_acc), _ptr(emitted), _stream(stream)))
 
 
 def spec_verify_round(m: Model, n_seq: int, seq_ids, draft, d: int, q_logits=None,

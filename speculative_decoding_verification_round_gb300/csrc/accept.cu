@@ -19,6 +19,10 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -456,4 +460,86 @@ void stoch_finalize(int n_seq, int d, int32_t* n_acc, int32_t* emitted, uint64_t
 
 void accept_init_attrs() {
   cudaFuncSetAttribute(row_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ST_MAX_SMEM);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the standalone stochastic accept.
+//
+// Its scratch (per-row max and integer-weight sums, per-sequence decisions,
+// and an error word) lives in one fixed-size array in the module's global
+// memory instead of memory from cudaMalloc.  Every GPU that loads this
+// library keeps the array (about 64 KB) until the process exits.  Host code
+// may not use the array's name as a device address; its address is looked up
+// once per device with cudaGetSymbolAddress, on the first call made while
+// that device is current.
+// ---------------------------------------------------------------------------
+constexpr int NOALLOC_MAX_ROWS = 4096;  // n_seq * (2d + 1)
+constexpr int NOALLOC_MAX_SEQS = 1024;
+
+struct NoAllocScratch {
+  float row_max[NOALLOC_MAX_ROWS];
+  unsigned long long row_sum[NOALLOC_MAX_ROWS];
+  int4 decision[NOALLOC_MAX_SEQS];
+  uint32_t err;
+};
+
+static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
+
+static std::mutex g_noalloc_mu;
+static std::vector<std::pair<int, NoAllocScratch*>> g_noalloc_ptrs;
+
+// Device address of this device's copy of the array (set-up on first use).
+static int noalloc_scratch(NoAllocScratch** out) {
+  int dev = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  for (auto& e : g_noalloc_ptrs)
+    if (e.first == dev) {
+      *out = e.second;
+      return SPEC_OK;
+    }
+  NoAllocScratch* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr)
+    return fail(SPEC_E_CUDA, std::string("cudaGetSymbolAddress of the fixed scratch: ") +
+                                 cudaGetErrorString(e));
+  accept_init_attrs();  // the row-statistics kernel's shared-memory limit, once per device
+  g_noalloc_ptrs.emplace_back(dev, p);
+  *out = p;
+  return SPEC_OK;
+}
+
+extern "C" int spec_accept_stochastic_noalloc(const float* p_logits, const float* q_logits,
+                                              const int32_t* draft, int n_seq, int d, int V,
+                                              float temperature, uint64_t seed,
+                                              const int32_t* seq_ids, uint64_t* emit_idx,
+                                              int32_t* n_acc, int32_t* emitted, void* stream) {
+  if (p_logits == nullptr || seq_ids == nullptr || emit_idx == nullptr || n_acc == nullptr ||
+      emitted == nullptr || (d > 0 && (draft == nullptr || q_logits == nullptr)))
+    return fail(SPEC_E_INVALID, "null argument");
+  if (n_seq < 1 || d < 0 || V < 1) return fail(SPEC_E_SHAPE, "n_seq >= 1, d >= 0, V >= 1 required");
+  if (!(temperature > 0.0f) || !isfinite(temperature))
+    return fail(SPEC_E_INVALID, "temperature must be finite and > 0");
+  if (n_seq > NOALLOC_MAX_SEQS || (long long)n_seq * (2 * d + 1) > NOALLOC_MAX_ROWS)
+    return fail(SPEC_E_SHAPE,
+                "spec_accept_stochastic_noalloc: n_seq * (2d + 1) must be <= 4096 and n_seq <= "
+                "1024 (fixed scratch); use spec_accept_stochastic for larger batches");
+  NoAllocScratch* sp = nullptr;
+  int rc = noalloc_scratch(&sp);
+  if (rc != SPEC_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the error word must start at zero
+  CUDA_TRY(cudaMemsetAsync(&sp->err, 0, sizeof(uint32_t), st));
+  StochScratch scr;
+  scr.row_max = sp->row_max;
+  scr.row_sum = sp->row_sum;
+  scr.decision = sp->decision;
+  scr.rows_cap = NOALLOC_MAX_ROWS;
+  scr.seq_cap = NOALLOC_MAX_SEQS;
+  rc = launch_accept_stochastic(p_logits, q_logits, draft, n_seq, d, V, temperature, seed, seq_ids,
+                                emit_idx, 0, 0, n_acc, emitted, scr, &sp->err, st);
+  if (rc != SPEC_OK) return rc;
+  stoch_finalize(n_seq, d, n_acc, emitted, emit_idx, &sp->err, st);
+  CUDA_TRY(cudaGetLastError());
+  return SPEC_OK;
 }
