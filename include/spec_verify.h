@@ -177,7 +177,10 @@ int spec_state_set(spec_model* m, int n, const int32_t* seq_ids,
 int spec_state_get(spec_model* m, int n, const int32_t* seq_ids, int32_t* n_past,
                    uint64_t* emit_idx, int32_t* anchor);
 
-/* Synchronises `stream`, reads and clears the device error word.
+/* Synchronises `stream`, reads and clears a device error word: the model's
+ * (m != NULL), else the one word this device's standalone entry points share
+ * (spec_linear_q, spec_accept_*): bit 0x10 there is a weight or activation
+ * copy that did not arrive within about a second.
  * Returns SPEC_OK or SPEC_E_INVALID (the bits are stored in *bits if not NULL). */
 int spec_error_check(spec_model* m, void* stream, uint32_t* bits);
 

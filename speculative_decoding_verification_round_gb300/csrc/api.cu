@@ -11,6 +11,7 @@
 // transaction in place; rejected KV rows need no restore because positions
 // are data and are overwritten by the next round.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -56,6 +57,14 @@ static void init_attrs_once() {
   accept_init_attrs();
   linear_init_attrs();
   g_attr_done.push_back(dev);
+}
+
+bool programmatic_launch() {
+  static const bool on = [] {
+    const char* e = std::getenv("SPEC_VERIFY_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return on;
 }
 
 static int sm_count() {
@@ -134,7 +143,8 @@ static int alloc_lin_scratch(const std::vector<const QMat*>& mats, int R, LinScr
     amax = std::max(amax, lin_amax_entries(*q, R));
   }
   tick = std::max(tick, (size_t)64);
-  const size_t bytes = part * sizeof(float) + amax * sizeof(float2) + tick * sizeof(unsigned) + 256;
+  const size_t bytes =
+      part * sizeof(float) + amax * sizeof(float2) + tick * sizeof(unsigned) + 16 + 256;
   if (cudaMalloc(base, bytes) != cudaSuccess) {
     cudaGetLastError();
     return fail(SPEC_E_OOM, "linear scratch");
@@ -148,7 +158,9 @@ static int alloc_lin_scratch(const std::vector<const QMat*>& mats, int R, LinScr
   p += amax * sizeof(float2);
   scr->tickets = (unsigned*)p;
   scr->n_tickets = tick;
-  CUDA_TRY(cudaMemset(scr->tickets, 0, tick * sizeof(unsigned)));
+  p += tick * sizeof(unsigned);
+  scr->err = (uint32_t*)p;  // the scratch's own error word (a model points it at its word)
+  CUDA_TRY(cudaMemset(scr->tickets, 0, tick * sizeof(unsigned) + 16));
   return SPEC_OK;
 }
 
@@ -157,8 +169,6 @@ extern "C" int spec_qmat_create(const spec_qweight* w, int max_rows, void* strea
   if (out == nullptr || w == nullptr) return fail(SPEC_E_INVALID, "null argument");
   *out = nullptr;
   if (max_rows < 1 || max_rows > 16 * 1024) return fail(SPEC_E_SHAPE, "max_rows out of range");
-  if (!aligned16(w->qs) || !aligned16(w->scales) || (w->qh && !aligned16(w->qh)))
-    ;  // canonical planes are read bytewise: no alignment requirement
   init_attrs_once();
   cudaStream_t st = as_stream(stream);
   spec_qmat* m = new spec_qmat();
@@ -169,6 +179,13 @@ extern "C" int spec_qmat_create(const spec_qweight* w, int max_rows, void* strea
   }
   m->max_rows = max_rows;
   rc = alloc_lin_scratch({&m->w}, max_rows, &m->scr, &m->scr_base);
+  if (rc == SPEC_OK) {
+    // a copy that never arrives is reported through the standalone entry
+    // points' error word (spec_error_check with no model)
+    Workspace* ws = nullptr;
+    rc = workspace_get(0, 0, &ws);
+    if (rc == SPEC_OK) m->scr.err = ws->err;
+  }
   if (rc == SPEC_OK && cudaStreamSynchronize(st) != cudaSuccess)
     rc = fail(SPEC_E_CUDA, std::string("repack: ") + cudaGetErrorString(cudaGetLastError()));
   if (rc != SPEC_OK) {
@@ -396,6 +413,7 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
     void* base = nullptr;
     TRY(alloc_lin_scratch(mats, R, &m->lscr, &base));
     m->allocs.push_back(base);
+    m->lscr.err = m->err;
   }
   m->sscr.rows_cap = stoch_rows_needed(D.max_seqs, D.max_nt - 1);
   m->sscr.seq_cap = D.max_seqs;

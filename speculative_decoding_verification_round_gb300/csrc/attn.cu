@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(128)
 attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
                   int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
                   __half* __restrict__ out) {
+  grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= R * nq) return;

@@ -35,42 +35,38 @@ int fail(int code, const std::string& msg);
 // ---------------------------------------------------------------------------
 // packed (streaming) layout of a block-quantised matrix
 // ---------------------------------------------------------------------------
-// The matrix is cut into tiles of 16 output rows and chunks of 64 along K
-// (two quantisation blocks).  For tile T, chunk c, lane l = 4g + t of a warp:
-//   qs word [T][c][l][j], j = k16 step (block b = j/2, half jj = j%2):
-//     nibble 0 -> row g,   k = 64c + 32b + 8t + 4jj + 0
-//     nibble 4 -> row g,   ...                     + 1
-//     nibble 2 -> row g,   ...                     + 2
-//     nibble 6 -> row g,   ...                     + 3
-//     nibble 1,5,3,7 -> the same four k of row g+8
-//   i.e. exactly the A fragment of mma.m16n8k16 (rows g/g+8) after the
-//   standard 0x6400 magic-number extraction, with the k order inside each
-//   32-block permuted so that lane t reads 8 consecutive activations.
-//   qh (Q6) word [T][c][l][h], h = block: two k16 steps, high 2-bit fields at
-//     bits 4..11 / 20..27 (step 2h) and 0..3 / 12..19 / 28..31 (step 2h+1,
-//     a rotate by 8 brings them to the step-2h positions).
-//   sc  [T][c][g][4] fp16: (row g, blk0), (row g+8, blk0), (g, blk1), (g+8, blk1).
-// K is zero-padded to a multiple of 64 (padding weights have q = 0, scale 0).
+// The matrix is cut into tiles of 16 output rows, grouped in pairs of two
+// tiles (one warp's work), and chunks of 64 along K (two quantisation
+// blocks).  Each (pair, chunk) is one contiguous record:
+//   [2 x 512 B nibble words][2 x 64 B fp16 scales][Q6: 2 x 256 B high fields]
+// For tile i of the quad and lane l = 4g + t, the 16-byte nibble vector at
+// i*512 + 16l holds the four k16 steps' mma.m16n8k16 A-fragment words of rows
+// g / g+8 (k order inside each 32-block permuted so that lane t reads 8
+// consecutive activations); the scales at 1024 + i*64 + 8g are (row g, blk0),
+// (row g+8, blk0), (g, blk1), (g+8, blk1); the Q6 high fields at
+// 1152 + i*256 + 8l are one word per block, pre-positioned for the
+// magic-number merge.  K is zero-padded to a multiple of 64 and N to a
+// multiple of 32 rows (padding weights have q = 0, scale 0).
 struct QMat {
   int qtype = 0;
   int N = 0, K = 0, Kp = 0;
-  int nch = 0;      // Kp / 64
-  int n_tiles = 0;  // N / 16
-  int S = 1;        // K-split segments (fixed per matrix: independent of nt)
-  uint4* qs = nullptr;   // [n_tiles][nch][32] uint4
-  uint2* qh = nullptr;   // [n_tiles][nch][32] uint2 (Q6)
-  uint2* sc = nullptr;   // [n_tiles][nch][8] uint2
-  void* base = nullptr;  // single allocation
-  size_t bytes = 0;      // streamed bytes (qs + qh + sc)
+  int nch = 0;       // Kp / 64
+  int n_tiles = 0;   // N / 16
+  int n_pairs = 0;   // ceil(n_tiles / 2): one warp's tiles
+  int n_grp = 0;     // CTA tile groups (8 pairs)
+  int rec_bytes = 0; // 1152 (Q4) or 1664 (Q6)
+  int S = 1;         // K-split segments (fixed per matrix: independent of nt)
+  uint8_t* rec = nullptr;  // [n_pairs][nch][rec_bytes]
+  void* base = nullptr;    // single allocation
+  size_t bytes = 0;        // streamed bytes
 };
 
 // Row permutation applied at repack: packed row p <- canonical row perm(p).
 enum PermKind { PERM_IDENTITY = 0, PERM_ROPE_PAIRS = 1, PERM_GATE_UP = 2 };
 
-// split_sms > 0: choose the K-split from the matrix shape and this SM count;
-// split_sms == 0: no K-split (S = 1).
-int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int split_sms,
-              cudaStream_t st, QMat* out);
+// sms: SM count of the device (sets the stream-K worker count).
+int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaStream_t st,
+              QMat* out);
 void qmat_free(QMat* q);
 
 // Epilogue kinds of the verify GEMM.
@@ -111,6 +107,7 @@ struct LinScratch {
   size_t n_tickets = 0;
   float2* amax_part = nullptr;   // LM-head argmax partials (value, index bits)
   size_t amax_entries = 0;
+  uint32_t* err = nullptr;       // device error word
 };
 
 size_t lin_part_floats(const QMat& w, int R);
@@ -170,6 +167,11 @@ void launch_commit(const int32_t* seq_ids, int n_seq, int d, int n_slots, const 
                    uint64_t* emit_idx, int32_t* anchor, const uint32_t* err,
                    cudaStream_t st);
 
+// Whether kernels that can overlap their predecessor's tail are launched as
+// programmatic dependents (default on; SPEC_VERIFY_PDL=0 in the environment
+// turns it off).
+bool programmatic_launch();
+
 // ---------------------------------------------------------------------------
 // device helpers
 // ---------------------------------------------------------------------------
@@ -196,6 +198,15 @@ __device__ __forceinline__ void mma_16816_zero(float (&d)[4], const uint32_t (&a
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Programmatic dependent launch.  grid_dep_wait blocks until the grids this
+// one depends on have completed and their writes are visible (it returns at
+// once for a plain launch); grid_dep_launch lets the stream's next kernel,
+// if it was launched programmatically, start before this grid completes.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {

@@ -6,14 +6,18 @@
 // from HBM exactly once per call, whatever nt is, and is applied to all
 // nt rows in registers:
 //
-//   * 16 output rows x 64 k per warp step; the 4-bit / 6-bit integers are
-//     turned into exact fp16 values with the 0x6400 magic-number trick and
-//     fed as the A operand of mma.sync m16n8k16 (f16 x f16 -> f32); the
-//     activations (n8 column tiles of verify rows) are the B operand;
+//   * a warp owns a pair of 16-row tiles; each 64-k chunk of the pair is one
+//     contiguous record in HBM, streamed with TMA bulk copies through a
+//     per-warp shared-memory ring; the CTA's slice of the activations is
+//     staged once in shared memory and shared by its 8 warps;
+//   * the 4-bit / 6-bit integers become exact fp16 values with the 0x6400
+//     magic-number trick and feed mma.sync m16n8k16 (f16 x f16 -> f32) as the
+//     A operand; the activations (n8 column tiles of verify rows) are B;
 //   * each 32-block is accumulated in a fresh fp32 fragment and folded into
 //     the running sum with one fp32 FMA by its fp16 scale;
-//   * K is split into S segments fixed per matrix (never per nt); the last
-//     CTA of a tile group sums the S partials in segment order;
+//   * K is split into S segments (S fixed per matrix, never per nt); the last
+//     CTA of a tile group to finish (a non-blocking ticket) adds the S
+//     partial sums in segment order;
 //   * epilogues: store, residual add, SwiGLU, RoPE + KV-cache write, and the
 //     LM head's fused per-row argmax.
 // Every output element is produced by the same instruction sequence for any
@@ -28,24 +32,31 @@
 
 namespace {
 
-constexpr int WARPS = 4;  // warps per CTA
-constexpr int TPW = 2;    // tiles (of 16 rows) per warp
-// Weight-stream ring per warp: NS stages of one 64-k chunk of TPW tiles,
-// filled with cp.async (16-byte copies that bypass L1) and consumed from
-// shared memory; NS - 1 chunks are in flight while one is computed.
+constexpr int WARPS = 8;     // warps per CTA
+constexpr int TPW = 2;       // tiles (of 16 rows) per warp: one pair
+constexpr int NS = 4;        // weight-ring stages per warp
+constexpr int NC_MAX = 16;   // chunks per K segment (the CTA's staged activation slice)
+constexpr int XSTRIDE = NC_MAX * 128 + 16;  // bytes per staged activation row (+16: no bank conflicts)
+constexpr int MAX_SPLIT = 64;
+
+// Record of one (pair, 64-k chunk): nibble words of the 2 tiles, their fp16
+// scales, then (Q6) the high 2-bit fields.
 template <int QT>
-struct Ring {
-  static constexpr int NS = QT == 4 ? 8 : 6;
-  static constexpr int QS = TPW * 512;                  // nibble words
-  static constexpr int SC = TPW * 64;                   // fp16 scales
-  static constexpr int QH = QT == 6 ? TPW * 256 : 0;    // 6-bit high fields
-  static constexpr int STAGE = QS + SC + QH;
-  static constexpr int WARP_BYTES = NS * STAGE;
-  static constexpr int CTA_BYTES = WARPS * WARP_BYTES;
+struct Rec {
+  static constexpr int QS = 0;                        // 2 x 512 B
+  static constexpr int SC = TPW * 512;                // 2 x 64 B
+  static constexpr int QH = SC + TPW * 64;            // 2 x 256 B (Q6)
+  static constexpr int BYTES = QH + (QT == 6 ? TPW * 256 : 0);  // 1152 / 1664
+};
+template <int QT, int NCT>
+struct Smem {
+  static constexpr int RING = WARPS * NS * Rec<QT>::BYTES;
+  static constexpr int X = 8 * NCT * XSTRIDE;
+  static constexpr int BYTES = RING + X;
 };
 
 // ---------------------------------------------------------------------------
-// repack: canonical planes -> streaming layout
+// repack: canonical planes -> streaming records
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int perm_row(int p, PermKind perm, int hd, int N) {
   if (perm == PERM_ROPE_PAIRS) {
@@ -72,54 +83,62 @@ __device__ __forceinline__ uint32_t canon_u(int qtype, const uint8_t* qs,
   return lo | (hi << 4);
 }
 
+// One thread per (tile T of the padded quads, chunk c, lane).  For lane
+// l = 4g + t, the nibble word of k16 step j (block b = j/2, half jj = j%2)
+// holds, in nibble slots 0,4,2,6, row g at k = 64c + 32b + 8t + 4jj + 0..3,
+// and in slots 1,5,3,7 row g+8 at the same k: exactly the A fragment of
+// mma.m16n8k16 after the magic-number extraction, with the k order inside
+// each 32-block permuted so that lane t reads 8 consecutive activations.
+// Q6 high fields of block b: step 2b at bits 4..11 / 20..27 of one word,
+// step 2b+1 where a rotate by 8 brings them to the same places.
 __global__ void pack_kernel(int qtype, const uint8_t* __restrict__ qs,
                             const uint8_t* __restrict__ qh,
-                            const uint16_t* __restrict__ scales, int N, int K,
-                            int nch, PermKind perm, int hd, uint4* __restrict__ oqs,
-                            uint2* __restrict__ oqh, uint2* __restrict__ osc) {
+                            const uint16_t* __restrict__ scales, int N, int K, int nch,
+                            int n_groups, PermKind perm, int hd, int rec_bytes,
+                            uint8_t* __restrict__ out) {
   const int n_tiles = N / 16;
-  size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  size_t total = (size_t)n_tiles * nch * 32;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)n_groups * TPW * nch * 32;
   if (idx >= total) return;
   const int lane = (int)(idx % 32);
   const int c = (int)((idx / 32) % nch);
   const int T = (int)(idx / 32 / nch);
+  const int Q = T / TPW, i = T % TPW;
   const int g = lane >> 2, t = lane & 3;
-  const int row_g = perm_row(T * 16 + g, perm, hd, N);
-  const int row_g8 = perm_row(T * 16 + g + 8, perm, hd, N);
-  // nibble slot i -> (row, element e): i = 0,4,2,6 -> row g e = 0,1,2,3;
-  //                                    i = 1,5,3,7 -> row g+8 e = 0,1,2,3.
+  uint8_t* rec = out + ((size_t)Q * nch + c) * rec_bytes;
+  const bool real = T < n_tiles;
+  const int row_g = real ? perm_row(T * 16 + g, perm, hd, N) : 0;
+  const int row_g8 = real ? perm_row(T * 16 + g + 8, perm, hd, N) : 0;
   const int slot_row8[8] = {0, 1, 0, 1, 0, 1, 0, 1};
   const int slot_e[8] = {0, 0, 2, 2, 1, 1, 3, 3};
-  // Q6 high-field bit positions of nibble slot i, step A / step B.
   const int posA[8] = {4, 8, 6, 10, 20, 24, 22, 26};
   uint32_t w[4], hw[2] = {0u, 0u};
   for (int j = 0; j < 4; j++) {
     const int b = j / 2, jj = j % 2;
     uint32_t word = 0;
-    for (int i = 0; i < 8; i++) {
-      int row = slot_row8[i] ? row_g8 : row_g;
-      int k = 64 * c + 32 * b + 8 * t + 4 * jj + slot_e[i];
-      uint32_t u = canon_u(qtype, qs, qh, row, K, k);
-      word |= (u & 0xFu) << (4 * i);
+    for (int s = 0; s < 8; s++) {
+      const int k = 64 * c + 32 * b + 8 * t + 4 * jj + slot_e[s];
+      const uint32_t u = real ? canon_u(qtype, qs, qh, slot_row8[s] ? row_g8 : row_g, K, k)
+                              : (qtype == 4 ? 8u : 32u);
+      word |= (u & 0xFu) << (4 * s);
       if (qtype == 6) {
-        int pos = jj == 0 ? posA[i] : (posA[i] + 24) % 32;  // rotl by 8 restores posA
+        const int pos = jj == 0 ? posA[s] : (posA[s] + 24) % 32;  // rotl by 8 restores posA
         hw[b] |= ((u >> 4) & 3u) << pos;
       }
     }
     w[j] = word;
   }
-  size_t o = ((size_t)T * nch + c) * 32 + lane;
-  oqs[o] = make_uint4(w[0], w[1], w[2], w[3]);
-  if (qtype == 6) oqh[o] = make_uint2(hw[0], hw[1]);
+  *reinterpret_cast<uint4*>(rec + Rec<4>::QS + i * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (qtype == 6)
+    *reinterpret_cast<uint2*>(rec + Rec<6>::QH + i * 256 + lane * 8) = make_uint2(hw[0], hw[1]);
   if (t == 0) {
     const int nb = K / 32;
     auto sc_of = [&](int row, int blk) -> uint32_t {
-      return blk < nb ? (uint32_t)scales[(size_t)row * nb + blk] : 0u;
+      return (real && blk < nb) ? (uint32_t)scales[(size_t)row * nb + blk] : 0u;
     };
-    uint32_t s0 = sc_of(row_g, 2 * c) | (sc_of(row_g8, 2 * c) << 16);
-    uint32_t s1 = sc_of(row_g, 2 * c + 1) | (sc_of(row_g8, 2 * c + 1) << 16);
-    osc[((size_t)T * nch + c) * 8 + g] = make_uint2(s0, s1);
+    const uint32_t s0 = sc_of(row_g, 2 * c) | (sc_of(row_g8, 2 * c) << 16);
+    const uint32_t s1 = sc_of(row_g, 2 * c + 1) | (sc_of(row_g8, 2 * c + 1) << 16);
+    *reinterpret_cast<uint2*>(rec + Rec<4>::SC + i * 64 + g * 8) = make_uint2(s0, s1);
   }
 }
 
@@ -127,82 +146,72 @@ __global__ void pack_kernel(int qtype, const uint8_t* __restrict__ qs,
 // the verify GEMM
 // ---------------------------------------------------------------------------
 struct LinArgs {
-  const uint4* qs;
-  const uint2* qh;
-  const uint2* sc;
+  const uint8_t* rec;
   const __half* x;
-  int N, K, nch, n_tiles, S, R, n_grp;
+  int N, K, nch, n_tiles, n_pairs, n_grp, S, R;
   LinEpi epi;
-  float* part;
-  unsigned* tickets;
-  float2* amax_part;
+  float* part;        // [S][ZG][n_tiles][NCT][32] float4
+  unsigned* tickets;  // [ZG][n_grp] K-split tickets, then [ZG] argmax tickets
+  float2* amax_part;  // [ZG][n_grp][16]
+  uint32_t* err;      // device error word (ERR_TIMEOUT on a copy that never arrived)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
-// Issue the copies of chunk c of this warp's tiles into ring stage `st`.
-template <int QT>
-__device__ __forceinline__ void issue_chunk(const LinArgs& a, unsigned char* st, int tile0, int c,
-                                            int lane) {
-#pragma unroll
-  for (int i = 0; i < TPW; i++) {
-    const int T = tile0 + i;
-    if (T >= a.n_tiles) continue;
-    const size_t u = (size_t)T * a.nch + c;
-    cp_async16(smem_addr(st + i * 512 + lane * 16), a.qs + u * 32 + lane);
-    if (lane < 4) cp_async16(smem_addr(st + Ring<QT>::QS + i * 64 + lane * 16), a.sc + u * 8 + 2 * lane);
-    if constexpr (QT == 6)
-      if (lane < 16)
-        cp_async16(smem_addr(st + Ring<QT>::QS + Ring<QT>::SC + i * 256 + lane * 16),
-                   a.qh + u * 32 + 2 * lane);
-  }
+// --- mbarrier + bulk-copy (TMA) helpers -----------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-
-// Activations (B operand) of chunk c for this lane: rows zrow0 + ct*8 + g,
-// k = 64c + 32b + 8t .. +7 (zero beyond R or K).
-template <int NCT>
-__device__ __forceinline__ void load_x(uint4 (&xb)[NCT][2], const LinArgs& a, int c, int zrow0,
-                                       int lane) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int ct = 0; ct < NCT; ct++) {
-    const int r = zrow0 + ct * 8 + g;
-#pragma unroll
-    for (int b = 0; b < 2; b++) {
-      const int k = 64 * c + 32 * b + 8 * t;
-      if (r < a.R && k < a.K)
-        xb[ct][b] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)r * a.K + k));
-      else
-        xb[ct][b] = make_uint4(0, 0, 0, 0);
-    }
-  }
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+// One contiguous global -> shared copy, completion counted on `bar`.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(10000)  // suspend at most ~10 us per try
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for a phase of `bar`: about a second at most, then false.
+constexpr int MBAR_TRIES = 1 << 17;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < MBAR_TRIES; i++)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 // A fragments of one k16 step from a packed nibble word (+ Q6 high fields).
 template <int QT>
 __device__ __forceinline__ void dequant_step(uint32_t w, uint32_t hx, uint32_t (&A)[4]) {
   const uint32_t MAG = 0x64006400u;
-  uint32_t w8 = w >> 8;
-  uint32_t r0 = lop3_and_or(w, 0x000F000Fu, MAG);
-  uint32_t r1 = lop3_and_or(w, 0x00F000F0u, MAG);
-  uint32_t r2 = lop3_and_or(w8, 0x000F000Fu, MAG);
-  uint32_t r3 = lop3_and_or(w8, 0x00F000F0u, MAG);
+  const uint32_t w8 = w >> 8;
+  uint32_t r0 = (w & 0x000F000Fu) | MAG;
+  uint32_t r1 = (w & 0x00F000F0u) | MAG;
+  uint32_t r2 = (w8 & 0x000F000Fu) | MAG;
+  uint32_t r3 = (w8 & 0x00F000F0u) | MAG;
   if constexpr (QT == 6) {
-    uint32_t hx2 = hx >> 2;
-    r0 = lop3_and_or(hx, 0x00300030u, r0);
-    r1 = lop3_and_or(hx, 0x03000300u, r1);
-    r2 = lop3_and_or(hx2, 0x00300030u, r2);
-    r3 = lop3_and_or(hx2, 0x03000300u, r3);
+    const uint32_t hx2 = hx >> 2;
+    r0 |= hx & 0x00300030u;
+    r1 |= hx & 0x03000300u;
+    r2 |= hx2 & 0x00300030u;
+    r3 |= hx2 & 0x03000300u;
   }
   // bits-0.. form: h = 1024 + u  -> q = h - (1024 + bias)
   // bits-4.. form: h = 1024 + 16u -> q = h/16 - (64 + bias)
@@ -221,19 +230,25 @@ __device__ __forceinline__ void dequant_step(uint32_t w, uint32_t hx, uint32_t (
   A[3] = *reinterpret_cast<uint32_t*>(&h3);
 }
 
+// One chunk: the pair's 2 tiles x 64 k against the staged activations.
 template <int QT, int NCT>
-__device__ __forceinline__ void compute_chunk(const unsigned char* st, const uint4 (&xb)[NCT][2],
-                                              int tile0, int n_tiles, int lane,
-                                              float (&acc)[TPW][NCT][4]) {
-  const int g = lane >> 2;
+__device__ __forceinline__ void compute_chunk(const unsigned char* st, const unsigned char* xs,
+                                              int j, int lane, float (&acc)[TPW][NCT][4]) {
+  using RC = Rec<QT>;
+  const int g = lane >> 2, t = lane & 3;
+  uint4 xb[NCT][2];
+#pragma unroll
+  for (int ct = 0; ct < NCT; ct++) {
+    const unsigned char* row = xs + (ct * 8 + g) * XSTRIDE + j * 128 + t * 16;
+    xb[ct][0] = *reinterpret_cast<const uint4*>(row);
+    xb[ct][1] = *reinterpret_cast<const uint4*>(row + 64);
+  }
 #pragma unroll
   for (int i = 0; i < TPW; i++) {
-    if (tile0 + i >= n_tiles) continue;
-    const uint4 aw = *reinterpret_cast<const uint4*>(st + i * 512 + lane * 16);
-    const uint2 sw = *reinterpret_cast<const uint2*>(st + Ring<QT>::QS + i * 64 + g * 8);
+    const uint4 aw = *reinterpret_cast<const uint4*>(st + RC::QS + i * 512 + lane * 16);
+    const uint2 sw = *reinterpret_cast<const uint2*>(st + RC::SC + i * 64 + g * 8);
     uint2 hw = make_uint2(0, 0);
-    if constexpr (QT == 6)
-      hw = *reinterpret_cast<const uint2*>(st + Ring<QT>::QS + Ring<QT>::SC + i * 256 + lane * 8);
+    if constexpr (QT == 6) hw = *reinterpret_cast<const uint2*>(st + RC::QH + i * 256 + lane * 8);
     const uint32_t words[4] = {aw.x, aw.y, aw.z, aw.w};
     const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&sw.x));
     const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&sw.y));
@@ -269,8 +284,8 @@ __device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi) {
 
 // Epilogue for one tile/column-tile fragment of finished sums.
 template <int NCT>
-__device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct,
-                                              int zrow0, int lane, const float (&v)[4],
+__device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, int zrow0,
+                                              int lane, const float (&v)[4],
                                               float (&bestv)[NCT][2], int (&besti)[NCT][2]) {
   const int g = lane >> 2, t = lane & 3;
   const LinEpi& e = a.epi;
@@ -278,69 +293,61 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct,
 #pragma unroll
   for (int c = 0; c < 2; c++) {
     const int r = zrow0 + ct * 8 + 2 * t + c;
-    const bool ok = r < a.R;
+    if (r >= a.R) continue;
     const float x0 = v[c], x1 = v[2 + c];  // rows g and g+8, column r
     switch (e.kind) {
       case EPI_STORE:
-        if (ok) {
+        e.y[(size_t)r * e.ldy + n0] = x0;
+        e.y[(size_t)r * e.ldy + n1] = x1;
+        break;
+      case EPI_RESID:
+        e.y[(size_t)r * e.ldy + n0] += x0;
+        e.y[(size_t)r * e.ldy + n1] += x1;
+        break;
+      case EPI_SWIGLU: {
+        const float sil = x0 / (1.0f + expf(-x0));
+        e.out16[(size_t)r * e.ldo + T * 8 + g] = __float2half_rn(sil * x1);
+        break;
+      }
+      case EPI_QKV: {
+        const int per_head = e.hd / 16;
+        const int hh = T / per_head, j = T % per_head;
+        const int i0 = 8 * j + g, i1 = e.hd / 2 + 8 * j + g;
+        const RowInfo ri = e.rows[r];
+        float y0 = x0, y1 = x1;
+        if (e.rope != nullptr && hh < e.nq + e.nkv) {
+          const int rp = ri.pos < e.max_ctx ? ri.pos : e.max_ctx - 1;  // invalid rows are flagged
+          const float2 cs = e.rope[(size_t)rp * (e.hd / 2) + i0];
+          y0 = fmaf(x0, cs.x, -x1 * cs.y);
+          y1 = fmaf(x1, cs.x, x0 * cs.y);
+        }
+        __half* dst;
+        if (hh < e.nq) {
+          dst = e.out16 + ((size_t)r * e.nq + hh) * e.hd;
+        } else {
+          const bool isk = hh < e.nq + e.nkv;
+          const int kvh = isk ? hh - e.nq : hh - e.nq - e.nkv;
+          if (ri.pos >= e.max_ctx) break;  // flagged by the row-info kernel
+          dst = (isk ? e.kcache : e.vcache) +
+                (((size_t)ri.slot * e.nkv + kvh) * e.max_ctx + ri.pos) * e.hd;
+        }
+        dst[i0] = __float2half_rn(y0);
+        dst[i1] = __float2half_rn(y1);
+        break;
+      }
+      case EPI_LMHEAD:
+        if (e.y != nullptr) {
           e.y[(size_t)r * e.ldy + n0] = x0;
           e.y[(size_t)r * e.ldy + n1] = x1;
         }
-        break;
-      case EPI_RESID:
-        if (ok) {
-          e.y[(size_t)r * e.ldy + n0] += x0;
-          e.y[(size_t)r * e.ldy + n1] += x1;
+        if (x0 != x0 || x1 != x1) atomicOr(e.err, ERR_NONFINITE);
+        if (amax_better(x0, n0, bestv[ct][c], besti[ct][c])) {
+          bestv[ct][c] = x0;
+          besti[ct][c] = n0;
         }
-        break;
-      case EPI_SWIGLU:
-        if (ok) {
-          const float sil = x0 / (1.0f + expf(-x0));
-          e.out16[(size_t)r * e.ldo + T * 8 + g] = __float2half_rn(sil * x1);
-        }
-        break;
-      case EPI_QKV:
-        if (ok) {
-          const int per_head = e.hd / 16;
-          const int hh = T / per_head, j = T % per_head;
-          const int i0 = 8 * j + g, i1 = e.hd / 2 + 8 * j + g;
-          const RowInfo ri = e.rows[r];
-          float y0 = x0, y1 = x1;
-          if (e.rope != nullptr && hh < e.nq + e.nkv) {
-            const int rp = ri.pos < e.max_ctx ? ri.pos : e.max_ctx - 1;  // invalid rows are flagged
-            const float2 cs = e.rope[(size_t)rp * (e.hd / 2) + i0];
-            y0 = x0 * cs.x - x1 * cs.y;
-            y1 = x1 * cs.x + x0 * cs.y;
-          }
-          __half* dst;
-          if (hh < e.nq) {
-            dst = e.out16 + ((size_t)r * e.nq + hh) * e.hd;
-          } else {
-            const bool isk = hh < e.nq + e.nkv;
-            const int kvh = isk ? hh - e.nq : hh - e.nq - e.nkv;
-            if (ri.pos >= e.max_ctx) break;  // flagged by the row-info kernel
-            dst = (isk ? e.kcache : e.vcache) +
-                  (((size_t)ri.slot * e.nkv + kvh) * e.max_ctx + ri.pos) * e.hd;
-          }
-          dst[i0] = __float2half_rn(y0);
-          dst[i1] = __float2half_rn(y1);
-        }
-        break;
-      case EPI_LMHEAD:
-        if (ok) {
-          if (e.y != nullptr) {
-            e.y[(size_t)r * e.ldy + n0] = x0;
-            e.y[(size_t)r * e.ldy + n1] = x1;
-          }
-          if (x0 != x0 || x1 != x1) atomicOr(e.err, ERR_NONFINITE);
-          if (amax_better(x0, n0, bestv[ct][c], besti[ct][c])) {
-            bestv[ct][c] = x0;
-            besti[ct][c] = n0;
-          }
-          if (amax_better(x1, n1, bestv[ct][c], besti[ct][c])) {
-            bestv[ct][c] = x1;
-            besti[ct][c] = n1;
-          }
+        if (amax_better(x1, n1, bestv[ct][c], besti[ct][c])) {
+          bestv[ct][c] = x1;
+          besti[ct][c] = n1;
         }
         break;
     }
@@ -350,15 +357,65 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct,
 template <int QT, int NCT>
 __global__ void __launch_bounds__(WARPS * 32)
 linear_q_kernel(const LinArgs a) {
-  extern __shared__ __align__(128) unsigned char ring_smem[];
-  constexpr int NS = Ring<QT>::NS;
+  extern __shared__ __align__(128) unsigned char smem[];
+  using RC = Rec<QT>;
+  __shared__ __align__(8) unsigned long long s_bar[WARPS][NS];
+  __shared__ __align__(8) unsigned long long s_xbar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  // column groups are the fastest grid index: the groups that stream the
+  // same weights run together and share them through L2
   const int z = blockIdx.x, grp = blockIdx.y, seg = blockIdx.z;
-  const int tile0 = (grp * WARPS + warp) * TPW;
+  const int ZG = gridDim.x;
+  const int pair = grp * WARPS + warp;
+  const int tile0 = pair * TPW;
   const int zrow0 = z * 8 * NCT;
   const int c_begin = (int)((long long)seg * a.nch / a.S);
-  const int c_end = (int)((long long)(seg + 1) * a.nch / a.S);
-  unsigned char* ring = ring_smem + warp * Ring<QT>::WARP_BYTES;
+  const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c_begin;
+  unsigned char* ring = smem + warp * NS * RC::BYTES;
+  const uint32_t ring_s = smem_addr(ring);
+  unsigned char* xs = smem + Smem<QT, NCT>::RING;
+  const uint32_t bar0 = smem_addr(&s_bar[warp][0]);
+  const uint32_t xbar = smem_addr(&s_xbar);
+
+  // ---- the weight ring of this warp: barriers and prologue.  Weights are
+  // ---- constant, so this runs before the grid dependency is resolved (with
+  // ---- a programmatic launch it overlaps the tail of the previous kernel).
+  const bool active = pair < a.n_pairs;
+  const uint8_t* src = a.rec + ((size_t)pair * a.nch + c_begin) * RC::BYTES;
+  if (active && lane == 0) {
+    for (int s = 0; s < NS; s++) mbar_init(bar0 + 8 * s, 1);
+    mbar_fence_init();
+    for (int j = 0; j < NS - 1 && j < nc; j++) {
+      mbar_expect_tx(bar0 + 8 * j, RC::BYTES);
+      bulk_copy(ring_s + j * RC::BYTES, src + (size_t)j * RC::BYTES, RC::BYTES, bar0 + 8 * j);
+    }
+  }
+  // ---- the activation slice (rows zrow0.., chunks c_begin..): zero what no
+  // ---- copy writes (rows >= R, a K tail), then one bulk copy per row.
+  const int kv = min(nc * 64, a.K - 64 * c_begin);
+  const int nrows = max(0, min(8 * NCT, a.R - zrow0));
+  for (int rr = warp; rr < 8 * NCT; rr += WARPS) {
+    const int from = rr < nrows ? kv * 2 : 0;
+    for (int o = from + lane * 16; o < nc * 128; o += 32 * 16)
+      *reinterpret_cast<uint4*>(xs + rr * XSTRIDE + o) = make_uint4(0, 0, 0, 0);
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(xbar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();  // zero fill of the slice and barrier inits are visible to all
+  // The activations, the scratch and the outputs belong to the stream's
+  // previous kernels: nothing below may touch global memory other than the
+  // weights before they have completed.
+  grid_dep_wait();
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(xbar, (uint32_t)(nrows * kv * 2));
+    for (int rr = 0; rr < nrows; rr++)
+      bulk_copy(smem_addr(xs + rr * XSTRIDE), a.x + (size_t)(zrow0 + rr) * a.K + 64 * c_begin,
+                (uint32_t)(kv * 2), xbar);
+  }
+  grid_dep_launch();  // the next kernel may start its own weight prefetch
 
   float acc[TPW][NCT][4];
 #pragma unroll
@@ -366,47 +423,55 @@ linear_q_kernel(const LinArgs a) {
 #pragma unroll
     for (int ct = 0; ct < NCT; ct++)
 #pragma unroll
-      for (int q = 0; q < 4; q++) acc[i][ct][q] = 0.0f;
+      for (int e = 0; e < 4; e++) acc[i][ct][e] = 0.0f;
 
-  if (tile0 < a.n_tiles) {
-    const int nc = c_end - c_begin;
-#pragma unroll
-    for (int j = 0; j < NS - 1; j++) {
-      if (j < nc) issue_chunk<QT>(a, ring + j * Ring<QT>::STAGE, tile0, c_begin + j, lane);
-      cp_async_commit();
-    }
-    uint4 xb[NCT][2], xn[NCT][2];
-    load_x<NCT>(xb, a, c_begin, zrow0, lane);
-    for (int j = 0; j < nc; j++) {
-      cp_async_wait<NS - 2>();  // chunk j has landed (this lane's copies)
-      __syncwarp();             // ... and every lane's
-      const int jn = j + NS - 1;
-      if (jn < nc) issue_chunk<QT>(a, ring + (jn % NS) * Ring<QT>::STAGE, tile0, c_begin + jn, lane);
-      cp_async_commit();
-      if (j + 1 < nc) load_x<NCT>(xn, a, c_begin + j + 1, zrow0, lane);
-      compute_chunk<QT, NCT>(ring + (j % NS) * Ring<QT>::STAGE, xb, tile0, a.n_tiles, lane, acc);
-#pragma unroll
-      for (int ct = 0; ct < NCT; ct++) {
-        xb[ct][0] = xn[ct][0];
-        xb[ct][1] = xn[ct][1];
+  bool ok = mbar_wait(xbar, 0);  // every warp waits for the slice (also the idle ones)
+  if (active) {
+    int s = 0;
+    uint32_t phase = 0;
+    int j = 0;
+    for (; j < nc && ok; j++) {
+      ok = mbar_wait(bar0 + 8 * s, phase);
+      if (!ok) break;
+      if (lane == 0 && j + NS - 1 < nc) {
+        // the stage before this one was consumed in iteration j - 1 (every
+        // lane passed its closing __syncwarp), so it can be refilled
+        const int sn = s == 0 ? NS - 1 : s - 1;
+        mbar_expect_tx(bar0 + 8 * sn, RC::BYTES);
+        bulk_copy(ring_s + sn * RC::BYTES, src + (size_t)(j + NS - 1) * RC::BYTES, RC::BYTES,
+                  bar0 + 8 * sn);
+      }
+      compute_chunk<QT, NCT>(ring + s * RC::BYTES, xs, j, lane, acc);
+      __syncwarp();
+      if (++s == NS) {
+        s = 0;
+        phase ^= 1u;
       }
     }
-    cp_async_wait<0>();
+    if (!ok) {
+      // a copy never arrived: flag it, then wait (bounded) for this warp's
+      // copies still in flight (records j .. j + NS - 2) before exiting
+      if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+      for (int jj = j; jj < nc && jj < j + NS - 1; jj++)
+        mbar_wait(bar0 + 8 * (jj % NS), (uint32_t)((jj / NS) & 1));
+    }
+  } else if (!ok && threadIdx.x == 0) {
+    atomicOr(a.err, ERR_TIMEOUT);
   }
+  if (!ok && threadIdx.x == 0) mbar_wait(xbar, 0);  // bounded drain of the slice copies
 
-  // ---- K-split: the last CTA of this (column group, tile group) sums the
-  // ---- S partials in segment order.
+  // ---- K-split: the last CTA of this (column group, tile group) to finish
+  // ---- adds the S partial sums in segment order.
   if (a.S > 1) {
     __shared__ int s_last;
-    const int ZG = gridDim.x;
-    if (tile0 < a.n_tiles) {
+    if (active) {
 #pragma unroll
       for (int i = 0; i < TPW; i++) {
         const int T = tile0 + i;
         if (T >= a.n_tiles) continue;
 #pragma unroll
         for (int ct = 0; ct < NCT; ct++) {
-          size_t o = ((((size_t)seg * ZG + z) * a.n_tiles + T) * NCT + ct) * 32 + lane;
+          const size_t o = ((((size_t)seg * ZG + z) * a.n_tiles + T) * NCT + ct) * 32 + lane;
           reinterpret_cast<float4*>(a.part)[o] =
               make_float4(acc[i][ct][0], acc[i][ct][1], acc[i][ct][2], acc[i][ct][3]);
         }
@@ -415,31 +480,41 @@ linear_q_kernel(const LinArgs a) {
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-      unsigned prev = atomicAdd(&a.tickets[z * a.n_grp + grp], 1u);
+      const unsigned prev = atomicAdd(&a.tickets[z * a.n_grp + grp], 1u);
       s_last = (prev == (unsigned)(a.S - 1));
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (tile0 < a.n_tiles) {
+    if (active) {
 #pragma unroll
       for (int i = 0; i < TPW; i++) {
         const int T = tile0 + i;
         if (T >= a.n_tiles) continue;
 #pragma unroll
         for (int ct = 0; ct < NCT; ct++) {
-          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int s = 0; s < a.S; s++) {
-            size_t o = ((((size_t)s * ZG + z) * a.n_tiles + T) * NCT + ct) * 32 + lane;
-            float4 p = __ldcg(reinterpret_cast<const float4*>(a.part) + o);
-            if (s == 0) {
-              sum = p;
-            } else {
-              sum.x += p.x; sum.y += p.y; sum.z += p.z; sum.w += p.w;
-            }
+          const float4* P = reinterpret_cast<const float4*>(a.part) +
+                            (((size_t)z * a.n_tiles + T) * NCT + ct) * 32 + lane;
+          const size_t step = (size_t)ZG * a.n_tiles * NCT * 32;  // one segment
+          float4 sum = __ldcg(P);
+          for (int s0 = 1; s0 < a.S; s0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++)  // eight partial loads in flight at a time
+              v[u] = s0 + u < a.S ? __ldcg(P + (size_t)(s0 + u) * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+              if (s0 + u < a.S) {
+                sum.x += v[u].x;
+                sum.y += v[u].y;
+                sum.z += v[u].z;
+                sum.w += v[u].w;
+              }
           }
-          acc[i][ct][0] = sum.x; acc[i][ct][1] = sum.y;
-          acc[i][ct][2] = sum.z; acc[i][ct][3] = sum.w;
+          acc[i][ct][0] = sum.x;
+          acc[i][ct][1] = sum.y;
+          acc[i][ct][2] = sum.z;
+          acc[i][ct][3] = sum.w;
         }
       }
     }
@@ -452,21 +527,25 @@ linear_q_kernel(const LinArgs a) {
 #pragma unroll
   for (int ct = 0; ct < NCT; ct++)
 #pragma unroll
-    for (int c = 0; c < 2; c++) { bestv[ct][c] = -INFINITY; besti[ct][c] = 0x7fffffff; }
-  if (tile0 < a.n_tiles) {
+    for (int c = 0; c < 2; c++) {
+      bestv[ct][c] = -INFINITY;
+      besti[ct][c] = 0x7fffffff;
+    }
+  if (active) {
 #pragma unroll
     for (int i = 0; i < TPW; i++) {
       const int T = tile0 + i;
       if (T >= a.n_tiles) continue;
 #pragma unroll
-      for (int ct = 0; ct < NCT; ct++) epilogue_frag<NCT>(a, T, ct, zrow0, lane, acc[i][ct], bestv, besti);
+      for (int ct = 0; ct < NCT; ct++)
+        epilogue_frag<NCT>(a, T, ct, zrow0, lane, acc[i][ct], bestv, besti);
     }
   }
   if (a.epi.kind != EPI_LMHEAD) return;
 
   // ---- fused argmax: warp (over the 8 row lanes g) -> CTA -> grid.
-  __shared__ float s_v[WARPS][8 * NCT];
-  __shared__ int s_i[WARPS][8 * NCT];
+  __shared__ float s_v[WARPS][16];
+  __shared__ int s_i[WARPS][16];
   __shared__ int s_last_am;
 #pragma unroll
   for (int ct = 0; ct < NCT; ct++)
@@ -476,13 +555,16 @@ linear_q_kernel(const LinArgs a) {
       int id = besti[ct][c];
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        int oi = __shfl_xor_sync(0xffffffffu, id, off);
-        if (amax_better(ov, oi, v, id)) { v = ov; id = oi; }
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, id, off);
+        if (amax_better(ov, oi, v, id)) {
+          v = ov;
+          id = oi;
+        }
       }
-      if ((lane >> 2) == 0) {
-        s_v[warp][ct * 8 + 2 * (lane & 3) + c] = v;
-        s_i[warp][ct * 8 + 2 * (lane & 3) + c] = id;
+      if (g == 0) {
+        s_v[warp][ct * 8 + 2 * t + c] = v;
+        s_i[warp][ct * 8 + 2 * t + c] = id;
       }
     }
   __syncthreads();
@@ -491,47 +573,62 @@ linear_q_kernel(const LinArgs a) {
     float v = s_v[0][col];
     int id = s_i[0][col];
     for (int w = 1; w < WARPS; w++)
-      if (amax_better(s_v[w][col], s_i[w][col], v, id)) { v = s_v[w][col]; id = s_i[w][col]; }
+      if (amax_better(s_v[w][col], s_i[w][col], v, id)) {
+        v = s_v[w][col];
+        id = s_i[w][col];
+      }
     a.amax_part[((size_t)z * a.n_grp + grp) * 16 + col] = make_float2(v, __int_as_float(id));
   }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned prev = atomicAdd(&a.tickets[gridDim.x * a.n_grp + z], 1u);
+    const unsigned prev = atomicAdd(&a.tickets[ZG * a.n_grp + z], 1u);
     s_last_am = (prev == (unsigned)(a.n_grp - 1));
   }
   __syncthreads();
   if (!s_last_am) return;
   __threadfence();
-  if (threadIdx.x < 8 * NCT) {
-    const int col = threadIdx.x;
-    const int r = zrow0 + col;
-    float v = -INFINITY;
-    int id = 0x7fffffff;
-    for (int gi = 0; gi < a.n_grp; gi++) {
-      float2 p = __ldcg(a.amax_part + ((size_t)z * a.n_grp + gi) * 16 + col);
-      int pi = __float_as_int(p.y);
-      if (amax_better(p.x, pi, v, id)) { v = p.x; id = pi; }
+  if (warp == 0) {
+    for (int col = 0; col < 8 * NCT; col++) {
+      float v = -INFINITY;
+      int id = 0x7fffffff;
+      for (int gi = lane; gi < a.n_grp; gi += 32) {
+        const float2 p = __ldcg(a.amax_part + ((size_t)z * a.n_grp + gi) * 16 + col);
+        const int pi = __float_as_int(p.y);
+        if (amax_better(p.x, pi, v, id)) {
+          v = p.x;
+          id = pi;
+        }
+      }
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, id, off);
+        if (amax_better(ov, oi, v, id)) {
+          v = ov;
+          id = oi;
+        }
+      }
+      const int r = zrow0 + col;
+      if (lane == 0 && r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = id == 0x7fffffff ? 0 : id;
     }
-    if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = id == 0x7fffffff ? 0 : id;
   }
-  if (threadIdx.x == 0) a.tickets[gridDim.x * a.n_grp + z] = 0u;
+  if (threadIdx.x == 0) a.tickets[ZG * a.n_grp + z] = 0u;
 }
 
 // K-split for a matrix: fixed by its shape and the device only (never by
-// nt, so rows stay bitwise nt-invariant).  Cost model: the launch runs
-// ceil(CTAs / resident slots) waves, each as long as one segment (nch / S
-// chunks) plus a start-up latency worth ~2 chunks and the partial-sum write
-// (~0.5 chunk); the last CTA of a group reads S partials (~0.45 chunk each).
-int choose_split(int n_tiles, int nch, int slots) {
-  const int n_grp = (n_tiles + WARPS * TPW - 1) / (WARPS * TPW);
-  const int s_max = std::max(1, nch / 2);
-  int best = 1;
+// nt, so rows stay bitwise nt-invariant), with at most NC_MAX chunks per
+// segment.  Cost model: ceil(CTAs / resident slots) waves, each as long as
+// one segment (nch / S chunks) plus a start-up latency worth ~2 chunks; the
+// last CTA of a group reads the S partials (~1/8 chunk each).
+int choose_split(int n_grp, int nch, int slots) {
+  const int s_min = (nch + NC_MAX - 1) / NC_MAX;
+  const int s_max = std::max(s_min, std::min(MAX_SPLIT, nch / 2));
+  int best = s_min;
   double best_cost = 1e30;
-  for (int S = 1; S <= s_max; S++) {
+  for (int S = s_min; S <= s_max; S++) {
     const double waves = std::ceil((double)n_grp * S / slots);
-    const double cost = waves * ((double)nch / S + 2.0 + (S > 1 ? 0.5 : 0.0)) +
-                        (S > 1 ? 0.45 * S : 0.0);
+    const double cost = waves * ((double)nch / S + 2.0) + 0.125 * (S - 1);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = S;
@@ -541,9 +638,18 @@ int choose_split(int n_tiles, int nch, int slots) {
 }
 
 template <int QT, int NCT>
-void launch_typed(const LinArgs& a, int ZG, cudaStream_t st) {
-  dim3 grid(ZG, a.n_grp, a.S);
-  linear_q_kernel<QT, NCT><<<grid, WARPS * 32, Ring<QT>::CTA_BYTES, st>>>(a);
+cudaError_t launch_typed(const LinArgs& a, int ZG, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ZG, a.n_grp, a.S);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = Smem<QT, NCT>::BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, linear_q_kernel<QT, NCT>, a);
 }
 
 }  // namespace
@@ -551,13 +657,14 @@ void launch_typed(const LinArgs& a, int ZG, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int split_sms,
-              cudaStream_t st, QMat* out) {
+int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaStream_t st,
+              QMat* out) {
   if (w == nullptr || out == nullptr) return fail(SPEC_E_INVALID, "null qweight");
   if (w->qtype != SPEC_Q4 && w->qtype != SPEC_Q6)
     return fail(SPEC_E_UNSUPPORTED, "qtype must be SPEC_Q4 or SPEC_Q6");
   if (w->N <= 0 || w->K <= 0 || w->N % 16 != 0 || w->K % 32 != 0)
     return fail(SPEC_E_SHAPE, "need N % 16 == 0 and K % 32 == 0");
+  if (w->K > 64 * NC_MAX * MAX_SPLIT) return fail(SPEC_E_SHAPE, "K above 65536 is not supported");
   if (w->qs == nullptr || w->scales == nullptr || (w->qtype == SPEC_Q6 && w->qh == nullptr))
     return fail(SPEC_E_INVALID, "missing weight plane");
   if (perm == PERM_ROPE_PAIRS && (head_dim % 16 != 0 || w->N % head_dim != 0))
@@ -571,37 +678,33 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int split_sms,
   q.Kp = (w->K + 63) / 64 * 64;
   q.nch = q.Kp / 64;
   q.n_tiles = q.N / 16;
-  if (split_sms > 0) {
+  q.n_pairs = (q.n_tiles + TPW - 1) / TPW;
+  q.n_grp = (q.n_pairs + WARPS - 1) / WARPS;
+  q.rec_bytes = q.qtype == 4 ? Rec<4>::BYTES : Rec<6>::BYTES;
+  {
     // resident CTAs per SM of the nt <= 8 variant (the split must not depend on nt)
     int per_sm = 0;
     if (q.qtype == 4)
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linear_q_kernel<4, 1>, WARPS * 32,
-                                                    Ring<4>::CTA_BYTES);
+                                                    Smem<4, 1>::BYTES);
     else
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linear_q_kernel<6, 1>, WARPS * 32,
-                                                    Ring<6>::CTA_BYTES);
+                                                    Smem<6, 1>::BYTES);
     cudaGetLastError();
-    q.S = choose_split(q.n_tiles, q.nch, split_sms * std::max(per_sm, 1));
-  } else {
-    q.S = 1;
+    q.S = choose_split(q.n_grp, q.nch, std::max(sms, 1) * std::max(per_sm, 1));
   }
-  const size_t units = (size_t)q.n_tiles * q.nch;
-  const size_t b_qs = units * 32 * sizeof(uint4);
-  const size_t b_qh = q.qtype == 6 ? units * 32 * sizeof(uint2) : 0;
-  const size_t b_sc = units * 8 * sizeof(uint2);
-  q.bytes = b_qs + b_qh + b_sc;
+  const size_t units = (size_t)q.n_pairs * q.nch;
+  q.bytes = units * q.rec_bytes;
   if (cudaMalloc(&q.base, q.bytes) != cudaSuccess) {
     cudaGetLastError();
     return fail(SPEC_E_OOM, "cudaMalloc of packed weights failed");
   }
-  q.qs = reinterpret_cast<uint4*>(q.base);
-  q.qh = q.qtype == 6 ? reinterpret_cast<uint2*>((char*)q.base + b_qs) : nullptr;
-  q.sc = reinterpret_cast<uint2*>((char*)q.base + b_qs + b_qh);
-  const size_t total = units * 32;
+  q.rec = reinterpret_cast<uint8_t*>(q.base);
+  const size_t total = units * TPW * 32;
   const int threads = 256;
   pack_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, st>>>(
-      q.qtype, (const uint8_t*)w->qs, (const uint8_t*)w->qh,
-      (const uint16_t*)w->scales, q.N, q.K, q.nch, perm, head_dim, q.qs, q.qh, q.sc);
+      q.qtype, (const uint8_t*)w->qs, (const uint8_t*)w->qh, (const uint16_t*)w->scales, q.N,
+      q.K, q.nch, q.n_pairs, perm, head_dim, q.rec_bytes, q.rec);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     cudaFree(q.base);
@@ -618,58 +721,52 @@ void qmat_free(QMat* q) {
 
 static int col_tiles(int R) { return R <= 8 ? 1 : 2; }
 static int col_groups(int R) { return (R + 8 * col_tiles(R) - 1) / (8 * col_tiles(R)); }
-static int tile_groups(const QMat& w) { return (w.n_tiles + WARPS * TPW - 1) / (WARPS * TPW); }
 
 size_t lin_part_floats(const QMat& w, int R) {
-  if (w.S <= 1) return 0;
-  return (size_t)w.S * col_groups(R) * w.n_tiles * col_tiles(R) * 32 * 4;
+  return w.S > 1 ? (size_t)w.S * col_groups(R) * w.n_tiles * col_tiles(R) * 32 * 4 : 0;
 }
 size_t lin_tickets_needed(const QMat& w, int R) {
-  return (size_t)col_groups(R) * tile_groups(w) + col_groups(R);  // K-split + argmax
+  return (size_t)col_groups(R) * w.n_grp + col_groups(R);  // K-split + argmax tickets
 }
-size_t lin_amax_entries(const QMat& w, int R) {
-  return (size_t)col_groups(R) * tile_groups(w) * 16;
-}
+size_t lin_amax_entries(const QMat& w, int R) { return (size_t)col_groups(R) * w.n_grp * 16; }
 
 int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
                   const LinScratch& scr, cudaStream_t st) {
   if (R < 1) return fail(SPEC_E_SHAPE, "linear: R must be >= 1");
+  if (scr.err == nullptr) return fail(SPEC_E_INVALID, "linear: no error word");
   if (lin_part_floats(w, R) > scr.part_floats || lin_tickets_needed(w, R) > scr.n_tickets ||
       (epi.kind == EPI_LMHEAD && lin_amax_entries(w, R) > scr.amax_entries))
     return fail(SPEC_E_SHAPE, "linear: scratch too small for this R");
   LinArgs a;
-  a.qs = w.qs;
-  a.qh = w.qh;
-  a.sc = w.sc;
+  a.rec = w.rec;
   a.x = x;
   a.N = w.N;
   a.K = w.K;
   a.nch = w.nch;
   a.n_tiles = w.n_tiles;
+  a.n_pairs = w.n_pairs;
+  a.n_grp = w.n_grp;
   a.S = w.S;
   a.R = R;
-  a.n_grp = tile_groups(w);
   a.epi = epi;
   a.part = scr.part;
   a.tickets = scr.tickets;
   a.amax_part = scr.amax_part;
+  a.err = scr.err;
   const int ZG = col_groups(R);
   const int nct = col_tiles(R);
-  if (w.qtype == 4) {
-    if (nct == 1) launch_typed<4, 1>(a, ZG, st);
-    else launch_typed<4, 2>(a, ZG, st);
-  } else {
-    if (nct == 1) launch_typed<6, 1>(a, ZG, st);
-    else launch_typed<6, 2>(a, ZG, st);
-  }
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (w.qtype == 4)
+    e = nct == 1 ? launch_typed<4, 1>(a, ZG, st) : launch_typed<4, 2>(a, ZG, st);
+  else
+    e = nct == 1 ? launch_typed<6, 1>(a, ZG, st) : launch_typed<6, 2>(a, ZG, st);
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("linear launch: ") + cudaGetErrorString(e));
   return SPEC_OK;
 }
 
 void linear_init_attrs() {
-  cudaFuncSetAttribute(linear_q_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<4>::CTA_BYTES);
-  cudaFuncSetAttribute(linear_q_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<4>::CTA_BYTES);
-  cudaFuncSetAttribute(linear_q_kernel<6, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<6>::CTA_BYTES);
-  cudaFuncSetAttribute(linear_q_kernel<6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<6>::CTA_BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<4, 1>::BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<4, 2>::BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<6, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<6, 1>::BYTES);
+  cudaFuncSetAttribute(linear_q_kernel<6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<6, 2>::BYTES);
 }

@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ gamma,
                                                       int H, float eps,
                                                       __half* __restrict__ out) {
+  grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
   const int r = blockIdx.x;
   const float4* x = reinterpret_cast<const float4*>(h + (size_t)r * H);
   float ss = 0.0f;
