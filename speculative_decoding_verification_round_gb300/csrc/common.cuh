@@ -53,9 +53,12 @@ struct QMat {
   int nch = 0;       // Kp / 64
   int n_tiles = 0;   // N / 16
   int n_pairs = 0;   // ceil(n_tiles / 2): one warp's tiles
-  int n_grp = 0;     // CTA tile groups (8 pairs)
+  int n_grp = 0;     // CTA tile groups (8 / kw pairs each)
   int rec_bytes = 0; // 1152 (Q4) or 1664 (Q6)
-  int S = 1;         // K-split segments (fixed per matrix: independent of nt)
+  int kw = 1;        // warps sharing one pair's K range inside a CTA
+  int S = 1;         // K segments across CTAs
+  int nc_cta = 0;    // chunks of one CTA's K range (at most)
+                     // (kw, S) are fixed per matrix: independent of nt
   uint8_t* rec = nullptr;  // [n_pairs][nch][rec_bytes]
   void* base = nullptr;    // single allocation
   size_t bytes = 0;        // streamed bytes

@@ -6,16 +6,18 @@
 // from HBM exactly once per call, whatever nt is, and is applied to all
 // nt rows in registers:
 //
-//   * a warp owns a pair of 16-row tiles; each 64-k chunk of the pair is one
-//     contiguous record in HBM, streamed with TMA bulk copies through a
-//     per-warp shared-memory ring; the CTA's slice of the activations is
-//     staged once in shared memory and shared by its 8 warps;
+//   * a warp owns a pair of 16-row tiles and a stretch of K; each 64-k chunk
+//     of the pair is one contiguous record in HBM, streamed with TMA bulk
+//     copies through a per-warp shared-memory ring; the CTA's slice of the
+//     activations is staged once in shared memory and shared by its warps;
 //   * the 4-bit / 6-bit integers become exact fp16 values with the 0x6400
 //     magic-number trick and feed mma.sync m16n8k16 (f16 x f16 -> f32) as the
 //     A operand; the activations (n8 column tiles of verify rows) are B;
 //   * each 32-block is accumulated in a fresh fp32 fragment and folded into
 //     the running sum with one fp32 FMA by its fp16 scale;
-//   * K is split into S segments (S fixed per matrix, never per nt); the last
+//   * K is split into S segments across CTAs and, inside a CTA, into KW
+//     slices across warps ((KW, S) fixed per matrix, never per nt); the
+//     slices are added in slice order through shared memory, and the last
 //     CTA of a tile group to finish (a non-blocking ticket) adds the S
 //     partial sums in segment order;
 //   * epilogues: store, residual add, SwiGLU, RoPE + KV-cache write, and the
@@ -27,6 +29,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 
 #include "common.cuh"
 
@@ -35,8 +38,7 @@ namespace {
 constexpr int WARPS = 8;     // warps per CTA
 constexpr int TPW = 2;       // tiles (of 16 rows) per warp: one pair
 constexpr int NS = 4;        // weight-ring stages per warp
-constexpr int NC_MAX = 16;   // chunks per K segment (the CTA's staged activation slice)
-constexpr int XSTRIDE = NC_MAX * 128 + 16;  // bytes per staged activation row (+16: no bank conflicts)
+constexpr int NC_CTA_MAX = 64;  // chunks of one CTA's K range (its staged activation slice)
 constexpr int MAX_SPLIT = 64;
 
 // Record of one (pair, 64-k chunk): nibble words of the 2 tiles, their fp16
@@ -48,12 +50,14 @@ struct Rec {
   static constexpr int QH = SC + TPW * 64;            // 2 x 256 B (Q6)
   static constexpr int BYTES = QH + (QT == 6 ? TPW * 256 : 0);  // 1152 / 1664
 };
-template <int QT, int NCT>
-struct Smem {
-  static constexpr int RING = WARPS * NS * Rec<QT>::BYTES;
-  static constexpr int X = 8 * NCT * XSTRIDE;
-  static constexpr int BYTES = RING + X;
-};
+template <int QT>
+constexpr int ring_bytes() { return WARPS * NS * Rec<QT>::BYTES; }
+// Staged activation row: the CTA's K range plus 64 bytes, so that the rows
+// g = 0..7 of a fragment load fall in distinct shared-memory banks.
+inline int x_stride(int nc) { return nc * 128 + 64; }
+inline int smem_bytes(int qtype, int nct, int nc) {
+  return (qtype == 4 ? ring_bytes<4>() : ring_bytes<6>()) + 8 * nct * x_stride(nc);
+}
 
 // ---------------------------------------------------------------------------
 // repack: canonical planes -> streaming records
@@ -149,6 +153,7 @@ struct LinArgs {
   const uint8_t* rec;
   const __half* x;
   int N, K, nch, n_tiles, n_pairs, n_grp, S, R;
+  int xstride;        // bytes per staged activation row
   LinEpi epi;
   float* part;        // [S][ZG][n_tiles][NCT][32] float4
   unsigned* tickets;  // [ZG][n_grp] K-split tickets, then [ZG] argmax tickets
@@ -233,13 +238,14 @@ __device__ __forceinline__ void dequant_step(uint32_t w, uint32_t hx, uint32_t (
 // One chunk: the pair's 2 tiles x 64 k against the staged activations.
 template <int QT, int NCT>
 __device__ __forceinline__ void compute_chunk(const unsigned char* st, const unsigned char* xs,
-                                              int j, int lane, float (&acc)[TPW][NCT][4]) {
+                                              int xstride, int j, int lane,
+                                              float (&acc)[TPW][NCT][4]) {
   using RC = Rec<QT>;
   const int g = lane >> 2, t = lane & 3;
   uint4 xb[NCT][2];
 #pragma unroll
   for (int ct = 0; ct < NCT; ct++) {
-    const unsigned char* row = xs + (ct * 8 + g) * XSTRIDE + j * 128 + t * 16;
+    const unsigned char* row = xs + (ct * 8 + g) * xstride + j * 128 + t * 16;
     xb[ct][0] = *reinterpret_cast<const uint4*>(row);
     xb[ct][1] = *reinterpret_cast<const uint4*>(row + 64);
   }
@@ -354,11 +360,12 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
   }
 }
 
-template <int QT, int NCT>
+template <int QT, int NCT, int KW>
 __global__ void __launch_bounds__(WARPS * 32)
 linear_q_kernel(const LinArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using RC = Rec<QT>;
+  constexpr int P = WARPS / KW;  // tile pairs of a CTA; KW warps share each pair's K range
   __shared__ __align__(8) unsigned long long s_bar[WARPS][NS];
   __shared__ __align__(8) unsigned long long s_xbar;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -367,14 +374,18 @@ linear_q_kernel(const LinArgs a) {
   // same weights run together and share them through L2
   const int z = blockIdx.x, grp = blockIdx.y, seg = blockIdx.z;
   const int ZG = gridDim.x;
-  const int pair = grp * WARPS + warp;
+  const int pp = warp % P, ks = warp / P;
+  const int pair = grp * P + pp;
   const int tile0 = pair * TPW;
   const int zrow0 = z * 8 * NCT;
+  // the CTA's K range (segment seg of S), then this warp's slice ks of KW
   const int c_begin = (int)((long long)seg * a.nch / a.S);
   const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c_begin;
+  const int w_lo = ks * nc / KW;
+  const int wn = (ks + 1) * nc / KW - w_lo;
   unsigned char* ring = smem + warp * NS * RC::BYTES;
   const uint32_t ring_s = smem_addr(ring);
-  unsigned char* xs = smem + Smem<QT, NCT>::RING;
+  unsigned char* xs = smem + ring_bytes<QT>();
   const uint32_t bar0 = smem_addr(&s_bar[warp][0]);
   const uint32_t xbar = smem_addr(&s_xbar);
 
@@ -382,11 +393,11 @@ linear_q_kernel(const LinArgs a) {
   // ---- constant, so this runs before the grid dependency is resolved (with
   // ---- a programmatic launch it overlaps the tail of the previous kernel).
   const bool active = pair < a.n_pairs;
-  const uint8_t* src = a.rec + ((size_t)pair * a.nch + c_begin) * RC::BYTES;
+  const uint8_t* src = a.rec + ((size_t)pair * a.nch + c_begin + w_lo) * RC::BYTES;
   if (active && lane == 0) {
     for (int s = 0; s < NS; s++) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
-    for (int j = 0; j < NS - 1 && j < nc; j++) {
+    for (int j = 0; j < NS - 1 && j < wn; j++) {
       mbar_expect_tx(bar0 + 8 * j, RC::BYTES);
       bulk_copy(ring_s + j * RC::BYTES, src + (size_t)j * RC::BYTES, RC::BYTES, bar0 + 8 * j);
     }
@@ -398,7 +409,7 @@ linear_q_kernel(const LinArgs a) {
   for (int rr = warp; rr < 8 * NCT; rr += WARPS) {
     const int from = rr < nrows ? kv * 2 : 0;
     for (int o = from + lane * 16; o < nc * 128; o += 32 * 16)
-      *reinterpret_cast<uint4*>(xs + rr * XSTRIDE + o) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(xs + rr * a.xstride + o) = make_uint4(0, 0, 0, 0);
   }
   if (threadIdx.x == 0) {
     mbar_init(xbar, 1);
@@ -412,7 +423,7 @@ linear_q_kernel(const LinArgs a) {
   if (threadIdx.x == 0) {
     mbar_expect_tx(xbar, (uint32_t)(nrows * kv * 2));
     for (int rr = 0; rr < nrows; rr++)
-      bulk_copy(smem_addr(xs + rr * XSTRIDE), a.x + (size_t)(zrow0 + rr) * a.K + 64 * c_begin,
+      bulk_copy(smem_addr(xs + rr * a.xstride), a.x + (size_t)(zrow0 + rr) * a.K + 64 * c_begin,
                 (uint32_t)(kv * 2), xbar);
   }
   grid_dep_launch();  // the next kernel may start its own weight prefetch
@@ -427,32 +438,35 @@ linear_q_kernel(const LinArgs a) {
 
   bool ok = mbar_wait(xbar, 0);  // every warp waits for the slice (also the idle ones)
   if (active) {
-    int s = 0;
-    uint32_t phase = 0;
+    // the loop is unrolled by the ring depth, so stage indices, parities and
+    // ring addresses are compile-time constants
     int j = 0;
-    for (; j < nc && ok; j++) {
-      ok = mbar_wait(bar0 + 8 * s, phase);
-      if (!ok) break;
-      if (lane == 0 && j + NS - 1 < nc) {
-        // the stage before this one was consumed in iteration j - 1 (every
-        // lane passed its closing __syncwarp), so it can be refilled
-        const int sn = s == 0 ? NS - 1 : s - 1;
-        mbar_expect_tx(bar0 + 8 * sn, RC::BYTES);
-        bulk_copy(ring_s + sn * RC::BYTES, src + (size_t)(j + NS - 1) * RC::BYTES, RC::BYTES,
-                  bar0 + 8 * sn);
-      }
-      compute_chunk<QT, NCT>(ring + s * RC::BYTES, xs, j, lane, acc);
-      __syncwarp();
-      if (++s == NS) {
-        s = 0;
-        phase ^= 1u;
+    const uint8_t* nxt = src + (size_t)(NS - 1) * RC::BYTES;  // next record to fetch
+    for (int j0 = 0; j0 < wn && ok; j0 += NS) {
+      const uint32_t phase = (uint32_t)((j0 / NS) & 1);
+#pragma unroll
+      for (int u = 0; u < NS; u++) {
+        j = j0 + u;
+        if (j >= wn) break;
+        ok = mbar_wait(bar0 + 8 * u, phase);
+        if (!ok) break;
+        if (lane == 0 && j + NS - 1 < wn) {
+          // the stage before this one was consumed in iteration j - 1 (every
+          // lane passed its closing __syncwarp), so it can be refilled
+          const int sn = (u + NS - 1) % NS;
+          mbar_expect_tx(bar0 + 8 * sn, RC::BYTES);
+          bulk_copy(ring_s + sn * RC::BYTES, nxt, RC::BYTES, bar0 + 8 * sn);
+        }
+        nxt += RC::BYTES;
+        compute_chunk<QT, NCT>(ring + u * RC::BYTES, xs, a.xstride, w_lo + j, lane, acc);
+        __syncwarp();
       }
     }
     if (!ok) {
       // a copy never arrived: flag it, then wait (bounded) for this warp's
-      // copies still in flight (records j .. j + NS - 2) before exiting
+      // copies still in flight (records j .. j + NS - 2) before going on
       if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
-      for (int jj = j; jj < nc && jj < j + NS - 1; jj++)
+      for (int jj = j; jj < wn && jj < j + NS - 1; jj++)
         mbar_wait(bar0 + 8 * (jj % NS), (uint32_t)((jj / NS) & 1));
     }
   } else if (!ok && threadIdx.x == 0) {
@@ -460,11 +474,42 @@ linear_q_kernel(const LinArgs a) {
   }
   if (!ok && threadIdx.x == 0) mbar_wait(xbar, 0);  // bounded drain of the slice copies
 
+  // ---- the KW slices of a pair: added in slice order through shared
+  // ---- memory (the rings are free now); slice 0's warp carries on.
+  if constexpr (KW > 1) {
+    float4* red = reinterpret_cast<float4*>(smem);
+    __syncthreads();
+    if (ks > 0 && active) {
+#pragma unroll
+      for (int i = 0; i < TPW; i++)
+#pragma unroll
+        for (int ct = 0; ct < NCT; ct++)
+          red[((((ks - 1) * P + pp) * TPW + i) * NCT + ct) * 32 + lane] =
+              make_float4(acc[i][ct][0], acc[i][ct][1], acc[i][ct][2], acc[i][ct][3]);
+    }
+    __syncthreads();
+    if (ks == 0 && active) {
+      for (int k = 1; k < KW; k++) {
+#pragma unroll
+        for (int i = 0; i < TPW; i++)
+#pragma unroll
+          for (int ct = 0; ct < NCT; ct++) {
+            const float4 v = red[((((k - 1) * P + pp) * TPW + i) * NCT + ct) * 32 + lane];
+            acc[i][ct][0] += v.x;
+            acc[i][ct][1] += v.y;
+            acc[i][ct][2] += v.z;
+            acc[i][ct][3] += v.w;
+          }
+      }
+    }
+  }
+  const bool owner = ks == 0 && active;  // holds the pair's sums from here on
+
   // ---- K-split: the last CTA of this (column group, tile group) to finish
   // ---- adds the S partial sums in segment order.
   if (a.S > 1) {
     __shared__ int s_last;
-    if (active) {
+    if (owner) {
 #pragma unroll
       for (int i = 0; i < TPW; i++) {
         const int T = tile0 + i;
@@ -477,46 +522,67 @@ linear_q_kernel(const LinArgs a) {
         }
       }
     }
-    __threadfence();
+    // release: the barrier orders every warp's partial stores before thread
+    // 0's gpu-scope fence and ticket; acquire: the last CTA's thread 0 fences
+    // after its ticket and the barrier passes that on (reads bypass L1)
     __syncthreads();
     if (threadIdx.x == 0) {
+      __threadfence();
       const unsigned prev = atomicAdd(&a.tickets[z * a.n_grp + grp], 1u);
       s_last = (prev == (unsigned)(a.S - 1));
+      if (s_last) __threadfence();
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    if (active) {
+    if (owner) {
+      // eight partial loads in flight per lane, over both tiles
+      constexpr int SB = 8 / (TPW * NCT);
+      const size_t step = (size_t)ZG * a.n_tiles * NCT * 32;  // one segment
+      const float4* P0 = reinterpret_cast<const float4*>(a.part) +
+                         ((size_t)z * a.n_tiles * NCT) * 32 + lane;
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 sum[TPW][NCT];
 #pragma unroll
-      for (int i = 0; i < TPW; i++) {
-        const int T = tile0 + i;
-        if (T >= a.n_tiles) continue;
+      for (int i = 0; i < TPW; i++)
 #pragma unroll
-        for (int ct = 0; ct < NCT; ct++) {
-          const float4* P = reinterpret_cast<const float4*>(a.part) +
-                            (((size_t)z * a.n_tiles + T) * NCT + ct) * 32 + lane;
-          const size_t step = (size_t)ZG * a.n_tiles * NCT * 32;  // one segment
-          float4 sum = __ldcg(P);
-          for (int s0 = 1; s0 < a.S; s0 += 8) {
-            float4 v[8];
+        for (int ct = 0; ct < NCT; ct++)
+          sum[i][ct] = tile0 + i < a.n_tiles ? __ldcg(P0 + ((size_t)(tile0 + i) * NCT + ct) * 32)
+                                             : zero4;
+      for (int s0 = 1; s0 < a.S; s0 += SB) {
+        float4 v[SB][TPW][NCT];
 #pragma unroll
-            for (int u = 0; u < 8; u++)  // eight partial loads in flight at a time
-              v[u] = s0 + u < a.S ? __ldcg(P + (size_t)(s0 + u) * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < SB; u++)
 #pragma unroll
-            for (int u = 0; u < 8; u++)
-              if (s0 + u < a.S) {
-                sum.x += v[u].x;
-                sum.y += v[u].y;
-                sum.z += v[u].z;
-                sum.w += v[u].w;
+          for (int i = 0; i < TPW; i++)
+#pragma unroll
+            for (int ct = 0; ct < NCT; ct++)
+              v[u][i][ct] = (s0 + u < a.S && tile0 + i < a.n_tiles)
+                                ? __ldcg(P0 + (size_t)(s0 + u) * step +
+                                         ((size_t)(tile0 + i) * NCT + ct) * 32)
+                                : zero4;
+#pragma unroll
+        for (int u = 0; u < SB; u++)
+          if (s0 + u < a.S) {
+#pragma unroll
+            for (int i = 0; i < TPW; i++)
+#pragma unroll
+              for (int ct = 0; ct < NCT; ct++) {
+                sum[i][ct].x += v[u][i][ct].x;
+                sum[i][ct].y += v[u][i][ct].y;
+                sum[i][ct].z += v[u][i][ct].z;
+                sum[i][ct].w += v[u][i][ct].w;
               }
           }
-          acc[i][ct][0] = sum.x;
-          acc[i][ct][1] = sum.y;
-          acc[i][ct][2] = sum.z;
-          acc[i][ct][3] = sum.w;
-        }
       }
+#pragma unroll
+      for (int i = 0; i < TPW; i++)
+#pragma unroll
+        for (int ct = 0; ct < NCT; ct++) {
+          acc[i][ct][0] = sum[i][ct].x;
+          acc[i][ct][1] = sum[i][ct].y;
+          acc[i][ct][2] = sum[i][ct].z;
+          acc[i][ct][3] = sum[i][ct].w;
+        }
     }
     if (threadIdx.x == 0) a.tickets[z * a.n_grp + grp] = 0u;  // ready for the next launch
   }
@@ -531,7 +597,7 @@ linear_q_kernel(const LinArgs a) {
       bestv[ct][c] = -INFINITY;
       besti[ct][c] = 0x7fffffff;
     }
-  if (active) {
+  if (owner) {
 #pragma unroll
     for (int i = 0; i < TPW; i++) {
       const int T = tile0 + i;
@@ -616,40 +682,63 @@ linear_q_kernel(const LinArgs a) {
   if (threadIdx.x == 0) a.tickets[ZG * a.n_grp + z] = 0u;
 }
 
-// K-split for a matrix: fixed by its shape and the device only (never by
-// nt, so rows stay bitwise nt-invariant), with at most NC_MAX chunks per
-// segment.  Cost model: ceil(CTAs / resident slots) waves, each as long as
-// one segment (nch / S chunks) plus a start-up latency worth ~2 chunks; the
-// last CTA of a group reads the S partials (~1/8 chunk each).
-int choose_split(int n_grp, int nch, int slots) {
-  const int s_min = (nch + NC_MAX - 1) / NC_MAX;
-  const int s_max = std::max(s_min, std::min(MAX_SPLIT, nch / 2));
-  int best = s_min;
-  double best_cost = 1e30;
-  for (int S = s_min; S <= s_max; S++) {
-    const double waves = std::ceil((double)n_grp * S / slots);
-    const double cost = waves * ((double)nch / S + 2.0) + 0.125 * (S - 1);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = S;
+using LinKernel = void (*)(LinArgs);
+LinKernel kernel_for(int qtype, int nct, int kw) {
+#define SPEC_LIN_K(QT_, NCT_, KW_) \
+  if (qtype == QT_ && nct == NCT_ && kw == KW_) return linear_q_kernel<QT_, NCT_, KW_>;
+  SPEC_LIN_K(4, 1, 1) SPEC_LIN_K(4, 1, 2) SPEC_LIN_K(4, 1, 4) SPEC_LIN_K(4, 1, 8)
+  SPEC_LIN_K(4, 2, 1) SPEC_LIN_K(4, 2, 2) SPEC_LIN_K(4, 2, 4) SPEC_LIN_K(4, 2, 8)
+  SPEC_LIN_K(6, 1, 1) SPEC_LIN_K(6, 1, 2) SPEC_LIN_K(6, 1, 4) SPEC_LIN_K(6, 1, 8)
+  SPEC_LIN_K(6, 2, 1) SPEC_LIN_K(6, 2, 2) SPEC_LIN_K(6, 2, 4) SPEC_LIN_K(6, 2, 8)
+#undef SPEC_LIN_K
+  return nullptr;
+}
+
+struct LinCfg {
+  int kw, S;
+};
+
+// (KW, S) of a matrix: fixed by its shape and the device only (never by nt,
+// so rows stay bitwise nt-invariant).  A latency model calibrated on GB300
+// with nt <= 8: an SM retires chunks at min(SM rate, warps x warp rate) (the
+// loop is issue-bound), a launch costs a fixed start-up, a K split adds a
+// ticket and the last CTA's partial loads (eight in flight per lane), more
+// waves add a start-up each.
+LinCfg choose_config(int qtype, int n_pairs, int nch, int sms) {
+  const double sm_rate = qtype == 4 ? 22.8 : 18.7;  // chunks / us / SM
+  const double warp_rate = qtype == 4 ? 2.4 : 2.0;  // chunks / us / warp
+  const double t_start = 2.0, t_split = 2.5, t_batch = 0.5, t_slices = 0.2, t_wave = 1.0;  // us
+  sms = std::max(sms, 1);
+  const int s_min = std::max(1, (nch + NC_CTA_MAX - 1) / NC_CTA_MAX);
+  const int s_max = std::max(s_min, std::min(MAX_SPLIT, nch));
+  LinCfg best{1, s_min};
+  double best_t = 1e30;
+  for (int kw : {1, 2, 4, 8}) {
+    const int P = WARPS / kw;
+    const int n_grp = (n_pairs + P - 1) / P;
+    for (int S = s_min; S <= s_max; S++) {
+      const int nc = (nch + S - 1) / S;
+      const int wn = (nc + kw - 1) / kw;  // chunks of the busiest warp
+      int per_sm = 0;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_for(qtype, 1, kw), WARPS * 32,
+                                                    smem_bytes(qtype, 1, nc));
+      cudaGetLastError();
+      per_sm = std::max(per_sm, 1);
+      const double ctas = (double)n_grp * S;
+      const double load = std::ceil(ctas / sms);  // CTAs of the busiest SM
+      const double resident = std::min((double)per_sm, load);
+      const double rate = std::min(sm_rate, WARPS * resident * warp_rate);
+      const double waves = std::ceil(ctas / ((double)sms * per_sm));
+      double t = load * WARPS * wn / rate + t_start + (waves - 1) * t_wave;
+      if (S > 1) t += t_split + t_batch * std::ceil((S - 1) / 4.0);
+      if (kw > 1) t += t_slices;
+      if (t < best_t - 1e-6) {
+        best_t = t;
+        best = LinCfg{kw, S};
+      }
     }
   }
   return best;
-}
-
-template <int QT, int NCT>
-cudaError_t launch_typed(const LinArgs& a, int ZG, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ZG, a.n_grp, a.S);
-  cfg.blockDim = dim3(WARPS * 32);
-  cfg.dynamicSmemBytes = Smem<QT, NCT>::BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = programmatic_launch() ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, linear_q_kernel<QT, NCT>, a);
 }
 
 }  // namespace
@@ -664,7 +753,7 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaS
     return fail(SPEC_E_UNSUPPORTED, "qtype must be SPEC_Q4 or SPEC_Q6");
   if (w->N <= 0 || w->K <= 0 || w->N % 16 != 0 || w->K % 32 != 0)
     return fail(SPEC_E_SHAPE, "need N % 16 == 0 and K % 32 == 0");
-  if (w->K > 64 * NC_MAX * MAX_SPLIT) return fail(SPEC_E_SHAPE, "K above 65536 is not supported");
+  if (w->K > 64 * NC_CTA_MAX * MAX_SPLIT) return fail(SPEC_E_SHAPE, "K above 262144 is not supported");
   if (w->qs == nullptr || w->scales == nullptr || (w->qtype == SPEC_Q6 && w->qh == nullptr))
     return fail(SPEC_E_INVALID, "missing weight plane");
   if (perm == PERM_ROPE_PAIRS && (head_dim % 16 != 0 || w->N % head_dim != 0))
@@ -679,20 +768,19 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaS
   q.nch = q.Kp / 64;
   q.n_tiles = q.N / 16;
   q.n_pairs = (q.n_tiles + TPW - 1) / TPW;
-  q.n_grp = (q.n_pairs + WARPS - 1) / WARPS;
   q.rec_bytes = q.qtype == 4 ? Rec<4>::BYTES : Rec<6>::BYTES;
-  {
-    // resident CTAs per SM of the nt <= 8 variant (the split must not depend on nt)
-    int per_sm = 0;
-    if (q.qtype == 4)
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linear_q_kernel<4, 1>, WARPS * 32,
-                                                    Smem<4, 1>::BYTES);
-    else
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linear_q_kernel<6, 1>, WARPS * 32,
-                                                    Smem<6, 1>::BYTES);
-    cudaGetLastError();
-    q.S = choose_split(q.n_grp, q.nch, std::max(sms, 1) * std::max(per_sm, 1));
+  LinCfg cfg = choose_config(q.qtype, q.n_pairs, q.nch, sms);
+  if (const char* e = std::getenv("SPEC_VERIFY_LINEAR_SPLIT")) {
+    // "KW:S" overrides the choice (for tests and tuning); ignored if invalid
+    int kw = 0, S = 0;
+    if (std::sscanf(e, "%d:%d", &kw, &S) == 2 && (kw == 1 || kw == 2 || kw == 4 || kw == 8) &&
+        S >= 1 && S <= std::min(MAX_SPLIT, q.nch) && (q.nch + S - 1) / S <= NC_CTA_MAX)
+      cfg = LinCfg{kw, S};
   }
+  q.kw = cfg.kw;
+  q.S = cfg.S;
+  q.n_grp = (q.n_pairs + WARPS / q.kw - 1) / (WARPS / q.kw);
+  q.nc_cta = (q.nch + q.S - 1) / q.S;
   const size_t units = (size_t)q.n_pairs * q.nch;
   q.bytes = units * q.rec_bytes;
   if (cudaMalloc(&q.base, q.bytes) != cudaSuccess) {
@@ -753,20 +841,30 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
   a.tickets = scr.tickets;
   a.amax_part = scr.amax_part;
   a.err = scr.err;
+  a.xstride = x_stride(w.nc_cta);
   const int ZG = col_groups(R);
   const int nct = col_tiles(R);
-  cudaError_t e;
-  if (w.qtype == 4)
-    e = nct == 1 ? launch_typed<4, 1>(a, ZG, st) : launch_typed<4, 2>(a, ZG, st);
-  else
-    e = nct == 1 ? launch_typed<6, 1>(a, ZG, st) : launch_typed<6, 2>(a, ZG, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ZG, w.n_grp, w.S);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = smem_bytes(w.qtype, nct, w.nc_cta);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  const LinKernel k = kernel_for(w.qtype, nct, w.kw);
+  if (k == nullptr) return fail(SPEC_E_INVALID, "linear: no kernel for this configuration");
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("linear launch: ") + cudaGetErrorString(e));
   return SPEC_OK;
 }
 
 void linear_init_attrs() {
-  cudaFuncSetAttribute(linear_q_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<4, 1>::BYTES);
-  cudaFuncSetAttribute(linear_q_kernel<4, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<4, 2>::BYTES);
-  cudaFuncSetAttribute(linear_q_kernel<6, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<6, 1>::BYTES);
-  cudaFuncSetAttribute(linear_q_kernel<6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<6, 2>::BYTES);
+  for (int qt : {4, 6})
+    for (int nct : {1, 2})
+      for (int kw : {1, 2, 4, 8})
+        cudaFuncSetAttribute(kernel_for(qt, nct, kw), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes(qt, nct, NC_CTA_MAX));
 }

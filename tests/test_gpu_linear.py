@@ -65,6 +65,32 @@ def test_linear_full_size_sweep(orc, dev, qtype, N, K):
         assert np.array_equal(y, y16[:nt]), f"row invariance broken at nt={nt}"
 
 
+@pytest.mark.parametrize("split", ["1:1", "1:5", "2:3", "4:1", "4:17", "8:2", "8:6"])
+@pytest.mark.parametrize("qtype,N,K", [(4, 272, 1056), (6, 144, 2080)])
+def test_linear_every_split_matches_oracle(orc, dev, monkeypatch, qtype, N, K, split):
+    """Every in-CTA K slicing (KW warps per tile pair) and several K segment
+    counts S, forced through SPEC_VERIFY_LINEAR_SPLIT: an odd number of tiles
+    (a padding tile), a ragged K tail, S up to one chunk per segment, slices
+    with no chunk at all.  All outputs against the oracle, rows bitwise equal
+    across nt, and the LM-head-free store path for R > 16."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    monkeypatch.setenv("SPEC_VERIFY_LINEAR_SPLIT", split)
+    g = np.random.default_rng(hash((qtype, N, K)) % 1000)
+    w = synth.q_weight(g, qtype, N, K)
+    x = synth.f16_normal(g, (40, K))
+    qm = sv.QMat(dev_weight(w, dev), max_rows=40)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    ref = orc.linear(oracle_qweight(orc, w), x)
+    y40 = run_linear(sv, qm, xd, 40)
+    assert rel_err(y40, ref) < 1e-5
+    y16 = run_linear(sv, qm, xd, 16)
+    assert np.array_equal(y16, y40[:16])
+    for nt in (1, 7, 8, 9):
+        assert np.array_equal(run_linear(sv, qm, xd, nt), y16[:nt]), f"nt={nt}"
+    assert sv.spec_error_check(None) == 0
+
+
 def test_linear_many_rows_column_groups(orc, dev):
     """R > 16 (several column groups in one launch, as the batched 12-sequence
     round uses): rows equal the nt <= 16 results bitwise."""
