@@ -115,7 +115,7 @@ int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
 typedef struct {
   int32_t n_layers; /* 0 allowed: LM head only (spec_lm_head) */
   int32_t hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
-  int32_t max_ctx;  /* KV positions per sequence */
+  int32_t max_ctx;  /* KV positions per sequence (at most 786432) */
   int32_t max_nt;   /* rows per sequence per round, <= SPEC_MAX_NT */
   int32_t max_seqs; /* sequence slots */
   float rms_eps;    /* e.g. 1e-6 */

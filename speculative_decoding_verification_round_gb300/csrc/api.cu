@@ -292,6 +292,7 @@ static int check_desc(const spec_model_desc* D, const spec_model_weights* W) {
   if (D->n_layers < 0 || D->hidden <= 0 || D->vocab <= 0 || D->max_nt < 1 ||
       D->max_nt > SPEC_MAX_NT || D->max_seqs < 1 || D->max_ctx < 1)
     return fail(SPEC_E_SHAPE, "bad model dimensions");
+  if (D->max_ctx > 786432) return fail(SPEC_E_SHAPE, "max_ctx above 786432 is not supported");
   if (D->hidden % 64 != 0) return fail(SPEC_E_SHAPE, "hidden must be a multiple of 64");
   if (D->vocab % 16 != 0) return fail(SPEC_E_SHAPE, "vocab must be a multiple of 16");
   if (!(D->rms_eps >= 0.0f)) return fail(SPEC_E_INVALID, "rms_eps must be >= 0");

@@ -46,7 +46,7 @@ __device__ __forceinline__ uint32_t tile_off(int p, int u) {
   return (uint32_t)(p * (HD * 2) + ((u ^ (p & 7)) << 4));
 }
 
-template <int HD>
+template <int HD, int DS>
 __global__ void __launch_bounds__(WARPS * 32)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
@@ -58,41 +58,59 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   const int G = nq / nkv, M = nt * G, Mmax_stride = M;  // rows of this (seq, kv head)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
+  // the row table and the committed cache belong to kernels that completed
+  // before the one this grid depends on; the new rows' K/V, q and the
+  // partials are that kernel's (or later) business
   const RowInfo last = rows[s * nt + nt - 1];
   const int pos_last = last.pos < max_ctx ? last.pos : max_ctx - 1;
-  if (c * CH > pos_last) return;  // no row of this sequence reaches this chunk
+  if (c * CH > pos_last) {
+    grid_dep_launch();
+    return;  // no row of this sequence reaches this chunk
+  }
   const int slot = last.slot;
+  const int new0 = min(rows[s * nt].pos, max_ctx);  // positions >= new0 are this round's
 
-  // ---- stage K and V of positions [c*CH, c*CH + CH)
-  {
-    const size_t head_base = ((size_t)slot * nkv + kvh) * max_ctx;
-    constexpr int UNITS = HD / 8;  // 16-byte units per row
+  // ---- stage K and V of positions [c*CH, c*CH + CH): the committed part
+  // ---- before the grid dependency resolves, the round's new rows after it;
+  // ---- K and V in separate copy groups so that S = Q K^T can start first
+  constexpr int UNITS = HD / 8;  // 16-byte units per row
+  const size_t head_base = ((size_t)slot * nkv + kvh) * max_ctx;
+  auto stage = [&](unsigned char* tile, const __half* cache, bool committed) {
     for (int idx = threadIdx.x; idx < CH * UNITS; idx += WARPS * 32) {
       const int p = idx / UNITS, u = idx % UNITS;
       const int pg = c * CH + p;
-      const uint32_t ko = smem_u32(Ks + tile_off<HD>(p, u));
-      const uint32_t vo = smem_u32(Vs + tile_off<HD>(p, u));
+      if ((pg < new0) != committed) continue;
+      const uint32_t so = smem_u32(tile + tile_off<HD>(p, u));
       if (pg < max_ctx) {
-        const __half* kg = kcache + (head_base + pg) * HD + u * 8;
-        const __half* vg = vcache + (head_base + pg) * HD + u * 8;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ko), "l"(kg));
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vo), "l"(vg));
+        const __half* src = cache + (head_base + pg) * HD + u * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(so), "l"(src));
       } else {
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(ko), "r"(0));
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vo), "r"(0));
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(so), "r"(0));
       }
     }
     asm volatile("cp.async.commit_group;");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
-  }
+  };
+  stage(Ks, kcache, true);
+  stage(Vs, vcache, true);
+  grid_dep_wait();
+  stage(Ks, kcache, false);
+  stage(Vs, vcache, false);
+  grid_dep_launch();
+  asm volatile("cp.async.wait_group 1;" ::: "memory");  // all of K (V's last group may still fly)
+  __syncthreads();
 
   const float sc_log2 = 1.4426950408889634f / sqrtf((float)HD);
   const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs);
+  // work items: (m tile, slice of the head dimensions); the DS warps of one
+  // m tile each compute S and P in full (the same instruction sequence) and
+  // O for HD / DS of the dimensions
   const int n_mt = (M + 15) / 16;
-  for (int mt = warp; mt < n_mt; mt += WARPS) {
+  const int n_items = n_mt * DS;
+  for (int it0 = 0; it0 < n_items; it0 += WARPS) {  // uniform trip count: the V barrier below
+    const int it = it0 + warp;
+    const int mt = it / DS, dh = it % DS;
     const int mA = mt * 16 + g, mB = mA + 8;
-    const bool okA = mA < M, okB = mB < M;
+    const bool okA = it < n_items && mA < M, okB = it < n_items && mB < M;
     int posA = -1, posB = -1;
     const __half* qA = nullptr;
     const __half* qB = nullptr;
@@ -179,9 +197,15 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
     // ---- O = P V (16 rows x HD dims).  P enters the fp16 MMA as an exact
     // ---- two-term split p = hi + lo (hi = fp16(p), lo = fp16(p - hi)), so
     // ---- the product carries ~22 bits of p instead of 11.
-    float oacc[HD / 8][4];
+    if (it0 == 0) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");  // V
+      __syncthreads();
+    }
+    constexpr int DN = HD / 8 / DS;  // n8 blocks of head dimensions of this warp
+    const int dn0 = dh * DN;
+    float oacc[DN][4];
 #pragma unroll
-    for (int dn = 0; dn < HD / 8; dn++)
+    for (int dn = 0; dn < DN; dn++)
 #pragma unroll
       for (int e = 0; e < 4; e++) oacc[dn][e] = 0.0f;
 #pragma unroll
@@ -200,10 +224,10 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
         }
       }
 #pragma unroll
-      for (int dn = 0; dn < HD / 8; dn += 2) {
+      for (int dn = 0; dn < DN; dn += 2) {
         const int mi = lane >> 3;
         const int key = 16 * kk + (lane & 7) + (mi & 1) * 8;
-        const int unit = dn + (mi >> 1);
+        const int unit = dn0 + dn + (mi >> 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vs_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
         mma_16816(oacc[dn], phi, b0, b1);
@@ -215,86 +239,83 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
     // ---- partials: part[s][kvh][c][m] = (o[HD], m, l)
     const size_t base = (((size_t)s * nkv + kvh) * nchunks + c) * (size_t)Mmax_stride;
     if (okA) {
-      float* dst = part + (base + mA) * (HD + 2);
+      float* dst = part + (base + mA) * (HD + 2) + 8 * dn0;
 #pragma unroll
-      for (int dn = 0; dn < HD / 8; dn++)
+      for (int dn = 0; dn < DN; dn++)
         *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][0], oacc[dn][1]);
-      if (t == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(mxA, lA);
+      if (t == 0 && dh == 0)
+        *reinterpret_cast<float2*>(part + (base + mA) * (HD + 2) + HD) = make_float2(mxA, lA);
     }
     if (okB) {
-      float* dst = part + (base + mB) * (HD + 2);
+      float* dst = part + (base + mB) * (HD + 2) + 8 * dn0;
 #pragma unroll
-      for (int dn = 0; dn < HD / 8; dn++)
+      for (int dn = 0; dn < DN; dn++)
         *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][2], oacc[dn][3]);
-      if (t == 0) *reinterpret_cast<float2*>(dst + HD) = make_float2(mxB, lB);
+      if (t == 0 && dh == 0)
+        *reinterpret_cast<float2*>(part + (base + mB) * (HD + 2) + HD) = make_float2(mxB, lB);
     }
   }
 }
 
-// One warp per (row, q head): merge chunks 0..P/CH in increasing order.
-// The chunk maxima are loaded in parallel (one chunk per lane), the global
-// max is a butterfly; the weighted sums then run over the chunks in order
-// with the loads of four chunks in flight at a time.
+// One CTA per (row, q head), one thread per head dimension: merge chunks
+// 0..P/CH in increasing order.  The loads of the first MB chunks' o values
+// go out together with every chunk's (m, l) (staged in shared memory), so a
+// context of up to MB chunks costs one round trip; the global max is exact
+// in any order, and each thread sums w_c * o_c[d] and w_c * l_c over the
+// chunks in order, w_c = exp2(m_c - max).
+constexpr int MERGE_MB = 40;
 template <int HD>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(HD)
 attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
                   int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
                   __half* __restrict__ out) {
   grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= R * nq) return;
-  const int r = wid / nq, h = wid % nq;
+  extern __shared__ float s_ml[];  // [nchunks] m, then [nchunks] l
+  float* s_m = s_ml;
+  float* s_l = s_ml + nchunks;
+  const int r = blockIdx.x / nq, h = blockIdx.x % nq;
+  const int d = threadIdx.x;
   const int s = r / nt, i = r % nt;
   const int G = nq / nkv, kvh = h / G, gh = h % G;
   const int M = nt * G, m = i * G + gh;
   const RowInfo ri = rows[r];
   const int pos = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
   const int nc = pos / CH + 1;
-  const size_t base = ((size_t)s * nkv + kvh) * nchunks;
   const size_t stride = (size_t)M * (HD + 2);  // floats between consecutive chunks
-  const float* p0 = part + (base * M + m) * (HD + 2);
+  const float* p0 = part + ((((size_t)s * nkv + kvh) * nchunks) * M + m) * (HD + 2);
+  grid_dep_wait();  // the partials come from the chunk kernel
+  float v[MERGE_MB];
+#pragma unroll
+  for (int u = 0; u < MERGE_MB; u++) v[u] = u < nc ? __ldcg(p0 + (size_t)u * stride + d) : 0.0f;
+  for (int c = d; c < nc; c += HD) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
+    s_m[c] = ml.x;
+    s_l[c] = ml.y;
+  }
+  __syncthreads();
   float mx = -INFINITY;
-  for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldg(p0 + c * stride + HD));
+  for (int c = 0; c < nc; c++) mx = fmaxf(mx, s_m[c]);
+  float o = 0.0f, l = 0.0f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  constexpr int PER = HD / 32;
-  float o[PER];
-#pragma unroll
-  for (int e = 0; e < PER; e++) o[e] = 0.0f;
-  float l = 0.0f;
-  int c = 0;
-  for (; c + 4 <= nc; c += 4) {
-    float2 ml[4];
-    float v[4][PER];
-#pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const float* src = p0 + (c + u) * stride;
-      ml[u] = __ldg(reinterpret_cast<const float2*>(src + HD));
-#pragma unroll
-      for (int e = 0; e < PER; e++) v[u][e] = __ldg(src + lane * PER + e);
+  for (int u = 0; u < MERGE_MB; u++)
+    if (u < nc) {
+      const float w = exp2f(s_m[u] - mx);
+      l = fmaf(s_l[u], w, l);
+      o = fmaf(v[u], w, o);
     }
+  for (int c = MERGE_MB; c < nc; c += 16) {  // long contexts: sixteen loads in flight
+    float v2[16];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const float w = exp2f(ml[u].x - mx);
-      l = fmaf(ml[u].y, w, l);
+    for (int u = 0; u < 16; u++) v2[u] = c + u < nc ? __ldcg(p0 + (size_t)(c + u) * stride + d) : 0.0f;
 #pragma unroll
-      for (int e = 0; e < PER; e++) o[e] = fmaf(v[u][e], w, o[e]);
-    }
+    for (int u = 0; u < 16; u++)
+      if (c + u < nc) {
+        const float w = exp2f(s_m[c + u] - mx);
+        l = fmaf(s_l[c + u], w, l);
+        o = fmaf(v2[u], w, o);
+      }
   }
-  for (; c < nc; c++) {
-    const float* src = p0 + c * stride;
-    const float2 ml = __ldg(reinterpret_cast<const float2*>(src + HD));
-    const float w = exp2f(ml.x - mx);
-    l = fmaf(ml.y, w, l);
-#pragma unroll
-    for (int e = 0; e < PER; e++) o[e] = fmaf(__ldg(src + lane * PER + e), w, o[e]);
-  }
-  const float inv = 1.0f / l;
-  __half* dst = out + (size_t)r * nq * HD + (size_t)h * HD + lane * PER;
-#pragma unroll
-  for (int e = 0; e < PER; e += 2)
-    *reinterpret_cast<__half2*>(dst + e) = __floats2half2_rn(o[e] * inv, o[e + 1] * inv);
+  out[(size_t)r * nq * HD + (size_t)h * HD + d] = __float2half_rn(o * (1.0f / l));
 }
 
 template <int HD>
@@ -302,15 +323,34 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
                   const RowInfo* rows, int n_seq, int nt, int nq, int nkv, int max_ctx,
                   float* part, __half* out, cudaStream_t st) {
   const int nchunks = (max_ctx + CH - 1) / CH;
-  const size_t smem = 2 * (size_t)CH * HD * 2;
-  dim3 grid(nchunks, nkv, n_seq);
-  attn_chunk_kernel<HD><<<grid, WARPS * 32, smem, st>>>(q, kcache, vcache, rows, nt, nq, nkv,
-                                                        max_ctx, nchunks, part);
   const int R = n_seq * nt;
-  const int warps = R * nq;
-  attn_merge_kernel<HD><<<(warps + 3) / 4, 128, 0, st>>>(part, rows, R, nt, nq, nkv, max_ctx,
-                                                        nchunks, out);
-  cudaError_t e = cudaGetLastError();
+  // both launched as programmatic dependents of the previous kernel: the
+  // chunk kernel stages the committed cache and the merge kernel starts up
+  // while their predecessors finish
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  cfg.gridDim = dim3(nchunks, nkv, n_seq);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = 2 * (size_t)CH * HD * 2;
+  // split the head dimensions of an m tile across warps while there are
+  // fewer m tiles than warps (the bits of every output do not depend on it)
+  const int n_mt = (nt * (nq / nkv) + 15) / 16;
+  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 4>
+                         : (n_mt == 2 ? attn_chunk_kernel<HD, 2> : attn_chunk_kernel<HD, 1>);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, chunk, q, kcache, vcache, rows, nt, nq, nkv, max_ctx,
+                                     nchunks, part);
+  if (e == cudaSuccess) {
+    cfg.gridDim = dim3(R * nq);
+    cfg.blockDim = dim3(HD);
+    cfg.dynamicSmemBytes = 2 * sizeof(float) * (size_t)nchunks;
+    e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, (const float*)part, rows, R, nt, nq, nkv,
+                           max_ctx, nchunks, out);
+  }
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
   return SPEC_OK;
 }
@@ -333,8 +373,10 @@ int attn_launch(const __half* q, const __half* kcache, const __half* vcache,
 }
 
 void attn_init_attrs() {
-  cudaFuncSetAttribute(attn_chunk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       2 * CH * 128 * 2);
-  cudaFuncSetAttribute(attn_chunk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       2 * CH * 64 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 128 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 128 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 128 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 64 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 64 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 64 * 2);
 }
