@@ -10,9 +10,11 @@
 //     of the pair is one contiguous record in HBM, streamed with TMA bulk
 //     copies through a per-warp shared-memory ring; the CTA's slice of the
 //     activations is staged once in shared memory and shared by its warps;
-//   * the 4-bit / 6-bit integers become exact fp16 values with the 0x6400
-//     magic-number trick and feed mma.sync m16n8k16 (f16 x f16 -> f32) as the
-//     A operand; the activations (n8 column tiles of verify rows) are B;
+//   * the 4-bit / 6-bit integers, masked into the mantissa from bit 4 up,
+//     are exact fp16 subnormals (16u * 2^-24) and feed
+//     mma.sync m16n8k16 (f16 x f16 -> f32) as the A operand; the activations
+//     (n8 column tiles of verify rows) are B, and the zero point enters as
+//     the C operand (-bias * sum(x), from two MMAs with a constant fragment);
 //   * each 32-block is accumulated in a fresh fp32 fragment and folded into
 //     the running sum with one fp32 FMA by its fp16 scale;
 //   * K is split into S segments across CTAs and, inside a CTA, into KW
@@ -37,7 +39,8 @@ namespace {
 
 constexpr int WARPS = 8;     // warps per CTA
 constexpr int TPW = 2;       // tiles (of 16 rows) per warp: one pair
-constexpr int NS = 4;        // weight-ring stages per warp
+constexpr int NS = 2;        // weight-ring stages per warp
+constexpr int CPS = 2;       // chunks per ring stage (consecutive records: one copy, one wait)
 constexpr int NC_CTA_MAX = 64;  // chunks of one CTA's K range (its staged activation slice)
 constexpr int MAX_SPLIT = 64;
 
@@ -51,7 +54,7 @@ struct Rec {
   static constexpr int BYTES = QH + (QT == 6 ? TPW * 256 : 0);  // 1152 / 1664
 };
 template <int QT>
-constexpr int ring_bytes() { return WARPS * NS * Rec<QT>::BYTES; }
+constexpr int ring_bytes() { return WARPS * NS * CPS * Rec<QT>::BYTES; }
 // Staged activation row: the CTA's K range plus 64 bytes, so that the rows
 // g = 0..7 of a fragment load fall in distinct shared-memory banks.
 inline int x_stride(int nc) { return nc * 128 + 64; }
@@ -202,40 +205,50 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-// A fragments of one k16 step from a packed nibble word (+ Q6 high fields).
+// A fragments of one k16 step from a packed nibble word (+ Q6 high fields),
+// as fp16 subnormals: a value u masked into the mantissa is exactly
+// u * 2^-24.  Every value is placed from mantissa bit 4 up (16u * 2^-24,
+// below 1024 * 2^-24 for 6 bits): the tensor cores accumulate products of
+// the very smallest subnormals with less precision, and at this scale the
+// sums are as accurate as those of centred fp16 integers.  The zero point is
+// subtracted through the MMA's C operand (see compute_chunk) and the 2^-20
+// unit is undone once, exactly, in the epilogue.
 template <int QT>
 __device__ __forceinline__ void dequant_step(uint32_t w, uint32_t hx, uint32_t (&A)[4]) {
-  const uint32_t MAG = 0x64006400u;
-  const uint32_t w8 = w >> 8;
-  uint32_t r0 = (w & 0x000F000Fu) | MAG;
-  uint32_t r1 = (w & 0x00F000F0u) | MAG;
-  uint32_t r2 = (w8 & 0x000F000Fu) | MAG;
-  uint32_t r3 = (w8 & 0x00F000F0u) | MAG;
-  if constexpr (QT == 6) {
-    const uint32_t hx2 = hx >> 2;
-    r0 |= hx & 0x00300030u;
-    r1 |= hx & 0x03000300u;
-    r2 |= hx2 & 0x00300030u;
-    r3 |= hx2 & 0x03000300u;
+  if constexpr (QT == 4) {
+    A[0] = (w << 4) & 0x00F000F0u;  // rows g, k 2t..2t+1
+    A[1] = w & 0x00F000F0u;         // rows g+8
+    A[2] = (w >> 4) & 0x00F000F0u;  // rows g, k 2t+8..2t+9
+    A[3] = (w >> 8) & 0x00F000F0u;  // rows g+8
+  } else {
+    const uint32_t w8 = w >> 8, hx2 = hx >> 2;
+    A[0] = ((w & 0x000F000Fu) | (hx & 0x00300030u)) << 4;
+    A[1] = (w & 0x00F000F0u) | (hx & 0x03000300u);
+    A[2] = ((w8 & 0x000F000Fu) | (hx2 & 0x00300030u)) << 4;
+    A[3] = (w8 & 0x00F000F0u) | (hx2 & 0x03000300u);
   }
-  // bits-0.. form: h = 1024 + u  -> q = h - (1024 + bias)
-  // bits-4.. form: h = 1024 + 16u -> q = h/16 - (64 + bias)
-  const __half2 sub = QT == 4 ? __half2half2(__ushort_as_half(0x6408))   // 1032
-                              : __half2half2(__ushort_as_half(0x6420));  // 1056
-  const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));      // 1/16
-  const __half2 off = QT == 4 ? __half2half2(__ushort_as_half(0xD480))   // -72
-                              : __half2half2(__ushort_as_half(0xD600));  // -96
-  __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&r0), sub);
-  __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&r1), sixteenth, off);
-  __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&r2), sub);
-  __half2 h3 = __hfma2(*reinterpret_cast<__half2*>(&r3), sixteenth, off);
-  A[0] = *reinterpret_cast<uint32_t*>(&h0);
-  A[1] = *reinterpret_cast<uint32_t*>(&h1);
-  A[2] = *reinterpret_cast<uint32_t*>(&h2);
-  A[3] = *reinterpret_cast<uint32_t*>(&h3);
+}
+
+// The unit of the dequantised fragments, undone in the epilogue: 2^20.
+constexpr float FRAG_UNIT = 1048576.0f;
+
+// The zero-point fragment: -16 * bias * 2^-24 (Q4: bias 8 -> -2^-17; Q6:
+// bias 32 -> -2^-15, both exact fp16).  Its product with a block's
+// activations is -bias * sum(x) in the fragments' unit.
+template <int QT>
+__device__ __forceinline__ void zero_point_frag(uint32_t (&A)[4]) {
+  const uint32_t z = QT == 4 ? 0x80808080u : 0x82008200u;
+  A[0] = z;
+  A[1] = z;
+  A[2] = z;
+  A[3] = z;
 }
 
 // One chunk: the pair's 2 tiles x 64 k against the staged activations.
+// Per 32-block and column tile, C = -bias * sum(x) (two MMAs with the
+// zero-point fragment, shared by both tiles) starts each block's fresh
+// accumulator; the block's two k16 MMAs add sum(u * x); one FMA per element
+// folds the block scale into the running sum.
 template <int QT, int NCT>
 __device__ __forceinline__ void compute_chunk(const unsigned char* st, const unsigned char* xs,
                                               int xstride, int j, int lane,
@@ -249,6 +262,16 @@ __device__ __forceinline__ void compute_chunk(const unsigned char* st, const uns
     xb[ct][0] = *reinterpret_cast<const uint4*>(row);
     xb[ct][1] = *reinterpret_cast<const uint4*>(row + 64);
   }
+  uint32_t Z[4];
+  zero_point_frag<QT>(Z);
+  float zc[NCT][2][4];
+#pragma unroll
+  for (int ct = 0; ct < NCT; ct++)
+#pragma unroll
+    for (int b = 0; b < 2; b++) {
+      mma_16816_zero(zc[ct][b], Z, xb[ct][b].x, xb[ct][b].y);
+      mma_16816(zc[ct][b], Z, xb[ct][b].z, xb[ct][b].w);
+    }
 #pragma unroll
   for (int i = 0; i < TPW; i++) {
     const uint4 aw = *reinterpret_cast<const uint4*>(st + RC::QS + i * 512 + lane * 16);
@@ -273,7 +296,7 @@ __device__ __forceinline__ void compute_chunk(const unsigned char* st, const uns
 #pragma unroll
       for (int ct = 0; ct < NCT; ct++) {
         float blk[4];
-        mma_16816_zero(blk, A0, xb[ct][b].x, xb[ct][b].y);
+        mma_16816_c(blk, A0, xb[ct][b].x, xb[ct][b].y, zc[ct][b]);
         mma_16816(blk, A1, xb[ct][b].z, xb[ct][b].w);
         acc[i][ct][0] = fmaf(sg, blk[0], acc[i][ct][0]);
         acc[i][ct][1] = fmaf(sg, blk[1], acc[i][ct][1]);
@@ -300,7 +323,9 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
   for (int c = 0; c < 2; c++) {
     const int r = zrow0 + ct * 8 + 2 * t + c;
     if (r >= a.R) continue;
-    const float x0 = v[c], x1 = v[2 + c];  // rows g and g+8, column r
+    // rows g and g+8, column r; the sums are in the fragments' units of the
+    // dequantised values: exact power-of-two scaling
+    const float x0 = v[c] * FRAG_UNIT, x1 = v[2 + c] * FRAG_UNIT;
     switch (e.kind) {
       case EPI_STORE:
         e.y[(size_t)r * e.ldy + n0] = x0;
@@ -383,7 +408,8 @@ linear_q_kernel(const LinArgs a) {
   const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c_begin;
   const int w_lo = ks * nc / KW;
   const int wn = (ks + 1) * nc / KW - w_lo;
-  unsigned char* ring = smem + warp * NS * RC::BYTES;
+  constexpr int SB = CPS * RC::BYTES;  // bytes of a full stage
+  unsigned char* ring = smem + warp * NS * SB;
   const uint32_t ring_s = smem_addr(ring);
   unsigned char* xs = smem + ring_bytes<QT>();
   const uint32_t bar0 = smem_addr(&s_bar[warp][0]);
@@ -397,9 +423,10 @@ linear_q_kernel(const LinArgs a) {
   if (active && lane == 0) {
     for (int s = 0; s < NS; s++) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
-    for (int j = 0; j < NS - 1 && j < wn; j++) {
-      mbar_expect_tx(bar0 + 8 * j, RC::BYTES);
-      bulk_copy(ring_s + j * RC::BYTES, src + (size_t)j * RC::BYTES, RC::BYTES, bar0 + 8 * j);
+    for (int q = 0; q < NS - 1 && q * CPS < wn; q++) {
+      const uint32_t nb = (uint32_t)min(CPS, wn - q * CPS) * RC::BYTES;
+      mbar_expect_tx(bar0 + 8 * q, nb);
+      bulk_copy(ring_s + q * SB, src + (size_t)q * SB, nb, bar0 + 8 * q);
     }
   }
   // ---- the activation slice (rows zrow0.., chunks c_begin..): zero what no
@@ -438,36 +465,42 @@ linear_q_kernel(const LinArgs a) {
 
   bool ok = mbar_wait(xbar, 0);  // every warp waits for the slice (also the idle ones)
   if (active) {
-    // the loop is unrolled by the ring depth, so stage indices, parities and
-    // ring addresses are compile-time constants
-    int j = 0;
-    const uint8_t* nxt = src + (size_t)(NS - 1) * RC::BYTES;  // next record to fetch
-    for (int j0 = 0; j0 < wn && ok; j0 += NS) {
-      const uint32_t phase = (uint32_t)((j0 / NS) & 1);
+    // stages of CPS consecutive chunks; the loop is unrolled by the ring
+    // depth, so stage indices, parities and ring addresses are constants
+    const int n_st = (wn + CPS - 1) / CPS;
+    int q = 0;
+    const uint8_t* nxt = src + (size_t)(NS - 1) * SB;  // next stage to fetch
+    for (int q0 = 0; q0 < n_st && ok; q0 += NS) {
+      const uint32_t phase = (uint32_t)((q0 / NS) & 1);
 #pragma unroll
       for (int u = 0; u < NS; u++) {
-        j = j0 + u;
-        if (j >= wn) break;
+        q = q0 + u;
+        if (q >= n_st) break;
         ok = mbar_wait(bar0 + 8 * u, phase);
         if (!ok) break;
-        if (lane == 0 && j + NS - 1 < wn) {
-          // the stage before this one was consumed in iteration j - 1 (every
+        if (lane == 0 && q + NS - 1 < n_st) {
+          // the stage before this one was consumed in stage q - 1 (every
           // lane passed its closing __syncwarp), so it can be refilled
           const int sn = (u + NS - 1) % NS;
-          mbar_expect_tx(bar0 + 8 * sn, RC::BYTES);
-          bulk_copy(ring_s + sn * RC::BYTES, nxt, RC::BYTES, bar0 + 8 * sn);
+          const uint32_t nb = (uint32_t)min(CPS, wn - (q + NS - 1) * CPS) * RC::BYTES;
+          mbar_expect_tx(bar0 + 8 * sn, nb);
+          bulk_copy(ring_s + sn * SB, nxt, nb, bar0 + 8 * sn);
         }
-        nxt += RC::BYTES;
-        compute_chunk<QT, NCT>(ring + u * RC::BYTES, xs, a.xstride, w_lo + j, lane, acc);
+        nxt += SB;
+#pragma unroll
+        for (int h = 0; h < CPS; h++)
+          if (q * CPS + h < wn)
+            compute_chunk<QT, NCT>(ring + u * SB + h * RC::BYTES, xs, a.xstride,
+                                   w_lo + q * CPS + h, lane, acc);
         __syncwarp();
       }
     }
     if (!ok) {
       // a copy never arrived: flag it, then wait (bounded) for this warp's
-      // copies still in flight (records j .. j + NS - 2) before going on
+      // copies still in flight (stages q .. q + NS - 2) before going on
       if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
-      for (int jj = j; jj < wn && jj < j + NS - 1; jj++)
-        mbar_wait(bar0 + 8 * (jj % NS), (uint32_t)((jj / NS) & 1));
+      for (int qq = q; qq < n_st && qq < q + NS - 1; qq++)
+        mbar_wait(bar0 + 8 * (qq % NS), (uint32_t)((qq / NS) & 1));
     }
   } else if (!ok && threadIdx.x == 0) {
     atomicOr(a.err, ERR_TIMEOUT);
