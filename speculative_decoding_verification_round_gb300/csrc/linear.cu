@@ -40,7 +40,7 @@ namespace {
 constexpr int WARPS = 8;     // warps per CTA
 constexpr int TPW = 2;       // tiles (of 16 rows) per warp: one pair
 constexpr int NS = 2;        // weight-ring stages per warp
-constexpr int CPS = 2;       // chunks per ring stage (consecutive records: one copy, one wait)
+constexpr int CPS = 3;       // chunks per ring stage (consecutive records: one copy, one wait)
 constexpr int NC_CTA_MAX = 64;  // chunks of one CTA's K range (its staged activation slice)
 constexpr int MAX_SPLIT = 64;
 
@@ -731,46 +731,62 @@ struct LinCfg {
   int kw, S;
 };
 
+// Latency model of one launch, fitted (least squares over CTA-timeline spans
+// of 7 shapes x 5-9 splits each, GB300, rms error ~5-6%) for the nt <= 8
+// (one column tile) and nt = 9..16 (two column tiles) kernels: an SM
+// retires chunks at min(SM rate, resident warps x warp rate), a launch costs
+// a fixed start-up, a K split adds a ticket and the last CTA's partial loads,
+// KW > 1 the shared-memory slice sum, and each further wave a start-up.
+struct LinModel {
+  double sm_rate[2], warp_rate[2];  // chunks / us (Q4, Q6)
+  double t_start, t_split, t_batch, t_slices, t_wave;  // us
+};
+constexpr LinModel MODEL_NCT[2] = {
+    {{32.4, 26.0}, {3.55, 2.82}, 2.46, 1.59, 0.70, 0.56, 3.08},
+    {{23.9, 20.9}, {2.37, 2.10}, 4.71, 1.66, 0.66, 0.0, 3.28},
+};
+
+double model_time(const LinModel& M, int qtype, int nct, int kw, int S, int n_pairs, int nch,
+                  int sms) {
+  const int P = WARPS / kw;
+  const int n_grp = (n_pairs + P - 1) / P;
+  const int nc = (nch + S - 1) / S;
+  const int wn = (nc + kw - 1) / kw;  // chunks of the busiest warp
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_for(qtype, nct, kw), WARPS * 32,
+                                                smem_bytes(qtype, nct, nc));
+  cudaGetLastError();
+  per_sm = std::max(per_sm, 1);
+  const int q = qtype == 4 ? 0 : 1;
+  const double ctas = (double)n_grp * S;
+  const double load = std::ceil(ctas / sms);  // CTAs of the busiest SM
+  const double resident = std::min((double)per_sm, load);
+  const double rate = std::min(M.sm_rate[q], WARPS * resident * M.warp_rate[q]);
+  const double waves = std::ceil(ctas / ((double)sms * per_sm));
+  double t = load * WARPS * wn / rate + M.t_start + (waves - 1) * M.t_wave;
+  if (S > 1) t += M.t_split + M.t_batch * std::ceil((S - 1) / 4.0);
+  if (kw > 1) t += M.t_slices;
+  return t;
+}
+
 // (KW, S) of a matrix: fixed by its shape and the device only (never by nt,
-// so rows stay bitwise nt-invariant).  A latency model calibrated on GB300
-// with nt <= 8: an SM retires chunks at min(SM rate, warps x warp rate) (the
-// loop is issue-bound), a launch costs a fixed start-up, a K split adds a
-// ticket and the last CTA's partial loads (eight in flight per lane), more
-// waves add a start-up each.
+// so rows stay bitwise nt-invariant); the one minimising the modelled
+// latency of an nt <= 8 launch plus that of an nt = 9..16 launch.
 LinCfg choose_config(int qtype, int n_pairs, int nch, int sms) {
-  const double sm_rate = qtype == 4 ? 22.8 : 18.7;  // chunks / us / SM
-  const double warp_rate = qtype == 4 ? 2.4 : 2.0;  // chunks / us / warp
-  const double t_start = 2.0, t_split = 2.5, t_batch = 0.5, t_slices = 0.2, t_wave = 1.0;  // us
   sms = std::max(sms, 1);
   const int s_min = std::max(1, (nch + NC_CTA_MAX - 1) / NC_CTA_MAX);
   const int s_max = std::max(s_min, std::min(MAX_SPLIT, nch));
   LinCfg best{1, s_min};
   double best_t = 1e30;
-  for (int kw : {1, 2, 4, 8}) {
-    const int P = WARPS / kw;
-    const int n_grp = (n_pairs + P - 1) / P;
+  for (int kw : {1, 2, 4, 8})
     for (int S = s_min; S <= s_max; S++) {
-      const int nc = (nch + S - 1) / S;
-      const int wn = (nc + kw - 1) / kw;  // chunks of the busiest warp
-      int per_sm = 0;
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_for(qtype, 1, kw), WARPS * 32,
-                                                    smem_bytes(qtype, 1, nc));
-      cudaGetLastError();
-      per_sm = std::max(per_sm, 1);
-      const double ctas = (double)n_grp * S;
-      const double load = std::ceil(ctas / sms);  // CTAs of the busiest SM
-      const double resident = std::min((double)per_sm, load);
-      const double rate = std::min(sm_rate, WARPS * resident * warp_rate);
-      const double waves = std::ceil(ctas / ((double)sms * per_sm));
-      double t = load * WARPS * wn / rate + t_start + (waves - 1) * t_wave;
-      if (S > 1) t += t_split + t_batch * std::ceil((S - 1) / 4.0);
-      if (kw > 1) t += t_slices;
+      const double t = model_time(MODEL_NCT[0], qtype, 1, kw, S, n_pairs, nch, sms) +
+                       model_time(MODEL_NCT[1], qtype, 2, kw, S, n_pairs, nch, sms);
       if (t < best_t - 1e-6) {
         best_t = t;
         best = LinCfg{kw, S};
       }
     }
-  }
   return best;
 }
 
