@@ -678,39 +678,51 @@ linear_q_kernel(const LinArgs a) {
       }
     a.amax_part[((size_t)z * a.n_grp + grp) * 16 + col] = make_float2(v, __int_as_float(id));
   }
-  __threadfence();
+  // release / acquire as for the K split: one fence by thread 0 each side
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const unsigned prev = atomicAdd(&a.tickets[ZG * a.n_grp + z], 1u);
     s_last_am = (prev == (unsigned)(a.n_grp - 1));
+    if (s_last_am) __threadfence();
   }
   __syncthreads();
   if (!s_last_am) return;
-  __threadfence();
-  if (warp == 0) {
-    for (int col = 0; col < 8 * NCT; col++) {
-      float v = -INFINITY;
-      int id = 0x7fffffff;
-      for (int gi = lane; gi < a.n_grp; gi += 32) {
-        const float2 p = __ldcg(a.amax_part + ((size_t)z * a.n_grp + gi) * 16 + col);
-        const int pi = __float_as_int(p.y);
-        if (amax_better(p.x, pi, v, id)) {
-          v = p.x;
+  // the grid's argmax of each column: one warp per column, eight group
+  // partials in flight per lane (the result is the unique (max, lowest
+  // index) pair, whatever the order)
+  for (int col = warp; col < 8 * NCT; col += WARPS) {
+    float v = -INFINITY;
+    int id = 0x7fffffff;
+    const float2* base = a.amax_part + (size_t)z * a.n_grp * 16 + col;
+    for (int g0 = 0; g0 < a.n_grp; g0 += 32 * 8) {
+      float2 p[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int gi = g0 + u * 32 + lane;
+        p[u] = gi < a.n_grp ? __ldcg(base + (size_t)gi * 16)
+                            : make_float2(-INFINITY, __int_as_float(0x7fffffff));
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int pi = __float_as_int(p[u].y);
+        if (amax_better(p[u].x, pi, v, id)) {
+          v = p[u].x;
           id = pi;
         }
       }
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, id, off);
-        if (amax_better(ov, oi, v, id)) {
-          v = ov;
-          id = oi;
-        }
-      }
-      const int r = zrow0 + col;
-      if (lane == 0 && r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = id == 0x7fffffff ? 0 : id;
     }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, id, off);
+      if (amax_better(ov, oi, v, id)) {
+        v = ov;
+        id = oi;
+      }
+    }
+    const int r = zrow0 + col;
+    if (lane == 0 && r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = id == 0x7fffffff ? 0 : id;
   }
   if (threadIdx.x == 0) a.tickets[ZG * a.n_grp + z] = 0u;
 }
