@@ -73,17 +73,23 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   // ---- stage K and V of positions [c*CH, c*CH + CH): the committed part
   // ---- before the grid dependency resolves, the round's new rows after it;
   // ---- K and V in separate copy groups so that S = Q K^T can start first
-  constexpr int UNITS = HD / 8;  // 16-byte units per row
+  constexpr int UNITS = HD / 8;              // 16-byte units per row
+  constexpr int RP = WARPS * 32 / UNITS;      // rows per pass of the CTA
+  const int u = threadIdx.x % UNITS, p0 = threadIdx.x / UNITS;
   const size_t head_base = ((size_t)slot * nkv + kvh) * max_ctx;
+  // a thread copies unit u of the rows p0, p0 + RP, ...: its swizzled column
+  // (u ^ (p & 7)) is the same for all of them (RP is a multiple of 8)
   auto stage = [&](unsigned char* tile, const __half* cache, bool committed) {
-    for (int idx = threadIdx.x; idx < CH * UNITS; idx += WARPS * 32) {
-      const int p = idx / UNITS, u = idx % UNITS;
-      const int pg = c * CH + p;
+    const uint32_t s0 = smem_u32(tile) + tile_off<HD>(p0, u);
+    const __half* g0 = cache + (head_base + (size_t)c * CH + p0) * HD + u * 8;
+#pragma unroll 4
+    for (int i = 0; i < CH / RP; i++) {
+      const int pg = c * CH + p0 + RP * i;
       if ((pg < new0) != committed) continue;
-      const uint32_t so = smem_u32(tile + tile_off<HD>(p, u));
+      const uint32_t so = s0 + (uint32_t)(i * RP * HD * 2);
       if (pg < max_ctx) {
-        const __half* src = cache + (head_base + pg) * HD + u * 8;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(so), "l"(src));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(so),
+                     "l"(g0 + (size_t)i * RP * HD));
       } else {
         asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(so), "r"(0));
       }
@@ -96,8 +102,6 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   stage(Ks, kcache, false);
   stage(Vs, vcache, false);
   grid_dep_launch();
-  asm volatile("cp.async.wait_group 1;" ::: "memory");  // all of K (V's last group may still fly)
-  __syncthreads();
 
   const float sc_log2 = 1.4426950408889634f / sqrtf((float)HD);
   const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs);
@@ -126,6 +130,21 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
       posB = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
       qB = q + ((size_t)(s * nt + i) * nq + kvh * G + gh) * HD;
     }
+    // ---- the q fragments of all k16 steps in one batch of loads (they
+    // ---- overlap the K copies of the first item)
+    uint32_t qa[HD / 16][4];
+#pragma unroll
+    for (int k = 0; k < HD / 16; k++) {
+      const int d0 = 16 * k + 2 * t;
+      qa[k][0] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0) : 0u;
+      qa[k][1] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0) : 0u;
+      qa[k][2] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0 + 8) : 0u;
+      qa[k][3] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0 + 8) : 0u;
+    }
+    if (it0 == 0) {
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // all of K (V's last group may fly)
+      __syncthreads();
+    }
     // ---- S = Q K^T over the chunk (16 rows x CH keys)
     float sacc[CH / 8][4];
 #pragma unroll
@@ -134,24 +153,14 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
       for (int e = 0; e < 4; e++) sacc[nb][e] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < HD / 16; kk += 2) {
-      uint32_t a0[4], a1[4];
-#pragma unroll
-      for (int h = 0; h < 2; h++) {
-        uint32_t* a = h == 0 ? a0 : a1;
-        const int d0 = 16 * (kk + h) + 2 * t;
-        a[0] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0) : 0u;
-        a[1] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0) : 0u;
-        a[2] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0 + 8) : 0u;
-        a[3] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0 + 8) : 0u;
-      }
 #pragma unroll
       for (int nb = 0; nb < CH / 8; nb++) {
         const int key = 8 * nb + (lane & 7);
         const int unit = 2 * kk + (lane >> 3);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(ks_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
-        mma_16816(sacc[nb], a0, b0, b1);
-        mma_16816(sacc[nb], a1, b2, b3);
+        mma_16816(sacc[nb], qa[kk], b0, b1);
+        mma_16816(sacc[nb], qa[kk + 1], b2, b3);
       }
     }
     // ---- mask, row max (fixed butterfly over the 4 lanes of a row)
@@ -258,11 +267,11 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
 }
 
 // One CTA per (row, q head), one thread per head dimension: merge chunks
-// 0..P/CH in increasing order.  The loads of the first MB chunks' o values
-// go out together with every chunk's (m, l) (staged in shared memory), so a
-// context of up to MB chunks costs one round trip; the global max is exact
-// in any order, and each thread sums w_c * o_c[d] and w_c * l_c over the
-// chunks in order, w_c = exp2(m_c - max).
+// 0..P/CH in increasing order.  The o loads of the first MB chunks go out
+// together with every chunk's (m, l), so a context of up to MB chunks costs
+// one round trip; the global max (exact in any order) is a block reduction,
+// the thread owning chunk c stores w_c = exp2(m_c - max) in shared memory,
+// and each thread sums w_c * o_c[d] and w_c * l_c over the chunks in order.
 constexpr int MERGE_MB = 40;
 template <int HD>
 __global__ void __launch_bounds__(HD)
@@ -270,11 +279,12 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
                   int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
                   __half* __restrict__ out) {
   grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
-  extern __shared__ float s_ml[];  // [nchunks] m, then [nchunks] l
-  float* s_m = s_ml;
+  extern __shared__ float s_ml[];  // [nchunks] w, then [nchunks] l
+  float* s_w = s_ml;
   float* s_l = s_ml + nchunks;
+  __shared__ float s_red[HD / 32];
   const int r = blockIdx.x / nq, h = blockIdx.x % nq;
-  const int d = threadIdx.x;
+  const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const int s = r / nt, i = r % nt;
   const int G = nq / nkv, kvh = h / G, gh = h % G;
   const int M = nt * G, m = i * G + gh;
@@ -287,19 +297,27 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
   float v[MERGE_MB];
 #pragma unroll
   for (int u = 0; u < MERGE_MB; u++) v[u] = u < nc ? __ldcg(p0 + (size_t)u * stride + d) : 0.0f;
+  float mx = -INFINITY;
   for (int c = d; c < nc; c += HD) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
-    s_m[c] = ml.x;
+    s_w[c] = ml.x;  // m for now
     s_l[c] = ml.y;
+    mx = fmaxf(mx, ml.x);
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_red[warp] = mx;
   __syncthreads();
-  float mx = -INFINITY;
-  for (int c = 0; c < nc; c++) mx = fmaxf(mx, s_m[c]);
+  mx = s_red[0];
+#pragma unroll
+  for (int w = 1; w < HD / 32; w++) mx = fmaxf(mx, s_red[w]);
+  for (int c = d; c < nc; c += HD) s_w[c] = exp2f(s_w[c] - mx);
+  __syncthreads();
   float o = 0.0f, l = 0.0f;
 #pragma unroll
   for (int u = 0; u < MERGE_MB; u++)
     if (u < nc) {
-      const float w = exp2f(s_m[u] - mx);
+      const float w = s_w[u];
       l = fmaf(s_l[u], w, l);
       o = fmaf(v[u], w, o);
     }
@@ -310,7 +328,7 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
 #pragma unroll
     for (int u = 0; u < 16; u++)
       if (c + u < nc) {
-        const float w = exp2f(s_m[c + u] - mx);
+        const float w = s_w[c + u];
         l = fmaf(s_l[c + u], w, l);
         o = fmaf(v2[u], w, o);
       }
