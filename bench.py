@@ -98,6 +98,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.start_line = 0
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
@@ -106,11 +107,23 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
+            # the first sample takes a while: start timing only once it is there
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and self.proc.poll() is None and self._lines() == 0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        self.start_line = self._lines()
         return self
+
+    def _lines(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -124,11 +137,13 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        rows = []
-        for line in open(self.path):
+        rows, before = [], []
+        for n, line in enumerate(open(self.path)):
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
-                rows.append(parts)
+                (rows if n >= self.start_line else before).append(parts)
+        if not rows and before:
+            rows = before[-1:]  # the timed region was shorter than the sampling interval
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -204,6 +219,32 @@ class L2Flush:
         self.buf.amax()
 
 
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "linear_q_traffic_decoder8_nt8.json")
+LINEAR_SRC = os.path.join(ROOT, "speculative_decoding_verification_round_gb300", "csrc", "linear.cu")
+
+
+def measured_traffic(shapes):
+    """DRAM bytes per verify-GEMM launch over one round's launch mix, from the
+    committed ncu record of these shapes -- or None when the record is
+    missing, lacks a shape, or was taken on a different linear.cu."""
+    import hashlib
+    try:
+        rec = json.load(open(TRAFFIC_RECORD))
+        sha = hashlib.sha256(open(LINEAR_SRC, "rb").read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if rec.get("linear_cu_sha256") != sha:
+        return None
+    total, n = 0.0, 0
+    for qt, N, K, count in shapes:
+        b = rec.get("dram_bytes_per_launch", {}).get(f"{qt}:{N}:{K}")
+        if b is None:
+            return None
+        total += b * count
+        n += count
+    return total / n
+
+
 def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
     """The verify GEMM at the decoder's shapes, nt = 8, timed alone with CUDA
     events on its stream; L2 flushed between launches.  Returns the achieved
@@ -242,7 +283,7 @@ def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
         qm.close()
         del w
     gbs = total_bytes / total_s / 1e9
-    return gbs, per, total_bytes / (4 * wl["n_layers"] + 1)
+    return gbs, per, total_bytes / (4 * wl["n_layers"] + 1), measured_traffic(shapes)
 
 
 def nt_sweep(sv, synth, dev, reps=20):
@@ -359,7 +400,7 @@ def run_ours(args):
 
     line = None
     if rank == 0:
-        gbs, per, bytes_per_launch = time_dominant_kernel(sv, synth, wl, dev, hbm_peak)
+        gbs, per, bytes_per_launch, traffic = time_dominant_kernel(sv, synth, wl, dev, hbm_peak)
         sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
         n_layers = wl["n_layers"]
         launches_per_round = 2 + 8 * n_layers + 2 + 2
@@ -393,7 +434,7 @@ def run_ours(args):
                             "gbs": round((weight_bytes + kv_bytes) / round_s / 1e9, 1),
                             "frac_of_hbm": round((weight_bytes + kv_bytes) / round_s / 1e9 / hbm_peak, 4)},
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None if traffic is None else round(traffic),
                          "kernel": "linear_q_kernel (verify GEMM), nt=8, one round's launch mix",
                          "algorithmic_bytes_per_launch": round(bytes_per_launch),
                          "peak_kind": peak_kind, "per_shape": per},

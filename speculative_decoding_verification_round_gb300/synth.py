@@ -22,6 +22,7 @@ Workloads (value distributions of the pages' configurations):
                        nt in {1,2,3,4,8,9,16}.
   * WL_DECODER8        8 layers, H=4096, 32/8 heads, hd 128, FFN 14336,
                        Q6 LM head V=151936, 4096 cached positions, nt=8.
+                       Q4 linears at the sweep's scale, LM head at LM_SCALE.
   * WL_DECODER14B      40 layers, H=5120, 40/8 heads, FFN 13824, Q6 LM head
                        V=248320, 12 sequences x 512 cached positions, nt=16,
                        T=0.7.
@@ -32,6 +33,10 @@ import numpy as np
 
 Q4_SCALE = 0.01   # fp16(|N(0,1)| * 0.01)
 Q6_SCALE = 0.005  # fp16(|N(0,1)| * 0.005)
+# The decoder workloads' Q6 LM head: fp16(|N(0,1)| * 0.0015), which gives
+# logits with a standard deviation of about 3 (at the sweep's 0.005 it is
+# 9-12, far peakier than a language model's)
+LM_SCALE = 0.0015
 
 WL_LMHEAD_GREEDY = dict(name="lmhead_greedy_H1024_V32000_nt3", hidden=1024,
                         vocab=32000, d=2, p_agree=0.74, seed=0)
@@ -44,11 +49,12 @@ WL_LINEAR_SWEEP = dict(name="linear_sweep_q4_5120x13824_q6_13824x5120",
 WL_DECODER8 = dict(name="decoder8_H4096_V151936_ctx4096_nt8", n_layers=8,
                    hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                    ffn=14336, vocab=151936, ctx=4096, n_seq=1, d=7,
-                   p_agree=0.74, lm_qtype=6, seed=0)
+                   p_agree=0.74, lm_qtype=6, lm_scale=LM_SCALE, seed=0)
 WL_DECODER14B = dict(name="decoder14b_40L_H5120_V248320_12seq_ctx512_nt16",
                      n_layers=40, hidden=5120, n_q_heads=40, n_kv_heads=8,
                      head_dim=128, ffn=13824, vocab=248320, ctx=512, n_seq=12,
-                     d=15, temperature=0.7, q_noise=0.5, lm_qtype=6, seed=0)
+                     d=15, temperature=0.7, q_noise=0.5, lm_qtype=6, lm_scale=LM_SCALE,
+                     seed=0)
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -168,7 +174,7 @@ def decoder_weights_torch(wl: dict, device, seed=None):
         W["wo"].append(q_weight_torch(gen, 4, H, nq * hd, device))
         W["wgu"].append(q_weight_torch(gen, 4, 2 * F, H, device))
         W["wd"].append(q_weight_torch(gen, 4, H, F, device))
-    W["lm_head"] = q_weight_torch(gen, wl.get("lm_qtype", 6), V, H, device)
+    W["lm_head"] = q_weight_torch(gen, wl.get("lm_qtype", 6), V, H, device, mult=wl.get("lm_scale"))
     W["embed"] = f16_normal_torch(gen, (V, H), device)
     g = torch.randn((2 * L + 1, H), generator=gen, device=device)
     W["norm_w"] = (1.0 + 0.1 * g).to(torch.float32)
