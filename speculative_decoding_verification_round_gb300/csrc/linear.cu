@@ -32,6 +32,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <string>
 
 #include "common.cuh"
 
@@ -832,11 +833,31 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaS
   q.rec_bytes = q.qtype == 4 ? Rec<4>::BYTES : Rec<6>::BYTES;
   LinCfg cfg = choose_config(q.qtype, q.n_pairs, q.nch, sms);
   if (const char* e = std::getenv("SPEC_VERIFY_LINEAR_SPLIT")) {
-    // "KW:S" overrides the choice (for tests and tuning); ignored if invalid
-    int kw = 0, S = 0;
-    if (std::sscanf(e, "%d:%d", &kw, &S) == 2 && (kw == 1 || kw == 2 || kw == 4 || kw == 8) &&
-        S >= 1 && S <= std::min(MAX_SPLIT, q.nch) && (q.nch + S - 1) / S <= NC_CTA_MAX)
-      cfg = LinCfg{kw, S};
+    // Overrides the choice (for tests and tuning): comma-separated entries,
+    // "KW:S" for every matrix or "N:K:KW:S" for the N x K ones (the last
+    // matching entry wins); invalid entries are ignored.
+    std::string list(e);
+    size_t at = 0;
+    while (at <= list.size()) {
+      const size_t end = std::min(list.find(',', at), list.size());
+      const std::string item = list.substr(at, end - at);
+      at = end + 1;
+      int v[4] = {0, 0, 0, 0};
+      const int n = std::sscanf(item.c_str(), "%d:%d:%d:%d", &v[0], &v[1], &v[2], &v[3]);
+      int kw = 0, S = 0;
+      if (n == 2) {
+        kw = v[0];
+        S = v[1];
+      } else if (n == 4 && v[0] == q.N && v[1] == q.K) {
+        kw = v[2];
+        S = v[3];
+      } else {
+        continue;
+      }
+      if ((kw == 1 || kw == 2 || kw == 4 || kw == 8) && S >= 1 &&
+          S <= std::min(MAX_SPLIT, q.nch) && (q.nch + S - 1) / S <= NC_CTA_MAX)
+        cfg = LinCfg{kw, S};
+    }
   }
   q.kw = cfg.kw;
   q.S = cfg.S;
