@@ -312,10 +312,53 @@ __device__ __forceinline__ bool amax_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// Global values an epilogue reads, gathered for all of a lane's fragments in
+// one batch of loads before any is used (a read-modify-write per element
+// would wait a full round trip each).
+struct EpiIn {
+  float old[4];    // RESID: the rows' current values (rows g, g+8 x 2 columns)
+  RowInfo ri[2];   // QKV: the 2 columns' (slot, position)
+  float2 cs[2];    // QKV: RoPE (cos, sin) of the tile's pair at each column's position
+};
+
+template <int NCT>
+__device__ __forceinline__ void epilogue_gather(const LinArgs& a, int T, int ct, int zrow0,
+                                                int lane, EpiIn& in) {
+  const int g = lane >> 2, t = lane & 3;
+  const LinEpi& e = a.epi;
+  const int n0 = T * 16 + g, n1 = n0 + 8;
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+    const int r = zrow0 + ct * 8 + 2 * t + c;
+    if (r >= a.R) continue;
+    if (e.kind == EPI_RESID) {
+      in.old[c] = e.y[(size_t)r * e.ldy + n0];
+      in.old[2 + c] = e.y[(size_t)r * e.ldy + n1];
+    } else if (e.kind == EPI_QKV) {
+      in.ri[c] = e.rows[r];
+    }
+  }
+}
+
+template <int NCT>
+__device__ __forceinline__ void epilogue_gather_rope(const LinArgs& a, int T, int lane, EpiIn& in) {
+  const LinEpi& e = a.epi;
+  const int g = lane >> 2;
+  const int per_head = e.hd / 16;
+  const int hh = T / per_head, j = T % per_head;
+  if (e.rope == nullptr || hh >= e.nq + e.nkv) return;
+  const int i0 = 8 * j + g;
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+    const int rp = in.ri[c].pos < e.max_ctx ? in.ri[c].pos : e.max_ctx - 1;  // invalid rows are flagged
+    in.cs[c] = e.rope[(size_t)max(rp, 0) * (e.hd / 2) + i0];
+  }
+}
+
 // Epilogue for one tile/column-tile fragment of finished sums.
 template <int NCT>
 __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, int zrow0,
-                                              int lane, const float (&v)[4],
+                                              int lane, const float (&v)[4], const EpiIn& in,
                                               float (&bestv)[NCT][2], int (&besti)[NCT][2]) {
   const int g = lane >> 2, t = lane & 3;
   const LinEpi& e = a.epi;
@@ -333,8 +376,8 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
         e.y[(size_t)r * e.ldy + n1] = x1;
         break;
       case EPI_RESID:
-        e.y[(size_t)r * e.ldy + n0] += x0;
-        e.y[(size_t)r * e.ldy + n1] += x1;
+        e.y[(size_t)r * e.ldy + n0] = in.old[c] + x0;
+        e.y[(size_t)r * e.ldy + n1] = in.old[2 + c] + x1;
         break;
       case EPI_SWIGLU: {
         const float sil = x0 / (1.0f + expf(-x0));
@@ -345,11 +388,10 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
         const int per_head = e.hd / 16;
         const int hh = T / per_head, j = T % per_head;
         const int i0 = 8 * j + g, i1 = e.hd / 2 + 8 * j + g;
-        const RowInfo ri = e.rows[r];
+        const RowInfo ri = in.ri[c];
         float y0 = x0, y1 = x1;
         if (e.rope != nullptr && hh < e.nq + e.nkv) {
-          const int rp = ri.pos < e.max_ctx ? ri.pos : e.max_ctx - 1;  // invalid rows are flagged
-          const float2 cs = e.rope[(size_t)rp * (e.hd / 2) + i0];
+          const float2 cs = in.cs[c];
           y0 = fmaf(x0, cs.x, -x1 * cs.y);
           y1 = fmaf(x1, cs.x, x0 * cs.y);
         }
@@ -632,13 +674,28 @@ linear_q_kernel(const LinArgs a) {
       besti[ct][c] = 0x7fffffff;
     }
   if (owner) {
+    EpiIn in[TPW][NCT];
+    if (a.epi.kind == EPI_RESID || a.epi.kind == EPI_QKV) {
+#pragma unroll
+      for (int i = 0; i < TPW; i++)
+#pragma unroll
+        for (int ct = 0; ct < NCT; ct++)
+          if (tile0 + i < a.n_tiles) epilogue_gather<NCT>(a, tile0 + i, ct, zrow0, lane, in[i][ct]);
+      if (a.epi.kind == EPI_QKV) {
+#pragma unroll
+        for (int i = 0; i < TPW; i++)
+#pragma unroll
+          for (int ct = 0; ct < NCT; ct++)
+            if (tile0 + i < a.n_tiles) epilogue_gather_rope<NCT>(a, tile0 + i, lane, in[i][ct]);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < TPW; i++) {
       const int T = tile0 + i;
       if (T >= a.n_tiles) continue;
 #pragma unroll
       for (int ct = 0; ct < NCT; ct++)
-        epilogue_frag<NCT>(a, T, ct, zrow0, lane, acc[i][ct], bestv, besti);
+        epilogue_frag<NCT>(a, T, ct, zrow0, lane, acc[i][ct], in[i][ct], bestv, besti);
     }
   }
   if (a.epi.kind != EPI_LMHEAD) return;
