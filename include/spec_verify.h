@@ -185,7 +185,10 @@ int spec_state_get(spec_model* m, int n, const int32_t* seq_ids, int32_t* n_past
 int spec_error_check(spec_model* m, void* stream, uint32_t* bits);
 
 /* 1 (default): spec_verify_round replays one captured CUDA graph per
- * (n_seq, d, mode) shape; 0: launches kernels one by one. */
+ * (n_seq, d, mode) shape -- for a greedy round the whole round, target pass,
+ * accept and commit; the caller's arrays are kernel arguments of the graph,
+ * updated in place when they change from one call to the next.  0: launches
+ * kernels one by one. */
 int spec_model_set_graphs(spec_model* m, int enable);
 
 /* Causal GQA attention of nt query rows per sequence over the KV cache of
@@ -284,7 +287,9 @@ typedef struct {
  *   q_logits fp32 [n_seq][d][vocab] (draft distributions; NULL iff greedy);
  *   sampling: HOST pointer;  n_acc int32 [n_seq]; emitted int32 [n_seq][d+1];
  *   logits_out fp32 [n_seq*(d+1)][vocab] or NULL.
- * 1 <= n_seq <= max_seqs, 0 <= d < max_nt. */
+ * 1 <= n_seq <= max_seqs, 0 <= d < max_nt.  All arrays are device memory,
+ * read and written in place on `stream`; n_acc and emitted must overlap
+ * neither each other nor seq_ids / draft (SPEC_E_INVALID otherwise). */
 int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_ids,
                       const int32_t* draft, int d, const float* q_logits,
                       const spec_sampling* sampling, int32_t* n_acc,

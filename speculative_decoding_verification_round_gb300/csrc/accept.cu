@@ -399,6 +399,36 @@ __global__ void commit_kernel(const int32_t* __restrict__ seq_ids, int n_seq, in
   anchor[slot] = e[a];
 }
 
+// Greedy accept and commit in one pass, for the verify round: one thread per
+// sequence takes the greedy decision above, then the commit below on the
+// same values, so the round ends with a single launch after the LM head.  A
+// programmatic dependent of the LM head: it waits for that grid's memory.
+__global__ void accept_commit_greedy_kernel(const GreedyRoundArgs a) {
+  grid_dep_wait();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= a.n_seq) return;
+  const int d = a.d;
+  const int32_t* am = a.argmax + (size_t)s * (d + 1);
+  const int32_t* dr = a.draft + (size_t)s * d;
+  int32_t* e = a.emitted + (size_t)s * (d + 1);
+  int n = 0;
+  while (n < d && am[n] == dr[n]) n++;
+  const int slot = a.seq_ids[s];
+  const int last = am[n];
+  if (*a.err != 0u || slot < 0 || slot >= a.n_slots || last < 0) {
+    a.n_acc[s] = -1;
+    for (int i = 0; i <= d; i++) e[i] = -1;
+    return;
+  }
+  for (int i = 0; i < n; i++) e[i] = dr[i];
+  e[n] = last;
+  for (int i = n + 1; i <= d; i++) e[i] = -1;
+  a.n_acc[s] = n;
+  a.n_past[slot] += n + 1;
+  a.emit_idx[slot] += (uint64_t)(n + 1);
+  a.anchor[slot] = last;
+}
+
 }  // namespace
 
 size_t stoch_rows_needed(int n_seq, int d) { return (size_t)n_seq * (2 * d + 1); }
@@ -450,6 +480,38 @@ void launch_commit(const int32_t* seq_ids, int n_seq, int d, int n_slots, const 
                    int32_t* anchor, const uint32_t* err, cudaStream_t st) {
   commit_kernel<<<(n_seq + 127) / 128, 128, 0, st>>>(seq_ids, n_seq, d, n_slots, n_acc_in, n_acc,
                                                      emitted, n_past, emit_idx, anchor, err);
+}
+
+void launch_accept_commit_greedy(const GreedyRoundArgs& a, cudaStream_t st) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  cfg.gridDim = dim3((a.n_seq + 127) / 128);
+  cfg.blockDim = dim3(128);
+  cudaLaunchKernelEx(&cfg, accept_commit_greedy_kernel, a);
+}
+
+cudaError_t accept_commit_node_retarget(cudaGraphExec_t ex, cudaGraphNode_t node,
+                                        const int32_t* draft, const int32_t* seq_ids,
+                                        int32_t* n_acc, int32_t* emitted) {
+  cudaKernelNodeParams p;
+  cudaError_t e = cudaGraphKernelNodeGetParams(node, &p);
+  if (e != cudaSuccess) return e;
+  if (p.func != reinterpret_cast<void*>(accept_commit_greedy_kernel) || p.kernelParams == nullptr)
+    return cudaErrorInvalidValue;
+  GreedyRoundArgs a = *static_cast<const GreedyRoundArgs*>(p.kernelParams[0]);
+  a.draft = draft;
+  a.seq_ids = seq_ids;
+  a.n_acc = n_acc;
+  a.emitted = emitted;
+  void* args[] = {&a};
+  p.kernelParams = args;
+  p.extra = nullptr;
+  return cudaGraphExecKernelNodeSetParams(ex, node, &p);
 }
 
 void stoch_finalize(int n_seq, int d, int32_t* n_acc, int32_t* emitted, uint64_t* emit_idx,

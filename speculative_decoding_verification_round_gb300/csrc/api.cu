@@ -222,6 +222,27 @@ extern "C" int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, floa
 // ---------------------------------------------------------------------------
 // model
 // ---------------------------------------------------------------------------
+// One instantiated verify graph.  The graph is kept beside its executable
+// because the node handles belong to it; the caller's arrays are kernel
+// arguments of the embedding node (draft, sequence ids) and, in a greedy
+// round graph, of the accept + commit node, retargeted when they change.
+struct RoundGraph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t embed = nullptr;
+  cudaGraphNode_t tail = nullptr;
+  const int32_t* draft = nullptr;
+  const int32_t* seq_ids = nullptr;
+  int32_t* n_acc = nullptr;
+  int32_t* emitted = nullptr;
+};
+
+static void round_graph_free(RoundGraph* g) {
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  *g = RoundGraph{};
+}
+
 struct spec_model {
   spec_model_desc d{};
   int device = 0, sms = 1;
@@ -248,7 +269,6 @@ struct spec_model {
   RowInfo* rows = nullptr;
   int32_t* tokens = nullptr;
   int32_t* seq_ids_buf = nullptr;
-  int32_t* draft_buf = nullptr;
   int32_t* nacc_tmp = nullptr;
   float* attn_part = nullptr;
   LinScratch lscr;
@@ -256,7 +276,7 @@ struct spec_model {
   std::vector<void*> allocs;
   bool use_graphs = true;
   cudaStream_t cap_stream = nullptr;
-  std::map<long long, cudaGraphExec_t> graphs;
+  std::map<long long, RoundGraph> graphs;
   size_t weight_bytes = 0;
 };
 
@@ -276,7 +296,7 @@ static int dalloc_t(spec_model* m, T** p, size_t count) {
 
 static void model_free(spec_model* m) {
   cudaDeviceSynchronize();
-  for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second);
+  for (auto& kv : m->graphs) round_graph_free(&kv.second);
   m->graphs.clear();
   for (auto* v : {&m->wqkv, &m->wo, &m->wgu, &m->wd})
     for (auto& q : *v) qmat_free(&q);
@@ -400,7 +420,6 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
   TRY(dalloc_t(m, &m->rows, R));
   TRY(dalloc_t(m, &m->tokens, R));
   TRY(dalloc_t(m, &m->seq_ids_buf, D.max_seqs));
-  TRY(dalloc_t(m, &m->draft_buf, (size_t)D.max_seqs * D.max_nt));
   TRY(dalloc_t(m, &m->nacc_tmp, D.max_seqs));
   // scratch
   std::vector<const QMat*> mats{&m->lm};
@@ -567,12 +586,37 @@ extern "C" int spec_error_check(spec_model* m, void* stream, uint32_t* bits) {
 // ---------------------------------------------------------------------------
 // the target pass
 // ---------------------------------------------------------------------------
-static int enqueue_forward(spec_model* m, int n_seq, int nt, bool write_logits, cudaStream_t st) {
+// The node that the last launch on a capturing stream created.
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
+static int last_captured_node(cudaStream_t st, cudaGraphNode_t* node) {
+  cudaStreamCaptureStatus cs;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t n = 0;
+  CUDA_TRY(cudaStreamGetCaptureInfo(st, &cs, nullptr, nullptr, &deps, nullptr, &n));
+  if (cs != cudaStreamCaptureStatusActive || n != 1)
+    return fail(SPEC_E_CUDA, "graph capture: no single last node");
+  *node = deps[0];
+  return SPEC_OK;
+}
+
+// The target pass over rows [anchor, draft[s][0..nt-2]] of each sequence;
+// embed_node (capture only) receives the embedding node.
+static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draft,
+                           const int32_t* seq_ids, bool write_logits, cudaStream_t st,
+                           cudaGraphNode_t* embed_node) {
   const spec_model_desc& D = m->d;
   const int R = n_seq * nt, H = D.hidden, F = D.ffn, hd = D.head_dim, nq = D.n_q_heads,
             nkv = D.n_kv_heads, V = D.vocab;
-  launch_embed_rows(m->embed, V, H, m->anchor, m->draft_buf, m->seq_ids_buf, n_seq, nt,
-                    m->n_past, D.max_seqs, D.max_ctx, m->rows, m->tokens, m->h, m->err, st);
+  launch_embed_rows(m->embed, V, H, m->anchor, draft, seq_ids, n_seq, nt, m->n_past, D.max_seqs,
+                    D.max_ctx, m->rows, m->tokens, m->h, m->err, st);
+  if (embed_node != nullptr) {
+    const int rc = last_captured_node(st, embed_node);
+    if (rc != SPEC_OK) return rc;
+  }
   for (int l = 0; l < D.n_layers; l++) {
     __half* kc = m->kc + m->layer_elems * l;
     __half* vc = m->vc + m->layer_elems * l;
@@ -619,27 +663,81 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, bool write_logits, 
   return linear_launch(m->lm, m->xa, R, el, m->lscr, st);
 }
 
-static int run_forward(spec_model* m, int n_seq, int nt, bool write_logits, cudaStream_t st) {
-  if (!m->use_graphs) return enqueue_forward(m, n_seq, nt, write_logits, st);
-  const long long key = ((long long)n_seq << 20) | ((long long)nt << 1) | (write_logits ? 1 : 0);
+// The target pass and, for a greedy round (greedy_tail), the fused accept +
+// commit; replayed from a captured graph per (n_seq, d, logits, tail) when
+// graphs are on.
+static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, const int32_t* seq_ids,
+                     bool write_logits, bool greedy_tail, int32_t* n_acc, int32_t* emitted,
+                     cudaStream_t st) {
+  auto enqueue = [&](cudaStream_t s, cudaGraphNode_t* embed_node,
+                     cudaGraphNode_t* tail_node) -> int {
+    int rc = enqueue_forward(m, n_seq, d + 1, draft, seq_ids, write_logits, s, embed_node);
+    if (rc != SPEC_OK || !greedy_tail) return rc;
+    GreedyRoundArgs a;
+    a.argmax = m->argmax;
+    a.draft = draft;
+    a.seq_ids = seq_ids;
+    a.n_acc = n_acc;
+    a.emitted = emitted;
+    a.n_past = m->n_past;
+    a.emit_idx = m->emit_idx;
+    a.anchor = m->anchor;
+    a.err = m->err;
+    a.n_seq = n_seq;
+    a.d = d;
+    a.n_slots = m->d.max_seqs;
+    launch_accept_commit_greedy(a, s);
+    return tail_node != nullptr ? last_captured_node(s, tail_node) : SPEC_OK;
+  };
+  if (!m->use_graphs) return enqueue(st, nullptr, nullptr);
+  const long long key = ((long long)n_seq << 20) | ((long long)(d + 1) << 2) |
+                        (write_logits ? 2 : 0) | (greedy_tail ? 1 : 0);
   auto it = m->graphs.find(key);
-  if (it == m->graphs.end()) {
-    cudaGraph_t g = nullptr;
-    CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
-    int rc = enqueue_forward(m, n_seq, nt, write_logits, m->cap_stream);
-    cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g);
-    if (rc != SPEC_OK) {
-      if (g) cudaGraphDestroy(g);
-      return rc;
+  if (it != m->graphs.end()) {
+    RoundGraph& g = it->second;
+    const bool moved_in = g.draft != draft || g.seq_ids != seq_ids;
+    const bool moved_out = greedy_tail && (g.n_acc != n_acc || g.emitted != emitted);
+    bool ok = true;
+    if (moved_in || moved_out) {
+      ok = embed_node_retarget(g.exec, g.embed, draft, seq_ids) == cudaSuccess;
+      if (ok && greedy_tail)
+        ok = accept_commit_node_retarget(g.exec, g.tail, draft, seq_ids, n_acc, emitted) ==
+             cudaSuccess;
     }
-    if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
-    cudaGraphExec_t ex = nullptr;
-    e = cudaGraphInstantiate(&ex, g, 0);
-    cudaGraphDestroy(g);
-    if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e));
-    it = m->graphs.emplace(key, ex).first;
+    if (ok) {
+      g.draft = draft;
+      g.seq_ids = seq_ids;
+      g.n_acc = n_acc;
+      g.emitted = emitted;
+    } else {  // a node that cannot be updated: capture the graph again
+      cudaGetLastError();
+      round_graph_free(&g);
+      m->graphs.erase(it);
+      it = m->graphs.end();
+    }
   }
-  CUDA_TRY(cudaGraphLaunch(it->second, st));
+  if (it == m->graphs.end()) {
+    RoundGraph g;
+    CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = enqueue(m->cap_stream, &g.embed, greedy_tail ? &g.tail : nullptr);
+    cudaError_t e = cudaStreamEndCapture(m->cap_stream, &g.graph);
+    if (rc != SPEC_OK || e != cudaSuccess) {
+      round_graph_free(&g);
+      if (rc != SPEC_OK) return rc;
+      return fail(SPEC_E_CUDA, std::string("graph capture: ") + cudaGetErrorString(e));
+    }
+    e = cudaGraphInstantiate(&g.exec, g.graph, 0);
+    if (e != cudaSuccess) {
+      round_graph_free(&g);
+      return fail(SPEC_E_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e));
+    }
+    g.draft = draft;
+    g.seq_ids = seq_ids;
+    g.n_acc = n_acc;
+    g.emitted = emitted;
+    it = m->graphs.emplace(key, g).first;
+  }
+  CUDA_TRY(cudaGraphLaunch(it->second.exec, st));
   return SPEC_OK;
 }
 
@@ -663,28 +761,26 @@ extern "C" int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_id
   } else if (q_logits != nullptr) {
     return fail(SPEC_E_INVALID, "q_logits must be NULL in greedy mode");
   }
+  // the kernels read seq_ids and draft in place and write n_acc and emitted
+  const size_t in_ids = sizeof(int32_t) * n_seq, in_draft = sizeof(int32_t) * n_seq * d,
+               out_em = sizeof(int32_t) * n_seq * (d + 1);
+  if (overlaps(emitted, out_em, seq_ids, in_ids) || overlaps(emitted, out_em, draft, in_draft) ||
+      overlaps(n_acc, in_ids, seq_ids, in_ids) || overlaps(n_acc, in_ids, draft, in_draft) ||
+      overlaps(n_acc, in_ids, emitted, out_em))
+    return fail(SPEC_E_INVALID, "n_acc / emitted overlap each other or seq_ids / draft");
   cudaStream_t st = as_stream(stream);
   const int nt = d + 1;
-  CUDA_TRY(cudaMemcpyAsync(m->seq_ids_buf, seq_ids, sizeof(int32_t) * n_seq,
-                           cudaMemcpyDeviceToDevice, st));
-  if (d > 0)
-    CUDA_TRY(cudaMemcpyAsync(m->draft_buf, draft, sizeof(int32_t) * n_seq * d,
-                             cudaMemcpyDeviceToDevice, st));
   const bool write_logits = !greedy || logits_out != nullptr;
-  int rc = run_forward(m, n_seq, nt, write_logits, st);
+  int rc = run_round(m, n_seq, d, draft, seq_ids, write_logits, greedy, n_acc, emitted, st);
   if (rc != SPEC_OK) return rc;
-  if (greedy) {
-    launch_accept_greedy(m->argmax, m->draft_buf, n_seq, d, m->nacc_tmp, emitted, st);
-  } else {
-    rc = launch_accept_stochastic(m->logits, q_logits, m->draft_buf, n_seq, d, D.vocab,
-                                  sampling->temperature, sampling->seed, m->seq_ids_buf,
-                                  m->emit_idx, 1, D.max_seqs, m->nacc_tmp, emitted, m->sscr,
-                                  m->err, st);
+  if (!greedy) {
+    rc = launch_accept_stochastic(m->logits, q_logits, draft, n_seq, d, D.vocab,
+                                  sampling->temperature, sampling->seed, seq_ids, m->emit_idx, 1,
+                                  D.max_seqs, m->nacc_tmp, emitted, m->sscr, m->err, st);
     if (rc != SPEC_OK) return rc;
+    launch_commit(seq_ids, n_seq, d, D.max_seqs, m->nacc_tmp, n_acc, emitted, m->n_past,
+                  m->emit_idx, m->anchor, m->err, st);
   }
-  launch_commit(m->seq_ids_buf, n_seq, d, D.max_seqs, m->nacc_tmp, n_acc, emitted, m->n_past,
-                m->emit_idx,
-                m->anchor, m->err, st);
   if (logits_out != nullptr)
     CUDA_TRY(cudaMemcpyAsync(logits_out, m->logits, sizeof(float) * n_seq * nt * D.vocab,
                              cudaMemcpyDeviceToDevice, st));

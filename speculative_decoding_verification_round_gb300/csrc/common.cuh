@@ -122,11 +122,28 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
 // ---------------------------------------------------------------------------
 // small ops (ops.cu)
 // ---------------------------------------------------------------------------
+struct EmbedArgs {
+  const __half* embed;
+  const int32_t* anchor;   // [max_seqs]
+  const int32_t* draft;    // [n_seq][nt - 1]
+  const int32_t* seq_ids;  // [n_seq]
+  const int32_t* n_past;   // [max_seqs]
+  RowInfo* rows;           // [n_seq * nt]
+  int32_t* tokens;         // [n_seq * nt]
+  float* h;                // [n_seq * nt][H]
+  uint32_t* err;
+  int V, H, nt, max_seqs, max_ctx;
+};
 void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
                        const int32_t* draft, const int32_t* seq_ids, int n_seq,
                        int nt, const int32_t* n_past, int max_seqs, int max_ctx,
                        RowInfo* rows, int32_t* tokens, float* h, uint32_t* err,
                        cudaStream_t st);
+// Points the embedding node of an instantiated graph (captured from
+// launch_embed_rows) at new draft and sequence-id arrays; the other arguments
+// keep their captured values.
+cudaError_t embed_node_retarget(cudaGraphExec_t ex, cudaGraphNode_t node, const int32_t* draft,
+                                const int32_t* seq_ids);
 void launch_rmsnorm(const float* h, const float* gamma, int R, int H, float eps,
                     __half* out, cudaStream_t st);
 void launch_rope_table(float2* tab, int max_ctx, int hd, float theta, cudaStream_t st);
@@ -169,6 +186,26 @@ void launch_commit(const int32_t* seq_ids, int n_seq, int d, int n_slots, const 
                    int32_t* n_acc, int32_t* emitted, int32_t* n_past,
                    uint64_t* emit_idx, int32_t* anchor, const uint32_t* err,
                    cudaStream_t st);
+
+// Greedy accept fused with the commit (the verify round's tail).
+struct GreedyRoundArgs {
+  const int32_t* argmax;   // [n_seq][d + 1]
+  const int32_t* draft;    // [n_seq][d]
+  const int32_t* seq_ids;  // [n_seq]
+  int32_t* n_acc;          // [n_seq]
+  int32_t* emitted;        // [n_seq][d + 1]
+  int32_t* n_past;         // [n_slots]
+  uint64_t* emit_idx;      // [n_slots]
+  int32_t* anchor;         // [n_slots]
+  const uint32_t* err;
+  int n_seq, d, n_slots;
+};
+void launch_accept_commit_greedy(const GreedyRoundArgs& a, cudaStream_t st);
+// Points the tail node of an instantiated round graph (captured from
+// launch_accept_commit_greedy) at new input and output arrays.
+cudaError_t accept_commit_node_retarget(cudaGraphExec_t ex, cudaGraphNode_t node,
+                                        const int32_t* draft, const int32_t* seq_ids,
+                                        int32_t* n_acc, int32_t* emitted);
 
 // Whether kernels that can overlap their predecessor's tail are launched as
 // programmatic dependents (default on; SPEC_VERIFY_PDL=0 in the environment

@@ -11,12 +11,12 @@
 
 namespace {
 
-__global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, int nt,
-                                const int32_t* __restrict__ n_past, int max_seqs,
-                                int max_ctx, RowInfo* __restrict__ rows,
-                                uint32_t* __restrict__ err) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= n_seq * nt) return;
+// Row r = (sequence s, offset i): the sequence's slot (checked) and the
+// row's absolute position n_past[slot] + i (checked against max_ctx; an
+// invalid position becomes max_ctx, where consumers write nothing).
+__device__ __forceinline__ RowInfo row_info(const int32_t* __restrict__ seq_ids, int r, int nt,
+                                            const int32_t* __restrict__ n_past, int max_seqs,
+                                            int max_ctx, uint32_t* __restrict__ err) {
   const int s = r / nt, i = r % nt;
   int slot = seq_ids[s];
   if (slot < 0 || slot >= max_seqs) {
@@ -26,35 +26,43 @@ __global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, 
   int pos = n_past[slot] + i;
   if (pos < 0 || pos >= max_ctx) {
     atomicOr(err, ERR_POS);
-    pos = max_ctx;  // consumers skip writes at pos >= max_ctx
+    pos = max_ctx;
   }
-  rows[r] = RowInfo{slot, pos};
+  return RowInfo{slot, pos};
 }
 
-// One CTA per verify row: token lookup (anchor for row 0, drafts after),
-// id check, fp16 -> fp32 copy of the embedding row.
-__global__ void embed_kernel(const __half* __restrict__ embed, int V, int H,
-                             const int32_t* __restrict__ anchor,
-                             const int32_t* __restrict__ draft,
-                             const RowInfo* __restrict__ rows, int nt,
-                             int32_t* __restrict__ tokens, float* __restrict__ h,
-                             uint32_t* __restrict__ err) {
+__global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, int nt,
+                                const int32_t* __restrict__ n_past, int max_seqs,
+                                int max_ctx, RowInfo* __restrict__ rows,
+                                uint32_t* __restrict__ err) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_seq * nt) return;
+  rows[r] = row_info(seq_ids, r, nt, n_past, max_seqs, max_ctx, err);
+}
+
+// One CTA per verify row: the row's (slot, position) record, token lookup
+// (anchor for row 0, drafts after), id check, fp16 -> fp32 copy of the
+// embedding row.  The arguments travel as one struct so that a captured
+// launch can be pointed at a new round's draft and sequence-id arrays.
+__global__ void embed_kernel(const EmbedArgs a) {
   const int r = blockIdx.x;
-  const int s = r / nt, i = r % nt;
+  const int s = r / a.nt, i = r % a.nt;
   __shared__ int s_tok;
   if (threadIdx.x == 0) {
-    int tok = i == 0 ? anchor[rows[r].slot] : draft[s * (nt - 1) + (i - 1)];
-    if (tok < 0 || tok >= V) {
-      atomicOr(err, ERR_TOKEN);
+    const RowInfo ri = row_info(a.seq_ids, r, a.nt, a.n_past, a.max_seqs, a.max_ctx, a.err);
+    a.rows[r] = ri;
+    int tok = i == 0 ? a.anchor[ri.slot] : a.draft[s * (a.nt - 1) + (i - 1)];
+    if (tok < 0 || tok >= a.V) {
+      atomicOr(a.err, ERR_TOKEN);
       tok = 0;
     }
     s_tok = tok;
-    tokens[r] = tok;
+    a.tokens[r] = tok;
   }
   __syncthreads();
-  const __half2* src = reinterpret_cast<const __half2*>(embed + (size_t)s_tok * H);
-  float2* dst = reinterpret_cast<float2*>(h + (size_t)r * H);
-  for (int j = threadIdx.x; j < H / 2; j += blockDim.x) dst[j] = __half22float2(src[j]);
+  const __half2* src = reinterpret_cast<const __half2*>(a.embed + (size_t)s_tok * a.H);
+  float2* dst = reinterpret_cast<float2*>(a.h + (size_t)r * a.H);
+  for (int j = threadIdx.x; j < a.H / 2; j += blockDim.x) dst[j] = __half22float2(src[j]);
 }
 
 // One CTA (256 threads) per row.  The sum of squares is reduced in a fixed
@@ -139,9 +147,38 @@ void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
                        const int32_t* draft, const int32_t* seq_ids, int n_seq, int nt,
                        const int32_t* n_past, int max_seqs, int max_ctx, RowInfo* rows,
                        int32_t* tokens, float* h, uint32_t* err, cudaStream_t st) {
-  launch_row_info(seq_ids, n_seq, nt, n_past, max_seqs, max_ctx, rows, err, st);
-  embed_kernel<<<n_seq * nt, 256, 0, st>>>(embed, V, H, anchor, draft, rows, nt, tokens,
-                                           h, err);
+  EmbedArgs a;
+  a.embed = embed;
+  a.anchor = anchor;
+  a.draft = draft;
+  a.seq_ids = seq_ids;
+  a.n_past = n_past;
+  a.rows = rows;
+  a.tokens = tokens;
+  a.h = h;
+  a.err = err;
+  a.V = V;
+  a.H = H;
+  a.nt = nt;
+  a.max_seqs = max_seqs;
+  a.max_ctx = max_ctx;
+  embed_kernel<<<n_seq * nt, 256, 0, st>>>(a);
+}
+
+cudaError_t embed_node_retarget(cudaGraphExec_t ex, cudaGraphNode_t node, const int32_t* draft,
+                                const int32_t* seq_ids) {
+  cudaKernelNodeParams p;
+  cudaError_t e = cudaGraphKernelNodeGetParams(node, &p);
+  if (e != cudaSuccess) return e;
+  if (p.func != reinterpret_cast<void*>(embed_kernel) || p.kernelParams == nullptr)
+    return cudaErrorInvalidValue;
+  EmbedArgs a = *static_cast<const EmbedArgs*>(p.kernelParams[0]);
+  a.draft = draft;
+  a.seq_ids = seq_ids;
+  void* args[] = {&a};
+  p.kernelParams = args;
+  p.extra = nullptr;
+  return cudaGraphExecKernelNodeSetParams(ex, node, &p);
 }
 
 void launch_rmsnorm(const float* h, const float* gamma, int R, int H, float eps,

@@ -87,6 +87,46 @@ def test_round_greedy_matches_oracle(orc, dev, graphs):
     assert anc2 == [int(em[s, n_acc[s]]) for s in range(n_seq)]
 
 
+def test_round_graph_follows_caller_buffers(dev):
+    """A greedy round without logits replays one captured graph per shape with
+    the caller's arrays as kernel arguments: rounds that alternate between two
+    sets of input and output arrays, and change d, give exactly what the same
+    rounds give launched kernel by kernel; outputs that overlap the inputs are
+    refused on the host."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    g = np.random.default_rng(47)
+    cfg, raw = small_decoder(g, L=2, V=512)
+    n_seq, max_ctx = 3, 260
+    ms = []
+    for graphs in (True, False):
+        m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, 4)
+        m.set_graphs(graphs)
+        fill_context(sv, m, np.random.default_rng(5), cfg, 4, max_ctx, dev)
+        sv.spec_state_set(m, [2, 0, 3], n_past=[40, 90, 7], emit_idx=[0, 0, 0], anchor=[1, 2, 3])
+        ms.append(m)
+    slots = [torch.tensor(x, dtype=torch.int32, device=dev) for x in ([2, 0, 3], [2, 0, 3])]
+    bufs = {(d, k): (torch.empty(n_seq, dtype=torch.int32, device=dev),
+                     torch.empty((n_seq, d + 1), dtype=torch.int32, device=dev))
+            for d in (3, 5) for k in (0, 1)}
+    for rnd, d in enumerate([5, 5, 3, 5, 3, 5]):
+        draft = torch.from_numpy(g.integers(0, cfg["vocab"], (n_seq, d)).astype(np.int32)).to(dev)
+        outs = []
+        for m in ms:
+            n_acc, em = bufs[(d, rnd % 2)]
+            sv.spec_verify_round(m, n_seq, slots[rnd % 2], draft, d, n_acc=n_acc, emitted=em)
+            assert sv.spec_error_check(m) == 0
+            outs.append((n_acc.cpu().numpy().copy(), em.cpu().numpy().copy(),
+                         sv.spec_state_get(m, [2, 0, 3])))
+        (na, ea, sa), (nb, eb, sb) = outs
+        assert np.array_equal(na, nb) and np.array_equal(ea, eb) and sa == sb, rnd
+        assert all(0 <= a <= d for a in na)
+    whole = torch.zeros(n_seq * 6 + n_seq, dtype=torch.int32, device=dev)
+    with pytest.raises(sv.SpecError):  # emitted over the drafts
+        sv.spec_verify_round(ms[0], n_seq, slots[0], whole[:n_seq * 5].view(n_seq, 5), 5,
+                             n_acc=bufs[(5, 0)][0], emitted=whole[n_seq:].view(n_seq, 6))
+
+
 def test_round_stochastic_matches_oracle(orc, dev):
     import speculative_decoding_verification_round_gb300 as sv
     from test_gpu_accept import sample_drafts_oracle
