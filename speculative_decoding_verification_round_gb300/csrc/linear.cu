@@ -249,7 +249,7 @@ __device__ __forceinline__ void zero_point_frag(uint32_t (&A)[4]) {
 // Per 32-block and column tile, C = -bias * sum(x) (two MMAs with the
 // zero-point fragment, shared by both tiles) starts each block's fresh
 // accumulator; the block's two k16 MMAs add sum(u * x); one FMA per element
-// folds the block scale into the running sum.
+// (packed in pairs) folds the block scale into the running sum.
 template <int QT, int NCT>
 __device__ __forceinline__ void compute_chunk(const unsigned char* st, const unsigned char* xs,
                                               int xstride, int j, int lane,
@@ -299,10 +299,15 @@ __device__ __forceinline__ void compute_chunk(const unsigned char* st, const uns
         float blk[4];
         mma_16816_c(blk, A0, xb[ct][b].x, xb[ct][b].y, zc[ct][b]);
         mma_16816(blk, A1, xb[ct][b].z, xb[ct][b].w);
-        acc[i][ct][0] = fmaf(sg, blk[0], acc[i][ct][0]);
-        acc[i][ct][1] = fmaf(sg, blk[1], acc[i][ct][1]);
-        acc[i][ct][2] = fmaf(sg8, blk[2], acc[i][ct][2]);
-        acc[i][ct][3] = fmaf(sg8, blk[3], acc[i][ct][3]);
+        // two packed FMAs (each half rounded exactly as fmaf)
+        const float2 r01 = __ffma2_rn(make_float2(sg, sg), make_float2(blk[0], blk[1]),
+                                      make_float2(acc[i][ct][0], acc[i][ct][1]));
+        const float2 r23 = __ffma2_rn(make_float2(sg8, sg8), make_float2(blk[2], blk[3]),
+                                      make_float2(acc[i][ct][2], acc[i][ct][3]));
+        acc[i][ct][0] = r01.x;
+        acc[i][ct][1] = r01.y;
+        acc[i][ct][2] = r23.x;
+        acc[i][ct][3] = r23.y;
       }
     }
   }
@@ -428,8 +433,11 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
   }
 }
 
+// Register budget: 3 CTAs per SM with one column tile (at most 80
+// registers; the shared memory never holds more than 3 CTAs either), 2 with
+// two (their accumulators and activation fragments need about 110).
 template <int QT, int NCT, int KW>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, NCT == 1 ? 3 : 2)
 linear_q_kernel(const LinArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using RC = Rec<QT>;
