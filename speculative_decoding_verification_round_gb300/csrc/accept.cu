@@ -399,34 +399,45 @@ __global__ void commit_kernel(const int32_t* __restrict__ seq_ids, int n_seq, in
   anchor[slot] = e[a];
 }
 
-// Greedy accept and commit in one pass, for the verify round: one thread per
-// sequence takes the greedy decision above, then the commit below on the
-// same values, so the round ends with a single launch after the LM head.  A
-// programmatic dependent of the LM head: it waits for that grid's memory.
+// Greedy accept and commit in one pass, for the verify round: one warp per
+// sequence, lane i holding row i's argmax and draft i (d + 1 <= 32), so the
+// first mismatch is one ballot and nothing waits on a chain of loads.  A
+// programmatic dependent of the LM head: the drafts and the slot, which the
+// round's target pass does not write, are read before the grid dependency
+// resolves; the argmax, the error word and the state after.
+static_assert(SPEC_MAX_NT <= 32, "one warp holds a sequence's d + 1 rows");
 __global__ void accept_commit_greedy_kernel(const GreedyRoundArgs a) {
-  grid_dep_wait();
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= a.n_seq) return;
+  const int lane = threadIdx.x & 31;
+  const int s = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int d = a.d;
-  const int32_t* am = a.argmax + (size_t)s * (d + 1);
-  const int32_t* dr = a.draft + (size_t)s * d;
-  int32_t* e = a.emitted + (size_t)s * (d + 1);
-  int n = 0;
-  while (n < d && am[n] == dr[n]) n++;
-  const int slot = a.seq_ids[s];
-  const int last = am[n];
-  if (*a.err != 0u || slot < 0 || slot >= a.n_slots || last < 0) {
-    a.n_acc[s] = -1;
-    for (int i = 0; i <= d; i++) e[i] = -1;
-    return;
+  const bool live = s < a.n_seq;
+  int slot = 0, dtok = -1;
+  if (live) {
+    slot = a.seq_ids[s];
+    if (lane < d) dtok = a.draft[(size_t)s * d + lane];
   }
-  for (int i = 0; i < n; i++) e[i] = dr[i];
-  e[n] = last;
-  for (int i = n + 1; i <= d; i++) e[i] = -1;
-  a.n_acc[s] = n;
-  a.n_past[slot] += n + 1;
-  a.emit_idx[slot] += (uint64_t)(n + 1);
-  a.anchor[slot] = last;
+  grid_dep_wait();
+  if (!live) return;  // whole warps
+  const int am = lane <= d ? a.argmax[(size_t)s * (d + 1) + lane] : -1;
+  const unsigned match = __ballot_sync(0xffffffffu, lane < d && am == dtok);
+  const int n = __ffs(~match) - 1;  // the first row whose argmax is not its draft, or d
+  const int last = __shfl_sync(0xffffffffu, am, n);
+  const bool bad = *a.err != 0u || slot < 0 || slot >= a.n_slots || last < 0;
+  if (lane <= d) {
+    int v = -1;
+    if (!bad) v = lane < n ? dtok : (lane == n ? last : -1);
+    a.emitted[(size_t)s * (d + 1) + lane] = v;
+  }
+  if (lane == 0) {
+    if (bad) {
+      a.n_acc[s] = -1;
+    } else {
+      a.n_acc[s] = n;
+      a.n_past[slot] += n + 1;
+      a.emit_idx[slot] += (uint64_t)(n + 1);
+      a.anchor[slot] = last;
+    }
+  }
 }
 
 }  // namespace
@@ -490,7 +501,7 @@ void launch_accept_commit_greedy(const GreedyRoundArgs& a, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = programmatic_launch() ? 1 : 0;
-  cfg.gridDim = dim3((a.n_seq + 127) / 128);
+  cfg.gridDim = dim3((a.n_seq + 3) / 4);  // 4 sequences (warps) per CTA
   cfg.blockDim = dim3(128);
   cudaLaunchKernelEx(&cfg, accept_commit_greedy_kernel, a);
 }

@@ -49,9 +49,20 @@ __global__ void embed_kernel(const EmbedArgs a) {
   const int s = r / a.nt, i = r % a.nt;
   __shared__ int s_tok;
   if (threadIdx.x == 0) {
-    const RowInfo ri = row_info(a.seq_ids, r, a.nt, a.n_past, a.max_seqs, a.max_ctx, a.err);
-    a.rows[r] = ri;
-    int tok = i == 0 ? a.anchor[ri.slot] : a.draft[s * (a.nt - 1) + (i - 1)];
+    // the same record as row_info, with the loads in two dependent levels:
+    // (slot, draft token), then (position, anchor)
+    const int raw = a.seq_ids[s];
+    const int dtok = i > 0 ? a.draft[s * (a.nt - 1) + (i - 1)] : 0;
+    const int slot = raw < 0 || raw >= a.max_seqs ? 0 : raw;
+    const int np = a.n_past[slot];
+    int tok = i == 0 ? a.anchor[slot] : dtok;
+    if (slot != raw) atomicOr(a.err, ERR_SEQ);
+    int pos = np + i;
+    if (pos < 0 || pos >= a.max_ctx) {
+      atomicOr(a.err, ERR_POS);
+      pos = a.max_ctx;
+    }
+    a.rows[r] = RowInfo{slot, pos};
     if (tok < 0 || tok >= a.V) {
       atomicOr(a.err, ERR_TOKEN);
       tok = 0;
