@@ -33,7 +33,8 @@ EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_li
             "spec_kv_read", "spec_model_debug_read",
             "spec_state_set", "spec_state_get", "spec_error_check", "spec_model_set_graphs",
             "spec_verify_attn", "spec_lm_head", "spec_accept_greedy",
-            "spec_accept_stochastic", "spec_accept_stochastic_noalloc", "spec_verify_round"]
+            "spec_accept_stochastic", "spec_accept_stochastic_noalloc", "spec_verify_round",
+            "spec_verify_round_host"]
 
 P = ctypes.c_void_p
 I32 = ctypes.c_int32
@@ -106,6 +107,8 @@ def lib():
                                                          U64, P, P, P, P, P]),
                 "spec_verify_round": (I32, [P, I32, P, P, I32, P, ctypes.POINTER(spec_sampling),
                                             P, P, P, P]),
+                "spec_verify_round_host": (I32, [P, I32, P, P, I32, P,
+                                                 ctypes.POINTER(spec_sampling), P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -323,3 +326,33 @@ def spec_verify_round(m: Model, n_seq: int, seq_ids, draft, d: int, q_logits=Non
     _check(lib().spec_verify_round(m.handle, int(n_seq), _ptr(seq_ids), _ptr(draft), int(d),
                                    _ptr(q_logits), ctypes.byref(sp), _ptr(n_acc), _ptr(emitted),
                                    _ptr(logits_out), _stream(stream)))
+
+
+def _host_i32(a, shape, name):
+    import numpy as np
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous
+            and a.size >= int(np.prod(shape))):
+        raise ValueError(f"{name}: a C-contiguous int32 numpy array of {shape} is required")
+    return a
+
+
+def spec_verify_round_host(m: Model, n_seq: int, seq_ids, draft, d: int, q_logits=None,
+                           greedy: bool = True, temperature: float = 1.0, seed: int = 0,
+                           n_acc=None, emitted=None, stream=None):
+    """spec_verify_round with host (numpy int32) seq_ids, draft, n_acc and emitted.
+    Returns (n_acc, emitted); they are valid on return (the call synchronises)."""
+    import numpy as np
+    sid = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    dr = np.ascontiguousarray(draft, dtype=np.int32) if d > 0 else None
+    if n_acc is None:
+        n_acc = np.empty(n_seq, np.int32)
+    if emitted is None:
+        emitted = np.empty((n_seq, d + 1), np.int32)
+    _host_i32(n_acc, (n_seq,), "n_acc")
+    _host_i32(emitted, (n_seq, d + 1), "emitted")
+    sp = spec_sampling(int(bool(greedy)), float(temperature), int(seed))
+    _check(lib().spec_verify_round_host(m.handle, int(n_seq), sid.ctypes.data,
+                                        None if dr is None else dr.ctypes.data, int(d),
+                                        _ptr(q_logits), ctypes.byref(sp), n_acc.ctypes.data,
+                                        emitted.ctypes.data, _stream(stream)))
+    return n_acc, emitted

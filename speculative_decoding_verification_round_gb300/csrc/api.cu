@@ -270,6 +270,12 @@ struct spec_model {
   int32_t* tokens = nullptr;
   int32_t* seq_ids_buf = nullptr;
   int32_t* nacc_tmp = nullptr;
+  // spec_verify_round_host: pinned staging and its device mirror, each
+  // [max_seqs] sequence ids / accept counts then [max_seqs][max_nt] ids
+  int32_t* io_host_in = nullptr;
+  int32_t* io_host_out = nullptr;
+  int32_t* io_dev_in = nullptr;
+  int32_t* io_dev_out = nullptr;
   float* attn_part = nullptr;
   LinScratch lscr;
   StochScratch sscr;
@@ -304,6 +310,8 @@ static void model_free(spec_model* m) {
   for (void* p : m->allocs) cudaFree(p);
   m->allocs.clear();
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  if (m->io_host_in) cudaFreeHost(m->io_host_in);
+  if (m->io_host_out) cudaFreeHost(m->io_host_out);
   delete m;
 }
 
@@ -421,6 +429,18 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
   TRY(dalloc_t(m, &m->tokens, R));
   TRY(dalloc_t(m, &m->seq_ids_buf, D.max_seqs));
   TRY(dalloc_t(m, &m->nacc_tmp, D.max_seqs));
+  {
+    const size_t io = (size_t)D.max_seqs * (1 + D.max_nt);
+    TRY(dalloc_t(m, &m->io_dev_in, io));
+    TRY(dalloc_t(m, &m->io_dev_out, io));
+    if (cudaHostAlloc(reinterpret_cast<void**>(&m->io_host_in), io * sizeof(int32_t),
+                      cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(reinterpret_cast<void**>(&m->io_host_out), io * sizeof(int32_t),
+                      cudaHostAllocDefault) != cudaSuccess) {
+      cudaGetLastError();
+      TRY(fail(SPEC_E_OOM, "pinned host staging"));
+    }
+  }
   // scratch
   std::vector<const QMat*> mats{&m->lm};
   for (int l = 0; l < L; l++) {
@@ -668,9 +688,16 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
 // graphs are on.
 static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, const int32_t* seq_ids,
                      bool write_logits, bool greedy_tail, int32_t* n_acc, int32_t* emitted,
-                     cudaStream_t st) {
+                     cudaStream_t st, bool host_io = false) {
+  // host_io: the inputs come from the pinned staging (copied to its device
+  // mirror first) and the outputs go back to it (greedy rounds only)
+  const size_t n_in = (size_t)n_seq * (1 + d), n_out = (size_t)n_seq * (2 + d);
   auto enqueue = [&](cudaStream_t s, cudaGraphNode_t* embed_node,
                      cudaGraphNode_t* tail_node) -> int {
+    if (host_io &&
+        cudaMemcpyAsync(m->io_dev_in, m->io_host_in, sizeof(int32_t) * n_in,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return fail(SPEC_E_CUDA, "staging copy in");
     int rc = enqueue_forward(m, n_seq, d + 1, draft, seq_ids, write_logits, s, embed_node);
     if (rc != SPEC_OK || !greedy_tail) return rc;
     GreedyRoundArgs a;
@@ -687,11 +714,16 @@ static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, cons
     a.d = d;
     a.n_slots = m->d.max_seqs;
     launch_accept_commit_greedy(a, s);
-    return tail_node != nullptr ? last_captured_node(s, tail_node) : SPEC_OK;
+    rc = tail_node != nullptr ? last_captured_node(s, tail_node) : SPEC_OK;
+    if (rc == SPEC_OK && host_io &&
+        cudaMemcpyAsync(m->io_host_out, m->io_dev_out, sizeof(int32_t) * n_out,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return fail(SPEC_E_CUDA, "staging copy out");
+    return rc;
   };
   if (!m->use_graphs) return enqueue(st, nullptr, nullptr);
-  const long long key = ((long long)n_seq << 20) | ((long long)(d + 1) << 2) |
-                        (write_logits ? 2 : 0) | (greedy_tail ? 1 : 0);
+  const long long key = ((long long)(host_io ? 1 : 0) << 40) | ((long long)n_seq << 20) |
+                        ((long long)(d + 1) << 2) | (write_logits ? 2 : 0) | (greedy_tail ? 1 : 0);
   auto it = m->graphs.find(key);
   if (it != m->graphs.end()) {
     RoundGraph& g = it->second;
@@ -785,6 +817,55 @@ extern "C" int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_id
     CUDA_TRY(cudaMemcpyAsync(logits_out, m->logits, sizeof(float) * n_seq * nt * D.vocab,
                              cudaMemcpyDeviceToDevice, st));
   CUDA_TRY(cudaGetLastError());
+  return SPEC_OK;
+}
+
+extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* seq_ids,
+                                      const int32_t* draft, int d, const float* q_logits,
+                                      const spec_sampling* sampling, int32_t* n_acc,
+                                      int32_t* emitted, void* stream) {
+  if (m == nullptr || seq_ids == nullptr || sampling == nullptr || n_acc == nullptr ||
+      emitted == nullptr)
+    return fail(SPEC_E_INVALID, "null argument");
+  const spec_model_desc& D = m->d;
+  if (D.n_layers == 0) return fail(SPEC_E_UNSUPPORTED, "verify round needs a decoder (n_layers > 0)");
+  if (n_seq < 1 || n_seq > D.max_seqs) return fail(SPEC_E_SHAPE, "n_seq outside [1, max_seqs]");
+  if (d < 0 || d + 1 > D.max_nt) return fail(SPEC_E_SHAPE, "d + 1 outside [1, max_nt]");
+  if (d > 0 && draft == nullptr) return fail(SPEC_E_INVALID, "null draft");
+  const bool greedy = sampling->greedy != 0;
+  if (!greedy) {
+    if (!(sampling->temperature > 0.0f) || !std::isfinite(sampling->temperature))
+      return fail(SPEC_E_INVALID, "temperature must be finite and > 0");
+    if (d > 0 && q_logits == nullptr) return fail(SPEC_E_INVALID, "stochastic accept needs q_logits");
+  } else if (q_logits != nullptr) {
+    return fail(SPEC_E_INVALID, "q_logits must be NULL in greedy mode");
+  }
+  cudaStream_t st = as_stream(stream);
+  // the staging is free: every call has synchronised before returning
+  std::memcpy(m->io_host_in, seq_ids, sizeof(int32_t) * n_seq);
+  if (d > 0) std::memcpy(m->io_host_in + n_seq, draft, sizeof(int32_t) * n_seq * d);
+  const int32_t* dseq = m->io_dev_in;
+  const int32_t* ddraft = d > 0 ? m->io_dev_in + n_seq : nullptr;
+  int32_t* dacc = m->io_dev_out;
+  int32_t* dem = m->io_dev_out + n_seq;
+  int rc = run_round(m, n_seq, d, ddraft, dseq, !greedy, greedy, dacc, dem, st, true);
+  if (rc != SPEC_OK) return rc;
+  if (!greedy) {
+    rc = launch_accept_stochastic(m->logits, q_logits, ddraft, n_seq, d, D.vocab,
+                                  sampling->temperature, sampling->seed, dseq, m->emit_idx, 1,
+                                  D.max_seqs, m->nacc_tmp, dem, m->sscr, m->err, st);
+    if (rc != SPEC_OK) {
+      cudaStreamSynchronize(st);
+      return rc;
+    }
+    launch_commit(dseq, n_seq, d, D.max_seqs, m->nacc_tmp, dacc, dem, m->n_past, m->emit_idx,
+                  m->anchor, m->err, st);
+    CUDA_TRY(cudaMemcpyAsync(m->io_host_out, m->io_dev_out, sizeof(int32_t) * n_seq * (2 + d),
+                             cudaMemcpyDeviceToHost, st));
+  }
+  CUDA_TRY(cudaStreamSynchronize(st));
+  std::memcpy(n_acc, m->io_host_out, sizeof(int32_t) * n_seq);
+  std::memcpy(emitted, m->io_host_out + n_seq, sizeof(int32_t) * n_seq * (d + 1));
   return SPEC_OK;
 }
 

@@ -127,6 +127,42 @@ def test_round_graph_follows_caller_buffers(dev):
                              n_acc=bufs[(5, 0)][0], emitted=whole[n_seq:].view(n_seq, 6))
 
 
+@pytest.mark.parametrize("graphs", [True, False])
+def test_round_host_buffers_match_device_buffers(dev, graphs):
+    """spec_verify_round_host (host arrays through the model's pinned
+    staging) gives exactly what spec_verify_round gives with device arrays,
+    greedy and stochastic, with d changing between rounds."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    g = np.random.default_rng(48)
+    cfg, raw = small_decoder(g, L=2, V=512)
+    n_seq, max_ctx = 2, 260
+    ms = []
+    for _ in range(2):
+        m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, 3)
+        m.set_graphs(graphs)
+        fill_context(sv, m, np.random.default_rng(6), cfg, 3, max_ctx, dev)
+        sv.spec_state_set(m, [1, 2], n_past=[30, 80], emit_idx=[4, 9], anchor=[5, 6])
+        ms.append(m)
+    slots = np.array([1, 2], np.int32)
+    for rnd, (d, greedy) in enumerate([(5, True), (5, True), (2, True), (4, False), (0, True)]):
+        draft = g.integers(0, cfg["vocab"], (n_seq, d)).astype(np.int32)
+        q = None
+        if not greedy:
+            q = torch.from_numpy((g.standard_normal((n_seq, d, cfg["vocab"])) * 2)
+                                 .astype(np.float32)).to(dev)
+        n_acc = torch.empty(n_seq, dtype=torch.int32, device=dev)
+        em = torch.empty((n_seq, d + 1), dtype=torch.int32, device=dev)
+        sv.spec_verify_round(ms[0], n_seq, torch.from_numpy(slots).to(dev),
+                             torch.from_numpy(draft).to(dev) if d else None, d, q, greedy, 0.8,
+                             77, n_acc, em)
+        na_h, em_h = sv.spec_verify_round_host(ms[1], n_seq, slots, draft, d, q, greedy, 0.8, 77)
+        assert sv.spec_error_check(ms[0]) == 0 and sv.spec_error_check(ms[1]) == 0
+        assert np.array_equal(n_acc.cpu().numpy(), na_h), rnd
+        assert np.array_equal(em.cpu().numpy(), em_h), rnd
+        assert sv.spec_state_get(ms[0], [1, 2]) == sv.spec_state_get(ms[1], [1, 2]), rnd
+
+
 def test_round_stochastic_matches_oracle(orc, dev):
     import speculative_decoding_verification_round_gb300 as sv
     from test_gpu_accept import sample_drafts_oracle
