@@ -371,9 +371,9 @@ def run_ours(args):
     ms_per_step = t_max / args.steps * 1e3
 
     # end to end through host buffers: spec_verify_round_host takes the
-    # drafts from host memory (through the model's pinned staging: H2D copy,
-    # the round and the D2H copy of (n_acc, emitted) in one graph launch) and
-    # returns the results in host memory, every step
+    # drafts from host memory (copied into the model's mapped pinned staging,
+    # which the round's kernels read and write in place: one graph launch)
+    # and returns (n_acc, emitted) in host memory, every step
     sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
     h_drafts = [np.array([c], dtype=np.int32) for c in drafts]
     h_sid = np.zeros(1, dtype=np.int32)
@@ -434,7 +434,7 @@ def run_ours(args):
                          "peak_kind": peak_kind, "per_shape": per},
             "sweep": sweep,
             "e2e": {"value": round(e2e_all / t_e2e, 2), "unit": "tok/s",
-                    "api": "spec_verify_round_host (host arrays, pinned staging)",
+                    "api": "spec_verify_round_host (host arrays, mapped pinned staging)",
                     "h2d_bytes_per_step": 4 * (1 + d), "d2h_bytes_per_step": 4 * (2 + d)},
             "gpu_launches": launches_per_round * args.steps,
             "clocks": clk.summary(),

@@ -298,12 +298,12 @@ int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_ids,
 /* The same verify round with seq_ids, draft, n_acc and emitted in HOST
  * memory (any host memory; shapes as for spec_verify_round; q_logits, when
  * given, stays a device array).  The inputs are copied into the model's
- * pinned staging, then one enqueue on `stream` moves them to the device, runs
- * the round and moves the outputs back -- for a greedy round with graphs on,
- * all of it is one graph launch -- and the call synchronises `stream` before
- * it copies the outputs out, so they are valid on return.  Calls on one model
- * must not overlap (the staging is the model's).  Errors: as
- * spec_verify_round, plus SPEC_E_CUDA from the copies or the synchronisation. */
+ * mapped pinned staging, which the kernels read and write in place (no
+ * copy engine steps; a greedy round with graphs on is one graph launch); the
+ * call synchronises `stream` before it copies the outputs out, so they are
+ * valid on return.  Calls on one model must not overlap (the staging is the
+ * model's).  Errors: as spec_verify_round, plus SPEC_E_CUDA from the
+ * synchronisation. */
 int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* seq_ids,
                            const int32_t* draft, int d, const float* q_logits,
                            const spec_sampling* sampling, int32_t* n_acc,

@@ -328,11 +328,14 @@ def spec_verify_round(m: Model, n_seq: int, seq_ids, draft, d: int, q_logits=Non
                                    _ptr(logits_out), _stream(stream)))
 
 
-def _host_i32(a, shape, name):
+def _host_i32(a, n, name):
+    """a as a C-contiguous int32 numpy array of at least n elements (no copy
+    when it already is one)."""
     import numpy as np
-    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous
-            and a.size >= int(np.prod(shape))):
-        raise ValueError(f"{name}: a C-contiguous int32 numpy array of {shape} is required")
+    if not (type(a) is np.ndarray and a.dtype == np.int32 and a.flags.c_contiguous):
+        a = np.ascontiguousarray(a, dtype=np.int32)
+    if a.size < n:
+        raise ValueError(f"{name}: {n} int32 values required, got {a.size}")
     return a
 
 
@@ -340,16 +343,20 @@ def spec_verify_round_host(m: Model, n_seq: int, seq_ids, draft, d: int, q_logit
                            greedy: bool = True, temperature: float = 1.0, seed: int = 0,
                            n_acc=None, emitted=None, stream=None):
     """spec_verify_round with host (numpy int32) seq_ids, draft, n_acc and emitted.
-    Returns (n_acc, emitted); they are valid on return (the call synchronises)."""
+    Returns (n_acc, emitted); they are valid on return (the call synchronises).
+    n_acc / emitted, when given, must be C-contiguous int32 arrays (written in
+    place)."""
     import numpy as np
-    sid = np.ascontiguousarray(seq_ids, dtype=np.int32)
-    dr = np.ascontiguousarray(draft, dtype=np.int32) if d > 0 else None
+    sid = _host_i32(seq_ids, n_seq, "seq_ids")
+    dr = _host_i32(draft, n_seq * d, "draft") if d > 0 else None
     if n_acc is None:
         n_acc = np.empty(n_seq, np.int32)
     if emitted is None:
         emitted = np.empty((n_seq, d + 1), np.int32)
-    _host_i32(n_acc, (n_seq,), "n_acc")
-    _host_i32(emitted, (n_seq, d + 1), "emitted")
+    for a, n, name in ((n_acc, n_seq, "n_acc"), (emitted, n_seq * (d + 1), "emitted")):
+        if not (type(a) is np.ndarray and a.dtype == np.int32 and a.flags.c_contiguous
+                and a.size >= n):
+            raise ValueError(f"{name}: a C-contiguous int32 numpy array of {n} values is required")
     sp = spec_sampling(int(bool(greedy)), float(temperature), int(seed))
     _check(lib().spec_verify_round_host(m.handle, int(n_seq), sid.ctypes.data,
                                         None if dr is None else dr.ctypes.data, int(d),

@@ -270,8 +270,9 @@ struct spec_model {
   int32_t* tokens = nullptr;
   int32_t* seq_ids_buf = nullptr;
   int32_t* nacc_tmp = nullptr;
-  // spec_verify_round_host: pinned staging and its device mirror, each
-  // [max_seqs] sequence ids / accept counts then [max_seqs][max_nt] ids
+  // spec_verify_round_host: mapped pinned staging (the kernels read the
+  // inputs and write the outputs there directly) and its device addresses,
+  // each [max_seqs] sequence ids / accept counts then [max_seqs][max_nt] ids
   int32_t* io_host_in = nullptr;
   int32_t* io_host_out = nullptr;
   int32_t* io_dev_in = nullptr;
@@ -431,14 +432,16 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
   TRY(dalloc_t(m, &m->nacc_tmp, D.max_seqs));
   {
     const size_t io = (size_t)D.max_seqs * (1 + D.max_nt);
-    TRY(dalloc_t(m, &m->io_dev_in, io));
-    TRY(dalloc_t(m, &m->io_dev_out, io));
     if (cudaHostAlloc(reinterpret_cast<void**>(&m->io_host_in), io * sizeof(int32_t),
-                      cudaHostAllocDefault) != cudaSuccess ||
+                      cudaHostAllocMapped) != cudaSuccess ||
         cudaHostAlloc(reinterpret_cast<void**>(&m->io_host_out), io * sizeof(int32_t),
-                      cudaHostAllocDefault) != cudaSuccess) {
+                      cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer(reinterpret_cast<void**>(&m->io_dev_in), m->io_host_in, 0) !=
+            cudaSuccess ||
+        cudaHostGetDevicePointer(reinterpret_cast<void**>(&m->io_dev_out), m->io_host_out, 0) !=
+            cudaSuccess) {
       cudaGetLastError();
-      TRY(fail(SPEC_E_OOM, "pinned host staging"));
+      TRY(fail(SPEC_E_OOM, "mapped pinned host staging"));
     }
   }
   // scratch
@@ -689,15 +692,10 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
 static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, const int32_t* seq_ids,
                      bool write_logits, bool greedy_tail, int32_t* n_acc, int32_t* emitted,
                      cudaStream_t st, bool host_io = false) {
-  // host_io: the inputs come from the pinned staging (copied to its device
-  // mirror first) and the outputs go back to it (greedy rounds only)
-  const size_t n_in = (size_t)n_seq * (1 + d), n_out = (size_t)n_seq * (2 + d);
+  // host_io: the arrays are the mapped staging's (a graph of its own, so
+  // that it never needs retargeting)
   auto enqueue = [&](cudaStream_t s, cudaGraphNode_t* embed_node,
                      cudaGraphNode_t* tail_node) -> int {
-    if (host_io &&
-        cudaMemcpyAsync(m->io_dev_in, m->io_host_in, sizeof(int32_t) * n_in,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return fail(SPEC_E_CUDA, "staging copy in");
     int rc = enqueue_forward(m, n_seq, d + 1, draft, seq_ids, write_logits, s, embed_node);
     if (rc != SPEC_OK || !greedy_tail) return rc;
     GreedyRoundArgs a;
@@ -714,12 +712,7 @@ static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, cons
     a.d = d;
     a.n_slots = m->d.max_seqs;
     launch_accept_commit_greedy(a, s);
-    rc = tail_node != nullptr ? last_captured_node(s, tail_node) : SPEC_OK;
-    if (rc == SPEC_OK && host_io &&
-        cudaMemcpyAsync(m->io_host_out, m->io_dev_out, sizeof(int32_t) * n_out,
-                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
-      return fail(SPEC_E_CUDA, "staging copy out");
-    return rc;
+    return tail_node != nullptr ? last_captured_node(s, tail_node) : SPEC_OK;
   };
   if (!m->use_graphs) return enqueue(st, nullptr, nullptr);
   const long long key = ((long long)(host_io ? 1 : 0) << 40) | ((long long)n_seq << 20) |
@@ -860,8 +853,6 @@ extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* s
     }
     launch_commit(dseq, n_seq, d, D.max_seqs, m->nacc_tmp, dacc, dem, m->n_past, m->emit_idx,
                   m->anchor, m->err, st);
-    CUDA_TRY(cudaMemcpyAsync(m->io_host_out, m->io_dev_out, sizeof(int32_t) * n_seq * (2 + d),
-                             cudaMemcpyDeviceToHost, st));
   }
   CUDA_TRY(cudaStreamSynchronize(st));
   std::memcpy(n_acc, m->io_host_out, sizeof(int32_t) * n_seq);
