@@ -16,6 +16,9 @@
 // shared by all nt x group query rows of that kv head (GQA), which are
 // processed as m16 tiles with mma.sync m16n8k16: S = Q K^T, softmax in fp32
 // (log2 domain), O = P V with P as an exact hi + lo pair of fp16 operands.
+// Each half of the chunk's keys is a separate warp's (max, sum, O); the two
+// are rescaled to the common max in one fixed order inside the CTA, so the
+// chunk partial is still one (m, l, o) per row.
 #include <math.h>
 
 #include "common.cuh"
@@ -46,8 +49,16 @@ __device__ __forceinline__ uint32_t tile_off(int p, int u) {
   return (uint32_t)(p * (HD * 2) + ((u ^ (p & 7)) << 4));
 }
 
+// Shared memory of the chunk kernel: the K and V tiles, then the key-half
+// exchange slots of the WARPS / 2 warp pairs (O fragments and (m, l)).
+inline size_t chunk_smem_bytes(int hd, int ds) {
+  return 2 * (size_t)CH * hd * 2 + (size_t)(WARPS / 2) * (hd / 8 / ds + 1) * 32 * 16;
+}
+
+// (2 CTAs per SM: what the shared memory holds; the register budget
+// follows, so that the 16-block O accumulator does not spill)
 template <int HD, int DS>
-__global__ void __launch_bounds__(WARPS * 32)
+__global__ void __launch_bounds__(WARPS * 32, 2)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
                   int nt, int nq, int nkv, int max_ctx, int nchunks, float* __restrict__ part) {
@@ -105,14 +116,22 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
 
   const float sc_log2 = 1.4426950408889634f / sqrtf((float)HD);
   const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs);
-  // work items: (m tile, slice of the head dimensions); the DS warps of one
-  // m tile each compute S and P in full (the same instruction sequence) and
-  // O for HD / DS of the dimensions
+  // work items: (m tile, slice of the head dimensions, half of the chunk's
+  // keys).  The two key halves of an (m tile, slice) are consecutive warps:
+  // each computes S, its own row max and P over its 64 keys (the same
+  // instruction sequence whatever nt is), and O for HD / DS dimensions; the
+  // half-1 warp hands (m, l, O) to the half-0 warp through shared memory,
+  // which rescales both to the common max in a fixed order.
+  constexpr int KS = 2, CHK = CH / KS;
+  constexpr int DN = HD / 8 / DS;  // n8 blocks of head dimensions of a warp
+  float4* x_o = reinterpret_cast<float4*>(smem + 2 * CH * HD * 2);  // [WARPS/2][DN][32]
+  float4* x_ml = x_o + (WARPS / 2) * DN * 32;                         // [WARPS/2][32]
   const int n_mt = (M + 15) / 16;
-  const int n_items = n_mt * DS;
-  for (int it0 = 0; it0 < n_items; it0 += WARPS) {  // uniform trip count: the V barrier below
+  const int n_items = n_mt * DS * KS;
+  for (int it0 = 0; it0 < n_items; it0 += WARPS) {  // uniform trip count: the barriers below
     const int it = it0 + warp;
-    const int mt = it / DS, dh = it % DS;
+    const int kh = it % KS, dh = (it / KS) % DS, mt = it / (KS * DS);
+    const int key0 = kh * CHK;
     const int mA = mt * 16 + g, mB = mA + 8;
     const bool okA = it < n_items && mA < M, okB = it < n_items && mB < M;
     int posA = -1, posB = -1;
@@ -145,17 +164,17 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
       asm volatile("cp.async.wait_group 1;" ::: "memory");  // all of K (V's last group may fly)
       __syncthreads();
     }
-    // ---- S = Q K^T over the chunk (16 rows x CH keys)
-    float sacc[CH / 8][4];
+    // ---- S = Q K^T over the half (16 rows x CHK keys)
+    float sacc[CHK / 8][4];
 #pragma unroll
-    for (int nb = 0; nb < CH / 8; nb++)
+    for (int nb = 0; nb < CHK / 8; nb++)
 #pragma unroll
       for (int e = 0; e < 4; e++) sacc[nb][e] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < HD / 16; kk += 2) {
 #pragma unroll
-      for (int nb = 0; nb < CH / 8; nb++) {
-        const int key = 8 * nb + (lane & 7);
+      for (int nb = 0; nb < CHK / 8; nb++) {
+        const int key = key0 + 8 * nb + (lane & 7);
         const int unit = 2 * kk + (lane >> 3);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(ks_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
@@ -163,13 +182,13 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
         mma_16816(sacc[nb], qa[kk + 1], b2, b3);
       }
     }
-    // ---- mask, row max (fixed butterfly over the 4 lanes of a row)
+    // ---- mask, row max over the half (fixed butterfly over the 4 lanes of a row)
     float mxA = -INFINITY, mxB = -INFINITY;
 #pragma unroll
-    for (int nb = 0; nb < CH / 8; nb++)
+    for (int nb = 0; nb < CHK / 8; nb++)
 #pragma unroll
       for (int e = 0; e < 2; e++) {
-        const int kg = c * CH + 8 * nb + 2 * t + e;
+        const int kg = c * CH + key0 + 8 * nb + 2 * t + e;
         float va = sacc[nb][e] * sc_log2, vb = sacc[nb][2 + e] * sc_log2;
         va = kg <= posA ? va : -INFINITY;
         vb = kg <= posB ? vb : -INFINITY;
@@ -188,7 +207,7 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
     // ---- p = exp2(s - m) in fp32; l = sum of p in a fixed order
     float lA = 0.0f, lB = 0.0f;
 #pragma unroll
-    for (int nb = 0; nb < CH / 8; nb++) {
+    for (int nb = 0; nb < CHK / 8; nb++) {
       sacc[nb][0] = exp2f(sacc[nb][0] - uA);
       sacc[nb][1] = exp2f(sacc[nb][1] - uA);
       sacc[nb][2] = exp2f(sacc[nb][2] - uB);
@@ -203,14 +222,13 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
       lA += __shfl_xor_sync(0xffffffffu, lA, off);
       lB += __shfl_xor_sync(0xffffffffu, lB, off);
     }
-    // ---- O = P V (16 rows x HD dims).  P enters the fp16 MMA as an exact
-    // ---- two-term split p = hi + lo (hi = fp16(p), lo = fp16(p - hi)), so
-    // ---- the product carries ~22 bits of p instead of 11.
+    // ---- O = P V over the half (16 rows x HD / DS dims).  P enters the fp16
+    // ---- MMA as an exact two-term split p = hi + lo (hi = fp16(p), lo =
+    // ---- fp16(p - hi)), so the product carries ~22 bits of p instead of 11.
     if (it0 == 0) {
       asm volatile("cp.async.wait_group 0;" ::: "memory");  // V
       __syncthreads();
     }
-    constexpr int DN = HD / 8 / DS;  // n8 blocks of head dimensions of this warp
     const int dn0 = dh * DN;
     float oacc[DN][4];
 #pragma unroll
@@ -218,7 +236,7 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
 #pragma unroll
       for (int e = 0; e < 4; e++) oacc[dn][e] = 0.0f;
 #pragma unroll
-    for (int kk = 0; kk < CH / 16; kk++) {
+    for (int kk = 0; kk < CHK / 16; kk++) {
       uint32_t phi[4], plo[4];
 #pragma unroll
       for (int h = 0; h < 2; h++) {         // key tiles 2kk (h = 0) and 2kk+1 (h = 1)
@@ -235,7 +253,7 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
 #pragma unroll
       for (int dn = 0; dn < DN; dn += 2) {
         const int mi = lane >> 3;
-        const int key = 16 * kk + (lane & 7) + (mi & 1) * 8;
+        const int key = key0 + 16 * kk + (lane & 7) + (mi & 1) * 8;
         const int unit = dn0 + dn + (mi >> 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vs_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
@@ -245,24 +263,50 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
         mma_16816(oacc[dn + 1], plo, b2, b3);
       }
     }
-    // ---- partials: part[s][kvh][c][m] = (o[HD], m, l)
-    const size_t base = (((size_t)s * nkv + kvh) * nchunks + c) * (size_t)Mmax_stride;
-    if (okA) {
-      float* dst = part + (base + mA) * (HD + 2) + 8 * dn0;
+    // ---- the two halves: half 1 hands over, half 0 combines
+    const int pr = warp >> 1;  // the pair's exchange slot
+    if (kh == 1 && it < n_items) {
 #pragma unroll
       for (int dn = 0; dn < DN; dn++)
-        *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][0], oacc[dn][1]);
-      if (t == 0 && dh == 0)
-        *reinterpret_cast<float2*>(part + (base + mA) * (HD + 2) + HD) = make_float2(mxA, lA);
+        x_o[(pr * DN + dn) * 32 + lane] = make_float4(oacc[dn][0], oacc[dn][1], oacc[dn][2], oacc[dn][3]);
+      x_ml[pr * 32 + lane] = make_float4(mxA, mxB, lA, lB);
     }
-    if (okB) {
-      float* dst = part + (base + mB) * (HD + 2) + 8 * dn0;
+    __syncthreads();
+    if (kh == 0 && it < n_items) {
+      const float4 ml = x_ml[pr * 32 + lane];
+      const float mA2 = fmaxf(mxA, ml.x), mB2 = fmaxf(mxB, ml.y);
+      const float vA = mA2 == -INFINITY ? 0.0f : mA2, vB = mB2 == -INFINITY ? 0.0f : mB2;
+      const float wA0 = exp2f(mxA - vA), wA1 = exp2f(ml.x - vA);
+      const float wB0 = exp2f(mxB - vB), wB1 = exp2f(ml.y - vB);
+      const float lA2 = fmaf(ml.z, wA1, lA * wA0), lB2 = fmaf(ml.w, wB1, lB * wB0);
 #pragma unroll
-      for (int dn = 0; dn < DN; dn++)
-        *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][2], oacc[dn][3]);
-      if (t == 0 && dh == 0)
-        *reinterpret_cast<float2*>(part + (base + mB) * (HD + 2) + HD) = make_float2(mxB, lB);
+      for (int dn = 0; dn < DN; dn++) {
+        const float4 o1 = x_o[(pr * DN + dn) * 32 + lane];
+        oacc[dn][0] = fmaf(o1.x, wA1, oacc[dn][0] * wA0);
+        oacc[dn][1] = fmaf(o1.y, wA1, oacc[dn][1] * wA0);
+        oacc[dn][2] = fmaf(o1.z, wB1, oacc[dn][2] * wB0);
+        oacc[dn][3] = fmaf(o1.w, wB1, oacc[dn][3] * wB0);
+      }
+      // ---- partials: part[s][kvh][c][m] = (o[HD], m, l)
+      const size_t base = (((size_t)s * nkv + kvh) * nchunks + c) * (size_t)Mmax_stride;
+      if (okA) {
+        float* dst = part + (base + mA) * (HD + 2) + 8 * dn0;
+#pragma unroll
+        for (int dn = 0; dn < DN; dn++)
+          *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][0], oacc[dn][1]);
+        if (t == 0 && dh == 0)
+          *reinterpret_cast<float2*>(part + (base + mA) * (HD + 2) + HD) = make_float2(mA2, lA2);
+      }
+      if (okB) {
+        float* dst = part + (base + mB) * (HD + 2) + 8 * dn0;
+#pragma unroll
+        for (int dn = 0; dn < DN; dn++)
+          *reinterpret_cast<float2*>(dst + 8 * dn + 2 * t) = make_float2(oacc[dn][2], oacc[dn][3]);
+        if (t == 0 && dh == 0)
+          *reinterpret_cast<float2*>(part + (base + mB) * (HD + 2) + HD) = make_float2(mB2, lB2);
+      }
     }
+    __syncthreads();  // the exchange slots are reused by the next items
   }
 }
 
@@ -354,12 +398,11 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
   cfg.numAttrs = programmatic_launch() ? 1 : 0;
   cfg.gridDim = dim3(nchunks, nkv, n_seq);
   cfg.blockDim = dim3(WARPS * 32);
-  cfg.dynamicSmemBytes = 2 * (size_t)CH * HD * 2;
-  // split the head dimensions of an m tile across warps while there are
-  // fewer m tiles than warps (the bits of every output do not depend on it)
+  // split the head dimensions of an m tile across warp pairs while there
+  // is one m tile (the bits of every output do not depend on it)
   const int n_mt = (nt * (nq / nkv) + 15) / 16;
-  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 4>
-                         : (n_mt == 2 ? attn_chunk_kernel<HD, 2> : attn_chunk_kernel<HD, 1>);
+  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2> : attn_chunk_kernel<HD, 1>;
+  cfg.dynamicSmemBytes = n_mt == 1 ? chunk_smem_bytes(HD, 2) : chunk_smem_bytes(HD, 1);
   cudaError_t e = cudaLaunchKernelEx(&cfg, chunk, q, kcache, vcache, rows, nt, nq, nkv, max_ctx,
                                      nchunks, part);
   if (e == cudaSuccess) {
@@ -391,10 +434,8 @@ int attn_launch(const __half* q, const __half* kcache, const __half* vcache,
 }
 
 void attn_init_attrs() {
-  cudaFuncSetAttribute(attn_chunk_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 128 * 2);
-  cudaFuncSetAttribute(attn_chunk_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 128 * 2);
-  cudaFuncSetAttribute(attn_chunk_kernel<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 128 * 2);
-  cudaFuncSetAttribute(attn_chunk_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 64 * 2);
-  cudaFuncSetAttribute(attn_chunk_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 64 * 2);
-  cudaFuncSetAttribute(attn_chunk_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * CH * 64 * 2);
+  cudaFuncSetAttribute(attn_chunk_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(128, 1));
+  cudaFuncSetAttribute(attn_chunk_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(128, 2));
+  cudaFuncSetAttribute(attn_chunk_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(64, 1));
+  cudaFuncSetAttribute(attn_chunk_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(64, 2));
 }

@@ -48,21 +48,15 @@ __global__ void embed_kernel(const EmbedArgs a) {
   const int r = blockIdx.x;
   const int s = r / a.nt, i = r % a.nt;
   __shared__ int s_tok;
+  // the same record as row_info, with the loads in two dependent levels:
+  // (slot, draft token), then (position, anchor); the token is published
+  // first so that the row copy does not wait for the record
+  int slot = 0, raw = 0;
   if (threadIdx.x == 0) {
-    // the same record as row_info, with the loads in two dependent levels:
-    // (slot, draft token), then (position, anchor)
-    const int raw = a.seq_ids[s];
+    raw = a.seq_ids[s];
     const int dtok = i > 0 ? a.draft[s * (a.nt - 1) + (i - 1)] : 0;
-    const int slot = raw < 0 || raw >= a.max_seqs ? 0 : raw;
-    const int np = a.n_past[slot];
+    slot = raw < 0 || raw >= a.max_seqs ? 0 : raw;
     int tok = i == 0 ? a.anchor[slot] : dtok;
-    if (slot != raw) atomicOr(a.err, ERR_SEQ);
-    int pos = np + i;
-    if (pos < 0 || pos >= a.max_ctx) {
-      atomicOr(a.err, ERR_POS);
-      pos = a.max_ctx;
-    }
-    a.rows[r] = RowInfo{slot, pos};
     if (tok < 0 || tok >= a.V) {
       atomicOr(a.err, ERR_TOKEN);
       tok = 0;
@@ -71,6 +65,15 @@ __global__ void embed_kernel(const EmbedArgs a) {
     a.tokens[r] = tok;
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    if (slot != raw) atomicOr(a.err, ERR_SEQ);
+    int pos = a.n_past[slot] + i;
+    if (pos < 0 || pos >= a.max_ctx) {
+      atomicOr(a.err, ERR_POS);
+      pos = a.max_ctx;
+    }
+    a.rows[r] = RowInfo{slot, pos};
+  }
   const __half2* src = reinterpret_cast<const __half2*>(a.embed + (size_t)s_tok * a.H);
   float2* dst = reinterpret_cast<float2*>(a.h + (size_t)r * a.H);
   for (int j = threadIdx.x; j < a.H / 2; j += blockDim.x) dst[j] = __half22float2(src[j]);
