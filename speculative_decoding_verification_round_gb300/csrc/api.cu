@@ -634,8 +634,10 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
   const spec_model_desc& D = m->d;
   const int R = n_seq * nt, H = D.hidden, F = D.ffn, hd = D.head_dim, nq = D.n_q_heads,
             nkv = D.n_kv_heads, V = D.vocab;
+  // the first RMSNorm runs inside the embedding kernel, the others as
+  // their own kernels
   launch_embed_rows(m->embed, V, H, m->anchor, draft, seq_ids, n_seq, nt, m->n_past, D.max_seqs,
-                    D.max_ctx, m->rows, m->tokens, m->h, m->err, st);
+                    D.max_ctx, m->rows, m->tokens, m->h, m->norm_w, D.rms_eps, m->xa, m->err, st);
   if (embed_node != nullptr) {
     const int rc = last_captured_node(st, embed_node);
     if (rc != SPEC_OK) return rc;
@@ -643,7 +645,8 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
   for (int l = 0; l < D.n_layers; l++) {
     __half* kc = m->kc + m->layer_elems * l;
     __half* vc = m->vc + m->layer_elems * l;
-    launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * l) * H, R, H, D.rms_eps, m->xa, st);
+    if (l > 0)
+      launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * l) * H, R, H, D.rms_eps, m->xa, st);
     LinEpi eq;
     eq.kind = EPI_QKV;
     eq.out16 = m->qbuf;
@@ -676,7 +679,8 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
     rc = linear_launch(m->wd[l], m->xs, R, er, m->lscr, st);
     if (rc) return rc;
   }
-  launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * D.n_layers) * H, R, H, D.rms_eps, m->xa, st);
+  if (D.n_layers > 0)
+    launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * D.n_layers) * H, R, H, D.rms_eps, m->xa, st);
   LinEpi el;
   el.kind = EPI_LMHEAD;
   el.y = write_logits ? m->logits : nullptr;

@@ -132,13 +132,17 @@ struct EmbedArgs {
   int32_t* tokens;         // [n_seq * nt]
   float* h;                // [n_seq * nt][H]
   uint32_t* err;
+  const float* gamma;  // the first RMSNorm's gains [H]
+  __half* xn;          // its output [n_seq * nt][H]
+  float eps;
   int V, H, nt, max_seqs, max_ctx;
 };
+// Embedding rows into h and, fused, the first RMSNorm of h into xn.
 void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
                        const int32_t* draft, const int32_t* seq_ids, int n_seq,
                        int nt, const int32_t* n_past, int max_seqs, int max_ctx,
-                       RowInfo* rows, int32_t* tokens, float* h, uint32_t* err,
-                       cudaStream_t st);
+                       RowInfo* rows, int32_t* tokens, float* h, const float* gamma,
+                       float eps, __half* xn, uint32_t* err, cudaStream_t st);
 // Points the embedding node of an instantiated graph (captured from
 // launch_embed_rows) at new draft and sequence-id arrays; the other arguments
 // keep their captured values.

@@ -40,10 +40,11 @@ __global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, 
   rows[r] = row_info(seq_ids, r, nt, n_past, max_seqs, max_ctx, err);
 }
 
-// One CTA per verify row: the row's (slot, position) record, token lookup
-// (anchor for row 0, drafts after), id check, fp16 -> fp32 copy of the
-// embedding row.  The arguments travel as one struct so that a captured
-// launch can be pointed at a new round's draft and sequence-id arrays.
+// One CTA (256 threads) per verify row: the row's (slot, position) record,
+// token lookup (anchor for row 0, drafts after), id check, fp16 -> fp32 copy
+// of the embedding row, and the first RMSNorm of the row.  The arguments
+// travel as one struct so that a captured launch can be pointed at a new
+// round's draft and sequence-id arrays.
 __global__ void embed_kernel(const EmbedArgs a) {
   const int r = blockIdx.x;
   const int s = r / a.nt, i = r % a.nt;
@@ -74,9 +75,46 @@ __global__ void embed_kernel(const EmbedArgs a) {
     }
     a.rows[r] = RowInfo{slot, pos};
   }
-  const __half2* src = reinterpret_cast<const __half2*>(a.embed + (size_t)s_tok * a.H);
-  float2* dst = reinterpret_cast<float2*>(a.h + (size_t)r * a.H);
-  for (int j = threadIdx.x; j < a.H / 2; j += blockDim.x) dst[j] = __half22float2(src[j]);
+  // the row into h, then the first RMSNorm of it into xn: the sum of squares
+  // in rmsnorm_kernel's order (thread-strided float4 partials, warp
+  // butterfly, warps in order), so the result is that kernel's, bit for bit
+  const uint2* src = reinterpret_cast<const uint2*>(a.embed + (size_t)s_tok * a.H);
+  float4* dst = reinterpret_cast<float4*>(a.h + (size_t)r * a.H);
+  float ss = 0.0f;
+  for (int j = threadIdx.x; j < a.H / 4; j += 256) {
+    const uint2 u = src[j];
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
+    dst[j] = v;
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  __shared__ float s_part[8];
+  __shared__ float s_inv;
+  if ((threadIdx.x & 31) == 0) s_part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.0f;
+    for (int w = 0; w < 8; w++) tot += s_part[w];
+    s_inv = 1.0f / sqrtf(tot / (float)a.H + a.eps);
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  const float4* gm = reinterpret_cast<const float4*>(a.gamma);
+  __half2* o = reinterpret_cast<__half2*>(a.xn + (size_t)r * a.H);
+  for (int j = threadIdx.x; j < a.H / 4; j += 256) {
+    const uint2 u = src[j];
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    const float4 gg = gm[j];
+    o[2 * j] = __floats2half2_rn(lo.x * inv * gg.x, lo.y * inv * gg.y);
+    o[2 * j + 1] = __floats2half2_rn(hi.x * inv * gg.z, hi.y * inv * gg.w);
+  }
 }
 
 // One CTA (256 threads) per row.  The sum of squares is reduced in a fixed
@@ -160,7 +198,8 @@ void launch_row_info(const int32_t* seq_ids, int n_seq, int nt, const int32_t* n
 void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
                        const int32_t* draft, const int32_t* seq_ids, int n_seq, int nt,
                        const int32_t* n_past, int max_seqs, int max_ctx, RowInfo* rows,
-                       int32_t* tokens, float* h, uint32_t* err, cudaStream_t st) {
+                       int32_t* tokens, float* h, const float* gamma, float eps, __half* xn,
+                       uint32_t* err, cudaStream_t st) {
   EmbedArgs a;
   a.embed = embed;
   a.anchor = anchor;
@@ -171,6 +210,9 @@ void launch_embed_rows(const __half* embed, int V, int H, const int32_t* anchor,
   a.tokens = tokens;
   a.h = h;
   a.err = err;
+  a.gamma = gamma;
+  a.xn = xn;
+  a.eps = eps;
   a.V = V;
   a.H = H;
   a.nt = nt;
