@@ -433,8 +433,9 @@ def run_ours(args):
         sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
         rsweep = round_sweep(sv, m, wl, dev) if not args.no_sweep else None
         n_layers = wl["n_layers"]
-        # embed, 8 per layer, final norm + LM head, fused accept + commit
-        launches_per_round = 1 + 8 * n_layers + 2 + 1
+        # embed (with the first norm), 8 per layer but the first layer's
+        # norm, final norm + LM head, fused accept + commit
+        launches_per_round = 1 + 8 * n_layers - 1 + 2 + 1
         weight_bytes = sum(p["N"] * p["K"] * (0.5625 if p["qtype"] == 4 else 0.8125) *
                            (n_layers if p["qtype"] == 4 else 1) for p in per)
         kv_bytes = n_layers * wl["n_kv_heads"] * (wl["ctx"] + d) * wl["head_dim"] * 2 * 2
