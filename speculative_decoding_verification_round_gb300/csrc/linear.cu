@@ -41,7 +41,14 @@ namespace {
 constexpr int WARPS = 8;     // warps per CTA
 constexpr int TPW = 2;       // tiles (of 16 rows) per warp: one pair
 constexpr int NS = 2;        // weight-ring stages per warp
-constexpr int CPS = 3;       // chunks per ring stage (consecutive records: one copy, one wait)
+// Chunks per ring stage (consecutive records: one copy, one wait) and the
+// CTAs per SM the register budget is set for, by the number of column tiles.
+// Two column tiles need ~110 registers (2 CTAs per SM); their shorter stages
+// keep the shared memory of a Q6 LM-head CTA low enough for 2 per SM too.
+template <int NCT>
+constexpr int cps() { return NCT == 1 ? 3 : 2; }
+template <int NCT>
+constexpr int min_blocks() { return NCT == 1 ? 3 : 2; }
 constexpr int NC_CTA_MAX = 64;  // chunks of one CTA's K range (its staged activation slice)
 constexpr int MAX_SPLIT = 64;
 
@@ -54,13 +61,14 @@ struct Rec {
   static constexpr int QH = SC + TPW * 64;            // 2 x 256 B (Q6)
   static constexpr int BYTES = QH + (QT == 6 ? TPW * 256 : 0);  // 1152 / 1664
 };
-template <int QT>
-constexpr int ring_bytes() { return WARPS * NS * CPS * Rec<QT>::BYTES; }
+inline int ring_bytes(int qtype, int nct) {
+  return WARPS * NS * (nct == 1 ? cps<1>() : cps<2>()) * (qtype == 4 ? Rec<4>::BYTES : Rec<6>::BYTES);
+}
 // Staged activation row: the CTA's K range plus 64 bytes, so that the rows
 // g = 0..7 of a fragment load fall in distinct shared-memory banks.
 inline int x_stride(int nc) { return nc * 128 + 64; }
 inline int smem_bytes(int qtype, int nct, int nc) {
-  return (qtype == 4 ? ring_bytes<4>() : ring_bytes<6>()) + 8 * nct * x_stride(nc);
+  return ring_bytes(qtype, nct) + 8 * nct * x_stride(nc);
 }
 
 // ---------------------------------------------------------------------------
@@ -433,11 +441,10 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
   }
 }
 
-// Register budget: 3 CTAs per SM with one column tile (at most 80
-// registers; the shared memory never holds more than 3 CTAs either), 2 with
-// two (their accumulators and activation fragments need about 110).
+// Register budget: min_blocks<NCT>() CTAs per SM (one column tile: at most
+// 80 registers, and the shared memory never holds more than 3 CTAs either).
 template <int QT, int NCT, int KW>
-__global__ void __launch_bounds__(WARPS * 32, NCT == 1 ? 3 : 2)
+__global__ void __launch_bounds__(WARPS * 32, min_blocks<NCT>())
 linear_q_kernel(const LinArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   using RC = Rec<QT>;
@@ -459,10 +466,11 @@ linear_q_kernel(const LinArgs a) {
   const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c_begin;
   const int w_lo = ks * nc / KW;
   const int wn = (ks + 1) * nc / KW - w_lo;
+  constexpr int CPS = cps<NCT>();
   constexpr int SB = CPS * RC::BYTES;  // bytes of a full stage
   unsigned char* ring = smem + warp * NS * SB;
   const uint32_t ring_s = smem_addr(ring);
-  unsigned char* xs = smem + ring_bytes<QT>();
+  unsigned char* xs = smem + WARPS * NS * SB;
   const uint32_t bar0 = smem_addr(&s_bar[warp][0]);
   const uint32_t xbar = smem_addr(&s_xbar);
 
