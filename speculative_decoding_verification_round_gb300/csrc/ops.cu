@@ -46,6 +46,7 @@ __global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, 
 // travel as one struct so that a captured launch can be pointed at a new
 // round's draft and sequence-id arrays.
 __global__ void embed_kernel(const EmbedArgs a) {
+  grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
   const int r = blockIdx.x;
   const int s = r / a.nt, i = r % a.nt;
   __shared__ int s_tok;
