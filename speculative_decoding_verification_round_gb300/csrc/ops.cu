@@ -11,6 +11,9 @@
 
 namespace {
 
+// Rows of up to NORM_REG_VEC * 1024 values are normalised from registers.
+constexpr int NORM_REG_VEC = 8;
+
 // Row r = (sequence s, offset i): the sequence's slot (checked) and the
 // row's absolute position n_past[slot] + i (checked against max_ctx; an
 // invalid position becomes max_ctx, where consumers write nothing).
@@ -78,20 +81,48 @@ __global__ void embed_kernel(const EmbedArgs a) {
   }
   // the row into h, then the first RMSNorm of it into xn: the sum of squares
   // in rmsnorm_kernel's order (thread-strided float4 partials, warp
-  // butterfly, warps in order), so the result is that kernel's, bit for bit
+  // butterfly, warps in order), so the result is that kernel's, bit for bit;
+  // a row of up to NORM_REG_VEC * 1024 values and its gains stay in registers
   const uint2* src = reinterpret_cast<const uint2*>(a.embed + (size_t)s_tok * a.H);
   float4* dst = reinterpret_cast<float4*>(a.h + (size_t)r * a.H);
+  const float4* gm = reinterpret_cast<const float4*>(a.gamma);
+  const int H4 = a.H / 4;
+  const bool in_regs = H4 <= NORM_REG_VEC * 256;
+  auto load = [&](int j) {
+    const uint2 w = src[j];
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  };
+  float4 v[NORM_REG_VEC], gg[NORM_REG_VEC];
   float ss = 0.0f;
-  for (int j = threadIdx.x; j < a.H / 4; j += 256) {
-    const uint2 u = src[j];
-    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    const float4 v = make_float4(lo.x, lo.y, hi.x, hi.y);
-    dst[j] = v;
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < NORM_REG_VEC; u++) {
+      const int j = threadIdx.x + 256 * u;
+      if (j < H4) {
+        v[u] = load(j);
+        gg[u] = gm[j];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NORM_REG_VEC; u++)
+      if (threadIdx.x + 256 * u < H4) {
+        dst[threadIdx.x + 256 * u] = v[u];
+        ss = fmaf(v[u].x, v[u].x, ss);
+        ss = fmaf(v[u].y, v[u].y, ss);
+        ss = fmaf(v[u].z, v[u].z, ss);
+        ss = fmaf(v[u].w, v[u].w, ss);
+      }
+  } else {
+    for (int j = threadIdx.x; j < H4; j += 256) {
+      const float4 b = load(j);
+      dst[j] = b;
+      ss = fmaf(b.x, b.x, ss);
+      ss = fmaf(b.y, b.y, ss);
+      ss = fmaf(b.z, b.z, ss);
+      ss = fmaf(b.w, b.w, ss);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -106,35 +137,65 @@ __global__ void embed_kernel(const EmbedArgs a) {
   }
   __syncthreads();
   const float inv = s_inv;
-  const float4* gm = reinterpret_cast<const float4*>(a.gamma);
   __half2* o = reinterpret_cast<__half2*>(a.xn + (size_t)r * a.H);
-  for (int j = threadIdx.x; j < a.H / 4; j += 256) {
-    const uint2 u = src[j];
-    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    const float4 gg = gm[j];
-    o[2 * j] = __floats2half2_rn(lo.x * inv * gg.x, lo.y * inv * gg.y);
-    o[2 * j + 1] = __floats2half2_rn(hi.x * inv * gg.z, hi.y * inv * gg.w);
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < NORM_REG_VEC; u++) {
+      const int j = threadIdx.x + 256 * u;
+      if (j < H4) {
+        o[2 * j] = __floats2half2_rn(v[u].x * inv * gg[u].x, v[u].y * inv * gg[u].y);
+        o[2 * j + 1] = __floats2half2_rn(v[u].z * inv * gg[u].z, v[u].w * inv * gg[u].w);
+      }
+    }
+  } else {
+    for (int j = threadIdx.x; j < H4; j += 256) {
+      const float4 b = load(j), c = gm[j];
+      o[2 * j] = __floats2half2_rn(b.x * inv * c.x, b.y * inv * c.y);
+      o[2 * j + 1] = __floats2half2_rn(b.z * inv * c.z, b.w * inv * c.w);
+    }
   }
 }
 
 // One CTA (256 threads) per row.  The sum of squares is reduced in a fixed
 // order (thread-strided partials, warp butterfly, then warps in order), so a
-// row's result does not depend on the other rows in the batch.
+// row's result does not depend on the other rows in the batch.  A row of up
+// to NORM_REG_VEC * 1024 values stays in registers between the two passes,
+// its gains loaded before the reduction (one round trip to memory).
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ h,
                                                       const float* __restrict__ gamma,
                                                       int H, float eps,
                                                       __half* __restrict__ out) {
   grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
   const int r = blockIdx.x;
+  const int H4 = H / 4;
   const float4* x = reinterpret_cast<const float4*>(h + (size_t)r * H);
+  const float4* gm = reinterpret_cast<const float4*>(gamma);
+  const bool in_regs = H4 <= NORM_REG_VEC * 256;
+  float4 v[NORM_REG_VEC], gg[NORM_REG_VEC];
   float ss = 0.0f;
-  for (int j = threadIdx.x; j < H / 4; j += 256) {
-    float4 v = x[j];
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < NORM_REG_VEC; u++) {
+      const int j = threadIdx.x + 256 * u;
+      v[u] = j < H4 ? x[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      gg[u] = j < H4 ? gm[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < NORM_REG_VEC; u++)
+      if (threadIdx.x + 256 * u < H4) {
+        ss = fmaf(v[u].x, v[u].x, ss);
+        ss = fmaf(v[u].y, v[u].y, ss);
+        ss = fmaf(v[u].z, v[u].z, ss);
+        ss = fmaf(v[u].w, v[u].w, ss);
+      }
+  } else {
+    for (int j = threadIdx.x; j < H4; j += 256) {
+      const float4 a = x[j];
+      ss = fmaf(a.x, a.x, ss);
+      ss = fmaf(a.y, a.y, ss);
+      ss = fmaf(a.z, a.z, ss);
+      ss = fmaf(a.w, a.w, ss);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -149,12 +210,22 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
   }
   __syncthreads();
   const float inv = s_inv;
-  const float4* gm = reinterpret_cast<const float4*>(gamma);
   __half2* o = reinterpret_cast<__half2*>(out + (size_t)r * H);
-  for (int j = threadIdx.x; j < H / 4; j += 256) {
-    float4 v = x[j], gg = gm[j];
-    o[2 * j] = __floats2half2_rn(v.x * inv * gg.x, v.y * inv * gg.y);
-    o[2 * j + 1] = __floats2half2_rn(v.z * inv * gg.z, v.w * inv * gg.w);
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < NORM_REG_VEC; u++) {
+      const int j = threadIdx.x + 256 * u;
+      if (j < H4) {
+        o[2 * j] = __floats2half2_rn(v[u].x * inv * gg[u].x, v[u].y * inv * gg[u].y);
+        o[2 * j + 1] = __floats2half2_rn(v[u].z * inv * gg[u].z, v[u].w * inv * gg[u].w);
+      }
+    }
+  } else {
+    for (int j = threadIdx.x; j < H4; j += 256) {
+      const float4 a = x[j], b = gm[j];
+      o[2 * j] = __floats2half2_rn(a.x * inv * b.x, a.y * inv * b.y);
+      o[2 * j + 1] = __floats2half2_rn(a.z * inv * b.z, a.w * inv * b.w);
+    }
   }
 }
 
