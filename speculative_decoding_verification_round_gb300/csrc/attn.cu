@@ -26,7 +26,7 @@
 namespace {
 
 constexpr int CH = ATTN_CHUNK;
-constexpr int WARPS = 4;
+constexpr int KS = 2;  // key halves of a chunk (one warp each)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -49,22 +49,38 @@ __device__ __forceinline__ uint32_t tile_off(int p, int u) {
   return (uint32_t)(p * (HD * 2) + ((u ^ (p & 7)) << 4));
 }
 
-// Shared memory of the chunk kernel: the K and V tiles, then the key-half
-// exchange slots of the WARPS / 2 warp pairs (O fragments and (m, l)).
-inline size_t chunk_smem_bytes(int hd, int ds) {
-  return 2 * (size_t)CH * hd * 2 + (size_t)(WARPS / 2) * (hd / 8 / ds + 1) * 32 * 16;
+// Shared memory of the chunk kernel: the K tile, the q rows of its m tiles,
+// the V tile, then -- unless they fit over K and q, which no warp reads any
+// more once every work item is in one round -- the key-half exchange slots
+// of the NW / 2 warp pairs (O fragments and (m, l)).
+struct ChunkSmem {
+  size_t q_off, v_off, slot_off, bytes;
+};
+inline ChunkSmem chunk_smem(int hd, int ds, int nw, int n_mt) {
+  ChunkSmem c;
+  const size_t kbytes = (size_t)CH * hd * 2, qbytes = (size_t)n_mt * 16 * hd * 2;
+  const size_t slots = (size_t)(nw / 2) * (hd / 8 / ds + 1) * 32 * 16;
+  const bool one_round = n_mt * ds * KS <= nw;
+  c.q_off = kbytes;
+  c.v_off = kbytes + qbytes;
+  const bool alias = one_round && slots <= kbytes + qbytes;
+  c.slot_off = alias ? 0 : c.v_off + kbytes;
+  c.bytes = c.v_off + kbytes + (alias ? 0 : slots);
+  return c;
 }
 
-// (2 CTAs per SM: what the shared memory holds; the register budget
-// follows, so that the 16-block O accumulator does not spill)
-template <int HD, int DS>
-__global__ void __launch_bounds__(WARPS * 32, 2)
+// 2 CTAs per SM (what the shared memory holds); with 8 warps that caps the
+// registers at 128, which the q fragments read from shared memory allow.
+template <int HD, int DS, int NW>
+__global__ void __launch_bounds__(NW * 32, 2)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
-                  int nt, int nq, int nkv, int max_ctx, int nchunks, float* __restrict__ part) {
+                  int nt, int nq, int nkv, int max_ctx, int nchunks, ChunkSmem lay,
+                  float* __restrict__ part) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* Ks = smem;
-  unsigned char* Vs = smem + CH * HD * 2;
+  unsigned char* Qs = smem + lay.q_off;
+  unsigned char* Vs = smem + lay.v_off;
   const int c = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
   const int G = nq / nkv, M = nt * G, Mmax_stride = M;  // rows of this (seq, kv head)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -85,7 +101,7 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   // ---- before the grid dependency resolves, the round's new rows after it;
   // ---- K and V in separate copy groups so that S = Q K^T can start first
   constexpr int UNITS = HD / 8;              // 16-byte units per row
-  constexpr int RP = WARPS * 32 / UNITS;      // rows per pass of the CTA
+  constexpr int RP = NW * 32 / UNITS;         // rows per pass of the CTA
   const int u = threadIdx.x % UNITS, p0 = threadIdx.x / UNITS;
   const size_t head_base = ((size_t)slot * nkv + kvh) * max_ctx;
   // a thread copies unit u of the rows p0, p0 + RP, ...: its swizzled column
@@ -111,59 +127,62 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   stage(Vs, vcache, true);
   grid_dep_wait();
   stage(Ks, kcache, false);
+  // the q rows of the CTA's m tiles (row m = query i * G + gh), swizzled like
+  // the cache tiles; rows past M are zero
+  const int n_mt = (M + 15) / 16;
+  {
+    const uint32_t qs0 = smem_u32(Qs);
+    for (int e = threadIdx.x; e < n_mt * 16 * UNITS; e += NW * 32) {
+      const int m = e / UNITS, uu = e % UNITS;
+      const uint32_t so = qs0 + tile_off<HD>(m, uu);
+      if (m < M) {
+        const __half* src = q + ((size_t)(s * nt + m / G) * nq + kvh * G + m % G) * HD + uu * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(so), "l"(src));
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(so), "r"(0));
+      }
+    }
+    asm volatile("cp.async.commit_group;");
+  }
   stage(Vs, vcache, false);
   grid_dep_launch();
 
   const float sc_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs);
+  const uint32_t ks_base = smem_u32(Ks), vs_base = smem_u32(Vs), qs_base = smem_u32(Qs);
   // work items: (m tile, slice of the head dimensions, half of the chunk's
   // keys).  The two key halves of an (m tile, slice) are consecutive warps:
   // each computes S, its own row max and P over its 64 keys (the same
   // instruction sequence whatever nt is), and O for HD / DS dimensions; the
   // half-1 warp hands (m, l, O) to the half-0 warp through shared memory,
   // which rescales both to the common max in a fixed order.
-  constexpr int KS = 2, CHK = CH / KS;
+  constexpr int CHK = CH / KS;
   constexpr int DN = HD / 8 / DS;  // n8 blocks of head dimensions of a warp
-  float4* x_o = reinterpret_cast<float4*>(smem + 2 * CH * HD * 2);  // [WARPS/2][DN][32]
-  float4* x_ml = x_o + (WARPS / 2) * DN * 32;                         // [WARPS/2][32]
-  const int n_mt = (M + 15) / 16;
+  float4* x_o = reinterpret_cast<float4*>(smem + lay.slot_off);  // [NW/2][DN][32]
+  float4* x_ml = x_o + (NW / 2) * DN * 32;                        // [NW/2][32]
   const int n_items = n_mt * DS * KS;
-  for (int it0 = 0; it0 < n_items; it0 += WARPS) {  // uniform trip count: the barriers below
+  for (int it0 = 0; it0 < n_items; it0 += NW) {  // uniform trip count: the barriers below
     const int it = it0 + warp;
     const int kh = it % KS, dh = (it / KS) % DS, mt = it / (KS * DS);
     const int key0 = kh * CHK;
     const int mA = mt * 16 + g, mB = mA + 8;
     const bool okA = it < n_items && mA < M, okB = it < n_items && mB < M;
     int posA = -1, posB = -1;
-    const __half* qA = nullptr;
-    const __half* qB = nullptr;
     if (okA) {
-      const int i = mA / G, gh = mA % G;
-      const RowInfo ri = rows[s * nt + i];
+      const RowInfo ri = rows[s * nt + mA / G];
       posA = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
-      qA = q + ((size_t)(s * nt + i) * nq + kvh * G + gh) * HD;
     }
     if (okB) {
-      const int i = mB / G, gh = mB % G;
-      const RowInfo ri = rows[s * nt + i];
+      const RowInfo ri = rows[s * nt + mB / G];
       posB = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
-      qB = q + ((size_t)(s * nt + i) * nq + kvh * G + gh) * HD;
-    }
-    // ---- the q fragments of all k16 steps in one batch of loads (they
-    // ---- overlap the K copies of the first item)
-    uint32_t qa[HD / 16][4];
-#pragma unroll
-    for (int k = 0; k < HD / 16; k++) {
-      const int d0 = 16 * k + 2 * t;
-      qa[k][0] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0) : 0u;
-      qa[k][1] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0) : 0u;
-      qa[k][2] = okA ? *reinterpret_cast<const uint32_t*>(qA + d0 + 8) : 0u;
-      qa[k][3] = okB ? *reinterpret_cast<const uint32_t*>(qB + d0 + 8) : 0u;
     }
     if (it0 == 0) {
-      asm volatile("cp.async.wait_group 1;" ::: "memory");  // all of K (V's last group may fly)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // K and q (V's last group may fly)
       __syncthreads();
     }
+    // the q fragment rows of this m tile for ldmatrix: lanes 0-7 rows 0-7,
+    // 8-15 rows 8-15 (first 8 dims of a k16 step), 16-31 the same rows for
+    // its second 8 dims
+    const int q_row = min(mt, n_mt - 1) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     // ---- S = Q K^T over the half (16 rows x CHK keys)
     float sacc[CHK / 8][4];
 #pragma unroll
@@ -172,14 +191,18 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
       for (int e = 0; e < 4; e++) sacc[nb][e] = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < HD / 16; kk += 2) {
+      uint32_t qa0[4], qa1[4];
+      ldsm_x4(qs_base + tile_off<HD>(q_row, 2 * kk + (lane >> 4)), qa0[0], qa0[1], qa0[2], qa0[3]);
+      ldsm_x4(qs_base + tile_off<HD>(q_row, 2 * kk + 2 + (lane >> 4)), qa1[0], qa1[1], qa1[2],
+              qa1[3]);
 #pragma unroll
       for (int nb = 0; nb < CHK / 8; nb++) {
         const int key = key0 + 8 * nb + (lane & 7);
         const int unit = 2 * kk + (lane >> 3);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(ks_base + tile_off<HD>(key, unit), b0, b1, b2, b3);
-        mma_16816(sacc[nb], qa[kk], b0, b1);
-        mma_16816(sacc[nb], qa[kk + 1], b2, b3);
+        mma_16816(sacc[nb], qa0, b0, b1);
+        mma_16816(sacc[nb], qa1, b2, b3);
       }
     }
     // ---- mask, row max over the half (fixed butterfly over the 4 lanes of a row)
@@ -397,14 +420,18 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
   cfg.attrs = at;
   cfg.numAttrs = programmatic_launch() ? 1 : 0;
   cfg.gridDim = dim3(nchunks, nkv, n_seq);
-  cfg.blockDim = dim3(WARPS * 32);
-  // split the head dimensions of an m tile across warp pairs while there
-  // is one m tile (the bits of every output do not depend on it)
+  // one m tile: warp pairs also split the head dimensions (4 warps); two m
+  // tiles: 4 warps; more: 8 warps, so that 4 m tiles are still one round of
+  // work items (the bits of every output depend on none of these choices)
   const int n_mt = (nt * (nq / nkv) + 15) / 16;
-  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2> : attn_chunk_kernel<HD, 1>;
-  cfg.dynamicSmemBytes = n_mt == 1 ? chunk_smem_bytes(HD, 2) : chunk_smem_bytes(HD, 1);
+  const int ds = n_mt == 1 ? 2 : 1, nw = n_mt <= 2 ? 4 : 8;
+  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2, 4>
+                         : (n_mt == 2 ? attn_chunk_kernel<HD, 1, 4> : attn_chunk_kernel<HD, 1, 8>);
+  const ChunkSmem lay = chunk_smem(HD, ds, nw, n_mt);
+  cfg.blockDim = dim3(nw * 32);
+  cfg.dynamicSmemBytes = lay.bytes;
   cudaError_t e = cudaLaunchKernelEx(&cfg, chunk, q, kcache, vcache, rows, nt, nq, nkv, max_ctx,
-                                     nchunks, part);
+                                     nchunks, lay, part);
   if (e == cudaSuccess) {
     cfg.gridDim = dim3(R * nq);
     cfg.blockDim = dim3(HD);
@@ -434,8 +461,11 @@ int attn_launch(const __half* q, const __half* kcache, const __half* vcache,
 }
 
 void attn_init_attrs() {
-  cudaFuncSetAttribute(attn_chunk_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(128, 1));
-  cudaFuncSetAttribute(attn_chunk_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(128, 2));
-  cudaFuncSetAttribute(attn_chunk_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(64, 1));
-  cudaFuncSetAttribute(attn_chunk_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, chunk_smem_bytes(64, 2));
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  for (auto k : {attn_chunk_kernel<128, 2, 4>, attn_chunk_kernel<128, 1, 4>,
+                 attn_chunk_kernel<128, 1, 8>, attn_chunk_kernel<64, 2, 4>,
+                 attn_chunk_kernel<64, 1, 4>, attn_chunk_kernel<64, 1, 8>})
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
