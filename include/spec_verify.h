@@ -309,6 +309,52 @@ int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* seq_ids,
                            const spec_sampling* sampling, int32_t* n_acc,
                            int32_t* emitted, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Adaptive draft depth: a host controller that picks the depth d of the next
+ * verify round ("Speculative Decoding (D5-R) -- Plan", status notes: per-round
+ * d from beta-smoothed per-depth acceptance, min-of-4 round-cost windows, a
+ * 10% switch hysteresis, optimism for depths not yet seen, capped at d = 7
+ * by the identity boundary).  Host only: no GPU work, no stream, no model.
+ *  - Position i = 1..d_max keeps decayed Beta counts (a_i, b_i).  A round at
+ *    depth d in which a sequence accepted n drafts adds 1 to a_i for
+ *    i <= min(n, d) and, if n < d, 1 to b_{n+1}; a negative n (a failed
+ *    sequence) adds nothing.  All counts are first multiplied by `decay`.
+ *  - p_i = (a_i + prior_accept) / (a_i + b_i + prior_accept + prior_reject)
+ *    (prior_reject = 0: a position never observed has p_i = 1).
+ *  - E(d) = sum_{k=0..d} prod_{i<=k} p_i tokens per round; c(d) = the
+ *    minimum of the depth's last `cost_window` round times; r(d) = E / c.
+ *  - While some depth in [d_min, d_max] has no round time, the deepest such
+ *    depth is next (its r counts as +infinity).  Otherwise the smallest
+ *    depth of maximal r replaces the current depth when its r exceeds the
+ *    current r by the factor (1 + hysteresis).  The first depth is d_max.
+ * Every double is rounded operation by operation, as written above. */
+typedef struct {
+  int32_t d_min, d_max;       /* 0 <= d_min <= d_max <= SPEC_MAX_NT - 1 */
+  double prior_accept;        /* >= 0 */
+  double prior_reject;        /* >= 0; prior_accept + prior_reject > 0 */
+  double decay;               /* (0, 1] */
+  double hysteresis;          /* >= 0 */
+  int32_t cost_window;        /* 1..64 round times per depth */
+} spec_depth_params;
+typedef struct spec_depth_ctl spec_depth_ctl;
+
+/* Defaults: d in [1, 7], prior (1, 0), decay 0.95, hysteresis 0.10, window 4. */
+void spec_depth_params_default(spec_depth_params* p);
+/* params NULL = the defaults.  SPEC_E_INVALID on a parameter out of range. */
+int spec_depth_ctl_create(const spec_depth_params* params, spec_depth_ctl** out);
+int spec_depth_ctl_destroy(spec_depth_ctl* c);
+/* The depth of the next round. */
+int spec_depth_ctl_next(const spec_depth_ctl* c, int32_t* d);
+/* A finished round: its depth d (in [d_min, d_max]), the n_seq accepted
+ * counts (HOST int32, e.g. spec_verify_round's n_acc copied back) and its
+ * time in seconds (finite, > 0).  *next_d (may be NULL) gets the next depth.
+ * SPEC_E_SHAPE / SPEC_E_INVALID leave the controller unchanged. */
+int spec_depth_ctl_observe(spec_depth_ctl* c, int32_t d, int32_t n_seq, const int32_t* n_acc,
+                           double round_seconds, int32_t* next_d);
+/* Diagnostics: p[0..d_max] (p[0] = 1) and r[0..d_max] (0 below d_min,
+ * +infinity for depths without a round time); either may be NULL. */
+int spec_depth_ctl_estimates(const spec_depth_ctl* c, double* p, double* r);
+
 #ifdef __cplusplus
 }
 #endif

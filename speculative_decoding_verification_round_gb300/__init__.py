@@ -34,7 +34,9 @@ EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_li
             "spec_state_set", "spec_state_get", "spec_error_check", "spec_model_set_graphs",
             "spec_verify_attn", "spec_lm_head", "spec_accept_greedy",
             "spec_accept_stochastic", "spec_accept_stochastic_noalloc", "spec_verify_round",
-            "spec_verify_round_host"]
+            "spec_verify_round_host", "spec_depth_params_default", "spec_depth_ctl_create",
+            "spec_depth_ctl_destroy", "spec_depth_ctl_next", "spec_depth_ctl_observe",
+            "spec_depth_ctl_estimates"]
 
 P = ctypes.c_void_p
 I32 = ctypes.c_int32
@@ -62,6 +64,12 @@ class spec_model_weights(ctypes.Structure):
     _fields_ = [("embed", P), ("norm_w", P), ("wqkv", ctypes.POINTER(spec_qweight)),
                 ("wo", ctypes.POINTER(spec_qweight)), ("wgu", ctypes.POINTER(spec_qweight)),
                 ("wd", ctypes.POINTER(spec_qweight)), ("lm_head", spec_qweight)]
+
+
+class spec_depth_params(ctypes.Structure):
+    _fields_ = [("d_min", I32), ("d_max", I32), ("prior_accept", ctypes.c_double),
+                ("prior_reject", ctypes.c_double), ("decay", ctypes.c_double),
+                ("hysteresis", ctypes.c_double), ("cost_window", I32)]
 
 
 class spec_sampling(ctypes.Structure):
@@ -109,6 +117,14 @@ def lib():
                                             P, P, P, P]),
                 "spec_verify_round_host": (I32, [P, I32, P, P, I32, P,
                                                  ctypes.POINTER(spec_sampling), P, P, P]),
+                "spec_depth_params_default": (None, [ctypes.POINTER(spec_depth_params)]),
+                "spec_depth_ctl_create": (I32, [ctypes.POINTER(spec_depth_params),
+                                                ctypes.POINTER(P)]),
+                "spec_depth_ctl_destroy": (I32, [P]),
+                "spec_depth_ctl_next": (I32, [P, ctypes.POINTER(I32)]),
+                "spec_depth_ctl_observe": (I32, [P, I32, I32, P, ctypes.c_double,
+                                                 ctypes.POINTER(I32)]),
+                "spec_depth_ctl_estimates": (I32, [P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -363,3 +379,51 @@ def spec_verify_round_host(m: Model, n_seq: int, seq_ids, draft, d: int, q_logit
                                         _ptr(q_logits), ctypes.byref(sp), n_acc.ctypes.data,
                                         emitted.ctypes.data, _stream(stream)))
     return n_acc, emitted
+
+
+class DepthController:
+    """The library's adaptive draft-depth controller (host only; rules in
+    include/spec_verify.h).  Keyword arguments override the defaults."""
+
+    def __init__(self, **kw):
+        prm = spec_depth_params()
+        lib().spec_depth_params_default(ctypes.byref(prm))
+        for k, v in kw.items():
+            setattr(prm, k, v)
+        self.params = prm
+        h = P()
+        _check(lib().spec_depth_ctl_create(ctypes.byref(prm), ctypes.byref(h)))
+        self.handle = h
+
+    def next_depth(self) -> int:
+        d = I32()
+        _check(lib().spec_depth_ctl_next(self.handle, ctypes.byref(d)))
+        return d.value
+
+    def observe(self, d: int, n_acc, round_seconds: float) -> int:
+        import numpy as np
+        a = np.ascontiguousarray(n_acc, dtype=np.int32)
+        nd = I32()
+        _check(lib().spec_depth_ctl_observe(self.handle, int(d), int(a.size),
+                                            a.ctypes.data if a.size else None,
+                                            float(round_seconds), ctypes.byref(nd)))
+        return nd.value
+
+    def estimates(self):
+        """(p[0..d_max], r[0..d_max]) as lists of floats."""
+        n = self.params.d_max + 1
+        p = (ctypes.c_double * n)()
+        r = (ctypes.c_double * n)()
+        _check(lib().spec_depth_ctl_estimates(self.handle, p, r))
+        return list(p), list(r)
+
+    def close(self):
+        if self.handle:
+            lib().spec_depth_ctl_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -15,7 +15,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libspecverify.so")
-SOURCES = ["api.cu", "linear.cu", "attn.cu", "ops.cu", "accept.cu"]
+SOURCES = ["api.cu", "linear.cu", "attn.cu", "ops.cu", "accept.cu", "depth.cu"]
+# host code whose doubles must be rounded operation by operation
+FILE_FLAGS = {"depth.cu": ["-Xcompiler", "-ffp-contract=off"]}
 HEADERS = [os.path.join(CSRC, "common.cuh"),
            os.path.join(os.path.dirname(HERE), "include", "spec_verify.h")]
 
@@ -37,7 +39,7 @@ def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, src.replace(".cu", ".o"))
     if not _stale(obj, path):
         return obj
-    cmd = [NVCC, *NVCC_FLAGS, "-c", path, "-o", obj + ".tmp"]
+    cmd = [NVCC, *NVCC_FLAGS, *FILE_FLAGS.get(src, []), "-c", path, "-o", obj + ".tmp"]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
