@@ -321,6 +321,87 @@ def round_sweep(sv, m, wl, dev, groups=5):
     return {"us": us, "nt9_16_over_nt1": round(worst / us["1"], 3)}
 
 
+def greedy_continuation(sv, m, wl, dev, d, rng, sid, n_acc, em1, p_agree):
+    """Untimed: the target's own greedy continuation of sequence 0 for d
+    positions (nt = 1 passes from a saved state, restored after), each
+    position kept with probability p_agree, else a random id -- the drafts
+    of one round at depth d."""
+    n_past, ei, anc = sv.spec_state_get(m, [0])
+    chain, tok = [], anc[0]
+    for i in range(d):
+        sv.spec_state_set(m, [0], n_past=[n_past[0] + i], anchor=[tok])
+        sv.spec_verify_round(m, 1, sid, None, 0, n_acc=n_acc, emitted=em1)
+        true_next = int(em1.item())
+        tok = true_next if rng.random() < p_agree else int(rng.integers(0, wl["vocab"]))
+        chain.append(tok)
+    sv.spec_state_set(m, [0], n_past=n_past, emit_idx=ei, anchor=anc)
+    return chain
+
+
+ADAPTIVE_ROUNDS = 64
+# (name, per-position draft agreement, deepest depth the controller may pick):
+# the workload's agreement with the controller's default cap of 7, and a
+# near-perfect drafter allowed the full 16-row verify block
+ADAPTIVE_CASES = (("p0.74_dmax7", None, 7), ("p0.95_dmax15", 0.95, 15))
+
+
+def adaptive_depth_run(sv, m, wl, dev, rounds=ADAPTIVE_ROUNDS):
+    """The adaptive draft-depth controller in the loop: each round's depth
+    comes from the controller, its drafts from the target's own greedy chain
+    (agreement p_agree per position), and the round's CUDA-event time plus
+    its accept count go back to the controller.  The same loop at the fixed
+    depth 7 runs beside it.  Reported per case: emitted tokens per second of
+    verify time, the depths chosen, and the controller's host time per call
+    (median, through the Python binding)."""
+    import torch
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    em1 = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+    # capture every depth's graph first, so that no timed round pays for it
+    for d in range(sv.SPEC_MAX_NT):
+        em = torch.zeros((1, d + 1), dtype=torch.int32, device=dev)
+        dr = torch.zeros((1, d), dtype=torch.int32, device=dev) if d else None
+        sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[1234])
+        sv.spec_verify_round(m, 1, sid, dr, d, n_acc=n_acc, emitted=em)
+    torch.cuda.synchronize()
+    out = {"rounds": rounds}
+    for name, p_agree, d_max in ADAPTIVE_CASES:
+        p_agree = wl["p_agree"] if p_agree is None else p_agree
+        case = {"p_agree": p_agree, "d_max": d_max}
+        for mode in ("adaptive", "static7"):
+            rng = np.random.default_rng(11)
+            sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[1234])
+            ctl = sv.DepthController(d_max=d_max) if mode == "adaptive" else None
+            tokens, secs, ctl_t, hist = 0, 0.0, [], {}
+            for _ in range(rounds):
+                d = ctl.next_depth() if ctl is not None else 7
+                chain = greedy_continuation(sv, m, wl, dev, d, rng, sid, n_acc, em1, p_agree)
+                dr = torch.tensor([chain], dtype=torch.int32, device=dev) if d else None
+                em = torch.zeros((1, d + 1), dtype=torch.int32, device=dev)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                sv.spec_verify_round(m, 1, sid, dr, d, n_acc=n_acc, emitted=em)
+                e1.record(st)
+                e1.synchronize()
+                t = e0.elapsed_time(e1) * 1e-3
+                a = int(n_acc.item())
+                tokens += a + 1
+                secs += t
+                hist[str(d)] = hist.get(str(d), 0) + 1
+                if ctl is not None:
+                    t0 = time.perf_counter()
+                    ctl.observe(d, [a], t)
+                    ctl_t.append(time.perf_counter() - t0)
+            case[mode] = {"tok_per_s": round(tokens / secs, 1), "depths": hist}
+            if ctl is not None:
+                case[mode]["controller_us_per_call"] = round(statistics.median(ctl_t) * 1e6, 2)
+                ctl.close()
+        out[name] = case
+    return out
+
+
 def nt_sweep(sv, synth, dev, reps=20):
     """The linear-layer sweep: Q4 5120x13824 and Q6 13824x5120 at each nt,
     L2 flushed between launches (verify-GEMM microseconds and GB/s)."""
@@ -366,7 +447,7 @@ def run_ours(args):
     wl = dict(synth.WL_DECODER8)
     d, V = wl["d"], wl["vocab"]
     max_ctx = wl["ctx"] + max(8 * (args.warmup + args.steps + 4),
-                              sv.SPEC_MAX_NT * ROUND_SWEEP_GROUP) + 64
+                              sv.SPEC_MAX_NT * ROUND_SWEEP_GROUP, sv.SPEC_MAX_NT * (ADAPTIVE_ROUNDS + 2)) + 64
     hbm_peak, peak_kind = peaks()
     m, W = build_model(sv, synth, wl, dev, max_ctx)
     del W
@@ -432,6 +513,7 @@ def run_ours(args):
         gbs, per, bytes_per_launch, traffic = time_dominant_kernel(sv, synth, wl, dev, hbm_peak)
         sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
         rsweep = round_sweep(sv, m, wl, dev) if not args.no_sweep else None
+        adaptive = adaptive_depth_run(sv, m, wl, dev) if not args.no_sweep else None
         n_layers = wl["n_layers"]
         # embed (with the first norm), 8 per layer but the first layer's
         # norm, final norm + LM head, fused accept + commit
@@ -472,6 +554,7 @@ def run_ours(args):
                          "peak_kind": peak_kind, "per_shape": per},
             "sweep": sweep,
             "round_sweep": rsweep,
+            "adaptive_depth": adaptive,
             "e2e": {"value": round(e2e_all / t_e2e, 2), "unit": "tok/s",
                     "api": "spec_verify_round_host (host arrays, mapped pinned staging)",
                     "h2d_bytes_per_step": 4 * (1 + d), "d2h_bytes_per_step": 4 * (2 + d)},
