@@ -402,6 +402,101 @@ def adaptive_depth_run(sv, m, wl, dev, rounds=ADAPTIVE_ROUNDS):
     return out
 
 
+FULL_ROUND_DRAFT_LAYERS = (6, 24)
+FULL_ROUND_REPS = 24
+
+
+def full_round_run(sv, synth, m, wl, dev, max_ctx, rounds=ADAPTIVE_ROUNDS):
+    """Whole rounds with the draft phase timed in ("Speculative Decoding
+    (D5-R) -- Plan", section 3: d sequential nt = 1 draft forwards, then one
+    nt = d + 1 target forward).  The draft is a 0.5B-class decoder on the same
+    engine: each draft forward is its graph-replayed d = 0 round, whose greedy
+    commit makes its token the next forward's input, all on the device.  Its
+    random-weight tokens are computed and dropped: the target verifies drafts
+    from its own greedy chain at agreement p_agree (synthetic acceptance), so
+    only the draft's cost enters.  Two draft depths: 6 layers (a quarter of
+    the 0.5B's 24, as the 8-layer target is a quarter-depth 32-layer model)
+    and the full 24.  Per depth d = 0..7: median round time and draft time per
+    token, emitted tokens per second as measured and as expected from the
+    agreement (E(d) over the median round time; the best static depth is
+    chosen on the latter); then the adaptive controller with d_min = 0
+    (d = 0 is plain decoding) on these round times."""
+    import torch
+    st = torch.cuda.current_stream()
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    dn = torch.zeros(1, dtype=torch.int32, device=dev)
+    dem = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    em1 = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    out = {"draft_shape": synth.WL_DRAFT05B["name"], "p_agree": wl["p_agree"]}
+    for n_layers in FULL_ROUND_DRAFT_LAYERS:
+        dwl = dict(synth.WL_DRAFT05B, n_layers=n_layers)
+        dm, W = build_model(sv, synth, dwl, dev, max_ctx)
+        del W
+        fill_context(sv, synth, dm, dwl, dev, seed=7)
+
+        def one_round(d, rng):
+            sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[1234])
+            sv.spec_state_set(dm, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[1234])
+            chain = greedy_continuation(sv, m, wl, dev, d, rng, sid, n_acc, em1, wl["p_agree"])
+            dr = torch.tensor([chain], dtype=torch.int32, device=dev) if d else None
+            em = torch.zeros((1, d + 1), dtype=torch.int32, device=dev)
+            torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(st)
+            for _ in range(d):
+                sv.spec_verify_round(dm, 1, sid, None, 0, n_acc=dn, emitted=dem)
+            ev[1].record(st)
+            sv.spec_verify_round(m, 1, sid, dr, d, n_acc=n_acc, emitted=em)
+            ev[2].record(st)
+            ev[2].synchronize()
+            return (ev[0].elapsed_time(ev[2]) * 1e-3, ev[0].elapsed_time(ev[1]) * 1e-3,
+                    int(n_acc.item()))
+
+        rng = np.random.default_rng(13)
+        for d in range(8):  # graphs and first-touch work outside the timed rounds
+            one_round(d, rng)
+        per_d, draft_tok = {}, []
+        for d in range(8):
+            rng = np.random.default_rng(17 + d)
+            ts, toks = [], 0
+            for _ in range(FULL_ROUND_REPS):
+                t, td, a = one_round(d, rng)
+                ts.append(t)
+                toks += a + 1
+                if d:
+                    draft_tok.append(td / d)
+            # drafts agree independently with probability p per position:
+            # E(d) = (1 - p^(d+1)) / (1 - p) tokens a round, noise-free
+            p = wl["p_agree"]
+            e_tok = (1.0 - p ** (d + 1)) / (1.0 - p)
+            t_med = statistics.median(ts)
+            per_d[str(d)] = {"round_us": round(t_med * 1e6, 1),
+                             "tok_per_s": round(toks / sum(ts), 1),
+                             "expected_tok_per_s": round(e_tok / t_med, 1)}
+        best = max(per_d, key=lambda k: per_d[k]["expected_tok_per_s"])
+        leg = {"draft_us_per_token": round(statistics.median(draft_tok) * 1e6, 1),
+               "by_depth": per_d, "best_static_d": int(best),
+               "best_over_plain_decode": round(per_d[best]["expected_tok_per_s"] /
+                                               per_d["0"]["expected_tok_per_s"], 3)}
+        rng = np.random.default_rng(11)
+        ctl = sv.DepthController(d_min=0, d_max=7)
+        toks, secs, hist = 0, 0.0, {}
+        for _ in range(rounds):
+            d = ctl.next_depth()
+            t, _, a = one_round(d, rng)
+            toks += a + 1
+            secs += t
+            hist[str(d)] = hist.get(str(d), 0) + 1
+            ctl.observe(d, [a], t)
+        ctl.close()
+        leg["adaptive"] = {"tok_per_s": round(toks / secs, 1), "depths": hist, "rounds": rounds}
+        out[f"draft{n_layers}L"] = leg
+        assert sv.spec_error_check(dm) == 0
+        dm.close()
+    return out
+
+
 def nt_sweep(sv, synth, dev, reps=20):
     """The linear-layer sweep: Q4 5120x13824 and Q6 13824x5120 at each nt,
     L2 flushed between launches (verify-GEMM microseconds and GB/s)."""
@@ -514,6 +609,7 @@ def run_ours(args):
         sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
         rsweep = round_sweep(sv, m, wl, dev) if not args.no_sweep else None
         adaptive = adaptive_depth_run(sv, m, wl, dev) if not args.no_sweep else None
+        full_round = full_round_run(sv, synth, m, wl, dev, max_ctx) if not args.no_sweep else None
         n_layers = wl["n_layers"]
         # embed (with the first norm), 8 per layer but the first layer's
         # norm, final norm + LM head, fused accept + commit
@@ -555,6 +651,7 @@ def run_ours(args):
             "sweep": sweep,
             "round_sweep": rsweep,
             "adaptive_depth": adaptive,
+            "full_round": full_round,
             "e2e": {"value": round(e2e_all / t_e2e, 2), "unit": "tok/s",
                     "api": "spec_verify_round_host (host arrays, mapped pinned staging)",
                     "h2d_bytes_per_step": 4 * (1 + d), "d2h_bytes_per_step": 4 * (2 + d)},

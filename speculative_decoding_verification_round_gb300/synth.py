@@ -50,6 +50,13 @@ WL_DECODER8 = dict(name="decoder8_H4096_V151936_ctx4096_nt8", n_layers=8,
                    hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                    ffn=14336, vocab=151936, ctx=4096, n_seq=1, d=7,
                    p_agree=0.74, lm_qtype=6, lm_scale=LM_SCALE, seed=0)
+# The draft of the full-round measurement: a 0.5B-class decoder with 4-bit
+# weights throughout (the pages pair their 7B/14B targets with a 0.5B q4_0
+# draft): 24 layers of H=896, 14 query / 2 KV heads of 64, FFN 4864, the
+# target's 151936-id vocabulary.
+WL_DRAFT05B = dict(name="draft05b_24L_H896_V151936", n_layers=24, hidden=896,
+                   n_q_heads=14, n_kv_heads=2, head_dim=64, ffn=4864, vocab=151936,
+                   ctx=4096, n_seq=1, lm_qtype=4, lm_scale=LM_SCALE, seed=5)
 WL_DECODER14B = dict(name="decoder14b_40L_H5120_V248320_12seq_ctx512_nt16",
                      n_layers=40, hidden=5120, n_q_heads=40, n_kv_heads=8,
                      head_dim=128, ffn=13824, vocab=248320, ctx=512, n_seq=12,

@@ -36,6 +36,8 @@ def attn_model(sv, dev, g, nq, nkv, hd, max_ctx, max_nt, max_seqs):
     (40, 8, 128, 3, 16, 512, 600),     # GQA 5, 80 query rows per kv head
     (4, 4, 64, 2, 1, 0, 64),           # first position, no context
     (8, 2, 128, 1, 5, 123, 130),       # ends 2 positions before max_ctx
+    (14, 2, 64, 1, 1, 4000, 4100),     # GQA 7 (the 0.5B-class draft), one decode row
+    (14, 2, 64, 2, 3, 257, 300),       # GQA 7, two m tiles per kv head
 ])
 def test_attention_matches_oracle_and_is_position_invariant(orc, dev, nq, nkv, hd, n_seq, nt,
                                                             n_past, max_ctx):
