@@ -158,6 +158,11 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 # the workload
 # --------------------------------------------------------------------------
+# HBM bytes per weight of each block format: the integers plus one fp16
+# scale per 32
+WEIGHT_BYTES = {4: 0.5625, 6: 0.8125, 8: 1.0625}
+
+
 def build_model(sv, synth, wl, dev, max_ctx):
     W = synth.decoder_weights_torch(wl, dev)
     desc = dict(n_layers=wl["n_layers"], hidden=wl["hidden"], n_q_heads=wl["n_q_heads"],
@@ -265,7 +270,7 @@ def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
         qm = sv.QMat(w, max_rows=16)
         x = synth.f16_normal_torch(gen, (nt, K), dev).view(torch.int16)
         y = torch.empty((nt, N), dtype=torch.float32, device=dev)
-        nbytes = N * K * (0.5625 if qt == 4 else 0.8125) + nt * K * 2 + nt * N * 4
+        nbytes = N * K * WEIGHT_BYTES[qt] + nt * K * 2 + nt * N * 4
         times = []
         for i in range(reps + 3):
             flush()
@@ -497,11 +502,12 @@ def full_round_run(sv, synth, m, wl, dev, max_ctx, rounds=ADAPTIVE_ROUNDS):
     return out
 
 
-def nt_sweep(sv, synth, dev, reps=20):
-    """The linear-layer sweep: Q4 5120x13824 and Q6 13824x5120 at each nt,
-    L2 flushed between launches (verify-GEMM microseconds and GB/s)."""
+def nt_sweep(sv, synth, dev, reps=20, wl=None):
+    """The linear-layer sweep: Q4 5120x13824 and Q6 13824x5120 (or the
+    given workload's matrices) at each nt, L2 flushed between launches
+    (verify-GEMM microseconds and GB/s)."""
     import torch
-    wl = synth.WL_LINEAR_SWEEP
+    wl = synth.WL_LINEAR_SWEEP if wl is None else wl
     gen = synth.torch_gen(wl["seed"], dev)
     st = torch.cuda.current_stream()
     flush = L2Flush(dev)
@@ -511,7 +517,7 @@ def nt_sweep(sv, synth, dev, reps=20):
         qm = sv.QMat(w, max_rows=16)
         x = synth.f16_normal_torch(gen, (16, K), dev).view(torch.int16)
         y = torch.empty((16, N), dtype=torch.float32, device=dev)
-        wbytes = N * K * (0.5625 if qt == 4 else 0.8125)
+        wbytes = N * K * WEIGHT_BYTES[qt]
         row = {}
         for nt in wl["nts"]:
             times = []
@@ -607,6 +613,7 @@ def run_ours(args):
     if rank == 0:
         gbs, per, bytes_per_launch, traffic = time_dominant_kernel(sv, synth, wl, dev, hbm_peak)
         sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
+        sweep_q8 = nt_sweep(sv, synth, dev, wl=synth.WL_LINEAR_SWEEP_Q8) if not args.no_sweep else None
         rsweep = round_sweep(sv, m, wl, dev) if not args.no_sweep else None
         adaptive = adaptive_depth_run(sv, m, wl, dev) if not args.no_sweep else None
         full_round = full_round_run(sv, synth, m, wl, dev, max_ctx) if not args.no_sweep else None
@@ -614,7 +621,7 @@ def run_ours(args):
         # embed (with the first norm), 8 per layer but the first layer's
         # norm, final norm + LM head, fused accept + commit
         launches_per_round = 1 + 8 * n_layers - 1 + 2 + 1
-        weight_bytes = sum(p["N"] * p["K"] * (0.5625 if p["qtype"] == 4 else 0.8125) *
+        weight_bytes = sum(p["N"] * p["K"] * WEIGHT_BYTES[p["qtype"]] *
                            (n_layers if p["qtype"] == 4 else 1) for p in per)
         kv_bytes = n_layers * wl["n_kv_heads"] * (wl["ctx"] + d) * wl["head_dim"] * 2 * 2
         round_s = ms_per_step * 1e-3
@@ -649,6 +656,7 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": round(bytes_per_launch),
                          "peak_kind": peak_kind, "per_shape": per},
             "sweep": sweep,
+            "sweep_q8": sweep_q8,
             "round_sweep": rsweep,
             "adaptive_depth": adaptive,
             "full_round": full_round,

@@ -61,6 +61,7 @@ extern "C" {
 
 #define SPEC_Q4 4 /* 4-bit signed ints in [-8, 7], blocks of 32, fp16 scale */
 #define SPEC_Q6 6 /* 6-bit signed ints in [-32, 31], blocks of 32, fp16 scale */
+#define SPEC_Q8 8 /* 8-bit signed ints in [-128, 127], blocks of 32, fp16 scale */
 
 #define SPEC_MAX_NT 16 /* rows per sequence in one round: anchor + up to 15 drafts */
 
@@ -69,16 +70,22 @@ void spec_last_error(char* buf, size_t len);
 
 /* ------------------------------------------------------------------------
  * Block-quantised matrix W[N][K] in canonical planes (device, caller-owned):
- *   qs     [N][K/32][16] bytes.  Byte j of block b holds element 32b+j in its
- *          low nibble and element 32b+j+16 in its high nibble.  Q4 stores
- *          u = q + 8; Q6 stores the low 4 bits of u = q + 32.
- *   qh     [N][K/32][8] bytes, Q6 only (NULL for Q4): the high 2 bits of u,
- *          element j of the block at bits 2*(j%4) of byte j/4.
+ *   qs     Q4 / Q6: [N][K/32][16] bytes.  Byte j of block b holds element
+ *          32b+j in its low nibble and element 32b+j+16 in its high nibble.
+ *          Q4 stores u = q + 8 (the q4_0 element order); Q6 stores the low 4
+ *          bits of u = q + 32.
+ *          Q8: [N][K/32][32] bytes, byte j of block b = element 32b+j as a
+ *          two's-complement int8 (the q8_0 element order).
+ *   qh     [N][K/32][8] bytes, Q6 only (NULL for Q4 and Q8): the high 2 bits
+ *          of u, element j of the block at bits 2*(j%4) of byte j/4.
  *   scales [N][K/32] fp16.  W[n][k] = scale[n][k/32] * q[n][k].
+ * The q4_0 / q8_0 weights of the pages' targets ("Speculative Decoding
+ * (D5-R) -- Plan", status notes: the verify machinery extended to q8_0/q4_0)
+ * are these planes with each block's scale split out of its bytes.
  * Preconditions: K % 32 == 0, N % 16 == 0.
  * ---------------------------------------------------------------------- */
 typedef struct {
-  int32_t qtype; /* SPEC_Q4 or SPEC_Q6 */
+  int32_t qtype; /* SPEC_Q4, SPEC_Q6 or SPEC_Q8 */
   int32_t N, K;
   const void* qs;
   const void* qh;
@@ -106,11 +113,12 @@ int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
                   void* stream);
 
 /* ------------------------------------------------------------------------
- * Decoder model: RMSNorm -> QKV (Q4) + rotate-half RoPE -> causal GQA
- * attention over the KV cache -> O (Q4) + residual -> RMSNorm -> gate/up (Q4)
- * + SwiGLU -> down (Q4) + residual, n_layers times; final RMSNorm; LM head
- * (Q4 or Q6) over the full vocabulary.  Residual stream fp32, activations
- * fp16, KV cache fp16.
+ * Decoder model: RMSNorm -> QKV + rotate-half RoPE -> causal GQA attention
+ * over the KV cache -> O + residual -> RMSNorm -> gate/up + SwiGLU -> down +
+ * residual, n_layers times; final RMSNorm; LM head over the full vocabulary.
+ * Every linear is a block-quantised matrix of any of the formats above
+ * (SPEC_Q4, SPEC_Q6, SPEC_Q8).  Residual stream fp32, activations fp16, KV
+ * cache fp16.
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t n_layers; /* 0 allowed: LM head only (spec_lm_head) */

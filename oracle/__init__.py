@@ -10,8 +10,8 @@ accept loop); this module compiles it with gcc and wraps it with numpy.
 
 Readings of the pages that the oracle encodes (each one is also listed in the
 design notes):
-  * canonical Q4/Q6 block layout (the pages name Q4/Q6 block formats but do
-    not fix a bit layout);
+  * canonical Q4/Q6/Q8 block layout (the pages name Q4/Q6 and q8_0/q4_0
+    block formats but do not fix a bit layout);
   * RMSNorm eps, rotate-half RoPE with theta, fp32 residual stream;
   * argmax ties go to the lowest index;
   * the strict rejection sampler's probabilities are integer weights
@@ -145,10 +145,10 @@ class QWeight:
     """Canonical planes of one block-quantised matrix [N][K] (host numpy)."""
 
     def __init__(self, qtype: int, qs, qh, scales, N: int, K: int):
-        assert qtype in (4, 6) and K % 32 == 0
+        assert qtype in (4, 6, 8) and K % 32 == 0
         self.qtype, self.N, self.K = qtype, int(N), int(K)
-        self.qs = _c(qs, np.uint8).reshape(N, K // 32, 16)
-        self.qh = None if qtype == 4 else _c(qh, np.uint8).reshape(N, K // 32, 8)
+        self.qs = _c(qs, np.uint8).reshape(N, K // 32, 32 if qtype == 8 else 16)
+        self.qh = None if qtype != 6 else _c(qh, np.uint8).reshape(N, K // 32, 8)
         self.scales = _c(scales, np.uint16).reshape(N, K // 32)
 
     def _struct(self) -> _QW:

@@ -70,12 +70,18 @@ void oracle_f16_to_f64(const uint16_t* h, int64_t n, double* out) {
 /*       j+16 (high nibble) of block b, stored as u = q + 8, q in [-8, 7].   */
 /*   Q6: low 4 bits of u = q + 32 in qs (same nibble order as Q4); high 2    */
 /*       bits in qh[n][b][8]: element j at bits 2*(j%4) of byte j/4.         */
+/*   Q8: qs[n][b][32] bytes; byte j is element j of block b as a two's-     */
+/*       complement int8, q in [-128, 127] (the q8_0 element order).        */
 /*   scales[n][b] fp16.  w[n][k] = float(scale) * float(q), exact in fp32.   */
 /* ------------------------------------------------------------------------ */
 static int q_elem(int qtype, const uint8_t* qs, const uint8_t* qh, int64_t n,
                   int64_t nb, int64_t k) {
   int64_t b = k / 32;
   int j = (int)(k % 32);
+  if (qtype == 8) {
+    int v = qs[(n * nb + b) * 32 + j];
+    return v >= 128 ? v - 256 : v;
+  }
   uint8_t byte = qs[(n * nb + b) * 16 + (j % 16)];
   int lo = (j < 16) ? (byte & 0xF) : (byte >> 4);
   if (qtype == 4) return lo - 8;

@@ -25,7 +25,7 @@ SPEC_E_CUDA = -3
 SPEC_E_OOM = -4
 SPEC_E_UNSUPPORTED = -5
 SPEC_E_TIMEOUT = -6
-SPEC_Q4, SPEC_Q6 = 4, 6
+SPEC_Q4, SPEC_Q6, SPEC_Q8 = 4, 6, 8
 SPEC_MAX_NT = 16
 
 EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_linear_q",

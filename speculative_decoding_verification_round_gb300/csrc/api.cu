@@ -343,8 +343,6 @@ static int check_desc(const spec_model_desc* D, const spec_model_weights* W) {
       if (W->wo[l].N != H || W->wo[l].K != nq * hd) return fail(SPEC_E_SHAPE, "wo shape");
       if (W->wgu[l].N != 2 * F || W->wgu[l].K != H) return fail(SPEC_E_SHAPE, "wgu shape");
       if (W->wd[l].N != H || W->wd[l].K != F) return fail(SPEC_E_SHAPE, "wd shape");
-      if (W->wqkv[l].qtype != SPEC_Q4 && W->wqkv[l].qtype != SPEC_Q6)
-        return fail(SPEC_E_UNSUPPORTED, "qtype");
     }
   }
   if (W->lm_head.N != D->vocab || W->lm_head.K != D->hidden) return fail(SPEC_E_SHAPE, "lm_head shape");

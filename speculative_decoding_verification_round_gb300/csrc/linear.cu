@@ -15,6 +15,8 @@
 //     mma.sync m16n8k16 (f16 x f16 -> f32) as the A operand; the activations
 //     (n8 column tiles of verify rows) are B, and the zero point enters as
 //     the C operand (-bias * sum(x), from two MMAs with a constant fragment);
+//     the 8-bit integers are centred exactly in fp16 (q * 2^-20, the same
+//     unit) and need no zero point;
 //   * each 32-block is accumulated in a fresh fp32 fragment and folded into
 //     the running sum with one fp32 FMA by its fp16 scale;
 //   * K is split into S segments across CTAs and, inside a CTA, into KW
@@ -45,24 +47,33 @@ constexpr int NS = 2;        // weight-ring stages per warp
 // CTAs per SM the register budget is set for, by the number of column tiles.
 // Two column tiles need ~110 registers (2 CTAs per SM); their shorter stages
 // keep the shared memory of a Q6 LM-head CTA low enough for 2 per SM too.
-template <int NCT>
-constexpr int cps() { return NCT == 1 ? 3 : 2; }
+// 8-bit records are twice as long: two chunks a stage at either width.
+template <int QT, int NCT>
+constexpr int cps() { return (NCT == 1 && QT != 8) ? 3 : 2; }
 template <int NCT>
 constexpr int min_blocks() { return NCT == 1 ? 3 : 2; }
 constexpr int NC_CTA_MAX = 64;  // chunks of one CTA's K range (its staged activation slice)
 constexpr int MAX_SPLIT = 64;
 
-// Record of one (pair, 64-k chunk): nibble words of the 2 tiles, their fp16
-// scales, then (Q6) the high 2-bit fields.
+// Record of one (pair, 64-k chunk): the integer words of the 2 tiles (nibbles;
+// bytes for Q8), their fp16 scales, then (Q6) the high 2-bit fields.
 template <int QT>
 struct Rec {
-  static constexpr int QS = 0;                        // 2 x 512 B
-  static constexpr int SC = TPW * 512;                // 2 x 64 B
-  static constexpr int QH = SC + TPW * 64;            // 2 x 256 B (Q6)
-  static constexpr int BYTES = QH + (QT == 6 ? TPW * 256 : 0);  // 1152 / 1664
+  static constexpr int QS_TILE = QT == 8 ? 1024 : 512;  // bytes of one tile's integers
+  static constexpr int QS = 0;
+  static constexpr int SC = TPW * QS_TILE;              // 2 x 64 B
+  static constexpr int QH = SC + TPW * 64;              // 2 x 256 B (Q6)
+  static constexpr int BYTES = QH + (QT == 6 ? TPW * 256 : 0);  // 1152 / 1664 / 2176
 };
+inline int rec_bytes(int qtype) {
+  return qtype == 4 ? Rec<4>::BYTES : (qtype == 6 ? Rec<6>::BYTES : Rec<8>::BYTES);
+}
+inline int stage_chunks(int qtype, int nct) {
+  if (qtype == 8) return nct == 1 ? cps<8, 1>() : cps<8, 2>();
+  return nct == 1 ? cps<4, 1>() : cps<4, 2>();
+}
 inline int ring_bytes(int qtype, int nct) {
-  return WARPS * NS * (nct == 1 ? cps<1>() : cps<2>()) * (qtype == 4 ? Rec<4>::BYTES : Rec<6>::BYTES);
+  return WARPS * NS * stage_chunks(qtype, nct) * rec_bytes(qtype);
 }
 // Staged activation row: the CTA's K range plus 64 bytes, so that the rows
 // g = 0..7 of a fragment load fall in distinct shared-memory banks.
@@ -125,28 +136,49 @@ __global__ void pack_kernel(int qtype, const uint8_t* __restrict__ qs,
   const bool real = T < n_tiles;
   const int row_g = real ? perm_row(T * 16 + g, perm, hd, N) : 0;
   const int row_g8 = real ? perm_row(T * 16 + g + 8, perm, hd, N) : 0;
-  const int slot_row8[8] = {0, 1, 0, 1, 0, 1, 0, 1};
-  const int slot_e[8] = {0, 0, 2, 2, 1, 1, 3, 3};
-  const int posA[8] = {4, 8, 6, 10, 20, 24, 22, 26};
-  uint32_t w[4], hw[2] = {0u, 0u};
-  for (int j = 0; j < 4; j++) {
-    const int b = j / 2, jj = j % 2;
-    uint32_t word = 0;
-    for (int s = 0; s < 8; s++) {
-      const int k = 64 * c + 32 * b + 8 * t + 4 * jj + slot_e[s];
-      const uint32_t u = real ? canon_u(qtype, qs, qh, slot_row8[s] ? row_g8 : row_g, K, k)
-                              : (qtype == 4 ? 8u : 32u);
-      word |= (u & 0xFu) << (4 * s);
-      if (qtype == 6) {
-        const int pos = jj == 0 ? posA[s] : (posA[s] + 24) % 32;  // rotl by 8 restores posA
-        hw[b] |= ((u >> 4) & 3u) << pos;
+  if (qtype == 8) {
+    // Q8: for block b and k pair j, one word holds bytes u = q + 128 of rows
+    // g, g, g+8, g+8 at k = 64c + 32b + 8t + 2j, +1 (the same k order as the
+    // 4-bit words): a byte permute turns it into two A registers.
+    const int nb = K / 32;
+    auto u8 = [&](int row, int k) -> uint32_t {
+      if (!real || k >= K) return 128u;
+      return (uint32_t)((int)(int8_t)qs[((size_t)row * nb + k / 32) * 32 + k % 32] + 128);
+    };
+    uint32_t w8[8];
+    for (int b = 0; b < 2; b++)
+      for (int j = 0; j < 4; j++) {
+        const int k = 64 * c + 32 * b + 8 * t + 2 * j;
+        w8[4 * b + j] = u8(row_g, k) | (u8(row_g, k + 1) << 8) | (u8(row_g8, k) << 16) |
+                        (u8(row_g8, k + 1) << 24);
       }
+    uint4* dst = reinterpret_cast<uint4*>(rec + Rec<8>::QS + i * Rec<8>::QS_TILE + lane * 32);
+    dst[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+    dst[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+  } else {
+    const int slot_row8[8] = {0, 1, 0, 1, 0, 1, 0, 1};
+    const int slot_e[8] = {0, 0, 2, 2, 1, 1, 3, 3};
+    const int posA[8] = {4, 8, 6, 10, 20, 24, 22, 26};
+    uint32_t w[4], hw[2] = {0u, 0u};
+    for (int j = 0; j < 4; j++) {
+      const int b = j / 2, jj = j % 2;
+      uint32_t word = 0;
+      for (int s = 0; s < 8; s++) {
+        const int k = 64 * c + 32 * b + 8 * t + 4 * jj + slot_e[s];
+        const uint32_t u = real ? canon_u(qtype, qs, qh, slot_row8[s] ? row_g8 : row_g, K, k)
+                                : (qtype == 4 ? 8u : 32u);
+        word |= (u & 0xFu) << (4 * s);
+        if (qtype == 6) {
+          const int pos = jj == 0 ? posA[s] : (posA[s] + 24) % 32;  // rotl by 8 restores posA
+          hw[b] |= ((u >> 4) & 3u) << pos;
+        }
+      }
+      w[j] = word;
     }
-    w[j] = word;
+    *reinterpret_cast<uint4*>(rec + Rec<4>::QS + i * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (qtype == 6)
+      *reinterpret_cast<uint2*>(rec + Rec<6>::QH + i * 256 + lane * 8) = make_uint2(hw[0], hw[1]);
   }
-  *reinterpret_cast<uint4*>(rec + Rec<4>::QS + i * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-  if (qtype == 6)
-    *reinterpret_cast<uint2*>(rec + Rec<6>::QH + i * 256 + lane * 8) = make_uint2(hw[0], hw[1]);
   if (t == 0) {
     const int nb = K / 32;
     auto sc_of = [&](int row, int blk) -> uint32_t {
@@ -154,7 +186,8 @@ __global__ void pack_kernel(int qtype, const uint8_t* __restrict__ qs,
     };
     const uint32_t s0 = sc_of(row_g, 2 * c) | (sc_of(row_g8, 2 * c) << 16);
     const uint32_t s1 = sc_of(row_g, 2 * c + 1) | (sc_of(row_g8, 2 * c + 1) << 16);
-    *reinterpret_cast<uint2*>(rec + Rec<4>::SC + i * 64 + g * 8) = make_uint2(s0, s1);
+    const int sc_off = qtype == 8 ? Rec<8>::SC : Rec<4>::SC;
+    *reinterpret_cast<uint2*>(rec + sc_off + i * 64 + g * 8) = make_uint2(s0, s1);
   }
 }
 
@@ -238,6 +271,23 @@ __device__ __forceinline__ void dequant_step(uint32_t w, uint32_t hx, uint32_t (
   }
 }
 
+// Two A registers from one Q8 word (bytes u = q + 128 of rows r, r, r', r'
+// at k, k+1): the byte permute makes each half 0x64uu, which is 1024 + u
+// exactly, and one packed FMA gives (1024 + u) * 2^-20 - 1152 * 2^-20 =
+// q * 2^-20.  That value is a multiple of 2^-24 below 2^-12, so it is an
+// fp16 number (a subnormal for |q| < 64) and the FMA is exact.  The unit
+// 2^-20 is the 4/6-bit fragments' (16u * 2^-24 from mantissa bit 4 up).
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const __half2 unit = __halves2half2(__ushort_as_half(0x0010), __ushort_as_half(0x0010));  // 2^-20
+  const __half2 off = __halves2half2(__ushort_as_half(0x9480), __ushort_as_half(0x9480));   // -1152 * 2^-20
+  const uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);  // rows r: k, k+1
+  const uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);  // rows r': k, k+1
+  const __half2 ha = __hfma2(*reinterpret_cast<const __half2*>(&a), unit, off);
+  const __half2 hb = __hfma2(*reinterpret_cast<const __half2*>(&b), unit, off);
+  lo = *reinterpret_cast<const uint32_t*>(&ha);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+}
+
 // The unit of the dequantised fragments, undone in the epilogue: 2^20.
 constexpr float FRAG_UNIT = 1048576.0f;
 
@@ -255,9 +305,9 @@ __device__ __forceinline__ void zero_point_frag(uint32_t (&A)[4]) {
 
 // One chunk: the pair's 2 tiles x 64 k against the staged activations.
 // Per 32-block and column tile, C = -bias * sum(x) (two MMAs with the
-// zero-point fragment, shared by both tiles) starts each block's fresh
-// accumulator; the block's two k16 MMAs add sum(u * x); one FMA per element
-// (packed in pairs) folds the block scale into the running sum.
+// zero-point fragment, shared by both tiles; zero for Q8) starts each
+// block's fresh accumulator; the block's two k16 MMAs add sum(u * x); one FMA
+// per element (packed in pairs) folds the block scale into the running sum.
 template <int QT, int NCT>
 __device__ __forceinline__ void compute_chunk(const unsigned char* st, const unsigned char* xs,
                                               int xstride, int j, int lane,
@@ -271,19 +321,24 @@ __device__ __forceinline__ void compute_chunk(const unsigned char* st, const uns
     xb[ct][0] = *reinterpret_cast<const uint4*>(row);
     xb[ct][1] = *reinterpret_cast<const uint4*>(row + 64);
   }
-  uint32_t Z[4];
-  zero_point_frag<QT>(Z);
   float zc[NCT][2][4];
+  if constexpr (QT != 8) {
+    uint32_t Z[4];
+    zero_point_frag<QT>(Z);
 #pragma unroll
-  for (int ct = 0; ct < NCT; ct++)
+    for (int ct = 0; ct < NCT; ct++)
 #pragma unroll
-    for (int b = 0; b < 2; b++) {
-      mma_16816_zero(zc[ct][b], Z, xb[ct][b].x, xb[ct][b].y);
-      mma_16816(zc[ct][b], Z, xb[ct][b].z, xb[ct][b].w);
-    }
+      for (int b = 0; b < 2; b++) {
+        mma_16816_zero(zc[ct][b], Z, xb[ct][b].x, xb[ct][b].y);
+        mma_16816(zc[ct][b], Z, xb[ct][b].z, xb[ct][b].w);
+      }
+  }
 #pragma unroll
   for (int i = 0; i < TPW; i++) {
-    const uint4 aw = *reinterpret_cast<const uint4*>(st + RC::QS + i * 512 + lane * 16);
+    uint4 aw, aw8 = make_uint4(0, 0, 0, 0);
+    aw = *reinterpret_cast<const uint4*>(st + RC::QS + i * RC::QS_TILE + lane * (QT == 8 ? 32 : 16));
+    if constexpr (QT == 8)
+      aw8 = *reinterpret_cast<const uint4*>(st + RC::QS + i * RC::QS_TILE + lane * 32 + 16);
     const uint2 sw = *reinterpret_cast<const uint2*>(st + RC::SC + i * 64 + g * 8);
     uint2 hw = make_uint2(0, 0);
     if constexpr (QT == 6) hw = *reinterpret_cast<const uint2*>(st + RC::QH + i * 256 + lane * 8);
@@ -298,14 +353,25 @@ __device__ __forceinline__ void compute_chunk(const unsigned char* st, const uns
         hB = __funnelshift_l(hA, hA, 8);
       }
       uint32_t A0[4], A1[4];
-      dequant_step<QT>(words[2 * b], hA, A0);
-      dequant_step<QT>(words[2 * b + 1], hB, A1);
+      if constexpr (QT == 8) {
+        const uint4 q = b == 0 ? aw : aw8;
+        dequant8(q.x, A0[0], A0[1]);
+        dequant8(q.y, A0[2], A0[3]);
+        dequant8(q.z, A1[0], A1[1]);
+        dequant8(q.w, A1[2], A1[3]);
+      } else {
+        dequant_step<QT>(words[2 * b], hA, A0);
+        dequant_step<QT>(words[2 * b + 1], hB, A1);
+      }
       const float sg = b == 0 ? s0.x : s1.x;   // row g
       const float sg8 = b == 0 ? s0.y : s1.y;  // row g+8
 #pragma unroll
       for (int ct = 0; ct < NCT; ct++) {
         float blk[4];
-        mma_16816_c(blk, A0, xb[ct][b].x, xb[ct][b].y, zc[ct][b]);
+        if constexpr (QT == 8)
+          mma_16816_zero(blk, A0, xb[ct][b].x, xb[ct][b].y);
+        else
+          mma_16816_c(blk, A0, xb[ct][b].x, xb[ct][b].y, zc[ct][b]);
         mma_16816(blk, A1, xb[ct][b].z, xb[ct][b].w);
         // two packed FMAs (each half rounded exactly as fmaf)
         const float2 r01 = __ffma2_rn(make_float2(sg, sg), make_float2(blk[0], blk[1]),
@@ -466,7 +532,7 @@ linear_q_kernel(const LinArgs a) {
   const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c_begin;
   const int w_lo = ks * nc / KW;
   const int wn = (ks + 1) * nc / KW - w_lo;
-  constexpr int CPS = cps<NCT>();
+  constexpr int CPS = cps<QT, NCT>();
   constexpr int SB = CPS * RC::BYTES;  // bytes of a full stage
   unsigned char* ring = smem + warp * NS * SB;
   const uint32_t ring_s = smem_addr(ring);
@@ -809,6 +875,8 @@ LinKernel kernel_for(int qtype, int nct, int kw) {
   SPEC_LIN_K(4, 2, 1) SPEC_LIN_K(4, 2, 2) SPEC_LIN_K(4, 2, 4) SPEC_LIN_K(4, 2, 8)
   SPEC_LIN_K(6, 1, 1) SPEC_LIN_K(6, 1, 2) SPEC_LIN_K(6, 1, 4) SPEC_LIN_K(6, 1, 8)
   SPEC_LIN_K(6, 2, 1) SPEC_LIN_K(6, 2, 2) SPEC_LIN_K(6, 2, 4) SPEC_LIN_K(6, 2, 8)
+  SPEC_LIN_K(8, 1, 1) SPEC_LIN_K(8, 1, 2) SPEC_LIN_K(8, 1, 4) SPEC_LIN_K(8, 1, 8)
+  SPEC_LIN_K(8, 2, 1) SPEC_LIN_K(8, 2, 2) SPEC_LIN_K(8, 2, 4) SPEC_LIN_K(8, 2, 8)
 #undef SPEC_LIN_K
   return nullptr;
 }
@@ -823,13 +891,16 @@ struct LinCfg {
 // retires chunks at min(SM rate, resident warps x warp rate), a launch costs
 // a fixed start-up, a K split adds a ticket and the last CTA's partial loads,
 // KW > 1 the shared-memory slice sum, and each further wave a start-up.
+// The Q8 rates are not fitted: an SM's rate is its share of the copy
+// bandwidth in 2176-byte chunks, a warp's that of Q4 (about as many
+// instructions per chunk).
 struct LinModel {
-  double sm_rate[2], warp_rate[2];  // chunks / us (Q4, Q6)
+  double sm_rate[3], warp_rate[3];  // chunks / us (Q4, Q6, Q8)
   double t_start, t_split, t_batch, t_slices, t_wave;  // us
 };
 constexpr LinModel MODEL_NCT[2] = {
-    {{32.4, 26.0}, {3.55, 2.82}, 2.46, 1.59, 0.70, 0.56, 3.08},
-    {{23.9, 20.9}, {2.37, 2.10}, 4.71, 1.66, 0.66, 0.0, 3.28},
+    {{32.4, 26.0, 20.0}, {3.55, 2.82, 3.4}, 2.46, 1.59, 0.70, 0.56, 3.08},
+    {{23.9, 20.9, 18.0}, {2.37, 2.10, 2.3}, 4.71, 1.66, 0.66, 0.0, 3.28},
 };
 
 double model_time(const LinModel& M, int qtype, int nct, int kw, int S, int n_pairs, int nch,
@@ -843,7 +914,7 @@ double model_time(const LinModel& M, int qtype, int nct, int kw, int S, int n_pa
                                                 smem_bytes(qtype, nct, nc));
   cudaGetLastError();
   per_sm = std::max(per_sm, 1);
-  const int q = qtype == 4 ? 0 : 1;
+  const int q = qtype == 4 ? 0 : (qtype == 6 ? 1 : 2);
   const double ctas = (double)n_grp * S;
   const double load = std::ceil(ctas / sms);  // CTAs of the busiest SM
   const double resident = std::min((double)per_sm, load);
@@ -884,8 +955,8 @@ LinCfg choose_config(int qtype, int n_pairs, int nch, int sms) {
 int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaStream_t st,
               QMat* out) {
   if (w == nullptr || out == nullptr) return fail(SPEC_E_INVALID, "null qweight");
-  if (w->qtype != SPEC_Q4 && w->qtype != SPEC_Q6)
-    return fail(SPEC_E_UNSUPPORTED, "qtype must be SPEC_Q4 or SPEC_Q6");
+  if (w->qtype != SPEC_Q4 && w->qtype != SPEC_Q6 && w->qtype != SPEC_Q8)
+    return fail(SPEC_E_UNSUPPORTED, "qtype must be SPEC_Q4, SPEC_Q6 or SPEC_Q8");
   if (w->N <= 0 || w->K <= 0 || w->N % 16 != 0 || w->K % 32 != 0)
     return fail(SPEC_E_SHAPE, "need N % 16 == 0 and K % 32 == 0");
   if (w->K > 64 * NC_CTA_MAX * MAX_SPLIT) return fail(SPEC_E_SHAPE, "K above 262144 is not supported");
@@ -903,7 +974,7 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaS
   q.nch = q.Kp / 64;
   q.n_tiles = q.N / 16;
   q.n_pairs = (q.n_tiles + TPW - 1) / TPW;
-  q.rec_bytes = q.qtype == 4 ? Rec<4>::BYTES : Rec<6>::BYTES;
+  q.rec_bytes = rec_bytes(q.qtype);
   LinCfg cfg = choose_config(q.qtype, q.n_pairs, q.nch, sms);
   if (const char* e = std::getenv("SPEC_VERIFY_LINEAR_SPLIT")) {
     // Overrides the choice (for tests and tuning): comma-separated entries,
@@ -1017,7 +1088,7 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
 }
 
 void linear_init_attrs() {
-  for (int qt : {4, 6})
+  for (int qt : {4, 6, 8})
     for (int nct : {1, 2})
       for (int kw : {1, 2, 4, 8})
         cudaFuncSetAttribute(kernel_for(qt, nct, kw), cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -33,6 +33,7 @@ import numpy as np
 
 Q4_SCALE = 0.01   # fp16(|N(0,1)| * 0.01)
 Q6_SCALE = 0.005  # fp16(|N(0,1)| * 0.005)
+Q8_SCALE = 0.000625  # fp16(|N(0,1)| * 0.000625): the Q4 weights' range at 8 bits
 # The decoder workloads' Q6 LM head: fp16(|N(0,1)| * 0.0015), which gives
 # logits with a standard deviation of about 3 (at the sweep's 0.005 it is
 # 9-12, far peakier than a language model's)
@@ -46,6 +47,8 @@ WL_ACCEPT_STOCH = dict(name="accept_stochastic_12seq_d7_V248320", n_seq=12, d=7,
 WL_LINEAR_SWEEP = dict(name="linear_sweep_q4_5120x13824_q6_13824x5120",
                        mats=[(4, 5120, 13824), (6, 13824, 5120)],
                        nts=[1, 2, 3, 4, 8, 9, 16], seed=0)
+WL_LINEAR_SWEEP_Q8 = dict(name="linear_sweep_q8_5120x13824",
+                          mats=[(8, 5120, 13824)], nts=[1, 2, 3, 4, 8, 9, 16], seed=1)
 WL_DECODER8 = dict(name="decoder8_H4096_V151936_ctx4096_nt8", n_layers=8,
                    hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
                    ffn=14336, vocab=151936, ctx=4096, n_seq=1, d=7,
@@ -71,15 +74,21 @@ def rng(seed: int) -> np.random.Generator:
 # --------------------------------------------------------------------------
 # host (numpy) generators, for sizes the oracle handles directly
 # --------------------------------------------------------------------------
+QT_RANGE = {4: (-8, 7), 6: (-32, 31), 8: (-128, 127)}
+QT_SCALE = {4: Q4_SCALE, 6: Q6_SCALE, 8: Q8_SCALE}
+
+
 def q_ints(g: np.random.Generator, qtype: int, N: int, K: int) -> np.ndarray:
-    lo, hi = (-8, 7) if qtype == 4 else (-32, 31)
+    lo, hi = QT_RANGE[qtype]
     return g.integers(lo, hi + 1, size=(N, K), dtype=np.int8)
 
 
 def pack_canonical(qtype: int, q: np.ndarray):
-    """ints q[N][K] -> (qs[N][K/32][16], qh[N][K/32][8] or None)."""
+    """ints q[N][K] -> (qs[N][K/32][16] (Q8: [32]), qh[N][K/32][8] or None)."""
     N, K = q.shape
     assert K % 32 == 0
+    if qtype == 8:  # one two's-complement byte per element, in element order
+        return np.ascontiguousarray(q.astype(np.int8).view(np.uint8).reshape(N, K // 32, 32)), None
     u = (q.astype(np.int16) + (8 if qtype == 4 else 32)).astype(np.uint8)
     u = u.reshape(N, K // 32, 32)
     lo = u & 0xF
@@ -99,7 +108,7 @@ def scales_f16(g: np.random.Generator, N: int, K: int, mult: float) -> np.ndarra
 
 def q_weight(g: np.random.Generator, qtype: int, N: int, K: int, mult=None):
     """Returns dict(qtype, N, K, q (ints), qs, qh, scales (fp16 bits))."""
-    mult = (Q4_SCALE if qtype == 4 else Q6_SCALE) if mult is None else mult
+    mult = QT_SCALE[qtype] if mult is None else mult
     q = q_ints(g, qtype, N, K)
     qs, qh = pack_canonical(qtype, q)
     return dict(qtype=qtype, N=N, K=K, q=q, qs=qs, qh=qh,
@@ -145,12 +154,13 @@ def torch_gen(seed: int, device):
 def q_weight_torch(gen, qtype: int, N: int, K: int, device, mult=None):
     """Uniform random planes on the device: a uniform byte is two uniform
     nibbles (u uniform in [0,15] <=> q uniform in [-8,7]); uniform qh bytes
-    give uniform 2-bit fields (u uniform in [0,63] for Q6)."""
+    give uniform 2-bit fields (u uniform in [0,63] for Q6); a uniform Q8
+    byte is q uniform in [-128,127]."""
     import torch
-    mult = (Q4_SCALE if qtype == 4 else Q6_SCALE) if mult is None else mult
+    mult = QT_SCALE[qtype] if mult is None else mult
     nb = K // 32
-    qs = torch.randint(0, 256, (N, nb, 16), generator=gen, device=device,
-                       dtype=torch.uint8)
+    qs = torch.randint(0, 256, (N, nb, 32 if qtype == 8 else 16), generator=gen,
+                       device=device, dtype=torch.uint8)
     qh = None
     if qtype == 6:
         qh = torch.randint(0, 256, (N, nb, 8), generator=gen, device=device,

@@ -28,7 +28,7 @@ def run_linear(sv, qm, x_dev, nt):
 
 
 @pytest.mark.parametrize("qtype,N,K", [(4, 48, 96), (6, 64, 160), (4, 16, 32), (6, 272, 544),
-                                       (4, 512, 1024)])
+                                       (4, 512, 1024), (8, 48, 96), (8, 272, 544), (8, 16, 32)])
 def test_linear_small_matches_oracle(orc, dev, qtype, N, K):
     """Several tiles and K chunks, ragged K tail (K % 64 == 32), ragged
     tile groups; every nt of the sweep."""
@@ -47,7 +47,7 @@ def test_linear_small_matches_oracle(orc, dev, qtype, N, K):
         assert np.array_equal(y, y16[:nt]), f"row invariance broken at nt={nt}"
 
 
-@pytest.mark.parametrize("qtype,N,K", [(4, 5120, 13824), (6, 13824, 5120)])
+@pytest.mark.parametrize("qtype,N,K", [(4, 5120, 13824), (6, 13824, 5120), (8, 5120, 13824)])
 def test_linear_full_size_sweep(orc, dev, qtype, N, K):
     """The linear sweep at full size: every nt, all outputs against the
     oracle (nt=16), and bitwise invariance of every row across nt."""
@@ -66,7 +66,7 @@ def test_linear_full_size_sweep(orc, dev, qtype, N, K):
 
 
 @pytest.mark.parametrize("split", ["1:1", "1:5", "2:3", "4:1", "4:17", "8:2", "8:6"])
-@pytest.mark.parametrize("qtype,N,K", [(4, 272, 1056), (6, 144, 2080)])
+@pytest.mark.parametrize("qtype,N,K", [(4, 272, 1056), (6, 144, 2080), (8, 208, 1568)])
 def test_linear_every_split_matches_oracle(orc, dev, monkeypatch, qtype, N, K, split):
     """Every in-CTA K slicing (KW warps per tile pair) and several K segment
     counts S, forced through SPEC_VERIFY_LINEAR_SPLIT: an odd number of tiles

@@ -57,11 +57,13 @@ def check_greedy(orc, logits_gpu, ref, draft, n_acc, em, nt):
     assert np.array_equal(n_acc, n_ref) and np.array_equal(em, em_ref)
 
 
-@pytest.mark.parametrize("graphs", [True, False])
-def test_round_greedy_matches_oracle(orc, dev, graphs):
+@pytest.mark.parametrize("graphs,qtype,lm_qtype", [(True, 4, 6), (False, 4, 6), (True, 8, 8),
+                                                  (True, 6, 4)])
+def test_round_greedy_matches_oracle(orc, dev, graphs, qtype, lm_qtype):
+    """Layer linears and LM head in each block format (Q4/Q6, q8_0, Q6/Q4)."""
     import speculative_decoding_verification_round_gb300 as sv
     g = np.random.default_rng(41)
-    cfg, raw = small_decoder(g)
+    cfg, raw = small_decoder(g, qtype=qtype, lm_qtype=lm_qtype)
     n_seq, d, max_ctx = 3, 5, 300
     m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, n_seq)
     m.set_graphs(graphs)

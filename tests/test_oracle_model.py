@@ -20,13 +20,13 @@ def test_f16_conversion_matches_numpy(orc):
     assert np.array_equal(back, ref.view(np.float16).astype(np.float64))
 
 
-@pytest.mark.parametrize("qtype", [4, 6])
+@pytest.mark.parametrize("qtype", [4, 6, 8])
 def test_unpack_round_trips_generator_ints(orc, qtype):
     g = np.random.default_rng(2)
     N, K = 48, 256
     w = synth.q_weight(g, qtype, N, K)
-    # every representable int appears in the first rows (exhaustive values)
-    lo, hi = (-8, 7) if qtype == 4 else (-32, 31)
+    # every representable int appears in the first row (exhaustive values)
+    lo, hi = {4: (-8, 7), 6: (-32, 31), 8: (-128, 127)}[qtype]
     vals = np.arange(lo, hi + 1, dtype=np.int8)
     w["q"][0, :vals.size] = vals
     w["qs"], w["qh"] = synth.pack_canonical(qtype, w["q"])
@@ -37,7 +37,20 @@ def test_unpack_round_trips_generator_ints(orc, qtype):
     assert np.array_equal(deq, expect)
 
 
-@pytest.mark.parametrize("qtype", [4, 6])
+def test_q8_block_is_twos_complement_bytes_in_element_order(orc):
+    """A q8_0 block written out by hand: byte j is element j as an int8
+    (0x80 = -128, 0xff = -1, 0x7f = 127), times the block's fp16 scale."""
+    blk = np.array([0x00, 0x01, 0x7f, 0x80, 0x81, 0xff, 0xfe, 0x40] + list(range(0x10, 0x28)),
+                   np.uint8)
+    qs = np.stack([blk, blk[::-1]]).reshape(1, 2, 32)
+    scales = np.array([[0.5, -0.25]], np.float16).view(np.uint16)
+    deq = orc.dequant(orc.QWeight(8, qs, None, scales, 1, 64))[0]
+    first = [0, 1, 127, -128, -127, -1, -2, 64] + list(range(16, 40))
+    assert deq[:32].tolist() == [0.5 * v for v in first]
+    assert deq[32:].tolist() == [-0.25 * v for v in first[::-1]]
+
+
+@pytest.mark.parametrize("qtype", [4, 6, 8])
 def test_one_hot_activation_returns_weight_column(orc, qtype):
     g = np.random.default_rng(3)
     N, K = 40, 128
@@ -54,7 +67,8 @@ def test_one_hot_activation_returns_weight_column(orc, qtype):
         assert np.array_equal(y[r], expect)
 
 
-@pytest.mark.parametrize("qtype,N,K,R", [(4, 64, 512, 3), (6, 80, 320, 9), (4, 16, 32, 1)])
+@pytest.mark.parametrize("qtype,N,K,R", [(4, 64, 512, 3), (6, 80, 320, 9), (4, 16, 32, 1),
+                                         (8, 48, 288, 5)])
 def test_linear_matches_numpy_float64_matmul(orc, qtype, N, K, R):
     g = np.random.default_rng(4)
     w = synth.q_weight(g, qtype, N, K)

@@ -41,14 +41,16 @@ def oracle_qweight(orc, w):
     return orc.QWeight(w["qtype"], w["qs"], w["qh"], w["scales"], w["N"], w["K"])
 
 
-def small_decoder(g, L=2, H=256, nq=4, nkv=2, hd=64, F=128, V=512, lm_qtype=6, mult=None):
-    """Block scales default to the workloads' (|N(0,1)| * 0.01 for Q4,
-    * 0.005 for Q6)."""
+def small_decoder(g, L=2, H=256, nq=4, nkv=2, hd=64, F=128, V=512, lm_qtype=6, mult=None,
+                  qtype=4):
+    """Layer linears in `qtype`, the LM head in `lm_qtype`.  Block scales
+    default to the workloads' (|N(0,1)| * 0.01 for Q4, * 0.005 for Q6,
+    * 0.000625 for Q8)."""
     mk = lambda qt, N, K: synth.q_weight(g, qt, N, K, mult=mult)
-    raw = dict(wqkv=[mk(4, (nq + 2 * nkv) * hd, H) for _ in range(L)],
-               wo=[mk(4, H, nq * hd) for _ in range(L)],
-               wgu=[mk(4, 2 * F, H) for _ in range(L)],
-               wd=[mk(4, H, F) for _ in range(L)], lm_head=mk(lm_qtype, V, H))
+    raw = dict(wqkv=[mk(qtype, (nq + 2 * nkv) * hd, H) for _ in range(L)],
+               wo=[mk(qtype, H, nq * hd) for _ in range(L)],
+               wgu=[mk(qtype, 2 * F, H) for _ in range(L)],
+               wd=[mk(qtype, H, F) for _ in range(L)], lm_head=mk(lm_qtype, V, H))
     raw["embed"] = synth.f16_normal(g, (V, H))
     raw["norm_w"] = synth.norm_gammas(g, 2 * L + 1, H)
     cfg = dict(n_layers=L, hidden=H, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd, ffn=F, vocab=V)
