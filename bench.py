@@ -95,11 +95,13 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path=None):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
         self.start_line = 0
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(),
+                                         f"spec_verify_clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -571,7 +573,7 @@ def run_ours(args):
     barrier(dist)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clocks_csv) as clk:
         torch.cuda.nvtx.range_push("timed")
         e0.record(st)
         for j in range(args.warmup, n_rounds):
@@ -808,6 +810,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the raw nvidia-smi clock samples in this file")
     args = ap.parse_args()
     if args.linear_only:
         linear_only(args.linear_only)

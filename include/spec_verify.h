@@ -256,7 +256,7 @@ int spec_accept_stochastic(const float* p_logits, const float* q_logits,
  * this entry point allocates no memory at all.  It is for callers that cannot
  * call cudaMalloc: code running while a stream is being captured into a CUDA
  * graph, code whose device memory is owned by a custom allocator that forbids
- * the driver's, and latency-critical loops that must not risk the implicit
+ * cudaMalloc, and latency-critical loops that must not risk the implicit
  * device synchronisation an allocation can cause.  (The pages have no
  * counterpart for this entry point; it is an addition of this library.)
  *  - Scratch is one fixed array in the library's device globals (about 64 KB
