@@ -800,6 +800,35 @@ def linear_only(spec: str, nt: int = 8, reps: int = 3):
     print("linear-only ok")
 
 
+def draft_only(n_layers: int, warm: int = 3, reps: int = 3):
+    """Profiling driver: nt = 1 forwards (graph-replayed d = 0 rounds) of the
+    0.5B-class draft at `n_layers` layers and a 4096-position context; the
+    last `reps` run inside the NVTX range "draft"."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from speculative_decoding_verification_round_gb300 import synth
+    dev = torch.device("cuda:0")
+    wl = dict(synth.WL_DRAFT05B, n_layers=n_layers)
+    dm, W = build_model(sv, synth, wl, dev, wl["ctx"] + 64)
+    del W
+    fill_context(sv, synth, dm, wl, dev, seed=7)
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    em = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    sv.spec_state_set(dm, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[1234])
+    for _ in range(warm):
+        sv.spec_verify_round(dm, 1, sid, None, 0, n_acc=n_acc, emitted=em)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("draft")
+    for _ in range(reps):
+        sv.spec_verify_round(dm, 1, sid, None, 0, n_acc=n_acc, emitted=em)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    assert sv.spec_error_check(dm) == 0
+    dm.close()
+    print("draft-only ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--linear-only", default=None,
@@ -812,9 +841,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None,
                     help="keep the raw nvidia-smi clock samples in this file")
+    ap.add_argument("--draft-only", type=int, default=None, metavar="LAYERS",
+                    help="profiling driver: nt = 1 forwards of the 0.5B-class draft")
     args = ap.parse_args()
     if args.linear_only:
         linear_only(args.linear_only)
+        return
+    if args.draft_only:
+        draft_only(args.draft_only)
         return
     if args.warmup < 3:
         args.warmup = 3
