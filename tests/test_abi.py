@@ -56,3 +56,25 @@ def test_host_side_checks_fail_closed_without_gpu(libpath):
     h = ctypes.c_void_p()
     assert L.spec_qmat_create(ctypes.byref(qw), 16, None, ctypes.byref(h)) != sv.SPEC_OK
     assert L.spec_accept_greedy(None, None, 1, 1, None, None, None) == sv.SPEC_E_INVALID
+
+
+def test_binding_constants_match_the_header():
+    """The binding's copies of the header's #defines (block formats, the row
+    limit, error codes) are the header's values."""
+    import speculative_decoding_verification_round_gb300 as sv
+    text = open(os.path.join(ROOT, "include", "spec_verify.h")).read()
+    defs = dict(re.findall(r"^#define\s+(SPEC_\w+)\s+\(?(-?\d+)\)?", text, flags=re.M))
+    for name in ["SPEC_OK", "SPEC_E_INVALID", "SPEC_E_SHAPE", "SPEC_E_CUDA", "SPEC_E_OOM",
+                 "SPEC_E_UNSUPPORTED", "SPEC_E_TIMEOUT", "SPEC_Q4", "SPEC_Q6", "SPEC_Q8",
+                 "SPEC_MAX_NT"]:
+        assert name in defs, name
+        assert getattr(sv, name) == int(defs[name]), name
+
+
+def test_q8_weight_without_its_plane_fails_closed(libpath):
+    import speculative_decoding_verification_round_gb300 as sv
+    L = sv.lib()
+    h = ctypes.c_void_p()
+    qw = sv.spec_qweight(sv.SPEC_Q8, 16, 64, None, None, None)
+    assert L.spec_qmat_create(ctypes.byref(qw), 16, None, ctypes.byref(h)) == sv.SPEC_E_INVALID
+    assert "plane" in sv.last_error()
