@@ -4,14 +4,16 @@ This module only draws random numbers and lays them out in the canonical
 block formats; it holds none of the verify round's arithmetic.  Both the CUDA
 path and the oracle are fed from here.
 
-Canonical block layout (the pages name 4-bit and 6-bit block formats, but do
-not fix the bits; this is the reading used throughout):
+Canonical block layout (the pages name 4-bit, 6-bit and 8-bit block formats,
+but do not fix the bits; this is the reading used throughout):
   * Q4, blocks of 32 along K: ``qs[n][b][16]`` bytes; byte j holds element j
     in its low nibble and element j+16 in its high nibble, stored as
     ``u = q + 8`` with ``q`` in [-8, 7].
   * Q6, blocks of 32: the low 4 bits of ``u = q + 32`` in ``qs`` (same nibble
     order), the high 2 bits in ``qh[n][b][8]``: element j at bits
     ``2*(j%4)`` of byte ``j//4``; ``q`` in [-32, 31].
+  * Q8 (q8_0), blocks of 32: ``qs[n][b][32]`` bytes, byte j = element j as
+    a two's-complement int8, ``q`` in [-128, 127].
   * ``scales[n][b]``: fp16 bits; weight = scale * q.
 
 Workloads (value distributions of the pages' configurations):
@@ -26,6 +28,9 @@ Workloads (value distributions of the pages' configurations):
   * WL_DECODER14B      40 layers, H=5120, 40/8 heads, FFN 13824, Q6 LM head
                        V=248320, 12 sequences x 512 cached positions, nt=16,
                        T=0.7.
+  * WL_LINEAR_SWEEP_Q8 q8_0 5120x13824 at the same nts.
+  * WL_DRAFT05B        a 0.5B-class draft: 24 layers, H=896, 14/2 heads of
+                       64, FFN 4864, V=151936, Q4 weights and LM head.
 """
 from __future__ import annotations
 
