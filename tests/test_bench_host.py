@@ -1,0 +1,84 @@
+"""Host-side logic of bench.py that the measurement contract rests on: the
+clock summary taken from nvidia-smi samples (only samples inside the timed
+region count; throttle reasons are reported) and the DRAM-traffic record
+(used only while it was taken on the current verify-GEMM source).  CPU only."""
+import hashlib
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def sample(mhz, mx=2070, hw="Not Active", thermal="Not Active", power="Not Active"):
+    return f"0, {mhz}, {mx}, 900.0, 0x0, {hw}, {thermal}, Not Active, {power}\n"
+
+
+def sampler_with(tmp_path, before, during):
+    path = tmp_path / "clocks.csv"
+    path.write_text("".join(before + during))
+    c = bench.ClockSampler(0, str(path))
+    c.proc = object()           # as if nvidia-smi had been started
+    c.start_line = len(before)  # lines present when the timed region began
+    return c
+
+
+def test_only_samples_inside_the_timed_region_count(tmp_path):
+    c = sampler_with(tmp_path, [sample(345), sample(345)],
+                     [sample(2070), sample(2055), sample(2070, power="Active")])
+    s = c.summary()
+    assert s["sm_mhz"] == 2070 and s["sm_max_mhz"] == 2070
+    assert s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_throttle_reasons_are_reported(tmp_path):
+    c = sampler_with(tmp_path, [], [sample(1500, hw="Active"), sample(1490, thermal="Active")])
+    s = c.summary()
+    assert s["sm_mhz"] == 1495
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+
+
+def test_a_region_shorter_than_the_interval_takes_the_last_sample(tmp_path):
+    c = sampler_with(tmp_path, [sample(2000), sample(2070)], [])
+    s = c.summary()
+    assert s["sm_mhz"] == 2070 and s["samples"] == 1
+
+
+def test_no_sampler_reports_unsampled():
+    c = bench.ClockSampler(0, "/nonexistent/clocks.csv")
+    assert c.summary()["reasons"] == ["unsampled"]
+
+
+def test_traffic_record_is_used_only_for_its_source(tmp_path, monkeypatch):
+    src = tmp_path / "linear.cu"
+    src.write_text("// kernel v1\n")
+    rec = tmp_path / "traffic.json"
+    rec.write_text(json.dumps({
+        "linear_cu_sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
+        "dram_bytes_per_launch": {"4:64:128": 100, "6:32:64": 400}}))
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(rec))
+    monkeypatch.setattr(bench, "LINEAR_SRC", str(src))
+    # per launch over the mix: (3 x 100 + 1 x 400) / 4
+    assert bench.measured_traffic([(4, 64, 128, 3), (6, 32, 64, 1)]) == pytest.approx(175.0)
+    assert bench.measured_traffic([(4, 64, 128, 1), (8, 16, 32, 1)]) is None  # shape not captured
+    src.write_text("// kernel v2\n")
+    assert bench.measured_traffic([(4, 64, 128, 3)]) is None                  # source changed
+
+
+def test_committed_traffic_record_shows_no_re_reads():
+    """The record under profiles/: every captured shape moved its packed
+    weight bytes once (within 10%).  A record older than linear.cu is not
+    used by the bench (traffic null) and is not judged here."""
+    rec = json.load(open(bench.TRAFFIC_RECORD))
+    sha = hashlib.sha256(open(bench.LINEAR_SRC, "rb").read()).hexdigest()
+    if rec["linear_cu_sha256"] != sha:
+        pytest.skip("the record predates linear.cu: the bench reports traffic null")
+    for key, b in rec["dram_bytes_per_launch"].items():
+        qt, N, K = map(int, key.split(":"))
+        alg = N * K * bench.WEIGHT_BYTES[qt]
+        assert 0.98 * alg <= b <= 1.10 * alg, key  # no re-reads
