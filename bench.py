@@ -1,21 +1,27 @@
 """Benchmark of the verify round on one GB300 (or N replicas).
 
-Step = one full greedy verify round (spec_verify_round) of the synthetic
-8-layer decoder: H=4096, 32 q / 8 kv heads of 128, SwiGLU FFN 14336, Q4
-linears, Q6 LM head over V=151936, 4096 cached positions, nt = 8 (anchor +
-7 drafts).  Drafts follow the target's own greedy chain with probability 0.74
-per position; they are recorded by an untimed pass of the same chain, and
-the timed steps replay that chain from the same starting state (every step
-recomputes the whole target pass: nothing is cached between steps).
+Step = one verify round of the batched 14B-shaped workload: a 40-layer
+decoder (H 5120, 40 query / 8 KV heads of 128, SwiGLU FFN 13824, Q4 linears,
+Q6 LM head over V = 248320), 12 sequences with 512 cached positions each,
+nt = 16 rows per sequence (anchor + 15 drafts: 192 rows in one weights-once
+target pass), strict rejection sampling at T = 0.7.  The draft logits come
+from a noisy-target drafter: the target's own nt = 1 logits along the draft
+chain plus N(0, 0.5) noise, each draft sampled from them.  The drafter runs
+untimed while the rounds are recorded; the timed steps replay the recorded
+rounds from the same starting state, and every step recomputes the whole
+target pass, the accept and the commit.
 
-Printed JSON line: value = emitted tokens per second of the rounds (accepted
-drafts + the one correction/bonus token per round), plus the verify-round
-latency, the weight-stream bandwidth of the verify GEMM against the HBM
-roofline, the nt sweep of the linear layers, the end-to-end number through
-host buffers, and the oracle's CPU rate.
+Printed JSON line: value = emitted tokens per second over the 12 sequences
+(accepted drafts + one correction or bonus token per sequence and round);
+the verify-round latency with graphs and with raw launches; the verify GEMM
+measured inside the round (CUDA events around each launch) against the
+tensor and HBM rooflines; the end-to-end rate through host buffers; the
+oracle's CPU rate; and compact legs for the other workloads (LM-head greedy
+round, standalone stochastic accept, linear sweep, 8-layer greedy decoder).
 
---impl reference times the CPU oracle (the plain fp64 reference of the same
-round) on the host cores, on the same workload and metric.
+--impl reference times the CPU oracle (the plain fp64 reference) on the
+same workload: each step is a bounded sample (one sequence, a 2-layer slice
+of the 40 layers plus the LM head), scaled to the full round.
 """
 from __future__ import annotations
 
@@ -37,12 +43,14 @@ METRIC = "verify-round µs at nt=1..16; weight-stream HBM GB/s vs peak; accepted
 
 
 def peaks():
+    """(HBM GB/s, sustained bf16 TFLOP/s, burst bf16 TFLOP/s, kind)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops_sustained"]), float(p["bf16_tflops"]),
+                "measured")
     except Exception:
-        return 6800.0, "fallback"
+        return 6800.0, 1700.0, 1900.0, "fallback"
 
 
 # --------------------------------------------------------------------------
@@ -90,18 +98,37 @@ def sum_over_ranks(dist, value: float, device=None) -> float:
 # --------------------------------------------------------------------------
 # clocks during the timed region
 # --------------------------------------------------------------------------
+def smi_id(local: int) -> str:
+    """The id nvidia-smi knows this process's CUDA device by: its PCI bus id
+    (CUDA_VISIBLE_DEVICES may renumber devices, nvidia-smi does not), else
+    its UUID, else the CUDA index."""
+    import torch
+    p = torch.cuda.get_device_properties(local)
+    try:
+        return f"{int(p.pci_domain_id):08X}:{int(p.pci_bus_id):02X}:{int(p.pci_device_id):02X}.0"
+    except Exception:
+        pass
+    try:
+        u = str(p.uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(local)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, path=None):
+    def __init__(self, gpu, path=None):
+        """gpu: what nvidia-smi --id takes (a PCI bus id, a UUID or an index)."""
         import tempfile
-        self.gpu = gpu_index
+        self.gpu = gpu
         self.proc = None
         self.start_line = 0
+        tag = "".join(ch if ch.isalnum() else "_" for ch in str(gpu))
         self.path = path or os.path.join(tempfile.gettempdir(),
-                                         f"spec_verify_clocks_rank{gpu_index}.csv")
+                                         f"spec_verify_clocks_{tag}.csv")
 
     def __enter__(self):
         try:
@@ -166,11 +193,17 @@ WEIGHT_BYTES = {4: 0.5625, 6: 0.8125, 8: 1.0625}
 
 
 def build_model(sv, synth, wl, dev, max_ctx):
+    """The workload's decoder with random-init weights (generated on the
+    device, repacked by the library; the canonical planes are dropped)."""
+    import torch
     W = synth.decoder_weights_torch(wl, dev)
     desc = dict(n_layers=wl["n_layers"], hidden=wl["hidden"], n_q_heads=wl["n_q_heads"],
                 n_kv_heads=wl["n_kv_heads"], head_dim=wl["head_dim"], ffn=wl["ffn"],
                 vocab=wl["vocab"], max_ctx=max_ctx, max_nt=sv.SPEC_MAX_NT, max_seqs=wl["n_seq"])
-    return sv.Model(desc, W), W
+    m = sv.Model(desc, W)
+    del W
+    torch.cuda.empty_cache()
+    return m
 
 
 def fill_context(sv, synth, m, wl, dev, seed=1):
@@ -226,14 +259,15 @@ class L2Flush:
         self.buf.amax()
 
 
-TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "linear_q_traffic_decoder8_nt8.json")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "linear_q_traffic_decoder14b_r192.json")
 LINEAR_SRC = os.path.join(ROOT, "speculative_decoding_verification_round_gb300", "csrc", "linear.cu")
 
 
 def measured_traffic(shapes):
-    """DRAM bytes per verify-GEMM launch over one round's launch mix, from the
-    committed ncu record of these shapes -- or None when the record is
-    missing, lacks a shape, or was taken on a different linear.cu."""
+    """DRAM bytes per verify-GEMM launch over a launch mix, from the committed
+    ncu record (profiles/, command inside) -- or None when the record is
+    missing, lacks a shape, or was taken on a different linear.cu.  shapes:
+    (qtype, N, K, launches[, rows]); a record key is "QT:N:K" or "QT:N:K:R"."""
     import hashlib
     try:
         rec = json.load(open(TRAFFIC_RECORD))
@@ -243,54 +277,15 @@ def measured_traffic(shapes):
     if rec.get("linear_cu_sha256") != sha:
         return None
     total, n = 0.0, 0
-    for qt, N, K, count in shapes:
-        b = rec.get("dram_bytes_per_launch", {}).get(f"{qt}:{N}:{K}")
+    for sh in shapes:
+        qt, N, K, count = sh[:4]
+        key = f"{qt}:{N}:{K}" + (f":{sh[4]}" if len(sh) > 4 else "")
+        b = rec.get("dram_bytes_per_launch", {}).get(key)
         if b is None:
             return None
         total += b * count
         n += count
     return total / n
-
-
-def time_dominant_kernel(sv, synth, wl, dev, hbm_peak, reps=20):
-    """The verify GEMM at the decoder's shapes, nt = 8, timed alone with CUDA
-    events on its stream; L2 flushed between launches.  Returns the achieved
-    weight-stream GB/s over one round's mix of launches (8 x [qkv, o,
-    gate/up, down] + the LM head)."""
-    import torch
-    H, F, hd, nq, nkv, V = (wl["hidden"], wl["ffn"], wl["head_dim"], wl["n_q_heads"],
-                            wl["n_kv_heads"], wl["vocab"])
-    shapes = [(4, (nq + 2 * nkv) * hd, H, wl["n_layers"]), (4, H, nq * hd, wl["n_layers"]),
-              (4, 2 * F, H, wl["n_layers"]), (4, H, F, wl["n_layers"]), (6, V, H, 1)]
-    gen = synth.torch_gen(5, dev)
-    st = torch.cuda.current_stream()
-    flush = L2Flush(dev)
-    nt = wl["d"] + 1
-    total_bytes, total_s, per = 0.0, 0.0, []
-    for qt, N, K, count in shapes:
-        w = synth.q_weight_torch(gen, qt, N, K, dev)
-        qm = sv.QMat(w, max_rows=16)
-        x = synth.f16_normal_torch(gen, (nt, K), dev).view(torch.int16)
-        y = torch.empty((nt, N), dtype=torch.float32, device=dev)
-        nbytes = N * K * WEIGHT_BYTES[qt] + nt * K * 2 + nt * N * 4
-        times = []
-        for i in range(reps + 3):
-            flush()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(st)
-            sv.spec_linear_q(qm, x, nt, y, st)
-            e1.record(st)
-            e1.synchronize()
-            if i >= 3:
-                times.append(e0.elapsed_time(e1) * 1e-3)
-        t = statistics.median(times)
-        per.append({"qtype": qt, "N": N, "K": K, "us": t * 1e6, "gbs": nbytes / t / 1e9})
-        total_bytes += nbytes * count
-        total_s += t * count
-        qm.close()
-        del w
-    gbs = total_bytes / total_s / 1e9
-    return gbs, per, total_bytes / (4 * wl["n_layers"] + 1), measured_traffic(shapes)
 
 
 ROUND_SWEEP_NTS = (1, 2, 3, 4, 8, 9, 16)
@@ -438,8 +433,7 @@ def full_round_run(sv, synth, m, wl, dev, max_ctx, rounds=ADAPTIVE_ROUNDS):
     out = {"draft_shape": synth.WL_DRAFT05B["name"], "p_agree": wl["p_agree"]}
     for n_layers in FULL_ROUND_DRAFT_LAYERS:
         dwl = dict(synth.WL_DRAFT05B, n_layers=n_layers)
-        dm, W = build_model(sv, synth, dwl, dev, max_ctx)
-        del W
+        dm = build_model(sv, synth, dwl, dev, max_ctx)
         fill_context(sv, synth, dm, dwl, dev, seed=7)
 
         def one_round(d, rng):
@@ -539,156 +533,325 @@ def nt_sweep(sv, synth, dev, reps=20, wl=None):
     return out
 
 
-def run_ours(args):
+# --------------------------------------------------------------------------
+# the batched stochastic workload (the step)
+# --------------------------------------------------------------------------
+def state0_of(wl):
+    n = wl["n_seq"]
+    return (list(range(n)), [wl["ctx"]] * n, [1000 * s for s in range(n)],
+            [(7919 * s + 1234) % wl["vocab"] for s in range(n)])
+
+
+def set_state(sv, m, st):
+    slots, n_past, ei, anc = st
+    sv.spec_state_set(m, slots, n_past=n_past, emit_idx=ei, anchor=anc)
+
+
+def record_stochastic(sv, synth, m, wl, dev, n_rounds, seed):
+    """Untimed: the speculative chain of all sequences, with the noisy-target
+    drafter.  Draft step i of a round: an nt = 1 target pass at the draft
+    position (a greedy d = 0 round with logits, state restored afterwards),
+    draft logits = those logits + N(0, q_noise), the draft sampled from
+    softmax(draft logits / T) (Gumbel-max on the device).  Then the round
+    itself (it commits).  Returns [(drafts [n_seq][d], q [n_seq][d][V])]."""
     import torch
-    import speculative_decoding_verification_round_gb300 as sv
-    from speculative_decoding_verification_round_gb300 import synth
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = init_dist(ws, "nccl")
-    wl = dict(synth.WL_DECODER8)
-    d, V = wl["d"], wl["vocab"]
-    max_ctx = wl["ctx"] + max(8 * (args.warmup + args.steps + 4),
-                              sv.SPEC_MAX_NT * ROUND_SWEEP_GROUP, sv.SPEC_MAX_NT * (ADAPTIVE_ROUNDS + 2)) + 64
-    hbm_peak, peak_kind = peaks()
-    m, W = build_model(sv, synth, wl, dev, max_ctx)
-    del W
-    torch.cuda.empty_cache()
-    fill_context(sv, synth, m, wl, dev, seed=1 + rank)
-    rng = np.random.default_rng(wl["seed"] + rank)
-    anchor = 1234
-    n_rounds = args.warmup + args.steps
-    drafts = record_chain(sv, synth, m, wl, dev, n_rounds, anchor, rng)
-    sid = torch.zeros(1, dtype=torch.int32, device=dev)
-    dr_dev = [torch.tensor([c], dtype=torch.int32, device=dev) for c in drafts]
-    n_acc = torch.zeros((n_rounds, 1), dtype=torch.int32, device=dev)
-    em = torch.zeros((n_rounds, 1, d + 1), dtype=torch.int32, device=dev)
+    n_seq, d, V, T = wl["n_seq"], wl["d"], wl["vocab"], wl["temperature"]
+    slots = list(range(n_seq))
+    sid = torch.arange(n_seq, dtype=torch.int32, device=dev)
+    gen = synth.torch_gen(seed, dev)
+    lg1 = torch.empty((n_seq, V), dtype=torch.float32, device=dev)
+    na1 = torch.empty(n_seq, dtype=torch.int32, device=dev)
+    em1 = torch.empty((n_seq, 1), dtype=torch.int32, device=dev)
+    n_acc = torch.empty(n_seq, dtype=torch.int32, device=dev)
+    em = torch.empty((n_seq, d + 1), dtype=torch.int32, device=dev)
+    rounds = []
+    for _ in range(n_rounds):
+        n_past, ei, anc = sv.spec_state_get(m, slots)
+        tok = list(anc)
+        qs = torch.empty((n_seq, d, V), dtype=torch.float32, device=dev)
+        dr = torch.empty((n_seq, d), dtype=torch.int32, device=dev)
+        for i in range(d):
+            sv.spec_state_set(m, slots, n_past=[p + i for p in n_past], anchor=tok)
+            sv.spec_verify_round(m, n_seq, sid, None, 0, n_acc=na1, emitted=em1, logits_out=lg1)
+            q_i = qs[:, i]
+            q_i.copy_(lg1)
+            q_i.add_(torch.randn((n_seq, V), generator=gen, device=dev), alpha=wl["q_noise"])
+            u = torch.rand((n_seq, V), generator=gen, device=dev)
+            x = torch.argmax(q_i / T - torch.log(-torch.log(u)), dim=1).to(torch.int32)
+            dr[:, i] = x
+            tok = x.tolist()
+        sv.spec_state_set(m, slots, n_past=n_past, emit_idx=ei, anchor=anc)
+        sv.spec_verify_round(m, n_seq, sid, dr, d, qs, False, T, seed, n_acc, em)
+        rounds.append((dr, qs))
+    assert sv.spec_error_check(m) == 0
+    return rounds
+
+
+def replay(sv, m, wl, dev, rounds, st0, warmup, steps, seed, clk=None):
+    """Warm-up rounds, then exactly `steps` rounds between two CUDA events
+    (device time); returns (seconds, n_acc [steps][n_seq] on the host)."""
+    import torch
+    n_seq, d, T = wl["n_seq"], wl["d"], wl["temperature"]
+    sid = torch.arange(n_seq, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros((warmup + steps, n_seq), dtype=torch.int32, device=dev)
+    em = torch.zeros((warmup + steps, n_seq, d + 1), dtype=torch.int32, device=dev)
     st = torch.cuda.current_stream()
-    # replay: warm-up rounds, then exactly K timed rounds
-    sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
-    for j in range(args.warmup):
-        sv.spec_verify_round(m, 1, sid, dr_dev[j], d, n_acc=n_acc[j], emitted=em[j])
-    torch.cuda.synchronize()
-    barrier(dist)
+    set_state(sv, m, st0)
+    for j in range(warmup):
+        dr, qs = rounds[j]
+        sv.spec_verify_round(m, n_seq, sid, dr, d, qs, False, T, seed, n_acc[j], em[j])
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local, args.clocks_csv) as clk:
-        torch.cuda.nvtx.range_push("timed")
+    if clk is not None:
+        clk.__enter__()
+    try:
         e0.record(st)
-        for j in range(args.warmup, n_rounds):
+        for j in range(warmup, warmup + steps):
+            dr, qs = rounds[j]
+            sv.spec_verify_round(m, n_seq, sid, dr, d, qs, False, T, seed, n_acc[j], em[j])
+        e1.record(st)
+        torch.cuda.synchronize()
+    finally:
+        if clk is not None:
+            clk.__exit__(None, None, None)
+    assert sv.spec_error_check(m) == 0
+    return e0.elapsed_time(e1) * 1e-3, n_acc[warmup:].cpu().numpy()
+
+
+def in_round_kernels(sv, m, wl, dev, rounds, st0, warmup, steps, seed):
+    """The round's kernels timed inside real rounds (spec_model_profile: raw
+    launches, a CUDA event before and after each GEMM / attention launch),
+    per kernel class: us per launch, achieved TFLOP/s and GB/s."""
+    set_state(sv, m, st0)
+    m.profile(True)
+    import torch
+    n_seq, d, T = wl["n_seq"], wl["d"], wl["temperature"]
+    sid = torch.arange(n_seq, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(n_seq, dtype=torch.int32, device=dev)
+    em = torch.zeros((n_seq, d + 1), dtype=torch.int32, device=dev)
+    for j in range(warmup + steps):
+        if j == warmup:
+            m.profile(True)  # totals of the timed rounds only
+        dr, qs = rounds[j]
+        sv.spec_verify_round(m, n_seq, sid, dr, d, qs, False, T, seed, n_acc, em)
+    names = {"qkv": sv.SPEC_PROF_QKV, "o": sv.SPEC_PROF_O, "gate_up": sv.SPEC_PROF_GATE_UP,
+             "down": sv.SPEC_PROF_DOWN, "lm_head": sv.SPEC_PROF_LM_HEAD,
+             "all_gemms": sv.SPEC_PROF_ALL_GEMMS, "attention": sv.SPEC_PROF_ATTN}
+    out = {}
+    for k, kind in names.items():
+        r = m.profile_read(kind)
+        n = max(r["launches"], 1)
+        out[k] = dict(launches=r["launches"], seconds=r["seconds"],
+                      us_per_launch=r["seconds"] / n * 1e6,
+                      tflops=r["flops"] / r["seconds"] / 1e12 if r["seconds"] else 0.0,
+                      gbs=r["bytes"] / r["seconds"] / 1e9 if r["seconds"] else 0.0,
+                      bytes_per_launch=r["bytes"] / n, flops_per_launch=r["flops"] / n)
+    m.profile(False)
+    assert sv.spec_error_check(m) == 0
+    return out
+
+
+def e2e_host(sv, m, wl, dev, rounds, st0, warmup, steps, seed):
+    """The same rounds through spec_verify_round_host: sequence ids and drafts
+    from host memory, the draft logits from pinned host memory (copied to the
+    device inside the call), n_acc and emitted back in host memory, every
+    step.  Returns (tokens, wall seconds, h2d bytes, d2h bytes per step)."""
+    import torch
+    n_seq, d, V, T = wl["n_seq"], wl["d"], wl["vocab"], wl["temperature"]
+    h_sid = np.arange(n_seq, dtype=np.int32)
+    h_dr = [dr.cpu().numpy() for dr, _ in rounds[:warmup + steps]]
+    h_q = []
+    for _, qs in rounds[:warmup + steps]:
+        t = torch.empty(qs.shape, dtype=torch.float32, pin_memory=True)
+        t.copy_(qs)
+        h_q.append(t)
+    h_acc = np.empty(n_seq, np.int32)
+    h_em = np.empty((n_seq, d + 1), np.int32)
+    set_state(sv, m, st0)
+    for j in range(warmup):
+        sv.spec_verify_round_host(m, n_seq, h_sid, h_dr[j], d, h_q[j], False, T, seed,
+                                  n_acc=h_acc, emitted=h_em)
+    torch.cuda.synchronize()
+    toks = 0
+    t0 = time.perf_counter()
+    for j in range(warmup, warmup + steps):
+        sv.spec_verify_round_host(m, n_seq, h_sid, h_dr[j], d, h_q[j], False, T, seed,
+                                  n_acc=h_acc, emitted=h_em)
+        toks += int((h_acc + 1).sum())
+    t = time.perf_counter() - t0
+    assert sv.spec_error_check(m) == 0
+    h2d = 4 * n_seq + 4 * n_seq * d + 4 * n_seq * d * V
+    d2h = 4 * n_seq + 4 * n_seq * (d + 1)
+    return toks, t, h2d, d2h
+
+
+# --------------------------------------------------------------------------
+# the other workloads (compact legs)
+# --------------------------------------------------------------------------
+def lmhead_leg(sv, synth, dev, hbm_peak, reps=50):
+    """H 1024, V 32000, d 2: the LM head (Q4, fused argmax, no logits) and the
+    greedy accept of drafts that agree with the target argmax w.p. 0.74; L2
+    flushed between rounds (18 MB of weights fit in L2)."""
+    import torch
+    wl = synth.WL_LMHEAD_GREEDY
+    H, V, d = wl["hidden"], wl["vocab"], wl["d"]
+    g = np.random.default_rng(wl["seed"])
+    w = synth.q_weight(g, 4, V, H)
+    x = synth.f16_normal(g, (d + 1, H))
+    dw = dict(qtype=4, N=V, K=H, qs=torch.from_numpy(w["qs"]).to(dev), qh=None,
+              scales=torch.from_numpy(w["scales"].view(np.int16)).to(dev))
+    m = sv.Model(dict(n_layers=0, hidden=H, vocab=V, max_nt=d + 1, max_seqs=1),
+                 dict(lm_head=dw, norm_w=torch.ones((1, H), dtype=torch.float32, device=dev)))
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    am = torch.empty(d + 1, dtype=torch.int32, device=dev)
+    sv.spec_lm_head(m, xd, d + 1, None, am)
+    dr_h = synth.greedy_drafts(g, am.cpu().numpy()[:d], V, wl["p_agree"])[None, :]
+    dr = torch.from_numpy(dr_h).to(dev)
+    n_acc = torch.empty(1, dtype=torch.int32, device=dev)
+    em = torch.empty((1, d + 1), dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+    st = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        sv.spec_lm_head(m, xd, d + 1, None, am)
+        sv.spec_accept_greedy(am.view(1, d + 1), dr, 1, d, n_acc, em)
+        e1.record(st)
+        e1.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    assert sv.spec_error_check(m) == 0
+    t = statistics.median(times)
+    nbytes = V * H * WEIGHT_BYTES[4] + (d + 1) * H * 2
+    m.close()
+    leg = {"us": round(t * 1e6, 2), "gbs": round(nbytes / t / 1e9, 1),
+           "frac_hbm": round(nbytes / t / 1e9 / hbm_peak, 3), "n_acc": int(n_acc.item()),
+           "l2": "flushed"}
+    return leg, dict(w=w, x=x, draft=dr_h)
+
+
+def accept_leg(sv, synth, dev, hbm_peak, reps=20):
+    """12 sequences, d 7, V 248320: the standalone strict rejection sampler
+    on p-logits N(0, 2) and draft logits p + N(0, 0.5), T 1, drafts sampled
+    from the draft logits; L2 flushed between calls."""
+    import torch
+    wl = synth.WL_ACCEPT_STOCH
+    n_seq, d, V, T = wl["n_seq"], wl["d"], wl["vocab"], wl["temperature"]
+    g = np.random.default_rng(wl["seed"])
+    p, q = synth.stochastic_logits(g, n_seq, d, V, wl["p_std"], wl["q_noise"])
+    pd, qd = torch.from_numpy(p).to(dev), torch.from_numpy(q).to(dev)
+    gen = synth.torch_gen(wl["seed"], dev)
+    u = torch.rand(qd.shape, generator=gen, device=dev)
+    dr = torch.argmax(qd / T - torch.log(-torch.log(u)), dim=2).to(torch.int32)
+    sid_h = (np.arange(n_seq) * 3 + 1).astype(np.int32)
+    sid = torch.from_numpy(sid_h).to(dev)
+    ei0 = torch.arange(n_seq, dtype=torch.int64, device=dev) * 1000
+    ei = ei0.clone()
+    n_acc = torch.empty(n_seq, dtype=torch.int32, device=dev)
+    em = torch.empty((n_seq, d + 1), dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+    st = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        flush()
+        ei.copy_(ei0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        sv.spec_accept_stochastic(pd, qd, dr, n_seq, d, V, T, 0x5EED, sid, ei, n_acc, em)
+        e1.record(st)
+        e1.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    assert sv.spec_error_check(None) == 0
+    t = statistics.median(times)
+    dense = 4.0 * V * n_seq * (2 * d + 1)
+    leg = {"us": round(t * 1e6, 2), "gbs_dense": round(dense / t / 1e9, 1),
+           "frac_hbm": round(dense / t / 1e9 / hbm_peak, 3),
+           "mean_accepted": round(float(n_acc.float().mean().item()), 3), "l2": "flushed"}
+    return leg, dict(p=p, q=q, draft=dr.cpu().numpy(), seq_ids=sid_h,
+                     emit_idx=(np.arange(n_seq) * 1000).astype(np.uint64), T=T)
+
+
+def decoder8_leg(sv, synth, dev, args, hbm_peak):
+    """The 8-layer H 4096 decoder, greedy, nt 8, 4096 cached positions, drafts
+    on the target's greedy chain w.p. 0.74: rounds graph-replayed and
+    raw-launched, and the round time at each nt."""
+    import torch
+    wl = dict(synth.WL_DECODER8)
+    d = wl["d"]
+    rounds = 20
+    max_ctx = wl["ctx"] + max(8 * (rounds + 4), sv.SPEC_MAX_NT * ROUND_SWEEP_GROUP,
+                              sv.SPEC_MAX_NT * (ADAPTIVE_ROUNDS + 2)) + 64
+    m = build_model(sv, synth, wl, dev, max_ctx)
+    fill_context(sv, synth, m, wl, dev, seed=1)
+    rng = np.random.default_rng(wl["seed"])
+    anchor = 1234
+    drafts = record_chain(sv, synth, m, wl, dev, rounds + 3, anchor, rng)
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    dr_dev = [torch.tensor([c], dtype=torch.int32, device=dev) for c in drafts]
+    n_acc = torch.zeros((rounds + 3, 1), dtype=torch.int32, device=dev)
+    em = torch.zeros((rounds + 3, 1, d + 1), dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+    leg = {}
+    for graphs in (True, False):
+        m.set_graphs(graphs)
+        sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
+        for j in range(3):
+            sv.spec_verify_round(m, 1, sid, dr_dev[j], d, n_acc=n_acc[j], emitted=em[j])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for j in range(3, rounds + 3):
             sv.spec_verify_round(m, 1, sid, dr_dev[j], d, n_acc=n_acc[j], emitted=em[j])
         e1.record(st)
         torch.cuda.synchronize()
-        torch.cuda.nvtx.range_pop()
-    barrier(dist)
-    torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / rounds
+        toks = int((n_acc[3:].cpu().numpy() + 1).sum())
+        key = "graph" if graphs else "raw"
+        leg[f"round_us_{key}"] = round(t * 1e6, 2)
+        leg[f"tok_s_{key}"] = round(toks / (t * rounds), 1)
+    m.set_graphs(True)
     assert sv.spec_error_check(m) == 0
-    elapsed = e0.elapsed_time(e1) * 1e-3
-    emitted_tokens = int((n_acc[args.warmup:].cpu().numpy() + 1).sum())
-    t_max = max_over_ranks(dist, elapsed, dev)
-    tokens_all = sum_over_ranks(dist, emitted_tokens, dev)
-    ms_per_step = t_max / args.steps * 1e3
-
-    # end to end through host buffers: spec_verify_round_host takes the
-    # drafts from host memory (copied into the model's mapped pinned staging,
-    # which the round's kernels read and write in place: one graph launch)
-    # and returns (n_acc, emitted) in host memory, every step
-    sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
-    h_drafts = [np.array([c], dtype=np.int32) for c in drafts]
-    h_sid = np.zeros(1, dtype=np.int32)
-    h_acc = np.empty(1, dtype=np.int32)
-    h_em = np.empty((1, d + 1), dtype=np.int32)
-    e2e_tok = 0
-    for j in range(args.warmup):
-        sv.spec_verify_round_host(m, 1, h_sid, h_drafts[j], d, n_acc=h_acc, emitted=h_em)
-    torch.cuda.synchronize()
-    barrier(dist)
-    t0 = time.perf_counter()
-    for j in range(args.warmup, n_rounds):
-        sv.spec_verify_round_host(m, 1, h_sid, h_drafts[j], d, n_acc=h_acc, emitted=h_em)
-        e2e_tok += int(h_acc[0]) + 1
-    t_e2e = max_over_ranks(dist, time.perf_counter() - t0, dev)
-    e2e_all = sum_over_ranks(dist, e2e_tok, dev)
-
-    line = None
-    if rank == 0:
-        gbs, per, bytes_per_launch, traffic = time_dominant_kernel(sv, synth, wl, dev, hbm_peak)
-        sweep = nt_sweep(sv, synth, dev) if not args.no_sweep else None
-        sweep_q8 = nt_sweep(sv, synth, dev, wl=synth.WL_LINEAR_SWEEP_Q8) if not args.no_sweep else None
-        rsweep = round_sweep(sv, m, wl, dev) if not args.no_sweep else None
-        adaptive = adaptive_depth_run(sv, m, wl, dev) if not args.no_sweep else None
-        full_round = full_round_run(sv, synth, m, wl, dev, max_ctx) if not args.no_sweep else None
-        n_layers = wl["n_layers"]
-        # embed (with the first norm), 8 per layer but the first layer's
-        # norm, final norm + LM head, fused accept + commit
-        launches_per_round = 1 + 8 * n_layers - 1 + 2 + 1
-        weight_bytes = sum(p["N"] * p["K"] * WEIGHT_BYTES[p["qtype"]] *
-                           (n_layers if p["qtype"] == 4 else 1) for p in per)
-        kv_bytes = n_layers * wl["n_kv_heads"] * (wl["ctx"] + d) * wl["head_dim"] * 2 * 2
-        round_s = ms_per_step * 1e-3
-        line = {
-            "metric": METRIC,
-            "value": round(tokens_all / t_max, 2),
-            "unit": "tok/s",
-            "n_gpus": ws,
-            "steps": args.steps,
-            "warmup": args.warmup,
-            "ms_per_step": round(ms_per_step, 4),
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "f16",
-            "precision": "Q4/Q6 block ints exact in f16, f16 activations, f32 accumulate",
-            "data": "synthetic (seeded N(0,1) activations and KV, uniform block ints, random-init weights)",
-            "config": {"workload": wl["name"], "n_layers": n_layers, "hidden": wl["hidden"],
-                       "heads": f"{wl['n_q_heads']}/{wl['n_kv_heads']}x{wl['head_dim']}",
-                       "ffn": wl["ffn"], "vocab": V, "context": wl["ctx"], "nt": d + 1,
-                       "n_seq": wl["n_seq"], "p_agree": wl["p_agree"], "graphs": True,
-                       "l2": "inputs larger than L2 (1.49 GB of weights per round)",
-                       "parallelism": f"replicas x{ws}"},
-            "verify_round_us": round(round_s * 1e6, 2),
-            "emitted_tokens_per_round": round(tokens_all / ws / args.steps, 3),
-            "round_bytes": {"weights": weight_bytes, "kv": kv_bytes,
-                            "gbs": round((weight_bytes + kv_bytes) / round_s / 1e9, 1),
-                            "frac_of_hbm": round((weight_bytes + kv_bytes) / round_s / 1e9 / hbm_peak, 4)},
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "traffic": None if traffic is None else round(traffic),
-                         "kernel": "linear_q_kernel (verify GEMM), nt=8, one round's launch mix",
-                         "algorithmic_bytes_per_launch": round(bytes_per_launch),
-                         "peak_kind": peak_kind, "per_shape": per},
-            "sweep": sweep,
-            "sweep_q8": sweep_q8,
-            "round_sweep": rsweep,
-            "adaptive_depth": adaptive,
-            "full_round": full_round,
-            "e2e": {"value": round(e2e_all / t_e2e, 2), "unit": "tok/s",
-                    "api": "spec_verify_round_host (host arrays, mapped pinned staging)",
-                    "h2d_bytes_per_step": 4 * (1 + d), "d2h_bytes_per_step": 4 * (2 + d)},
-            "gpu_launches": launches_per_round * args.steps,
-            "clocks": clk.summary(),
-        }
-        if ws == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(W=None, wl=wl, drafts=drafts[:1], anchor=anchor,
-                                                m=m, sv=sv, dev=dev)
+    wbytes = (wl["n_layers"] * ((wl["n_q_heads"] + 2 * wl["n_kv_heads"]) * wl["head_dim"] * wl["hidden"]
+                                + wl["hidden"] * wl["n_q_heads"] * wl["head_dim"]
+                                + 3 * wl["ffn"] * wl["hidden"]) * WEIGHT_BYTES[4]
+              + wl["vocab"] * wl["hidden"] * WEIGHT_BYTES[6])
+    kv = wl["n_layers"] * wl["n_kv_heads"] * (wl["ctx"] + d) * wl["head_dim"] * 4
+    leg["round_frac_hbm"] = round((wbytes + kv) / (leg["round_us_graph"] * 1e-6) / 1e9 / hbm_peak, 3)
+    if not args.no_legs:
+        rs = round_sweep(sv, m, wl, dev)
+        leg["round_sweep_us"] = rs["us"]
+        leg["nt9_16_over_nt1"] = rs["nt9_16_over_nt1"]
+    extras = {}
+    if args.extras:
+        extras["adaptive_depth"] = adaptive_depth_run(sv, m, wl, dev)
+        extras["full_round"] = full_round_run(sv, synth, m, wl, dev, max_ctx)
     m.close()
-    if line is not None:
-        print(json.dumps(line))
-    if dist is not None:
-        dist.destroy_process_group()
+    return leg, extras, drafts[3], anchor
+
+
+def compact_sweep(sw):
+    out = {}
+    for name, row in sw.items():
+        nts = sorted(row, key=int)
+        out[name] = {"us": {k: row[k]["us"] for k in nts}, "gbs_nt8": row.get("8", {}).get("gbs"),
+                     "nt16_over_nt1": round(row["16"]["us"] / row["1"]["us"], 3)}
+    return out
 
 
 # --------------------------------------------------------------------------
-# the CPU oracle on the same workload
+# the CPU oracle (cpu_baseline leg and the reference arm)
 # --------------------------------------------------------------------------
-def oracle_model_host(wl, dev_or_cpu="cpu"):
-    """The decoder's canonical weights on the host, generated by the same
-    seeded generator (on the GPU when there is one)."""
+def oracle_model_host(wl):
+    """The decoder's canonical weights on the host, from the same seeded
+    generator (run on the GPU when there is one)."""
     import torch
     import oracle
     from speculative_decoding_verification_round_gb300 import synth
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
     W = synth.decoder_weights_torch(wl, gen_dev)
+
     def hw(w):
         return oracle.QWeight(w["qtype"], w["qs"].cpu().numpy(),
                               None if w["qh"] is None else w["qh"].cpu().numpy(),
@@ -720,67 +883,286 @@ def oracle_context(wl, seed=1):
     return kc, vc
 
 
-def oracle_round(orc, om, kc, vc, wl, anchor, draft):
-    tokens = np.array([[anchor] + list(draft)], np.int32)
-    logits = om.forward(tokens, [wl["ctx"]], kc, vc)
-    am = np.array([[orc.argmax(r) for r in logits]], np.int32)
-    n_acc, em = orc.accept_greedy(am, np.array([draft], np.int32))
-    return int(n_acc[0]) + 1
+SLICE_LAYERS = 2
 
 
-def cpu_baseline(W, wl, drafts, anchor, m=None, sv=None, dev=None):
+class OracleSlice:
+    """The oracle on a bounded sample of the batched workload: ONE sequence
+    through a 2-layer slice of the 40 layers plus the LM head, nt 16, and the
+    stochastic accept; drafts from the noisy-target drafter (the oracle's own
+    nt = 1 passes + N(0, 0.5), sampled by the harness sampler), built once.
+    A full round is estimated as n_seq x (n_layers / 2 x t(2 layers) +
+    t(LM head) + t(accept))."""
+
+    def __init__(self, wl, seed=99):
+        import oracle
+        oracle.build()
+        self.o = oracle
+        self.wl = wl
+        sl = dict(wl, n_layers=SLICE_LAYERS)
+        self.om = oracle_model_host(sl)
+        self.kc, self.vc = oracle_context(sl, seed=2)
+        d, V, T, ctx = wl["d"], wl["vocab"], wl["temperature"], wl["ctx"]
+        g = np.random.default_rng(seed)
+        self.anchor = int(g.integers(0, V))
+        self.seed = seed
+        kco, vco = self.kc.copy(), self.vc.copy()
+        tok = self.anchor
+        self.q = np.zeros((1, d, V), np.float32)
+        self.draft = np.zeros((1, d), np.int32)
+        for i in range(d):
+            p_i = self.om.forward(np.array([[tok]], np.int32), [ctx + i], kco, vco)[0]
+            self.q[0, i] = p_i + (g.standard_normal(V) * wl["q_noise"]).astype(np.float32)
+            W, S = oracle.row_weights(self.q[0, i], T)
+            U = oracle.uniforms(seed, i, 0, 1)
+            tok = oracle.weight_pick(W, S, int(U[0]))
+            self.draft[0, i] = tok
+        # the LM head alone, to split the slice's time
+        x = np.zeros((d + 1, wl["hidden"]), np.uint16)
+        t0 = time.perf_counter()
+        oracle.linear(self.om.lm_head, x)
+        self.t_lm = time.perf_counter() - t0
+
+    def step(self):
+        """One sample: returns (emitted tokens of the sequence, seconds of the
+        sample, estimated seconds of a full round)."""
+        wl, o = self.wl, self.o
+        d, T = wl["d"], wl["temperature"]
+        tokens = np.concatenate([[[self.anchor]], self.draft], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        lg = self.om.forward(tokens, [wl["ctx"]], self.kc.copy(), self.vc.copy())
+        t1 = time.perf_counter()
+        n_acc, _, _ = o.accept_stochastic(lg.reshape(1, d + 1, -1), self.q, self.draft, T,
+                                          self.seed, [0], [0])
+        t2 = time.perf_counter()
+        t_layers = max(t1 - t0 - self.t_lm, 0.0)
+        full = wl["n_seq"] * (wl["n_layers"] / SLICE_LAYERS * t_layers + self.t_lm + (t2 - t1))
+        return int(n_acc[0]) + 1, t2 - t0, full
+
+
+def cores_used():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def cpu_baseline(wl5, tokens_per_round, legs_in):
+    """The oracle as it stands, timed on the host cores: the headline as a
+    scaled 2-layer slice, and each leg's own workload."""
     import oracle
-    oracle.build()
-    om = oracle_model_host(wl)
-    kc, vc = oracle_context(wl)
-    t0 = time.perf_counter()
-    toks = oracle_round(oracle, om, kc, vc, wl, anchor, drafts[0])
-    t = time.perf_counter() - t0
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": round(toks / t, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"one full verify round of {wl['name']} (nt={wl['d'] + 1}, all "
-                      f"{wl['n_layers']} layers + LM head, fp64), {t:.1f} s"}
+    sl = OracleSlice(wl5)
+    _, t_sample, t_round = sl.step()
+    out = {"value": round(tokens_per_round / t_round, 4), "unit": "tok/s", "cores": cores_used(),
+           "kind": "oracle",
+           "sample": (f"one sequence of {wl5['name']}: a {SLICE_LAYERS}-layer slice + LM head, "
+                      f"nt {wl5['d'] + 1}, fp64, + the stochastic accept ({t_sample:.1f} s); "
+                      f"scaled to the full round ({wl5['n_seq']} sequences x "
+                      f"{wl5['n_layers']} layers: {t_round:.1f} s); tokens per round "
+                      f"{tokens_per_round:.2f} from the GPU rounds of the same workload")}
+    per = {}
+    if "lmhead" in legs_in:
+        a = legs_in["lmhead"]
+        qw = oracle.QWeight(4, a["w"]["qs"], None, a["w"]["scales"], a["w"]["N"], a["w"]["K"])
+        t0 = time.perf_counter()
+        lg = oracle.linear(qw, a["x"])
+        am = np.array([[oracle.argmax(r) for r in lg]], np.int32)
+        oracle.accept_greedy(am, a["draft"])
+        per["lmhead_greedy_us"] = round((time.perf_counter() - t0) * 1e6, 1)
+    if "accept" in legs_in:
+        a = legs_in["accept"]
+        t0 = time.perf_counter()
+        oracle.accept_stochastic(a["p"], a["q"], a["draft"], a["T"], 0x5EED, a["seq_ids"],
+                                 a["emit_idx"])
+        per["accept_stochastic_us"] = round((time.perf_counter() - t0) * 1e6, 1)
+    if "decoder8" in legs_in:
+        a = legs_in["decoder8"]
+        wl = a["wl"]
+        om = oracle_model_host(wl)
+        kc, vc = oracle_context(wl)
+        tokens = np.array([[a["anchor"]] + list(a["draft"])], np.int32)
+        t0 = time.perf_counter()
+        lg = om.forward(tokens, [wl["ctx"]], kc, vc)
+        am = np.array([[oracle.argmax(r) for r in lg]], np.int32)
+        n_acc, _ = oracle.accept_greedy(am, np.array([a["draft"]], np.int32))
+        per["decoder8_round_us"] = round((time.perf_counter() - t0) * 1e6, 1)
+    out["per_workload"] = per
+    return out
 
 
 def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
         return
-    import oracle
     from speculative_decoding_verification_round_gb300 import synth
-    oracle.build()
-    wl = dict(synth.WL_DECODER8)
-    om = oracle_model_host(wl)
-    kc0, vc0 = oracle_context(wl)
-    rng = np.random.default_rng(wl["seed"])
-    anchor = 1234
-    draft = [int(x) for x in rng.integers(0, wl["vocab"], wl["d"])]
+    wl = dict(synth.WL_DECODER14B)
+    sl = OracleSlice(wl)
     for _ in range(args.warmup):
-        oracle_round(oracle, om, kc0.copy(), vc0.copy(), wl, anchor, draft)
-    t0 = time.perf_counter()
-    toks = 0
+        sl.step()
+    toks, t_samples, t_full = 0, 0.0, 0.0
     for _ in range(args.steps):
-        toks += oracle_round(oracle, om, kc0.copy(), vc0.copy(), wl, anchor, draft)
-    t = time.perf_counter() - t0
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    val = toks / t
-    sample = (f"{args.steps} full verify rounds of {wl['name']} on the CPU oracle "
-              f"(fp64, all layers + LM head)")
+        tk, ts, tf = sl.step()
+        toks += tk * wl["n_seq"]
+        t_samples += ts
+        t_full += tf
+    val = toks / t_full
+    sample = (f"{args.steps} samples, each one sequence through a {SLICE_LAYERS}-layer slice "
+              f"of {wl['name']} + LM head + the stochastic accept on the CPU oracle (fp64); "
+              f"{t_samples:.1f} s in all, scaled to full rounds of {wl['n_seq']} sequences x "
+              f"{wl['n_layers']} layers; tokens per round = {wl['n_seq']} x the sample's "
+              f"emitted count")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "tok/s",
+        "impl": "reference", "metric": METRIC, "value": round(val, 5), "unit": "tok/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t / args.steps * 1e3, 2), "higher_is_better": True,
+        "ms_per_step": round(t_full / args.steps * 1e3, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl["name"], "nt": wl["d"] + 1},
-        "cpu_baseline": {"value": round(val, 4), "unit": "tok/s", "cores": cores,
+        "config": {"workload": wl["name"], "n_seq": wl["n_seq"], "nt": wl["d"] + 1,
+                   "temperature": wl["temperature"]},
+        "cpu_baseline": {"value": round(val, 5), "unit": "tok/s", "cores": cores_used(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(val, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": round(val, 5), "unit": "tok/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
 
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from speculative_decoding_verification_round_gb300 import synth
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    hbm_peak, tc_sustained, tc_burst, peak_kind = peaks()
+    wl = dict(synth.WL_DECODER14B)
+    n_seq, d, V, T = wl["n_seq"], wl["d"], wl["vocab"], wl["temperature"]
+    seed = 0x5EED + rank
+    n_rounds = args.warmup + args.steps
+    max_ctx = wl["ctx"] + (d + 1) * (n_rounds + 2) + 64
+    m = build_model(sv, synth, wl, dev, max_ctx)
+    fill_context(sv, synth, m, wl, dev, seed=2 + rank)
+    st0 = state0_of(wl)
+    set_state(sv, m, st0)
+    rounds = record_stochastic(sv, synth, m, wl, dev, n_rounds, seed)
+
+    # the timed steps: graph-replayed rounds
+    barrier(dist)
+    torch.cuda.synchronize()
+    clk = ClockSampler(smi_id(local), args.clocks_csv)
+    elapsed, n_acc = replay(sv, m, wl, dev, rounds, st0, args.warmup, args.steps, seed, clk)
+    barrier(dist)
+    torch.cuda.synchronize()
+    emitted = int((n_acc + 1).sum())
+    t_max = max_over_ranks(dist, elapsed, dev)
+    tokens_all = sum_over_ranks(dist, emitted, dev)
+    ms_per_step = t_max / args.steps * 1e3
+
+    # end to end through host buffers (every rank: same work, max time)
+    e2e_tok, t_e2e, h2d, d2h = e2e_host(sv, m, wl, dev, rounds, st0, args.warmup, args.steps, seed)
+    t_e2e = max_over_ranks(dist, t_e2e, dev)
+    e2e_all = sum_over_ranks(dist, e2e_tok, dev)
+
+    line = None
+    if rank == 0:
+        # the same rounds launched kernel by kernel, then timed per kernel class
+        m.set_graphs(False)
+        t_raw, _ = replay(sv, m, wl, dev, rounds, st0, args.warmup, args.steps, seed)
+        m.set_graphs(True)
+        kern = in_round_kernels(sv, m, wl, dev, rounds, st0, min(args.warmup, 3),
+                                min(args.steps, 5), seed)
+        R = n_seq * (d + 1)
+        gem = kern["all_gemms"]
+        tflops = gem["tflops"]
+        n_layers = wl["n_layers"]
+        shapes = [(4, (wl["n_q_heads"] + 2 * wl["n_kv_heads"]) * wl["head_dim"], wl["hidden"], n_layers, R),
+                  (4, wl["hidden"], wl["n_q_heads"] * wl["head_dim"], n_layers, R),
+                  (4, 2 * wl["ffn"], wl["hidden"], n_layers, R),
+                  (4, wl["hidden"], wl["ffn"], n_layers, R), (6, V, wl["hidden"], 1, R)]
+        traffic = measured_traffic(shapes)
+        weight_bytes = sum(N * K * WEIGHT_BYTES[qt] * c for qt, N, K, c, _ in shapes)
+        kv_bytes = n_layers * n_seq * wl["n_kv_heads"] * (wl["ctx"] + d + 1) * wl["head_dim"] * 4
+        round_s = ms_per_step * 1e-3
+        gemm_us_step = gem["seconds"] / max(min(args.steps, 5), 1) * 1e6
+        del rounds
+        torch.cuda.empty_cache()
+        m.close()
+        torch.cuda.empty_cache()
+        legs, legs_in, extras = {}, {}, {}
+        if not args.no_legs:
+            legs["lmhead_greedy_H1024_V32000_nt3"], legs_in["lmhead"] = lmhead_leg(sv, synth, dev, hbm_peak)
+            legs["accept_stochastic_12seq_d7_V248320"], legs_in["accept"] = accept_leg(sv, synth, dev, hbm_peak)
+            legs["linear_sweep"] = compact_sweep(nt_sweep(sv, synth, dev))
+            dec8, extras, dr8, anc8 = decoder8_leg(sv, synth, dev, args, hbm_peak)
+            legs["decoder8_H4096_V151936_ctx4096_nt8"] = dec8
+            legs_in["decoder8"] = dict(wl=dict(synth.WL_DECODER8), draft=dr8, anchor=anc8)
+        line = {
+            "metric": METRIC,
+            "value": round(tokens_all / t_max, 2),
+            "unit": "tok/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16",
+            "precision": "Q4/Q6 block ints, f16 activations, f32 accumulate; integer-weight sampler",
+            "data": "synthetic (seeded N(0,1) activations and KV, uniform block ints, random-init "
+                    "weights; draft logits = target nt=1 logits + N(0,0.5))",
+            "config": {"workload": wl["name"], "n_layers": n_layers, "hidden": wl["hidden"],
+                       "heads": f"{wl['n_q_heads']}/{wl['n_kv_heads']}x{wl['head_dim']}",
+                       "ffn": wl["ffn"], "vocab": V, "context": wl["ctx"], "n_seq": n_seq,
+                       "nt": d + 1, "rows": R, "temperature": T, "mode": "stochastic",
+                       "drafter": "noisy target (target nt=1 logits + N(0,0.5)), untimed",
+                       "graphs": True,
+                       "l2": "inputs larger than L2 (7.2 GB of weights per round)",
+                       "parallelism": f"replicas x{ws}"},
+            "verify_round_us": round(round_s * 1e6, 1),
+            "verify_round_us_raw_launch": round(t_raw / args.steps * 1e6, 1),
+            "emitted_tokens_per_round": round(tokens_all / ws / args.steps, 3),
+            "round_bytes": {"weights": weight_bytes, "kv": kv_bytes,
+                            "gbs": round((weight_bytes + kv_bytes) / round_s / 1e9, 1),
+                            "frac_of_hbm": round((weight_bytes + kv_bytes) / round_s / 1e9 / hbm_peak, 4)},
+            "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": tc_sustained,
+                         "unit": "TFLOP/s", "frac": round(tflops / tc_sustained, 4),
+                         "traffic": None if traffic is None else round(traffic),
+                         "kernel": f"verify GEMM (all {4 * n_layers + 1} launches of a round, "
+                                   f"{R} rows), timed inside raw-launched rounds",
+                         "algorithmic_flops_per_launch": round(gem["flops_per_launch"]),
+                         "algorithmic_bytes_per_launch": round(gem["bytes_per_launch"]),
+                         "hbm_gbs": round(gem["gbs"], 1), "hbm_peak": hbm_peak,
+                         "hbm_frac": round(gem["gbs"] / hbm_peak, 4),
+                         "gemm_us_per_step": round(gemm_us_step, 1),
+                         "peak_kind": f"{peak_kind} bf16 sustained (fp16 = bf16 rate)"},
+            "kernels_in_round": {k: {"us_per_launch": round(v["us_per_launch"], 2),
+                                     "tflops": round(v["tflops"], 1), "gbs": round(v["gbs"], 1)}
+                                 for k, v in kern.items()},
+            "e2e": {"value": round(e2e_all / t_e2e, 2), "unit": "tok/s",
+                    "api": "spec_verify_round_host (ids and drafts from host arrays, draft "
+                           "logits from pinned host memory, outputs to host arrays)",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": (1 + 8 * n_layers - 1 + 2 + 4) * args.steps,
+            "clocks": clk.summary(),
+        }
+        if extras:
+            line.update(extras)
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, tokens_all / args.steps, legs_in)
+        line["workloads"] = legs  # last: the compact legs end the line
+    else:
+        m.close()
+    if line is not None:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# profiling drivers (no JSON line)
+# --------------------------------------------------------------------------
 def linear_only(spec: str, nt: int = 8, reps: int = 3):
-    """Profiling driver: spec_linear_q at nt on packed synthetic matrices,
-    `spec` = 'QT:N:K,QT:N:K,...', each launched `reps` times."""
+    """spec_linear_q at nt on packed synthetic matrices, `spec` =
+    'QT:N:K,QT:N:K,...', each launched `reps` times."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
     from speculative_decoding_verification_round_gb300 import synth
@@ -789,7 +1171,7 @@ def linear_only(spec: str, nt: int = 8, reps: int = 3):
     for item in spec.split(","):
         qt, N, K = (int(v) for v in item.split(":"))
         w = synth.q_weight_torch(gen, qt, N, K, dev)
-        qm = sv.QMat(w, max_rows=16)
+        qm = sv.QMat(w, max_rows=max(nt, 16))
         x = synth.f16_normal_torch(gen, (nt, K), dev).view(torch.int16)
         y = torch.empty((nt, N), dtype=torch.float32, device=dev)
         for _ in range(reps):
@@ -800,17 +1182,48 @@ def linear_only(spec: str, nt: int = 8, reps: int = 3):
     print("linear-only ok")
 
 
+def round_only(n_layers: int, warm: int = 2, reps: int = 2):
+    """Stochastic rounds of the batched workload at `n_layers` layers (the
+    last `reps` inside the NVTX range "rounds"), for launch lists."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from speculative_decoding_verification_round_gb300 import synth
+    dev = torch.device("cuda:0")
+    wl = dict(synth.WL_DECODER14B, n_layers=n_layers)
+    n = warm + reps
+    m = build_model(sv, synth, wl, dev, wl["ctx"] + (wl["d"] + 1) * (n + 2) + 64)
+    fill_context(sv, synth, m, wl, dev, seed=2)
+    st0 = state0_of(wl)
+    set_state(sv, m, st0)
+    rounds = record_stochastic(sv, synth, m, wl, dev, n, 0x5EED)
+    set_state(sv, m, st0)
+    sid = torch.arange(wl["n_seq"], dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(wl["n_seq"], dtype=torch.int32, device=dev)
+    em = torch.zeros((wl["n_seq"], wl["d"] + 1), dtype=torch.int32, device=dev)
+    for j in range(n):
+        if j == warm:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("rounds")
+        dr, qs = rounds[j]
+        sv.spec_verify_round(m, wl["n_seq"], sid, dr, wl["d"], qs, False, wl["temperature"],
+                             0x5EED, n_acc, em)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    assert sv.spec_error_check(m) == 0
+    m.close()
+    print("round-only ok")
+
+
 def draft_only(n_layers: int, warm: int = 3, reps: int = 3):
-    """Profiling driver: nt = 1 forwards (graph-replayed d = 0 rounds) of the
-    0.5B-class draft at `n_layers` layers and a 4096-position context; the
-    last `reps` run inside the NVTX range "draft"."""
+    """nt = 1 forwards (graph-replayed d = 0 rounds) of the 0.5B-class draft
+    at `n_layers` layers and a 4096-position context; the last `reps` run
+    inside the NVTX range "draft"."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
     from speculative_decoding_verification_round_gb300 import synth
     dev = torch.device("cuda:0")
     wl = dict(synth.WL_DRAFT05B, n_layers=n_layers)
-    dm, W = build_model(sv, synth, wl, dev, wl["ctx"] + 64)
-    del W
+    dm = build_model(sv, synth, wl, dev, wl["ctx"] + 64)
     fill_context(sv, synth, dm, wl, dev, seed=7)
     sid = torch.zeros(1, dtype=torch.int32, device=dev)
     n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -831,21 +1244,30 @@ def draft_only(n_layers: int, warm: int = 3, reps: int = 3):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--linear-only", default=None,
-                    help="profiling driver: QT:N:K[,QT:N:K...] verify-GEMM launches only")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="only the headline workload (no LM-head, accept, sweep, decoder-8 legs)")
+    ap.add_argument("--extras", action="store_true",
+                    help="also the adaptive-depth and full-round (with draft) legs on decoder-8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-csv", default=None,
                     help="keep the raw nvidia-smi clock samples in this file")
+    ap.add_argument("--linear-only", default=None,
+                    help="profiling driver: QT:N:K[,QT:N:K...] verify-GEMM launches only")
+    ap.add_argument("--linear-rows", type=int, default=8, help="rows of --linear-only")
+    ap.add_argument("--round-only", type=int, default=None, metavar="LAYERS",
+                    help="profiling driver: stochastic rounds of the batched workload")
     ap.add_argument("--draft-only", type=int, default=None, metavar="LAYERS",
                     help="profiling driver: nt = 1 forwards of the 0.5B-class draft")
     args = ap.parse_args()
     if args.linear_only:
-        linear_only(args.linear_only)
+        linear_only(args.linear_only, nt=args.linear_rows)
+        return
+    if args.round_only:
+        round_only(args.round_only)
         return
     if args.draft_only:
         draft_only(args.draft_only)
@@ -853,10 +1275,6 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        # each oracle step is a full fp64 round (seconds of CPU work): bound
-        # the run to a few minutes
-        args.steps = min(args.steps, 5)
-        args.warmup = min(args.warmup, 3)
         run_reference(args)
     else:
         run_ours(args)

@@ -40,6 +40,18 @@
  *  - The library allocates device memory only in *_create, and, for the
  *    standalone entry points that need scratch, on first use per device
  *    (a cached, growing workspace).
+ *  - Two environment variables, read once (at matrix / model creation for
+ *    the first, at the first launch for the second), change how kernels are
+ *    launched but never what they compute beyond the summation order of
+ *    one GEMM's K split:
+ *      SPEC_VERIFY_LINEAR_SPLIT  "KW:S" (every matrix) or "N:K:KW:S" entries,
+ *        comma-separated: the K split of the verify GEMM (KW warps of a CTA
+ *        and S CTAs share a tile's K range) instead of the library's choice.
+ *        The split is fixed per matrix, so rows stay bitwise equal across nt
+ *        under any setting; results under two settings may differ in the
+ *        last bits.  Meant for tests and tuning.
+ *      SPEC_VERIFY_PDL=0  launch every kernel as a plain stream-ordered
+ *        launch (no programmatic dependent launch).  Results are unchanged.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -199,6 +211,44 @@ int spec_error_check(spec_model* m, void* stream, uint32_t* bits);
  * kernels one by one. */
 int spec_model_set_graphs(spec_model* m, int enable);
 
+/* In-round kernel timing.  enable = 1: the model's later rounds launch their
+ * kernels one by one (no graph), with a CUDA event recorded before and after
+ * each verify-GEMM launch and each attention launch (chunk + merge kernels);
+ * the events see each kernel inside a real round (its inputs written by the
+ * kernel before it, the caches as the round leaves them), at the price of
+ * the serialisation an event imposes between neighbouring kernels.  Calling
+ * it (enable 0 or 1) synchronises the device and clears the totals. */
+int spec_model_profile(spec_model* m, int enable);
+
+/* Kernel classes of spec_model_profile_read. */
+#define SPEC_PROF_QKV 0       /* QKV GEMM + RoPE + KV write */
+#define SPEC_PROF_O 1         /* O GEMM + residual */
+#define SPEC_PROF_GATE_UP 2   /* gate/up GEMM + SwiGLU */
+#define SPEC_PROF_DOWN 3      /* down GEMM + residual */
+#define SPEC_PROF_LM_HEAD 4   /* LM head (+ logits) + argmax */
+#define SPEC_PROF_ALL_GEMMS 5 /* classes 0-4 together */
+#define SPEC_PROF_ATTN 6      /* verify attention (chunk + merge kernels) */
+
+/* Totals since the last spec_model_profile call for one kernel class (HOST
+ * outputs, each may be NULL): summed event-to-event seconds, launches, and
+ * the algorithmic bytes (packed weights once, activations in, outputs out;
+ * 0 for attention, whose bytes depend on positions held on the device) and
+ * flops (2 * rows * N * K) of those launches.  Synchronises the device. */
+int spec_model_profile_read(spec_model* m, int kind, double* seconds, int64_t* launches,
+                            double* bytes, double* flops);
+
+/* Test hook for the fail-closed path of the verify GEMM's bounded waits.
+ * Every wait of a GEMM CTA on its copies (weights and activations, TMA bulk
+ * copies completing on an mbarrier) gives up after about a second (131072
+ * suspended tries of about 10 us), sets ERR_TIMEOUT (0x10) in the model's
+ * error word, waits with the full budget for the copies it issued and
+ * finishes without using them, so the round commits nothing and writes -1
+ * outputs.  This call sets the try budget of the FIRST wait of each GEMM CTA
+ * (on its activation slice) for the model's later rounds; 0 makes that wait
+ * give up at once.  Drains always keep the full budget.
+ * 0 <= tries <= 131072; synchronises the device and drops captured graphs. */
+int spec_model_set_wait_budget(spec_model* m, int tries);
+
 /* Causal GQA attention of nt query rows per sequence over the KV cache of
  * `layer`, bitwise position-invariant: row i of sequence s (absolute
  * position n_past[s] + i) is computed exactly as it would be at nt = 1
@@ -254,11 +304,11 @@ int spec_accept_stochastic(const float* p_logits, const float* q_logits,
 
 /* Same computation, arguments and results as spec_accept_stochastic, but
  * this entry point allocates no memory at all.  It is for callers that cannot
- * call cudaMalloc: code running while a stream is being captured into a CUDA
- * graph, code whose device memory is owned by a custom allocator that forbids
- * cudaMalloc, and latency-critical loops that must not risk the implicit
- * device synchronisation an allocation can cause.  (The pages have no
- * counterpart for this entry point; it is an addition of this library.)
+ * call cudaMalloc: code whose device memory is owned by a custom allocator
+ * or a fixed arena that forbids outside allocations, and latency-critical
+ * loops that must not risk the implicit device synchronisation an
+ * allocation can cause.  (The pages have no counterpart for this entry
+ * point; it is an addition of this library.)
  *  - Scratch is one fixed array in the library's device globals (about 64 KB
  *    per GPU that loads the library, held until the process exits), so the
  *    batch is limited: n_seq <= 1024 and n_seq * (2d + 1) <= 4096; larger
@@ -291,7 +341,9 @@ typedef struct {
  * and the LM head), then the accept step, then the commit:
  *   n_past += n_acc + 1, emit_idx += n_acc + 1, anchor = last emitted token.
  * The new KV rows are written in place; rejected rows are overwritten later.
- *   seq_ids int32 [n_seq] (distinct slots < max_seqs); draft int32 [n_seq][d];
+ *   seq_ids int32 [n_seq] (distinct slots < max_seqs: a slot named twice, or
+ *   out of range, sets the device error word and the round commits nothing);
+ *   draft int32 [n_seq][d];
  *   q_logits fp32 [n_seq][d][vocab] (draft distributions; NULL iff greedy);
  *   sampling: HOST pointer;  n_acc int32 [n_seq]; emitted int32 [n_seq][d+1];
  *   logits_out fp32 [n_seq*(d+1)][vocab] or NULL.
@@ -304,10 +356,12 @@ int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_ids,
                       int32_t* emitted, float* logits_out, void* stream);
 
 /* The same verify round with seq_ids, draft, n_acc and emitted in HOST
- * memory (any host memory; shapes as for spec_verify_round; q_logits, when
- * given, stays a device array).  The inputs are copied into the model's
- * mapped pinned staging, which the kernels read and write in place (no
- * copy engine steps; a greedy round with graphs on is one graph launch); the
+ * memory (any host memory; shapes as for spec_verify_round).  q_logits may
+ * be device memory or host memory; host q_logits (pinned for full copy
+ * bandwidth) are first copied into a buffer the model allocated at creation.
+ * The small inputs are copied into the model's mapped pinned staging, which
+ * the kernels read and write in place (no copy engine steps; a greedy round
+ * with graphs on is one graph launch); the
  * call synchronises `stream` before it copies the outputs out, so they are
  * valid on return.  Calls on one model must not overlap (the staging is the
  * model's).  Errors: as spec_verify_round, plus SPEC_E_CUDA from the
@@ -319,10 +373,11 @@ int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* seq_ids,
 
 /* ---------------------------------------------------------------------------
  * Adaptive draft depth: a host controller that picks the depth d of the next
- * verify round ("Speculative Decoding (D5-R) -- Plan", status notes: per-round
- * d from beta-smoothed per-depth acceptance, min-of-4 round-cost windows, a
- * 10% switch hysteresis, optimism for depths not yet seen, capped at d = 7
- * by the identity boundary).  Host only: no GPU work, no stream, no model.
+ * verify round ("Speculative Decoding (D5-R) -- Plan", status notes, which
+ * list the ingredients: smoothed acceptance estimates, a window of measured
+ * round costs, hysteresis, trying unmeasured depths first, a cap on d; the
+ * rules below are this library's reading).  Host only: no GPU work, no
+ * stream, no model.
  *  - Position i = 1..d_max keeps decayed Beta counts (a_i, b_i).  A round at
  *    depth d in which a sequence accepted n drafts adds 1 to a_i for
  *    i <= min(n, d) and, if n < d, 1 to b_{n+1}; a negative n (a failed

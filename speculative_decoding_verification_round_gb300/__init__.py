@@ -27,11 +27,14 @@ SPEC_E_UNSUPPORTED = -5
 SPEC_E_TIMEOUT = -6
 SPEC_Q4, SPEC_Q6, SPEC_Q8 = 4, 6, 8
 SPEC_MAX_NT = 16
+SPEC_PROF_QKV, SPEC_PROF_O, SPEC_PROF_GATE_UP, SPEC_PROF_DOWN = 0, 1, 2, 3
+SPEC_PROF_LM_HEAD, SPEC_PROF_ALL_GEMMS, SPEC_PROF_ATTN = 4, 5, 6
 
 EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_linear_q",
             "spec_model_create", "spec_model_destroy", "spec_model_kv_cache", "spec_kv_fill",
             "spec_kv_read", "spec_model_debug_read",
             "spec_state_set", "spec_state_get", "spec_error_check", "spec_model_set_graphs",
+            "spec_model_set_wait_budget", "spec_model_profile", "spec_model_profile_read",
             "spec_verify_attn", "spec_lm_head", "spec_accept_greedy",
             "spec_accept_stochastic", "spec_accept_stochastic_noalloc", "spec_verify_round",
             "spec_verify_round_host", "spec_depth_params_default", "spec_depth_ctl_create",
@@ -106,6 +109,12 @@ def lib():
                 "spec_state_get": (I32, [P, I32, P, P, P, P]),
                 "spec_error_check": (I32, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
                 "spec_model_set_graphs": (I32, [P, I32]),
+                "spec_model_set_wait_budget": (I32, [P, I32]),
+                "spec_model_profile": (I32, [P, I32]),
+                "spec_model_profile_read": (I32, [P, I32, ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_int64),
+                                                  ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_double)]),
                 "spec_verify_attn": (I32, [P, I32, I32, P, I32, P, P, P, P, P]),
                 "spec_lm_head": (I32, [P, P, I32, P, P, P]),
                 "spec_accept_greedy": (I32, [P, P, I32, I32, P, P, P]),
@@ -247,6 +256,23 @@ class Model:
     def set_graphs(self, enable: bool):
         _check(lib().spec_model_set_graphs(self.handle, int(bool(enable))))
 
+    def profile(self, enable: bool):
+        """In-round kernel timing on (raw launches, events around each GEMM and
+        attention launch) or off; clears the totals."""
+        _check(lib().spec_model_profile(self.handle, int(bool(enable))))
+
+    def profile_read(self, kind: int) -> dict:
+        """Totals of one kernel class since the last profile() call."""
+        t, b, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+        n = ctypes.c_int64()
+        _check(lib().spec_model_profile_read(self.handle, int(kind), ctypes.byref(t),
+                                             ctypes.byref(n), ctypes.byref(b), ctypes.byref(f)))
+        return dict(seconds=t.value, launches=n.value, bytes=b.value, flops=f.value)
+
+    def set_wait_budget(self, tries: int):
+        """Test hook: try budget of each GEMM CTA's first copy wait (see the header)."""
+        _check(lib().spec_model_set_wait_budget(self.handle, int(tries)))
+
 
 def spec_kv_fill(m: Model, layer: int, seq: int, pos0: int, n_pos: int, k, v, stream=None):
     """k, v: fp16 tensors [n_kv_heads][n_pos][head_dim] (device or pinned host)."""
@@ -358,7 +384,8 @@ def _host_i32(a, n, name):
 def spec_verify_round_host(m: Model, n_seq: int, seq_ids, draft, d: int, q_logits=None,
                            greedy: bool = True, temperature: float = 1.0, seed: int = 0,
                            n_acc=None, emitted=None, stream=None):
-    """spec_verify_round with host (numpy int32) seq_ids, draft, n_acc and emitted.
+    """spec_verify_round with host (numpy int32) seq_ids, draft, n_acc and emitted;
+    q_logits a device tensor, a (pinned) host tensor or a float32 numpy array.
     Returns (n_acc, emitted); they are valid on return (the call synchronises).
     n_acc / emitted, when given, must be C-contiguous int32 arrays (written in
     place)."""
@@ -374,9 +401,15 @@ def spec_verify_round_host(m: Model, n_seq: int, seq_ids, draft, d: int, q_logit
                 and a.size >= n):
             raise ValueError(f"{name}: a C-contiguous int32 numpy array of {n} values is required")
     sp = spec_sampling(int(bool(greedy)), float(temperature), int(seed))
+    if type(q_logits) is np.ndarray:  # host q_logits: copied by the library
+        if not (q_logits.dtype == np.float32 and q_logits.flags.c_contiguous):
+            raise ValueError("q_logits: a C-contiguous float32 array is required")
+        qp = ctypes.c_void_p(q_logits.ctypes.data)
+    else:
+        qp = _ptr(q_logits)
     _check(lib().spec_verify_round_host(m.handle, int(n_seq), sid.ctypes.data,
                                         None if dr is None else dr.ctypes.data, int(d),
-                                        _ptr(q_logits), ctypes.byref(sp), n_acc.ctypes.data,
+                                        qp, ctypes.byref(sp), n_acc.ctypes.data,
                                         emitted.ctypes.data, _stream(stream)))
     return n_acc, emitted
 

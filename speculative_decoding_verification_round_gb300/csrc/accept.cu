@@ -442,7 +442,7 @@ __global__ void accept_commit_greedy_kernel(const GreedyRoundArgs a) {
 
 }  // namespace
 
-size_t stoch_rows_needed(int n_seq, int d) { return (size_t)n_seq * (2 * d + 1); }
+size_t stoch_rows_needed(int n_seq, int d) { return (size_t)n_seq * (2 * (size_t)d + 1); }
 
 void launch_accept_greedy(const int32_t* argmax, const int32_t* draft, int n_seq, int d,
                           int32_t* n_acc, int32_t* emitted, cudaStream_t st) {
@@ -456,6 +456,8 @@ int launch_accept_stochastic(const float* p, const float* q, const int32_t* draf
                              int32_t* emitted, const StochScratch& scr, uint32_t* err,
                              cudaStream_t st) {
   const size_t nrows = stoch_rows_needed(n_seq, d);
+  if (nrows * ST_CLUSTER > (size_t)INT32_MAX)
+    return fail(SPEC_E_SHAPE, "stochastic accept: n_seq * (2d + 1) too large");
   if (nrows > scr.rows_cap || (size_t)n_seq > scr.seq_cap)
     return fail(SPEC_E_SHAPE, "stochastic accept: scratch too small");
   const int slice = (V + ST_CLUSTER - 1) / ST_CLUSTER;
@@ -593,7 +595,7 @@ extern "C" int spec_accept_stochastic_noalloc(const float* p_logits, const float
   if (n_seq < 1 || d < 0 || V < 1) return fail(SPEC_E_SHAPE, "n_seq >= 1, d >= 0, V >= 1 required");
   if (!(temperature > 0.0f) || !isfinite(temperature))
     return fail(SPEC_E_INVALID, "temperature must be finite and > 0");
-  if (n_seq > NOALLOC_MAX_SEQS || (long long)n_seq * (2 * d + 1) > NOALLOC_MAX_ROWS)
+  if (n_seq > NOALLOC_MAX_SEQS || (long long)n_seq * (2LL * d + 1) > NOALLOC_MAX_ROWS)
     return fail(SPEC_E_SHAPE,
                 "spec_accept_stochastic_noalloc: n_seq * (2d + 1) must be <= 4096 and n_seq <= "
                 "1024 (fixed scratch); use spec_accept_stochastic for larger batches");

@@ -278,10 +278,21 @@ struct spec_model {
   int32_t* io_dev_in = nullptr;
   int32_t* io_dev_out = nullptr;
   float* attn_part = nullptr;
+  float* qhost_buf = nullptr;  // [max_seqs][max_nt - 1][vocab]: host q_logits of the host entry
   LinScratch lscr;
   StochScratch sscr;
   std::vector<void*> allocs;
   bool use_graphs = true;
+  // in-round kernel timing (spec_model_profile): events around each GEMM and
+  // attention launch of raw-launched rounds
+  struct ProfRec {
+    cudaEvent_t a, b;
+    int kind;
+    double bytes, flops;
+  };
+  bool prof = false;
+  std::vector<ProfRec> prof_recs;
+  std::vector<cudaEvent_t> prof_pool;
   cudaStream_t cap_stream = nullptr;
   std::map<long long, RoundGraph> graphs;
   size_t weight_bytes = 0;
@@ -303,6 +314,11 @@ static int dalloc_t(spec_model* m, T** p, size_t count) {
 
 static void model_free(spec_model* m) {
   cudaDeviceSynchronize();
+  for (auto& r : m->prof_recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (cudaEvent_t e : m->prof_pool) cudaEventDestroy(e);
   for (auto& kv : m->graphs) round_graph_free(&kv.second);
   m->graphs.clear();
   for (auto* v : {&m->wqkv, &m->wo, &m->wgu, &m->wd})
@@ -423,6 +439,8 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
   TRY(dalloc_t(m, &m->h, (size_t)R * H));
   TRY(dalloc_t(m, &m->xa, (size_t)R * H));
   TRY(dalloc_t(m, &m->logits, (size_t)R * V));
+  if (D.max_nt > 1 && L > 0)
+    TRY(dalloc_t(m, &m->qhost_buf, (size_t)D.max_seqs * (D.max_nt - 1) * V));
   TRY(dalloc_t(m, &m->argmax, R));
   TRY(dalloc_t(m, &m->rows, R));
   TRY(dalloc_t(m, &m->tokens, R));
@@ -550,6 +568,54 @@ extern "C" int spec_model_set_graphs(spec_model* m, int enable) {
   return SPEC_OK;
 }
 
+extern "C" int spec_model_profile(spec_model* m, int enable) {
+  if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
+  CUDA_TRY(cudaDeviceSynchronize());
+  for (auto& r : m->prof_recs) {
+    m->prof_pool.push_back(r.a);
+    m->prof_pool.push_back(r.b);
+  }
+  m->prof_recs.clear();
+  m->prof = enable != 0;
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_profile_read(spec_model* m, int kind, double* seconds,
+                                       int64_t* launches, double* bytes, double* flops) {
+  if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
+  if (kind < 0 || kind > SPEC_PROF_ATTN) return fail(SPEC_E_INVALID, "unknown kernel class");
+  CUDA_TRY(cudaDeviceSynchronize());
+  double t = 0.0, b = 0.0, f = 0.0;
+  int64_t n = 0;
+  for (const auto& r : m->prof_recs) {
+    const bool gemm = r.kind != SPEC_PROF_ATTN;
+    if (!(r.kind == kind || (kind == SPEC_PROF_ALL_GEMMS && gemm))) continue;
+    float ms = 0.0f;
+    CUDA_TRY(cudaEventElapsedTime(&ms, r.a, r.b));
+    t += ms * 1e-3;
+    b += r.bytes;
+    f += r.flops;
+    n++;
+  }
+  if (seconds) *seconds = t;
+  if (launches) *launches = n;
+  if (bytes) *bytes = b;
+  if (flops) *flops = f;
+  return SPEC_OK;
+}
+
+extern "C" int spec_model_set_wait_budget(spec_model* m, int tries) {
+  if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
+  if (tries < 0 || tries > LIN_WAIT_TRIES) return fail(SPEC_E_INVALID, "tries outside [0, 131072]");
+  if (tries == m->lscr.wait_tries) return SPEC_OK;
+  // the budget is a kernel argument: graphs captured with the old one go
+  CUDA_TRY(cudaDeviceSynchronize());
+  for (auto& kv : m->graphs) round_graph_free(&kv.second);
+  m->graphs.clear();
+  m->lscr.wait_tries = tries;
+  return SPEC_OK;
+}
+
 extern "C" int spec_state_set(spec_model* m, int n, const int32_t* seq_ids,
                               const int32_t* n_past, const uint64_t* emit_idx,
                               const int32_t* anchor) {
@@ -624,6 +690,42 @@ static int last_captured_node(cudaStream_t st, cudaGraphNode_t* node) {
   return SPEC_OK;
 }
 
+// In-round timing: an event pair around one launch (profiling rounds only).
+static cudaEvent_t prof_event(spec_model* m) {
+  if (!m->prof_pool.empty()) {
+    cudaEvent_t e = m->prof_pool.back();
+    m->prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+template <typename F>
+static int timed_launch(spec_model* m, cudaStream_t st, int kind, double bytes, double flops,
+                        F&& launch) {
+  if (!m->prof) return launch();
+  spec_model::ProfRec r{prof_event(m), prof_event(m), kind, bytes, flops};
+  if (r.a) cudaEventRecord(r.a, st);
+  const int rc = launch();
+  if (r.b) cudaEventRecord(r.b, st);
+  if (r.a && r.b) {
+    m->prof_recs.push_back(r);
+  } else {
+    if (r.a) m->prof_pool.push_back(r.a);
+    if (r.b) m->prof_pool.push_back(r.b);
+  }
+  return rc;
+}
+// Algorithmic bytes of one GEMM launch: the packed weights once, the fp16
+// activations in, the outputs (fp32 or fp16) out.
+static double gemm_bytes(const QMat& w, int R, int out_bytes) {
+  return (double)w.bytes + (double)R * w.K * 2 + (double)R * w.N * out_bytes;
+}
+
 // The target pass over rows [anchor, draft[s][0..nt-2]] of each sequence;
 // embed_node (capture only) receives the embedding node.
 static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draft,
@@ -656,25 +758,35 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
     eq.nkv = nkv;
     eq.hd = hd;
     eq.max_ctx = D.max_ctx;
-    int rc = linear_launch(m->wqkv[l], m->xa, R, eq, m->lscr, st);
+    const QMat &wq = m->wqkv[l], &wo = m->wo[l], &wg = m->wgu[l], &wd = m->wd[l];
+    auto flops = [R](const QMat& w) { return 2.0 * R * w.N * (double)w.K; };
+    int rc = timed_launch(m, st, SPEC_PROF_QKV, gemm_bytes(wq, R, 2), flops(wq),
+                          [&] { return linear_launch(wq, m->xa, R, eq, m->lscr, st); });
     if (rc) return rc;
-    rc = attn_launch(m->qbuf, kc, vc, m->rows, n_seq, nt, nq, nkv, hd, D.max_ctx, m->attn_part,
-                     m->ao, st);
+    // attention: its bytes depend on the sequences' positions, which only
+    // the device holds; the caller accounts for them
+    rc = timed_launch(m, st, SPEC_PROF_ATTN, 0.0, 0.0, [&] {
+                        return attn_launch(m->qbuf, kc, vc, m->rows, n_seq, nt, nq, nkv, hd,
+                                           D.max_ctx, m->attn_part, m->ao, st);
+                      });
     if (rc) return rc;
     LinEpi er;
     er.kind = EPI_RESID;
     er.y = m->h;
     er.ldy = H;
-    rc = linear_launch(m->wo[l], m->ao, R, er, m->lscr, st);
+    rc = timed_launch(m, st, SPEC_PROF_O, gemm_bytes(wo, R, 8), flops(wo),
+                      [&] { return linear_launch(wo, m->ao, R, er, m->lscr, st); });
     if (rc) return rc;
     launch_rmsnorm(m->h, m->norm_w + (size_t)(2 * l + 1) * H, R, H, D.rms_eps, m->xa, st);
     LinEpi es;
     es.kind = EPI_SWIGLU;
     es.out16 = m->xs;
     es.ldo = F;
-    rc = linear_launch(m->wgu[l], m->xa, R, es, m->lscr, st);
+    rc = timed_launch(m, st, SPEC_PROF_GATE_UP, gemm_bytes(wg, R, 1), flops(wg),
+                      [&] { return linear_launch(wg, m->xa, R, es, m->lscr, st); });
     if (rc) return rc;
-    rc = linear_launch(m->wd[l], m->xs, R, er, m->lscr, st);
+    rc = timed_launch(m, st, SPEC_PROF_DOWN, gemm_bytes(wd, R, 8), flops(wd),
+                      [&] { return linear_launch(wd, m->xs, R, er, m->lscr, st); });
     if (rc) return rc;
   }
   if (D.n_layers > 0)
@@ -685,7 +797,9 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
   el.ldy = V;
   el.argmax = m->argmax;
   el.err = m->err;
-  return linear_launch(m->lm, m->xa, R, el, m->lscr, st);
+  return timed_launch(m, st, SPEC_PROF_LM_HEAD, gemm_bytes(m->lm, R, write_logits ? 4 : 0),
+                      2.0 * R * m->lm.N * (double)m->lm.K,
+                      [&] { return linear_launch(m->lm, m->xa, R, el, m->lscr, st); });
 }
 
 // The target pass and, for a greedy round (greedy_tail), the fused accept +
@@ -716,7 +830,7 @@ static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, cons
     launch_accept_commit_greedy(a, s);
     return tail_node != nullptr ? last_captured_node(s, tail_node) : SPEC_OK;
   };
-  if (!m->use_graphs) return enqueue(st, nullptr, nullptr);
+  if (!m->use_graphs || m->prof) return enqueue(st, nullptr, nullptr);
   const long long key = ((long long)(host_io ? 1 : 0) << 40) | ((long long)n_seq << 20) |
                         ((long long)(d + 1) << 2) | (write_logits ? 2 : 0) | (greedy_tail ? 1 : 0);
   auto it = m->graphs.find(key);
@@ -836,6 +950,19 @@ extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* s
     return fail(SPEC_E_INVALID, "q_logits must be NULL in greedy mode");
   }
   cudaStream_t st = as_stream(stream);
+  // q_logits in host memory are copied into the model's buffer first
+  if (!greedy && d > 0) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, q_logits) != cudaSuccess) {
+      cudaGetLastError();
+      pa.type = cudaMemoryTypeUnregistered;
+    }
+    if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged) {
+      CUDA_TRY(cudaMemcpyAsync(m->qhost_buf, q_logits, sizeof(float) * n_seq * d * D.vocab,
+                               cudaMemcpyHostToDevice, st));
+      q_logits = m->qhost_buf;
+    }
+  }
   // the staging is free: every call has synchronised before returning
   std::memcpy(m->io_host_in, seq_ids, sizeof(int32_t) * n_seq);
   if (d > 0) std::memcpy(m->io_host_in + n_seq, draft, sizeof(int32_t) * n_seq * d);

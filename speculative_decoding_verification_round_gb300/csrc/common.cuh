@@ -19,7 +19,7 @@ enum : uint32_t {
   ERR_TOKEN = 1u << 0,     // token id outside [0, vocab)
   ERR_POS = 1u << 1,       // n_past + nt > max_ctx
   ERR_NONFINITE = 1u << 2, // NaN/Inf logit
-  ERR_SEQ = 1u << 3,       // sequence slot outside [0, max_seqs)
+  ERR_SEQ = 1u << 3,       // sequence slot outside [0, max_seqs), or named twice in a round
   ERR_TIMEOUT = 1u << 4,   // a bounded wait gave up
 };
 
@@ -103,7 +103,12 @@ struct LinEpi {
   uint32_t* err = nullptr;
 };
 
+// Tries of a bounded mbarrier wait (each suspends for at most ~10 us):
+// about a second in all.
+constexpr int LIN_WAIT_TRIES = 1 << 17;
+
 struct LinScratch {
+  int wait_tries = LIN_WAIT_TRIES;  // budget of a GEMM's first copy wait
   float* part = nullptr;         // K-split partials
   size_t part_floats = 0;
   unsigned* tickets = nullptr;   // zero-initialised, reset by their last user

@@ -1,7 +1,9 @@
 // depth.cu -- the adaptive draft-depth controller: host code only, no GPU
-// work ("Speculative Decoding (D5-R) -- Plan", status notes: per-round depth
-// from beta-smoothed per-depth acceptance, min-of-4 round-cost windows, a 10%
-// switch hysteresis, optimism for depths not yet seen, capped at d = 7).
+// work.  Source: "Speculative Decoding (D5-R) -- Plan", status notes, which
+// name only the ingredients of the page's controller (smoothed acceptance
+// estimates, a short window of measured round costs, hysteresis, trying
+// depths that have no measurement yet, an upper cap on d).  The concrete
+// rules below are this library's reading of those ingredients.
 //
 // Rules (the header states them for callers):
 //  * position i = 1..d_max holds decayed Beta counts (a_i, b_i); a round at

@@ -204,6 +204,7 @@ struct LinArgs {
   unsigned* tickets;  // [ZG][n_grp] K-split tickets, then [ZG] argmax tickets
   float2* amax_part;  // [ZG][n_grp][16]
   uint32_t* err;      // device error word (ERR_TIMEOUT on a copy that never arrived)
+  int first_tries;    // try budget of the first wait (the activation slice)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -240,9 +241,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for a phase of `bar`: about a second at most, then false.
-constexpr int MBAR_TRIES = 1 << 17;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < MBAR_TRIES; i++)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          int tries = LIN_WAIT_TRIES) {
+  for (int i = 0; i < tries; i++)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -588,7 +589,9 @@ linear_q_kernel(const LinArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; e++) acc[i][ct][e] = 0.0f;
 
-  bool ok = mbar_wait(xbar, 0);  // every warp waits for the slice (also the idle ones)
+  // every warp waits for the slice (also the idle ones); its budget is the
+  // one wait a caller may shorten, to exercise the path below
+  bool ok = mbar_wait(xbar, 0, a.first_tries);
   if (active) {
     // stages of CPS consecutive chunks; the loop is unrolled by the ring
     // depth, so stage indices, parities and ring addresses are constants
@@ -1067,6 +1070,7 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
   a.tickets = scr.tickets;
   a.amax_part = scr.amax_part;
   a.err = scr.err;
+  a.first_tries = scr.wait_tries;
   a.xstride = x_stride(w.nc_cta);
   const int ZG = col_groups(R);
   const int nct = col_tiles(R);

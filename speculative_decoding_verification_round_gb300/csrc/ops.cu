@@ -34,6 +34,17 @@ __device__ __forceinline__ RowInfo row_info(const int32_t* __restrict__ seq_ids,
   return RowInfo{slot, pos};
 }
 
+// Two sequences of one round naming the same slot would race on its KV rows
+// and commit twice ("Model-neutral Speculative Decoding", "Capabilities fail
+// closed"): sequence s compares its slot with those of sequences 0..s-1 and
+// flags ERR_SEQ on a repeat, which makes the round commit nothing.
+__device__ __forceinline__ bool slot_repeats(const int32_t* __restrict__ seq_ids, int s,
+                                             int raw, int t0, int step) {
+  for (int j = t0; j < s; j += step)
+    if (seq_ids[j] == raw) return true;
+  return false;
+}
+
 __global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, int nt,
                                 const int32_t* __restrict__ n_past, int max_seqs,
                                 int max_ctx, RowInfo* __restrict__ rows,
@@ -41,6 +52,8 @@ __global__ void row_info_kernel(const int32_t* __restrict__ seq_ids, int n_seq, 
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= n_seq * nt) return;
   rows[r] = row_info(seq_ids, r, nt, n_past, max_seqs, max_ctx, err);
+  if (r % nt == 0 && slot_repeats(seq_ids, r / nt, seq_ids[r / nt], 0, 1))
+    atomicOr(err, ERR_SEQ);
 }
 
 // One CTA (256 threads) per verify row: the row's (slot, position) record,
@@ -52,13 +65,14 @@ __global__ void embed_kernel(const EmbedArgs a) {
   grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
   const int r = blockIdx.x;
   const int s = r / a.nt, i = r % a.nt;
-  __shared__ int s_tok;
+  __shared__ int s_tok, s_raw;
   // the same record as row_info, with the loads in two dependent levels:
   // (slot, draft token), then (position, anchor); the token is published
   // first so that the row copy does not wait for the record
   int slot = 0, raw = 0;
   if (threadIdx.x == 0) {
     raw = a.seq_ids[s];
+    s_raw = raw;
     const int dtok = i > 0 ? a.draft[s * (a.nt - 1) + (i - 1)] : 0;
     slot = raw < 0 || raw >= a.max_seqs ? 0 : raw;
     int tok = i == 0 ? a.anchor[slot] : dtok;
@@ -79,6 +93,9 @@ __global__ void embed_kernel(const EmbedArgs a) {
     }
     a.rows[r] = RowInfo{slot, pos};
   }
+  // the sequence's first row checks that no earlier sequence names its slot
+  if (i == 0 && slot_repeats(a.seq_ids, s, s_raw, threadIdx.x, blockDim.x))
+    atomicOr(a.err, ERR_SEQ);
   // the row into h, then the first RMSNorm of it into xn: the sum of squares
   // in rmsnorm_kernel's order (thread-strided float4 partials, warp
   // butterfly, warps in order), so the result is that kernel's, bit for bit;

@@ -182,13 +182,16 @@ def test_stochastic_nonfinite_logit_fails_closed(dev):
 
 
 def test_stochastic_v16_distribution_chi2(orc, dev):
-    """GPU Monte Carlo over many sampler slots against the exact
-    distribution of the first emitted token (d=1, V=16): drafts come from q
-    by the harness sampler, the target row after the draft depends on it."""
+    """GPU Monte Carlo of 10^7 rounds (d = 1, V = 16) against the exact
+    distribution of the first emitted token that the exact-rational
+    enumeration gives for the integer decision rules.  Drafts are drawn from
+    the draft's integer weights (exactly Wq/Sq, by a host generator); the
+    target row after the draft depends on it; every round has its own
+    sampler counter (emitted slot, sequence id)."""
     from scipy.stats import chi2
     import speculative_decoding_verification_round_gb300 as sv
     from oracle import exact_v16 as ev
-    V, n_seq, batches, T = 16, 4096, 24, 1.0
+    V, n_seq, batches, T = 16, 1 << 16, 153, 1.0   # 10,027,008 rounds
     pair = ev.ToyPair(V=V, seed=21, T=T)
     exp0 = np.array([float(x) for x in
                      ev.emitted_conditionals(pair, 1, "implementation", check=False)[(0, ())]])
@@ -199,20 +202,24 @@ def test_stochastic_v16_distribution_chi2(orc, dev):
     lp1 = np.stack([(np.random.default_rng([21, 1, x]).standard_normal(V) * 2.0).astype(np.float32)
                     for x in range(V)])
     Wq, Sq = orc.row_weights(lq0, T)
+    cum = np.cumsum(np.asarray(Wq, np.uint64).astype(np.int64))
+    assert int(cum[-1]) == int(Sq)
     q = np.broadcast_to(lq0, (n_seq, 1, V)).copy()
     seq_ids = np.arange(n_seq)
+    hr = np.random.default_rng(2024)
     counts = np.zeros(V)
     for b in range(batches):
-        emit = np.full(n_seq, b * 7919, np.uint64) + np.arange(n_seq, dtype=np.uint64) * 1000003
-        draft = np.array([[orc.weight_pick(Wq, Sq, int(orc.uniforms(77, int(e), int(s), 1)[0]))]
-                          for e, s in zip(emit, seq_ids)], np.int32)
+        u = hr.integers(0, int(Sq), n_seq)
+        draft = np.searchsorted(cum, u, side="right").astype(np.int32)[:, None]
         p = np.empty((n_seq, 2, V), np.float32)
         p[:, 0] = lp0
         p[:, 1] = lp1[draft[:, 0]]
+        emit = np.full(n_seq, 2 * b, np.uint64)  # slots 2b, 2b+1: distinct per batch
         n_g, em_g, _, bits = run_stochastic(sv, dev, p, q, draft, T, 31337, seq_ids, emit)
         assert bits == 0
         counts += np.bincount(em_g[:, 0], minlength=V)
     n = counts.sum()
+    assert n == n_seq * batches >= 10 ** 7
     mask = exp0 * n > 5
     stat = (((counts - exp0 * n) ** 2) / (exp0 * n))[mask].sum()
     assert stat < chi2.ppf(1 - 1e-3, mask.sum() - 1), (stat, counts, exp0 * n)
