@@ -124,6 +124,18 @@ int spec_qmat_destroy(spec_qmat* m);
 int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
                   void* stream);
 
+/* The same product on the tensor cores, as multi-sequence rounds run it
+ * (tcgen05.mma with tensor-memory accumulators; rows are the N dimension):
+ * each 64-k chunk of W is dequantised once per CTA to fp16 w = fp16(q *
+ * scale) (one rounding, relative error <= 2^-11 per weight) and the sum is
+ * accumulated in fp32 over all K.  Every row is computed by the same
+ * instructions whatever R is, so a row's result does not depend on the other
+ * rows; it differs from spec_linear_q's in the last bits (that kernel keeps
+ * each 32-block's sum exact and applies the scale in fp32).
+ * 1 <= R <= max_rows (launched in blocks of 256 rows). */
+int spec_linear_q_tc(const spec_qmat* w, const uint16_t* x, int R, float* y,
+                     void* stream);
+
 /* ------------------------------------------------------------------------
  * Decoder model: RMSNorm -> QKV + rotate-half RoPE -> causal GQA attention
  * over the KV cache -> O + residual -> RMSNorm -> gate/up + SwiGLU -> down +
@@ -210,6 +222,16 @@ int spec_error_check(spec_model* m, void* stream, uint32_t* bits);
  * updated in place when they change from one call to the next.  0: launches
  * kernels one by one. */
 int spec_model_set_graphs(spec_model* m, int enable);
+
+/* Which GEMM a round's linear layers (and LM head) run on is chosen by the
+ * round's number of sequences, never by d: rounds of at least `min_seqs`
+ * sequences use the tensor-core GEMM of spec_linear_q_tc, the others the
+ * GEMM of spec_linear_q.  So a sequence's rows are bitwise the same at every
+ * depth d for a given batch size, and greedy speculative decoding of a batch
+ * is byte-identical to plain decoding of the same batch.  Default 2; 0 turns
+ * the tensor-core GEMM off.  Synchronises the device and drops captured
+ * graphs. */
+int spec_model_set_tc_min_seqs(spec_model* m, int min_seqs);
 
 /* In-round kernel timing.  enable = 1: the model's later rounds launch their
  * kernels one by one (no graph), with a CUDA event recorded before and after

@@ -31,6 +31,7 @@ SPEC_PROF_QKV, SPEC_PROF_O, SPEC_PROF_GATE_UP, SPEC_PROF_DOWN = 0, 1, 2, 3
 SPEC_PROF_LM_HEAD, SPEC_PROF_ALL_GEMMS, SPEC_PROF_ATTN = 4, 5, 6
 
 EXPORTED = ["spec_last_error", "spec_qmat_create", "spec_qmat_destroy", "spec_linear_q",
+            "spec_linear_q_tc", "spec_model_set_tc_min_seqs",
             "spec_model_create", "spec_model_destroy", "spec_model_kv_cache", "spec_kv_fill",
             "spec_kv_read", "spec_model_debug_read",
             "spec_state_set", "spec_state_get", "spec_error_check", "spec_model_set_graphs",
@@ -98,6 +99,8 @@ def lib():
                 "spec_qmat_create": (I32, [ctypes.POINTER(spec_qweight), I32, P, ctypes.POINTER(P)]),
                 "spec_qmat_destroy": (I32, [P]),
                 "spec_linear_q": (I32, [P, P, I32, P, P]),
+                "spec_linear_q_tc": (I32, [P, P, I32, P, P]),
+                "spec_model_set_tc_min_seqs": (I32, [P, I32]),
                 "spec_model_create": (I32, [ctypes.POINTER(spec_model_desc),
                                             ctypes.POINTER(spec_model_weights), P, ctypes.POINTER(P)]),
                 "spec_model_destroy": (I32, [P]),
@@ -208,6 +211,11 @@ def spec_linear_q(w: QMat, x, nt: int, y, stream=None):
     _check(lib().spec_linear_q(w.handle, _ptr(x), int(nt), _ptr(y), _stream(stream)))
 
 
+def spec_linear_q_tc(w: QMat, x, R: int, y, stream=None):
+    """The same product on the tensor-core GEMM of multi-sequence rounds."""
+    _check(lib().spec_linear_q_tc(w.handle, _ptr(x), int(R), _ptr(y), _stream(stream)))
+
+
 # ---------------------------------------------------------------------------
 # the decoder model
 # ---------------------------------------------------------------------------
@@ -255,6 +263,10 @@ class Model:
 
     def set_graphs(self, enable: bool):
         _check(lib().spec_model_set_graphs(self.handle, int(bool(enable))))
+
+    def set_tc_min_seqs(self, min_seqs: int):
+        """Rounds of at least min_seqs sequences use the tensor-core GEMM (0: never)."""
+        _check(lib().spec_model_set_tc_min_seqs(self.handle, int(min_seqs)))
 
     def profile(self, enable: bool):
         """In-round kernel timing on (raw launches, events around each GEMM and

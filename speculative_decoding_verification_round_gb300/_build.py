@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libspecverify.so")
-SOURCES = ["api.cu", "linear.cu", "attn.cu", "ops.cu", "accept.cu", "depth.cu"]
+SOURCES = ["api.cu", "linear.cu", "tcgemm.cu", "attn.cu", "ops.cu", "accept.cu", "depth.cu"]
 # host code whose doubles must be rounded operation by operation
 FILE_FLAGS = {"depth.cu": ["-Xcompiler", "-ffp-contract=off"]}
 HEADERS = [os.path.join(CSRC, "common.cuh"),

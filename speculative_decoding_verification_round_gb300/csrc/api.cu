@@ -46,6 +46,7 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 void attn_init_attrs();
 void accept_init_attrs();
 void linear_init_attrs();
+void tc_init_attrs();
 static std::mutex g_attr_mu;
 static std::vector<int> g_attr_done;
 static void init_attrs_once() {
@@ -56,6 +57,7 @@ static void init_attrs_once() {
   attn_init_attrs();
   accept_init_attrs();
   linear_init_attrs();
+  tc_init_attrs();
   g_attr_done.push_back(dev);
 }
 
@@ -141,15 +143,20 @@ static int alloc_lin_scratch(const std::vector<const QMat*>& mats, int R, LinScr
     part = std::max(part, lin_part_floats(*q, R));
     tick = std::max(tick, lin_tickets_needed(*q, R));
     amax = std::max(amax, lin_amax_entries(*q, R));
+    part = std::max(part, tc_part_floats(*q, R));
+    tick = std::max(tick, tc_tickets_needed(*q));
   }
   tick = std::max(tick, (size_t)64);
-  const size_t bytes =
-      part * sizeof(float) + amax * sizeof(float2) + tick * sizeof(unsigned) + 16 + 256;
+  const size_t keys = 256;  // packed argmax maxima of the tensor-core LM head
+  const size_t bytes = keys * sizeof(unsigned long long) + part * sizeof(float) +
+                       amax * sizeof(float2) + tick * sizeof(unsigned) + 16 + 256;
   if (cudaMalloc(base, bytes) != cudaSuccess) {
     cudaGetLastError();
     return fail(SPEC_E_OOM, "linear scratch");
   }
   char* p = (char*)*base;
+  scr->amax_keys = (unsigned long long*)p;
+  p += keys * sizeof(unsigned long long);
   scr->part = (float*)p;
   scr->part_floats = part;
   p += part * sizeof(float);
@@ -161,6 +168,7 @@ static int alloc_lin_scratch(const std::vector<const QMat*>& mats, int R, LinScr
   p += tick * sizeof(unsigned);
   scr->err = (uint32_t*)p;  // the scratch's own error word (a model points it at its word)
   CUDA_TRY(cudaMemset(scr->tickets, 0, tick * sizeof(unsigned) + 16));
+  CUDA_TRY(cudaMemset(scr->amax_keys, 0, keys * sizeof(unsigned long long)));
   return SPEC_OK;
 }
 
@@ -205,6 +213,18 @@ extern "C" int spec_qmat_destroy(spec_qmat* m) {
   if (m->scr_base) cudaFree(m->scr_base);
   delete m;
   return SPEC_OK;
+}
+
+extern "C" int spec_linear_q_tc(const spec_qmat* w, const uint16_t* x, int R, float* y,
+                                void* stream) {
+  if (w == nullptr || x == nullptr || y == nullptr) return fail(SPEC_E_INVALID, "null argument");
+  if (R < 1 || R > w->max_rows) return fail(SPEC_E_SHAPE, "R outside [1, max_rows]");
+  if (!aligned16(x)) return fail(SPEC_E_SHAPE, "x must be 16-byte aligned");
+  LinEpi e;
+  e.kind = EPI_STORE;
+  e.y = y;
+  e.ldy = w->w.N;
+  return tc_linear_launch(w->w, reinterpret_cast<const __half*>(x), R, e, w->scr, as_stream(stream));
 }
 
 extern "C" int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
@@ -283,6 +303,7 @@ struct spec_model {
   StochScratch sscr;
   std::vector<void*> allocs;
   bool use_graphs = true;
+  int tc_min_seqs = 2;  // rounds of at least this many sequences use the tensor-core GEMM
   // in-round kernel timing (spec_model_profile): events around each GEMM and
   // attention launch of raw-launched rounds
   struct ProfRec {
@@ -568,6 +589,17 @@ extern "C" int spec_model_set_graphs(spec_model* m, int enable) {
   return SPEC_OK;
 }
 
+extern "C" int spec_model_set_tc_min_seqs(spec_model* m, int min_seqs) {
+  if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
+  if (min_seqs < 0) return fail(SPEC_E_INVALID, "min_seqs must be >= 0");
+  if (min_seqs == m->tc_min_seqs) return SPEC_OK;
+  CUDA_TRY(cudaDeviceSynchronize());
+  for (auto& kv : m->graphs) round_graph_free(&kv.second);
+  m->graphs.clear();
+  m->tc_min_seqs = min_seqs;
+  return SPEC_OK;
+}
+
 extern "C" int spec_model_profile(spec_model* m, int enable) {
   if (m == nullptr) return fail(SPEC_E_INVALID, "null model");
   CUDA_TRY(cudaDeviceSynchronize());
@@ -732,6 +764,13 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
                            const int32_t* seq_ids, bool write_logits, cudaStream_t st,
                            cudaGraphNode_t* embed_node) {
   const spec_model_desc& D = m->d;
+  // the GEMM is chosen by the number of sequences, never by nt: a round's
+  // rows are bitwise the same at every depth d
+  const bool tc = m->tc_min_seqs > 0 && n_seq >= m->tc_min_seqs;
+  auto linear_launch = [tc](const QMat& w, const __half* x, int R, const LinEpi& e,
+                            const LinScratch& scr, cudaStream_t s) {
+    return tc ? tc_linear_launch(w, x, R, e, scr, s) : ::linear_launch(w, x, R, e, scr, s);
+  };
   const int R = n_seq * nt, H = D.hidden, F = D.ffn, hd = D.head_dim, nq = D.n_q_heads,
             nkv = D.n_kv_heads, V = D.vocab;
   // the first RMSNorm runs inside the embedding kernel, the others as

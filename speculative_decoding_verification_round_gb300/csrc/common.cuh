@@ -59,6 +59,7 @@ struct QMat {
   int S = 1;         // K segments across CTAs
   int nc_cta = 0;    // chunks of one CTA's K range (at most)
                      // (kw, S) are fixed per matrix: independent of nt
+  int tc_S = 1;      // K segments of the tensor-core GEMM (multi-sequence rounds)
   uint8_t* rec = nullptr;  // [n_pairs][nch][rec_bytes]
   void* base = nullptr;    // single allocation
   size_t bytes = 0;        // streamed bytes
@@ -115,6 +116,7 @@ struct LinScratch {
   size_t n_tickets = 0;
   float2* amax_part = nullptr;   // LM-head argmax partials (value, index bits)
   size_t amax_entries = 0;
+  unsigned long long* amax_keys = nullptr;  // [256] packed maxima of the tensor-core LM head (zeroed)
   uint32_t* err = nullptr;       // device error word
 };
 
@@ -123,6 +125,15 @@ size_t lin_tickets_needed(const QMat& w, int R);
 size_t lin_amax_entries(const QMat& w, int R);
 int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
                   const LinScratch& scr, cudaStream_t st);
+
+// The tensor-core (tcgen05) verify GEMM of multi-sequence rounds (tcgemm.cu):
+// 1 <= R <= 256 rows per launch, the same epilogues.
+int tc_npad(int R);
+int tc_choose_split(int N, int nch, int sms);
+size_t tc_part_floats(const QMat& w, int R);
+size_t tc_tickets_needed(const QMat& w);
+int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
+                     const LinScratch& scr, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // small ops (ops.cu)

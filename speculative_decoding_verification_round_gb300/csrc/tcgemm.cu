@@ -1,0 +1,806 @@
+// tcgemm.cu -- the verify GEMM of multi-sequence rounds on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// "Speculative Decoding (D5-R) -- Plan", section 1: the batched verify is one
+// weights-once pass.  With many sequences in a round (the batched workload:
+// 12 sequences x 16 rows = 192 rows) the pass is no longer bound by the
+// weight stream but by the contraction itself (2 x 192 flops per weight), so
+// it runs on tcgen05.mma with the activation rows as the N dimension:
+//
+//   * a CTA owns 128 weight rows (4 pairs of the packed streaming layout, one
+//     TMEM lane each) and one of S segments of K; its accumulator is
+//     128 x Npad fp32 in tensor memory (Npad = the rows rounded up to 16);
+//   * warp 0 streams the packed weight records into a shared-memory ring with
+//     TMA bulk copies; warp 1 loads the activation tile of each 64-k chunk
+//     with a 2-D TMA tensor copy (128-byte swizzle, rows past R read as zero);
+//   * warps 3-6 dequantise each chunk into an fp16 A tile in the UMMA
+//     K-major 128-byte-swizzle layout: w = fp16(q * scale), one rounding (the
+//     block integers are exact in fp16, the product is rounded once);
+//   * one thread of warp 2 issues four tcgen05.mma (M 128, N Npad, K 16) per
+//     chunk and commits them to the stage's "empty" barrier;
+//   * after the last chunk the same four warps read the accumulator back
+//     (tcgen05.ld), add the K segments in segment order (the last CTA of a
+//     tile, by a ticket) and run the fused epilogue (store, residual add,
+//     SwiGLU, RoPE + KV write, LM head logits + argmax).
+// Each output element is one accumulation chain whose instructions do not
+// depend on the other rows of the batch, so a row's result is the same in
+// every batch this kernel runs.
+//
+// Every wait is bounded (mbarrier try_wait with a suspend hint, about a
+// second in all); one that gives up sets ERR_TIMEOUT and the CTA stops
+// issuing work, waits (bounded) for what it issued and frees its tensor
+// memory before it returns.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int TC_M = 128;           // weight rows of a CTA
+constexpr int TC_THREADS = 224;     // 7 warps
+constexpr int TC_EPI_WARP0 = 3;     // warps 3..6: dequant, then epilogue
+constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16
+constexpr int TC_MAX_ST = 4;
+constexpr int TC_MAX_RAW = 8;
+
+template <int QT>
+struct TcRec {  // the packed record of one (pair, 64-k chunk): see linear.cu
+  static constexpr int QS_TILE = QT == 8 ? 1024 : 512;
+  static constexpr int SC = 2 * QS_TILE;
+  static constexpr int QH = SC + 128;
+  static constexpr int BYTES = QH + (QT == 6 ? 512 : 0);
+};
+
+struct TcArgs {
+  const uint8_t* rec;  // [n_pairs][nch][rec]
+  int N, K, nch, n_pairs, n_mt, S, R, Npad, tmem_cols, stages, raw_depth;
+  LinEpi epi;
+  float* part;          // [S][n_mt][Npad][128] K-split partials
+  unsigned* tickets;    // [n_mt] K-split tickets, then [1] argmax ticket
+  unsigned long long* amax_key;  // [Npad] LM head: packed (value, index) maxima
+  uint32_t* err;
+  int wait_tries;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// --- mbarrier --------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(10000)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false after `tries` suspended tries, or at once when another
+// role of the CTA has given up (abort != 0).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int tries,
+                                          const volatile int* abort = nullptr) {
+  for (int i = 0; i < tries; i++) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+  }
+  return false;
+}
+
+// --- copies ----------------------------------------------------------------
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// 2-D tiled TMA load: box of the tensor map at (x = k, y = row).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --- tcgen05 ---------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B,
+// 8-row atoms of 1024 B (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+// Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
+// M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of 16-byte unit u (k = 8u..8u+7) of row r in a K-major
+// 128-byte-swizzled tile of 64-k rows.
+__device__ __forceinline__ uint32_t sw128_off(int r, int u) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
+}
+
+// fp16 weights of one k16 step's word for rows g and g+8 (4 + 4 values):
+// the integers u are placed in the low bits of each half, made 1024 + u by
+// the fp16 exponent of 1024, then (1024 + u) - (1024 + bias) = q exactly and
+// q * scale rounded once.  lo/hi: k pairs (0,1) and (2,3) of each row.
+template <int QT>
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t hx, __half2 sg, __half2 sg8,
+                                        __half2 (&rg)[2], __half2 (&rg8)[2]) {
+  constexpr uint32_t MAGIC = 0x64006400u;
+  const __half2 off = QT == 4 ? __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408))
+                              : __halves2half2(__ushort_as_half(0x6420), __ushort_as_half(0x6420));
+  uint32_t u[4];
+  if constexpr (QT == 4) {
+    u[0] = (w & 0x000F000Fu) | MAGIC;          // row g,   k 0,1
+    u[1] = ((w >> 8) & 0x000F000Fu) | MAGIC;   // row g,   k 2,3
+    u[2] = ((w >> 4) & 0x000F000Fu) | MAGIC;   // row g+8, k 0,1
+    u[3] = ((w >> 12) & 0x000F000Fu) | MAGIC;  // row g+8, k 2,3
+  } else {
+    const uint32_t w8 = w >> 8, hx2 = hx >> 2;
+    u[0] = (w & 0x000F000Fu) | (hx & 0x00300030u) | MAGIC;
+    u[1] = (w8 & 0x000F000Fu) | (hx2 & 0x00300030u) | MAGIC;
+    u[2] = ((w >> 4) & 0x000F000Fu) | ((hx >> 4) & 0x00300030u) | MAGIC;
+    u[3] = ((w8 >> 4) & 0x000F000Fu) | ((hx2 >> 4) & 0x00300030u) | MAGIC;
+  }
+  rg[0] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[0]), off), sg);
+  rg[1] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[1]), off), sg);
+  rg8[0] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[2]), off), sg8);
+  rg8[1] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[3]), off), sg8);
+}
+
+// Q8: one word holds u = q + 128 of rows r, r, r', r' at k, k+1.
+__device__ __forceinline__ void dq_word8(uint32_t w, __half2 sg, __half2 sg8, __half2& rg,
+                                         __half2& rg8) {
+  const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  const uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);
+  rg = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&a), off), sg);
+  rg8 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), off), sg8);
+}
+
+__device__ __forceinline__ uint4 pack4(__half2 a, __half2 b, __half2 c, __half2 d) {
+  return make_uint4(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b),
+                    *reinterpret_cast<const uint32_t*>(&c), *reinterpret_cast<const uint32_t*>(&d));
+}
+
+// Order-preserving 32-bit key of a float (-0 taken as +0, so that the two
+// zeros tie and the lower id wins, as in the other argmax paths).
+__device__ __forceinline__ uint32_t f32_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ void epi_bar() {  // the four epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// The dequant of one 64-k chunk of one pair (two 16-row tiles) by one lane:
+// lane unit (g, t) holds rows g and g+8 of each tile at k = 32b + 8t .. +7.
+// The lane -> (g, t) map makes both the record loads and the swizzled
+// stores of every 8-lane phase hit 8 distinct bank groups.
+template <int QT>
+__device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned char* atile,
+                                              int pair_in_cta, int lane) {
+  using RC = TcRec<QT>;
+  const int ph = lane >> 3, j = lane & 7;
+  const int p = j & 1, t0 = (j >> 1) & 1, t1 = j >> 2;
+  const int g = 4 * (p ^ (ph >> 1)) + 2 * (t0 ^ (ph & 1)) + p, t = 2 * t1 + t0;
+  const int l = 4 * g + t;  // the record's lane index of this unit
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    const uint2 sw = *reinterpret_cast<const uint2*>(raw + RC::SC + i * 64 + g * 8);
+    const __half2 s0 = *reinterpret_cast<const __half2*>(&sw.x);  // (row g, row g+8), block 0
+    const __half2 s1 = *reinterpret_cast<const __half2*>(&sw.y);  // block 1
+    const int r0 = 32 * pair_in_cta + 16 * i + g;                 // A-tile row of row g
+    unsigned char* row_g = atile;
+#pragma unroll
+    for (int b = 0; b < 2; b++) {
+      const __half2 sg = b == 0 ? __low2half2(s0) : __low2half2(s1);
+      const __half2 sg8 = b == 0 ? __high2half2(s0) : __high2half2(s1);
+      uint4 vg, vg8;
+      if constexpr (QT == 8) {
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + i * RC::QS_TILE + l * 32 + b * 16);
+        __half2 a[4], c[4];
+        dq_word8(q.x, sg, sg8, a[0], c[0]);
+        dq_word8(q.y, sg, sg8, a[1], c[1]);
+        dq_word8(q.z, sg, sg8, a[2], c[2]);
+        dq_word8(q.w, sg, sg8, a[3], c[3]);
+        vg = pack4(a[0], a[1], a[2], a[3]);
+        vg8 = pack4(c[0], c[1], c[2], c[3]);
+      } else {
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + i * RC::QS_TILE + l * 16);
+        uint32_t hA = 0, hB = 0;
+        if constexpr (QT == 6) {
+          const uint2 hw = *reinterpret_cast<const uint2*>(raw + RC::QH + i * 256 + l * 8);
+          hA = b == 0 ? hw.x : hw.y;
+          hB = __funnelshift_l(hA, hA, 8);
+        }
+        const uint32_t w0 = b == 0 ? q.x : q.z, w1 = b == 0 ? q.y : q.w;
+        __half2 a0[2], c0[2], a1[2], c1[2];
+        dq_word<QT>(w0, hA, sg, sg8, a0, c0);  // k 0..3
+        dq_word<QT>(w1, hB, sg, sg8, a1, c1);  // k 4..7
+        vg = pack4(a0[0], a0[1], a1[0], a1[1]);
+        vg8 = pack4(c0[0], c0[1], c1[0], c1[1]);
+      }
+      const int u = 4 * b + t;
+      *reinterpret_cast<uint4*>(row_g + sw128_off(r0, u)) = vg;
+      *reinterpret_cast<uint4*>(row_g + sw128_off(r0 + 8, u)) = vg8;
+    }
+  }
+}
+
+// Epilogue of 32 finished columns (activation rows col0..col0+31) of this
+// thread's weight row n: v[c] is the sum for row col0 + c.
+__device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, const float (&v)[32],
+                                              int lane, uint32_t* s_key, int quad) {
+  const LinEpi& e = a.epi;
+  const bool real = n < a.N;
+  switch (e.kind) {
+    case EPI_STORE:
+    case EPI_RESID:
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const int r = col0 + c;
+        if (real && r < a.R) {
+          float* p = e.y + (size_t)r * e.ldy + n;
+          *p = e.kind == EPI_RESID ? *p + v[c] : v[c];
+        }
+      }
+      break;
+    case EPI_SWIGLU: {
+      // rows g (gate j) and g+8 (up j) of each 16-row tile are lanes l, l+8
+      const int g = n & 15, T = n >> 4;
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const float up = __shfl_xor_sync(0xffffffffu, v[c], 8);
+        const int r = col0 + c;
+        if (g < 8 && real && r < a.R) {
+          const float x0 = v[c];
+          const float sil = x0 / (1.0f + expf(-x0));
+          e.out16[(size_t)r * e.ldo + T * 8 + g] = __float2half_rn(sil * up);
+        }
+      }
+      break;
+    }
+    case EPI_QKV: {
+      const int g = n & 15, T = n >> 4;
+      const int per_head = e.hd / 16;
+      const int hh = T / per_head, jj = T % per_head;
+      const int i0 = 8 * jj + (g & 7), i1 = e.hd / 2 + 8 * jj + (g & 7);
+      const bool rope = e.rope != nullptr && hh < e.nq + e.nkv;
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const float x1 = __shfl_xor_sync(0xffffffffu, v[c], 8);
+        const int r = col0 + c;
+        if (g >= 8 || !real || r >= a.R) continue;
+        const float x0 = v[c];
+        const RowInfo ri = e.rows[r];
+        float y0 = x0, y1 = x1;
+        if (rope) {
+          const int rp = ri.pos < e.max_ctx ? ri.pos : e.max_ctx - 1;
+          const float2 cs = e.rope[(size_t)max(rp, 0) * (e.hd / 2) + i0];
+          y0 = fmaf(x0, cs.x, -x1 * cs.y);
+          y1 = fmaf(x1, cs.x, x0 * cs.y);
+        }
+        __half* dst;
+        if (hh < e.nq) {
+          dst = e.out16 + ((size_t)r * e.nq + hh) * e.hd;
+        } else {
+          const bool isk = hh < e.nq + e.nkv;
+          const int kvh = isk ? hh - e.nq : hh - e.nq - e.nkv;
+          if (ri.pos >= e.max_ctx) continue;  // flagged by the embedding kernel
+          dst = (isk ? e.kcache : e.vcache) + (((size_t)ri.slot * e.nkv + kvh) * e.max_ctx + ri.pos) * e.hd;
+        }
+        dst[i0] = __float2half_rn(y0);
+        dst[i1] = __float2half_rn(y1);
+      }
+      break;
+    }
+    case EPI_LMHEAD: {
+      // the CTA's best (value, lowest id) of each column: a warp reduction
+      // of order-preserving keys, then the four warps through shared memory
+      bool bad = false;
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const int r = col0 + c;
+        if (r >= a.R) continue;  // uniform across the warp
+        if (e.y != nullptr && real) e.y[(size_t)r * e.ldy + n] = v[c];
+        bad |= real && v[c] != v[c];
+        const uint32_t key = real ? f32_key(v[c]) : 0u;
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+        const uint32_t id = key == kmax && real ? (uint32_t)n : 0xffffffffu;
+        const uint32_t imin = __reduce_min_sync(0xffffffffu, id);
+        if (lane == 0) {
+          s_key[(quad * 2) * 256 + r] = kmax;
+          s_key[(quad * 2 + 1) * 256 + r] = imin;
+        }
+      }
+      if (bad) atomicOr(e.err, ERR_NONFINITE);
+      break;
+    }
+  }
+}
+
+template <int QT>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
+  using RC = TcRec<QT>;
+  extern __shared__ unsigned char smem_dyn[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) unsigned long long s_bar[4 * TC_MAX_ST + 2 * TC_MAX_RAW + 1];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort, s_last;
+  __shared__ uint32_t s_key[8 * 256];  // LM head: [warp quad][key, id][column]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, seg = blockIdx.y;
+  const int ST = a.stages, RAWN = a.raw_depth;
+  const int B_BYTES = a.Npad * 128;
+  unsigned char* A0 = smem;
+  unsigned char* B0 = smem + ST * TC_A_BYTES;
+  unsigned char* RAW0 = B0 + ST * B_BYTES;
+  const int RAW_BYTES = 4 * RC::BYTES;
+  // barriers: a_full[ST], b_full[ST], empty[ST], (spare)[ST], raw_full[RAW], raw_empty[RAW], acc
+  const uint32_t bar0 = smem_u32(s_bar);
+  auto A_FULL = [&](int s) { return bar0 + 8 * s; };
+  auto B_FULL = [&](int s) { return bar0 + 8 * (TC_MAX_ST + s); };
+  auto EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_MAX_ST + s); };
+  auto RAW_FULL = [&](int r) { return bar0 + 8 * (4 * TC_MAX_ST + r); };
+  auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (4 * TC_MAX_ST + TC_MAX_RAW + r); };
+  const uint32_t ACC = bar0 + 8 * (4 * TC_MAX_ST + 2 * TC_MAX_RAW);
+
+  // this CTA's K range (chunks) and pairs
+  const int c0 = (int)((long long)seg * a.nch / a.S);
+  const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c0;
+  const int pair0 = mt * 4;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; s++) {
+      mbar_init(A_FULL(s), 128);
+      mbar_init(B_FULL(s), 1);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int r = 0; r < RAWN; r++) {
+      mbar_init(RAW_FULL(r), 1);
+      mbar_init(RAW_EMPTY(r), 128);
+    }
+    mbar_init(ACC, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_abort = 0;
+  }
+  if (warp == 2) {  // tensor memory for the accumulator: whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  auto give_up = [&]() {
+    atomicOr(a.err, ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  int issued = 0;  // copies issued by this thread (producers): drained on abort
+  if (warp == 0) {
+    // ---- weight records: one bulk copy per pair and chunk (weights are
+    // ---- constant: this starts before the grid dependency resolves)
+    if (lane == 0) {
+      for (int c = 0; c < nc && !*abort_flag; c++) {
+        const int r = c % RAWN, ur = c / RAWN;
+        if (ur > 0 && !mbar_wait(RAW_EMPTY(r), (ur - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
+          give_up();
+          break;
+        }
+        issued = c + 1;
+        int np = 0;
+        for (int p = 0; p < 4; p++) np += pair0 + p < a.n_pairs;
+        mbar_expect_tx(RAW_FULL(r), (uint32_t)(np * RC::BYTES));
+        for (int p = 0; p < 4; p++)
+          if (pair0 + p < a.n_pairs)
+            bulk_copy(smem_u32(RAW0 + r * RAW_BYTES + p * RC::BYTES),
+                      a.rec + ((size_t)(pair0 + p) * a.nch + c0 + c) * RC::BYTES, RC::BYTES,
+                      RAW_FULL(r));
+      }
+    }
+    grid_dep_wait();
+  } else if (warp == 1) {
+    // ---- activation tiles (written by the previous kernels)
+    grid_dep_wait();
+    if (lane == 0) {
+      for (int c = 0; c < nc && !*abort_flag; c++) {
+        const int s = c % ST, us = c / ST;
+        if (us > 0 && !mbar_wait(EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
+          give_up();
+          break;
+        }
+        issued = c + 1;
+        mbar_expect_tx(B_FULL(s), (uint32_t)B_BYTES);
+        tma_load_2d(smem_u32(B0 + s * B_BYTES), &tmx, (c0 + c) * 64, 0, B_FULL(s));
+      }
+    }
+  } else if (warp == 2) {
+    // ---- MMA issue: one thread
+    grid_dep_wait();
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(a.Npad);
+      int c = 0;
+      for (; c < nc && !*abort_flag; c++) {
+        const int s = c % ST, us = c / ST;
+        if (!mbar_wait(A_FULL(s), us & 1, LIN_WAIT_TRIES, abort_flag) ||
+            !mbar_wait(B_FULL(s), us & 1, LIN_WAIT_TRIES, abort_flag)) {
+          give_up();
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(smem_u32(A0 + s * TC_A_BYTES));
+        const uint64_t bd = smem_desc_sw128(smem_u32(B0 + s * B_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++)  // 16 k (32 bytes) per instruction
+          tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(EMPTY(s));
+      }
+      tc_commit(ACC);  // completes when every MMA issued above has
+    }
+  } else {
+    // ---- dequant (warps 3..6: one pair of the CTA's four each)
+    const int pc = warp - TC_EPI_WARP0;
+    grid_dep_wait();
+    for (int c = 0; c < nc && !*abort_flag; c++) {
+      const int r = c % RAWN, ur = c / RAWN, s = c % ST, us = c / ST;
+      // the first wait's budget is the one a caller may shorten (test hook)
+      bool ok = mbar_wait(RAW_FULL(r), ur & 1, c == 0 ? a.wait_tries : LIN_WAIT_TRIES, abort_flag);
+      if (ok && us > 0) ok = mbar_wait(EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag);
+      if (!ok) {
+        give_up();
+        break;
+      }
+      unsigned char* at = A0 + s * TC_A_BYTES;
+      if (pair0 + pc < a.n_pairs) {
+        dequant_chunk<QT>(RAW0 + r * RAW_BYTES + pc * RC::BYTES, at, pc, lane);
+      } else {  // rows past the matrix: zeros
+        for (int q = lane; q < 32 * 8 / 1; q += 32) {
+          const int rr = 32 * pc + q / 8, u = q % 8;
+          *reinterpret_cast<uint4*>(at + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      mbar_arrive(RAW_EMPTY(r));
+      fence_proxy_async();  // the A tile, to the tensor core's proxy
+      mbar_arrive(A_FULL(s));
+    }
+  }
+  grid_dep_launch();
+
+  // ---- epilogue: warps 3..6 (TMEM lane quadrant warp % 4)
+  if (warp >= TC_EPI_WARP0) {
+    const int quad = warp & 3;
+    const int m = 32 * quad + lane;  // TMEM lane = weight row of the tile
+    const int n = mt * TC_M + m;
+    const bool acc_ok = mbar_wait(ACC, 0, LIN_WAIT_TRIES);
+    if (!acc_ok) give_up();
+    tc_fence_after();
+    const bool aborted = *abort_flag != 0;
+    // K split: every CTA leaves its partial; the last of the tile adds the
+    // segments in order
+    bool finisher = true;
+    if (a.S > 1) {
+      for (int col0 = 0; col0 < a.Npad; col0 += 32) {
+        uint32_t v[32];
+        tc_ld32(tmem + ((uint32_t)(32 * quad) << 16) + col0, v);
+        float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * TC_M + m;
+#pragma unroll
+        for (int c = 0; c < 32; c++) dst[(size_t)c * TC_M] = __uint_as_float(v[c]);
+      }
+      epi_bar();
+      if (threadIdx.x == TC_EPI_WARP0 * 32) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.tickets[mt], 1u);
+        s_last = prev == (unsigned)(a.S - 1);
+        if (s_last) __threadfence();
+      }
+      epi_bar();
+      finisher = s_last != 0;
+    }
+    if (finisher) {
+      for (int col0 = 0; col0 < a.Npad; col0 += 32) {
+        float v[32];
+        if (a.S > 1) {
+          const float* src = a.part + ((size_t)mt * a.Npad + col0) * TC_M + m;
+          const size_t step = (size_t)a.n_mt * a.Npad * TC_M;
+#pragma unroll
+          for (int c = 0; c < 32; c++) v[c] = __ldcg(src + (size_t)c * TC_M);
+          for (int s2 = 1; s2 < a.S; s2++)
+#pragma unroll
+            for (int c = 0; c < 32; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_M);
+        } else {
+          uint32_t u[32];
+          tc_ld32(tmem + ((uint32_t)(32 * quad) << 16) + col0, u);
+#pragma unroll
+          for (int c = 0; c < 32; c++) v[c] = __uint_as_float(u[c]);
+        }
+        if (!aborted) tc_epilogue32(a, n, col0, v, lane, s_key, quad);
+      }
+      if (a.S > 1 && threadIdx.x == TC_EPI_WARP0 * 32) a.tickets[mt] = 0u;
+      if (a.epi.kind == EPI_LMHEAD) {
+        // the CTA's best of each column -> one packed 64-bit maximum per
+        // column (value key high, inverted id low: ties go to the lowest id);
+        // an aborted CTA still takes its ticket, so the state is reset
+        epi_bar();
+        for (int r = threadIdx.x - TC_EPI_WARP0 * 32; r < a.R && !aborted; r += 128) {
+          uint32_t bk = s_key[r], bi = s_key[256 + r];
+          for (int q = 1; q < 4; q++) {
+            const uint32_t k2 = s_key[(2 * q) * 256 + r], i2 = s_key[(2 * q + 1) * 256 + r];
+            if (k2 > bk || (k2 == bk && i2 < bi)) {
+              bk = k2;
+              bi = i2;
+            }
+          }
+          atomicMax(&a.amax_key[r], ((unsigned long long)bk << 32) | (unsigned long long)(~bi));
+        }
+        epi_bar();
+        if (threadIdx.x == TC_EPI_WARP0 * 32) {
+          __threadfence();
+          const unsigned prev = atomicAdd(&a.tickets[a.n_mt], 1u);
+          s_last = prev == (unsigned)(a.n_mt - 1);
+          if (s_last) __threadfence();
+        }
+        epi_bar();
+        if (s_last) {  // every tile's maxima are in: the argmax, and reset
+          for (int r = threadIdx.x - TC_EPI_WARP0 * 32; r < a.Npad; r += 128) {
+            const unsigned long long k = __ldcg(&a.amax_key[r]);
+            if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = (int)(~(uint32_t)k);
+            a.amax_key[r] = 0ull;
+          }
+          if (threadIdx.x == TC_EPI_WARP0 * 32) a.tickets[a.n_mt] = 0u;
+        }
+      }
+    }
+  }
+  // ---- every copy and MMA this CTA issued has landed (the producers' last
+  // ---- copies are consumed or drained): free the tensor memory
+  if ((warp == 0 || warp == 1) && lane == 0 && *abort_flag) {
+    // the last copy issued into each ring slot has landed (bounded): the
+    // phase it completes is (uses of the slot - 1)
+    const int depth = warp == 0 ? RAWN : ST;
+    for (int q = 0; q < depth && q < issued; q++) {
+      const int uses = (issued - 1 - q) / depth + 1;
+      mbar_wait(warp == 0 ? RAW_FULL(q) : B_FULL(q), (uses - 1) & 1, LIN_WAIT_TRIES);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(a.tmem_cols)
+                 : "memory");
+  }
+}
+
+using TcKernel = void (*)(const CUtensorMap, const TcArgs);
+TcKernel tc_kernel_for(int qtype) {
+  if (qtype == 4) return tc_linear_kernel<4>;
+  if (qtype == 6) return tc_linear_kernel<6>;
+  if (qtype == 8) return tc_linear_kernel<8>;
+  return nullptr;
+}
+
+int tc_rec_bytes(int qtype) {
+  return qtype == 4 ? TcRec<4>::BYTES : (qtype == 6 ? TcRec<6>::BYTES : TcRec<8>::BYTES);
+}
+
+constexpr int TC_SMEM_MAX = 227 * 1024 - 10 * 1024;  // dynamic part (the static part is ~9 KB)
+
+// Stages of a launch: A/B stages and raw-ring depth that fit the shared memory.
+void tc_stages(int qtype, int Npad, int* st, int* raw) {
+  const int raw_bytes = 4 * tc_rec_bytes(qtype);
+  int s = TC_MAX_ST;
+  for (; s > 2; s--)
+    if (1024 + s * (TC_A_BYTES + Npad * 128) + 3 * raw_bytes <= TC_SMEM_MAX) break;
+  const int left = TC_SMEM_MAX - 1024 - s * (TC_A_BYTES + Npad * 128);
+  *st = s;
+  *raw = std::max(2, std::min(TC_MAX_RAW, left / raw_bytes));
+}
+size_t tc_smem_bytes(int qtype, int Npad, int st, int raw) {
+  return 1024 + (size_t)st * (TC_A_BYTES + Npad * 128) + (size_t)raw * 4 * tc_rec_bytes(qtype);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+}  // namespace
+
+int tc_npad(int R) { return std::max(16, (R + 15) / 16 * 16); }
+int tc_mtiles(const QMat& w) { return (w.N + TC_M - 1) / TC_M; }
+
+// K segments of a matrix for the tensor-core GEMM: the fewest waves of
+// one-CTA-per-SM launches, each CTA's chunk count, plus a small cost per
+// extra segment (its partial written and read back).
+int tc_choose_split(int N, int nch, int sms) {
+  const int n_mt = (N + TC_M - 1) / TC_M;
+  int best = 1;
+  double best_t = 1e30;
+  for (int S = 1; S <= 8 && S <= nch; S++) {
+    const double waves = std::ceil((double)n_mt * S / std::max(sms, 1));
+    const double t = waves * std::ceil((double)nch / S) + (S > 1 ? 2.0 * S : 0.0);
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = S;
+    }
+  }
+  return best;
+}
+
+size_t tc_part_floats(const QMat& w, int R) {
+  return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, 256)) * TC_M : 0;
+}
+size_t tc_tickets_needed(const QMat& w) { return (size_t)tc_mtiles(w) + 1; }
+
+static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& epi,
+                           const LinScratch& scr, cudaStream_t st) {
+  if (R < 1 || R > 256) return fail(SPEC_E_SHAPE, "tensor-core GEMM: 1 <= rows <= 256 per launch");
+  if (scr.err == nullptr) return fail(SPEC_E_INVALID, "tensor-core GEMM: no error word");
+  if (tc_part_floats(w, R) > scr.part_floats || tc_tickets_needed(w) > scr.n_tickets ||
+      (epi.kind == EPI_LMHEAD && scr.amax_keys == nullptr))
+    return fail(SPEC_E_SHAPE, "tensor-core GEMM: scratch too small for this R");
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || w.K % 8 != 0)
+    return fail(SPEC_E_SHAPE, "tensor-core GEMM: x must be 16-byte aligned");
+  auto enc = encode_fn();
+  if (enc == nullptr) return fail(SPEC_E_CUDA, "cuTensorMapEncodeTiled is not available");
+  const int Npad = tc_npad(R);
+  // the activations x [R][K] fp16: box of 64 k x Npad rows, 128-byte swizzle;
+  // rows past R are out of the tensor and read as zero
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {(cuuint64_t)w.K, (cuuint64_t)R};
+  const cuuint64_t gstride[1] = {(cuuint64_t)w.K * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)Npad};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult cr = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(x), gdim,
+                          gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(SPEC_E_CUDA, "cuTensorMapEncodeTiled failed: " + std::to_string((int)cr));
+  TcArgs a;
+  a.rec = w.rec;
+  a.N = w.N;
+  a.K = w.K;
+  a.nch = w.nch;
+  a.n_pairs = w.n_pairs;
+  a.n_mt = tc_mtiles(w);
+  a.S = w.tc_S;
+  a.R = R;
+  a.Npad = Npad;
+  a.tmem_cols = Npad <= 32 ? 32 : (Npad <= 64 ? 64 : (Npad <= 128 ? 128 : 256));
+  tc_stages(w.qtype, Npad, &a.stages, &a.raw_depth);
+  a.epi = epi;
+  a.part = scr.part;
+  a.tickets = scr.tickets;
+  a.amax_key = scr.amax_keys;
+  a.err = scr.err;
+  a.wait_tries = scr.wait_tries > 0 ? LIN_WAIT_TRIES : 0;
+  const TcKernel k = tc_kernel_for(w.qtype);
+  if (k == nullptr) return fail(SPEC_E_INVALID, "tensor-core GEMM: no kernel for this format");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_mt, a.S);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.stages, a.raw_depth);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k, map, a);
+  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("tensor-core GEMM launch: ") + cudaGetErrorString(e));
+  return SPEC_OK;
+}
+
+// Rows in blocks of at most 256 (one accumulator of 256 columns); every row
+// is computed by the same instructions whichever block it falls in.
+int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
+                     const LinScratch& scr, cudaStream_t st) {
+  if (R < 1) return fail(SPEC_E_SHAPE, "tensor-core GEMM: R must be >= 1");
+  for (int r0 = 0; r0 < R; r0 += 256) {
+    LinEpi e = epi;
+    const size_t o = (size_t)r0;
+    switch (epi.kind) {
+      case EPI_STORE:
+      case EPI_RESID:
+        e.y = epi.y + o * epi.ldy;
+        break;
+      case EPI_SWIGLU:
+        e.out16 = epi.out16 + o * epi.ldo;
+        break;
+      case EPI_QKV:
+        e.out16 = epi.out16 + o * epi.nq * epi.hd;
+        e.rows = epi.rows + o;
+        break;
+      case EPI_LMHEAD:
+        if (epi.y != nullptr) e.y = epi.y + o * epi.ldy;
+        if (epi.argmax != nullptr) e.argmax = epi.argmax + o;
+        break;
+    }
+    const int rc = tc_launch_block(w, x + o * w.K, std::min(256, R - r0), e, scr, st);
+    if (rc != SPEC_OK) return rc;
+  }
+  return SPEC_OK;
+}
+
+void tc_init_attrs() {
+  for (int qt : {4, 6, 8})
+    cudaFuncSetAttribute(tc_kernel_for(qt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         TC_SMEM_MAX);
+}

@@ -585,8 +585,17 @@ def test_decoder14b_noisy_target_drafter_round(orc, dev):
     tokens = np.concatenate([anchors[:, None], draft], 1).astype(np.int32)
     ref = om.forward(tokens, [ctx] * n_seq, kc.copy(), vc.copy())
     err = rel_err(lg, ref)
-    print(f"14B-shape 2-layer slice, 192 rows: max |dlogit|/(1+|ref|) = {err:.3e}; "
-          f"accepted per sequence {n_acc.tolist()}")
+    per_seq = [rel_err(lg[s * (d + 1):(s + 1) * (d + 1)], ref[s * (d + 1):(s + 1) * (d + 1)])
+               for s in range(n_seq)]
+    print(f"14B-shape 2-layer slice, 192 rows: max |dlogit|/(1+|ref|) = {err:.3e}; per sequence "
+          f"{[f'{e:.1e}' for e in per_seq]}; accepted per sequence {n_acc.tolist()}")
+    if err > LOGIT_RTOL:
+        s = int(np.argmax(per_seq))
+        rows = lg[s * (d + 1):(s + 1) * (d + 1)]
+        ref1 = om.forward(tokens[s:s + 1], [ctx], np.ascontiguousarray(kc[:, s:s + 1]),
+                          np.ascontiguousarray(vc[:, s:s + 1]))
+        print("worst sequence", s, "per row", [f"{rel_err(rows[i], ref1[i]):.1e}" for i in range(d + 1)],
+              "oracle batched vs alone", f"{rel_err(ref[s * (d + 1):(s + 1) * (d + 1)], ref1):.1e}")
     assert err <= LOGIT_RTOL
     n_r, em_r, ei_r = orc.accept_stochastic(lg.reshape(n_seq, d + 1, V), q, draft, T, seed, slots,
                                             ei0)
