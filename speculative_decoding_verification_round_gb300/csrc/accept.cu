@@ -244,13 +244,18 @@ __global__ void decide_kernel(const float* __restrict__ p, const float* __restri
 }
 
 // ---------------------------------------------------------------------------
-// stochastic, step 3: resample one row per sequence.  One CTA per sequence:
-// per-warp sums of the masses over contiguous ranges (exact 128-bit integer
-// sums, order-free), a prefix over warps to find the range holding the
-// threshold, then one warp scans that range with a 128-bit warp prefix.
+// stochastic, step 3: resample one row per sequence.  One cluster of RS_CL
+// CTAs per sequence cuts the row into RS_CL x RS_WARPS warp ranges; each warp
+// sums the exact 128-bit masses of its range (order-free integers); rank 0
+// reads every range sum through distributed shared memory, draws the
+// threshold and finds the range that holds it; the CTA owning that range
+// cuts it into RS_WARPS sub-ranges the same way, and the warp owning the
+// right one scans it with a 128-bit warp prefix.
 // ---------------------------------------------------------------------------
-constexpr int RS_THREADS = 1024;
+constexpr int RS_CL = 8;
+constexpr int RS_THREADS = 512;
 constexpr int RS_WARPS = RS_THREADS / 32;
+constexpr int RS_RANGES = RS_CL * RS_WARPS;
 
 __device__ __forceinline__ u128 shfl_u128(u128 v, int src) {
   uint64_t lo = (uint64_t)v, hi = (uint64_t)(v >> 64);
@@ -275,16 +280,29 @@ __device__ __forceinline__ u128 mass_of(int mode, const float* prow, const float
   return a > b ? a - b : (u128)0;
 }
 
+// The sum of the masses of [v0, v1) over one warp (every lane gets it).
+__device__ __forceinline__ u128 warp_mass(int mode, const float* prow, const float* qrow, int v0,
+                                          int v1, float T, float mp, float mq, uint64_t S,
+                                          uint64_t Sq, int lane) {
+  u128 acc = 0;
+  for (int v = v0 + lane; v < v1; v += 32) acc += mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += shfl_u128(acc, lane ^ off);
+  return acc;
+}
+
 __global__ void __launch_bounds__(RS_THREADS)
 resample_kernel(const float* __restrict__ p, const float* __restrict__ q, int n_seq, int d,
                 int V, float T, const float* __restrict__ row_max,
                 const unsigned long long* __restrict__ row_sum,
                 const int4* __restrict__ decision, int32_t* __restrict__ em,
                 uint32_t* __restrict__ err) {
-  const int s = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int s = blockIdx.x / RS_CL;
   const int4 dec = decision[s];
   const int mode = dec.w;
-  if (mode == 0) return;
+  if (mode == 0) return;  // every CTA of the cluster returns: nothing syncs
   const int a = dec.x, row = dec.y;
   const uint32_t U2 = (uint32_t)dec.z;
   const int rows_per_seq = 2 * d + 1;
@@ -297,63 +315,92 @@ resample_kernel(const float* __restrict__ p, const float* __restrict__ q, int n_
   const uint64_t S = row_sum[rp];
   const uint64_t Sq = mode == 1 ? row_sum[rq] : 0ull;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int span = (V + RS_WARPS - 1) / RS_WARPS;
-  const int v0 = warp * span, v1 = min(V, v0 + span);
-  u128 acc = 0;
-  for (int v = v0 + lane; v < v1; v += 32) acc += mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += shfl_u128(acc, lane ^ off);
   __shared__ u128 s_w[RS_WARPS];
-  __shared__ int s_pick;
-  if (lane == 0) s_w[warp] = acc;
-  if (threadIdx.x == 0) s_pick = -1;
-  __syncthreads();
-  if (warp == 0) {
-    // total, threshold, and the warp range that holds it (lane 0 serially)
-    if (lane == 0) {
+  __shared__ u128 s_rem;
+  __shared__ int s_range;
+  const int span = (V + RS_RANGES - 1) / RS_RANGES;
+  {
+    const int wr = rank * RS_WARPS + warp;
+    const int v0 = min(V, wr * span), v1 = min(V, v0 + span);
+    const u128 m = warp_mass(mode, prow, qrow, v0, v1, T, mp, mq, S, Sq, lane);
+    if (lane == 0) s_w[warp] = m;
+  }
+  cluster.sync();
+  if (rank == 0) {
+    // every range sum into rank 0's shared memory (one remote load each, in
+    // parallel), then the total in range order, the threshold and the range
+    // that holds it
+    __shared__ u128 s_all[RS_RANGES];
+    for (int k = threadIdx.x; k < RS_RANGES; k += RS_THREADS)
+      s_all[k] = cluster.map_shared_rank(s_w, k / RS_WARPS)[k % RS_WARPS];
+    __syncthreads();
+    if (threadIdx.x == 0) {
       u128 total = 0;
-      for (int w = 0; w < RS_WARPS; w++) total += s_w[w];
+      for (int k = 0; k < RS_RANGES; k++) total += s_all[k];
+      s_range = -1;
       if (total == 0) {
         atomicOr(err, ERR_NONFINITE);
       } else {
         const u128 t = scaled_threshold(U2, total);
         u128 cum = 0;
-        int w = 0;
-        for (; w < RS_WARPS; w++) {
-          if (cum + s_w[w] > t) break;
-          cum += s_w[w];
+        for (int k = 0; k < RS_RANGES; k++) {
+          if (cum + s_all[k] > t) {
+            s_range = k;
+            s_rem = t - cum;
+            break;
+          }
+          cum += s_all[k];
         }
-        // stash (w, t - cum) for the scan warp
-        s_w[0] = t - cum;
-        s_pick = -2 - w;
       }
     }
   }
+  cluster.sync();
+  const int range = *cluster.map_shared_rank(&s_range, 0);
+  const u128 rem0 = *cluster.map_shared_rank(&s_rem, 0);
+  cluster.sync();  // rank 0's shared memory stays until every CTA has read it
+  if (range < 0 || rank != range / RS_WARPS) return;
+  // the owning CTA: the range cut into RS_WARPS sub-ranges
+  const int u0 = min(V, range * span), u1 = min(V, u0 + span);
+  const int sspan = (u1 - u0 + RS_WARPS - 1) / RS_WARPS;
+  const int w0 = min(u1, u0 + warp * sspan), w1 = min(u1, w0 + sspan);
+  const u128 sub = warp_mass(mode, prow, qrow, w0, w1, T, mp, mq, S, Sq, lane);
+  __syncthreads();  // s_w is reused
+  if (lane == 0) s_w[warp] = sub;
   __syncthreads();
-  if (s_pick == -1) return;
-  const int w = -2 - s_pick;
-  const u128 rem = s_w[0];  // threshold relative to the start of warp w's range
+  __shared__ int s_sub;
+  __shared__ u128 s_rem2;
+  if (threadIdx.x == 0) {
+    u128 cum = 0;
+    s_sub = RS_WARPS - 1;
+    s_rem2 = 0;
+    for (int k = 0; k < RS_WARPS; k++) {
+      if (cum + s_w[k] > rem0) {
+        s_sub = k;
+        s_rem2 = rem0 - cum;
+        break;
+      }
+      cum += s_w[k];
+    }
+  }
   __syncthreads();
-  if (warp == 0) {
-    const int u0 = w * span, u1 = min(V, u0 + span);
-    u128 base = 0;
-    int found = -1;
-    for (int vb = u0; vb < u1 && found < 0; vb += 32) {
-      const int v = vb + lane;
-      u128 m = v < u1 ? mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq) : (u128)0;
-      // inclusive warp prefix
+  if (warp != s_sub) return;
+  const u128 rem = s_rem2;
+  u128 base = 0;
+  int found = -1;
+  for (int vb = w0; vb < w1 && found < 0; vb += 32) {
+    const int v = vb + lane;
+    u128 m = v < w1 ? mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq) : (u128)0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const u128 o = shfl_up_u128(m, off);
-        if (lane >= off) m += o;
-      }
-      const bool hit = v < u1 && base + m > rem;
-      const unsigned ball = __ballot_sync(0xffffffffu, hit);
-      if (ball) found = vb + __ffs(ball) - 1;
-      base += shfl_u128(m, 31);
+    for (int off = 1; off < 32; off <<= 1) {  // inclusive warp prefix
+      const u128 o = shfl_up_u128(m, off);
+      if (lane >= off) m += o;
     }
-    if (lane == 0) em[(size_t)s * (d + 1) + a] = found;
+    const bool hit = v < w1 && base + m > rem;
+    const unsigned ball = __ballot_sync(0xffffffffu, hit);
+    if (ball) found = vb + __ffs(ball) - 1;
+    base += shfl_u128(m, 31);
   }
+  if (lane == 0) em[(size_t)s * (d + 1) + a] = found;
 }
 
 // Standalone accept: on a device error the outputs read -1 and the sampler
@@ -481,9 +528,15 @@ int launch_accept_stochastic(const float* p, const float* q, const int32_t* draf
   decide_kernel<<<(n_seq + 63) / 64, 64, 0, st>>>(p, q, draft, n_seq, d, V, T, seed, seq_ids,
                                                   emit_idx, emit_by_slot, n_slots, scr.row_max, scr.row_sum,
                                                   scr.decision, n_acc, emitted, err);
-  resample_kernel<<<n_seq, RS_THREADS, 0, st>>>(p, q, n_seq, d, V, T, scr.row_max, scr.row_sum,
-                                                scr.decision, emitted, err);
   e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("stochastic accept: ") + cudaGetErrorString(e));
+  cfg.gridDim = dim3((unsigned)(n_seq * RS_CL));
+  cfg.blockDim = dim3(RS_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  attr[0].val.clusterDim.x = RS_CL;
+  e = cudaLaunchKernelEx(&cfg, resample_kernel, p, q, n_seq, d, V, T, (const float*)scr.row_max,
+                         (const unsigned long long*)scr.row_sum, (const int4*)scr.decision, emitted,
+                         err);
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("stochastic accept: ") + cudaGetErrorString(e));
   return SPEC_OK;
 }

@@ -549,8 +549,10 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         uint32_t v[32];
         tc_ld32(tmem + ((uint32_t)(32 * quad) << 16) + col0, v);
         float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * TC_M + m;
+        // Npad is a multiple of 16: the last group of 32 may be half outside
 #pragma unroll
-        for (int c = 0; c < 32; c++) dst[(size_t)c * TC_M] = __uint_as_float(v[c]);
+        for (int c = 0; c < 32; c++)
+          if (col0 + c < a.Npad) dst[(size_t)c * TC_M] = __uint_as_float(v[c]);
       }
       epi_bar();
       if (threadIdx.x == TC_EPI_WARP0 * 32) {
@@ -569,10 +571,12 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           const float* src = a.part + ((size_t)mt * a.Npad + col0) * TC_M + m;
           const size_t step = (size_t)a.n_mt * a.Npad * TC_M;
 #pragma unroll
-          for (int c = 0; c < 32; c++) v[c] = __ldcg(src + (size_t)c * TC_M);
+          for (int c = 0; c < 32; c++)
+            v[c] = col0 + c < a.Npad ? __ldcg(src + (size_t)c * TC_M) : 0.0f;
           for (int s2 = 1; s2 < a.S; s2++)
 #pragma unroll
-            for (int c = 0; c < 32; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_M);
+            for (int c = 0; c < 32; c++)
+              if (col0 + c < a.Npad) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_M);
         } else {
           uint32_t u[32];
           tc_ld32(tmem + ((uint32_t)(32 * quad) << 16) + col0, u);
