@@ -13,11 +13,14 @@
 //   * warp 0 streams the packed weight records into a shared-memory ring with
 //     TMA bulk copies; warp 1 loads the activation tile of each 64-k chunk
 //     with a 2-D TMA tensor copy (128-byte swizzle, rows past R read as zero);
-//   * warps 3-6 dequantise each chunk into an fp16 A tile in the UMMA
-//     K-major 128-byte-swizzle layout: w = fp16(q * scale), one rounding (the
-//     block integers are exact in fp16, the product is rounded once);
-//   * one thread of warp 2 issues four tcgen05.mma (M 128, N Npad, K 16) per
-//     chunk and commits them to the stage's "empty" barrier;
+//   * warps 3-6 dequantise each chunk into TWO fp16 A tiles in the UMMA
+//     K-major 128-byte-swizzle layout, hi = fp16(q * scale) and lo =
+//     fp16(q * scale - hi): q * scale has at most 11 + 8 significant bits,
+//     so lo holds the rest exactly and hi + lo IS the weight -- every
+//     product the tensor core forms is exact, as in the oracle;
+//   * one thread of warp 2 issues eight tcgen05.mma (M 128, N Npad, K 16:
+//     hi and lo for each 16-k step) per chunk into the one accumulator and
+//     commits them to the stage's "empty" barrier;
 //   * after the last chunk the same four warps read the accumulator back
 //     (tcgen05.ld), add the K segments in segment order (the last CTA of a
 //     tile, by a ticket) and run the fused epilogue (store, residual add,
@@ -44,7 +47,7 @@ namespace {
 constexpr int TC_M = 128;           // weight rows of a CTA
 constexpr int TC_THREADS = 224;     // 7 warps
 constexpr int TC_EPI_WARP0 = 3;     // warps 3..6: dequant, then epilogue
-constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16
+constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16 (one of hi / lo)
 constexpr int TC_MAX_ST = 4;
 constexpr int TC_MAX_RAW = 8;
 
@@ -175,13 +178,13 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int u) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
 }
 
-// fp16 weights of one k16 step's word for rows g and g+8 (4 + 4 values):
-// the integers u are placed in the low bits of each half, made 1024 + u by
-// the fp16 exponent of 1024, then (1024 + u) - (1024 + bias) = q exactly and
-// q * scale rounded once.  lo/hi: k pairs (0,1) and (2,3) of each row.
+// The integers of one k16 step's word for rows g and g+8 (4 + 4 values) as
+// exact fp16: each u is placed in the low bits of a half, made 1024 + u by
+// the fp16 exponent of 1024, then (1024 + u) - (1024 + bias) = q exactly.
+// [0]/[1]: k pairs (0,1) and (2,3) of each row.
 template <int QT>
-__device__ __forceinline__ void dq_word(uint32_t w, uint32_t hx, __half2 sg, __half2 sg8,
-                                        __half2 (&rg)[2], __half2 (&rg8)[2]) {
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t hx, __half2 (&rg)[2],
+                                        __half2 (&rg8)[2]) {
   constexpr uint32_t MAGIC = 0x64006400u;
   const __half2 off = QT == 4 ? __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408))
                               : __halves2half2(__ushort_as_half(0x6420), __ushort_as_half(0x6420));
@@ -198,20 +201,29 @@ __device__ __forceinline__ void dq_word(uint32_t w, uint32_t hx, __half2 sg, __h
     u[2] = ((w >> 4) & 0x000F000Fu) | ((hx >> 4) & 0x00300030u) | MAGIC;
     u[3] = ((w8 >> 4) & 0x000F000Fu) | ((hx2 >> 4) & 0x00300030u) | MAGIC;
   }
-  rg[0] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[0]), off), sg);
-  rg[1] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[1]), off), sg);
-  rg8[0] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[2]), off), sg8);
-  rg8[1] = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&u[3]), off), sg8);
+  rg[0] = __hsub2(*reinterpret_cast<const __half2*>(&u[0]), off);
+  rg[1] = __hsub2(*reinterpret_cast<const __half2*>(&u[1]), off);
+  rg8[0] = __hsub2(*reinterpret_cast<const __half2*>(&u[2]), off);
+  rg8[1] = __hsub2(*reinterpret_cast<const __half2*>(&u[3]), off);
 }
 
 // Q8: one word holds u = q + 128 of rows r, r, r', r' at k, k+1.
-__device__ __forceinline__ void dq_word8(uint32_t w, __half2 sg, __half2 sg8, __half2& rg,
-                                         __half2& rg8) {
+__device__ __forceinline__ void dq_word8(uint32_t w, __half2& rg, __half2& rg8) {
   const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
   const uint32_t a = __byte_perm(w, 0x64646464u, 0x4140);
   const uint32_t b = __byte_perm(w, 0x64646464u, 0x4342);
-  rg = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&a), off), sg);
-  rg8 = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&b), off), sg8);
+  rg = __hsub2(*reinterpret_cast<const __half2*>(&a), off);
+  rg8 = __hsub2(*reinterpret_cast<const __half2*>(&b), off);
+}
+
+// w = q * s as an exact pair: hi = fp16(q * s), lo = fp16(q * s - hi).  q is
+// an integer of at most 8 bits and s has 11, so q * s has at most 19
+// significant bits and a multiple of s's last place; hi takes the leading
+// 11 (rounded), and the remainder q * s - hi has at most 8 and is a multiple
+// of 2^-24 or coarser: the fused multiply-add rounds nothing.
+__device__ __forceinline__ void split2(__half2 q, __half2 s, __half2& hi, __half2& lo) {
+  hi = __hmul2(q, s);
+  lo = __hfma2(q, s, __hneg2(hi));
 }
 
 __device__ __forceinline__ uint4 pack4(__half2 a, __half2 b, __half2 c, __half2 d) {
@@ -233,10 +245,11 @@ __device__ __forceinline__ void epi_bar() {  // the four epilogue warps
 // The dequant of one 64-k chunk of one pair (two 16-row tiles) by one lane:
 // lane unit (g, t) holds rows g and g+8 of each tile at k = 32b + 8t .. +7.
 // The lane -> (g, t) map makes both the record loads and the swizzled
-// stores of every 8-lane phase hit 8 distinct bank groups.
+// stores of every 8-lane phase hit 8 distinct bank groups.  Each weight goes
+// to the hi tile and its exact remainder to the lo tile.
 template <int QT>
-__device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned char* atile,
-                                              int pair_in_cta, int lane) {
+__device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned char* ahi,
+                                              unsigned char* alo, int pair_in_cta, int lane) {
   using RC = TcRec<QT>;
   const int ph = lane >> 3, j = lane & 7;
   const int p = j & 1, t0 = (j >> 1) & 1, t1 = j >> 2;
@@ -248,21 +261,17 @@ __device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned
     const __half2 s0 = *reinterpret_cast<const __half2*>(&sw.x);  // (row g, row g+8), block 0
     const __half2 s1 = *reinterpret_cast<const __half2*>(&sw.y);  // block 1
     const int r0 = 32 * pair_in_cta + 16 * i + g;                 // A-tile row of row g
-    unsigned char* row_g = atile;
 #pragma unroll
     for (int b = 0; b < 2; b++) {
       const __half2 sg = b == 0 ? __low2half2(s0) : __low2half2(s1);
       const __half2 sg8 = b == 0 ? __high2half2(s0) : __high2half2(s1);
-      uint4 vg, vg8;
+      __half2 qg[4], qg8[4];  // exact integers, k pairs (0,1) .. (6,7)
       if constexpr (QT == 8) {
         const uint4 q = *reinterpret_cast<const uint4*>(raw + i * RC::QS_TILE + l * 32 + b * 16);
-        __half2 a[4], c[4];
-        dq_word8(q.x, sg, sg8, a[0], c[0]);
-        dq_word8(q.y, sg, sg8, a[1], c[1]);
-        dq_word8(q.z, sg, sg8, a[2], c[2]);
-        dq_word8(q.w, sg, sg8, a[3], c[3]);
-        vg = pack4(a[0], a[1], a[2], a[3]);
-        vg8 = pack4(c[0], c[1], c[2], c[3]);
+        dq_word8(q.x, qg[0], qg8[0]);
+        dq_word8(q.y, qg[1], qg8[1]);
+        dq_word8(q.z, qg[2], qg8[2]);
+        dq_word8(q.w, qg[3], qg8[3]);
       } else {
         const uint4 q = *reinterpret_cast<const uint4*>(raw + i * RC::QS_TILE + l * 16);
         uint32_t hA = 0, hB = 0;
@@ -273,14 +282,23 @@ __device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned
         }
         const uint32_t w0 = b == 0 ? q.x : q.z, w1 = b == 0 ? q.y : q.w;
         __half2 a0[2], c0[2], a1[2], c1[2];
-        dq_word<QT>(w0, hA, sg, sg8, a0, c0);  // k 0..3
-        dq_word<QT>(w1, hB, sg, sg8, a1, c1);  // k 4..7
-        vg = pack4(a0[0], a0[1], a1[0], a1[1]);
-        vg8 = pack4(c0[0], c0[1], c1[0], c1[1]);
+        dq_word<QT>(w0, hA, a0, c0);  // k 0..3
+        dq_word<QT>(w1, hB, a1, c1);  // k 4..7
+        qg[0] = a0[0]; qg[1] = a0[1]; qg[2] = a1[0]; qg[3] = a1[1];
+        qg8[0] = c0[0]; qg8[1] = c0[1]; qg8[2] = c1[0]; qg8[3] = c1[1];
+      }
+      __half2 hg[4], lg[4], hg8[4], lg8[4];
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        split2(qg[e], sg, hg[e], lg[e]);
+        split2(qg8[e], sg8, hg8[e], lg8[e]);
       }
       const int u = 4 * b + t;
-      *reinterpret_cast<uint4*>(row_g + sw128_off(r0, u)) = vg;
-      *reinterpret_cast<uint4*>(row_g + sw128_off(r0 + 8, u)) = vg8;
+      const uint32_t og = sw128_off(r0, u), og8 = sw128_off(r0 + 8, u);
+      *reinterpret_cast<uint4*>(ahi + og) = pack4(hg[0], hg[1], hg[2], hg[3]);
+      *reinterpret_cast<uint4*>(ahi + og8) = pack4(hg8[0], hg8[1], hg8[2], hg8[3]);
+      *reinterpret_cast<uint4*>(alo + og) = pack4(lg[0], lg[1], lg[2], lg[3]);
+      *reinterpret_cast<uint4*>(alo + og8) = pack4(lg8[0], lg8[1], lg8[2], lg8[3]);
     }
   }
 }
@@ -393,8 +411,8 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   const int mt = blockIdx.x, seg = blockIdx.y;
   const int ST = a.stages, RAWN = a.raw_depth;
   const int B_BYTES = a.Npad * 128;
-  unsigned char* A0 = smem;
-  unsigned char* B0 = smem + ST * TC_A_BYTES;
+  unsigned char* A0 = smem;  // [ST][hi, lo] tiles
+  unsigned char* B0 = smem + ST * 2 * TC_A_BYTES;
   unsigned char* RAW0 = B0 + ST * B_BYTES;
   const int RAW_BYTES = 4 * RC::BYTES;
   // barriers: a_full[ST], b_full[ST], empty[ST], (spare)[ST], raw_full[RAW], raw_empty[RAW], acc
@@ -494,11 +512,14 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           break;
         }
         tc_fence_after();
-        const uint64_t ad = smem_desc_sw128(smem_u32(A0 + s * TC_A_BYTES));
+        const uint64_t ah = smem_desc_sw128(smem_u32(A0 + s * 2 * TC_A_BYTES));
+        const uint64_t al = smem_desc_sw128(smem_u32(A0 + (s * 2 + 1) * TC_A_BYTES));
         const uint64_t bd = smem_desc_sw128(smem_u32(B0 + s * B_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++)  // 16 k (32 bytes) per instruction
-          tc_mma(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
+          tc_mma(tmem, ah + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          tc_mma(tmem, al + 2 * kk, bd + 2 * kk, idesc, 1u);
+        }
         tc_commit(EMPTY(s));
       }
       tc_commit(ACC);  // completes when every MMA issued above has
@@ -516,13 +537,14 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         give_up();
         break;
       }
-      unsigned char* at = A0 + s * TC_A_BYTES;
+      unsigned char* at = A0 + s * 2 * TC_A_BYTES;
       if (pair0 + pc < a.n_pairs) {
-        dequant_chunk<QT>(RAW0 + r * RAW_BYTES + pc * RC::BYTES, at, pc, lane);
+        dequant_chunk<QT>(RAW0 + r * RAW_BYTES + pc * RC::BYTES, at, at + TC_A_BYTES, pc, lane);
       } else {  // rows past the matrix: zeros
-        for (int q = lane; q < 32 * 8 / 1; q += 32) {
+        for (int q = lane; q < 32 * 8; q += 32) {
           const int rr = 32 * pc + q / 8, u = q % 8;
           *reinterpret_cast<uint4*>(at + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(at + TC_A_BYTES + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
         }
       }
       mbar_arrive(RAW_EMPTY(r));
@@ -661,13 +683,13 @@ void tc_stages(int qtype, int Npad, int* st, int* raw) {
   const int raw_bytes = 4 * tc_rec_bytes(qtype);
   int s = TC_MAX_ST;
   for (; s > 2; s--)
-    if (1024 + s * (TC_A_BYTES + Npad * 128) + 3 * raw_bytes <= TC_SMEM_MAX) break;
-  const int left = TC_SMEM_MAX - 1024 - s * (TC_A_BYTES + Npad * 128);
+    if (1024 + s * (2 * TC_A_BYTES + Npad * 128) + 3 * raw_bytes <= TC_SMEM_MAX) break;
+  const int left = TC_SMEM_MAX - 1024 - s * (2 * TC_A_BYTES + Npad * 128);
   *st = s;
   *raw = std::max(2, std::min(TC_MAX_RAW, left / raw_bytes));
 }
 size_t tc_smem_bytes(int qtype, int Npad, int st, int raw) {
-  return 1024 + (size_t)st * (TC_A_BYTES + Npad * 128) + (size_t)raw * 4 * tc_rec_bytes(qtype);
+  return 1024 + (size_t)st * (2 * TC_A_BYTES + Npad * 128) + (size_t)raw * 4 * tc_rec_bytes(qtype);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
