@@ -1160,9 +1160,10 @@ def run_ours(args):
 # --------------------------------------------------------------------------
 # profiling drivers (no JSON line)
 # --------------------------------------------------------------------------
-def linear_only(spec: str, nt: int = 8, reps: int = 3):
-    """spec_linear_q at nt on packed synthetic matrices, `spec` =
-    'QT:N:K,QT:N:K,...', each launched `reps` times."""
+def linear_only(spec: str, nt: int = 8, reps: int = 3, tc: bool = False):
+    """spec_linear_q (or, with tc, spec_linear_q_tc) at nt rows on packed
+    synthetic matrices, `spec` = 'QT:N:K,QT:N:K,...', each launched `reps`
+    times."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
     from speculative_decoding_verification_round_gb300 import synth
@@ -1175,8 +1176,9 @@ def linear_only(spec: str, nt: int = 8, reps: int = 3):
         x = synth.f16_normal_torch(gen, (nt, K), dev).view(torch.int16)
         y = torch.empty((nt, N), dtype=torch.float32, device=dev)
         for _ in range(reps):
-            sv.spec_linear_q(qm, x, nt, y)
+            (sv.spec_linear_q_tc if tc else sv.spec_linear_q)(qm, x, nt, y)
         torch.cuda.synchronize()
+        assert sv.spec_error_check(None) == 0
         qm.close()
         del w
     print("linear-only ok")
@@ -1258,13 +1260,15 @@ def main():
     ap.add_argument("--linear-only", default=None,
                     help="profiling driver: QT:N:K[,QT:N:K...] verify-GEMM launches only")
     ap.add_argument("--linear-rows", type=int, default=8, help="rows of --linear-only")
+    ap.add_argument("--linear-tc", action="store_true",
+                    help="--linear-only on the tensor-core GEMM of multi-sequence rounds")
     ap.add_argument("--round-only", type=int, default=None, metavar="LAYERS",
                     help="profiling driver: stochastic rounds of the batched workload")
     ap.add_argument("--draft-only", type=int, default=None, metavar="LAYERS",
                     help="profiling driver: nt = 1 forwards of the 0.5B-class draft")
     args = ap.parse_args()
     if args.linear_only:
-        linear_only(args.linear_only, nt=args.linear_rows)
+        linear_only(args.linear_only, nt=args.linear_rows, tc=args.linear_tc)
         return
     if args.round_only:
         round_only(args.round_only)

@@ -311,16 +311,21 @@ __device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, 
   const bool real = n < a.N;
   switch (e.kind) {
     case EPI_STORE:
-    case EPI_RESID:
 #pragma unroll
-      for (int c = 0; c < 32; c++) {
-        const int r = col0 + c;
-        if (real && r < a.R) {
-          float* p = e.y + (size_t)r * e.ldy + n;
-          *p = e.kind == EPI_RESID ? *p + v[c] : v[c];
-        }
-      }
+      for (int c = 0; c < 32; c++)
+        if (real && col0 + c < a.R) e.y[(size_t)(col0 + c) * e.ldy + n] = v[c];
       break;
+    case EPI_RESID: {
+      // the 32 old values in one batch of loads, then the stores
+      float old[32];
+#pragma unroll
+      for (int c = 0; c < 32; c++)
+        old[c] = real && col0 + c < a.R ? e.y[(size_t)(col0 + c) * e.ldy + n] : 0.0f;
+#pragma unroll
+      for (int c = 0; c < 32; c++)
+        if (real && col0 + c < a.R) e.y[(size_t)(col0 + c) * e.ldy + n] = old[c] + v[c];
+      break;
+    }
     case EPI_SWIGLU: {
       // rows g (gate j) and g+8 (up j) of each 16-row tile are lanes l, l+8
       const int g = n & 15, T = n >> 4;
@@ -342,17 +347,30 @@ __device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, 
       const int hh = T / per_head, jj = T % per_head;
       const int i0 = 8 * jj + (g & 7), i1 = e.hd / 2 + 8 * jj + (g & 7);
       const bool rope = e.rope != nullptr && hh < e.nq + e.nkv;
+      // the columns' (slot, position) records and RoPE factors in one batch
+      // of loads before any is used
+      RowInfo ri_c[32];
+      float2 cs_c[32];
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const int r = min(col0 + c, a.R - 1);
+        ri_c[c] = e.rows[r];
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c++) {
+        const int rp = ri_c[c].pos < e.max_ctx ? ri_c[c].pos : e.max_ctx - 1;
+        cs_c[c] = rope ? e.rope[(size_t)max(rp, 0) * (e.hd / 2) + i0] : make_float2(1.0f, 0.0f);
+      }
 #pragma unroll
       for (int c = 0; c < 32; c++) {
         const float x1 = __shfl_xor_sync(0xffffffffu, v[c], 8);
         const int r = col0 + c;
         if (g >= 8 || !real || r >= a.R) continue;
         const float x0 = v[c];
-        const RowInfo ri = e.rows[r];
+        const RowInfo ri = ri_c[c];
         float y0 = x0, y1 = x1;
         if (rope) {
-          const int rp = ri.pos < e.max_ctx ? ri.pos : e.max_ctx - 1;
-          const float2 cs = e.rope[(size_t)max(rp, 0) * (e.hd / 2) + i0];
+          const float2 cs = cs_c[c];
           y0 = fmaf(x0, cs.x, -x1 * cs.y);
           y1 = fmaf(x1, cs.x, x0 * cs.y);
         }

