@@ -48,7 +48,7 @@ constexpr int TC_M = 128;           // weight rows of a CTA
 constexpr int TC_THREADS = 224;     // 7 warps
 constexpr int TC_EPI_WARP0 = 3;     // warps 3..6: dequant, then epilogue
 constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16 (one of hi / lo)
-constexpr int TC_MAX_ST = 4;
+constexpr int TC_MAX_ST = 6;    // stages of either ring (A: hi + lo tiles; B: activation tiles)
 constexpr int TC_MAX_RAW = 8;
 
 template <int QT>
@@ -61,7 +61,8 @@ struct TcRec {  // the packed record of one (pair, 64-k chunk): see linear.cu
 
 struct TcArgs {
   const uint8_t* rec;  // [n_pairs][nch][rec]
-  int N, K, nch, n_pairs, n_mt, S, R, Npad, tmem_cols, stages, raw_depth;
+  int N, K, nch, n_pairs, n_mt, S, R, Npad, tmem_cols;
+  int a_stages, b_stages, raw_depth;  // ring depths: A (hi + lo), activations, raw records
   LinEpi epi;
   float* part;          // [S][n_mt][Npad][128] K-split partials
   unsigned* tickets;    // [n_mt] K-split tickets, then [1] argmax ticket
@@ -427,17 +428,20 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, seg = blockIdx.y;
-  const int ST = a.stages, RAWN = a.raw_depth;
+  const int STA = a.a_stages, STB = a.b_stages, RAWN = a.raw_depth;
   const int B_BYTES = a.Npad * 128;
-  unsigned char* A0 = smem;  // [ST][hi, lo] tiles
-  unsigned char* B0 = smem + ST * 2 * TC_A_BYTES;
-  unsigned char* RAW0 = B0 + ST * B_BYTES;
+  unsigned char* A0 = smem;  // [STA][hi, lo] tiles
+  unsigned char* B0 = smem + STA * 2 * TC_A_BYTES;
+  unsigned char* RAW0 = B0 + STB * B_BYTES;
   const int RAW_BYTES = 4 * RC::BYTES;
-  // barriers: a_full[ST], b_full[ST], empty[ST], (spare)[ST], raw_full[RAW], raw_empty[RAW], acc
+  // barriers: a_full[STA], b_full[STB], a_empty[STA], b_empty[STB], raw_full[RAW],
+  // raw_empty[RAW], acc.  The two rings are freed separately (one commit
+  // each), so activation tiles are fetched a full ring ahead of their MMAs.
   const uint32_t bar0 = smem_u32(s_bar);
   auto A_FULL = [&](int s) { return bar0 + 8 * s; };
   auto B_FULL = [&](int s) { return bar0 + 8 * (TC_MAX_ST + s); };
-  auto EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_MAX_ST + s); };
+  auto A_EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_MAX_ST + s); };
+  auto B_EMPTY = [&](int s) { return bar0 + 8 * (3 * TC_MAX_ST + s); };
   auto RAW_FULL = [&](int r) { return bar0 + 8 * (4 * TC_MAX_ST + r); };
   auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (4 * TC_MAX_ST + TC_MAX_RAW + r); };
   const uint32_t ACC = bar0 + 8 * (4 * TC_MAX_ST + 2 * TC_MAX_RAW);
@@ -448,10 +452,13 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   const int pair0 = mt * 4;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < ST; s++) {
+    for (int s = 0; s < STA; s++) {
       mbar_init(A_FULL(s), 128);
+      mbar_init(A_EMPTY(s), 1);
+    }
+    for (int s = 0; s < STB; s++) {
       mbar_init(B_FULL(s), 1);
-      mbar_init(EMPTY(s), 1);
+      mbar_init(B_EMPTY(s), 1);
     }
     for (int r = 0; r < RAWN; r++) {
       mbar_init(RAW_FULL(r), 1);
@@ -506,8 +513,8 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     grid_dep_wait();
     if (lane == 0) {
       for (int c = 0; c < nc && !*abort_flag; c++) {
-        const int s = c % ST, us = c / ST;
-        if (us > 0 && !mbar_wait(EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
+        const int s = c % STB, us = c / STB;
+        if (us > 0 && !mbar_wait(B_EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
           give_up();
           break;
         }
@@ -523,22 +530,23 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       const uint32_t idesc = idesc_f16(a.Npad);
       int c = 0;
       for (; c < nc && !*abort_flag; c++) {
-        const int s = c % ST, us = c / ST;
-        if (!mbar_wait(A_FULL(s), us & 1, LIN_WAIT_TRIES, abort_flag) ||
-            !mbar_wait(B_FULL(s), us & 1, LIN_WAIT_TRIES, abort_flag)) {
+        const int sa = c % STA, ua = c / STA, sb = c % STB, ub = c / STB;
+        if (!mbar_wait(A_FULL(sa), ua & 1, LIN_WAIT_TRIES, abort_flag) ||
+            !mbar_wait(B_FULL(sb), ub & 1, LIN_WAIT_TRIES, abort_flag)) {
           give_up();
           break;
         }
         tc_fence_after();
-        const uint64_t ah = smem_desc_sw128(smem_u32(A0 + s * 2 * TC_A_BYTES));
-        const uint64_t al = smem_desc_sw128(smem_u32(A0 + (s * 2 + 1) * TC_A_BYTES));
-        const uint64_t bd = smem_desc_sw128(smem_u32(B0 + s * B_BYTES));
+        const uint64_t ah = smem_desc_sw128(smem_u32(A0 + sa * 2 * TC_A_BYTES));
+        const uint64_t al = smem_desc_sw128(smem_u32(A0 + (sa * 2 + 1) * TC_A_BYTES));
+        const uint64_t bd = smem_desc_sw128(smem_u32(B0 + sb * B_BYTES));
 #pragma unroll
         for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
           tc_mma(tmem, ah + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
           tc_mma(tmem, al + 2 * kk, bd + 2 * kk, idesc, 1u);
         }
-        tc_commit(EMPTY(s));
+        tc_commit(A_EMPTY(sa));
+        tc_commit(B_EMPTY(sb));
       }
       tc_commit(ACC);  // completes when every MMA issued above has
     }
@@ -547,10 +555,10 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     const int pc = warp - TC_EPI_WARP0;
     grid_dep_wait();
     for (int c = 0; c < nc && !*abort_flag; c++) {
-      const int r = c % RAWN, ur = c / RAWN, s = c % ST, us = c / ST;
+      const int r = c % RAWN, ur = c / RAWN, s = c % STA, us = c / STA;
       // the first wait's budget is the one a caller may shorten (test hook)
       bool ok = mbar_wait(RAW_FULL(r), ur & 1, c == 0 ? a.wait_tries : LIN_WAIT_TRIES, abort_flag);
-      if (ok && us > 0) ok = mbar_wait(EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag);
+      if (ok && us > 0) ok = mbar_wait(A_EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag);
       if (!ok) {
         give_up();
         break;
@@ -666,7 +674,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   if ((warp == 0 || warp == 1) && lane == 0 && *abort_flag) {
     // the last copy issued into each ring slot has landed (bounded): the
     // phase it completes is (uses of the slot - 1)
-    const int depth = warp == 0 ? RAWN : ST;
+    const int depth = warp == 0 ? RAWN : STB;
     for (int q = 0; q < depth && q < issued; q++) {
       const int uses = (issued - 1 - q) / depth + 1;
       mbar_wait(warp == 0 ? RAW_FULL(q) : B_FULL(q), (uses - 1) & 1, LIN_WAIT_TRIES);
@@ -696,18 +704,24 @@ int tc_rec_bytes(int qtype) {
 
 constexpr int TC_SMEM_MAX = 227 * 1024 - 10 * 1024;  // dynamic part (the static part is ~9 KB)
 
-// Stages of a launch: A/B stages and raw-ring depth that fit the shared memory.
-void tc_stages(int qtype, int Npad, int* st, int* raw) {
-  const int raw_bytes = 4 * tc_rec_bytes(qtype);
-  int s = TC_MAX_ST;
-  for (; s > 2; s--)
-    if (1024 + s * (2 * TC_A_BYTES + Npad * 128) + 3 * raw_bytes <= TC_SMEM_MAX) break;
-  const int left = TC_SMEM_MAX - 1024 - s * (2 * TC_A_BYTES + Npad * 128);
-  *st = s;
+// Ring depths of a launch that fit the shared memory: the activation ring
+// as deep as possible (it hides the L2 latency of a tile, fetched when the
+// MMAs of the chunk a ring earlier complete), three A stages (the dequant
+// of a chunk overlaps two chunks of MMAs), then the raw-record ring.
+void tc_rings(int qtype, int Npad, int* sta, int* stb, int* raw) {
+  const int raw_bytes = 4 * tc_rec_bytes(qtype), b_bytes = Npad * 128;
+  *sta = 3;
+  *raw = 3;
+  int b = TC_MAX_ST;
+  while (b > 2 && 1024 + 3 * 2 * TC_A_BYTES + b * b_bytes + 3 * raw_bytes > TC_SMEM_MAX) b--;
+  if (1024 + 3 * 2 * TC_A_BYTES + b * b_bytes + 3 * raw_bytes > TC_SMEM_MAX) *sta = 2;
+  *stb = b;
+  const int left = TC_SMEM_MAX - 1024 - *sta * 2 * TC_A_BYTES - b * b_bytes;
   *raw = std::max(2, std::min(TC_MAX_RAW, left / raw_bytes));
 }
-size_t tc_smem_bytes(int qtype, int Npad, int st, int raw) {
-  return 1024 + (size_t)st * (2 * TC_A_BYTES + Npad * 128) + (size_t)raw * 4 * tc_rec_bytes(qtype);
+size_t tc_smem_bytes(int qtype, int Npad, int sta, int stb, int raw) {
+  return 1024 + (size_t)sta * 2 * TC_A_BYTES + (size_t)stb * Npad * 128 +
+         (size_t)raw * 4 * tc_rec_bytes(qtype);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -788,7 +802,7 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   a.R = R;
   a.Npad = Npad;
   a.tmem_cols = Npad <= 32 ? 32 : (Npad <= 64 ? 64 : (Npad <= 128 ? 128 : 256));
-  tc_stages(w.qtype, Npad, &a.stages, &a.raw_depth);
+  tc_rings(w.qtype, Npad, &a.a_stages, &a.b_stages, &a.raw_depth);
   a.epi = epi;
   a.part = scr.part;
   a.tickets = scr.tickets;
@@ -800,7 +814,7 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_mt, a.S);
   cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.stages, a.raw_depth);
+  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.a_stages, a.b_stages, a.raw_depth);
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
