@@ -45,8 +45,10 @@
 namespace {
 
 constexpr int TC_M = 128;           // weight rows of a CTA
-constexpr int TC_THREADS = 224;     // 7 warps
-constexpr int TC_EPI_WARP0 = 3;     // warps 3..6: dequant, then epilogue
+constexpr int TC_THREADS = 352;     // 11 warps
+constexpr int TC_EPI_WARP0 = 3;     // warps 3..10: dequant, then epilogue
+constexpr int TC_EPI_THREADS = 256; // 8 warps: two per TMEM lane quadrant
+constexpr int EW = 16;              // epilogue columns per TMEM load
 constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16 (one of hi / lo)
 constexpr int TC_MAX_ST = 6;    // stages of either ring (A: hi + lo tiles; B: activation tiles)
 constexpr int TC_MAX_RAW = 8;
@@ -160,19 +162,16 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-
 // Byte offset of 16-byte unit u (k = 8u..8u+7) of row r in a K-major
 // 128-byte-swizzled tile of 64-k rows.
 __device__ __forceinline__ uint32_t sw128_off(int r, int u) {
@@ -239,25 +238,24 @@ __device__ __forceinline__ uint32_t f32_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ void epi_bar() {  // the four epilogue warps
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+__device__ __forceinline__ void epi_bar() {  // the eight epilogue warps
+  asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-// The dequant of one 64-k chunk of one pair (two 16-row tiles) by one lane:
+// The dequant of one 64-k chunk of one 16-row tile i of a pair by one lane:
 // lane unit (g, t) holds rows g and g+8 of each tile at k = 32b + 8t .. +7.
 // The lane -> (g, t) map makes both the record loads and the swizzled
 // stores of every 8-lane phase hit 8 distinct bank groups.  Each weight goes
 // to the hi tile and its exact remainder to the lo tile.
 template <int QT>
-__device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned char* ahi,
-                                              unsigned char* alo, int pair_in_cta, int lane) {
+__device__ __forceinline__ void dequant_tile(const unsigned char* raw, unsigned char* ahi,
+                                             unsigned char* alo, int pair_in_cta, int i, int lane) {
   using RC = TcRec<QT>;
   const int ph = lane >> 3, j = lane & 7;
   const int p = j & 1, t0 = (j >> 1) & 1, t1 = j >> 2;
   const int g = 4 * (p ^ (ph >> 1)) + 2 * (t0 ^ (ph & 1)) + p, t = 2 * t1 + t0;
   const int l = 4 * g + t;  // the record's lane index of this unit
-#pragma unroll
-  for (int i = 0; i < 2; i++) {
+  {
     const uint2 sw = *reinterpret_cast<const uint2*>(raw + RC::SC + i * 64 + g * 8);
     const __half2 s0 = *reinterpret_cast<const __half2*>(&sw.x);  // (row g, row g+8), block 0
     const __half2 s1 = *reinterpret_cast<const __half2*>(&sw.y);  // block 1
@@ -304,26 +302,26 @@ __device__ __forceinline__ void dequant_chunk(const unsigned char* raw, unsigned
   }
 }
 
-// Epilogue of 32 finished columns (activation rows col0..col0+31) of this
+// Epilogue of EW finished columns (activation rows col0..col0+EW-1) of this
 // thread's weight row n: v[c] is the sum for row col0 + c.
-__device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, const float (&v)[32],
+__device__ __forceinline__ void tc_epilogue(const TcArgs& a, int n, int col0, const float (&v)[EW],
                                               int lane, uint32_t* s_key, int quad) {
   const LinEpi& e = a.epi;
   const bool real = n < a.N;
   switch (e.kind) {
     case EPI_STORE:
 #pragma unroll
-      for (int c = 0; c < 32; c++)
+      for (int c = 0; c < EW; c++)
         if (real && col0 + c < a.R) e.y[(size_t)(col0 + c) * e.ldy + n] = v[c];
       break;
     case EPI_RESID: {
-      // the 32 old values in one batch of loads, then the stores
-      float old[32];
+      // the EW old values in one batch of loads, then the stores
+      float old[EW];
 #pragma unroll
-      for (int c = 0; c < 32; c++)
+      for (int c = 0; c < EW; c++)
         old[c] = real && col0 + c < a.R ? e.y[(size_t)(col0 + c) * e.ldy + n] : 0.0f;
 #pragma unroll
-      for (int c = 0; c < 32; c++)
+      for (int c = 0; c < EW; c++)
         if (real && col0 + c < a.R) e.y[(size_t)(col0 + c) * e.ldy + n] = old[c] + v[c];
       break;
     }
@@ -331,7 +329,7 @@ __device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, 
       // rows g (gate j) and g+8 (up j) of each 16-row tile are lanes l, l+8
       const int g = n & 15, T = n >> 4;
 #pragma unroll
-      for (int c = 0; c < 32; c++) {
+      for (int c = 0; c < EW; c++) {
         const float up = __shfl_xor_sync(0xffffffffu, v[c], 8);
         const int r = col0 + c;
         if (g < 8 && real && r < a.R) {
@@ -350,20 +348,20 @@ __device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, 
       const bool rope = e.rope != nullptr && hh < e.nq + e.nkv;
       // the columns' (slot, position) records and RoPE factors in one batch
       // of loads before any is used
-      RowInfo ri_c[32];
-      float2 cs_c[32];
+      RowInfo ri_c[EW];
+      float2 cs_c[EW];
 #pragma unroll
-      for (int c = 0; c < 32; c++) {
+      for (int c = 0; c < EW; c++) {
         const int r = min(col0 + c, a.R - 1);
         ri_c[c] = e.rows[r];
       }
 #pragma unroll
-      for (int c = 0; c < 32; c++) {
+      for (int c = 0; c < EW; c++) {
         const int rp = ri_c[c].pos < e.max_ctx ? ri_c[c].pos : e.max_ctx - 1;
         cs_c[c] = rope ? e.rope[(size_t)max(rp, 0) * (e.hd / 2) + i0] : make_float2(1.0f, 0.0f);
       }
 #pragma unroll
-      for (int c = 0; c < 32; c++) {
+      for (int c = 0; c < EW; c++) {
         const float x1 = __shfl_xor_sync(0xffffffffu, v[c], 8);
         const int r = col0 + c;
         if (g >= 8 || !real || r >= a.R) continue;
@@ -394,7 +392,7 @@ __device__ __forceinline__ void tc_epilogue32(const TcArgs& a, int n, int col0, 
       // of order-preserving keys, then the four warps through shared memory
       bool bad = false;
 #pragma unroll
-      for (int c = 0; c < 32; c++) {
+      for (int c = 0; c < EW; c++) {
         const int r = col0 + c;
         if (r >= a.R) continue;  // uniform across the warp
         if (e.y != nullptr && real) e.y[(size_t)r * e.ldy + n] = v[c];
@@ -453,7 +451,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STA; s++) {
-      mbar_init(A_FULL(s), 128);
+      mbar_init(A_FULL(s), TC_EPI_THREADS);
       mbar_init(A_EMPTY(s), 1);
     }
     for (int s = 0; s < STB; s++) {
@@ -462,7 +460,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     }
     for (int r = 0; r < RAWN; r++) {
       mbar_init(RAW_FULL(r), 1);
-      mbar_init(RAW_EMPTY(r), 128);
+      mbar_init(RAW_EMPTY(r), TC_EPI_THREADS);
     }
     mbar_init(ACC, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -551,8 +549,8 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       tc_commit(ACC);  // completes when every MMA issued above has
     }
   } else {
-    // ---- dequant (warps 3..6: one pair of the CTA's four each)
-    const int pc = warp - TC_EPI_WARP0;
+    // ---- dequant (warps 3..10: one 16-row tile of the CTA's eight each)
+    const int pc = (warp - TC_EPI_WARP0) >> 1, tile = (warp - TC_EPI_WARP0) & 1;
     grid_dep_wait();
     for (int c = 0; c < nc && !*abort_flag; c++) {
       const int r = c % RAWN, ur = c / RAWN, s = c % STA, us = c / STA;
@@ -565,10 +563,10 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       }
       unsigned char* at = A0 + s * 2 * TC_A_BYTES;
       if (pair0 + pc < a.n_pairs) {
-        dequant_chunk<QT>(RAW0 + r * RAW_BYTES + pc * RC::BYTES, at, at + TC_A_BYTES, pc, lane);
+        dequant_tile<QT>(RAW0 + r * RAW_BYTES + pc * RC::BYTES, at, at + TC_A_BYTES, pc, tile, lane);
       } else {  // rows past the matrix: zeros
-        for (int q = lane; q < 32 * 8; q += 32) {
-          const int rr = 32 * pc + q / 8, u = q % 8;
+        for (int q = lane; q < 16 * 8; q += 32) {
+          const int rr = 32 * pc + 16 * tile + q / 8, u = q % 8;
           *reinterpret_cast<uint4*>(at + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(at + TC_A_BYTES + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
         }
@@ -580,11 +578,15 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   }
   grid_dep_launch();
 
-  // ---- epilogue: warps 3..6 (TMEM lane quadrant warp % 4)
+  // ---- epilogue: warps 3..10; warp w reads TMEM lane quadrant w % 4 and
+  // ---- every other group of EW columns (the two warps of a quadrant split
+  // ---- the columns)
   if (warp >= TC_EPI_WARP0) {
-    const int quad = warp & 3;
+    const int quad = warp & 3, half = (warp - TC_EPI_WARP0) >> 2;
+    const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..255
     const int m = 32 * quad + lane;  // TMEM lane = weight row of the tile
     const int n = mt * TC_M + m;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
     const bool acc_ok = mbar_wait(ACC, 0, LIN_WAIT_TRIES);
     if (!acc_ok) give_up();
     tc_fence_after();
@@ -593,17 +595,15 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     // segments in order
     bool finisher = true;
     if (a.S > 1) {
-      for (int col0 = 0; col0 < a.Npad; col0 += 32) {
-        uint32_t v[32];
-        tc_ld32(tmem + ((uint32_t)(32 * quad) << 16) + col0, v);
+      for (int col0 = half * EW; col0 < a.Npad; col0 += 2 * EW) {
+        uint32_t v[EW];
+        tc_ld16(trow + col0, v);
         float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * TC_M + m;
-        // Npad is a multiple of 16: the last group of 32 may be half outside
 #pragma unroll
-        for (int c = 0; c < 32; c++)
-          if (col0 + c < a.Npad) dst[(size_t)c * TC_M] = __uint_as_float(v[c]);
+        for (int c = 0; c < EW; c++) dst[(size_t)c * TC_M] = __uint_as_float(v[c]);
       }
       epi_bar();
-      if (threadIdx.x == TC_EPI_WARP0 * 32) {
+      if (et == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&a.tickets[mt], 1u);
         s_last = prev == (unsigned)(a.S - 1);
@@ -613,33 +613,31 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       finisher = s_last != 0;
     }
     if (finisher) {
-      for (int col0 = 0; col0 < a.Npad; col0 += 32) {
-        float v[32];
+      for (int col0 = half * EW; col0 < a.Npad; col0 += 2 * EW) {
+        float v[EW];
         if (a.S > 1) {
           const float* src = a.part + ((size_t)mt * a.Npad + col0) * TC_M + m;
           const size_t step = (size_t)a.n_mt * a.Npad * TC_M;
 #pragma unroll
-          for (int c = 0; c < 32; c++)
-            v[c] = col0 + c < a.Npad ? __ldcg(src + (size_t)c * TC_M) : 0.0f;
+          for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * TC_M);
           for (int s2 = 1; s2 < a.S; s2++)
 #pragma unroll
-            for (int c = 0; c < 32; c++)
-              if (col0 + c < a.Npad) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_M);
+            for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_M);
         } else {
-          uint32_t u[32];
-          tc_ld32(tmem + ((uint32_t)(32 * quad) << 16) + col0, u);
+          uint32_t u[EW];
+          tc_ld16(trow + col0, u);
 #pragma unroll
-          for (int c = 0; c < 32; c++) v[c] = __uint_as_float(u[c]);
+          for (int c = 0; c < EW; c++) v[c] = __uint_as_float(u[c]);
         }
-        if (!aborted) tc_epilogue32(a, n, col0, v, lane, s_key, quad);
+        if (!aborted) tc_epilogue(a, n, col0, v, lane, s_key, quad);
       }
-      if (a.S > 1 && threadIdx.x == TC_EPI_WARP0 * 32) a.tickets[mt] = 0u;
+      if (a.S > 1 && et == 0) a.tickets[mt] = 0u;
       if (a.epi.kind == EPI_LMHEAD) {
         // the CTA's best of each column -> one packed 64-bit maximum per
         // column (value key high, inverted id low: ties go to the lowest id);
         // an aborted CTA still takes its ticket, so the state is reset
         epi_bar();
-        for (int r = threadIdx.x - TC_EPI_WARP0 * 32; r < a.R && !aborted; r += 128) {
+        for (int r = et; r < a.R && !aborted; r += TC_EPI_THREADS) {
           uint32_t bk = s_key[r], bi = s_key[256 + r];
           for (int q = 1; q < 4; q++) {
             const uint32_t k2 = s_key[(2 * q) * 256 + r], i2 = s_key[(2 * q + 1) * 256 + r];
@@ -651,7 +649,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           atomicMax(&a.amax_key[r], ((unsigned long long)bk << 32) | (unsigned long long)(~bi));
         }
         epi_bar();
-        if (threadIdx.x == TC_EPI_WARP0 * 32) {
+        if (et == 0) {
           __threadfence();
           const unsigned prev = atomicAdd(&a.tickets[a.n_mt], 1u);
           s_last = prev == (unsigned)(a.n_mt - 1);
@@ -659,12 +657,12 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         }
         epi_bar();
         if (s_last) {  // every tile's maxima are in: the argmax, and reset
-          for (int r = threadIdx.x - TC_EPI_WARP0 * 32; r < a.Npad; r += 128) {
+          for (int r = et; r < a.Npad; r += TC_EPI_THREADS) {
             const unsigned long long k = __ldcg(&a.amax_key[r]);
             if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = (int)(~(uint32_t)k);
             a.amax_key[r] = 0ull;
           }
-          if (threadIdx.x == TC_EPI_WARP0 * 32) a.tickets[a.n_mt] = 0u;
+          if (et == 0) a.tickets[a.n_mt] = 0u;
         }
       }
     }
