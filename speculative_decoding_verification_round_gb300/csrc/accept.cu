@@ -116,6 +116,7 @@ __global__ void accept_greedy_kernel(const int32_t* __restrict__ argmax,
 constexpr int ST_CLUSTER = 8;
 constexpr int ST_THREADS = 512;
 constexpr int ST_MAX_SMEM = 200 * 1024;  // z slice per CTA: V <= 8 * 51200
+constexpr int ST_ILP = 8;                // independent elements per thread step
 
 __global__ void __launch_bounds__(ST_THREADS)
 row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int d, int V,
@@ -135,14 +136,27 @@ row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int d
                              : q + ((size_t)s * d + (rr - d - 1)) * V;
   const int slice = (V + ST_CLUSTER - 1) / ST_CLUSTER;
   const int v0 = rank * slice, v1 = min(V, v0 + slice);
+  // ST_ILP independent elements per step of each thread (the division and
+  // the exp are long dependent chains): loads first, then the arithmetic
   float mx = -INFINITY;
   bool bad = false;
-  for (int v = v0 + threadIdx.x; v < v1; v += ST_THREADS) {
-    const float l = __ldcs(src + v);
-    bad |= !isfinite(l);
-    const float z = __fdiv_rn(l, T);
-    zs[v - v0] = z;
-    mx = fmaxf(mx, z);
+  for (int vb = v0 + threadIdx.x; vb < v1; vb += ST_THREADS * ST_ILP) {
+    float l[ST_ILP];
+#pragma unroll
+    for (int u = 0; u < ST_ILP; u++) {
+      const int v = vb + u * ST_THREADS;
+      l[u] = v < v1 ? __ldcs(src + v) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < ST_ILP; u++) {
+      const int v = vb + u * ST_THREADS;
+      if (v < v1) {
+        bad |= !isfinite(l[u]);
+        const float z = __fdiv_rn(l[u], T);
+        zs[v - v0] = z;
+        mx = fmaxf(mx, z);
+      }
+    }
   }
   if (bad) atomicOr(err, ERR_NONFINITE);
 #pragma unroll
@@ -157,9 +171,19 @@ row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int d
   cluster.sync();
   float gmax = -INFINITY;
   for (int rk = 0; rk < ST_CLUSTER; rk++) gmax = fmaxf(gmax, *cluster.map_shared_rank(&s_cmax, rk));
-  unsigned long long acc = 0ull;
-  for (int v = v0 + threadIdx.x; v < v1; v += ST_THREADS)
-    acc += int_weight(__fsub_rn(zs[v - v0], gmax));
+  unsigned long long accs[ST_ILP];
+#pragma unroll
+  for (int u = 0; u < ST_ILP; u++) accs[u] = 0ull;
+  for (int vb = v0 + threadIdx.x; vb < v1; vb += ST_THREADS * ST_ILP) {
+#pragma unroll
+    for (int u = 0; u < ST_ILP; u++) {
+      const int v = vb + u * ST_THREADS;
+      if (v < v1) accs[u] += int_weight(__fsub_rn(zs[v - v0], gmax));
+    }
+  }
+  unsigned long long acc = 0ull;  // integer sums: exact in any order
+#pragma unroll
+  for (int u = 0; u < ST_ILP; u++) acc += accs[u];
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if ((threadIdx.x & 31) == 0) s_red64[threadIdx.x >> 5] = acc;

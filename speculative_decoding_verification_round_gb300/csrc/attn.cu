@@ -69,10 +69,12 @@ inline ChunkSmem chunk_smem(int hd, int ds, int nw, int n_mt) {
   return c;
 }
 
-// 2 CTAs per SM (what the shared memory holds); with 8 warps that caps the
-// registers at 128, which the q fragments read from shared memory allow.
+// 2 CTAs per SM (what the shared memory holds) up to 8 warps; with 8 warps
+// that caps the registers at 128, which the q fragments read from shared
+// memory allow.  12 warps (5 or 6 m tiles: every work item in one round)
+// run one CTA per SM.
 template <int HD, int DS, int NW>
-__global__ void __launch_bounds__(NW * 32, 2)
+__global__ void __launch_bounds__(NW * 32, NW > 8 ? 1 : 2)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
                   int nt, int nq, int nkv, int max_ctx, int nchunks, ChunkSmem lay,
@@ -104,13 +106,16 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   constexpr int RP = NW * 32 / UNITS;         // rows per pass of the CTA
   const int u = threadIdx.x % UNITS, p0 = threadIdx.x / UNITS;
   const size_t head_base = ((size_t)slot * nkv + kvh) * max_ctx;
-  // a thread copies unit u of the rows p0, p0 + RP, ...: its swizzled column
-  // (u ^ (p & 7)) is the same for all of them (RP is a multiple of 8)
+  // a thread copies unit u of the rows p0, p0 + RP, ... below CH: its
+  // swizzled column (u ^ (p & 7)) is the same for all of them (RP is a
+  // multiple of 8; it need not divide CH)
+  static_assert(RP % 8 == 0, "rows per pass must keep the swizzle column");
   auto stage = [&](unsigned char* tile, const __half* cache, bool committed) {
     const uint32_t s0 = smem_u32(tile) + tile_off<HD>(p0, u);
     const __half* g0 = cache + (head_base + (size_t)c * CH + p0) * HD + u * 8;
 #pragma unroll 4
-    for (int i = 0; i < CH / RP; i++) {
+    for (int i = 0; i < (CH + RP - 1) / RP; i++) {
+      if (p0 + RP * i >= CH) break;
       const int pg = c * CH + p0 + RP * i;
       if ((pg < new0) != committed) continue;
       const uint32_t so = s0 + (uint32_t)(i * RP * HD * 2);
@@ -333,25 +338,26 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   }
 }
 
-// One CTA per (row, q head), one thread per head dimension: merge chunks
-// 0..P/CH in increasing order.  The o loads of the first MB chunks go out
-// together with every chunk's (m, l), so a context of up to MB chunks costs
-// one round trip; the global max (exact in any order) is a block reduction,
-// the thread owning chunk c stores w_c = exp2(m_c - max) in shared memory,
-// and each thread sums w_c * o_c[d] and w_c * l_c over the chunks in order.
-constexpr int MERGE_MB = 40;
+// One warp per (row, q head), eight per CTA: merge chunks 0..P/CH in
+// increasing order.  The chunks' (m, l) are loaded 32 at a time (one per
+// lane) and the global max (exact in any order) is a warp reduction; the
+// weights w_c = exp2(m_c - max) are broadcast by shuffle, and each lane sums
+// w_c * o_c[d] for its HD / 32 head dimensions and w_c * l_c over the
+// chunks in order, eight chunks' o loads in flight at a time.  The
+// arithmetic of a row does not depend on the other rows.
+constexpr int MERGE_WARPS = 8;
+constexpr int MERGE_BATCH = 8;
 template <int HD>
-__global__ void __launch_bounds__(HD)
+__global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
                   int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
                   __half* __restrict__ out) {
   grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
-  extern __shared__ float s_ml[];  // [nchunks] w, then [nchunks] l
-  float* s_w = s_ml;
-  float* s_l = s_ml + nchunks;
-  __shared__ float s_red[HD / 32];
-  const int r = blockIdx.x / nq, h = blockIdx.x % nq;
-  const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  constexpr int DPL = HD / 32;  // head dimensions of a lane (4 or 2)
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * MERGE_WARPS + (threadIdx.x >> 5);
+  if (item >= R * nq) return;  // whole warps
+  const int r = item / nq, h = item % nq;
   const int s = r / nt, i = r % nt;
   const int G = nq / nkv, kvh = h / G, gh = h % G;
   const int M = nt * G, m = i * G + gh;
@@ -361,46 +367,54 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
   const size_t stride = (size_t)M * (HD + 2);  // floats between consecutive chunks
   const float* p0 = part + ((((size_t)s * nkv + kvh) * nchunks) * M + m) * (HD + 2);
   grid_dep_wait();  // the partials come from the chunk kernel
-  float v[MERGE_MB];
-#pragma unroll
-  for (int u = 0; u < MERGE_MB; u++) v[u] = u < nc ? __ldcg(p0 + (size_t)u * stride + d) : 0.0f;
   float mx = -INFINITY;
-  for (int c = d; c < nc; c += HD) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
-    s_w[c] = ml.x;  // m for now
-    s_l[c] = ml.y;
-    mx = fmaxf(mx, ml.x);
-  }
+  for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(p0 + (size_t)c * stride + HD));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if (lane == 0) s_red[warp] = mx;
-  __syncthreads();
-  mx = s_red[0];
+  float o[DPL], l = 0.0f;
 #pragma unroll
-  for (int w = 1; w < HD / 32; w++) mx = fmaxf(mx, s_red[w]);
-  for (int c = d; c < nc; c += HD) s_w[c] = exp2f(s_w[c] - mx);
-  __syncthreads();
-  float o = 0.0f, l = 0.0f;
+  for (int k = 0; k < DPL; k++) o[k] = 0.0f;
+  for (int cb = 0; cb < nc; cb += 32) {
+    const int c = cb + lane;
+    float2 ml = make_float2(0.0f, 0.0f);
+    if (c < nc) ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
+    const float w = c < nc ? exp2f(ml.x - mx) : 0.0f;
+    const int nb = min(32, nc - cb);
+    for (int u0 = 0; u0 < nb; u0 += MERGE_BATCH) {
+      float ov[MERGE_BATCH][DPL];
 #pragma unroll
-  for (int u = 0; u < MERGE_MB; u++)
-    if (u < nc) {
-      const float w = s_w[u];
-      l = fmaf(s_l[u], w, l);
-      o = fmaf(v[u], w, o);
-    }
-  for (int c = MERGE_MB; c < nc; c += 16) {  // long contexts: sixteen loads in flight
-    float v2[16];
-#pragma unroll
-    for (int u = 0; u < 16; u++) v2[u] = c + u < nc ? __ldcg(p0 + (size_t)(c + u) * stride + d) : 0.0f;
-#pragma unroll
-    for (int u = 0; u < 16; u++)
-      if (c + u < nc) {
-        const float w = s_w[c + u];
-        l = fmaf(s_l[c + u], w, l);
-        o = fmaf(v2[u], w, o);
+      for (int u = 0; u < MERGE_BATCH; u++) {
+        const float* src = p0 + (size_t)(cb + u0 + u) * stride + lane * DPL;
+        if (u0 + u < nb) {
+          if constexpr (DPL == 4) {
+            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+            ov[u][0] = t.x;
+            ov[u][1] = t.y;
+            ov[u][2] = t.z;
+            ov[u][3] = t.w;
+          } else {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+            ov[u][0] = t.x;
+            ov[u][1] = t.y;
+          }
+        }
       }
+#pragma unroll
+      for (int u = 0; u < MERGE_BATCH; u++) {
+        const float wu = __shfl_sync(0xffffffffu, w, (u0 + u) & 31);
+        const float lu = __shfl_sync(0xffffffffu, ml.y, (u0 + u) & 31);
+        if (u0 + u < nb) {
+          l = fmaf(lu, wu, l);
+#pragma unroll
+          for (int k = 0; k < DPL; k++) o[k] = fmaf(ov[u][k], wu, o[k]);
+        }
+      }
+    }
   }
-  out[(size_t)r * nq * HD + (size_t)h * HD + d] = __float2half_rn(o * (1.0f / l));
+  const float inv = 1.0f / l;
+  __half* dst = out + (size_t)r * nq * HD + (size_t)h * HD + lane * DPL;
+#pragma unroll
+  for (int k = 0; k < DPL; k++) dst[k] = __float2half_rn(o[k] * inv);
 }
 
 template <int HD>
@@ -424,18 +438,21 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
   // tiles: 4 warps; more: 8 warps, so that 4 m tiles are still one round of
   // work items (the bits of every output depend on none of these choices)
   const int n_mt = (nt * (nq / nkv) + 15) / 16;
-  const int ds = n_mt == 1 ? 2 : 1, nw = n_mt <= 2 ? 4 : 8;
+  const int ds = n_mt == 1 ? 2 : 1;
+  const int nw = n_mt <= 2 ? 4 : (n_mt <= 4 || n_mt > 6 ? 8 : 12);
   auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2, 4>
-                         : (n_mt == 2 ? attn_chunk_kernel<HD, 1, 4> : attn_chunk_kernel<HD, 1, 8>);
+               : n_mt == 2 ? attn_chunk_kernel<HD, 1, 4>
+               : nw == 12  ? attn_chunk_kernel<HD, 1, 12>
+                           : attn_chunk_kernel<HD, 1, 8>;
   const ChunkSmem lay = chunk_smem(HD, ds, nw, n_mt);
   cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = lay.bytes;
   cudaError_t e = cudaLaunchKernelEx(&cfg, chunk, q, kcache, vcache, rows, nt, nq, nkv, max_ctx,
                                      nchunks, lay, part);
   if (e == cudaSuccess) {
-    cfg.gridDim = dim3(R * nq);
-    cfg.blockDim = dim3(HD);
-    cfg.dynamicSmemBytes = 2 * sizeof(float) * (size_t)nchunks;
+    cfg.gridDim = dim3((R * nq + MERGE_WARPS - 1) / MERGE_WARPS);
+    cfg.blockDim = dim3(MERGE_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, (const float*)part, rows, R, nt, nq, nkv,
                            max_ctx, nchunks, out);
   }
@@ -465,7 +482,8 @@ void attn_init_attrs() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   for (auto k : {attn_chunk_kernel<128, 2, 4>, attn_chunk_kernel<128, 1, 4>,
-                 attn_chunk_kernel<128, 1, 8>, attn_chunk_kernel<64, 2, 4>,
-                 attn_chunk_kernel<64, 1, 4>, attn_chunk_kernel<64, 1, 8>})
+                 attn_chunk_kernel<128, 1, 8>, attn_chunk_kernel<128, 1, 12>,
+                 attn_chunk_kernel<64, 2, 4>, attn_chunk_kernel<64, 1, 4>,
+                 attn_chunk_kernel<64, 1, 8>, attn_chunk_kernel<64, 1, 12>})
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
