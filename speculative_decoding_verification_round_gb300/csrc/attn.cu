@@ -384,18 +384,15 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
       float ov[MERGE_BATCH][DPL];
 #pragma unroll
       for (int u = 0; u < MERGE_BATCH; u++) {
+        // a partial row is HD + 2 floats: only 8-byte alignment holds, so
+        // the lane's dimensions come as float2 pairs
         const float* src = p0 + (size_t)(cb + u0 + u) * stride + lane * DPL;
         if (u0 + u < nb) {
-          if constexpr (DPL == 4) {
-            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
-            ov[u][0] = t.x;
-            ov[u][1] = t.y;
-            ov[u][2] = t.z;
-            ov[u][3] = t.w;
-          } else {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
-            ov[u][0] = t.x;
-            ov[u][1] = t.y;
+#pragma unroll
+          for (int k = 0; k < DPL; k += 2) {
+            const float2 t = __ldcg(reinterpret_cast<const float2*>(src + k));
+            ov[u][k] = t.x;
+            ov[u][k + 1] = t.y;
           }
         }
       }
