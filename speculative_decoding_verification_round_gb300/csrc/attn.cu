@@ -338,15 +338,16 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   }
 }
 
-// One warp per (row, q head), eight per CTA: merge chunks 0..P/CH in
+// One warp per (row, q head), two per CTA: merge chunks 0..P/CH in
 // increasing order.  The chunks' (m, l) are loaded 32 at a time (one per
 // lane) and the global max (exact in any order) is a warp reduction; the
 // weights w_c = exp2(m_c - max) are broadcast by shuffle, and each lane sums
 // w_c * o_c[d] for its HD / 32 head dimensions and w_c * l_c over the
-// chunks in order, eight chunks' o loads in flight at a time.  The
-// arithmetic of a row does not depend on the other rows.
-constexpr int MERGE_WARPS = 8;
-constexpr int MERGE_BATCH = 8;
+// chunks in order, MERGE_BATCH chunks' o loads in flight at a time (the
+// first batch issued together with the (m, l) loads).  The arithmetic of a
+// row does not depend on the other rows.
+constexpr int MERGE_WARPS = 2;
+constexpr int MERGE_BATCH = 16;
 template <int HD>
 __global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
@@ -366,9 +367,26 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
   const int nc = pos / CH + 1;
   const size_t stride = (size_t)M * (HD + 2);  // floats between consecutive chunks
   const float* p0 = part + ((((size_t)s * nkv + kvh) * nchunks) * M + m) * (HD + 2);
+  // a partial row is HD + 2 floats: only 8-byte alignment holds, so a
+  // lane's dimensions come as float2 pairs
+  auto load_o = [&](int c, float (&o)[DPL]) {
+    const float* src = p0 + (size_t)c * stride + lane * DPL;
+#pragma unroll
+    for (int k = 0; k < DPL; k += 2) {
+      const float2 t = __ldcg(reinterpret_cast<const float2*>(src + k));
+      o[k] = t.x;
+      o[k + 1] = t.y;
+    }
+  };
   grid_dep_wait();  // the partials come from the chunk kernel
-  float mx = -INFINITY;
-  for (int c = lane; c < nc; c += 32) mx = fmaxf(mx, __ldcg(p0 + (size_t)c * stride + HD));
+  float ov[MERGE_BATCH][DPL];
+#pragma unroll
+  for (int u = 0; u < MERGE_BATCH; u++)
+    if (u < nc) load_o(u, ov[u]);
+  float2 ml0 = make_float2(-INFINITY, 0.0f);
+  if (lane < nc) ml0 = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)lane * stride + HD));
+  float mx = ml0.x;
+  for (int c = lane + 32; c < nc; c += 32) mx = fmaxf(mx, __ldcg(p0 + (size_t)c * stride + HD));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
   float o[DPL], l = 0.0f;
@@ -376,25 +394,18 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
   for (int k = 0; k < DPL; k++) o[k] = 0.0f;
   for (int cb = 0; cb < nc; cb += 32) {
     const int c = cb + lane;
-    float2 ml = make_float2(0.0f, 0.0f);
-    if (c < nc) ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
+    float2 ml = ml0;
+    if (cb > 0) {
+      ml = make_float2(0.0f, 0.0f);
+      if (c < nc) ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
+    }
     const float w = c < nc ? exp2f(ml.x - mx) : 0.0f;
     const int nb = min(32, nc - cb);
     for (int u0 = 0; u0 < nb; u0 += MERGE_BATCH) {
-      float ov[MERGE_BATCH][DPL];
+      if (cb > 0 || u0 > 0) {
 #pragma unroll
-      for (int u = 0; u < MERGE_BATCH; u++) {
-        // a partial row is HD + 2 floats: only 8-byte alignment holds, so
-        // the lane's dimensions come as float2 pairs
-        const float* src = p0 + (size_t)(cb + u0 + u) * stride + lane * DPL;
-        if (u0 + u < nb) {
-#pragma unroll
-          for (int k = 0; k < DPL; k += 2) {
-            const float2 t = __ldcg(reinterpret_cast<const float2*>(src + k));
-            ov[u][k] = t.x;
-            ov[u][k + 1] = t.y;
-          }
-        }
+        for (int u = 0; u < MERGE_BATCH; u++)
+          if (u0 + u < nb) load_o(cb + u0 + u, ov[u]);
       }
 #pragma unroll
       for (int u = 0; u < MERGE_BATCH; u++) {
