@@ -425,6 +425,79 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
   for (int k = 0; k < DPL; k++) dst[k] = __float2half_rn(o[k] * inv);
 }
 
+// The merge for long contexts (more than 16 chunks): one CTA per (row, q
+// head), one thread per head dimension, the same arithmetic in the same
+// order as attn_merge_kernel (results are bitwise the same): merge chunks
+// 0..P/CH in increasing order.  The o loads of the first MB chunks go out
+// together with every chunk's (m, l), so a context of up to MB chunks costs
+// one round trip; the global max (exact in any order) is a block reduction,
+// the thread owning chunk c stores w_c = exp2(m_c - max) in shared memory,
+// and each thread sums w_c * o_c[d] and w_c * l_c over the chunks in order.
+constexpr int MERGE_MB = 40;
+template <int HD>
+__global__ void __launch_bounds__(HD)
+attn_merge_cta_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
+                  int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
+                  __half* __restrict__ out) {
+  grid_dep_launch();  // a programmatically launched GEMM may prefetch its weights now
+  extern __shared__ float s_ml[];  // [nchunks] w, then [nchunks] l
+  float* s_w = s_ml;
+  float* s_l = s_ml + nchunks;
+  __shared__ float s_red[HD / 32];
+  const int r = blockIdx.x / nq, h = blockIdx.x % nq;
+  const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  const int s = r / nt, i = r % nt;
+  const int G = nq / nkv, kvh = h / G, gh = h % G;
+  const int M = nt * G, m = i * G + gh;
+  const RowInfo ri = rows[r];
+  const int pos = ri.pos < max_ctx ? ri.pos : max_ctx - 1;
+  const int nc = pos / CH + 1;
+  const size_t stride = (size_t)M * (HD + 2);  // floats between consecutive chunks
+  const float* p0 = part + ((((size_t)s * nkv + kvh) * nchunks) * M + m) * (HD + 2);
+  grid_dep_wait();  // the partials come from the chunk kernel
+  float v[MERGE_MB];
+#pragma unroll
+  for (int u = 0; u < MERGE_MB; u++) v[u] = u < nc ? __ldcg(p0 + (size_t)u * stride + d) : 0.0f;
+  float mx = -INFINITY;
+  for (int c = d; c < nc; c += HD) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)c * stride + HD));
+    s_w[c] = ml.x;  // m for now
+    s_l[c] = ml.y;
+    mx = fmaxf(mx, ml.x);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) s_red[warp] = mx;
+  __syncthreads();
+  mx = s_red[0];
+#pragma unroll
+  for (int w = 1; w < HD / 32; w++) mx = fmaxf(mx, s_red[w]);
+  for (int c = d; c < nc; c += HD) s_w[c] = exp2f(s_w[c] - mx);
+  __syncthreads();
+  float o = 0.0f, l = 0.0f;
+#pragma unroll
+  for (int u = 0; u < MERGE_MB; u++)
+    if (u < nc) {
+      const float w = s_w[u];
+      l = fmaf(s_l[u], w, l);
+      o = fmaf(v[u], w, o);
+    }
+  for (int c = MERGE_MB; c < nc; c += 16) {  // long contexts: sixteen loads in flight
+    float v2[16];
+#pragma unroll
+    for (int u = 0; u < 16; u++) v2[u] = c + u < nc ? __ldcg(p0 + (size_t)(c + u) * stride + d) : 0.0f;
+#pragma unroll
+    for (int u = 0; u < 16; u++)
+      if (c + u < nc) {
+        const float w = s_w[c + u];
+        l = fmaf(s_l[c + u], w, l);
+        o = fmaf(v2[u], w, o);
+      }
+  }
+  out[(size_t)r * nq * HD + (size_t)h * HD + d] = __float2half_rn(o * (1.0f / l));
+}
+
+
 template <int HD>
 int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
                   const RowInfo* rows, int n_seq, int nt, int nq, int nkv, int max_ctx,
@@ -458,11 +531,22 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
   cudaError_t e = cudaLaunchKernelEx(&cfg, chunk, q, kcache, vcache, rows, nt, nq, nkv, max_ctx,
                                      nchunks, lay, part);
   if (e == cudaSuccess) {
-    cfg.gridDim = dim3((R * nq + MERGE_WARPS - 1) / MERGE_WARPS);
-    cfg.blockDim = dim3(MERGE_WARPS * 32);
-    cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, (const float*)part, rows, R, nt, nq, nkv,
-                           max_ctx, nchunks, out);
+    // the model's chunk count picks the merge (never nt): a warp per (row,
+    // head) for short contexts, a CTA per (row, head) -- every chunk's loads
+    // in flight at once -- for long ones; both compute the same bits
+    if (nchunks <= MERGE_BATCH) {
+      cfg.gridDim = dim3((R * nq + MERGE_WARPS - 1) / MERGE_WARPS);
+      cfg.blockDim = dim3(MERGE_WARPS * 32);
+      cfg.dynamicSmemBytes = 0;
+      e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, (const float*)part, rows, R, nt, nq,
+                             nkv, max_ctx, nchunks, out);
+    } else {
+      cfg.gridDim = dim3(R * nq);
+      cfg.blockDim = dim3(HD);
+      cfg.dynamicSmemBytes = 2 * sizeof(float) * (size_t)nchunks;
+      e = cudaLaunchKernelEx(&cfg, attn_merge_cta_kernel<HD>, (const float*)part, rows, R, nt, nq,
+                             nkv, max_ctx, nchunks, out);
+    }
   }
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("attention launch: ") + cudaGetErrorString(e));
   return SPEC_OK;

@@ -744,9 +744,12 @@ int tc_mtiles(const QMat& w) { return (w.N + TC_M - 1) / TC_M; }
 
 // K segments of a matrix for the tensor-core GEMM: the fewest waves of
 // one-CTA-per-SM launches, each CTA's chunk count, plus a small cost per
-// extra segment (its partial written and read back).
+// extra segment (its partial written and read back).  Only matrices whose
+// tiles do not fill the SMs are split: beyond one wave the partials (128 x
+// rows x 4 bytes per tile and segment) would spill from L2 to DRAM.
 int tc_choose_split(int N, int nch, int sms) {
   const int n_mt = (N + TC_M - 1) / TC_M;
+  if (n_mt >= sms) return 1;
   int best = 1;
   double best_t = 1e30;
   for (int S = 1; S <= 8 && S <= nch; S++) {
