@@ -19,6 +19,7 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -109,162 +110,220 @@ __global__ void accept_greedy_kernel(const int32_t* __restrict__ argmax,
 }
 
 // ---------------------------------------------------------------------------
-// stochastic, step 1: per-row (max z, S = sum W) with a cluster of CTAs per
-// row; each CTA keeps its slice of z in shared memory, so the row is read
-// from HBM once.  Rows: p rows 0..d then q rows 0..d-1 of every sequence.
+// stochastic, step 1: per-row max z and S = sum W, over every row the accept
+// may need (p rows 0..d, then q rows 0..d-1 of every sequence), in two
+// streaming passes of many short CTAs, each over a segment of one row:
+//   1. the largest logit of the row (z = l / T is monotone in l for T > 0,
+//      so max z = fl(max l / T)): one atomicMax of an order-preserving key
+//      per CTA, and the non-finite check;
+//   2. S = sum of the integer weights: each CTA adds its segment's exact
+//      64-bit sum (integer sums do not depend on the order).
+// The second pass walks the segments in the reverse order of the first, so
+// the rows it starts with are the ones the first pass left in L2.
 // ---------------------------------------------------------------------------
-constexpr int ST_CLUSTER = 8;
-constexpr int ST_THREADS = 512;
-constexpr int ST_MAX_SMEM = 200 * 1024;  // z slice per CTA: V <= 8 * 51200
-constexpr int ST_ILP = 8;                // independent elements per thread step
+constexpr int ST_THREADS = 256;
+constexpr int ST_SEG = 4096;  // logits per CTA (about)
+constexpr int ST_VEC = 4;     // float4 loads in flight per thread and step
 
-__global__ void __launch_bounds__(ST_THREADS)
-row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int d, int V,
-                 float T, float* __restrict__ row_max,
-                 unsigned long long* __restrict__ row_sum, uint32_t* __restrict__ err) {
-  extern __shared__ float zs[];
-  __shared__ float s_red[ST_THREADS / 32];
-  __shared__ unsigned long long s_red64[ST_THREADS / 32];
-  __shared__ float s_cmax;
-  __shared__ unsigned long long s_csum;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
-  const int row = blockIdx.x / ST_CLUSTER;  // global row id: seq * (2d+1) + rr
+// Order-preserving 32-bit key of a float (-0 taken as +0).  Keys of the
+// same row are only compared and turned back into the value.
+__device__ __forceinline__ uint32_t max_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// The row's max z from the key of its largest logit.
+__device__ __forceinline__ float row_zmax(uint32_t key, float T) {
+  const float m = key_value(key);
+  return T == 1.0f ? m : __fdiv_rn(m, T);
+}
+__device__ __forceinline__ float zval(float l, float T) {
+  return T == 1.0f ? l : __fdiv_rn(l, T);  // x / 1 is x exactly
+}
+
+int st_segments(int V) { return std::max(1, std::min(64, (V + ST_SEG - 1) / ST_SEG)); }
+
+__device__ __forceinline__ const float* stoch_row(const float* p, const float* q, int d, int V,
+                                                  int row) {
   const int rows_per_seq = 2 * d + 1;
   const int s = row / rows_per_seq, rr = row % rows_per_seq;
-  const float* src = rr <= d ? p + ((size_t)s * (d + 1) + rr) * V
-                             : q + ((size_t)s * d + (rr - d - 1)) * V;
-  const int slice = (V + ST_CLUSTER - 1) / ST_CLUSTER;
-  const int v0 = rank * slice, v1 = min(V, v0 + slice);
-  // ST_ILP independent elements per step of each thread (the division and
-  // the exp are long dependent chains): loads first, then the arithmetic
+  return rr <= d ? p + ((size_t)s * (d + 1) + rr) * V : q + ((size_t)s * d + (rr - d - 1)) * V;
+}
+
+// Calls f(value) for every logit of src[s0, s1): float4 loads over the
+// 16-byte-aligned middle, ST_VEC of them issued before any is used, and
+// scalar loads at the two ends.
+template <class F>
+__device__ __forceinline__ void for_segment(const float* src, int s0, int s1, F&& f) {
+  const int tid = threadIdx.x;
+  int a0 = s0 + (int)((4u - ((uint32_t)(reinterpret_cast<uintptr_t>(src + s0) >> 2) & 3u)) & 3u);
+  if (a0 > s1) a0 = s1;
+  const int n4 = (s1 - a0) >> 2, a1 = a0 + 4 * n4;
+  for (int v = s0 + tid; v < a0; v += ST_THREADS) f(__ldcs(src + v));
+  for (int v = a1 + tid; v < s1; v += ST_THREADS) f(__ldcs(src + v));
+  const float4* s4 = reinterpret_cast<const float4*>(src + a0);
+  for (int i = tid; i < n4; i += ST_THREADS * ST_VEC) {
+    float4 t[ST_VEC];
+#pragma unroll
+    for (int u = 0; u < ST_VEC; u++)
+      t[u] = i + u * ST_THREADS < n4 ? __ldcs(s4 + i + u * ST_THREADS)
+                                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+    for (int u = 0; u < ST_VEC; u++)
+      if (i + u * ST_THREADS < n4) {
+        f(t[u].x);
+        f(t[u].y);
+        f(t[u].z);
+        f(t[u].w);
+      }
+  }
+}
+
+__global__ void __launch_bounds__(ST_THREADS)
+row_max_kernel(const float* __restrict__ p, const float* __restrict__ q, int d, int V, int nseg,
+               uint32_t* __restrict__ row_key, uint32_t* __restrict__ err) {
+  __shared__ float s_red[ST_THREADS / 32];
+  __shared__ int s_bad;
+  const int row = blockIdx.x / nseg, sg = blockIdx.x % nseg;
+  const float* src = stoch_row(p, q, d, V, row);
+  const int s0 = (int)((long long)sg * V / nseg), s1 = (int)((long long)(sg + 1) * V / nseg);
+  if (threadIdx.x == 0) s_bad = 0;
   float mx = -INFINITY;
   bool bad = false;
-  for (int vb = v0 + threadIdx.x; vb < v1; vb += ST_THREADS * ST_ILP) {
-    float l[ST_ILP];
-#pragma unroll
-    for (int u = 0; u < ST_ILP; u++) {
-      const int v = vb + u * ST_THREADS;
-      l[u] = v < v1 ? __ldcs(src + v) : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < ST_ILP; u++) {
-      const int v = vb + u * ST_THREADS;
-      if (v < v1) {
-        bad |= !isfinite(l[u]);
-        const float z = __fdiv_rn(l[u], T);
-        zs[v - v0] = z;
-        mx = fmaxf(mx, z);
-      }
-    }
-  }
-  if (bad) atomicOr(err, ERR_NONFINITE);
+  for_segment(src, s0, s1, [&](float l) {
+    bad |= !isfinite(l);
+    mx = fmaxf(mx, l);
+  });
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  __syncthreads();
+  if (bad) s_bad = 1;
   if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = mx;
   __syncthreads();
   if (threadIdx.x == 0) {
     float m = s_red[0];
     for (int w = 1; w < ST_THREADS / 32; w++) m = fmaxf(m, s_red[w]);
-    s_cmax = m;
+    atomicMax(&row_key[row], max_key(m));
+    if (s_bad) atomicOr(err, ERR_NONFINITE);
   }
-  cluster.sync();
-  float gmax = -INFINITY;
-  for (int rk = 0; rk < ST_CLUSTER; rk++) gmax = fmaxf(gmax, *cluster.map_shared_rank(&s_cmax, rk));
-  unsigned long long accs[ST_ILP];
-#pragma unroll
-  for (int u = 0; u < ST_ILP; u++) accs[u] = 0ull;
-  for (int vb = v0 + threadIdx.x; vb < v1; vb += ST_THREADS * ST_ILP) {
-#pragma unroll
-    for (int u = 0; u < ST_ILP; u++) {
-      const int v = vb + u * ST_THREADS;
-      if (v < v1) accs[u] += int_weight(__fsub_rn(zs[v - v0], gmax));
-    }
-  }
+}
+
+__global__ void __launch_bounds__(ST_THREADS)
+row_sum_kernel(const float* __restrict__ p, const float* __restrict__ q, int d, int V, int nseg,
+               float T, const uint32_t* __restrict__ row_key,
+               unsigned long long* __restrict__ row_sum) {
+  __shared__ unsigned long long s_red[ST_THREADS / 32];
+  const int id = (int)gridDim.x - 1 - (int)blockIdx.x;  // reverse of the max pass
+  const int row = id / nseg, sg = id % nseg;
+  const float* src = stoch_row(p, q, d, V, row);
+  const int s0 = (int)((long long)sg * V / nseg), s1 = (int)((long long)(sg + 1) * V / nseg);
+  const float zmax = row_zmax(row_key[row], T);
   unsigned long long acc = 0ull;  // integer sums: exact in any order
-#pragma unroll
-  for (int u = 0; u < ST_ILP; u++) acc += accs[u];
+  for_segment(src, s0, s1, [&](float l) { acc += int_weight(__fsub_rn(zval(l, T), zmax)); });
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if ((threadIdx.x & 31) == 0) s_red64[threadIdx.x >> 5] = acc;
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = acc;
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned long long t = 0ull;
-    for (int w = 0; w < ST_THREADS / 32; w++) t += s_red64[w];
-    s_csum = t;
+    for (int w = 0; w < ST_THREADS / 32; w++) t += s_red[w];
+    atomicAdd(&row_sum[row], t);
   }
-  cluster.sync();
-  if (rank == 0 && threadIdx.x == 0) {
-    unsigned long long tot = 0ull;
-    for (int rk = 0; rk < ST_CLUSTER; rk++) tot += *cluster.map_shared_rank(&s_csum, rk);
-    row_max[row] = gmax;
-    row_sum[row] = tot;
-  }
-  cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
 // ---------------------------------------------------------------------------
-// stochastic, step 2: the sequential accept scan, one thread per sequence.
+// stochastic, step 2: the accept scan, one warp per sequence.  The scan is
+// sequential by definition (stop at the first rejection or invalid draft),
+// but its tests are independent: lane i evaluates position base + i (its
+// draft, the two weights, its own sampler counter), and the first stopping
+// position is one ballot.  Nothing past that position changes the outcome.
 // decision[s] = (a, row to sample from, U2, mode: 1 residual / 2 bonus / 0 error)
 // ---------------------------------------------------------------------------
-__global__ void decide_kernel(const float* __restrict__ p, const float* __restrict__ q,
-                              const int32_t* __restrict__ draft, int n_seq, int d, int V,
-                              float T, uint64_t seed, const int32_t* __restrict__ seq_ids,
-                              const uint64_t* __restrict__ emit_idx, int emit_by_slot,
-                              int n_slots,
-                              const float* __restrict__ row_max,
-                              const unsigned long long* __restrict__ row_sum,
-                              int4* __restrict__ decision, int32_t* __restrict__ n_acc,
-                              int32_t* __restrict__ em, uint32_t* __restrict__ err) {
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= n_seq) return;
+constexpr int DC_WARPS = 4;  // sequences per CTA
+
+__global__ void __launch_bounds__(DC_WARPS * 32)
+decide_kernel(const float* __restrict__ p, const float* __restrict__ q,
+              const int32_t* __restrict__ draft, int n_seq, int d, int V, float T, uint64_t seed,
+              const int32_t* __restrict__ seq_ids, const uint64_t* __restrict__ emit_idx,
+              int emit_by_slot, int n_slots, const uint32_t* __restrict__ row_key,
+              const unsigned long long* __restrict__ row_sum, int4* __restrict__ decision,
+              int32_t* __restrict__ n_acc, int32_t* __restrict__ em, uint32_t* __restrict__ err) {
+  const int lane = threadIdx.x & 31;
+  const int s = blockIdx.x * DC_WARPS + (threadIdx.x >> 5);
+  if (s >= n_seq) return;  // whole warps
   const int rows_per_seq = 2 * d + 1;
   const uint32_t sid = (uint32_t)seq_ids[s];
   int32_t* e = em + (size_t)s * (d + 1);
-  for (int i = 0; i <= d; i++) e[i] = -1;
   if (emit_by_slot && (int)sid >= n_slots) {  // also catches negative ids
-    atomicOr(err, ERR_SEQ);
-    decision[s] = make_int4(0, 0, 0, 0);
-    n_acc[s] = -1;
+    for (int i = lane; i <= d; i += 32) e[i] = -1;
+    if (lane == 0) {
+      atomicOr(err, ERR_SEQ);
+      decision[s] = make_int4(0, 0, 0, 0);
+      n_acc[s] = -1;
+    }
     return;
   }
   const uint64_t e0 = emit_idx[emit_by_slot ? (int)sid : s];
-  int a = 0;
-  for (; a < d; a++) {
-    const int x = draft[(size_t)s * d + a];
-    if (x < 0 || x >= V) {
-      atomicOr(err, ERR_TOKEN);
-      decision[s] = make_int4(a, a, 0, 0);
-      n_acc[s] = -1;
-      return;
+  for (int base = 0; base <= d; base += 32) {
+    const int a = base + lane;
+    // lane a < d: accept test of draft a; lane a == d: the bonus draw
+    bool stop = false, invalid = false;
+    uint32_t U1 = 0u;
+    int x = -1;
+    if (a < d) {
+      x = draft[(size_t)s * d + a];
+      invalid = x < 0 || x >= V;
+      if (!invalid) {
+        const int rp = s * rows_per_seq + a, rq = s * rows_per_seq + d + 1 + a;
+        const float zp = zval(p[((size_t)s * (d + 1) + a) * V + x], T);
+        const float zq = zval(q[((size_t)s * d + a) * V + x], T);
+        const uint64_t Wx = int_weight(__fsub_rn(zp, row_zmax(row_key[rp], T)));
+        const uint64_t Wqx = int_weight(__fsub_rn(zq, row_zmax(row_key[rq], T)));
+        const uint64_t S = row_sum[rp], Sq = row_sum[rq];
+        uint32_t U[4];
+        uniforms(seed, e0 + (uint64_t)a, sid, U);
+        bool acc;
+        if (Wqx == 0ull) {
+          acc = Wx > 0ull;
+        } else {
+          const u128 lhs = (u128)U[0] * (u128)Wqx * (u128)S;
+          const u128 rhs = ((u128)Wx << 32) * (u128)Sq;
+          acc = lhs < rhs;
+        }
+        U1 = U[1];
+        stop = !acc;
+      } else {
+        stop = true;
+      }
+    } else if (a == d) {
+      uint32_t U[4];
+      uniforms(seed, e0 + (uint64_t)d, sid, U);
+      U1 = U[1];
+      stop = true;  // the bonus: every draft accepted
     }
-    const int rp = s * rows_per_seq + a, rq = s * rows_per_seq + d + 1 + a;
-    const float zp = __fdiv_rn(p[((size_t)s * (d + 1) + a) * V + x], T);
-    const float zq = __fdiv_rn(q[((size_t)s * d + a) * V + x], T);
-    const uint64_t Wx = int_weight(__fsub_rn(zp, row_max[rp]));
-    const uint64_t Wqx = int_weight(__fsub_rn(zq, row_max[rq]));
-    const uint64_t S = row_sum[rp], Sq = row_sum[rq];
-    uint32_t U[4];
-    uniforms(seed, e0 + (uint64_t)a, sid, U);
-    bool acc;
-    if (Wqx == 0ull) {
-      acc = Wx > 0ull;
-    } else {
-      const u128 lhs = (u128)U[0] * (u128)Wqx * (u128)S;
-      const u128 rhs = ((u128)Wx << 32) * (u128)Sq;
-      acc = lhs < rhs;
+    const unsigned ball = __ballot_sync(0xffffffffu, a <= d && stop);
+    if (a <= d) e[a] = -1;
+    if (ball == 0u) {  // all 32 positions accepted
+      e[a] = x;
+      continue;
     }
-    if (!acc) {
-      decision[s] = make_int4(a, a, (int)U[1], 1);
-      n_acc[s] = a;
-      return;
+    const int f = __ffs(ball) - 1;  // first stopping lane
+    if (lane < f) e[a] = x;
+    if (lane == f) {
+      if (invalid) {
+        atomicOr(err, ERR_TOKEN);
+        decision[s] = make_int4(a, a, 0, 0);
+        n_acc[s] = -1;
+      } else {
+        decision[s] = make_int4(a, a, (int)U1, a == d ? 2 : 1);
+        n_acc[s] = a;
+      }
     }
-    e[a] = x;
+    for (int i = base + 32 + lane; i <= d; i += 32) e[i] = -1;
+    return;
   }
-  uint32_t U[4];
-  uniforms(seed, e0 + (uint64_t)d, sid, U);
-  decision[s] = make_int4(d, d, (int)U[1], 2);
-  n_acc[s] = d;
 }
 
 // ---------------------------------------------------------------------------
@@ -294,22 +353,36 @@ __device__ __forceinline__ u128 shfl_up_u128(u128 v, int delta) {
   return ((u128)hi << 64) | lo;
 }
 
-__device__ __forceinline__ u128 mass_of(int mode, const float* prow, const float* qrow,
-                                        int v, float T, float mp, float mq, uint64_t S,
-                                        uint64_t Sq) {
-  const uint64_t W = int_weight(__fsub_rn(__fdiv_rn(prow[v], T), mp));
+// The residual (mode 1: max(0, W Sq - Wq S)) or target (mode 2: W) mass of
+// one token from its two logits.
+__device__ __forceinline__ u128 mass_from(int mode, float lp, float lq, float T, float mp,
+                                          float mq, uint64_t S, uint64_t Sq) {
+  const uint64_t W = int_weight(__fsub_rn(zval(lp, T), mp));
   if (mode == 2) return (u128)W;
-  const uint64_t Wq = int_weight(__fsub_rn(__fdiv_rn(qrow[v], T), mq));
+  const uint64_t Wq = int_weight(__fsub_rn(zval(lq, T), mq));
   const u128 a = (u128)W * Sq, b = (u128)Wq * S;
   return a > b ? a - b : (u128)0;
 }
+
+constexpr int RS_ILP = 8;  // tokens per lane whose loads are issued before any is used
 
 // The sum of the masses of [v0, v1) over one warp (every lane gets it).
 __device__ __forceinline__ u128 warp_mass(int mode, const float* prow, const float* qrow, int v0,
                                           int v1, float T, float mp, float mq, uint64_t S,
                                           uint64_t Sq, int lane) {
   u128 acc = 0;
-  for (int v = v0 + lane; v < v1; v += 32) acc += mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq);
+  for (int vb = v0 + lane; vb < v1; vb += 32 * RS_ILP) {
+    float lp[RS_ILP], lq[RS_ILP];
+#pragma unroll
+    for (int u = 0; u < RS_ILP; u++) {
+      const int v = vb + 32 * u;
+      lp[u] = v < v1 ? prow[v] : 0.0f;
+      lq[u] = v < v1 && mode == 1 ? qrow[v] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < RS_ILP; u++)
+      if (vb + 32 * u < v1) acc += mass_from(mode, lp[u], lq[u], T, mp, mq, S, Sq);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += shfl_u128(acc, lane ^ off);
   return acc;
@@ -317,7 +390,7 @@ __device__ __forceinline__ u128 warp_mass(int mode, const float* prow, const flo
 
 __global__ void __launch_bounds__(RS_THREADS)
 resample_kernel(const float* __restrict__ p, const float* __restrict__ q, int n_seq, int d,
-                int V, float T, const float* __restrict__ row_max,
+                int V, float T, const uint32_t* __restrict__ row_key,
                 const unsigned long long* __restrict__ row_sum,
                 const int4* __restrict__ decision, int32_t* __restrict__ em,
                 uint32_t* __restrict__ err) {
@@ -334,8 +407,8 @@ resample_kernel(const float* __restrict__ p, const float* __restrict__ q, int n_
   const int rq = s * rows_per_seq + d + 1 + (row < d ? row : 0);
   const float* prow = p + ((size_t)s * (d + 1) + row) * V;
   const float* qrow = mode == 1 ? q + ((size_t)s * d + row) * V : nullptr;
-  const float mp = row_max[rp];
-  const float mq = mode == 1 ? row_max[rq] : 0.0f;
+  const float mp = row_zmax(row_key[rp], T);
+  const float mq = mode == 1 ? row_zmax(row_key[rq], T) : 0.0f;
   const uint64_t S = row_sum[rp];
   const uint64_t Sq = mode == 1 ? row_sum[rq] : 0ull;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -413,7 +486,8 @@ resample_kernel(const float* __restrict__ p, const float* __restrict__ q, int n_
   int found = -1;
   for (int vb = w0; vb < w1 && found < 0; vb += 32) {
     const int v = vb + lane;
-    u128 m = v < w1 ? mass_of(mode, prow, qrow, v, T, mp, mq, S, Sq) : (u128)0;
+    u128 m = v < w1 ? mass_from(mode, prow[v], mode == 1 ? qrow[v] : 0.0f, T, mp, mq, S, Sq)
+                    : (u128)0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {  // inclusive warp prefix
       const u128 o = shfl_up_u128(m, off);
@@ -527,38 +601,35 @@ int launch_accept_stochastic(const float* p, const float* q, const int32_t* draf
                              int32_t* emitted, const StochScratch& scr, uint32_t* err,
                              cudaStream_t st) {
   const size_t nrows = stoch_rows_needed(n_seq, d);
-  if (nrows * ST_CLUSTER > (size_t)INT32_MAX)
+  const int nseg = st_segments(V);
+  if (nrows * (size_t)nseg > (size_t)INT32_MAX || (size_t)n_seq * RS_CL > (size_t)INT32_MAX)
     return fail(SPEC_E_SHAPE, "stochastic accept: n_seq * (2d + 1) too large");
   if (nrows > scr.rows_cap || (size_t)n_seq > scr.seq_cap)
     return fail(SPEC_E_SHAPE, "stochastic accept: scratch too small");
-  const int slice = (V + ST_CLUSTER - 1) / ST_CLUSTER;
-  const size_t smem = (size_t)slice * sizeof(float);
-  if (smem > ST_MAX_SMEM) return fail(SPEC_E_SHAPE, "stochastic accept: vocabulary too large");
+  // the per-row maxima (keys) and sums are accumulated by atomics from zero
+  CUDA_TRY(cudaMemsetAsync(scr.row_key, 0, nrows * sizeof(uint32_t), st));
+  CUDA_TRY(cudaMemsetAsync(scr.row_sum, 0, nrows * sizeof(unsigned long long), st));
+  const unsigned grid = (unsigned)(nrows * (size_t)nseg);
+  row_max_kernel<<<grid, ST_THREADS, 0, st>>>(p, q, d, V, nseg, scr.row_key, err);
+  row_sum_kernel<<<grid, ST_THREADS, 0, st>>>(p, q, d, V, nseg, T, scr.row_key, scr.row_sum);
+  decide_kernel<<<(n_seq + DC_WARPS - 1) / DC_WARPS, DC_WARPS * 32, 0, st>>>(
+      p, q, draft, n_seq, d, V, T, seed, seq_ids, emit_idx, emit_by_slot, n_slots, scr.row_key,
+      scr.row_sum, scr.decision, n_acc, emitted, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("stochastic accept: ") + cudaGetErrorString(e));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(nrows * ST_CLUSTER));
-  cfg.blockDim = dim3(ST_THREADS);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = ST_CLUSTER;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, row_stats_kernel, p, q, d, V, T, scr.row_max,
-                                     scr.row_sum, err);
-  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("row stats: ") + cudaGetErrorString(e));
-  decide_kernel<<<(n_seq + 63) / 64, 64, 0, st>>>(p, q, draft, n_seq, d, V, T, seed, seq_ids,
-                                                  emit_idx, emit_by_slot, n_slots, scr.row_max, scr.row_sum,
-                                                  scr.decision, n_acc, emitted, err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("stochastic accept: ") + cudaGetErrorString(e));
   cfg.gridDim = dim3((unsigned)(n_seq * RS_CL));
   cfg.blockDim = dim3(RS_THREADS);
   cfg.dynamicSmemBytes = 0;
   attr[0].val.clusterDim.x = RS_CL;
-  e = cudaLaunchKernelEx(&cfg, resample_kernel, p, q, n_seq, d, V, T, (const float*)scr.row_max,
+  e = cudaLaunchKernelEx(&cfg, resample_kernel, p, q, n_seq, d, V, T, (const uint32_t*)scr.row_key,
                          (const unsigned long long*)scr.row_sum, (const int4*)scr.decision, emitted,
                          err);
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("stochastic accept: ") + cudaGetErrorString(e));
@@ -610,9 +681,7 @@ void stoch_finalize(int n_seq, int d, int32_t* n_acc, int32_t* emitted, uint64_t
                                                              err);
 }
 
-void accept_init_attrs() {
-  cudaFuncSetAttribute(row_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ST_MAX_SMEM);
-}
+void accept_init_attrs() {}
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the standalone stochastic accept.
@@ -629,7 +698,7 @@ constexpr int NOALLOC_MAX_ROWS = 4096;  // n_seq * (2d + 1)
 constexpr int NOALLOC_MAX_SEQS = 1024;
 
 struct NoAllocScratch {
-  float row_max[NOALLOC_MAX_ROWS];
+  uint32_t row_key[NOALLOC_MAX_ROWS];
   unsigned long long row_sum[NOALLOC_MAX_ROWS];
   int4 decision[NOALLOC_MAX_SEQS];
   uint32_t err;
@@ -683,7 +752,7 @@ extern "C" int spec_accept_stochastic_noalloc(const float* p_logits, const float
   // the array keeps the previous call's contents: the error word must start at zero
   CUDA_TRY(cudaMemsetAsync(&sp->err, 0, sizeof(uint32_t), st));
   StochScratch scr;
-  scr.row_max = sp->row_max;
+  scr.row_key = sp->row_key;
   scr.row_sum = sp->row_sum;
   scr.decision = sp->decision;
   scr.rows_cap = NOALLOC_MAX_ROWS;

@@ -107,7 +107,12 @@ static int workspace_get(size_t rows, size_t seqs, Workspace** out) {
       cudaFree(w.st_base);
       w.st_base = nullptr;
     }
-    size_t bytes = rows * (sizeof(float) + sizeof(unsigned long long)) + seqs * sizeof(int4) + 64;
+    // each part starts on a 256-byte boundary (the decisions are 16-byte
+    // int4 stores, whatever the row count)
+    auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+    const size_t sum_bytes = up(rows * sizeof(unsigned long long));
+    const size_t dec_bytes = up(seqs * sizeof(int4));
+    const size_t bytes = sum_bytes + dec_bytes + up(rows * sizeof(uint32_t));
     if (cudaMalloc(&w.st_base, bytes) != cudaSuccess) {
       cudaGetLastError();
       w.st = StochScratch();
@@ -115,10 +120,8 @@ static int workspace_get(size_t rows, size_t seqs, Workspace** out) {
     }
     char* p = (char*)w.st_base;
     w.st.row_sum = (unsigned long long*)p;
-    p += rows * sizeof(unsigned long long);
-    w.st.decision = (int4*)p;
-    p += seqs * sizeof(int4);
-    w.st.row_max = (float*)p;
+    w.st.decision = (int4*)(p + sum_bytes);
+    w.st.row_key = (uint32_t*)(p + sum_bytes + dec_bytes);
     w.st.rows_cap = rows;
     w.st.seq_cap = seqs;
   }
@@ -497,7 +500,7 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
   }
   m->sscr.rows_cap = stoch_rows_needed(D.max_seqs, D.max_nt - 1);
   m->sscr.seq_cap = D.max_seqs;
-  TRY(dalloc_t(m, &m->sscr.row_max, m->sscr.rows_cap));
+  TRY(dalloc_t(m, &m->sscr.row_key, m->sscr.rows_cap));
   TRY(dalloc_t(m, &m->sscr.row_sum, m->sscr.rows_cap));
   TRY(dalloc_t(m, &m->sscr.decision, m->sscr.seq_cap));
   if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
@@ -1093,6 +1096,7 @@ extern "C" int spec_accept_stochastic(const float* p_logits, const float* q_logi
   if (n_seq < 1 || d < 0 || V < 1) return fail(SPEC_E_SHAPE, "n_seq >= 1, d >= 0, V >= 1 required");
   if (!(temperature > 0.0f) || !std::isfinite(temperature))
     return fail(SPEC_E_INVALID, "temperature must be finite and > 0");
+  init_attrs_once();  // the row-statistics kernel's shared-memory limit
   Workspace* w = nullptr;
   int rc = workspace_get(stoch_rows_needed(n_seq, d), n_seq, &w);
   if (rc != SPEC_OK) return rc;

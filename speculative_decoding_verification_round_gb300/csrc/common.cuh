@@ -187,7 +187,7 @@ int attn_launch(const __half* q, const __half* kcache, const __half* vcache,
 // accept (accept.cu)
 // ---------------------------------------------------------------------------
 struct StochScratch {
-  float* row_max = nullptr;            // [n_seq][2d+1]
+  uint32_t* row_key = nullptr;         // [n_seq][2d+1]: order key of the row's largest logit
   unsigned long long* row_sum = nullptr;  // [n_seq][2d+1]
   int4* decision = nullptr;            // [n_seq]: (a, row, U2, flags)
   size_t rows_cap = 0;

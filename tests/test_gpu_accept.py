@@ -223,3 +223,32 @@ def test_stochastic_v16_distribution_chi2(orc, dev):
     mask = exp0 * n > 5
     stat = (((counts - exp0 * n) ** 2) / (exp0 * n))[mask].sum()
     assert stat < chi2.ppf(1 - 1e-3, mask.sum() - 1), (stat, counts, exp0 * n)
+
+
+def test_stochastic_accept_first_call_in_fresh_process():
+    """The standalone accept works as the first call a process makes (no
+    model or matrix created before it sets the kernels' attributes)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import numpy as np, torch\n"
+        "import speculative_decoding_verification_round_gb300 as sv\n"
+        "dev = torch.device('cuda:0')\n"
+        "g = np.random.default_rng(5)\n"
+        "n, d, V = 3, 4, 50000\n"
+        "p = torch.from_numpy(g.standard_normal((n, d + 1, V), dtype=np.float32)).to(dev)\n"
+        "q = torch.from_numpy(g.standard_normal((n, d, V), dtype=np.float32)).to(dev)\n"
+        "dr = torch.zeros((n, d), dtype=torch.int32, device=dev)\n"
+        "sid = torch.arange(n, dtype=torch.int32, device=dev)\n"
+        "ei = torch.zeros(n, dtype=torch.int64, device=dev)\n"
+        "na = torch.empty(n, dtype=torch.int32, device=dev)\n"
+        "em = torch.empty((n, d + 1), dtype=torch.int32, device=dev)\n"
+        "sv.spec_accept_stochastic(p, q, dr, n, d, V, 1.0, 7, sid, ei, na, em)\n"
+        "torch.cuda.synchronize()\n"
+        "assert sv.spec_error_check(None) == 0\n"
+        "print('ok', na.cpu().tolist())\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
