@@ -132,7 +132,7 @@ int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
  * instructions whatever R is, so a row's result does not depend on the other
  * rows; it differs from spec_linear_q's in the last bits (that kernel keeps
  * each 32-block's sum exact and applies the scale in fp32).
- * 1 <= R <= max_rows (launched in blocks of 256 rows). */
+ * 1 <= R <= max_rows (launched in blocks of 192 rows). */
 int spec_linear_q_tc(const spec_qmat* w, const uint16_t* x, int R, float* y,
                      void* stream);
 

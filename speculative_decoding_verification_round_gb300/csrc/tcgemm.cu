@@ -7,21 +7,23 @@
 // weight stream but by the contraction itself (2 x 192 flops per weight), so
 // it runs on tcgen05.mma with the activation rows as the N dimension:
 //
-//   * a CTA owns 128 weight rows (4 pairs of the packed streaming layout, one
-//     TMEM lane each) and one of S segments of K; its accumulator is
-//     128 x Npad fp32 in tensor memory (Npad = the rows rounded up to 16);
+//   * a CTA owns 256 weight rows (8 pairs of the packed streaming layout) as
+//     two 128-row halves, each with its own 128 x Npad fp32 accumulator in
+//     tensor memory (one TMEM lane per weight row; Npad = the rows rounded up
+//     to 16), and one of S segments of K.  Both halves use each activation
+//     tile, so a tile and every handshake of a chunk serve twice the MMAs;
 //   * warp 0 streams the packed weight records into a shared-memory ring with
 //     TMA bulk copies; warp 1 loads the activation tile of each 64-k chunk
 //     with a 2-D TMA tensor copy (128-byte swizzle, rows past R read as zero);
-//   * warps 3-6 dequantise each chunk into TWO fp16 A tiles in the UMMA
-//     K-major 128-byte-swizzle layout, hi = fp16(q * scale) and lo =
+//   * warps 3-10 dequantise each chunk into TWO fp16 A tiles per half in the
+//     UMMA K-major 128-byte-swizzle layout, hi = fp16(q * scale) and lo =
 //     fp16(q * scale - hi): q * scale has at most 11 + 8 significant bits,
 //     so lo holds the rest exactly and hi + lo IS the weight -- every
 //     product the tensor core forms is exact, as in the oracle;
-//   * one thread of warp 2 issues eight tcgen05.mma (M 128, N Npad, K 16:
-//     hi and lo for each 16-k step) per chunk into the one accumulator and
-//     commits them to the stage's "empty" barrier;
-//   * after the last chunk the same four warps read the accumulator back
+//   * one thread of warp 2 issues sixteen tcgen05.mma (M 128, N Npad, K 16:
+//     hi and lo of each half for each 16-k step) per chunk and commits them
+//     to the stages' "empty" barriers;
+//   * after the last chunk the same eight warps read the accumulators back
 //     (tcgen05.ld), add the K segments in segment order (the last CTA of a
 //     tile, by a ticket) and run the fused epilogue (store, residual add,
 //     SwiGLU, RoPE + KV write, LM head logits + argmax).
@@ -44,14 +46,20 @@
 
 namespace {
 
-constexpr int TC_M = 128;           // weight rows of a CTA
+constexpr int TC_M = 128;           // weight rows of an accumulator (the MMA's M)
+constexpr int TC_HALVES = 2;        // accumulators of a CTA
+constexpr int TC_ROWS = TC_M * TC_HALVES;  // weight rows of a CTA
+constexpr int TC_PAIRS = TC_ROWS / 32;     // packed pairs of a CTA
 constexpr int TC_THREADS = 352;     // 11 warps
 constexpr int TC_EPI_WARP0 = 3;     // warps 3..10: dequant, then epilogue
-constexpr int TC_EPI_THREADS = 256; // 8 warps: two per TMEM lane quadrant
+constexpr int TC_EPI_THREADS = 256; // 8 warps: two per TMEM lane quadrant (one per half)
 constexpr int EW = 16;              // epilogue columns per TMEM load
 constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16 (one of hi / lo)
-constexpr int TC_MAX_ST = 6;    // stages of either ring (A: hi + lo tiles; B: activation tiles)
+constexpr int TC_A_STAGE = TC_HALVES * 2 * TC_A_BYTES;  // hi and lo of both halves
+constexpr int TC_A_ST = 2;      // A stages
+constexpr int TC_MAX_ST = 6;    // stages of the activation ring
 constexpr int TC_MAX_RAW = 8;
+constexpr int TC_MAX_R = 192;   // activation rows of one launch (Npad <= 192)
 
 template <int QT>
 struct TcRec {  // the packed record of one (pair, 64-k chunk): see linear.cu
@@ -64,9 +72,10 @@ struct TcRec {  // the packed record of one (pair, 64-k chunk): see linear.cu
 struct TcArgs {
   const uint8_t* rec;  // [n_pairs][nch][rec]
   int N, K, nch, n_pairs, n_mt, S, R, Npad, tmem_cols;
-  int a_stages, b_stages, raw_depth;  // ring depths: A (hi + lo), activations, raw records
+  int acc_stride;       // TMEM columns between the two accumulators
+  int b_stages, raw_depth;  // ring depths: activations, raw records (A: TC_A_ST)
   LinEpi epi;
-  float* part;          // [S][n_mt][Npad][128] K-split partials
+  float* part;          // [S][n_mt][Npad][256] K-split partials
   unsigned* tickets;    // [n_mt] K-split tickets, then [1] argmax ticket
   unsigned long long* amax_key;  // [Npad] LM head: packed (value, index) maxima
   uint32_t* err;
@@ -305,7 +314,7 @@ __device__ __forceinline__ void dequant_tile(const unsigned char* raw, unsigned 
 // Epilogue of EW finished columns (activation rows col0..col0+EW-1) of this
 // thread's weight row n: v[c] is the sum for row col0 + c.
 __device__ __forceinline__ void tc_epilogue(const TcArgs& a, int n, int col0, const float (&v)[EW],
-                                              int lane, uint32_t* s_key, int quad) {
+                                              int lane, uint32_t* s_key, int slot) {
   const LinEpi& e = a.epi;
   const bool real = n < a.N;
   switch (e.kind) {
@@ -389,7 +398,7 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, int n, int col0, co
     }
     case EPI_LMHEAD: {
       // the CTA's best (value, lowest id) of each column: a warp reduction
-      // of order-preserving keys, then the four warps through shared memory
+      // of order-preserving keys, then the eight warps through shared memory
       bool bad = false;
 #pragma unroll
       for (int c = 0; c < EW; c++) {
@@ -402,8 +411,8 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, int n, int col0, co
         const uint32_t id = key == kmax && real ? (uint32_t)n : 0xffffffffu;
         const uint32_t imin = __reduce_min_sync(0xffffffffu, id);
         if (lane == 0) {
-          s_key[(quad * 2) * 256 + r] = kmax;
-          s_key[(quad * 2 + 1) * 256 + r] = imin;
+          s_key[(slot * 2) * TC_MAX_R + r] = kmax;
+          s_key[(slot * 2 + 1) * TC_MAX_R + r] = imin;
         }
       }
       if (bad) atomicOr(e.err, ERR_NONFINITE);
@@ -419,38 +428,40 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   extern __shared__ unsigned char smem_dyn[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) unsigned long long s_bar[4 * TC_MAX_ST + 2 * TC_MAX_RAW + 1];
+  __shared__ __align__(8) unsigned long long s_bar[2 * TC_A_ST + 2 * TC_MAX_ST + 2 * TC_MAX_RAW + 1];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_last;
-  __shared__ uint32_t s_key[8 * 256];  // LM head: [warp quad][key, id][column]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, seg = blockIdx.y;
-  const int STA = a.a_stages, STB = a.b_stages, RAWN = a.raw_depth;
+  const int STB = a.b_stages, RAWN = a.raw_depth;
   const int B_BYTES = a.Npad * 128;
-  unsigned char* A0 = smem;  // [STA][hi, lo] tiles
-  unsigned char* B0 = smem + STA * 2 * TC_A_BYTES;
+  unsigned char* A0 = smem;  // [TC_A_ST][half][hi, lo] tiles
+  unsigned char* B0 = smem + TC_A_ST * TC_A_STAGE;
   unsigned char* RAW0 = B0 + STB * B_BYTES;
-  const int RAW_BYTES = 4 * RC::BYTES;
-  // barriers: a_full[STA], b_full[STB], a_empty[STA], b_empty[STB], raw_full[RAW],
+  const int RAW_BYTES = TC_PAIRS * RC::BYTES;
+  // LM head: the best (key, id) of each column from each epilogue warp,
+  // [half * 4 + quadrant][key, id][column], in the A ring once every MMA is done
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(A0);
+  // barriers: a_full[A], a_empty[A], b_full[STB], b_empty[STB], raw_full[RAW],
   // raw_empty[RAW], acc.  The two rings are freed separately (one commit
   // each), so activation tiles are fetched a full ring ahead of their MMAs.
   const uint32_t bar0 = smem_u32(s_bar);
   auto A_FULL = [&](int s) { return bar0 + 8 * s; };
-  auto B_FULL = [&](int s) { return bar0 + 8 * (TC_MAX_ST + s); };
-  auto A_EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_MAX_ST + s); };
-  auto B_EMPTY = [&](int s) { return bar0 + 8 * (3 * TC_MAX_ST + s); };
-  auto RAW_FULL = [&](int r) { return bar0 + 8 * (4 * TC_MAX_ST + r); };
-  auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (4 * TC_MAX_ST + TC_MAX_RAW + r); };
-  const uint32_t ACC = bar0 + 8 * (4 * TC_MAX_ST + 2 * TC_MAX_RAW);
+  auto A_EMPTY = [&](int s) { return bar0 + 8 * (TC_A_ST + s); };
+  auto B_FULL = [&](int s) { return bar0 + 8 * (2 * TC_A_ST + s); };
+  auto B_EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_A_ST + TC_MAX_ST + s); };
+  auto RAW_FULL = [&](int r) { return bar0 + 8 * (2 * TC_A_ST + 2 * TC_MAX_ST + r); };
+  auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (2 * TC_A_ST + 2 * TC_MAX_ST + TC_MAX_RAW + r); };
+  const uint32_t ACC = bar0 + 8 * (2 * TC_A_ST + 2 * TC_MAX_ST + 2 * TC_MAX_RAW);
 
   // this CTA's K range (chunks) and pairs
   const int c0 = (int)((long long)seg * a.nch / a.S);
   const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c0;
-  const int pair0 = mt * 4;
+  const int pair0 = mt * TC_PAIRS;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STA; s++) {
+    for (int s = 0; s < TC_A_ST; s++) {
       mbar_init(A_FULL(s), TC_EPI_THREADS);
       mbar_init(A_EMPTY(s), 1);
     }
@@ -466,7 +477,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_abort = 0;
   }
-  if (warp == 2) {  // tensor memory for the accumulator: whole warp
+  if (warp == 2) {  // tensor memory for the accumulators: whole warp
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&s_tmem)),
                  "r"(a.tmem_cols)
@@ -488,6 +499,8 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     // ---- weight records: one bulk copy per pair and chunk (weights are
     // ---- constant: this starts before the grid dependency resolves)
     if (lane == 0) {
+      int np = 0;
+      for (int p = 0; p < TC_PAIRS; p++) np += pair0 + p < a.n_pairs;
       for (int c = 0; c < nc && !*abort_flag; c++) {
         const int r = c % RAWN, ur = c / RAWN;
         if (ur > 0 && !mbar_wait(RAW_EMPTY(r), (ur - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
@@ -495,14 +508,11 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           break;
         }
         issued = c + 1;
-        int np = 0;
-        for (int p = 0; p < 4; p++) np += pair0 + p < a.n_pairs;
         mbar_expect_tx(RAW_FULL(r), (uint32_t)(np * RC::BYTES));
-        for (int p = 0; p < 4; p++)
-          if (pair0 + p < a.n_pairs)
-            bulk_copy(smem_u32(RAW0 + r * RAW_BYTES + p * RC::BYTES),
-                      a.rec + ((size_t)(pair0 + p) * a.nch + c0 + c) * RC::BYTES, RC::BYTES,
-                      RAW_FULL(r));
+        for (int p = 0; p < np; p++)
+          bulk_copy(smem_u32(RAW0 + r * RAW_BYTES + p * RC::BYTES),
+                    a.rec + ((size_t)(pair0 + p) * a.nch + c0 + c) * RC::BYTES, RC::BYTES,
+                    RAW_FULL(r));
       }
     }
     grid_dep_wait();
@@ -528,20 +538,25 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       const uint32_t idesc = idesc_f16(a.Npad);
       int c = 0;
       for (; c < nc && !*abort_flag; c++) {
-        const int sa = c % STA, ua = c / STA, sb = c % STB, ub = c / STB;
+        const int sa = c % TC_A_ST, ua = c / TC_A_ST, sb = c % STB, ub = c / STB;
         if (!mbar_wait(A_FULL(sa), ua & 1, LIN_WAIT_TRIES, abort_flag) ||
             !mbar_wait(B_FULL(sb), ub & 1, LIN_WAIT_TRIES, abort_flag)) {
           give_up();
           break;
         }
         tc_fence_after();
-        const uint64_t ah = smem_desc_sw128(smem_u32(A0 + sa * 2 * TC_A_BYTES));
-        const uint64_t al = smem_desc_sw128(smem_u32(A0 + (sa * 2 + 1) * TC_A_BYTES));
         const uint64_t bd = smem_desc_sw128(smem_u32(B0 + sb * B_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
-          tc_mma(tmem, ah + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-          tc_mma(tmem, al + 2 * kk, bd + 2 * kk, idesc, 1u);
+        for (int h = 0; h < TC_HALVES; h++) {
+          const unsigned char* at = A0 + sa * TC_A_STAGE + h * 2 * TC_A_BYTES;
+          const uint64_t ah = smem_desc_sw128(smem_u32(at));
+          const uint64_t al = smem_desc_sw128(smem_u32(at + TC_A_BYTES));
+          const uint32_t d = tmem + (uint32_t)(h * a.acc_stride);
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
+            tc_mma(d, ah + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            tc_mma(d, al + 2 * kk, bd + 2 * kk, idesc, 1u);
+          }
         }
         tc_commit(A_EMPTY(sa));
         tc_commit(B_EMPTY(sb));
@@ -549,11 +564,12 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       tc_commit(ACC);  // completes when every MMA issued above has
     }
   } else {
-    // ---- dequant (warps 3..10: one 16-row tile of the CTA's eight each)
+    // ---- dequant (warps 3..10: 16-row tile t of each half's eight; pair
+    // ---- pc of the half)
     const int pc = (warp - TC_EPI_WARP0) >> 1, tile = (warp - TC_EPI_WARP0) & 1;
     grid_dep_wait();
     for (int c = 0; c < nc && !*abort_flag; c++) {
-      const int r = c % RAWN, ur = c / RAWN, s = c % STA, us = c / STA;
+      const int r = c % RAWN, ur = c / RAWN, s = c % TC_A_ST, us = c / TC_A_ST;
       // the first wait's budget is the one a caller may shorten (test hook)
       bool ok = mbar_wait(RAW_FULL(r), ur & 1, c == 0 ? a.wait_tries : LIN_WAIT_TRIES, abort_flag);
       if (ok && us > 0) ok = mbar_wait(A_EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag);
@@ -561,32 +577,37 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         give_up();
         break;
       }
-      unsigned char* at = A0 + s * 2 * TC_A_BYTES;
-      if (pair0 + pc < a.n_pairs) {
-        dequant_tile<QT>(RAW0 + r * RAW_BYTES + pc * RC::BYTES, at, at + TC_A_BYTES, pc, tile, lane);
-      } else {  // rows past the matrix: zeros
-        for (int q = lane; q < 16 * 8; q += 32) {
-          const int rr = 32 * pc + 16 * tile + q / 8, u = q % 8;
-          *reinterpret_cast<uint4*>(at + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(at + TC_A_BYTES + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int h = 0; h < TC_HALVES; h++) {
+        unsigned char* at = A0 + s * TC_A_STAGE + h * 2 * TC_A_BYTES;
+        const int pp = h * (TC_PAIRS / TC_HALVES) + pc;  // pair of the CTA
+        if (pair0 + pp < a.n_pairs) {
+          dequant_tile<QT>(RAW0 + r * RAW_BYTES + pp * RC::BYTES, at, at + TC_A_BYTES, pc, tile,
+                           lane);
+        } else {  // rows past the matrix: zeros
+          for (int q = lane; q < 16 * 8; q += 32) {
+            const int rr = 32 * pc + 16 * tile + q / 8, u = q % 8;
+            *reinterpret_cast<uint4*>(at + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(at + TC_A_BYTES + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
+          }
         }
       }
       mbar_arrive(RAW_EMPTY(r));
-      fence_proxy_async();  // the A tile, to the tensor core's proxy
+      fence_proxy_async();  // the A tiles, to the tensor core's proxy
       mbar_arrive(A_FULL(s));
     }
   }
   grid_dep_launch();
 
-  // ---- epilogue: warps 3..10; warp w reads TMEM lane quadrant w % 4 and
-  // ---- every other group of EW columns (the two warps of a quadrant split
-  // ---- the columns)
+  // ---- epilogue: warps 3..10; warp w reads TMEM lane quadrant w % 4 of
+  // ---- half (w - 3) / 4, every column
   if (warp >= TC_EPI_WARP0) {
     const int quad = warp & 3, half = (warp - TC_EPI_WARP0) >> 2;
+    const int slot = half * 4 + quad;
     const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..255
-    const int m = 32 * quad + lane;  // TMEM lane = weight row of the tile
-    const int n = mt * TC_M + m;
-    const uint32_t trow = tmem + ((uint32_t)(32 * quad) << 16);
+    const int m = TC_M * half + 32 * quad + lane;    // weight row of the CTA
+    const int n = mt * TC_ROWS + m;
+    const uint32_t trow = tmem + (uint32_t)(half * a.acc_stride) + ((uint32_t)(32 * quad) << 16);
     const bool acc_ok = mbar_wait(ACC, 0, LIN_WAIT_TRIES);
     if (!acc_ok) give_up();
     tc_fence_after();
@@ -595,12 +616,12 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     // segments in order
     bool finisher = true;
     if (a.S > 1) {
-      for (int col0 = half * EW; col0 < a.Npad; col0 += 2 * EW) {
+      for (int col0 = 0; col0 < a.Npad; col0 += EW) {
         uint32_t v[EW];
         tc_ld16(trow + col0, v);
-        float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * TC_M + m;
+        float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * TC_ROWS + m;
 #pragma unroll
-        for (int c = 0; c < EW; c++) dst[(size_t)c * TC_M] = __uint_as_float(v[c]);
+        for (int c = 0; c < EW; c++) dst[(size_t)c * TC_ROWS] = __uint_as_float(v[c]);
       }
       epi_bar();
       if (et == 0) {
@@ -613,23 +634,23 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       finisher = s_last != 0;
     }
     if (finisher) {
-      for (int col0 = half * EW; col0 < a.Npad; col0 += 2 * EW) {
+      for (int col0 = 0; col0 < a.Npad; col0 += EW) {
         float v[EW];
         if (a.S > 1) {
-          const float* src = a.part + ((size_t)mt * a.Npad + col0) * TC_M + m;
-          const size_t step = (size_t)a.n_mt * a.Npad * TC_M;
+          const float* src = a.part + ((size_t)mt * a.Npad + col0) * TC_ROWS + m;
+          const size_t step = (size_t)a.n_mt * a.Npad * TC_ROWS;
 #pragma unroll
-          for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * TC_M);
+          for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * TC_ROWS);
           for (int s2 = 1; s2 < a.S; s2++)
 #pragma unroll
-            for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_M);
+            for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_ROWS);
         } else {
           uint32_t u[EW];
           tc_ld16(trow + col0, u);
 #pragma unroll
           for (int c = 0; c < EW; c++) v[c] = __uint_as_float(u[c]);
         }
-        if (!aborted) tc_epilogue(a, n, col0, v, lane, s_key, quad);
+        if (!aborted) tc_epilogue(a, n, col0, v, lane, s_key, slot);
       }
       if (a.S > 1 && et == 0) a.tickets[mt] = 0u;
       if (a.epi.kind == EPI_LMHEAD) {
@@ -638,9 +659,9 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         // an aborted CTA still takes its ticket, so the state is reset
         epi_bar();
         for (int r = et; r < a.R && !aborted; r += TC_EPI_THREADS) {
-          uint32_t bk = s_key[r], bi = s_key[256 + r];
-          for (int q = 1; q < 4; q++) {
-            const uint32_t k2 = s_key[(2 * q) * 256 + r], i2 = s_key[(2 * q + 1) * 256 + r];
+          uint32_t bk = s_key[r], bi = s_key[TC_MAX_R + r];
+          for (int q = 1; q < 2 * 4; q++) {
+            const uint32_t k2 = s_key[(2 * q) * TC_MAX_R + r], i2 = s_key[(2 * q + 1) * TC_MAX_R + r];
             if (k2 > bk || (k2 == bk && i2 < bi)) {
               bk = k2;
               bi = i2;
@@ -700,26 +721,26 @@ int tc_rec_bytes(int qtype) {
   return qtype == 4 ? TcRec<4>::BYTES : (qtype == 6 ? TcRec<6>::BYTES : TcRec<8>::BYTES);
 }
 
-constexpr int TC_SMEM_MAX = 227 * 1024 - 10 * 1024;  // dynamic part (the static part is ~9 KB)
+constexpr int TC_SMEM_MAX = 227 * 1024 - 2 * 1024;  // dynamic part (the static part is < 1 KB)
 
-// Ring depths of a launch that fit the shared memory: the activation ring
-// as deep as possible (it hides the L2 latency of a tile, fetched when the
-// MMAs of the chunk a ring earlier complete), three A stages (the dequant
-// of a chunk overlaps two chunks of MMAs), then the raw-record ring.
-void tc_rings(int qtype, int Npad, int* sta, int* stb, int* raw) {
-  const int raw_bytes = 4 * tc_rec_bytes(qtype), b_bytes = Npad * 128;
-  *sta = 3;
-  *raw = 3;
+// Ring depths of a launch that fit the shared memory: two A stages (64 KB
+// each: the dequant of a chunk overlaps the MMAs of the one before), then
+// the raw-record ring (weights from DRAM: the longest latency) as deep as
+// two activation stages leave room for, up to six, then the activation ring
+// (tiles from L2) as deep as the rest allows.
+void tc_rings(int qtype, int Npad, int* stb, int* raw) {
+  const int raw_bytes = TC_PAIRS * tc_rec_bytes(qtype), b_bytes = Npad * 128;
+  const int fixed = 1024 + TC_A_ST * TC_A_STAGE;
+  auto raw_for = [&](int b) { return std::min(TC_MAX_RAW, (TC_SMEM_MAX - fixed - b * b_bytes) / raw_bytes); };
+  const int want = std::min(6, raw_for(2));
   int b = TC_MAX_ST;
-  while (b > 2 && 1024 + 3 * 2 * TC_A_BYTES + b * b_bytes + 3 * raw_bytes > TC_SMEM_MAX) b--;
-  if (1024 + 3 * 2 * TC_A_BYTES + b * b_bytes + 3 * raw_bytes > TC_SMEM_MAX) *sta = 2;
+  while (b > 2 && raw_for(b) < want) b--;
   *stb = b;
-  const int left = TC_SMEM_MAX - 1024 - *sta * 2 * TC_A_BYTES - b * b_bytes;
-  *raw = std::max(2, std::min(TC_MAX_RAW, left / raw_bytes));
+  *raw = std::max(2, raw_for(b));
 }
-size_t tc_smem_bytes(int qtype, int Npad, int sta, int stb, int raw) {
-  return 1024 + (size_t)sta * 2 * TC_A_BYTES + (size_t)stb * Npad * 128 +
-         (size_t)raw * 4 * tc_rec_bytes(qtype);
+size_t tc_smem_bytes(int qtype, int Npad, int stb, int raw) {
+  return 1024 + (size_t)TC_A_ST * TC_A_STAGE + (size_t)stb * Npad * 128 +
+         (size_t)raw * TC_PAIRS * tc_rec_bytes(qtype);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -740,15 +761,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int tc_npad(int R) { return std::max(16, (R + 15) / 16 * 16); }
-int tc_mtiles(const QMat& w) { return (w.N + TC_M - 1) / TC_M; }
+int tc_mtiles(const QMat& w) { return (w.N + TC_ROWS - 1) / TC_ROWS; }
 
 // K segments of a matrix for the tensor-core GEMM: the fewest waves of
 // one-CTA-per-SM launches, each CTA's chunk count, plus a small cost per
 // extra segment (its partial written and read back).  Only matrices whose
-// tiles do not fill the SMs are split: beyond one wave the partials (128 x
+// tiles do not fill the SMs are split: beyond one wave the partials (256 x
 // rows x 4 bytes per tile and segment) would spill from L2 to DRAM.
 int tc_choose_split(int N, int nch, int sms) {
-  const int n_mt = (N + TC_M - 1) / TC_M;
+  const int n_mt = (N + TC_ROWS - 1) / TC_ROWS;
   if (n_mt >= sms) return 1;
   int best = 1;
   double best_t = 1e30;
@@ -764,13 +785,13 @@ int tc_choose_split(int N, int nch, int sms) {
 }
 
 size_t tc_part_floats(const QMat& w, int R) {
-  return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, 256)) * TC_M : 0;
+  return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, TC_MAX_R)) * TC_ROWS : 0;
 }
 size_t tc_tickets_needed(const QMat& w) { return (size_t)tc_mtiles(w) + 1; }
 
 static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& epi,
                            const LinScratch& scr, cudaStream_t st) {
-  if (R < 1 || R > 256) return fail(SPEC_E_SHAPE, "tensor-core GEMM: 1 <= rows <= 256 per launch");
+  if (R < 1 || R > TC_MAX_R) return fail(SPEC_E_SHAPE, "tensor-core GEMM: 1 <= rows <= 192 per launch");
   if (scr.err == nullptr) return fail(SPEC_E_INVALID, "tensor-core GEMM: no error word");
   if (tc_part_floats(w, R) > scr.part_floats || tc_tickets_needed(w) > scr.n_tickets ||
       (epi.kind == EPI_LMHEAD && scr.amax_keys == nullptr))
@@ -802,8 +823,10 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   a.S = w.tc_S;
   a.R = R;
   a.Npad = Npad;
-  a.tmem_cols = Npad <= 32 ? 32 : (Npad <= 64 ? 64 : (Npad <= 128 ? 128 : 256));
-  tc_rings(w.qtype, Npad, &a.a_stages, &a.b_stages, &a.raw_depth);
+  // two accumulators of Npad columns, a power of two apart
+  a.acc_stride = Npad <= 16 ? 16 : (Npad <= 32 ? 32 : (Npad <= 64 ? 64 : (Npad <= 128 ? 128 : 256)));
+  a.tmem_cols = std::max(32, 2 * a.acc_stride);
+  tc_rings(w.qtype, Npad, &a.b_stages, &a.raw_depth);
   a.epi = epi;
   a.part = scr.part;
   a.tickets = scr.tickets;
@@ -815,7 +838,9 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_mt, a.S);
   cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.a_stages, a.b_stages, a.raw_depth);
+  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.b_stages, a.raw_depth);
+  if (cfg.dynamicSmemBytes > (size_t)TC_SMEM_MAX)
+    return fail(SPEC_E_SHAPE, "tensor-core GEMM: rings do not fit the shared memory");
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -827,12 +852,13 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   return SPEC_OK;
 }
 
-// Rows in blocks of at most 256 (one accumulator of 256 columns); every row
-// is computed by the same instructions whichever block it falls in.
+// Rows in blocks of at most 192 (the accumulators' columns and the rings fit
+// the tensor and shared memory); every row is computed by the same
+// instructions whichever block it falls in.
 int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
                      const LinScratch& scr, cudaStream_t st) {
   if (R < 1) return fail(SPEC_E_SHAPE, "tensor-core GEMM: R must be >= 1");
-  for (int r0 = 0; r0 < R; r0 += 256) {
+  for (int r0 = 0; r0 < R; r0 += TC_MAX_R) {
     LinEpi e = epi;
     const size_t o = (size_t)r0;
     switch (epi.kind) {
@@ -852,7 +878,7 @@ int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
         if (epi.argmax != nullptr) e.argmax = epi.argmax + o;
         break;
     }
-    const int rc = tc_launch_block(w, x + o * w.K, std::min(256, R - r0), e, scr, st);
+    const int rc = tc_launch_block(w, x + o * w.K, std::min(TC_MAX_R, R - r0), e, scr, st);
     if (rc != SPEC_OK) return rc;
   }
   return SPEC_OK;

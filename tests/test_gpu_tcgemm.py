@@ -81,7 +81,7 @@ def test_tc_small_matches_oracle(orc, dev, qtype, N, K):
                                        (4, 27648, 5120)])
 def test_tc_full_size_matches_oracle(orc, dev, qtype, N, K):
     """The linear sweep's matrices and the batched workload's gate/up at the
-    batched round's 192 rows (and 256, one full accumulator); rows at other
+    batched round's 192 rows (one full launch); rows at other
     batch sizes bitwise equal."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
@@ -96,7 +96,7 @@ def test_tc_full_size_matches_oracle(orc, dev, qtype, N, K):
     rows = np.r_[0:8, 100:108, 184:192]  # a sample of rows (the fp64 products are large)
     ref, s2 = references(orc, wh, xh[rows])
     check(y192[rows], ref, s2, K)
-    y300 = run_tc(sv, qm, xb, 300)      # two launches: 256 + 44 rows
+    y300 = run_tc(sv, qm, xb, 300)      # two launches: 192 + 108 rows
     assert np.array_equal(y300[:192], y192)
     for R in (1, 16, 100, 256):
         assert np.array_equal(run_tc(sv, qm, xb, R), y300[:R]), f"R={R}"
