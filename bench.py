@@ -259,22 +259,23 @@ class L2Flush:
         self.buf.amax()
 
 
-TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "linear_q_traffic_decoder14b_r192.json")
-LINEAR_SRC = os.path.join(ROOT, "speculative_decoding_verification_round_gb300", "csrc", "linear.cu")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "tc_linear_traffic_decoder14b_r192.json")
+GEMM_SRC = os.path.join(ROOT, "speculative_decoding_verification_round_gb300", "csrc", "tcgemm.cu")
 
 
 def measured_traffic(shapes):
     """DRAM bytes per verify-GEMM launch over a launch mix, from the committed
     ncu record (profiles/, command inside) -- or None when the record is
-    missing, lacks a shape, or was taken on a different linear.cu.  shapes:
-    (qtype, N, K, launches[, rows]); a record key is "QT:N:K" or "QT:N:K:R"."""
+    missing, lacks a shape, or was taken on a different kernel source (the
+    record's source_sha256 against GEMM_SRC).  shapes: (qtype, N, K,
+    launches[, rows]); a record key is "QT:N:K" or "QT:N:K:R"."""
     import hashlib
     try:
         rec = json.load(open(TRAFFIC_RECORD))
-        sha = hashlib.sha256(open(LINEAR_SRC, "rb").read()).hexdigest()
+        sha = hashlib.sha256(open(GEMM_SRC, "rb").read()).hexdigest()
     except (OSError, ValueError):
         return None
-    if rec.get("linear_cu_sha256") != sha:
+    if rec.get("source_sha256") != sha:
         return None
     total, n = 0.0, 0
     for sh in shapes:
@@ -1216,6 +1217,37 @@ def round_only(n_layers: int, warm: int = 2, reps: int = 2):
     print("round-only ok")
 
 
+def decoder8_only(warm: int = 3, reps: int = 3):
+    """Greedy nt = 8 rounds of the 8-layer H 4096 decoder (graph-replayed,
+    drafts on the target's greedy chain); the last `reps` run inside the
+    NVTX range "rounds", for launch lists."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    from speculative_decoding_verification_round_gb300 import synth
+    dev = torch.device("cuda:0")
+    wl = dict(synth.WL_DECODER8)
+    d, n = wl["d"], warm + reps
+    m = build_model(sv, synth, wl, dev, wl["ctx"] + 8 * (n + 4) + 64)
+    fill_context(sv, synth, m, wl, dev, seed=1)
+    anchor = 1234
+    drafts = record_chain(sv, synth, m, wl, dev, n, anchor, np.random.default_rng(wl["seed"]))
+    sid = torch.zeros(1, dtype=torch.int32, device=dev)
+    n_acc = torch.zeros(1, dtype=torch.int32, device=dev)
+    em = torch.zeros((1, d + 1), dtype=torch.int32, device=dev)
+    sv.spec_state_set(m, [0], n_past=[wl["ctx"]], emit_idx=[0], anchor=[anchor])
+    for j in range(n):
+        if j == warm:
+            torch.cuda.synchronize()
+            torch.cuda.nvtx.range_push("rounds")
+        dr = torch.tensor([drafts[j]], dtype=torch.int32, device=dev)
+        sv.spec_verify_round(m, 1, sid, dr, d, n_acc=n_acc, emitted=em)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    assert sv.spec_error_check(m) == 0
+    m.close()
+    print("decoder8-only ok")
+
+
 def draft_only(n_layers: int, warm: int = 3, reps: int = 3):
     """nt = 1 forwards (graph-replayed d = 0 rounds) of the 0.5B-class draft
     at `n_layers` layers and a 4096-position context; the last `reps` run
@@ -1264,6 +1296,8 @@ def main():
                     help="--linear-only on the tensor-core GEMM of multi-sequence rounds")
     ap.add_argument("--round-only", type=int, default=None, metavar="LAYERS",
                     help="profiling driver: stochastic rounds of the batched workload")
+    ap.add_argument("--decoder8-only", action="store_true",
+                    help="profiling driver: greedy nt=8 rounds of the 8-layer decoder (NVTX 'rounds')")
     ap.add_argument("--draft-only", type=int, default=None, metavar="LAYERS",
                     help="profiling driver: nt = 1 forwards of the 0.5B-class draft")
     args = ap.parse_args()
@@ -1272,6 +1306,9 @@ def main():
         return
     if args.round_only:
         round_only(args.round_only)
+        return
+    if args.decoder8_only:
+        decoder8_only()
         return
     if args.draft_only:
         draft_only(args.draft_only)

@@ -126,13 +126,13 @@ int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
 
 /* The same product on the tensor cores, as multi-sequence rounds run it
  * (tcgen05.mma with tensor-memory accumulators; rows are the N dimension):
- * each 64-k chunk of W is dequantised once per CTA to fp16 w = fp16(q *
- * scale) (one rounding, relative error <= 2^-11 per weight) and the sum is
- * accumulated in fp32 over all K.  Every row is computed by the same
- * instructions whatever R is, so a row's result does not depend on the other
- * rows; it differs from spec_linear_q's in the last bits (that kernel keeps
- * each 32-block's sum exact and applies the scale in fp32).
- * 1 <= R <= max_rows (launched in blocks of 192 rows). */
+ * each weight q * scale enters as an exact pair of fp16 numbers, hi =
+ * fp16(q * scale) and lo = q * scale - hi (two MMAs per 16-k step), so every
+ * product is exact and only the fp32 accumulation over K rounds.  Every row
+ * is computed by the same instructions whatever R is, so a row's result does
+ * not depend on the other rows; it differs from spec_linear_q's in the last
+ * bits (that kernel accumulates each 32-block's integer sum and applies the
+ * scale in fp32).  1 <= R <= max_rows (launched in blocks of 192 rows). */
 int spec_linear_q_tc(const spec_qmat* w, const uint16_t* x, int R, float* y,
                      void* stream);
 
@@ -266,8 +266,9 @@ int spec_model_profile_read(spec_model* m, int kind, double* seconds, int64_t* l
  * error word, waits with the full budget for the copies it issued and
  * finishes without using them, so the round commits nothing and writes -1
  * outputs.  This call sets the try budget of the FIRST wait of each GEMM CTA
- * (on its activation slice) for the model's later rounds; 0 makes that wait
- * give up at once.  Drains always keep the full budget.
+ * on its copies (the activation slice of the spec_linear_q kernel, the first
+ * weight records of the tensor-core kernel) for the model's later rounds; 0
+ * makes that wait give up at once.  Drains always keep the full budget.
  * 0 <= tries <= 131072; synchronises the device and drops captured graphs. */
 int spec_model_set_wait_budget(spec_model* m, int tries);
 

@@ -7,11 +7,12 @@
 // weight stream but by the contraction itself (2 x 192 flops per weight), so
 // it runs on tcgen05.mma with the activation rows as the N dimension:
 //
-//   * a CTA owns 256 weight rows (8 pairs of the packed streaming layout) as
-//     two 128-row halves, each with its own 128 x Npad fp32 accumulator in
-//     tensor memory (one TMEM lane per weight row; Npad = the rows rounded up
-//     to 16), and one of S segments of K.  Both halves use each activation
-//     tile, so a tile and every handshake of a chunk serve twice the MMAs;
+//   * a CTA owns 128 or 256 weight rows (4 or 8 pairs of the packed
+//     streaming layout; 256 for matrices with more 128-row tiles than SMs) as
+//     one or two 128-row halves, each with its own 128 x Npad fp32
+//     accumulator in tensor memory (one TMEM lane per weight row; Npad = the
+//     rows rounded up to 16), and one of S segments of K.  Two halves share
+//     each activation tile and chunk handshake (twice the MMAs per chunk);
 //   * warp 0 streams the packed weight records into a shared-memory ring with
 //     TMA bulk copies; warp 1 loads the activation tile of each 64-k chunk
 //     with a 2-D TMA tensor copy (128-byte swizzle, rows past R read as zero);
@@ -47,16 +48,14 @@
 namespace {
 
 constexpr int TC_M = 128;           // weight rows of an accumulator (the MMA's M)
-constexpr int TC_HALVES = 2;        // accumulators of a CTA
-constexpr int TC_ROWS = TC_M * TC_HALVES;  // weight rows of a CTA
-constexpr int TC_PAIRS = TC_ROWS / 32;     // packed pairs of a CTA
+constexpr int TC_HALVES = 2;        // accumulators of a CTA, at most
 constexpr int TC_THREADS = 352;     // 11 warps
 constexpr int TC_EPI_WARP0 = 3;     // warps 3..10: dequant, then epilogue
 constexpr int TC_EPI_THREADS = 256; // 8 warps: two per TMEM lane quadrant (one per half)
 constexpr int EW = 16;              // epilogue columns per TMEM load
 constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16 (one of hi / lo)
-constexpr int TC_A_STAGE = TC_HALVES * 2 * TC_A_BYTES;  // hi and lo of both halves
-constexpr int TC_A_ST = 2;      // A stages
+constexpr int TC_A_HALF = 2 * TC_A_BYTES;  // hi and lo tiles of one half
+constexpr int TC_MAX_A = 3;     // A stages (two with two halves)
 constexpr int TC_MAX_ST = 6;    // stages of the activation ring
 constexpr int TC_MAX_RAW = 8;
 constexpr int TC_MAX_R = 192;   // activation rows of one launch (Npad <= 192)
@@ -72,8 +71,9 @@ struct TcRec {  // the packed record of one (pair, 64-k chunk): see linear.cu
 struct TcArgs {
   const uint8_t* rec;  // [n_pairs][nch][rec]
   int N, K, nch, n_pairs, n_mt, S, R, Npad, tmem_cols;
+  int halves;           // 128-row halves (accumulators) of a CTA: 1 or 2
   int acc_stride;       // TMEM columns between the two accumulators
-  int b_stages, raw_depth;  // ring depths: activations, raw records (A: TC_A_ST)
+  int a_stages, b_stages, raw_depth;  // ring depths: A tiles, activations, raw records
   LinEpi epi;
   float* part;          // [S][n_mt][Npad][256] K-split partials
   unsigned* tickets;    // [n_mt] K-split tickets, then [1] argmax ticket
@@ -428,18 +428,19 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   extern __shared__ unsigned char smem_dyn[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) unsigned long long s_bar[2 * TC_A_ST + 2 * TC_MAX_ST + 2 * TC_MAX_RAW + 1];
+  __shared__ __align__(8) unsigned long long s_bar[2 * TC_MAX_A + 2 * TC_MAX_ST + 2 * TC_MAX_RAW + 1];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x, seg = blockIdx.y;
-  const int STB = a.b_stages, RAWN = a.raw_depth;
+  const int H = a.halves, STA = a.a_stages, STB = a.b_stages, RAWN = a.raw_depth;
+  const int CTA_ROWS = TC_M * H, CTA_PAIRS = 4 * H, A_STAGE = H * TC_A_HALF;
   const int B_BYTES = a.Npad * 128;
-  unsigned char* A0 = smem;  // [TC_A_ST][half][hi, lo] tiles
-  unsigned char* B0 = smem + TC_A_ST * TC_A_STAGE;
+  unsigned char* A0 = smem;  // [STA][half][hi, lo] tiles
+  unsigned char* B0 = smem + STA * A_STAGE;
   unsigned char* RAW0 = B0 + STB * B_BYTES;
-  const int RAW_BYTES = TC_PAIRS * RC::BYTES;
+  const int RAW_BYTES = CTA_PAIRS * RC::BYTES;
   // LM head: the best (key, id) of each column from each epilogue warp,
   // [half * 4 + quadrant][key, id][column], in the A ring once every MMA is done
   uint32_t* s_key = reinterpret_cast<uint32_t*>(A0);
@@ -448,20 +449,20 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   // each), so activation tiles are fetched a full ring ahead of their MMAs.
   const uint32_t bar0 = smem_u32(s_bar);
   auto A_FULL = [&](int s) { return bar0 + 8 * s; };
-  auto A_EMPTY = [&](int s) { return bar0 + 8 * (TC_A_ST + s); };
-  auto B_FULL = [&](int s) { return bar0 + 8 * (2 * TC_A_ST + s); };
-  auto B_EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_A_ST + TC_MAX_ST + s); };
-  auto RAW_FULL = [&](int r) { return bar0 + 8 * (2 * TC_A_ST + 2 * TC_MAX_ST + r); };
-  auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (2 * TC_A_ST + 2 * TC_MAX_ST + TC_MAX_RAW + r); };
-  const uint32_t ACC = bar0 + 8 * (2 * TC_A_ST + 2 * TC_MAX_ST + 2 * TC_MAX_RAW);
+  auto A_EMPTY = [&](int s) { return bar0 + 8 * (TC_MAX_A + s); };
+  auto B_FULL = [&](int s) { return bar0 + 8 * (2 * TC_MAX_A + s); };
+  auto B_EMPTY = [&](int s) { return bar0 + 8 * (2 * TC_MAX_A + TC_MAX_ST + s); };
+  auto RAW_FULL = [&](int r) { return bar0 + 8 * (2 * TC_MAX_A + 2 * TC_MAX_ST + r); };
+  auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (2 * TC_MAX_A + 2 * TC_MAX_ST + TC_MAX_RAW + r); };
+  const uint32_t ACC = bar0 + 8 * (2 * TC_MAX_A + 2 * TC_MAX_ST + 2 * TC_MAX_RAW);
 
   // this CTA's K range (chunks) and pairs
   const int c0 = (int)((long long)seg * a.nch / a.S);
   const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c0;
-  const int pair0 = mt * TC_PAIRS;
+  const int pair0 = mt * CTA_PAIRS;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TC_A_ST; s++) {
+    for (int s = 0; s < STA; s++) {
       mbar_init(A_FULL(s), TC_EPI_THREADS);
       mbar_init(A_EMPTY(s), 1);
     }
@@ -500,7 +501,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     // ---- constant: this starts before the grid dependency resolves)
     if (lane == 0) {
       int np = 0;
-      for (int p = 0; p < TC_PAIRS; p++) np += pair0 + p < a.n_pairs;
+      for (int p = 0; p < CTA_PAIRS; p++) np += pair0 + p < a.n_pairs;
       for (int c = 0; c < nc && !*abort_flag; c++) {
         const int r = c % RAWN, ur = c / RAWN;
         if (ur > 0 && !mbar_wait(RAW_EMPTY(r), (ur - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
@@ -538,7 +539,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       const uint32_t idesc = idesc_f16(a.Npad);
       int c = 0;
       for (; c < nc && !*abort_flag; c++) {
-        const int sa = c % TC_A_ST, ua = c / TC_A_ST, sb = c % STB, ub = c / STB;
+        const int sa = c % STA, ua = c / STA, sb = c % STB, ub = c / STB;
         if (!mbar_wait(A_FULL(sa), ua & 1, LIN_WAIT_TRIES, abort_flag) ||
             !mbar_wait(B_FULL(sb), ub & 1, LIN_WAIT_TRIES, abort_flag)) {
           give_up();
@@ -548,7 +549,8 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         const uint64_t bd = smem_desc_sw128(smem_u32(B0 + sb * B_BYTES));
 #pragma unroll
         for (int h = 0; h < TC_HALVES; h++) {
-          const unsigned char* at = A0 + sa * TC_A_STAGE + h * 2 * TC_A_BYTES;
+          if (h >= H) break;
+          const unsigned char* at = A0 + sa * A_STAGE + h * TC_A_HALF;
           const uint64_t ah = smem_desc_sw128(smem_u32(at));
           const uint64_t al = smem_desc_sw128(smem_u32(at + TC_A_BYTES));
           const uint32_t d = tmem + (uint32_t)(h * a.acc_stride);
@@ -569,7 +571,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     const int pc = (warp - TC_EPI_WARP0) >> 1, tile = (warp - TC_EPI_WARP0) & 1;
     grid_dep_wait();
     for (int c = 0; c < nc && !*abort_flag; c++) {
-      const int r = c % RAWN, ur = c / RAWN, s = c % TC_A_ST, us = c / TC_A_ST;
+      const int r = c % RAWN, ur = c / RAWN, s = c % STA, us = c / STA;
       // the first wait's budget is the one a caller may shorten (test hook)
       bool ok = mbar_wait(RAW_FULL(r), ur & 1, c == 0 ? a.wait_tries : LIN_WAIT_TRIES, abort_flag);
       if (ok && us > 0) ok = mbar_wait(A_EMPTY(s), (us - 1) & 1, LIN_WAIT_TRIES, abort_flag);
@@ -579,8 +581,9 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       }
 #pragma unroll
       for (int h = 0; h < TC_HALVES; h++) {
-        unsigned char* at = A0 + s * TC_A_STAGE + h * 2 * TC_A_BYTES;
-        const int pp = h * (TC_PAIRS / TC_HALVES) + pc;  // pair of the CTA
+        if (h >= H) break;
+        unsigned char* at = A0 + s * A_STAGE + h * TC_A_HALF;
+        const int pp = 4 * h + pc;  // pair of the CTA
         if (pair0 + pp < a.n_pairs) {
           dequant_tile<QT>(RAW0 + r * RAW_BYTES + pp * RC::BYTES, at, at + TC_A_BYTES, pc, tile,
                            lane);
@@ -599,14 +602,17 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   }
   grid_dep_launch();
 
-  // ---- epilogue: warps 3..10; warp w reads TMEM lane quadrant w % 4 of
-  // ---- half (w - 3) / 4, every column
+  // ---- epilogue: warps 3..10; warp w reads TMEM lane quadrant w % 4; with
+  // ---- two halves warp w takes half (w - 3) / 4, every column, with one
+  // ---- the two warps of a quadrant take every other group of EW columns
   if (warp >= TC_EPI_WARP0) {
-    const int quad = warp & 3, half = (warp - TC_EPI_WARP0) >> 2;
-    const int slot = half * 4 + quad;
+    const int quad = warp & 3, wh = (warp - TC_EPI_WARP0) >> 2;
+    const int half = H == 2 ? wh : 0;
+    const int col_first = H == 2 ? 0 : wh * EW, col_step = H == 2 ? EW : 2 * EW;
+    const int slot = wh * 4 + quad;
     const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..255
     const int m = TC_M * half + 32 * quad + lane;    // weight row of the CTA
-    const int n = mt * TC_ROWS + m;
+    const int n = mt * CTA_ROWS + m;
     const uint32_t trow = tmem + (uint32_t)(half * a.acc_stride) + ((uint32_t)(32 * quad) << 16);
     const bool acc_ok = mbar_wait(ACC, 0, LIN_WAIT_TRIES);
     if (!acc_ok) give_up();
@@ -616,12 +622,12 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     // segments in order
     bool finisher = true;
     if (a.S > 1) {
-      for (int col0 = 0; col0 < a.Npad; col0 += EW) {
+      for (int col0 = col_first; col0 < a.Npad; col0 += col_step) {
         uint32_t v[EW];
         tc_ld16(trow + col0, v);
-        float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * TC_ROWS + m;
+        float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * CTA_ROWS + m;
 #pragma unroll
-        for (int c = 0; c < EW; c++) dst[(size_t)c * TC_ROWS] = __uint_as_float(v[c]);
+        for (int c = 0; c < EW; c++) dst[(size_t)c * CTA_ROWS] = __uint_as_float(v[c]);
       }
       epi_bar();
       if (et == 0) {
@@ -634,16 +640,16 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       finisher = s_last != 0;
     }
     if (finisher) {
-      for (int col0 = 0; col0 < a.Npad; col0 += EW) {
+      for (int col0 = col_first; col0 < a.Npad; col0 += col_step) {
         float v[EW];
         if (a.S > 1) {
-          const float* src = a.part + ((size_t)mt * a.Npad + col0) * TC_ROWS + m;
-          const size_t step = (size_t)a.n_mt * a.Npad * TC_ROWS;
+          const float* src = a.part + ((size_t)mt * a.Npad + col0) * CTA_ROWS + m;
+          const size_t step = (size_t)a.n_mt * a.Npad * CTA_ROWS;
 #pragma unroll
-          for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * TC_ROWS);
+          for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * CTA_ROWS);
           for (int s2 = 1; s2 < a.S; s2++)
 #pragma unroll
-            for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * TC_ROWS);
+            for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * CTA_ROWS);
         } else {
           uint32_t u[EW];
           tc_ld16(trow + col0, u);
@@ -659,8 +665,11 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         // an aborted CTA still takes its ticket, so the state is reset
         epi_bar();
         for (int r = et; r < a.R && !aborted; r += TC_EPI_THREADS) {
-          uint32_t bk = s_key[r], bi = s_key[TC_MAX_R + r];
-          for (int q = 1; q < 2 * 4; q++) {
+          // the slots that saw column r: all eight with two halves, else the
+          // four warps of the column's group
+          const int q0 = H == 2 ? 0 : ((r / EW) & 1) * 4, q1 = H == 2 ? 8 : q0 + 4;
+          uint32_t bk = s_key[(2 * q0) * TC_MAX_R + r], bi = s_key[(2 * q0 + 1) * TC_MAX_R + r];
+          for (int q = q0 + 1; q < q1; q++) {
             const uint32_t k2 = s_key[(2 * q) * TC_MAX_R + r], i2 = s_key[(2 * q + 1) * TC_MAX_R + r];
             if (k2 > bk || (k2 == bk && i2 < bi)) {
               bk = k2;
@@ -723,14 +732,16 @@ int tc_rec_bytes(int qtype) {
 
 constexpr int TC_SMEM_MAX = 227 * 1024 - 2 * 1024;  // dynamic part (the static part is < 1 KB)
 
-// Ring depths of a launch that fit the shared memory: two A stages (64 KB
-// each: the dequant of a chunk overlaps the MMAs of the one before), then
-// the raw-record ring (weights from DRAM: the longest latency) as deep as
-// two activation stages leave room for, up to six, then the activation ring
-// (tiles from L2) as deep as the rest allows.
-void tc_rings(int qtype, int Npad, int* stb, int* raw) {
-  const int raw_bytes = TC_PAIRS * tc_rec_bytes(qtype), b_bytes = Npad * 128;
-  const int fixed = 1024 + TC_A_ST * TC_A_STAGE;
+// Ring depths of a launch that fit the shared memory: A stages (two of
+// 64 KB with two halves, three of 32 KB with one: the dequant of a chunk
+// overlaps the MMAs of the one before), then the raw-record ring (weights
+// from DRAM: the longest latency) as deep as two activation stages leave
+// room for, up to six, then the activation ring (tiles from L2) as deep as
+// the rest allows.
+void tc_rings(int qtype, int Npad, int halves, int* sta, int* stb, int* raw) {
+  const int raw_bytes = 4 * halves * tc_rec_bytes(qtype), b_bytes = Npad * 128;
+  *sta = halves == 2 ? 2 : 3;
+  const int fixed = 1024 + *sta * halves * TC_A_HALF;
   auto raw_for = [&](int b) { return std::min(TC_MAX_RAW, (TC_SMEM_MAX - fixed - b * b_bytes) / raw_bytes); };
   const int want = std::min(6, raw_for(2));
   int b = TC_MAX_ST;
@@ -738,9 +749,9 @@ void tc_rings(int qtype, int Npad, int* stb, int* raw) {
   *stb = b;
   *raw = std::max(2, raw_for(b));
 }
-size_t tc_smem_bytes(int qtype, int Npad, int stb, int raw) {
-  return 1024 + (size_t)TC_A_ST * TC_A_STAGE + (size_t)stb * Npad * 128 +
-         (size_t)raw * TC_PAIRS * tc_rec_bytes(qtype);
+size_t tc_smem_bytes(int qtype, int Npad, int halves, int sta, int stb, int raw) {
+  return 1024 + (size_t)sta * halves * TC_A_HALF + (size_t)stb * Npad * 128 +
+         (size_t)raw * 4 * halves * tc_rec_bytes(qtype);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -761,21 +772,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int tc_npad(int R) { return std::max(16, (R + 15) / 16 * 16); }
-int tc_mtiles(const QMat& w) { return (w.N + TC_ROWS - 1) / TC_ROWS; }
+int tc_mtiles(const QMat& w) { return (w.N + TC_M * w.tc_H - 1) / (TC_M * w.tc_H); }
 
-// K segments of a matrix for the tensor-core GEMM: the fewest waves of
-// one-CTA-per-SM launches, each CTA's chunk count, plus a small cost per
-// extra segment (its partial written and read back).  Only matrices whose
-// tiles do not fill the SMs are split: beyond one wave the partials (256 x
-// rows x 4 bytes per tile and segment) would spill from L2 to DRAM.
-int tc_choose_split(int N, int nch, int sms) {
-  const int n_mt = (N + TC_ROWS - 1) / TC_ROWS;
-  if (n_mt >= sms) return 1;
+// Halves of a CTA for a matrix: two (256 rows, each activation tile and
+// chunk handshake serving twice the MMAs) when 128-row tiles would be more
+// than one wave of one-CTA-per-SM launches, else one (more, shorter tiles,
+// less K splitting).
+int tc_choose_halves(int N, int sms) { return (N + TC_M - 1) / TC_M > sms ? 2 : 1; }
+
+// K segments of a matrix for the tensor-core GEMM: only matrices whose tiles
+// do not fill the SMs are split, and only as far as one wave of
+// one-CTA-per-SM launches holds every segment (beyond one wave the partials,
+// CTA rows x activation rows x 4 bytes per tile and segment, leave L2 for
+// DRAM while the weights stream); among those, the fewest chunks per CTA
+// plus a small cost per extra segment (its partial written and read back).
+int tc_choose_split(int N, int nch, int sms, int halves) {
+  const int n_mt = (N + TC_M * halves - 1) / (TC_M * halves);
   int best = 1;
   double best_t = 1e30;
-  for (int S = 1; S <= 8 && S <= nch; S++) {
-    const double waves = std::ceil((double)n_mt * S / std::max(sms, 1));
-    const double t = waves * std::ceil((double)nch / S) + (S > 1 ? 2.0 * S : 0.0);
+  for (int S = 1; S <= 8 && S <= nch && (S == 1 || n_mt * S <= sms); S++) {
+    const double t = std::ceil((double)nch / S) + (S > 1 ? 2.0 * S : 0.0);
     if (t < best_t - 1e-9) {
       best_t = t;
       best = S;
@@ -785,7 +801,8 @@ int tc_choose_split(int N, int nch, int sms) {
 }
 
 size_t tc_part_floats(const QMat& w, int R) {
-  return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, TC_MAX_R)) * TC_ROWS : 0;
+  return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, TC_MAX_R)) * TC_M * w.tc_H
+                    : 0;
 }
 size_t tc_tickets_needed(const QMat& w) { return (size_t)tc_mtiles(w) + 1; }
 
@@ -823,10 +840,11 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   a.S = w.tc_S;
   a.R = R;
   a.Npad = Npad;
-  // two accumulators of Npad columns, a power of two apart
+  // one accumulator of Npad columns per half, a power of two apart
+  a.halves = w.tc_H;
   a.acc_stride = Npad <= 16 ? 16 : (Npad <= 32 ? 32 : (Npad <= 64 ? 64 : (Npad <= 128 ? 128 : 256)));
-  a.tmem_cols = std::max(32, 2 * a.acc_stride);
-  tc_rings(w.qtype, Npad, &a.b_stages, &a.raw_depth);
+  a.tmem_cols = std::max(32, a.halves * a.acc_stride);
+  tc_rings(w.qtype, Npad, a.halves, &a.a_stages, &a.b_stages, &a.raw_depth);
   a.epi = epi;
   a.part = scr.part;
   a.tickets = scr.tickets;
@@ -838,7 +856,7 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_mt, a.S);
   cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.b_stages, a.raw_depth);
+  cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.halves, a.a_stages, a.b_stages, a.raw_depth);
   if (cfg.dynamicSmemBytes > (size_t)TC_SMEM_MAX)
     return fail(SPEC_E_SHAPE, "tensor-core GEMM: rings do not fit the shared memory");
   cfg.stream = st;

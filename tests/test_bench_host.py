@@ -55,14 +55,14 @@ def test_no_sampler_reports_unsampled():
 
 
 def test_traffic_record_is_used_only_for_its_source(tmp_path, monkeypatch):
-    src = tmp_path / "linear.cu"
+    src = tmp_path / "tcgemm.cu"
     src.write_text("// kernel v1\n")
     rec = tmp_path / "traffic.json"
     rec.write_text(json.dumps({
-        "linear_cu_sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
+        "source_sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
         "dram_bytes_per_launch": {"4:64:128": 100, "6:32:64": 400}}))
     monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(rec))
-    monkeypatch.setattr(bench, "LINEAR_SRC", str(src))
+    monkeypatch.setattr(bench, "GEMM_SRC", str(src))
     # per launch over the mix: (3 x 100 + 1 x 400) / 4
     assert bench.measured_traffic([(4, 64, 128, 3), (6, 32, 64, 1)]) == pytest.approx(175.0)
     assert bench.measured_traffic([(4, 64, 128, 1), (8, 16, 32, 1)]) is None  # shape not captured
@@ -73,15 +73,19 @@ def test_traffic_record_is_used_only_for_its_source(tmp_path, monkeypatch):
 
 def test_committed_traffic_record_shows_no_re_reads():
     """The record under profiles/: every captured shape moved its packed
-    weight bytes once (within 10%).  A record older than linear.cu is not
-    used by the bench (traffic null) and is not judged here."""
+    weight bytes once (within 10%, plus the activation rows it reads and the
+    outputs it writes).  A record older than the kernel's source is not used
+    by the bench (traffic null) and is not judged here."""
     if not os.path.exists(bench.TRAFFIC_RECORD):
         pytest.skip("no traffic record for the bench's workload: the bench reports traffic null")
     rec = json.load(open(bench.TRAFFIC_RECORD))
-    sha = hashlib.sha256(open(bench.LINEAR_SRC, "rb").read()).hexdigest()
-    if rec["linear_cu_sha256"] != sha:
-        pytest.skip("the record predates linear.cu: the bench reports traffic null")
+    sha = hashlib.sha256(open(bench.GEMM_SRC, "rb").read()).hexdigest()
+    if rec["source_sha256"] != sha:
+        pytest.skip("the record predates the kernel source: the bench reports traffic null")
     for key, b in rec["dram_bytes_per_launch"].items():
-        qt, N, K = map(int, key.split(":")[:3])
-        alg = N * K * bench.WEIGHT_BYTES[qt]
-        assert 0.98 * alg <= b <= 1.10 * alg, key  # no re-reads
+        f = list(map(int, key.split(":")))
+        qt, N, K = f[:3]
+        R = f[3] if len(f) > 3 else 0
+        w = N * K * bench.WEIGHT_BYTES[qt]
+        io = R * K * 2 + R * N * 4  # fp16 activations in, fp32 outputs out
+        assert 0.98 * w <= b <= 1.10 * (w + io), key  # no re-reads
