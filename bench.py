@@ -1142,7 +1142,9 @@ def run_ours(args):
                     "api": "spec_verify_round_host (ids and drafts from host arrays, draft "
                            "logits from pinned host memory, outputs to host arrays)",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": (1 + 8 * n_layers - 1 + 2 + 4) * args.steps,
+            # embed + 8 per layer (the first norm inside embed) + final norm and
+            # LM head + row max, row sum, decide, resample + commit
+            "gpu_launches": (1 + 8 * n_layers - 1 + 2 + 5) * args.steps,
             "clocks": clk.summary(),
         }
         if extras:
