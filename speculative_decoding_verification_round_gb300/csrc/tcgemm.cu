@@ -49,10 +49,11 @@ namespace {
 
 constexpr int TC_M = 128;           // weight rows of an accumulator (the MMA's M)
 constexpr int TC_HALVES = 2;        // accumulators of a CTA, at most
-constexpr int TC_THREADS = 352;     // 11 warps
-constexpr int TC_EPI_WARP0 = 3;     // warps 3..10: dequant, then epilogue
-constexpr int TC_EPI_THREADS = 256; // 8 warps: two per TMEM lane quadrant (one per half)
-constexpr int EW = 16;              // epilogue columns per TMEM load
+constexpr int TC_DQ_WARPS = 16;     // dequant (then epilogue) warps
+constexpr int TC_THREADS = (3 + TC_DQ_WARPS) * 32;  // 19 warps
+constexpr int TC_EPI_WARP0 = 3;     // warps 3..18: dequant, then epilogue
+constexpr int TC_EPI_THREADS = TC_DQ_WARPS * 32;   // four warps per TMEM lane quadrant
+constexpr int EW = 8;               // epilogue columns per TMEM load
 constexpr int TC_A_BYTES = TC_M * 128;  // one 64-k chunk of 128 rows, fp16 (one of hi / lo)
 constexpr int TC_A_HALF = 2 * TC_A_BYTES;  // hi and lo tiles of one half
 constexpr int TC_MAX_A = 3;     // A stages (two with two halves)
@@ -171,13 +172,12 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+// EW consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
+        "=r"(v[7])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -247,8 +247,8 @@ __device__ __forceinline__ uint32_t f32_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ void epi_bar() {  // the eight epilogue warps
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+__device__ __forceinline__ void epi_bar() {  // the dequant / epilogue warps
+  asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI_THREADS) : "memory");
 }
 
 // The dequant of one 64-k chunk of one 16-row tile i of a pair by one lane:
@@ -258,7 +258,8 @@ __device__ __forceinline__ void epi_bar() {  // the eight epilogue warps
 // to the hi tile and its exact remainder to the lo tile.
 template <int QT>
 __device__ __forceinline__ void dequant_tile(const unsigned char* raw, unsigned char* ahi,
-                                             unsigned char* alo, int pair_in_cta, int i, int lane) {
+                                             unsigned char* alo, int pair_in_cta, int i, int lane,
+                                             int b_lo, int b_hi) {
   using RC = TcRec<QT>;
   const int ph = lane >> 3, j = lane & 7;
   const int p = j & 1, t0 = (j >> 1) & 1, t1 = j >> 2;
@@ -271,6 +272,7 @@ __device__ __forceinline__ void dequant_tile(const unsigned char* raw, unsigned 
     const int r0 = 32 * pair_in_cta + 16 * i + g;                 // A-tile row of row g
 #pragma unroll
     for (int b = 0; b < 2; b++) {
+      if (b < b_lo || b >= b_hi) continue;
       const __half2 sg = b == 0 ? __low2half2(s0) : __low2half2(s1);
       const __half2 sg8 = b == 0 ? __high2half2(s0) : __high2half2(s1);
       __half2 qg[4], qg8[4];  // exact integers, k pairs (0,1) .. (6,7)
@@ -566,9 +568,14 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       tc_commit(ACC);  // completes when every MMA issued above has
     }
   } else {
-    // ---- dequant (warps 3..10: 16-row tile t of each half's eight; pair
-    // ---- pc of the half)
-    const int pc = (warp - TC_EPI_WARP0) >> 1, tile = (warp - TC_EPI_WARP0) & 1;
+    // ---- dequant (warps 3..18).  Two halves: warp w' = w - 3 takes 16-row
+    // ---- tile w' & 1 of pair (w' & 7) / 2 of half w' / 8, both 32-k blocks.
+    // ---- One half: 16-row tile w' / 2 (pair w' / 4, tile (w' / 2) & 1),
+    // ---- 32-k block w' & 1.
+    const int wq = warp - TC_EPI_WARP0;
+    const int dh = H == 2 ? wq >> 3 : 0;
+    const int pc = H == 2 ? (wq & 7) >> 1 : wq >> 2, tile = H == 2 ? wq & 1 : (wq >> 1) & 1;
+    const int b_lo = H == 2 ? 0 : wq & 1, b_hi = H == 2 ? 2 : b_lo + 1;
     grid_dep_wait();
     for (int c = 0; c < nc && !*abort_flag; c++) {
       const int r = c % RAWN, ur = c / RAWN, s = c % STA, us = c / STA;
@@ -579,17 +586,16 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         give_up();
         break;
       }
-#pragma unroll
-      for (int h = 0; h < TC_HALVES; h++) {
-        if (h >= H) break;
-        unsigned char* at = A0 + s * A_STAGE + h * TC_A_HALF;
-        const int pp = 4 * h + pc;  // pair of the CTA
+      {
+        unsigned char* at = A0 + s * A_STAGE + dh * TC_A_HALF;
+        const int pp = 4 * dh + pc;  // pair of the CTA
         if (pair0 + pp < a.n_pairs) {
           dequant_tile<QT>(RAW0 + r * RAW_BYTES + pp * RC::BYTES, at, at + TC_A_BYTES, pc, tile,
-                           lane);
-        } else {  // rows past the matrix: zeros
-          for (int q = lane; q < 16 * 8; q += 32) {
-            const int rr = 32 * pc + 16 * tile + q / 8, u = q % 8;
+                           lane, b_lo, b_hi);
+        } else {  // rows past the matrix: zeros (the warp's 16-byte units)
+          const int nu = 4 * (b_hi - b_lo);
+          for (int q = lane; q < 16 * nu; q += 32) {
+            const int rr = 32 * pc + 16 * tile + q / nu, u = 4 * b_lo + q % nu;
             *reinterpret_cast<uint4*>(at + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4*>(at + TC_A_BYTES + sw128_off(rr, u)) = make_uint4(0, 0, 0, 0);
           }
@@ -602,15 +608,16 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   }
   grid_dep_launch();
 
-  // ---- epilogue: warps 3..10; warp w reads TMEM lane quadrant w % 4; with
-  // ---- two halves warp w takes half (w - 3) / 4, every column, with one
-  // ---- the two warps of a quadrant take every other group of EW columns
+  // ---- epilogue: warps 3..18; warp w reads TMEM lane quadrant w % 4 and
+  // ---- is the wi-th of the four warps of that quadrant, wi = (w - 3) / 4:
+  // ---- with two halves it takes half wi / 2 and every other group of EW
+  // ---- columns, with one every fourth group
   if (warp >= TC_EPI_WARP0) {
-    const int quad = warp & 3, wh = (warp - TC_EPI_WARP0) >> 2;
-    const int half = H == 2 ? wh : 0;
-    const int col_first = H == 2 ? 0 : wh * EW, col_step = H == 2 ? EW : 2 * EW;
-    const int slot = wh * 4 + quad;
-    const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..255
+    const int quad = warp & 3, wi = (warp - TC_EPI_WARP0) >> 2;
+    const int half = H == 2 ? wi >> 1 : 0;
+    const int cw = H == 2 ? wi & 1 : wi, col_first = cw * EW, col_step = H == 2 ? 2 * EW : 4 * EW;
+    const int slot = wi * 4 + quad;
+    const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..511
     const int m = TC_M * half + 32 * quad + lane;    // weight row of the CTA
     const int n = mt * CTA_ROWS + m;
     const uint32_t trow = tmem + (uint32_t)(half * a.acc_stride) + ((uint32_t)(32 * quad) << 16);
@@ -624,7 +631,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     if (a.S > 1) {
       for (int col0 = col_first; col0 < a.Npad; col0 += col_step) {
         uint32_t v[EW];
-        tc_ld16(trow + col0, v);
+        tc_ld(trow + col0, v);
         float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * CTA_ROWS + m;
 #pragma unroll
         for (int c = 0; c < EW; c++) dst[(size_t)c * CTA_ROWS] = __uint_as_float(v[c]);
@@ -652,7 +659,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
             for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * CTA_ROWS);
         } else {
           uint32_t u[EW];
-          tc_ld16(trow + col0, u);
+          tc_ld(trow + col0, u);
 #pragma unroll
           for (int c = 0; c < EW; c++) v[c] = __uint_as_float(u[c]);
         }
@@ -665,11 +672,13 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         // an aborted CTA still takes its ticket, so the state is reset
         epi_bar();
         for (int r = et; r < a.R && !aborted; r += TC_EPI_THREADS) {
-          // the slots that saw column r: all eight with two halves, else the
-          // four warps of the column's group
-          const int q0 = H == 2 ? 0 : ((r / EW) & 1) * 4, q1 = H == 2 ? 8 : q0 + 4;
-          uint32_t bk = s_key[(2 * q0) * TC_MAX_R + r], bi = s_key[(2 * q0 + 1) * TC_MAX_R + r];
-          for (int q = q0 + 1; q < q1; q++) {
+          // the slots that saw column r: the four quadrants of the warps of
+          // the column's group (of each half)
+          const int cr = H == 2 ? (r / EW) & 1 : (r / EW) & 3;
+          const int nsl = 4 * H;
+          uint32_t bk = 0u, bi = 0xffffffffu;
+          for (int e = 0; e < nsl; e++) {
+            const int q = (H == 2 ? (2 * (e >> 2) + cr) : cr) * 4 + (e & 3);
             const uint32_t k2 = s_key[(2 * q) * TC_MAX_R + r], i2 = s_key[(2 * q + 1) * TC_MAX_R + r];
             if (k2 > bk || (k2 == bk && i2 < bi)) {
               bk = k2;
