@@ -130,7 +130,7 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
 // The tensor-core (tcgen05) verify GEMM of multi-sequence rounds (tcgemm.cu):
 // 1 <= R <= 256 rows per launch, the same epilogues.
 int tc_npad(int R);
-int tc_choose_halves(int N, int sms);
+int tc_choose_halves(int N, int nch, int sms);
 int tc_choose_split(int N, int nch, int sms, int halves);
 size_t tc_part_floats(const QMat& w, int R);
 size_t tc_tickets_needed(const QMat& w);

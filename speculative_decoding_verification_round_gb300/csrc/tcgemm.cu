@@ -783,11 +783,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int tc_npad(int R) { return std::max(16, (R + 15) / 16 * 16); }
 int tc_mtiles(const QMat& w) { return (w.N + TC_M * w.tc_H - 1) / (TC_M * w.tc_H); }
 
-// Halves of a CTA for a matrix: two (256 rows, each activation tile and
-// chunk handshake serving twice the MMAs) when 128-row tiles would be more
-// than one wave of one-CTA-per-SM launches, else one (more, shorter tiles,
-// less K splitting).
-int tc_choose_halves(int N, int sms) { return (N + TC_M - 1) / TC_M > sms ? 2 : 1; }
+// Halves of a CTA for a matrix: two (256 rows: each activation tile and
+// chunk handshake serve twice the MMAs) when the 256-row tiles hold at least
+// 20 chunks per SM, else one (more, shorter tiles: fewer K segments, less
+// fixed cost per CTA and more CTAs sharing the epilogue).  Measured inside
+// the 192-row round: two halves for down 5120x13824 (88 vs 93 us), gate/up
+// 27648x5120 and the LM head; one for QKV 7168x5120 (65 vs 70) and O
+// 5120x5120.
+int tc_choose_halves(int N, int nch, int sms) {
+  const long long units = (long long)((N + 2 * TC_M - 1) / (2 * TC_M)) * nch;
+  return units >= 20LL * sms ? 2 : 1;
+}
 
 // K segments of a matrix for the tensor-core GEMM: only matrices whose tiles
 // do not fill the SMs are split, and only as far as one wave of

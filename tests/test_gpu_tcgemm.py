@@ -84,11 +84,12 @@ def test_tc_small_matches_oracle(orc, dev, qtype, N, K):
 
 
 @pytest.mark.parametrize("qtype,N,K", [(4, 5120, 13824), (6, 13824, 5120), (8, 5120, 13824),
-                                       (4, 27648, 5120)])
+                                       (4, 27648, 5120), (4, 13920, 5120), (8, 10016, 5120)])
 def test_tc_full_size_matches_oracle(orc, dev, qtype, N, K):
     """The linear sweep's matrices and the batched workload's gate/up at the
     batched round's 192 rows (one full launch); rows at other
-    batch sizes bitwise equal."""
+    batch sizes bitwise equal.  The last two run 256-row CTAs whose last
+    tile is ragged (96 and 32 real rows)."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
     gen = synth.torch_gen(40 + qtype, dev)
