@@ -11,10 +11,11 @@
 // Neither step depends on nt or on the other rows of the batch, so row i of
 // an nt-row round equals the nt = 1 result at the same position bit for bit.
 //
-// One CTA per (chunk, kv head, sequence): the chunk's K and V tiles are
-// staged once in shared memory (cp.async, XOR-swizzled 16-byte units) and
-// shared by all nt x group query rows of that kv head (GQA), which are
-// processed as m16 tiles with mma.sync m16n8k16: S = Q K^T, softmax in fp32
+// One CTA per (chunk, kv head, sequence) -- or, with five or more m tiles
+// of query rows, per group of two m tiles of them: the chunk's K and V tiles
+// are staged in shared memory (cp.async, XOR-swizzled 16-byte units) and
+// shared by the CTA's query rows of that kv head (GQA, nt x group rows),
+// which are processed as m16 tiles with mma.sync m16n8k16: S = Q K^T, softmax in fp32
 // (log2 domain), O = P V with P as an exact hi + lo pair of fp16 operands.
 // Each half of the chunk's keys is a separate warp's (max, sum, O); the two
 // are rescaled to the common max in one fixed order inside the CTA, so the
@@ -71,20 +72,24 @@ inline ChunkSmem chunk_smem(int hd, int ds, int nw, int n_mt) {
 
 // 2 CTAs per SM (what the shared memory holds) up to 8 warps; with 8 warps
 // that caps the registers at 128, which the q fragments read from shared
-// memory allow.  12 warps (5 or 6 m tiles: every work item in one round)
-// run one CTA per SM.
+// memory allow.
 template <int HD, int DS, int NW>
-__global__ void __launch_bounds__(NW * 32, NW > 8 ? 1 : 2)
+__global__ void __launch_bounds__(NW * 32, 2)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
-                  int nt, int nq, int nkv, int max_ctx, int nchunks, ChunkSmem lay,
-                  float* __restrict__ part) {
+                  int nt, int nq, int nkv, int max_ctx, int nchunks, int mt_group,
+                  ChunkSmem lay, float* __restrict__ part) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* Ks = smem;
   unsigned char* Qs = smem + lay.q_off;
   unsigned char* Vs = smem + lay.v_off;
-  const int c = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int c = blockIdx.x, s = blockIdx.z;
   const int G = nq / nkv, M = nt * G, Mmax_stride = M;  // rows of this (seq, kv head)
+  // the (seq, kv head)'s m tiles are cut into groups of mt_group, one CTA
+  // each: this CTA's tiles are mt0 .. mt0 + n_mt - 1
+  const int n_mt_all = (M + 15) / 16, n_grp = (n_mt_all + mt_group - 1) / mt_group;
+  const int kvh = blockIdx.y / n_grp, mt0 = (blockIdx.y % n_grp) * mt_group;
+  const int n_mt = min(mt_group, n_mt_all - mt0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   // the row table and the committed cache belong to kernels that completed
@@ -134,12 +139,11 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   stage(Ks, kcache, false);
   // the q rows of the CTA's m tiles (row m = query i * G + gh), swizzled like
   // the cache tiles; rows past M are zero
-  const int n_mt = (M + 15) / 16;
   {
     const uint32_t qs0 = smem_u32(Qs);
     for (int e = threadIdx.x; e < n_mt * 16 * UNITS; e += NW * 32) {
-      const int m = e / UNITS, uu = e % UNITS;
-      const uint32_t so = qs0 + tile_off<HD>(m, uu);
+      const int ml = e / UNITS, uu = e % UNITS, m = mt0 * 16 + ml;
+      const uint32_t so = qs0 + tile_off<HD>(ml, uu);
       if (m < M) {
         const __half* src = q + ((size_t)(s * nt + m / G) * nq + kvh * G + m % G) * HD + uu * 8;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(so), "l"(src));
@@ -167,7 +171,7 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
   const int n_items = n_mt * DS * KS;
   for (int it0 = 0; it0 < n_items; it0 += NW) {  // uniform trip count: the barriers below
     const int it = it0 + warp;
-    const int kh = it % KS, dh = (it / KS) % DS, mt = it / (KS * DS);
+    const int kh = it % KS, dh = (it / KS) % DS, mtl = it / (KS * DS), mt = mt0 + mtl;
     const int key0 = kh * CHK;
     const int mA = mt * 16 + g, mB = mA + 8;
     const bool okA = it < n_items && mA < M, okB = it < n_items && mB < M;
@@ -187,7 +191,7 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
     // the q fragment rows of this m tile for ldmatrix: lanes 0-7 rows 0-7,
     // 8-15 rows 8-15 (first 8 dims of a k16 step), 16-31 the same rows for
     // its second 8 dims
-    const int q_row = min(mt, n_mt - 1) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int q_row = min(mtl, n_mt - 1) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     // ---- S = Q K^T over the half (16 rows x CHK keys)
     float sacc[CHK / 8][4];
 #pragma unroll
@@ -514,22 +518,24 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
   cfg.stream = st;
   cfg.attrs = at;
   cfg.numAttrs = programmatic_launch() ? 1 : 0;
-  cfg.gridDim = dim3(nchunks, nkv, n_seq);
   // one m tile: warp pairs also split the head dimensions (4 warps); two m
-  // tiles: 4 warps; more: 8 warps, so that 4 m tiles are still one round of
-  // work items (the bits of every output depend on none of these choices)
+  // tiles: 4 warps; three or four: 8 warps, so that they are one round of
+  // work items; five or more: CTAs of two m tiles (4 warps, two CTAs per SM)
+  // (the bits of every output depend on none of these choices)
   const int n_mt = (nt * (nq / nkv) + 15) / 16;
+  const int mt_group = n_mt <= 4 ? n_mt : 2;
+  const int n_grp = (n_mt + mt_group - 1) / mt_group;
   const int ds = n_mt == 1 ? 2 : 1;
-  const int nw = n_mt <= 2 ? 4 : (n_mt <= 4 || n_mt > 6 ? 8 : 12);
+  const int nw = mt_group <= 2 ? 4 : 8;
   auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2, 4>
-               : n_mt == 2 ? attn_chunk_kernel<HD, 1, 4>
-               : nw == 12  ? attn_chunk_kernel<HD, 1, 12>
+               : nw == 4   ? attn_chunk_kernel<HD, 1, 4>
                            : attn_chunk_kernel<HD, 1, 8>;
-  const ChunkSmem lay = chunk_smem(HD, ds, nw, n_mt);
+  const ChunkSmem lay = chunk_smem(HD, ds, nw, mt_group);
+  cfg.gridDim = dim3(nchunks, nkv * n_grp, n_seq);
   cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = lay.bytes;
   cudaError_t e = cudaLaunchKernelEx(&cfg, chunk, q, kcache, vcache, rows, nt, nq, nkv, max_ctx,
-                                     nchunks, lay, part);
+                                     nchunks, mt_group, lay, part);
   if (e == cudaSuccess) {
     // the model's chunk count picks the merge (never nt): a warp per (row,
     // head) for short contexts, a CTA per (row, head) -- every chunk's loads
@@ -574,8 +580,7 @@ void attn_init_attrs() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   for (auto k : {attn_chunk_kernel<128, 2, 4>, attn_chunk_kernel<128, 1, 4>,
-                 attn_chunk_kernel<128, 1, 8>, attn_chunk_kernel<128, 1, 12>,
-                 attn_chunk_kernel<64, 2, 4>, attn_chunk_kernel<64, 1, 4>,
-                 attn_chunk_kernel<64, 1, 8>, attn_chunk_kernel<64, 1, 12>})
+                 attn_chunk_kernel<128, 1, 8>, attn_chunk_kernel<64, 2, 4>,
+                 attn_chunk_kernel<64, 1, 4>, attn_chunk_kernel<64, 1, 8>})
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
