@@ -181,12 +181,15 @@ __device__ __forceinline__ void for_segment(const float* src, int s0, int s1, F&
   }
 }
 
+// q_only: the grid covers the q rows only (the p rows' keys came from the
+// LM head); CTA b then takes q row b / nseg of the sequences in order.
 __global__ void __launch_bounds__(ST_THREADS)
 row_max_kernel(const float* __restrict__ p, const float* __restrict__ q, int d, int V, int nseg,
-               uint32_t* __restrict__ row_key, uint32_t* __restrict__ err) {
+               int q_only, uint32_t* __restrict__ row_key, uint32_t* __restrict__ err) {
   __shared__ float s_red[ST_THREADS / 32];
   __shared__ int s_bad;
-  const int row = blockIdx.x / nseg, sg = blockIdx.x % nseg;
+  const int ri = blockIdx.x / nseg, sg = blockIdx.x % nseg;
+  const int row = q_only ? (ri / d) * (2 * d + 1) + d + 1 + ri % d : ri;
   const float* src = stoch_row(p, q, d, V, row);
   const int s0 = (int)((long long)sg * V / nseg), s1 = (int)((long long)(sg + 1) * V / nseg);
   if (threadIdx.x == 0) s_bad = 0;
@@ -599,7 +602,7 @@ int launch_accept_stochastic(const float* p, const float* q, const int32_t* draf
                              int d, int V, float T, uint64_t seed, const int32_t* seq_ids,
                              uint64_t* emit_idx, int emit_by_slot, int n_slots, int32_t* n_acc,
                              int32_t* emitted, const StochScratch& scr, uint32_t* err,
-                             cudaStream_t st) {
+                             cudaStream_t st, bool p_keys_ready) {
   const size_t nrows = stoch_rows_needed(n_seq, d);
   const int nseg = st_segments(V);
   if (nrows * (size_t)nseg > (size_t)INT32_MAX || (size_t)n_seq * RS_CL > (size_t)INT32_MAX)
@@ -607,10 +610,16 @@ int launch_accept_stochastic(const float* p, const float* q, const int32_t* draf
   if (nrows > scr.rows_cap || (size_t)n_seq > scr.seq_cap)
     return fail(SPEC_E_SHAPE, "stochastic accept: scratch too small");
   // the per-row maxima (keys) and sums are accumulated by atomics from zero
-  CUDA_TRY(cudaMemsetAsync(scr.row_key, 0, nrows * sizeof(uint32_t), st));
+  // (the round's LM head has written the p rows' keys and zeroed the q rows')
+  if (!p_keys_ready) CUDA_TRY(cudaMemsetAsync(scr.row_key, 0, nrows * sizeof(uint32_t), st));
   CUDA_TRY(cudaMemsetAsync(scr.row_sum, 0, nrows * sizeof(unsigned long long), st));
   const unsigned grid = (unsigned)(nrows * (size_t)nseg);
-  row_max_kernel<<<grid, ST_THREADS, 0, st>>>(p, q, d, V, nseg, scr.row_key, err);
+  const size_t qrows = (size_t)n_seq * d;
+  if (!p_keys_ready)
+    row_max_kernel<<<grid, ST_THREADS, 0, st>>>(p, q, d, V, nseg, 0, scr.row_key, err);
+  else if (qrows > 0)
+    row_max_kernel<<<(unsigned)(qrows * nseg), ST_THREADS, 0, st>>>(p, q, d, V, nseg, 1, scr.row_key,
+                                                                     err);
   row_sum_kernel<<<grid, ST_THREADS, 0, st>>>(p, q, d, V, nseg, T, scr.row_key, scr.row_sum);
   decide_kernel<<<(n_seq + DC_WARPS - 1) / DC_WARPS, DC_WARPS * 32, 0, st>>>(
       p, q, draft, n_seq, d, V, T, seed, seq_ids, emit_idx, emit_by_slot, n_slots, scr.row_key,

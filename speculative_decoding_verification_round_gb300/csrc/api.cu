@@ -764,8 +764,8 @@ static double gemm_bytes(const QMat& w, int R, int out_bytes) {
 // The target pass over rows [anchor, draft[s][0..nt-2]] of each sequence;
 // embed_node (capture only) receives the embedding node.
 static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draft,
-                           const int32_t* seq_ids, bool write_logits, cudaStream_t st,
-                           cudaGraphNode_t* embed_node) {
+                           const int32_t* seq_ids, bool write_logits, bool sampler_keys,
+                           cudaStream_t st, cudaGraphNode_t* embed_node) {
   const spec_model_desc& D = m->d;
   // the GEMM is chosen by the number of sequences, never by nt: a round's
   // rows are bitwise the same at every depth d
@@ -839,6 +839,11 @@ static int enqueue_forward(spec_model* m, int n_seq, int nt, const int32_t* draf
   el.ldy = V;
   el.argmax = m->argmax;
   el.err = m->err;
+  if (sampler_keys) {  // a stochastic round: the sampler's row maxima come from here
+    el.row_key = m->sscr.row_key;
+    el.rk_nt = nt;
+    el.rk_stride = 2 * nt - 1;
+  }
   return timed_launch(m, st, SPEC_PROF_LM_HEAD, gemm_bytes(m->lm, R, write_logits ? 4 : 0),
                       2.0 * R * m->lm.N * (double)m->lm.K,
                       [&] { return linear_launch(m->lm, m->xa, R, el, m->lscr, st); });
@@ -854,7 +859,8 @@ static int run_round(spec_model* m, int n_seq, int d, const int32_t* draft, cons
   // that it never needs retargeting)
   auto enqueue = [&](cudaStream_t s, cudaGraphNode_t* embed_node,
                      cudaGraphNode_t* tail_node) -> int {
-    int rc = enqueue_forward(m, n_seq, d + 1, draft, seq_ids, write_logits, s, embed_node);
+    int rc = enqueue_forward(m, n_seq, d + 1, draft, seq_ids, write_logits,
+                             write_logits && !greedy_tail, s, embed_node);
     if (rc != SPEC_OK || !greedy_tail) return rc;
     GreedyRoundArgs a;
     a.argmax = m->argmax;
@@ -959,7 +965,7 @@ extern "C" int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_id
   if (!greedy) {
     rc = launch_accept_stochastic(m->logits, q_logits, draft, n_seq, d, D.vocab,
                                   sampling->temperature, sampling->seed, seq_ids, m->emit_idx, 1,
-                                  D.max_seqs, m->nacc_tmp, emitted, m->sscr, m->err, st);
+                                  D.max_seqs, m->nacc_tmp, emitted, m->sscr, m->err, st, true);
     if (rc != SPEC_OK) return rc;
     launch_commit(seq_ids, n_seq, d, D.max_seqs, m->nacc_tmp, n_acc, emitted, m->n_past,
                   m->emit_idx, m->anchor, m->err, st);
@@ -1017,7 +1023,7 @@ extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* s
   if (!greedy) {
     rc = launch_accept_stochastic(m->logits, q_logits, ddraft, n_seq, d, D.vocab,
                                   sampling->temperature, sampling->seed, dseq, m->emit_idx, 1,
-                                  D.max_seqs, m->nacc_tmp, dem, m->sscr, m->err, st);
+                                  D.max_seqs, m->nacc_tmp, dem, m->sscr, m->err, st, true);
     if (rc != SPEC_OK) {
       cudaStreamSynchronize(st);
       return rc;

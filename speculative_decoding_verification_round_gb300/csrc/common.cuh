@@ -103,7 +103,29 @@ struct LinEpi {
   // LMHEAD
   int32_t* argmax = nullptr;
   uint32_t* err = nullptr;
+  // LMHEAD of a stochastic round: each logits row's order key of its largest
+  // logit (the sampler's maximum) goes to the accept's per-row keys, where
+  // row r (sequence r / rk_nt, row r % rk_nt) is entry
+  // (r / rk_nt) * rk_stride + r % rk_nt, and the same sequence's draft-row
+  // entries rk_nt .. rk_stride - 1 are zeroed for the accept's max pass;
+  // rk_row0 is the global index of this launch's row 0
+  uint32_t* row_key = nullptr;
+  int rk_row0 = 0, rk_nt = 1, rk_stride = 1;
 };
+
+// Order-preserving 32-bit key of a float (-0 taken as +0): the key of the
+// largest logit of a row, shared by the LM head's argmax and the sampler.
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// The LM head's sampler outputs for one of its rows (see LinEpi::row_key).
+__device__ __forceinline__ void write_row_key(const LinEpi& e, int r, uint32_t key) {
+  const int g = e.rk_row0 + r, s = g / e.rk_nt, i = g - s * e.rk_nt;
+  uint32_t* k = e.row_key + (size_t)s * e.rk_stride;
+  k[i] = key;
+  if (i < e.rk_stride - e.rk_nt) k[e.rk_nt + i] = 0u;  // draft row i of the sequence
+}
 
 // Tries of a bounded mbarrier wait (each suspends for at most ~10 us):
 // about a second in all.
@@ -198,12 +220,15 @@ struct StochScratch {
 size_t stoch_rows_needed(int n_seq, int d);
 void launch_accept_greedy(const int32_t* argmax, const int32_t* draft, int n_seq,
                           int d, int32_t* n_acc, int32_t* emitted, cudaStream_t st);
+// p_keys_ready: the p rows' maximum keys are already in scr.row_key and the
+// q rows' keys zeroed (written by the round's LM head, LinEpi::row_key), so
+// only the q rows get a max pass.
 int launch_accept_stochastic(const float* p, const float* q, const int32_t* draft,
                              int n_seq, int d, int V, float T, uint64_t seed,
                              const int32_t* seq_ids, uint64_t* emit_idx,
                              int emit_by_slot, int n_slots, int32_t* n_acc,
                              int32_t* emitted, const StochScratch& scr,
-                             uint32_t* err, cudaStream_t st);
+                             uint32_t* err, cudaStream_t st, bool p_keys_ready = false);
 void launch_commit(const int32_t* seq_ids, int n_seq, int d, int n_slots, const int32_t* n_acc_in,
                    int32_t* n_acc, int32_t* emitted, int32_t* n_past,
                    uint64_t* emit_idx, int32_t* anchor, const uint32_t* err,

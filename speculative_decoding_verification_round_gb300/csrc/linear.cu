@@ -494,7 +494,9 @@ __device__ __forceinline__ void epilogue_frag(const LinArgs& a, int T, int ct, i
           e.y[(size_t)r * e.ldy + n0] = x0;
           e.y[(size_t)r * e.ldy + n1] = x1;
         }
-        if (x0 != x0 || x1 != x1) atomicOr(e.err, ERR_NONFINITE);
+        // NaN is an error; for the sampler (row keys requested) so is +-inf
+        if (x0 != x0 || x1 != x1 || (e.row_key != nullptr && (isinf(x0) || isinf(x1))))
+          atomicOr(e.err, ERR_NONFINITE);
         if (amax_better(x0, n0, bestv[ct][c], besti[ct][c])) {
           bestv[ct][c] = x0;
           besti[ct][c] = n0;
@@ -866,6 +868,7 @@ linear_q_kernel(const LinArgs a) {
     }
     const int r = zrow0 + col;
     if (lane == 0 && r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = id == 0x7fffffff ? 0 : id;
+    if (lane == 0 && r < a.R && a.epi.row_key != nullptr) write_row_key(a.epi, r, logit_key(v));
   }
   if (threadIdx.x == 0) a.tickets[ZG * a.n_grp + z] = 0u;
 }

@@ -240,12 +240,9 @@ __device__ __forceinline__ uint4 pack4(__half2 a, __half2 b, __half2 c, __half2 
                     *reinterpret_cast<const uint32_t*>(&c), *reinterpret_cast<const uint32_t*>(&d));
 }
 
-// Order-preserving 32-bit key of a float (-0 taken as +0, so that the two
-// zeros tie and the lower id wins, as in the other argmax paths).
-__device__ __forceinline__ uint32_t f32_key(float f) {
-  const uint32_t u = __float_as_uint(f + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+// Order-preserving key of a logit (-0 taken as +0, so that the two zeros
+// tie and the lower id wins, as in the other argmax paths).
+__device__ __forceinline__ uint32_t f32_key(float f) { return logit_key(f); }
 
 __device__ __forceinline__ void epi_bar() {  // the dequant / epilogue warps
   asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI_THREADS) : "memory");
@@ -407,7 +404,8 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, int n, int col0, co
         const int r = col0 + c;
         if (r >= a.R) continue;  // uniform across the warp
         if (e.y != nullptr && real) e.y[(size_t)r * e.ldy + n] = v[c];
-        bad |= real && v[c] != v[c];
+        // NaN is an error; for the sampler (row keys requested) so is +-inf
+        bad |= real && (v[c] != v[c] || (e.row_key != nullptr && isinf(v[c])));
         const uint32_t key = real ? f32_key(v[c]) : 0u;
         const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
         const uint32_t id = key == kmax && real ? (uint32_t)n : 0xffffffffu;
@@ -699,6 +697,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           for (int r = et; r < a.Npad; r += TC_EPI_THREADS) {
             const unsigned long long k = __ldcg(&a.amax_key[r]);
             if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = (int)(~(uint32_t)k);
+            if (r < a.R && a.epi.row_key != nullptr) write_row_key(a.epi, r, (uint32_t)(k >> 32));
             a.amax_key[r] = 0ull;
           }
           if (et == 0) a.tickets[a.n_mt] = 0u;
@@ -909,6 +908,7 @@ int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
       case EPI_LMHEAD:
         if (epi.y != nullptr) e.y = epi.y + o * epi.ldy;
         if (epi.argmax != nullptr) e.argmax = epi.argmax + o;
+        e.rk_row0 = epi.rk_row0 + r0;
         break;
     }
     const int rc = tc_launch_block(w, x + o * w.K, std::min(TC_MAX_R, R - r0), e, scr, st);

@@ -168,13 +168,19 @@ def test_round_host_buffers_match_device_buffers(dev, graphs):
         assert sv.spec_state_get(ms[0], [1, 2]) == sv.spec_state_get(ms[1], [1, 2]), rnd
 
 
-def test_round_stochastic_matches_oracle(orc, dev):
+@pytest.mark.parametrize("tc", [True, False])
+def test_round_stochastic_matches_oracle(orc, dev, tc):
+    """Strict rejection sampling in the round, on either GEMM (the LM head
+    writes the sampler's row maxima itself): decisions bit-exact against the
+    oracle's accept on the round's own fp32 logits."""
     import speculative_decoding_verification_round_gb300 as sv
     from test_gpu_accept import sample_drafts_oracle
     g = np.random.default_rng(42)
     cfg, raw = small_decoder(g, V=1024)
     n_seq, d, max_ctx, T, seed = 2, 4, 200, 0.7, 1234
     m = to_device_model(sv, cfg, raw, dev, max_ctx, 8, 4)
+    if not tc:
+        m.set_tc_min_seqs(0)
     fill_context(sv, m, g, cfg, 4, max_ctx, dev)
     slots = [3, 1]
     n_past, ei0 = [50, 120], [7, 1000]
