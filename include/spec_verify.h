@@ -381,7 +381,9 @@ int spec_verify_round(spec_model* m, int n_seq, const int32_t* seq_ids,
 /* The same verify round with seq_ids, draft, n_acc and emitted in HOST
  * memory (any host memory; shapes as for spec_verify_round).  q_logits may
  * be device memory or host memory; host q_logits (pinned for full copy
- * bandwidth) are first copied into a buffer the model allocated at creation.
+ * bandwidth) are copied into a buffer the model allocated at creation, on a
+ * stream of the model's own, while the round's target pass (which does not
+ * read them) runs; the accept waits for the copy.
  * The small inputs are copied into the model's mapped pinned staging, which
  * the kernels read and write in place (no copy engine steps; a greedy round
  * with graphs on is one graph launch); the

@@ -302,6 +302,8 @@ struct spec_model {
   int32_t* io_dev_out = nullptr;
   float* attn_part = nullptr;
   float* qhost_buf = nullptr;  // [max_seqs][max_nt - 1][vocab]: host q_logits of the host entry
+  cudaStream_t q_stream = nullptr;  // their copy, beside the round's target pass
+  cudaEvent_t q_done = nullptr;
   LinScratch lscr;
   StochScratch sscr;
   std::vector<void*> allocs;
@@ -351,6 +353,8 @@ static void model_free(spec_model* m) {
   for (void* p : m->allocs) cudaFree(p);
   m->allocs.clear();
   if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+  if (m->q_stream) cudaStreamDestroy(m->q_stream);
+  if (m->q_done) cudaEventDestroy(m->q_done);
   if (m->io_host_in) cudaFreeHost(m->io_host_in);
   if (m->io_host_out) cudaFreeHost(m->io_host_out);
   delete m;
@@ -503,6 +507,12 @@ extern "C" int spec_model_create(const spec_model_desc* desc, const spec_model_w
   TRY(dalloc_t(m, &m->sscr.row_key, m->sscr.rows_cap));
   TRY(dalloc_t(m, &m->sscr.row_sum, m->sscr.rows_cap));
   TRY(dalloc_t(m, &m->sscr.decision, m->sscr.seq_cap));
+  if (m->qhost_buf != nullptr &&
+      (cudaStreamCreateWithFlags(&m->q_stream, cudaStreamNonBlocking) != cudaSuccess ||
+       cudaEventCreateWithFlags(&m->q_done, cudaEventDisableTiming) != cudaSuccess)) {
+    cudaGetLastError();
+    TRY(fail(SPEC_E_CUDA, "q_logits copy stream"));
+  }
   if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
     TRY(fail(SPEC_E_CUDA, "capture stream"));
   cudaError_t e = cudaStreamSynchronize(st);
@@ -999,6 +1009,7 @@ extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* s
   }
   cudaStream_t st = as_stream(stream);
   // q_logits in host memory are copied into the model's buffer first
+  bool q_from_host = false;
   if (!greedy && d > 0) {
     cudaPointerAttributes pa;
     if (cudaPointerGetAttributes(&pa, q_logits) != cudaSuccess) {
@@ -1006,8 +1017,13 @@ extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* s
       pa.type = cudaMemoryTypeUnregistered;
     }
     if (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged) {
+      // on the model's copy stream, beside the target pass (which does not
+      // read them); the accept waits for it.  The buffer is free: every call
+      // has synchronised before returning.
       CUDA_TRY(cudaMemcpyAsync(m->qhost_buf, q_logits, sizeof(float) * n_seq * d * D.vocab,
-                               cudaMemcpyHostToDevice, st));
+                               cudaMemcpyHostToDevice, m->q_stream));
+      CUDA_TRY(cudaEventRecord(m->q_done, m->q_stream));
+      q_from_host = true;
       q_logits = m->qhost_buf;
     }
   }
@@ -1019,8 +1035,12 @@ extern "C" int spec_verify_round_host(spec_model* m, int n_seq, const int32_t* s
   int32_t* dacc = m->io_dev_out;
   int32_t* dem = m->io_dev_out + n_seq;
   int rc = run_round(m, n_seq, d, ddraft, dseq, !greedy, greedy, dacc, dem, st, true);
-  if (rc != SPEC_OK) return rc;
+  if (rc != SPEC_OK) {
+    if (q_from_host) cudaStreamSynchronize(m->q_stream);
+    return rc;
+  }
   if (!greedy) {
+    if (q_from_host) CUDA_TRY(cudaStreamWaitEvent(st, m->q_done, 0));
     rc = launch_accept_stochastic(m->logits, q_logits, ddraft, n_seq, d, D.vocab,
                                   sampling->temperature, sampling->seed, dseq, m->emit_idx, 1,
                                   D.max_seqs, m->nacc_tmp, dem, m->sscr, m->err, st, true);
