@@ -70,11 +70,13 @@ inline ChunkSmem chunk_smem(int hd, int ds, int nw, int n_mt) {
   return c;
 }
 
-// 2 CTAs per SM (what the shared memory holds) up to 8 warps; with 8 warps
-// that caps the registers at 128, which the q fragments read from shared
-// memory allow.
+// Residency: the 4-warp CTA of whole head dimensions (up to two m tiles,
+// 72 KB of shared memory at head_dim 128) is held to 168 registers so that
+// three CTAs share an SM (12 warps; batched round 41.5 -> 37.5 us per layer);
+// the others to two CTAs per SM (with 8 warps that caps the registers at
+// 128, which the q fragments read from shared memory allow).
 template <int HD, int DS, int NW>
-__global__ void __launch_bounds__(NW * 32, 2)
+__global__ void __launch_bounds__(NW * 32, (NW == 4 && DS == 1) ? 3 : 2)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
                   int nt, int nq, int nkv, int max_ctx, int nchunks, int mt_group,
@@ -347,12 +349,14 @@ attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcach
 // lane) and the global max (exact in any order) is a warp reduction; the
 // weights w_c = exp2(m_c - max) are broadcast by shuffle, and each lane sums
 // w_c * o_c[d] for its HD / 32 head dimensions and w_c * l_c over the
-// chunks in order, MERGE_BATCH chunks' o loads in flight at a time (the
-// first batch issued together with the (m, l) loads).  The arithmetic of a
-// row does not depend on the other rows.
+// chunks in order, MB chunks' o loads in flight at a time (the first batch
+// issued together with the (m, l) loads).  MB is the smallest of 4, 8, 16
+// that holds the model's chunk count: its registers set the residency
+// (batched round: MB 8 instead of 16 took the merge 11.4 -> 9.7 us).  The
+// arithmetic of a row depends neither on MB nor on the other rows.
 constexpr int MERGE_WARPS = 2;
-constexpr int MERGE_BATCH = 16;
-template <int HD>
+constexpr int MERGE_MAX = 16;  // chunks of the warp merge; the CTA merge beyond
+template <int HD, int MB>
 __global__ void __launch_bounds__(MERGE_WARPS * 32)
 attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ rows,
                   int R, int nt, int nq, int nkv, int max_ctx, int nchunks,
@@ -383,9 +387,9 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
     }
   };
   grid_dep_wait();  // the partials come from the chunk kernel
-  float ov[MERGE_BATCH][DPL];
+  float ov[MB][DPL];
 #pragma unroll
-  for (int u = 0; u < MERGE_BATCH; u++)
+  for (int u = 0; u < MB; u++)
     if (u < nc) load_o(u, ov[u]);
   float2 ml0 = make_float2(-INFINITY, 0.0f);
   if (lane < nc) ml0 = __ldcg(reinterpret_cast<const float2*>(p0 + (size_t)lane * stride + HD));
@@ -405,14 +409,14 @@ attn_merge_kernel(const float* __restrict__ part, const RowInfo* __restrict__ ro
     }
     const float w = c < nc ? exp2f(ml.x - mx) : 0.0f;
     const int nb = min(32, nc - cb);
-    for (int u0 = 0; u0 < nb; u0 += MERGE_BATCH) {
+    for (int u0 = 0; u0 < nb; u0 += MB) {
       if (cb > 0 || u0 > 0) {
 #pragma unroll
-        for (int u = 0; u < MERGE_BATCH; u++)
+        for (int u = 0; u < MB; u++)
           if (u0 + u < nb) load_o(cb + u0 + u, ov[u]);
       }
 #pragma unroll
-      for (int u = 0; u < MERGE_BATCH; u++) {
+      for (int u = 0; u < MB; u++) {
         const float wu = __shfl_sync(0xffffffffu, w, (u0 + u) & 31);
         const float lu = __shfl_sync(0xffffffffu, ml.y, (u0 + u) & 31);
         if (u0 + u < nb) {
@@ -540,12 +544,15 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
     // the model's chunk count picks the merge (never nt): a warp per (row,
     // head) for short contexts, a CTA per (row, head) -- every chunk's loads
     // in flight at once -- for long ones; both compute the same bits
-    if (nchunks <= MERGE_BATCH) {
+    if (nchunks <= MERGE_MAX) {
       cfg.gridDim = dim3((R * nq + MERGE_WARPS - 1) / MERGE_WARPS);
       cfg.blockDim = dim3(MERGE_WARPS * 32);
       cfg.dynamicSmemBytes = 0;
-      e = cudaLaunchKernelEx(&cfg, attn_merge_kernel<HD>, (const float*)part, rows, R, nt, nq,
-                             nkv, max_ctx, nchunks, out);
+      auto merge = nchunks <= 4   ? attn_merge_kernel<HD, 4>
+                   : nchunks <= 8 ? attn_merge_kernel<HD, 8>
+                                  : attn_merge_kernel<HD, 16>;
+      e = cudaLaunchKernelEx(&cfg, merge, (const float*)part, rows, R, nt, nq, nkv, max_ctx,
+                             nchunks, out);
     } else {
       cfg.gridDim = dim3(R * nq);
       cfg.blockDim = dim3(HD);

@@ -77,7 +77,7 @@ struct TcArgs {
   int a_stages, b_stages, raw_depth;  // ring depths: A tiles, activations, raw records
   LinEpi epi;
   float* part;          // [S][n_mt][Npad][256] K-split partials
-  unsigned* tickets;    // [n_mt] K-split tickets, then [1] argmax ticket
+  unsigned* tickets;    // [n_mt] K-split arrivals, [n_mt] departures, [1] argmax ticket
   unsigned long long* amax_key;  // [Npad] LM head: packed (value, index) maxima
   uint32_t* err;
   int wait_tries;
@@ -244,6 +244,17 @@ __device__ __forceinline__ uint4 pack4(__half2 a, __half2 b, __half2 c, __half2 
 // tie and the lower id wins, as in the other argmax paths).
 __device__ __forceinline__ uint32_t f32_key(float f) { return logit_key(f); }
 
+// Bounded wait until the counter at p reaches target (acquire).
+constexpr int TC_MEET_TRIES = 1 << 20;
+__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target) {
+  for (int i = 0; i < TC_MEET_TRIES; i++) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
 __device__ __forceinline__ void epi_bar() {  // the dequant / epilogue warps
   asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI_THREADS) : "memory");
 }
@@ -614,6 +625,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     const int quad = warp & 3, wi = (warp - TC_EPI_WARP0) >> 2;
     const int half = H == 2 ? wi >> 1 : 0;
     const int cw = H == 2 ? wi & 1 : wi, col_first = cw * EW, col_step = H == 2 ? 2 * EW : 4 * EW;
+    const int ncw = H == 2 ? 2 : 4;  // warps sharing a TMEM lane quadrant's columns
     const int slot = wi * 4 + quad;
     const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..511
     const int m = TC_M * half + 32 * quad + lane;    // weight row of the CTA
@@ -622,9 +634,20 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     const bool acc_ok = mbar_wait(ACC, 0, LIN_WAIT_TRIES);
     if (!acc_ok) give_up();
     tc_fence_after();
-    const bool aborted = *abort_flag != 0;
-    // K split: every CTA leaves its partial; the last of the tile adds the
-    // segments in order
+    bool aborted = *abort_flag != 0;
+    // K split: every CTA leaves its partial.  Then the S CTAs of the tile
+    // (one cooperative launch: all resident at once) meet at a counter, and
+    // each adds the segments, in segment order, for its own share of the
+    // columns -- the LM head's last CTA of the tile adds them all (its
+    // argmax gathers every column of the CTA).  Either way every output is
+    // the same in-order sum.
+    const bool split_fin = a.S > 1 && a.epi.kind != EPI_LMHEAD;
+    const int ngrp = a.Npad / EW;
+    int g0 = 0, g1 = ngrp;
+    if (split_fin) {
+      g0 = (int)((long long)seg * ngrp / a.S);
+      g1 = (int)((long long)(seg + 1) * ngrp / a.S);
+    }
     bool finisher = true;
     if (a.S > 1) {
       for (int col0 = col_first; col0 < a.Npad; col0 += col_step) {
@@ -638,14 +661,28 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       if (et == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&a.tickets[mt], 1u);
-        s_last = prev == (unsigned)(a.S - 1);
-        if (s_last) __threadfence();
+        if (split_fin) {
+          // arrive [mt], depart [n_mt + mt]: the last CTA past the meeting
+          // resets both (every CTA of the tile arrives, aborted or not)
+          if (!wait_count(&a.tickets[mt], (unsigned)a.S)) give_up();
+          __threadfence();
+          if (atomicAdd(&a.tickets[a.n_mt + mt], 1u) == (unsigned)(a.S - 1)) {
+            a.tickets[mt] = 0u;
+            a.tickets[a.n_mt + mt] = 0u;
+          }
+          s_last = 1;
+        } else {
+          s_last = prev == (unsigned)(a.S - 1);
+          if (s_last) __threadfence();
+        }
       }
       epi_bar();
       finisher = s_last != 0;
+      aborted = *abort_flag != 0;
     }
     if (finisher) {
-      for (int col0 = col_first; col0 < a.Npad; col0 += col_step) {
+      for (int gi = g0 + cw; gi < g1; gi += ncw) {
+        const int col0 = gi * EW;
         float v[EW];
         if (a.S > 1) {
           const float* src = a.part + ((size_t)mt * a.Npad + col0) * CTA_ROWS + m;
@@ -663,7 +700,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         }
         if (!aborted) tc_epilogue(a, n, col0, v, lane, s_key, slot);
       }
-      if (a.S > 1 && et == 0) a.tickets[mt] = 0u;
+      if (a.S > 1 && !split_fin && et == 0) a.tickets[mt] = 0u;
       if (a.epi.kind == EPI_LMHEAD) {
         // the CTA's best of each column -> one packed 64-bit maximum per
         // column (value key high, inverted id low: ties go to the lowest id);
@@ -688,7 +725,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         epi_bar();
         if (et == 0) {
           __threadfence();
-          const unsigned prev = atomicAdd(&a.tickets[a.n_mt], 1u);
+          const unsigned prev = atomicAdd(&a.tickets[2 * a.n_mt], 1u);
           s_last = prev == (unsigned)(a.n_mt - 1);
           if (s_last) __threadfence();
         }
@@ -700,7 +737,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
             if (r < a.R && a.epi.row_key != nullptr) write_row_key(a.epi, r, (uint32_t)(k >> 32));
             a.amax_key[r] = 0ull;
           }
-          if (et == 0) a.tickets[a.n_mt] = 0u;
+          if (et == 0) a.tickets[2 * a.n_mt] = 0u;
         }
       }
     }
@@ -818,7 +855,7 @@ size_t tc_part_floats(const QMat& w, int R) {
   return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, TC_MAX_R)) * TC_M * w.tc_H
                     : 0;
 }
-size_t tc_tickets_needed(const QMat& w) { return (size_t)tc_mtiles(w) + 1; }
+size_t tc_tickets_needed(const QMat& w) { return 2 * (size_t)tc_mtiles(w) + 1; }
 
 static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& epi,
                            const LinScratch& scr, cudaStream_t st) {
@@ -874,11 +911,22 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   if (cfg.dynamicSmemBytes > (size_t)TC_SMEM_MAX)
     return fail(SPEC_E_SHAPE, "tensor-core GEMM: rings do not fit the shared memory");
   cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  // a K split's CTAs wait on one another: a cooperative launch, which
+  // guarantees they are all resident (the split keeps the grid to one wave)
+  cudaLaunchAttribute at[2];
+  int nat = 0;
+  if (programmatic_launch()) {
+    at[nat].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[nat].val.programmaticStreamSerializationAllowed = 1;
+    nat++;
+  }
+  if (a.S > 1) {
+    at[nat].id = cudaLaunchAttributeCooperative;
+    at[nat].val.cooperative = 1;
+    nat++;
+  }
   cfg.attrs = at;
-  cfg.numAttrs = programmatic_launch() ? 1 : 0;
+  cfg.numAttrs = nat;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k, map, a);
   if (e != cudaSuccess) return fail(SPEC_E_CUDA, std::string("tensor-core GEMM launch: ") + cudaGetErrorString(e));
   return SPEC_OK;
