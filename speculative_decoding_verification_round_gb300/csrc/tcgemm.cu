@@ -819,36 +819,42 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int tc_npad(int R) { return std::max(16, (R + 15) / 16 * 16); }
 int tc_mtiles(const QMat& w) { return (w.N + TC_M * w.tc_H - 1) / (TC_M * w.tc_H); }
 
-// Halves of a CTA for a matrix: two (256 rows: each activation tile and
-// chunk handshake serve twice the MMAs) when the 256-row tiles hold at least
-// 20 chunks per SM, else one (more, shorter tiles: fewer K segments, less
-// fixed cost per CTA and more CTAs sharing the epilogue).  Measured inside
-// the 192-row round: two halves for down 5120x13824 (88 vs 93 us), gate/up
-// 27648x5120 and the LM head; one for QKV 7168x5120 (65 vs 70) and O
-// 5120x5120.
-int tc_choose_halves(int N, int nch, int sms) {
-  const long long units = (long long)((N + 2 * TC_M - 1) / (2 * TC_M)) * nch;
-  return units >= 20LL * sms ? 2 : 1;
-}
-
-// K segments of a matrix for the tensor-core GEMM: only matrices whose tiles
-// do not fill the SMs are split, and only as far as one wave of
-// one-CTA-per-SM launches holds every segment (beyond one wave the partials,
-// CTA rows x activation rows x 4 bytes per tile and segment, leave L2 for
-// DRAM while the weights stream); among those, the fewest chunks per CTA
-// plus a small cost per extra segment (its partial written and read back).
-int tc_choose_split(int N, int nch, int sms, int halves) {
+// Launch shape of a matrix: CTA height (one or two 128-row halves) and K
+// split, from an estimate of the busiest CTA's time in chunk steps of a
+// one-half CTA.  A two-half chunk costs about 1.4 one-half chunks (the
+// activation tile and the chunk's handshakes serve twice the MMAs: measured
+// 1.67 vs 1.2 us inside the 192-row round); a K split costs a little per
+// segment (the tile's CTAs meet, then each adds all segments for a share of
+// the columns); a split keeps the grid to one wave, and tiles beyond one
+// wave run in waves.  Inside the 192-row round this picks two halves for
+// every matrix of the 40-layer model (QKV 7168x5120 65 -> 48 us, O
+// 5120x5120 46 -> 44 us against one half); one half wins for small N, where
+// two-half tiles could not fill the SMs.
+static double tc_estimate(int N, int nch, int sms, int halves, int* split) {
   const int n_mt = (N + TC_M * halves - 1) / (TC_M * halves);
-  int best = 1;
-  double best_t = 1e30;
+  const double per_chunk = halves == 2 ? 1.4 : 1.0;
+  int best_s = 1;
+  double best = 1e30;
   for (int S = 1; S <= 8 && S <= nch && (S == 1 || n_mt * S <= sms); S++) {
-    const double t = std::ceil((double)nch / S) + (S > 1 ? 2.0 * S : 0.0);
-    if (t < best_t - 1e-9) {
-      best_t = t;
-      best = S;
+    const double waves = S == 1 ? std::ceil((double)n_mt / sms) : 1.0;
+    const double t = waves * std::ceil((double)nch / S) * per_chunk + (S > 1 ? 0.25 * S : 0.0);
+    if (t < best - 1e-9) {
+      best = t;
+      best_s = S;
     }
   }
+  if (split != nullptr) *split = best_s;
   return best;
+}
+
+int tc_choose_halves(int N, int nch, int sms) {
+  return tc_estimate(N, nch, sms, 2, nullptr) < tc_estimate(N, nch, sms, 1, nullptr) ? 2 : 1;
+}
+
+int tc_choose_split(int N, int nch, int sms, int halves) {
+  int S = 1;
+  tc_estimate(N, nch, sms, halves, &S);
+  return S;
 }
 
 size_t tc_part_floats(const QMat& w, int R) {
