@@ -59,7 +59,7 @@ struct QMat {
   int S = 1;         // K segments across CTAs
   int nc_cta = 0;    // chunks of one CTA's K range (at most)
                      // (kw, S) are fixed per matrix: independent of nt
-  int tc_S = 1;      // K segments of the tensor-core GEMM (multi-sequence rounds)
+  int tc_P = 1;      // CTAs (runs of work) of the tensor-core GEMM (multi-sequence rounds)
   int tc_H = 2;      // 128-row halves of a tensor-core GEMM CTA (1 or 2)
   uint8_t* rec = nullptr;  // [n_pairs][nch][rec_bytes]
   void* base = nullptr;    // single allocation
@@ -153,7 +153,7 @@ int linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
 // 1 <= R <= 256 rows per launch, the same epilogues.
 int tc_npad(int R);
 int tc_choose_halves(int N, int nch, int sms);
-int tc_choose_split(int N, int nch, int sms, int halves);
+int tc_choose_ctas(int N, int nch, int sms, int halves);
 size_t tc_part_floats(const QMat& w, int R);
 size_t tc_tickets_needed(const QMat& w);
 int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,

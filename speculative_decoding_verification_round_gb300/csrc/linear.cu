@@ -1012,7 +1012,7 @@ int qmat_pack(const spec_qweight* w, PermKind perm, int head_dim, int sms, cudaS
   q.kw = cfg.kw;
   q.S = cfg.S;
   q.tc_H = tc_choose_halves(q.N, q.nch, sms);
-  q.tc_S = tc_choose_split(q.N, q.nch, sms, q.tc_H);
+  q.tc_P = tc_choose_ctas(q.N, q.nch, sms, q.tc_H);
   q.n_grp = (q.n_pairs + WARPS / q.kw - 1) / (WARPS / q.kw);
   q.nc_cta = (q.nch + q.S - 1) / q.S;
   const size_t units = (size_t)q.n_pairs * q.nch;

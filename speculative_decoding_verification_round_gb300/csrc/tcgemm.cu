@@ -71,12 +71,12 @@ struct TcRec {  // the packed record of one (pair, 64-k chunk): see linear.cu
 
 struct TcArgs {
   const uint8_t* rec;  // [n_pairs][nch][rec]
-  int N, K, nch, n_pairs, n_mt, S, R, Npad, tmem_cols;
+  int N, K, nch, n_pairs, n_mt, P, R, Npad, tmem_cols;  // P: CTAs (runs of work)
   int halves;           // 128-row halves (accumulators) of a CTA: 1 or 2
   int acc_stride;       // TMEM columns between the two accumulators
   int a_stages, b_stages, raw_depth;  // ring depths: A tiles, activations, raw records
   LinEpi epi;
-  float* part;          // [S][n_mt][Npad][256] K-split partials
+  float* part;          // [P][Npad][256] a CTA's partial of a shared tile's piece
   unsigned* tickets;    // [n_mt] K-split arrivals, [n_mt] departures, [1] argmax ticket
   unsigned long long* amax_key;  // [Npad] LM head: packed (value, index) maxima
   uint32_t* err;
@@ -432,19 +432,21 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, int n, int col0, co
   }
 }
 
-template <int QT>
+// RUNS: the cut may give a CTA two pieces (one run per SM); without it every
+// CTA has one piece (one run per tile, or a K split) and the main loops are
+// those of a single tile.
+template <int QT, bool RUNS>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   using RC = TcRec<QT>;
   extern __shared__ unsigned char smem_dyn[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) unsigned long long s_bar[2 * TC_MAX_A + 2 * TC_MAX_ST + 2 * TC_MAX_RAW + 1];
+  __shared__ __align__(8) unsigned long long s_bar[2 * TC_MAX_A + 2 * TC_MAX_ST + 2 * TC_MAX_RAW + 3];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, seg = blockIdx.y;
   const int H = a.halves, STA = a.a_stages, STB = a.b_stages, RAWN = a.raw_depth;
   const int CTA_ROWS = TC_M * H, CTA_PAIRS = 4 * H, A_STAGE = H * TC_A_HALF;
   const int B_BYTES = a.Npad * 128;
@@ -456,8 +458,10 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   // [half * 4 + quadrant][key, id][column], in the A ring once every MMA is done
   uint32_t* s_key = reinterpret_cast<uint32_t*>(A0);
   // barriers: a_full[A], a_empty[A], b_full[STB], b_empty[STB], raw_full[RAW],
-  // raw_empty[RAW], acc.  The two rings are freed separately (one commit
-  // each), so activation tiles are fetched a full ring ahead of their MMAs.
+  // raw_empty[RAW], acc (the last piece's MMAs done), acc0 (the first of two
+  // pieces' MMAs done), tfree (the first piece's accumulator read out).  The
+  // two rings are freed separately (one commit each), so activation tiles
+  // are fetched a full ring ahead of their MMAs.
   const uint32_t bar0 = smem_u32(s_bar);
   auto A_FULL = [&](int s) { return bar0 + 8 * s; };
   auto A_EMPTY = [&](int s) { return bar0 + 8 * (TC_MAX_A + s); };
@@ -466,11 +470,32 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
   auto RAW_FULL = [&](int r) { return bar0 + 8 * (2 * TC_MAX_A + 2 * TC_MAX_ST + r); };
   auto RAW_EMPTY = [&](int r) { return bar0 + 8 * (2 * TC_MAX_A + 2 * TC_MAX_ST + TC_MAX_RAW + r); };
   const uint32_t ACC = bar0 + 8 * (2 * TC_MAX_A + 2 * TC_MAX_ST + 2 * TC_MAX_RAW);
+  const uint32_t ACC0 = ACC + 8, TFREE = ACC + 16;
 
-  // this CTA's K range (chunks) and pairs
-  const int c0 = (int)((long long)seg * a.nch / a.S);
-  const int nc = (int)((long long)(seg + 1) * a.nch / a.S) - c0;
-  const int pair0 = mt * CTA_PAIRS;
+  // This CTA's run of work: the (tile, 64-k chunk) units of the matrix in
+  // tile-major order are cut into P runs of equal length (+-1), never longer
+  // than a tile.  A run is the part of tile tA from chunk kA (lenA chunks)
+  // and, when it crosses into the next tile, that tile's first lenB chunks:
+  // at most two pieces.  The next tile's head goes first (read out of tensor
+  // memory into the run's partial mid-run); tA's part, which ends the tile
+  // or lies inside it, stays in tensor memory to the end.  P = n_mt x S cuts
+  // every tile into S aligned segments (a plain K split).
+  // (32-bit: the host keeps P x n_mt x nch below 2^31)
+  int nc, tA, kA, lenA;
+  {
+    const unsigned T = (unsigned)a.n_mt * (unsigned)a.nch;
+    const unsigned U0 = blockIdx.x * T / (unsigned)a.P;
+    const unsigned U1 = (blockIdx.x + 1) * T / (unsigned)a.P;
+    tA = (int)(U0 / (unsigned)a.nch);
+    kA = (int)U0 - tA * a.nch;
+    const unsigned E = (unsigned)(tA + 1) * (unsigned)a.nch;  // end of the first tile
+    nc = (int)(U1 - U0);
+    lenA = RUNS ? (int)((U1 < E ? U1 : E) - U0) : nc;
+  }
+  const int lenB = nc - lenA;
+  const bool two = RUNS && lenB > 0;
+  auto pair_of = [&](int c) { return (two && c < lenB ? tA + 1 : tA) * CTA_PAIRS; };
+  auto kchunk_of = [&](int c) { return two && c < lenB ? c : kA + c - lenB; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STA; s++) {
@@ -486,6 +511,8 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       mbar_init(RAW_EMPTY(r), TC_EPI_THREADS);
     }
     mbar_init(ACC, 1);
+    mbar_init(ACC0, 1);
+    mbar_init(TFREE, TC_EPI_THREADS);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_abort = 0;
   }
@@ -505,25 +532,59 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     atomicOr(a.err, ERR_TIMEOUT);
     *abort_flag = 1;
   };
+  // The epilogue warps' TMEM lane quadrant, rows and columns: warp w reads
+  // quadrant w % 4 and is the wi-th of the four warps of that quadrant,
+  // wi = (w - 3) / 4: with two halves it takes half wi / 2 and every other
+  // group of EW columns, with one every fourth group.
+  struct EpiMap {
+    int quad, wi, cw, col_first, col_step, ncw, m;
+    uint32_t trow;
+  };
+  auto epi_map = [&]() {
+    EpiMap e;
+    e.quad = warp & 3;
+    e.wi = (warp - TC_EPI_WARP0) >> 2;
+    const int half = H == 2 ? e.wi >> 1 : 0;
+    e.cw = H == 2 ? e.wi & 1 : e.wi;
+    e.col_first = e.cw * EW;
+    e.col_step = H == 2 ? 2 * EW : 4 * EW;
+    e.ncw = H == 2 ? 2 : 4;  // warps sharing a quadrant's columns
+    e.m = TC_M * half + 32 * e.quad + lane;  // weight row of the tile
+    e.trow = tmem + (uint32_t)(half * a.acc_stride) + ((uint32_t)(32 * e.quad) << 16);
+    return e;
+  };
+  // an epilogue thread's row of the accumulator -> this CTA's partial
+  // ([P][Npad][rows] fp32: a warp's 32 rows of a column are 128 bytes)
+  auto store_part = [&]() {
+    const EpiMap e = epi_map();
+    for (int col0 = e.col_first; col0 < a.Npad; col0 += e.col_step) {
+      uint32_t v[EW];
+      tc_ld(e.trow + col0, v);
+      float* dst = a.part + ((size_t)blockIdx.x * a.Npad + col0) * CTA_ROWS + e.m;
+#pragma unroll
+      for (int c = 0; c < EW; c++) dst[(size_t)c * CTA_ROWS] = __uint_as_float(v[c]);
+    }
+  };
 
   int issued = 0;  // copies issued by this thread (producers): drained on abort
   if (warp == 0) {
     // ---- weight records: one bulk copy per pair and chunk (weights are
     // ---- constant: this starts before the grid dependency resolves)
     if (lane == 0) {
-      int np = 0;
-      for (int p = 0; p < CTA_PAIRS; p++) np += pair0 + p < a.n_pairs;
       for (int c = 0; c < nc && !*abort_flag; c++) {
         const int r = c % RAWN, ur = c / RAWN;
         if (ur > 0 && !mbar_wait(RAW_EMPTY(r), (ur - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
           give_up();
           break;
         }
+        const int pair0 = pair_of(c), kc = kchunk_of(c);
+        int np = 0;
+        for (int p = 0; p < CTA_PAIRS; p++) np += pair0 + p < a.n_pairs;
         issued = c + 1;
         mbar_expect_tx(RAW_FULL(r), (uint32_t)(np * RC::BYTES));
         for (int p = 0; p < np; p++)
           bulk_copy(smem_u32(RAW0 + r * RAW_BYTES + p * RC::BYTES),
-                    a.rec + ((size_t)(pair0 + p) * a.nch + c0 + c) * RC::BYTES, RC::BYTES,
+                    a.rec + ((size_t)(pair0 + p) * a.nch + kc) * RC::BYTES, RC::BYTES,
                     RAW_FULL(r));
       }
     }
@@ -540,7 +601,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         }
         issued = c + 1;
         mbar_expect_tx(B_FULL(s), (uint32_t)B_BYTES);
-        tma_load_2d(smem_u32(B0 + s * B_BYTES), &tmx, (c0 + c) * 64, 0, B_FULL(s));
+        tma_load_2d(smem_u32(B0 + s * B_BYTES), &tmx, kchunk_of(c) * 64, 0, B_FULL(s));
       }
     }
   } else if (warp == 2) {
@@ -548,6 +609,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     grid_dep_wait();
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(a.Npad);
+      bool announced = false;
       int c = 0;
       for (; c < nc && !*abort_flag; c++) {
         const int sa = c % STA, ua = c / STA, sb = c % STB, ub = c / STB;
@@ -556,7 +618,20 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           give_up();
           break;
         }
+        // a second piece starts in the tensor memory the first one's
+        // accumulator held: wait until the epilogue warps have read it out
+        if (two && c == lenB) {
+          if (!mbar_wait(TFREE, 0, LIN_WAIT_TRIES, abort_flag)) {
+            give_up();
+            break;
+          }
+          // the head's partial is written: announce it to its tile's finisher
+          __threadfence();
+          atomicAdd(&a.tickets[tA + 1], 1u);
+          announced = true;
+        }
         tc_fence_after();
+        const bool fresh = c == 0 || (two && c == lenB);  // a piece's first chunk
         const uint64_t bd = smem_desc_sw128(smem_u32(B0 + sb * B_BYTES));
 #pragma unroll
         for (int h = 0; h < TC_HALVES; h++) {
@@ -567,12 +642,20 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
           const uint32_t d = tmem + (uint32_t)(h * a.acc_stride);
 #pragma unroll
           for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
-            tc_mma(d, ah + 2 * kk, bd + 2 * kk, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+            tc_mma(d, ah + 2 * kk, bd + 2 * kk, idesc, (!fresh || kk > 0) ? 1u : 0u);
             tc_mma(d, al + 2 * kk, bd + 2 * kk, idesc, 1u);
           }
         }
         tc_commit(A_EMPTY(sa));
         tc_commit(B_EMPTY(sb));
+        if (two && c == lenB - 1) tc_commit(ACC0);  // the first piece's MMAs
+      }
+      if (two && c < lenB) tc_commit(ACC0);  // gave up before it: keep the count
+      // a run that gave up still announces its head, so that the counters
+      // end the launch at zero (its outputs are void: ERR_TIMEOUT is set)
+      if (two && !announced) {
+        __threadfence();
+        atomicAdd(&a.tickets[tA + 1], 1u);
       }
       tc_commit(ACC);  // completes when every MMA issued above has
     }
@@ -598,7 +681,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       {
         unsigned char* at = A0 + s * A_STAGE + dh * TC_A_HALF;
         const int pp = 4 * dh + pc;  // pair of the CTA
-        if (pair0 + pp < a.n_pairs) {
+        if (pair_of(c) + pp < a.n_pairs) {
           dequant_tile<QT>(RAW0 + r * RAW_BYTES + pp * RC::BYTES, at, at + TC_A_BYTES, pc, tile,
                            lane, b_lo, b_hi);
         } else {  // rows past the matrix: zeros (the warp's 16-byte units)
@@ -613,132 +696,156 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
       mbar_arrive(RAW_EMPTY(r));
       fence_proxy_async();  // the A tiles, to the tensor core's proxy
       mbar_arrive(A_FULL(s));
+      if (two && c == lenB) {
+        // the head's accumulator -> this run's partial, once its MMAs are
+        // done (tA's first chunk is already staged); the MMA thread then
+        // announces it and starts tA's part in the freed tensor memory
+        if (!mbar_wait(ACC0, 0, LIN_WAIT_TRIES, abort_flag)) {
+          give_up();
+          break;
+        }
+        tc_fence_after();
+        store_part();
+        tc_fence_before();
+        mbar_arrive(TFREE);
+      }
     }
   }
   grid_dep_launch();
 
-  // ---- epilogue: warps 3..18; warp w reads TMEM lane quadrant w % 4 and
-  // ---- is the wi-th of the four warps of that quadrant, wi = (w - 3) / 4:
-  // ---- with two halves it takes half wi / 2 and every other group of EW
-  // ---- columns, with one every fourth group
+  // ---- epilogue (warps 3..18): the piece in tensor memory, tile tA's part.
+  // ---- A tile that is this CTA's alone is finished from tensor memory.  A
+  // ---- tile cut into several pieces is summed in k order: with runs, by
+  // ---- the run holding its end (the other pieces' partials, then its own
+  // ---- part from tensor memory); with a K split, the tile's CTAs meet and
+  // ---- each adds all segments for its own share of the columns (an even
+  // ---- share of the reads).  The CTAs that wait on others belong to one
+  // ---- cooperative launch: all resident at once.
   if (warp >= TC_EPI_WARP0) {
-    const int quad = warp & 3, wi = (warp - TC_EPI_WARP0) >> 2;
-    const int half = H == 2 ? wi >> 1 : 0;
-    const int cw = H == 2 ? wi & 1 : wi, col_first = cw * EW, col_step = H == 2 ? 2 * EW : 4 * EW;
-    const int ncw = H == 2 ? 2 : 4;  // warps sharing a TMEM lane quadrant's columns
-    const int slot = wi * 4 + quad;
+    const EpiMap em = epi_map();
+    const int cw = em.cw, ncw = em.ncw, m = em.m;
+    const uint32_t trow = em.trow;
+    const int slot = em.wi * 4 + em.quad;
     const int et = threadIdx.x - TC_EPI_WARP0 * 32;  // 0..511
-    const int m = TC_M * half + 32 * quad + lane;    // weight row of the CTA
-    const int n = mt * CTA_ROWS + m;
-    const uint32_t trow = tmem + (uint32_t)(half * a.acc_stride) + ((uint32_t)(32 * quad) << 16);
+    const int ngrp = a.Npad / EW;
+    const unsigned T = (unsigned)a.n_mt * (unsigned)a.nch;
     const bool acc_ok = mbar_wait(ACC, 0, LIN_WAIT_TRIES);
     if (!acc_ok) give_up();
     tc_fence_after();
     bool aborted = *abort_flag != 0;
-    // K split: every CTA leaves its partial.  Then the S CTAs of the tile
-    // (one cooperative launch: all resident at once) meet at a counter, and
-    // each adds the segments, in segment order, for its own share of the
-    // columns -- the LM head's last CTA of the tile adds them all (its
-    // argmax gathers every column of the CTA).  Either way every output is
-    // the same in-order sum.
-    const bool split_fin = a.S > 1 && a.epi.kind != EPI_LMHEAD;
-    const int ngrp = a.Npad / EW;
-    int g0 = 0, g1 = ngrp;
-    if (split_fin) {
-      g0 = (int)((long long)seg * ngrp / a.S);
-      g1 = (int)((long long)(seg + 1) * ngrp / a.S);
+    // the runs holding the tile's first and last unit: its pieces, in k order
+    auto owner = [&](unsigned u) { return (int)(((u + 1) * (unsigned)a.P - 1) / T); };
+    const int t = tA;
+    const int lo = owner((unsigned)t * (unsigned)a.nch);
+    const int hi = owner((unsigned)(t + 1) * (unsigned)a.nch - 1);
+    const int nseg = hi - lo + 1;
+    const int n = t * CTA_ROWS + m;
+    int g0 = 0, g1 = ngrp;  // column groups this CTA finishes
+    int nsum = 0;           // partials it adds (runs lo, lo + 1, ...)
+    bool from_tmem = true;  // then its own piece
+    if (nseg > 1) {
+      if (RUNS && (int)blockIdx.x != hi) {  // a piece before the tile's end
+        store_part();
+        epi_bar();
+        if (et == 0) {
+          __threadfence();
+          atomicAdd(&a.tickets[t], 1u);
+        }
+        g1 = 0;
+      } else if (RUNS) {  // the tile's end: wait for the other pieces
+        if (et == 0) {
+          if (!wait_count(&a.tickets[t], (unsigned)(nseg - 1))) give_up();
+          __threadfence();
+          a.tickets[t] = 0u;
+        }
+        epi_bar();
+        aborted = *abort_flag != 0;
+        nsum = nseg - 1;
+      } else {  // K split
+        store_part();
+        epi_bar();
+        if (et == 0) {
+          // arrivals [t], departures [n_mt + t]: the last CTA past the
+          // meeting resets both (every CTA of the tile arrives, aborted or not)
+          __threadfence();
+          atomicAdd(&a.tickets[t], 1u);
+          if (!wait_count(&a.tickets[t], (unsigned)nseg)) give_up();
+          __threadfence();
+          if (atomicAdd(&a.tickets[a.n_mt + t], 1u) == (unsigned)(nseg - 1)) {
+            a.tickets[t] = 0u;
+            a.tickets[a.n_mt + t] = 0u;
+          }
+        }
+        epi_bar();
+        aborted = *abort_flag != 0;
+        const int j = (int)blockIdx.x - lo;  // this CTA's segment
+        g0 = j * ngrp / nseg;
+        g1 = (j + 1) * ngrp / nseg;
+        nsum = nseg;
+        from_tmem = false;
+      }
     }
-    bool finisher = true;
-    if (a.S > 1) {
-      for (int col0 = col_first; col0 < a.Npad; col0 += col_step) {
-        uint32_t v[EW];
-        tc_ld(trow + col0, v);
-        float* dst = a.part + (((size_t)seg * a.n_mt + mt) * a.Npad + col0) * CTA_ROWS + m;
+    const size_t pstride = (size_t)a.Npad * CTA_ROWS;  // floats between partials
+    for (int gi = g0 + cw; gi < g1; gi += ncw) {
+      const int col0 = gi * EW;
+      float v[EW];
+      if (nsum > 0) {  // the partials in k order
+        const float* src = a.part + (size_t)lo * pstride + (size_t)col0 * CTA_ROWS + m;
 #pragma unroll
-        for (int c = 0; c < EW; c++) dst[(size_t)c * CTA_ROWS] = __uint_as_float(v[c]);
+        for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * CTA_ROWS);
+        for (int q = 1; q < nsum; q++) {
+          src += pstride;
+#pragma unroll
+          for (int c = 0; c < EW; c++) v[c] += __ldcg(src + (size_t)c * CTA_ROWS);
+        }
+      }
+      if (from_tmem) {  // then this CTA's own piece
+        uint32_t u[EW];
+        tc_ld(trow + col0, u);
+#pragma unroll
+        for (int c = 0; c < EW; c++)
+          v[c] = nsum > 0 ? v[c] + __uint_as_float(u[c]) : __uint_as_float(u[c]);
+      }
+      if (!aborted) tc_epilogue(a, n, col0, v, lane, s_key, slot);
+    }
+    if (a.epi.kind == EPI_LMHEAD) {
+      // (one whole tile per CTA) the CTA's best of each column -> one packed
+      // 64-bit maximum per column (value key high, inverted id low: ties go
+      // to the lowest id); an aborted CTA still takes its ticket, so the
+      // state is reset
+      epi_bar();
+      for (int r = et; r < a.R && !aborted; r += TC_EPI_THREADS) {
+        // the slots that saw column r: the four quadrants of the warps of
+        // the column's group (of each half)
+        const int cr = H == 2 ? (r / EW) & 1 : (r / EW) & 3;
+        const int nsl = 4 * H;
+        uint32_t bk = 0u, bi = 0xffffffffu;
+        for (int e = 0; e < nsl; e++) {
+          const int q = (H == 2 ? (2 * (e >> 2) + cr) : cr) * 4 + (e & 3);
+          const uint32_t k2 = s_key[(2 * q) * TC_MAX_R + r], i2 = s_key[(2 * q + 1) * TC_MAX_R + r];
+          if (k2 > bk || (k2 == bk && i2 < bi)) {
+            bk = k2;
+            bi = i2;
+          }
+        }
+        atomicMax(&a.amax_key[r], ((unsigned long long)bk << 32) | (unsigned long long)(~bi));
       }
       epi_bar();
       if (et == 0) {
         __threadfence();
-        const unsigned prev = atomicAdd(&a.tickets[mt], 1u);
-        if (split_fin) {
-          // arrive [mt], depart [n_mt + mt]: the last CTA past the meeting
-          // resets both (every CTA of the tile arrives, aborted or not)
-          if (!wait_count(&a.tickets[mt], (unsigned)a.S)) give_up();
-          __threadfence();
-          if (atomicAdd(&a.tickets[a.n_mt + mt], 1u) == (unsigned)(a.S - 1)) {
-            a.tickets[mt] = 0u;
-            a.tickets[a.n_mt + mt] = 0u;
-          }
-          s_last = 1;
-        } else {
-          s_last = prev == (unsigned)(a.S - 1);
-          if (s_last) __threadfence();
-        }
+        const unsigned prev = atomicAdd(&a.tickets[2 * a.n_mt], 1u);
+        s_last = prev == (unsigned)(a.n_mt - 1);
+        if (s_last) __threadfence();
       }
       epi_bar();
-      finisher = s_last != 0;
-      aborted = *abort_flag != 0;
-    }
-    if (finisher) {
-      for (int gi = g0 + cw; gi < g1; gi += ncw) {
-        const int col0 = gi * EW;
-        float v[EW];
-        if (a.S > 1) {
-          const float* src = a.part + ((size_t)mt * a.Npad + col0) * CTA_ROWS + m;
-          const size_t step = (size_t)a.n_mt * a.Npad * CTA_ROWS;
-#pragma unroll
-          for (int c = 0; c < EW; c++) v[c] = __ldcg(src + (size_t)c * CTA_ROWS);
-          for (int s2 = 1; s2 < a.S; s2++)
-#pragma unroll
-            for (int c = 0; c < EW; c++) v[c] += __ldcg(src + s2 * step + (size_t)c * CTA_ROWS);
-        } else {
-          uint32_t u[EW];
-          tc_ld(trow + col0, u);
-#pragma unroll
-          for (int c = 0; c < EW; c++) v[c] = __uint_as_float(u[c]);
+      if (s_last) {  // every tile's maxima are in: the argmax, and reset
+        for (int r = et; r < a.Npad; r += TC_EPI_THREADS) {
+          const unsigned long long k = __ldcg(&a.amax_key[r]);
+          if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = (int)(~(uint32_t)k);
+          if (r < a.R && a.epi.row_key != nullptr) write_row_key(a.epi, r, (uint32_t)(k >> 32));
+          a.amax_key[r] = 0ull;
         }
-        if (!aborted) tc_epilogue(a, n, col0, v, lane, s_key, slot);
-      }
-      if (a.S > 1 && !split_fin && et == 0) a.tickets[mt] = 0u;
-      if (a.epi.kind == EPI_LMHEAD) {
-        // the CTA's best of each column -> one packed 64-bit maximum per
-        // column (value key high, inverted id low: ties go to the lowest id);
-        // an aborted CTA still takes its ticket, so the state is reset
-        epi_bar();
-        for (int r = et; r < a.R && !aborted; r += TC_EPI_THREADS) {
-          // the slots that saw column r: the four quadrants of the warps of
-          // the column's group (of each half)
-          const int cr = H == 2 ? (r / EW) & 1 : (r / EW) & 3;
-          const int nsl = 4 * H;
-          uint32_t bk = 0u, bi = 0xffffffffu;
-          for (int e = 0; e < nsl; e++) {
-            const int q = (H == 2 ? (2 * (e >> 2) + cr) : cr) * 4 + (e & 3);
-            const uint32_t k2 = s_key[(2 * q) * TC_MAX_R + r], i2 = s_key[(2 * q + 1) * TC_MAX_R + r];
-            if (k2 > bk || (k2 == bk && i2 < bi)) {
-              bk = k2;
-              bi = i2;
-            }
-          }
-          atomicMax(&a.amax_key[r], ((unsigned long long)bk << 32) | (unsigned long long)(~bi));
-        }
-        epi_bar();
-        if (et == 0) {
-          __threadfence();
-          const unsigned prev = atomicAdd(&a.tickets[2 * a.n_mt], 1u);
-          s_last = prev == (unsigned)(a.n_mt - 1);
-          if (s_last) __threadfence();
-        }
-        epi_bar();
-        if (s_last) {  // every tile's maxima are in: the argmax, and reset
-          for (int r = et; r < a.Npad; r += TC_EPI_THREADS) {
-            const unsigned long long k = __ldcg(&a.amax_key[r]);
-            if (r < a.R && a.epi.argmax != nullptr) a.epi.argmax[r] = (int)(~(uint32_t)k);
-            if (r < a.R && a.epi.row_key != nullptr) write_row_key(a.epi, r, (uint32_t)(k >> 32));
-            a.amax_key[r] = 0ull;
-          }
-          if (et == 0) a.tickets[2 * a.n_mt] = 0u;
-        }
+        if (et == 0) a.tickets[2 * a.n_mt] = 0u;
       }
     }
   }
@@ -764,10 +871,10 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
 }
 
 using TcKernel = void (*)(const CUtensorMap, const TcArgs);
-TcKernel tc_kernel_for(int qtype) {
-  if (qtype == 4) return tc_linear_kernel<4>;
-  if (qtype == 6) return tc_linear_kernel<6>;
-  if (qtype == 8) return tc_linear_kernel<8>;
+TcKernel tc_kernel_for(int qtype, bool runs) {
+  if (qtype == 4) return runs ? tc_linear_kernel<4, true> : tc_linear_kernel<4, false>;
+  if (qtype == 6) return runs ? tc_linear_kernel<6, true> : tc_linear_kernel<6, false>;
+  if (qtype == 8) return runs ? tc_linear_kernel<8, true> : tc_linear_kernel<8, false>;
   return nullptr;
 }
 
@@ -819,31 +926,58 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int tc_npad(int R) { return std::max(16, (R + 15) / 16 * 16); }
 int tc_mtiles(const QMat& w) { return (w.N + TC_M * w.tc_H - 1) / (TC_M * w.tc_H); }
 
-// Launch shape of a matrix: CTA height (one or two 128-row halves) and K
-// split, from an estimate of the busiest CTA's time in chunk steps of a
-// one-half CTA.  A two-half chunk costs about 1.4 one-half chunks (the
-// activation tile and the chunk's handshakes serve twice the MMAs: measured
-// 1.67 vs 1.2 us inside the 192-row round); a K split costs a little per
-// segment (the tile's CTAs meet, then each adds all segments for a share of
-// the columns); a split keeps the grid to one wave, and tiles beyond one
-// wave run in waves.  Inside the 192-row round this picks two halves for
-// every matrix of the 40-layer model (QKV 7168x5120 65 -> 48 us, O
-// 5120x5120 46 -> 44 us against one half); one half wins for small N, where
-// two-half tiles could not fill the SMs.
-static double tc_estimate(int N, int nch, int sms, int halves, int* split) {
+// Launch shape of a matrix: CTA height (one or two 128-row halves) and the
+// cut of its (tile, chunk) units into runs, from an estimate of the longest
+// run in chunk steps of a one-half CTA.  A two-half chunk costs about 1.4
+// one-half chunks (the activation tile and the chunk's handshakes serve
+// twice the MMAs: measured 1.67 vs 1.2 us inside the 192-row round).  Cuts:
+//   * one run per tile, in waves when there are more tiles than SMs;
+//   * a K split, S aligned runs per tile (n_mt x S <= SMs): each CTA also
+//     writes and meets, a small cost per segment;
+//   * one run per SM over all units (a run may end one tile and start the
+//     next): the most even, but such a run reads its first piece out of
+//     tensor memory before it starts the second (about 2.5 chunks).
+// Inside the 192-row round this gives two halves everywhere: QKV 7168x5120
+// S = 5, O 5120x5120 S = 7, down 5120x13824 S = 7, gate/up 27648x5120 one
+// run per SM (108 tiles: 80 -> 57 chunks for the busiest CTA), the LM head
+// one run per tile; one half wins for small N.
+// The most pieces any tile has when n_mt x nch units are cut into P runs.
+static int tc_max_pieces(int n_mt, int nch, int P) {
+  const long long T = (long long)n_mt * nch;
+  auto owner = [&](long long u) { return (int)(((u + 1) * P - 1) / T); };
+  int most = 1;
+  for (int t = 0; t < n_mt; t++)
+    most = std::max(most, owner((long long)(t + 1) * nch - 1) - owner((long long)t * nch) + 1);
+  return most;
+}
+
+static double tc_estimate(int N, int nch, int sms, int halves, int* ctas) {
   const int n_mt = (N + TC_M * halves - 1) / (TC_M * halves);
   const double per_chunk = halves == 2 ? 1.4 : 1.0;
-  int best_s = 1;
-  double best = 1e30;
-  for (int S = 1; S <= 8 && S <= nch && (S == 1 || n_mt * S <= sms); S++) {
-    const double waves = S == 1 ? std::ceil((double)n_mt / sms) : 1.0;
-    const double t = waves * std::ceil((double)nch / S) * per_chunk + (S > 1 ? 0.25 * S : 0.0);
-    if (t < best - 1e-9) {
-      best = t;
-      best_s = S;
+  const long long T = (long long)n_mt * nch;
+  int best_p = n_mt;
+  double best = std::ceil((double)n_mt / sms) * nch * per_chunk;  // one run per tile
+  if (n_mt < sms) {
+    for (int S = 2; S <= 8 && S <= nch && n_mt * S <= sms; S++) {
+      const double t = std::ceil((double)nch / S) * per_chunk + 0.25 * S;
+      if (t < best - 1e-9) {
+        best = t;
+        best_p = n_mt * S;
+      }
+    }
+    const int P = (int)std::min<long long>(sms, T);
+    // runs: a tile's end finishes it from the other pieces' partials, so
+    // keep to at most three pieces a tile
+    if (P > n_mt && P % n_mt != 0 && tc_max_pieces(n_mt, nch, P) <= 3) {
+      const long long run = (T + P - 1) / P;
+      const double t = run * per_chunk + 2.5;
+      if (t < best - 1e-9) {
+        best = t;
+        best_p = P;
+      }
     }
   }
-  if (split != nullptr) *split = best_s;
+  if (ctas != nullptr) *ctas = best_p;
   return best;
 }
 
@@ -851,14 +985,14 @@ int tc_choose_halves(int N, int nch, int sms) {
   return tc_estimate(N, nch, sms, 2, nullptr) < tc_estimate(N, nch, sms, 1, nullptr) ? 2 : 1;
 }
 
-int tc_choose_split(int N, int nch, int sms, int halves) {
-  int S = 1;
-  tc_estimate(N, nch, sms, halves, &S);
-  return S;
+int tc_choose_ctas(int N, int nch, int sms, int halves) {
+  int P = 1;
+  tc_estimate(N, nch, sms, halves, &P);
+  return P;
 }
 
 size_t tc_part_floats(const QMat& w, int R) {
-  return w.tc_S > 1 ? (size_t)w.tc_S * tc_mtiles(w) * tc_npad(std::min(R, TC_MAX_R)) * TC_M * w.tc_H
+  return w.tc_P > tc_mtiles(w) ? (size_t)w.tc_P * tc_npad(std::min(R, TC_MAX_R)) * TC_M * w.tc_H
                     : 0;
 }
 size_t tc_tickets_needed(const QMat& w) { return 2 * (size_t)tc_mtiles(w) + 1; }
@@ -894,7 +1028,10 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   a.nch = w.nch;
   a.n_pairs = w.n_pairs;
   a.n_mt = tc_mtiles(w);
-  a.S = w.tc_S;
+  // the LM head's argmax gathers whole tiles: one run per tile
+  a.P = epi.kind == EPI_LMHEAD ? a.n_mt : w.tc_P;
+  if ((long long)(a.P + 1) * a.n_mt * a.nch >= (1ll << 31))
+    return fail(SPEC_E_SHAPE, "tensor-core GEMM: matrix too large for the 32-bit work cut");
   a.R = R;
   a.Npad = Npad;
   // one accumulator of Npad columns per half, a power of two apart
@@ -908,17 +1045,18 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
   a.amax_key = scr.amax_keys;
   a.err = scr.err;
   a.wait_tries = scr.wait_tries > 0 ? LIN_WAIT_TRIES : 0;
-  const TcKernel k = tc_kernel_for(w.qtype);
+  // runs that cross a tile boundary: not every tile cut into aligned segments
+  const TcKernel k = tc_kernel_for(w.qtype, a.P > a.n_mt && a.P % a.n_mt != 0);
   if (k == nullptr) return fail(SPEC_E_INVALID, "tensor-core GEMM: no kernel for this format");
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_mt, a.S);
+  cfg.gridDim = dim3(a.P);
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = tc_smem_bytes(w.qtype, Npad, a.halves, a.a_stages, a.b_stages, a.raw_depth);
   if (cfg.dynamicSmemBytes > (size_t)TC_SMEM_MAX)
     return fail(SPEC_E_SHAPE, "tensor-core GEMM: rings do not fit the shared memory");
   cfg.stream = st;
-  // a K split's CTAs wait on one another: a cooperative launch, which
-  // guarantees they are all resident (the split keeps the grid to one wave)
+  // the CTAs of a shared tile wait on one another: a cooperative launch,
+  // which guarantees they are all resident (such cuts keep to one wave)
   cudaLaunchAttribute at[2];
   int nat = 0;
   if (programmatic_launch()) {
@@ -926,7 +1064,7 @@ static int tc_launch_block(const QMat& w, const __half* x, int R, const LinEpi& 
     at[nat].val.programmaticStreamSerializationAllowed = 1;
     nat++;
   }
-  if (a.S > 1) {
+  if (a.P > a.n_mt) {
     at[nat].id = cudaLaunchAttributeCooperative;
     at[nat].val.cooperative = 1;
     nat++;
@@ -973,6 +1111,7 @@ int tc_linear_launch(const QMat& w, const __half* x, int R, const LinEpi& epi,
 
 void tc_init_attrs() {
   for (int qt : {4, 6, 8})
-    cudaFuncSetAttribute(tc_kernel_for(qt), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         TC_SMEM_MAX);
+    for (bool runs : {false, true})
+      cudaFuncSetAttribute(tc_kernel_for(qt, runs), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           TC_SMEM_MAX);
 }

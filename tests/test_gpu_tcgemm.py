@@ -84,12 +84,16 @@ def test_tc_small_matches_oracle(orc, dev, qtype, N, K):
 
 
 @pytest.mark.parametrize("qtype,N,K", [(4, 5120, 13824), (6, 13824, 5120), (8, 5120, 13824),
-                                       (4, 27648, 5120), (4, 13920, 5120), (8, 10016, 5120)])
+                                       (4, 27648, 5120), (4, 13920, 5120), (8, 10016, 5120),
+                                       (4, 4096, 14336), (6, 28672, 4096), (8, 25616, 5120)])
 def test_tc_full_size_matches_oracle(orc, dev, qtype, N, K):
-    """The linear sweep's matrices and the batched workload's gate/up at the
-    batched round's 192 rows (one full launch); rows at other
-    batch sizes bitwise equal.  The last two run 256-row CTAs whose last
-    tile is ragged (96 and 32 real rows)."""
+    """The linear sweep's matrices, the batched workload's gate/up and the
+    8-layer decoder's down and gate/up at the batched round's 192 rows (one
+    full launch); rows at other batch sizes bitwise equal.  Cuts: K splits
+    (5120x13824, 13824x5120, 4096x14336, ...) and one run per SM, whose runs
+    end one tile and start the next (27648x5120, 28672x4096, 25616x5120);
+    13920, 10016 and 25616 rows leave the last 256-row tile ragged (96, 32
+    and 16 real rows)."""
     import torch
     import speculative_decoding_verification_round_gb300 as sv
     gen = synth.torch_gen(40 + qtype, dev)
