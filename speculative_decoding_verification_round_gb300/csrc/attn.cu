@@ -70,13 +70,16 @@ inline ChunkSmem chunk_smem(int hd, int ds, int nw, int n_mt) {
   return c;
 }
 
-// Residency: the 4-warp CTA of whole head dimensions (up to two m tiles,
-// 72 KB of shared memory at head_dim 128) is held to 168 registers so that
-// three CTAs share an SM (12 warps; batched round 41.5 -> 37.5 us per layer);
-// the others to two CTAs per SM (with 8 warps that caps the registers at
-// 128, which the q fragments read from shared memory allow).
-template <int HD, int DS, int NW>
-__global__ void __launch_bounds__(NW * 32, (NW == 4 && DS == 1) ? 3 : 2)
+// Residency MINB CTAs per SM.  Two, as the shared memory holds (with 8 warps
+// that caps the registers at 128, which the q fragments read from shared
+// memory allow).  Three for the 4-warp CTA of whole head dimensions (up to
+// two m tiles, 72 KB of shared memory at head_dim 128) when one chunk's
+// CTAs alone fill the SMs: held to 168 registers, 12 warps an SM (batched
+// round, 12 sequences: 41.5 -> 37.5 us per layer; one sequence over a long
+// context, the 8-layer decoder at nt 8, is faster at two).  The register
+// cap changes no arithmetic: the bits are those of the two-CTA build.
+template <int HD, int DS, int NW, int MINB>
+__global__ void __launch_bounds__(NW * 32, MINB)
 attn_chunk_kernel(const __half* __restrict__ q, const __half* __restrict__ kcache,
                   const __half* __restrict__ vcache, const RowInfo* __restrict__ rows,
                   int nt, int nq, int nkv, int max_ctx, int nchunks, int mt_group,
@@ -531,9 +534,16 @@ int attn_launch_t(const __half* q, const __half* kcache, const __half* vcache,
   const int n_grp = (n_mt + mt_group - 1) / mt_group;
   const int ds = n_mt == 1 ? 2 : 1;
   const int nw = mt_group <= 2 ? 4 : 8;
-  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2, 4>
-               : nw == 4   ? attn_chunk_kernel<HD, 1, 4>
-                           : attn_chunk_kernel<HD, 1, 8>;
+  static const int sms = [] {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+  }();
+  const bool dense = (long long)n_seq * nkv * n_grp >= sms;
+  auto chunk = n_mt == 1 ? attn_chunk_kernel<HD, 2, 4, 2>
+               : nw == 4 ? (dense ? attn_chunk_kernel<HD, 1, 4, 3> : attn_chunk_kernel<HD, 1, 4, 2>)
+                         : attn_chunk_kernel<HD, 1, 8, 2>;
   const ChunkSmem lay = chunk_smem(HD, ds, nw, mt_group);
   cfg.gridDim = dim3(nchunks, nkv * n_grp, n_seq);
   cfg.blockDim = dim3(nw * 32);
@@ -586,8 +596,9 @@ void attn_init_attrs() {
   int dev = 0, optin = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  for (auto k : {attn_chunk_kernel<128, 2, 4>, attn_chunk_kernel<128, 1, 4>,
-                 attn_chunk_kernel<128, 1, 8>, attn_chunk_kernel<64, 2, 4>,
-                 attn_chunk_kernel<64, 1, 4>, attn_chunk_kernel<64, 1, 8>})
+  for (auto k : {attn_chunk_kernel<128, 2, 4, 2>, attn_chunk_kernel<128, 1, 4, 2>,
+                 attn_chunk_kernel<128, 1, 4, 3>, attn_chunk_kernel<128, 1, 8, 2>,
+                 attn_chunk_kernel<64, 2, 4, 2>, attn_chunk_kernel<64, 1, 4, 2>,
+                 attn_chunk_kernel<64, 1, 4, 3>, attn_chunk_kernel<64, 1, 8, 2>})
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }

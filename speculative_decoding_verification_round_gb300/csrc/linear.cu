@@ -230,6 +230,19 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// The same for streamed weights, with an L2 policy of evict first: each
+// weight is read once, and the L2 keeps the round's activations and cache
+// instead (8-layer decoder round at nt 8: 587 -> 577 us).
+__device__ __forceinline__ void bulk_copy_weights(uint32_t dst, const void* src, uint32_t bytes,
+                                                  uint32_t bar) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -554,7 +567,7 @@ linear_q_kernel(const LinArgs a) {
     for (int q = 0; q < NS - 1 && q * CPS < wn; q++) {
       const uint32_t nb = (uint32_t)min(CPS, wn - q * CPS) * RC::BYTES;
       mbar_expect_tx(bar0 + 8 * q, nb);
-      bulk_copy(ring_s + q * SB, src + (size_t)q * SB, nb, bar0 + 8 * q);
+      bulk_copy_weights(ring_s + q * SB, src + (size_t)q * SB, nb, bar0 + 8 * q);
     }
   }
   // ---- the activation slice (rows zrow0.., chunks c_begin..): zero what no
@@ -614,7 +627,7 @@ linear_q_kernel(const LinArgs a) {
           const int sn = (u + NS - 1) % NS;
           const uint32_t nb = (uint32_t)min(CPS, wn - (q + NS - 1) * CPS) * RC::BYTES;
           mbar_expect_tx(bar0 + 8 * sn, nb);
-          bulk_copy(ring_s + sn * SB, nxt, nb, bar0 + 8 * sn);
+          bulk_copy_weights(ring_s + sn * SB, nxt, nb, bar0 + 8 * sn);
         }
         nxt += SB;
 #pragma unroll

@@ -120,12 +120,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int tri
 }
 
 // --- copies ----------------------------------------------------------------
+// Bulk copy of streamed weights with an L2 policy (evict first: each weight
+// is read once, and the L2 keeps the round's activations, partials and
+// cache instead; gate/up 27648x5120 inside the 192-row round 122 -> 116 us).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
+                                          uint32_t bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
       : "memory");
 }
 // 2-D tiled TMA load: box of the tensor map at (x = k, y = row).
@@ -571,6 +579,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
     // ---- weight records: one bulk copy per pair and chunk (weights are
     // ---- constant: this starts before the grid dependency resolves)
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first();
       for (int c = 0; c < nc && !*abort_flag; c++) {
         const int r = c % RAWN, ur = c / RAWN;
         if (ur > 0 && !mbar_wait(RAW_EMPTY(r), (ur - 1) & 1, LIN_WAIT_TRIES, abort_flag)) {
@@ -585,7 +594,7 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         for (int p = 0; p < np; p++)
           bulk_copy(smem_u32(RAW0 + r * RAW_BYTES + p * RC::BYTES),
                     a.rec + ((size_t)(pair0 + p) * a.nch + kc) * RC::BYTES, RC::BYTES,
-                    RAW_FULL(r));
+                    RAW_FULL(r), pol);
       }
     }
     grid_dep_wait();
@@ -634,17 +643,22 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         const bool fresh = c == 0 || (two && c == lenB);  // a piece's first chunk
         const uint64_t bd = smem_desc_sw128(smem_u32(B0 + sb * B_BYTES));
 #pragma unroll
-        for (int h = 0; h < TC_HALVES; h++) {
-          if (h >= H) break;
-          const unsigned char* at = A0 + sa * A_STAGE + h * TC_A_HALF;
-          const uint64_t ah = smem_desc_sw128(smem_u32(at));
-          const uint64_t al = smem_desc_sw128(smem_u32(at + TC_A_BYTES));
-          const uint32_t d = tmem + (uint32_t)(h * a.acc_stride);
+        // per 16-k step: hi of each half, then lo of each half (each
+        // accumulator still adds hi before lo, step by step; the halves'
+        // MMAs alternate)
+        const unsigned char* at0 = A0 + sa * A_STAGE;
+        const uint64_t ah0 = smem_desc_sw128(smem_u32(at0));
+        const uint64_t al0 = smem_desc_sw128(smem_u32(at0 + TC_A_BYTES));
+        const uint64_t ah1 = smem_desc_sw128(smem_u32(at0 + TC_A_HALF));
+        const uint64_t al1 = smem_desc_sw128(smem_u32(at0 + TC_A_HALF + TC_A_BYTES));
+        const uint32_t d0 = tmem, d1 = tmem + (uint32_t)a.acc_stride;
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
-            tc_mma(d, ah + 2 * kk, bd + 2 * kk, idesc, (!fresh || kk > 0) ? 1u : 0u);
-            tc_mma(d, al + 2 * kk, bd + 2 * kk, idesc, 1u);
-          }
+        for (int kk = 0; kk < 4; kk++) {  // 16 k (32 bytes) per instruction
+          const uint32_t acc = (!fresh || kk > 0) ? 1u : 0u;
+          tc_mma(d0, ah0 + 2 * kk, bd + 2 * kk, idesc, acc);
+          if (H == 2) tc_mma(d1, ah1 + 2 * kk, bd + 2 * kk, idesc, acc);
+          tc_mma(d0, al0 + 2 * kk, bd + 2 * kk, idesc, 1u);
+          if (H == 2) tc_mma(d1, al1 + 2 * kk, bd + 2 * kk, idesc, 1u);
         }
         tc_commit(A_EMPTY(sa));
         tc_commit(B_EMPTY(sb));

@@ -83,3 +83,33 @@ def test_attention_matches_oracle_and_is_position_invariant(orc, dev, nq, nkv, h
             sv.spec_verify_attn(m, 0, 1, sid[s:s + 1], 1, T(q[r:r + 1]), T(kn[r:r + 1]),
                                 T(vn[r:r + 1]), one)
             assert torch.equal(one[0], out[r]), (s, i)
+
+
+def test_attention_rows_do_not_depend_on_the_batch(dev):
+    """A sequence's rows are bitwise the same alone and in a batch of twelve
+    (the batched workload's shape: GQA 5, 16 rows, m tiles in groups of two):
+    the batch's chunk columns fill the SMs and take the build held to three
+    CTAs an SM, the lone sequence's the two-CTA build."""
+    import torch
+    import speculative_decoding_verification_round_gb300 as sv
+    nq, nkv, hd, nt, max_ctx, n_seq = 40, 8, 128, 16, 600, 12
+    g = np.random.default_rng(77)
+    m = attn_model(sv, dev, g, nq, nkv, hd, max_ctx, nt, n_seq)
+    kc = synth.f16_normal(g, (n_seq, nkv, max_ctx, hd))
+    vc = synth.f16_normal(g, (n_seq, nkv, max_ctx, hd))
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+    for s in range(n_seq):
+        sv.spec_kv_fill(m, 0, s, 0, max_ctx, T(kc[s]), T(vc[s]))
+    pasts = [500 + 7 * s for s in range(n_seq)]
+    sv.spec_state_set(m, list(range(n_seq)), n_past=pasts)
+    R = n_seq * nt
+    q = synth.f16_normal(g, (R, nq, hd))
+    kn = synth.f16_normal(g, (R, nkv, hd))
+    vn = synth.f16_normal(g, (R, nkv, hd))
+    sid = torch.arange(n_seq, dtype=torch.int32, device=dev)
+    out = torch.empty((R, nq * hd), dtype=torch.int16, device=dev)
+    sv.spec_verify_attn(m, 0, n_seq, sid, nt, T(q), T(kn), T(vn), out)
+    alone = torch.empty((nt, nq * hd), dtype=torch.int16, device=dev)
+    sv.spec_verify_attn(m, 0, 1, sid[:1], nt, T(q[:nt]), T(kn[:nt]), T(vn[:nt]), alone)
+    assert sv.spec_error_check(m) == 0
+    assert torch.equal(alone, out[:nt])
