@@ -132,7 +132,11 @@ int spec_linear_q(const spec_qmat* w, const uint16_t* x, int nt, float* y,
  * is computed by the same instructions whatever R is, so a row's result does
  * not depend on the other rows; it differs from spec_linear_q's in the last
  * bits (that kernel accumulates each 32-block's integer sum and applies the
- * scale in fp32).  1 <= R <= max_rows (launched in blocks of 192 rows). */
+ * scale in fp32).  The matrix's (tile, 64-k chunk) work is cut once, at
+ * creation, from N, K and the SM count (never from R): one CTA per tile, a
+ * K split, or one run per SM that may cross a tile boundary; a tile cut
+ * across CTAs is summed in k order, its CTAs launched cooperatively (all
+ * resident).  1 <= R <= max_rows (launched in blocks of 192 rows). */
 int spec_linear_q_tc(const spec_qmat* w, const uint16_t* x, int R, float* y,
                      void* stream);
 

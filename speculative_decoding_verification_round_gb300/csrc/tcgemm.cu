@@ -7,16 +7,19 @@
 // weight stream but by the contraction itself (2 x 192 flops per weight), so
 // it runs on tcgen05.mma with the activation rows as the N dimension:
 //
-//   * a CTA owns 128 or 256 weight rows (4 or 8 pairs of the packed
-//     streaming layout; 256 for matrices with more 128-row tiles than SMs) as
-//     one or two 128-row halves, each with its own 128 x Npad fp32
-//     accumulator in tensor memory (one TMEM lane per weight row; Npad = the
-//     rows rounded up to 16), and one of S segments of K.  Two halves share
-//     each activation tile and chunk handshake (twice the MMAs per chunk);
+//   * a CTA's work is a run of (tile, 64-k chunk) units: a tile is 128 or
+//     256 weight rows (4 or 8 pairs of the packed streaming layout) as one
+//     or two 128-row halves, each with its own 128 x Npad fp32 accumulator
+//     in tensor memory (one TMEM lane per weight row; Npad = the rows
+//     rounded up to 16).  The cut is fixed per matrix: one run per tile, a
+//     K split (S aligned segments a tile), or one run per SM over all units
+//     (a run may end one tile and start the next).  Two halves share each
+//     activation tile and chunk handshake (twice the MMAs per chunk);
 //   * warp 0 streams the packed weight records into a shared-memory ring with
-//     TMA bulk copies; warp 1 loads the activation tile of each 64-k chunk
-//     with a 2-D TMA tensor copy (128-byte swizzle, rows past R read as zero);
-//   * warps 3-10 dequantise each chunk into TWO fp16 A tiles per half in the
+//     TMA bulk copies (L2 policy evict first: each weight is read once);
+//     warp 1 loads the activation tile of each 64-k chunk with a 2-D TMA
+//     tensor copy (128-byte swizzle, rows past R read as zero);
+//   * warps 3-18 dequantise each chunk into TWO fp16 A tiles per half in the
 //     UMMA K-major 128-byte-swizzle layout, hi = fp16(q * scale) and lo =
 //     fp16(q * scale - hi): q * scale has at most 11 + 8 significant bits,
 //     so lo holds the rest exactly and hi + lo IS the weight -- every
@@ -24,18 +27,20 @@
 //   * one thread of warp 2 issues sixteen tcgen05.mma (M 128, N Npad, K 16:
 //     hi and lo of each half for each 16-k step) per chunk and commits them
 //     to the stages' "empty" barriers;
-//   * after the last chunk the same eight warps read the accumulators back
-//     (tcgen05.ld), add the K segments in segment order (the last CTA of a
-//     tile, by a ticket) and run the fused epilogue (store, residual add,
-//     SwiGLU, RoPE + KV write, LM head logits + argmax).
-// Each output element is one accumulation chain whose instructions do not
-// depend on the other rows of the batch, so a row's result is the same in
-// every batch this kernel runs.
+//   * after the last chunk the same sixteen warps read the accumulators back
+//     (tcgen05.ld), add the pieces of a tile cut across CTAs in k order
+//     (partials in L2; the CTAs that wait on others are one cooperative
+//     launch) and run the fused epilogue (store, residual add, SwiGLU, RoPE
+//     + KV write, LM head logits + argmax).
+// Each output element is the same sequence of fp32 additions (chunk by chunk
+// into an accumulator, then the pieces of its tile in k order) whatever the
+// other rows of the batch, so a row's result is the same in every batch
+// this kernel runs.
 //
 // Every wait is bounded (mbarrier try_wait with a suspend hint, about a
-// second in all); one that gives up sets ERR_TIMEOUT and the CTA stops
-// issuing work, waits (bounded) for what it issued and frees its tensor
-// memory before it returns.
+// second in all; the pieces' meeting counter, a tenth of a second); one that
+// gives up sets ERR_TIMEOUT and the CTA stops issuing work, waits (bounded)
+// for what it issued and frees its tensor memory before it returns.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
