@@ -365,6 +365,40 @@ def test_gemm_copy_wait_timeout_fails_closed(dev, graphs, n_seq):
         m.set_wait_budget(-1)
 
 
+def test_tc_runs_timeout_leaves_counters_clear(dev):
+    """A two-sequence round whose gate/up (25600x1024: 100 two-half tiles x
+    16 chunks) is cut into one run per SM, so runs end one tile and start the
+    next and the tile ends wait for the other pieces at per-tile counters.
+    With the first copy wait's budget at zero every CTA gives up and the
+    round fails closed; the counters still end at zero: the next round's
+    logits equal, bit for bit, those of the same round on a model that never
+    gave up."""
+    import speculative_decoding_verification_round_gb300 as sv
+    g = np.random.default_rng(61)
+    cfg, raw = small_decoder(g, L=1, H=1024, nq=8, nkv=2, hd=128, F=12800, V=512)
+    V = cfg["vocab"]
+    state = ([100, 120], [3, 4], [5, 6])
+    models = []
+    for _ in range(2):
+        m = to_device_model(sv, cfg, raw, dev, 300, 16, 2)
+        fill_context(sv, m, np.random.default_rng(7), cfg, 2, 300, dev)
+        sv.spec_state_set(m, [0, 1], n_past=state[0], emit_idx=state[1], anchor=state[2])
+        models.append(m)
+    ref, m = models
+    draft = g.integers(0, V, (2, 3)).astype(np.int32)
+    m.set_wait_budget(0)
+    n_acc, em, _, bits = gpu_round(sv, m, dev, draft, 3, [1, 0], V=V)
+    assert bits & 0x10, bits
+    assert (n_acc == -1).all() and (em == -1).all()
+    assert sv.spec_state_get(m, [0, 1]) == state
+    m.set_wait_budget(131072)
+    got = gpu_round(sv, m, dev, draft, 3, [1, 0], V=V)
+    want = gpu_round(sv, ref, dev, draft, 3, [1, 0], V=V)
+    assert got[3] == 0 and want[3] == 0
+    assert np.array_equal(got[2], want[2])
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+
+
 def test_invalid_draft_and_position_fail_closed(dev):
     import speculative_decoding_verification_round_gb300 as sv
     g = np.random.default_rng(44)
