@@ -18,7 +18,7 @@ LIB = os.path.join(BUILD, "libspecverify.so")
 SOURCES = ["api.cu", "linear.cu", "tcgemm.cu", "attn.cu", "ops.cu", "accept.cu", "depth.cu"]
 # host code whose doubles must be rounded operation by operation
 FILE_FLAGS = {"depth.cu": ["-Xcompiler", "-ffp-contract=off"]}
-HEADERS = [os.path.join(CSRC, "common.cuh"),
+HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "tc_ops.cuh"),
            os.path.join(os.path.dirname(HERE), "include", "spec_verify.h")]
 
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -49,11 +49,10 @@
 #include <string>
 
 #include "common.cuh"
+#include "tc_ops.cuh"
 
 namespace {
 
-constexpr int TC_M = 128;           // weight rows of an accumulator (the MMA's M)
-constexpr int TC_HALVES = 2;        // accumulators of a CTA, at most
 constexpr int TC_DQ_WARPS = 16;     // dequant (then epilogue) warps
 constexpr int TC_THREADS = (3 + TC_DQ_WARPS) * 32;  // 19 warps
 constexpr int TC_EPI_WARP0 = 3;     // warps 3..18: dequant, then epilogue
@@ -87,118 +86,6 @@ struct TcArgs {
   uint32_t* err;
   int wait_tries;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// --- mbarrier --------------------------------------------------------------
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(10000)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait; false after `tries` suspended tries, or at once when another
-// role of the CTA has given up (abort != 0).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int tries,
-                                          const volatile int* abort = nullptr) {
-  for (int i = 0; i < tries; i++) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort != nullptr && *abort) return false;
-  }
-  return false;
-}
-
-// --- copies ----------------------------------------------------------------
-// Bulk copy of streamed weights with an L2 policy (evict first: each weight
-// is read once, and the L2 keeps the round's activations, partials and
-// cache instead; gate/up 27648x5120 inside the 192-row round 122 -> 116 us).
-__device__ __forceinline__ uint64_t l2_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
-      "%2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
-      : "memory");
-}
-// 2-D tiled TMA load: box of the tensor map at (x = k, y = row).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// --- tcgen05 ---------------------------------------------------------------
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B,
-// 8-row atoms of 1024 B (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
-         (2ull << 61);
-}
-// Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
-// M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_f16(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
-}
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-// EW consecutive accumulator columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld(uint32_t taddr, uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// Byte offset of 16-byte unit u (k = 8u..8u+7) of row r in a K-major
-// 128-byte-swizzled tile of 64-k rows.
-__device__ __forceinline__ uint32_t sw128_off(int r, int u) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((u ^ (r & 7)) << 4));
-}
 
 // The integers of one k16 step's word for rows g and g+8 (4 + 4 values) as
 // exact fp16: each u is placed in the low bits of a half, made 1024 + u by
@@ -647,7 +534,6 @@ tc_linear_kernel(const __grid_constant__ CUtensorMap tmx, const TcArgs a) {
         tc_fence_after();
         const bool fresh = c == 0 || (two && c == lenB);  // a piece's first chunk
         const uint64_t bd = smem_desc_sw128(smem_u32(B0 + sb * B_BYTES));
-#pragma unroll
         // per 16-k step: hi of each half, then lo of each half (each
         // accumulator still adds hi before lo, step by step; the halves'
         // MMAs alternate)
